@@ -1,0 +1,421 @@
+#!/usr/bin/env python3
+"""Benchmark of the libqw decoder forward pass on GB300.
+
+Default workload (N=1): the 28-layer Qwen3-0.6B shape with seeded random bf16 weights,
+batch 1, a 5-token uniform-random prompt, prefill + 64 greedy decode steps. One bench step
+is one such generation (KV reset + reserve, prefill, 64 decode steps replayed from CUDA
+graphs, each step feeding its pick back on the device). ``value`` counts the generated
+tokens (65 per step: one from the prefill, one per decode step) per second of device
+time with inputs resident in HBM; ``e2e`` is the same metric through ``qw_generate`` from
+pinned host buffers (prompt copied in, picks copied out, every step).
+
+Other workloads: ``--config 0`` (one block + tied head, 16 decode steps),
+``--config 2`` (batch 64, 1024-token prefill each, 128 decode steps; decode tokens/s),
+``--config 3`` (batch 16 x 512-token prefill; prefill tokens/s), ``--config 4`` (batch 8,
+cached lengths uniform in [1024, 32768] injected by the synthetic KV fill, 32 decode
+steps; decode tokens/s).
+
+Multi-GPU: replicas only (independent sequences per GPU, no collective on the data path);
+``value`` is the sum over ranks of the units processed divided by the slowest rank's time.
+
+``--impl reference`` times the fp64 CPU oracle on this host on a bounded sample of the same
+workload (the only other program this bench runs).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "decode tok/s (B=1/64) & prefill tok/s, Qwen3-0.6B shape; % of HBM/TC roofline"
+
+CONFIGS = {
+    0: dict(workload="qwen3-0.6b-shape 1 block + tied head, B=1, 5-token prompt, prefill + 16 greedy decode steps",
+            shape=synth.ONE_BLOCK, B=1, prompt=5, n_decode=16, unit="tok/s", kind="generate"),
+    1: dict(workload="qwen3-0.6b-shape 28 layers, B=1, 5-token prompt, prefill + 64 greedy decode steps",
+            shape=synth.QWEN3_0_6B, B=1, prompt=5, n_decode=64, unit="tok/s", kind="generate"),
+    2: dict(workload="qwen3-0.6b-shape 28 layers, B=64, 1024-token prefill each, 128 greedy decode steps",
+            shape=synth.QWEN3_0_6B, B=64, prompt=1024, n_decode=128, unit="tok/s", kind="decode"),
+    3: dict(workload="qwen3-0.6b-shape 28 layers, prefill B=16 x 512 tokens",
+            shape=synth.QWEN3_0_6B, B=16, prompt=512, n_decode=0, unit="tok/s", kind="prefill"),
+    4: dict(workload="qwen3-0.6b-shape 28 layers, B=8, cached lengths U[1024, 32768] (paged, 16-token pages), "
+                     "32 greedy decode steps",
+            shape=synth.QWEN3_0_6B, B=8, prompt=None, n_decode=32, unit="tok/s", kind="decode_long"),
+}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ---------------------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------------------
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d.get("hbm_gbs", 6800.0), d.get("bf16_tflops", 1900.0), d.get("bf16_tflops_sustained", 1700.0), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def kernel_bytes(kind: int, s, T: int, B: int) -> float:
+    """Algorithmic bytes of one launch of a kernel kind (weights once + activations in/out)."""
+    D, I, QD, KD, V = s.hidden, s.inter, s.n_heads * s.head_dim, s.n_kv_heads * s.head_dim, s.vocab
+    QKV = QD + 2 * KD
+    if kind == 1:   # q|k|v projection (+ fused input RMSNorm)
+        return QKV * D * 2 + T * D * 4 + T * QKV * 4 + D * 2
+    if kind == 4:   # o_proj + residual
+        return D * QD * 2 + T * QD * 2 + 2 * T * D * 4
+    if kind == 5:   # gate/up + SiLU*mul (+ fused post-attention RMSNorm)
+        return 2 * I * D * 2 + T * D * 4 + T * I * 2 + D * 2
+    if kind == 6:   # down_proj + residual
+        return D * I * 2 + T * I * 2 + 2 * T * D * 4
+    if kind == 7:   # final norm + tied LM head + argmax
+        return V * D * 2 + B * D * 4 + D * 2
+    return float("nan")
+
+
+KIND_NAMES = {1: "qkv_proj(rmsnorm fused)", 2: "qknorm_rope_append", 3: "attention", 4: "o_proj+residual",
+              5: "gate_up+silu_mul(rmsnorm fused)", 6: "down_proj+residual", 7: "lm_head+argmax"}
+
+
+def run_ours(args, cfg, rank, world):
+    import torch
+    import decode_qwen3_decoder_gb300 as pkg
+    pkg.build()
+    qw = pkg.qw
+    dev = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(dev)
+    s = cfg["shape"]
+    B, P, ND = cfg["B"], cfg["prompt"], cfg["n_decode"]
+    t0 = time.time()
+    w = synth.Weights(s, seed=0)
+    named = dict(w.named())
+    log(f"[rank {rank}] weights drawn in {time.time() - t0:.1f}s")
+    max_ctx = P + ND + 16
+    eng = qw.Engine(s, named, max_tokens=max(B * P, 8), max_batch=max(B, 8), max_context=max_ctx,
+                    kv_pages=B * ((max_ctx + 15) // 16) + 8, max_seqs=max(B, 8))
+    del named, w
+    st = eng.stream
+    seqs = list(range(B))
+    prompt = synth.make_tokens(s.vocab, B * P, 1000 + args.config + 17 * rank)
+    d_prompt = torch.tensor(prompt, dtype=torch.int32, device="cuda")
+    d_cur = torch.zeros(B, dtype=torch.int32, device="cuda")
+    d_out = torch.zeros((ND + 1, B), dtype=torch.int32, device="cuda")
+    launches = [0]
+
+    def one_step():
+        qw.qw_kv_reset(eng.kv, -1, st)
+        for sq in seqs:
+            qw.qw_kv_reserve(eng.kv, sq, P + ND, st)
+        qw.qw_prefill(eng.model, eng.kv, seqs, [P] * B, d_prompt.data_ptr(), 0, d_cur.data_ptr(), st)
+        launches[0] += qw.qw_last_launch_count(eng.model)
+        with torch.cuda.stream(st):
+            d_out[0].copy_(d_cur)
+        for i in range(1, ND + 1):
+            qw.qw_decode_step(eng.model, eng.kv, seqs, d_cur.data_ptr(), 0, d_cur.data_ptr(), st)
+            launches[0] += qw.qw_last_launch_count(eng.model)
+            with torch.cuda.stream(st):
+                d_out[i].copy_(d_cur)
+
+    for _ in range(args.warmup):
+        one_step()
+    st.synchronize()
+    status = qw.qw_sync_status(eng.model, st)
+    if status != 0:
+        raise RuntimeError(f"device status {status} after warm-up: {qw.qw_last_error()}")
+    gpu_uuid = "0"
+    try:
+        gpu_uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        if not gpu_uuid.startswith("GPU-"):
+            gpu_uuid = "GPU-" + gpu_uuid
+    except Exception:
+        gpu_uuid = str(dev)
+    barrier(world)
+    launches[0] = 0
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(gpu_uuid) as clk:
+        torch.cuda.synchronize()
+        e0.record(st)
+        for _ in range(args.steps):
+            one_step()
+        e1.record(st)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms = e0.elapsed_time(e1)
+    ms_max = reduce_max(ms, world)
+    gpu_launches = launches[0]
+    tokens_per_step = B * (ND + 1)
+    value = tokens_per_step * args.steps * world / (ms_max / 1e3)
+    status = qw.qw_sync_status(eng.model, st)
+    if status != 0:
+        raise RuntimeError(f"device status {status} in the timed region: {qw.qw_last_error()}")
+
+    # ---- decode-step latency alone (same graphs), for the record ----
+    qw.qw_kv_reset(eng.kv, -1, st)
+    for sq in seqs:
+        qw.qw_kv_reserve(eng.kv, sq, P + ND, st)
+    qw.qw_prefill(eng.model, eng.kv, seqs, [P] * B, d_prompt.data_ptr(), 0, d_cur.data_ptr(), st)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(st)
+    for i in range(ND):
+        qw.qw_decode_step(eng.model, eng.kv, seqs, d_cur.data_ptr(), 0, d_cur.data_ptr(), st)
+    b.record(st)
+    st.synchronize()
+    decode_us = a.elapsed_time(b) * 1e3 / ND
+
+    # ---- per-kernel timing with CUDA events around each launch of one kernel kind ----
+    hbm, bf16_burst, bf16_sust, peak_src = peaks()
+    kinds = {}
+    n_launch_per_step = {1: s.n_layers, 4: s.n_layers, 5: s.n_layers, 6: s.n_layers, 7: 1}
+    for kind, nl in n_launch_per_step.items():
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * nl)]
+        handles = (qw.ctypes.c_void_p * (2 * nl))(*[ev.cuda_event for ev in evs])
+        durs = []
+        qw.qw_kv_reset(eng.kv, -1, st)
+        for sq in seqs:
+            qw.qw_kv_reserve(eng.kv, sq, P + ND, st)
+        qw.qw_prefill(eng.model, eng.kv, seqs, [P] * B, d_prompt.data_ptr(), 0, d_cur.data_ptr(), st)
+        qw.qw_profile_set(eng.model, kind, handles, 2 * nl)
+        for i in range(min(ND, 16)):
+            qw.qw_decode_step(eng.model, eng.kv, seqs, d_cur.data_ptr(), 0, d_cur.data_ptr(), st)
+            st.synchronize()
+            if i >= 2:
+                durs.extend(evs[2 * j].elapsed_time(evs[2 * j + 1]) for j in range(nl))
+        qw.qw_profile_set(eng.model, 0, None, 0)
+        st.synchronize()
+        avg_us = statistics.mean(durs) * 1e3
+        kinds[kind] = dict(name=KIND_NAMES[kind], launches_per_step=nl, avg_us=avg_us,
+                           total_us_per_step=avg_us * nl, bytes=kernel_bytes(kind, s, B, B))
+    dom = max(kinds, key=lambda k: kinds[k]["total_us_per_step"])
+    dk = kinds[dom]
+    achieved = dk["bytes"] / (dk["avg_us"] * 1e-6) / 1e9
+    roofline = {"bound": "hbm", "kernel": dk["name"], "achieved": round(achieved, 1), "peak": hbm,
+                "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / hbm, 4),
+                "traffic": None, "algorithmic_bytes_per_launch": dk["bytes"],
+                "avg_launch_us": round(dk["avg_us"], 3)}
+    step_bytes = sum(kernel_bytes(k, s, B, B) * n for k, n in n_launch_per_step.items())
+    # ---- end to end through qw_generate with pinned host buffers ----
+    h_prompt = torch.empty(B * P, dtype=torch.int32, pin_memory=True).numpy()
+    h_prompt[:] = prompt
+    h_out = torch.empty((B, ND + 1), dtype=torch.int32, pin_memory=True).numpy()
+    e2e_steps = max(1, min(args.steps, 5))
+    for i in range(e2e_steps + 1):
+        if i == 1:
+            t_e2e = time.perf_counter()
+        qw.qw_kv_reset(eng.kv, -1, st)
+        for sq in seqs:
+            qw.qw_kv_reserve(eng.kv, sq, P + ND, st)
+        qw.qw_generate(eng.model, eng.kv, seqs, [P] * B, h_prompt, ND, h_out, st)
+    e2e_s = time.perf_counter() - t_e2e
+    e2e_val = reduce_sum(tokens_per_step * e2e_steps / e2e_s, world)
+    ref_ids = d_out.t().cpu().numpy()
+    if not np.array_equal(h_out, ref_ids):
+        log("warning: qw_generate picks differ from the device loop's picks")
+
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": cfg["unit"], "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded random-init bf16 weights N(0,0.02), uniform-random token ids)",
+        "config": {"workload": cfg["workload"], "batch": B, "prompt_tokens": P, "decode_steps": ND,
+                   "tokens_per_step": tokens_per_step, "parallelism": f"replicas x{world} (no collective)",
+                   "l2": "weights (1.19 GB per decode step) exceed L2; no flush",
+                   "decode_step_us": round(decode_us, 2),
+                   "decode_step_bytes": step_bytes,
+                   "decode_step_hbm_frac": round(step_bytes / (decode_us * 1e-6) / 1e9 / hbm, 4)},
+        "roofline": roofline,
+        "kernels": {KIND_NAMES[k]: {"avg_us": round(v["avg_us"], 3), "per_step_us": round(v["total_us_per_step"], 2),
+                                    "GB/s": round(v["bytes"] / (v["avg_us"] * 1e-6) / 1e9, 1)}
+                    for k, v in kinds.items()},
+        "e2e": {"value": round(e2e_val, 2), "unit": cfg["unit"], "h2d_bytes_per_step": B * P * 4,
+                "d2h_bytes_per_step": B * (ND + 1) * 4},
+        "gpu_launches": gpu_launches,
+        "clocks": clk.summary(),
+    }
+    eng.close()
+    return out
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def reduce_max(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def reduce_sum(v, world):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------------------
+# oracle timing (cpu_baseline leg and the reference arm)
+# ---------------------------------------------------------------------------------------
+def oracle_sample(cfg, n_decode: int, seed: int):
+    """Generated tokens per second of the fp64 oracle on prefill + n_decode greedy steps."""
+    import oracle
+    s = cfg["shape"]
+    m = oracle.Model(synth.Weights(s, seed=0))
+    for i in range(s.n_layers):
+        m.layer(i)
+    _ = m.embed32
+    prompt = synth.make_tokens(s.vocab, cfg["prompt"], seed).tolist()
+    t0 = time.perf_counter()
+    oracle.generate(m, prompt, n_decode, keep_hidden=False)
+    dt = time.perf_counter() - t0
+    return (n_decode + 1) / dt, dt
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def cpu_baseline(cfg, n_decode=8):
+    v, dt = oracle_sample(cfg, n_decode, 4242)
+    return {"value": round(v, 4), "unit": cfg["unit"], "cores": cores(), "kind": "oracle",
+            "sample": f"fp64 NumPy oracle, {cfg['prompt']}-token prompt prefill + {n_decode} greedy decode steps "
+                      f"of the same model shape, batch 1 ({dt:.1f} s)"}
+
+
+def run_reference(args, cfg):
+    samples = []
+    n_dec = 4
+    for i in range(args.warmup + args.steps):
+        v, dt = oracle_sample(cfg, n_dec, 5000 + i)
+        if i >= args.warmup:
+            samples.append(dt)
+    tokens = (n_dec + 1) * args.steps
+    total = sum(samples)
+    val = tokens / total
+    return {"impl": "reference", "metric": METRIC, "value": round(val, 4), "unit": cfg["unit"], "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded random-init bf16 weights widened to fp64)",
+            "config": {"workload": cfg["workload"], "sample": f"prefill {cfg['prompt']} + {n_dec} decode steps per step"},
+            "cpu_baseline": {"value": round(val, 4), "unit": cfg["unit"], "cores": cores(), "kind": "oracle",
+                             "sample": f"prefill + {n_dec} greedy decode steps per bench step"},
+            "e2e": {"value": round(val, 4), "unit": cfg["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=1, choices=[0, 1])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    cfg = CONFIGS[args.config]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, cfg)), flush=True)
+        return
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    out = run_ours(args, cfg, rank, world)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            out["cpu_baseline"] = cpu_baseline(cfg)
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

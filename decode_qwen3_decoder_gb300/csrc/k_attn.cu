@@ -1,0 +1,265 @@
+// Grouped-query causal attention over the paged KV cache (Paso 5 of "Dentro de un LLM:
+// Inferencia en Python puro para Qwen3-0.6B en MLX").
+//
+// k_attn_paged: split-KV flash-decode. One CTA per (query token, KV head, split of the
+// key range); it serves both query heads of its KV head (head h reads KV head h / 2), so
+// every K/V byte is loaded once for the two heads. Each of the 4 warps walks pages of 16
+// keys with an online softmax in fp32 (exp2 domain); lanes split head_dim into 16-byte
+// chunks and the two half-warps take alternate keys. Warps merge through shared memory;
+// splits merge with log-sum-exp weights in the CTA that finishes last (an atomic ticket,
+// no waiting). The query at position p sees keys 0..p of its sequence (the causal rule by
+// position; the new token's own K/V were appended before this kernel runs).
+#include <utility>
+
+#include "qw_internal.h"
+
+namespace {
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(const LaunchCtx& c, void (*kern)(KArgs...), dim3 grid, dim3 block,
+                     size_t smem, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = c.stream;
+    cudaLaunchAttribute attr[1];
+    cfg.numAttrs = 0;
+    if (c.pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    if (c.counter) ++*c.counter;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+__device__ __forceinline__ uint4 ldg_nc(const void* p) {
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+
+__device__ __forceinline__ float dot8q(const float* q, const uint4 k) {
+    float a = q[0] * bf_lo(k.x);
+    a = fmaf(q[1], bf_hi(k.x), a);
+    a = fmaf(q[2], bf_lo(k.y), a);
+    a = fmaf(q[3], bf_hi(k.y), a);
+    a = fmaf(q[4], bf_lo(k.z), a);
+    a = fmaf(q[5], bf_hi(k.z), a);
+    a = fmaf(q[6], bf_lo(k.w), a);
+    a = fmaf(q[7], bf_hi(k.w), a);
+    return a;
+}
+
+__device__ __forceinline__ float half_warp_sum(float v) {
+    v += __shfl_xor_sync(0xffffffffu, v, 8);
+    v += __shfl_xor_sync(0xffffffffu, v, 4);
+    v += __shfl_xor_sync(0xffffffffu, v, 2);
+    v += __shfl_xor_sync(0xffffffffu, v, 1);
+    return v;
+}
+
+}  // namespace
+
+struct AttnP {
+    const bf16* q;      // [T][n_heads][128]
+    int n_heads, n_kv;
+    TokView tv;
+    KVView kv;
+    int layer;
+    int chunk;          // keys per split (multiple of 16)
+    int n_splits;       // grid.x; partial buffers have this many slots per (token, head)
+    float* part_o;      // [T][n_heads][n_splits][128]
+    float* part_ml;     // [T][n_heads][n_splits][2]
+    int* counters;      // [T][n_kv]
+    bf16* out;          // [T][n_heads * 128]
+    float scale_log2;   // head_dim^-0.5 * log2(e)
+};
+
+constexpr int AW = 4;  // warps per CTA
+
+__global__ void __launch_bounds__(AW * 32) k_attn_paged(AttnP p) {
+    pdl_wait();
+    const int t = blockIdx.z, g = blockIdx.y, s = blockIdx.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int pos = p.tv.pos[t], seq = p.tv.seq[t];
+    const int n_keys = pos + 1;
+    const int n_act = (n_keys + p.chunk - 1) / p.chunk;
+    if (s >= n_act) return;
+    const int k0 = s * p.chunk, k1 = min(k0 + p.chunk, n_keys);
+    const int half = lane >> 4, dl = (lane & 15) * 8;
+
+    float q0[8], q1[8];
+    {
+        const bf16* qp = p.q + ((size_t)t * p.n_heads + 2 * g) * 128 + dl;
+        const uint4 a = *reinterpret_cast<const uint4*>(qp);
+        const uint4 b = *reinterpret_cast<const uint4*>(qp + 128);
+        const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            q0[2 * i] = bf_lo(aw[i]) * p.scale_log2;
+            q0[2 * i + 1] = bf_hi(aw[i]) * p.scale_log2;
+            q1[2 * i] = bf_lo(bw[i]) * p.scale_log2;
+            q1[2 * i + 1] = bf_hi(bw[i]) * p.scale_log2;
+        }
+    }
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float o0[8], o1[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o0[i] = o1[i] = 0.f;
+
+    const bf16* Kl = p.kv.k + (size_t)p.layer * p.kv.layer_stride;
+    const bf16* Vl = p.kv.v + (size_t)p.layer * p.kv.layer_stride;
+    const int* pt = p.kv.page_table + (size_t)seq * p.kv.max_pages_per_seq;
+    const int p0 = k0 >> 4, p1 = (k1 + 15) >> 4;
+
+    for (int pg = p0 + warp; pg < p1; pg += AW) {
+        const int page = pt[pg];
+        if (page < 0 || page >= p.kv.n_pages) continue;  // reported by the append kernel
+        const int nvalid = min(16, k1 - pg * 16);
+        const size_t off = ((size_t)page * p.n_kv + g) * 16 * 128 + dl;
+        uint4 kr[8], vr[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) kr[i] = ldg_nc(Kl + off + (size_t)(2 * i + half) * 128);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) vr[i] = ldg_nc(Vl + off + (size_t)(2 * i + half) * 128);
+        float s0[8], s1[8];
+        float pm0 = -INFINITY, pm1 = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float d0 = half_warp_sum(dot8q(q0, kr[i]));
+            const float d1 = half_warp_sum(dot8q(q1, kr[i]));
+            const bool valid = (2 * i + half) < nvalid;
+            s0[i] = valid ? d0 : -INFINITY;
+            s1[i] = valid ? d1 : -INFINITY;
+            pm0 = fmaxf(pm0, s0[i]);
+            pm1 = fmaxf(pm1, s1[i]);
+        }
+        pm0 = fmaxf(pm0, __shfl_xor_sync(0xffffffffu, pm0, 16));
+        pm1 = fmaxf(pm1, __shfl_xor_sync(0xffffffffu, pm1, 16));
+        const float n0 = fmaxf(m0, pm0), n1 = fmaxf(m1, pm1);
+        const float a0 = exp2f(m0 - n0), a1 = exp2f(m1 - n1);
+        m0 = n0;
+        m1 = n1;
+        l0 *= a0;
+        l1 *= a1;
+#pragma unroll
+        for (int d = 0; d < 8; ++d) {
+            o0[d] *= a0;
+            o1[d] *= a1;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float e0 = exp2f(s0[i] - m0), e1 = exp2f(s1[i] - m1);
+            l0 += e0;
+            l1 += e1;
+            const uint32_t vw[4] = {vr[i].x, vr[i].y, vr[i].z, vr[i].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float va = bf_lo(vw[j]), vb = bf_hi(vw[j]);
+                o0[2 * j] = fmaf(e0, va, o0[2 * j]);
+                o0[2 * j + 1] = fmaf(e0, vb, o0[2 * j + 1]);
+                o1[2 * j] = fmaf(e1, va, o1[2 * j]);
+                o1[2 * j + 1] = fmaf(e1, vb, o1[2 * j + 1]);
+            }
+        }
+    }
+    // the two half-warps saw alternate keys with the same running max
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 16);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 16);
+#pragma unroll
+    for (int d = 0; d < 8; ++d) {
+        o0[d] += __shfl_xor_sync(0xffffffffu, o0[d], 16);
+        o1[d] += __shfl_xor_sync(0xffffffffu, o1[d], 16);
+    }
+
+    __shared__ float sm_o[AW][2][128];
+    __shared__ float sm_m[AW][2], sm_l[AW][2];
+    __shared__ int sm_last;
+    if (lane < 16) {
+#pragma unroll
+        for (int d = 0; d < 8; ++d) {
+            sm_o[warp][0][dl + d] = o0[d];
+            sm_o[warp][1][dl + d] = o1[d];
+        }
+    }
+    if (lane == 0) {
+        sm_m[warp][0] = m0;
+        sm_m[warp][1] = m1;
+        sm_l[warp][0] = l0;
+        sm_l[warp][1] = l1;
+    }
+    __syncthreads();
+
+    // 128 threads: thread -> (head hh, dims 2*(tid%64), +1)
+    const int hh = threadIdx.x >> 6, d2 = (threadIdx.x & 63) * 2;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < AW; ++w) M = fmaxf(M, sm_m[w][hh]);
+    float L = 0.f, O0 = 0.f, O1 = 0.f;
+#pragma unroll
+    for (int w = 0; w < AW; ++w) {
+        const float f = exp2f(sm_m[w][hh] - M);
+        L += sm_l[w][hh] * f;
+        O0 += sm_o[w][hh][d2] * f;
+        O1 += sm_o[w][hh][d2 + 1] * f;
+    }
+    const int head = 2 * g + hh;
+    bf16* outp = p.out + ((size_t)t * p.n_heads + head) * 128 + d2;
+    if (n_act == 1) {
+        *reinterpret_cast<uint32_t*>(outp) = pack_bf2(O0 / L, O1 / L);
+        pdl_launch();
+        return;
+    }
+    const size_t slot = ((size_t)t * p.n_heads + head) * p.n_splits + s;
+    *reinterpret_cast<float2*>(p.part_o + slot * 128 + d2) = make_float2(O0, O1);
+    if ((threadIdx.x & 63) == 0) *reinterpret_cast<float2*>(p.part_ml + slot * 2) = make_float2(M, L);
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const int ticket = atomicAdd(p.counters + (size_t)t * p.n_kv + g, 1);
+        sm_last = (ticket == n_act - 1);
+    }
+    __syncthreads();
+    if (!sm_last) return;
+    __threadfence();
+    const size_t base = ((size_t)t * p.n_heads + head) * p.n_splits;
+    float MM = -INFINITY;
+    for (int j = 0; j < n_act; ++j) MM = fmaxf(MM, __ldcg(p.part_ml + (base + j) * 2));
+    float LL = 0.f, A0 = 0.f, A1 = 0.f;
+    for (int j = 0; j < n_act; ++j) {
+        const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml + (base + j) * 2));
+        const float f = exp2f(ml.x - MM);
+        const float2 ov = __ldcg(reinterpret_cast<const float2*>(p.part_o + (base + j) * 128 + d2));
+        LL += ml.y * f;
+        A0 += ov.x * f;
+        A1 += ov.y * f;
+    }
+    *reinterpret_cast<uint32_t*>(outp) = pack_bf2(A0 / LL, A1 / LL);
+    if (threadIdx.x == 0) p.counters[(size_t)t * p.n_kv + g] = 0;
+    pdl_launch();
+}
+
+cudaError_t launch_attn_paged(const LaunchCtx& c, int T, int layer, const bf16* q, int n_heads,
+                              int n_kv, TokView tv, KVView kv, int chunk, int n_splits,
+                              float* part_o, float* part_ml, int* counters, bf16* out) {
+    AttnP p;
+    p.q = q;
+    p.n_heads = n_heads;
+    p.n_kv = n_kv;
+    p.tv = tv;
+    p.kv = kv;
+    p.layer = layer;
+    p.chunk = chunk;
+    p.n_splits = n_splits;
+    p.part_o = part_o;
+    p.part_ml = part_ml;
+    p.counters = counters;
+    p.out = out;
+    p.scale_log2 = 0.08838834764831845f * 1.4426950408889634f;  // 128^-0.5 * log2(e)
+    return launch_k(c, k_attn_paged, dim3(n_splits, n_kv, T), dim3(AW * 32), 0, p);
+}

@@ -1,0 +1,414 @@
+// Tensor-core GEMM for the projections of the decoder (Pasos 5, 6 and 8 of "Dentro de un
+// LLM: Inferencia en Python puro para Qwen3-0.6B en MLX") when a call carries more than 8
+// token rows: prefill and batched decode.
+//
+// The product is computed transposed, D^T[m][t] = sum_k W[m][k] * H[t][k]: the weight tile
+// (128 output features) is the A operand and the token tile (BN = 64/128/256 rows) the B
+// operand, both K-major bf16 in shared memory with the 128-byte swizzle, fed by TMA
+// (cp.async.bulk.tensor) through an mbarrier ring. One elected thread issues
+// tcgen05.mma.cta_group::1.kind::f16 (M=128, N=BN, K=16) into an fp32 accumulator in TMEM;
+// the four epilogue warps read it back with tcgen05.ld.32x32b (thread = output feature,
+// registers = tokens), so every store of a token row is a coalesced 32-feature run.
+// Epilogues: plain fp32 store (q|k|v), residual add into the fp32 stream (o_proj,
+// down_proj), SiLU(gate) * up from two accumulators fed by the gate and up tiles (SwiGLU),
+// and the LM head's per-token argmax (+ optional logits).
+//
+// Every mbarrier wait is bounded: after ~2 s it sets QW_DEV_TIMEOUT in the status word and
+// the CTA skips the rest of its work, frees its TMEM and exits.
+#include <utility>
+
+#include "qw_internal.h"
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;  // 64 bf16 = 128 bytes = one swizzle row
+constexpr int GEMM_THREADS = 192;
+constexpr unsigned long long kWaitNs = 2000000000ull;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase with the given parity. Returns false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    uint32_t n = 0;
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((++n & 255u) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > kWaitNs) return false;
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)map) : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row groups 1024 B
+// apart (SBO), descriptor version 1, start address in 16-byte units.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)1 << 16;            // leading byte offset (unused for swizzled K-major)
+    d |= (uint64_t)(1024 >> 4) << 32;  // stride byte offset
+    d |= (uint64_t)1 << 46;            // version
+    d |= (uint64_t)2 << 61;            // SWIZZLE_128B
+    return d;
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulate, bf16 A and B, both K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+#define TMEM_LD32(taddr, r)                                                                              \
+    asm volatile(                                                                                        \
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15," \
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"                       \
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),           \
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),       \
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),    \
+          "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),    \
+          "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])                                            \
+        : "r"(taddr))
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+template <int BN, int NA>
+struct GemmCfg {
+    static constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int STAGE_BYTES = NA * A_BYTES + B_BYTES;
+    static constexpr int STAGES = (200 * 1024 / STAGE_BYTES) > 8 ? 8 : (200 * 1024 / STAGE_BYTES);
+    static constexpr int TMEM_COLS_RAW = NA * BN;
+    static constexpr int TMEM_COLS = TMEM_COLS_RAW <= 32 ? 32 : TMEM_COLS_RAW <= 64 ? 64
+                                   : TMEM_COLS_RAW <= 128 ? 128 : TMEM_COLS_RAW <= 256 ? 256 : 512;
+    static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + 256;
+};
+
+struct GemmKParams {
+    int a_row0, a2_row0, K, T, ld_out;
+    float* out_f32;
+    bf16* out_bf16;
+    float* logits;
+    unsigned long long* best;
+    int* status;
+};
+
+}  // namespace
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
+              const __grid_constant__ CUtensorMap tmB, GemmKParams p) {
+    constexpr int NA = (EPI == EPI_SILU_MUL) ? 2 : 1;
+    using C = GemmCfg<BN, NA>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + C::STAGES;
+    uint64_t* accf = bars + 2 * C::STAGES;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    unsigned long long* sbest = reinterpret_cast<unsigned long long*>(smem_raw);  // reused after the main loop
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m_tile = blockIdx.x, n0 = blockIdx.y * BN;
+    const int nk = p.K / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(smem_u32(full + s), 1);
+            mbar_init(smem_u32(empty + s), 1);
+        }
+        mbar_init(smem_u32(accf), 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 4 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        if (NA == 2) tma_prefetch_desc(&tmA2);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 5) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(C::TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    pdl_wait();
+
+    if (warp == 4) {
+        // ---------------- TMA producer ----------------
+        if (lane == 0) {
+            for (int kb = 0; kb < nk; ++kb) {
+                const int s = kb % C::STAGES;
+                const uint32_t ph = (uint32_t)(kb / C::STAGES) & 1u;
+                if (!mbar_wait(smem_u32(empty + s), ph ^ 1u, abort_flag)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                const uint32_t st = smem_u32(smem + s * C::STAGE_BYTES);
+                mbar_expect_tx(smem_u32(full + s), C::STAGE_BYTES);
+                tma_load_2d(st, &tmA, smem_u32(full + s), kb * BK, p.a_row0 + m_tile * BM);
+                if (NA == 2) tma_load_2d(st + C::A_BYTES, &tmA2, smem_u32(full + s), kb * BK, p.a2_row0 + m_tile * BM);
+                tma_load_2d(st + NA * C::A_BYTES, &tmB, smem_u32(full + s), kb * BK, n0);
+            }
+        }
+    } else if (warp == 5) {
+        // ---------------- MMA issuer ----------------
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_bf16(BM, BN);
+            bool ok = true;
+            for (int kb = 0; kb < nk; ++kb) {
+                const int s = kb % C::STAGES;
+                const uint32_t ph = (uint32_t)(kb / C::STAGES) & 1u;
+                if (!mbar_wait(smem_u32(full + s), ph, abort_flag)) {
+                    ok = false;
+                    *abort_flag = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t st = smem_u32(smem + s * C::STAGE_BYTES);
+                const uint64_t ad = sw128_desc(st);
+                const uint64_t bd = sw128_desc(st + NA * C::A_BYTES);
+#pragma unroll
+                for (int k = 0; k < BK / 16; ++k) {
+                    const uint32_t acc = (kb > 0 || k > 0) ? 1u : 0u;
+                    umma_bf16(tmem, ad + 2 * k, bd + 2 * k, idesc, acc);
+                    if (NA == 2) {
+                        const uint64_t a2 = sw128_desc(st + C::A_BYTES);
+                        umma_bf16(tmem + BN, a2 + 2 * k, bd + 2 * k, idesc, acc);
+                    }
+                }
+                umma_commit(smem_u32(empty + s));  // frees the stage once these MMAs finish
+            }
+            if (ok) umma_commit(smem_u32(accf));
+        }
+    } else {
+        // ---------------- epilogue warps 0-3: TMEM lanes 32w .. 32w+31 ----------------
+        const bool ok = mbar_wait(smem_u32(accf), 0u, abort_flag);
+        tc_fence_after();
+        if (!ok) {
+            if (lane == 0) atomicOr(p.status, QW_DEV_TIMEOUT);
+        } else {
+            const int f = m_tile * BM + warp * 32 + lane;  // output feature of this thread
+            const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                uint32_t r[32];
+                TMEM_LD32(trow + c0, r);
+                if (EPI == EPI_SILU_MUL) {
+                    uint32_t u[32];
+                    TMEM_LD32(trow + BN + c0, u);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int tok = n0 + c0 + j;
+                        if (tok < p.T) {
+                            const float g = __uint_as_float(r[j]), uu = __uint_as_float(u[j]);
+                            p.out_bf16[(size_t)tok * p.ld_out + f] = __float2bfloat16_rn(g / (1.0f + expf(-g)) * uu);
+                        }
+                    }
+                } else {
+                    tmem_wait_ld();
+                    if (EPI == EPI_STORE_F32) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const int tok = n0 + c0 + j;
+                            if (tok < p.T) p.out_f32[(size_t)tok * p.ld_out + f] = __uint_as_float(r[j]);
+                        }
+                    } else if (EPI == EPI_RESID_F32) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const int tok = n0 + c0 + j;
+                            if (tok < p.T) p.out_f32[(size_t)tok * p.ld_out + f] += __uint_as_float(r[j]);
+                        }
+                    } else {  // EPI_ARGMAX
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            const int tok = n0 + c0 + j;
+                            const float v = __uint_as_float(r[j]);
+                            if (p.logits && tok < p.T) p.logits[(size_t)tok * p.ld_out + f] = v;
+                            const unsigned long long key = warp_max_u64(argmax_key(v, f));
+                            if (lane == 0) sbest[warp * BN + c0 + j] = key;
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (EPI == EPI_ARGMAX && *abort_flag == 0) {
+        for (int c = threadIdx.x; c < BN; c += GEMM_THREADS) {
+            const int tok = n0 + c;
+            if (tok < p.T) {
+                unsigned long long b = sbest[c];
+                for (int w = 1; w < 4; ++w) b = u64_max(b, sbest[w * BN + c]);
+                atomicMax(p.best + tok, b);
+            }
+        }
+    }
+    if (*abort_flag && threadIdx.x == 0) atomicOr(p.status, QW_DEV_TIMEOUT);
+    if (warp == 5) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS)
+                     : "memory");
+    }
+    pdl_launch();
+}
+
+namespace {
+
+template <int BN, int EPI>
+cudaError_t gemm_go(const LaunchCtx& c, const GemmArgs& a, int bn_idx) {
+    constexpr int NA = (EPI == EPI_SILU_MUL) ? 2 : 1;
+    using C = GemmCfg<BN, NA>;
+    static_assert(C::SMEM <= 227 * 1024, "shared memory budget");
+    static_assert(4 * BN * 8 <= C::STAGES * C::STAGE_BYTES, "argmax scratch fits in the stage ring");
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    GemmKParams p;
+    p.a_row0 = a.a_row0;
+    p.a2_row0 = a.a2_row0;
+    p.K = a.K;
+    p.T = a.T;
+    p.ld_out = a.ld_out;
+    p.out_f32 = a.out_f32;
+    p.out_bf16 = a.out_bf16;
+    p.logits = a.logits;
+    p.best = a.best;
+    p.status = a.status;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.M / BM, (a.T + BN - 1) / BN);
+    cfg.blockDim = dim3(GEMM_THREADS);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = c.stream;
+    cudaLaunchAttribute attr[1];
+    cfg.numAttrs = 0;
+    if (c.pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    if (c.counter) ++*c.counter;
+    return cudaLaunchKernelEx(&cfg, k_gemm_tc<BN, EPI>, *a.tmA, *a.tmA2, a.tmB[bn_idx], p);
+}
+
+template <int EPI>
+cudaError_t gemm_bn(const LaunchCtx& c, const GemmArgs& a) {
+    if (a.T <= 64) return gemm_go<64, EPI>(c, a, 0);
+    if (a.T <= 128) return gemm_go<128, EPI>(c, a, 1);
+    return gemm_go<256, EPI>(c, a, 2);
+}
+
+typedef CUresult (*PFN_encodeTiled_t)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                      const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                      CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+PFN_encodeTiled_t get_encode() {
+    static PFN_encodeTiled_t fn = nullptr;
+    if (!fn) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_encodeTiled_t)ptr;
+    }
+    return fn;
+}
+
+bool encode_one(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    PFN_encodeTiled_t enc = get_encode();
+    if (!enc) return false;
+    if (((uintptr_t)base & 15) || (cols * 2) % 16) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+// box_rows == 0: encode three maps at map[0..2] with token boxes of 64, 128 and 256 rows.
+bool gemm_tc_encode_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    if (box_rows) return encode_one(map, base, rows, cols, box_rows);
+    return encode_one(map + 0, base, rows, cols, 64) && encode_one(map + 1, base, rows, cols, 128) &&
+           encode_one(map + 2, base, rows, cols, 256);
+}
+
+cudaError_t launch_gemm_tc(const LaunchCtx& c, int epi, const GemmArgs& a) {
+    if (a.M % BM || a.K % BK || a.T < 1) return cudaErrorInvalidValue;
+    switch (epi) {
+        case EPI_STORE_F32: return gemm_bn<EPI_STORE_F32>(c, a);
+        case EPI_RESID_F32: return gemm_bn<EPI_RESID_F32>(c, a);
+        case EPI_SILU_MUL: return gemm_bn<EPI_SILU_MUL>(c, a);
+        case EPI_ARGMAX: return gemm_bn<EPI_ARGMAX>(c, a);
+        default: return cudaErrorInvalidValue;
+    }
+}

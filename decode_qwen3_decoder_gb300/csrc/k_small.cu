@@ -1,0 +1,543 @@
+// Bandwidth-bound kernels of the decoder step: step bookkeeping + embedding gather,
+// RMSNorm, the small-batch GEMV family (RMSNorm fused in the prologue), QK-norm + RoPE +
+// paged KV append, the argmax finalize, and the synthetic KV fill.
+//
+// Page: "Dentro de un LLM: Inferencia en Python puro para Qwen3-0.6B en MLX".
+#include <utility>
+
+#include "qw_internal.h"
+
+namespace {
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(const LaunchCtx& c, void (*kern)(KArgs...), dim3 grid, dim3 block,
+                     size_t smem, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = c.stream;
+    cudaLaunchAttribute attr[1];
+    cfg.numAttrs = 0;
+    if (c.pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    if (c.counter) ++*c.counter;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+    uint4 r;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p));
+    return r;
+}
+
+// 8 bf16 weights (one 16-byte chunk) against 8 fp32 activations.
+__device__ __forceinline__ float dot8(const uint4 w, const float4 a0, const float4 a1, float acc) {
+    acc = fmaf(bf_lo(w.x), a0.x, acc);
+    acc = fmaf(bf_hi(w.x), a0.y, acc);
+    acc = fmaf(bf_lo(w.y), a0.z, acc);
+    acc = fmaf(bf_hi(w.y), a0.w, acc);
+    acc = fmaf(bf_lo(w.z), a1.x, acc);
+    acc = fmaf(bf_hi(w.z), a1.y, acc);
+    acc = fmaf(bf_lo(w.w), a1.z, acc);
+    acc = fmaf(bf_hi(w.w), a1.w, acc);
+    return acc;
+}
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g)); }
+
+}  // namespace
+
+// =======================================================================================
+// Step begin: embedding gather (Paso 2) + per-token sequence/position bookkeeping (Paso 9:
+// positions continue from the sequence's current length).
+// =======================================================================================
+__global__ void __launch_bounds__(256) k_step_begin(StepDesc sd, const int32_t* __restrict__ ids,
+                                                    const bf16* __restrict__ embed, int vocab,
+                                                    int hidden, float* __restrict__ x, TokView tv,
+                                                    KVView kv, int* status) {
+    pdl_wait();
+    const int t = blockIdx.x;
+    int b = 0;
+    while (b + 1 < sd.B && sd.start[b + 1] <= t) ++b;
+    const int id = ids[t];
+    const bool bad = (id < 0) || (id >= vocab);
+    const bf16* src = embed + (size_t)(bad ? 0 : id) * hidden;
+    float* dst = x + (size_t)t * hidden;
+    for (int k = threadIdx.x * 4; k < hidden; k += blockDim.x * 4) {
+        uint2 w = *reinterpret_cast<const uint2*>(src + k);
+        float4 o = bad ? make_float4(0.f, 0.f, 0.f, 0.f)
+                       : make_float4(bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y));
+        *reinterpret_cast<float4*>(dst + k) = o;
+    }
+    if (threadIdx.x == 0) {
+        const int seq = sd.seq[b];
+        tv.seq[t] = seq;
+        tv.pos[t] = kv.len[seq] + (t - sd.start[b]);
+        if (t == sd.start[b + 1] - 1) tv.last[b] = t;
+        if (bad) atomicOr(status, QW_DEV_BAD_TOKEN);
+    }
+    pdl_launch();
+}
+
+cudaError_t launch_step_begin(const LaunchCtx& c, const StepDesc& sd, const int32_t* ids,
+                              const bf16* embed, int vocab, int hidden, float* x, TokView tv,
+                              KVView kv, int* status) {
+    return launch_k(c, k_step_begin, dim3(sd.T), dim3(256), 0, sd, ids, embed, vocab, hidden, x, tv,
+                    kv, status);
+}
+
+// =======================================================================================
+// RMSNorm (Paso 3) of fp32 rows into bf16 GEMM operands: h = x * rsqrt(mean(x^2) + eps) * w.
+// One warp per row; `rows` optionally gathers (the LM head reads each sequence's last row).
+// =======================================================================================
+__global__ void __launch_bounds__(256) k_rmsnorm(const float* __restrict__ x, const int* __restrict__ rows,
+                                                 int n_rows, int hidden, const bf16* __restrict__ w,
+                                                 float eps, bf16* __restrict__ h) {
+    pdl_wait();
+    const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (r < n_rows) {
+        const float* xr = x + (size_t)(rows ? rows[r] : r) * hidden;
+        float ss = 0.f;
+        for (int k = lane * 4; k < hidden; k += 128) {
+            float4 v = *reinterpret_cast<const float4*>(xr + k);
+            ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+        }
+        const float rs = rsqrtf(warp_sum(ss) / (float)hidden + eps);
+        bf16* hr = h + (size_t)r * hidden;
+        for (int k = lane * 4; k < hidden; k += 128) {
+            float4 v = *reinterpret_cast<const float4*>(xr + k);
+            uint2 wb = *reinterpret_cast<const uint2*>(w + k);
+            uint2 o;
+            o.x = pack_bf2(v.x * rs * bf_lo(wb.x), v.y * rs * bf_hi(wb.x));
+            o.y = pack_bf2(v.z * rs * bf_lo(wb.y), v.w * rs * bf_hi(wb.y));
+            *reinterpret_cast<uint2*>(hr + k) = o;
+        }
+    }
+    pdl_launch();
+}
+
+cudaError_t launch_rmsnorm(const LaunchCtx& c, const float* x, const int* rows, int n_rows,
+                           int hidden, const bf16* w, float eps, bf16* h) {
+    return launch_k(c, k_rmsnorm, dim3((n_rows + 7) / 8), dim3(256), 0, x, rows, n_rows, hidden, w,
+                    eps, h);
+}
+
+// =======================================================================================
+// GEMV family for T <= 8 token rows: out[t][n] = sum_k W[n][k] * a[t][k].
+//
+// Each warp owns RPW output rows at a time; every lane streams one 16-byte chunk of each
+// row per 256 columns, so a warp reads whole rows with coalesced 512-byte requests, in
+// passes of 1024 columns that keep RPW*4 16-byte loads per lane in flight. The activations sit in
+// shared memory as fp32. MODE selects the prologue/epilogue:
+//   G_QKV    : a = bf16(rms_norm(x) * w_in)  (Paso 3 fused), out fp32 (Paso 5 projections)
+//   G_GATEUP : a = bf16(rms_norm(x) * w_post), act = bf16(silu(Wg a) * (Wu a))  (Paso 6)
+//   G_RESID  : a = bf16 activations, x += W a  (o_proj / down_proj + residual, Paso 7)
+//   G_LMHEAD : a = bf16(rms_norm(x[last]) * w_final), logits, packed argmax (Paso 8)
+// =======================================================================================
+enum { G_QKV = 0, G_GATEUP = 1, G_RESID = 2, G_LMHEAD = 3 };
+
+struct GemvP {
+    const float* x;
+    const int* rows;
+    const bf16* norm_w;
+    float eps;
+    const bf16* act;
+    const bf16* W;
+    const bf16* W2;
+    int n_out;
+    int K;
+    int T;
+    float* out;
+    bf16* out_bf16;
+    unsigned long long* best;
+};
+
+constexpr int GEMV_WARPS = 4;
+
+template <int TT, int MODE, int KC, int RPW>
+__global__ void __launch_bounds__(GEMV_WARPS * 32) k_gemv(GemvP p) {
+    extern __shared__ float4 smem_f4[];
+    float* hs = reinterpret_cast<float*>(smem_f4);  // [TT][K] fp32
+    constexpr int K = KC * 256;
+    constexpr int NW = (MODE == G_GATEUP) ? 2 : 1;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    pdl_wait();
+
+    // ---- prologue: activations into shared memory --------------------------------------
+    if (MODE == G_RESID) {
+        for (int i = tid; i < TT * K / 8; i += blockDim.x) {
+            const int t = i / (K / 8), k8 = (i % (K / 8)) * 8;
+            float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+            if (t < p.T) {
+                uint4 w = *reinterpret_cast<const uint4*>(p.act + (size_t)t * K + k8);
+                a0 = make_float4(bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y));
+                a1 = make_float4(bf_lo(w.z), bf_hi(w.z), bf_lo(w.w), bf_hi(w.w));
+            }
+            *reinterpret_cast<float4*>(hs + t * K + k8) = a0;
+            *reinterpret_cast<float4*>(hs + t * K + k8 + 4) = a1;
+        }
+    } else {
+        __shared__ float rs[TT];
+        for (int t = warp; t < TT; t += GEMV_WARPS) {
+            float ss = 0.f;
+            if (t < p.T) {
+                const float* xr = p.x + (size_t)(p.rows ? p.rows[t] : t) * K;
+                for (int k = lane * 4; k < K; k += 128) {
+                    float4 v = *reinterpret_cast<const float4*>(xr + k);
+                    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+                }
+            }
+            ss = warp_sum(ss);
+            if (lane == 0) rs[t] = rsqrtf(ss / (float)K + p.eps);
+        }
+        __syncthreads();
+        for (int i = tid; i < TT * K / 4; i += blockDim.x) {
+            const int t = i / (K / 4), k4 = (i % (K / 4)) * 4;
+            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (t < p.T) {
+                const float* xr = p.x + (size_t)(p.rows ? p.rows[t] : t) * K;
+                float4 v = *reinterpret_cast<const float4*>(xr + k4);
+                uint2 wb = *reinterpret_cast<const uint2*>(p.norm_w + k4);
+                const float r = rs[t];
+                // round to bf16: the projection operand precision of the tensor-core path
+                uint32_t lo = pack_bf2(v.x * r * bf_lo(wb.x), v.y * r * bf_hi(wb.x));
+                uint32_t hi = pack_bf2(v.z * r * bf_lo(wb.y), v.w * r * bf_hi(wb.y));
+                o = make_float4(bf_lo(lo), bf_hi(lo), bf_lo(hi), bf_hi(hi));
+            }
+            *reinterpret_cast<float4*>(hs + t * K + k4) = o;
+        }
+    }
+    __syncthreads();
+
+    // ---- main loop ---------------------------------------------------------------------
+    const int gw = blockIdx.x * GEMV_WARPS + warp;
+    const int nw = gridDim.x * GEMV_WARPS;
+    unsigned long long best[TT];
+#pragma unroll
+    for (int t = 0; t < TT; ++t) best[t] = 0ull;
+
+    for (int r0 = gw * RPW; r0 < p.n_out; r0 += nw * RPW) {
+        float acc[RPW][NW][TT];
+#pragma unroll
+        for (int rr = 0; rr < RPW; ++rr)
+#pragma unroll
+            for (int n = 0; n < NW; ++n)
+#pragma unroll
+                for (int t = 0; t < TT; ++t) acc[rr][n][t] = 0.f;
+        // passes of 4 chunks (1024 columns): RPW*NW*4 16-byte loads in flight per lane
+#pragma unroll 1
+        for (int c0 = 0; c0 < KC; c0 += 4) {
+            uint4 wv[RPW][NW][4];
+#pragma unroll
+            for (int rr = 0; rr < RPW; ++rr) {
+                const int row = min(r0 + rr, p.n_out - 1);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const size_t off = (size_t)row * K + (c0 + c) * 256 + lane * 8;
+                    wv[rr][0][c] = ldg_stream(p.W + off);
+                    if (NW == 2) wv[rr][NW - 1][c] = ldg_stream(p.W2 + off);
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                for (int t = 0; t < TT; ++t) {
+                    const float* a = hs + t * K + (c0 + c) * 256 + lane * 8;
+                    const float4 a0 = *reinterpret_cast<const float4*>(a);
+                    const float4 a1 = *reinterpret_cast<const float4*>(a + 4);
+#pragma unroll
+                    for (int rr = 0; rr < RPW; ++rr)
+#pragma unroll
+                        for (int n = 0; n < NW; ++n) acc[rr][n][t] = dot8(wv[rr][n][c], a0, a1, acc[rr][n][t]);
+                }
+            }
+        }
+#pragma unroll
+        for (int rr = 0; rr < RPW; ++rr) {
+            const int row = r0 + rr;
+#pragma unroll
+            for (int n = 0; n < NW; ++n)
+#pragma unroll
+                for (int t = 0; t < TT; ++t) acc[rr][n][t] = warp_sum(acc[rr][n][t]);
+            if (row < p.n_out) {
+#pragma unroll
+                for (int t = 0; t < TT; ++t) {
+                    if (lane == t && t < p.T) {
+                        if (MODE == G_QKV) {
+                            p.out[(size_t)t * p.n_out + row] = acc[rr][0][t];
+                        } else if (MODE == G_RESID) {
+                            p.out[(size_t)t * p.n_out + row] += acc[rr][0][t];
+                        } else if (MODE == G_GATEUP) {
+                            const float g = acc[rr][0][t], u = acc[rr][NW - 1][t];
+                            p.out_bf16[(size_t)t * p.n_out + row] = __float2bfloat16_rn(silu_f(g) * u);
+                        } else {
+                            if (p.out) p.out[(size_t)t * p.n_out + row] = acc[rr][0][t];
+                            best[t] = u64_max(best[t], argmax_key(acc[rr][0][t], row));
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    if (MODE == G_LMHEAD) {
+        __shared__ unsigned long long sbest[GEMV_WARPS][TT];
+#pragma unroll
+        for (int t = 0; t < TT; ++t)
+            if (lane == t) sbest[warp][t] = best[t];
+        __syncthreads();
+        if (tid < TT && tid < p.T) {
+            unsigned long long b = 0ull;
+            for (int w = 0; w < GEMV_WARPS; ++w) b = u64_max(b, sbest[w][tid]);
+            atomicMax(p.best + tid, b);
+        }
+    }
+    pdl_launch();
+}
+
+namespace {
+
+int g_num_sms = 0;
+
+int num_sms() {
+    if (g_num_sms == 0) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
+        if (g_num_sms <= 0) g_num_sms = 148;
+    }
+    return g_num_sms;
+}
+
+template <int TT, int MODE, int KC, int RPW>
+cudaError_t gemv_go(const LaunchCtx& c, const GemvP& p, int max_ctas) {
+    const size_t smem = (size_t)TT * KC * 256 * sizeof(float);
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(k_gemv<TT, MODE, KC, RPW>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    const int per_cta = GEMV_WARPS * RPW;
+    int grid = (p.n_out + per_cta - 1) / per_cta;
+    if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
+    return launch_k(c, k_gemv<TT, MODE, KC, RPW>, dim3(grid), dim3(GEMV_WARPS * 32), smem, p);
+}
+
+// Rows per warp iteration: 4 rows x 4 chunks = 256 bytes in flight per lane for 1-2 tokens;
+// fewer rows for more tokens to bound the fp32 accumulators and activation registers.
+template <int MODE, int KC>
+cudaError_t gemv_kc(const LaunchCtx& c, const GemvP& p, int max_ctas) {
+    constexpr int NW = (MODE == G_GATEUP) ? 2 : 1;
+    // the long-K matrices (o_proj, down_proj) have few rows: fewer rows per warp, more CTAs
+    constexpr int R12 = (KC >= 8 ? 2 : 4) / NW;
+    if (p.T <= 1) return gemv_go<1, MODE, KC, R12>(c, p, max_ctas);
+    if (p.T <= 2) return gemv_go<2, MODE, KC, R12>(c, p, max_ctas);
+    if (p.T <= 4) return gemv_go<4, MODE, KC, 2 / NW>(c, p, max_ctas);
+    return gemv_go<8, MODE, KC, 1>(c, p, max_ctas);
+}
+
+template <int MODE>
+cudaError_t gemv_dispatch(const LaunchCtx& c, const GemvP& p, int max_ctas) {
+    if (p.T < 1 || p.T > 8) return cudaErrorInvalidValue;
+    switch (p.K) {
+        case 1024: return gemv_kc<MODE, 4>(c, p, max_ctas);
+        case 2048: return gemv_kc<MODE, 8>(c, p, max_ctas);
+        case 3072: return gemv_kc<MODE, 12>(c, p, max_ctas);
+        case 4096: return gemv_kc<MODE, 16>(c, p, max_ctas);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_gemv_qkv(const LaunchCtx& c, int T, const float* x, const bf16* norm_w, float eps,
+                            const bf16* W, int n_out, int K, float* out) {
+    GemvP p = {};
+    p.x = x; p.norm_w = norm_w; p.eps = eps; p.W = W; p.n_out = n_out; p.K = K; p.T = T; p.out = out;
+    return gemv_dispatch<G_QKV>(c, p, 0);
+}
+
+cudaError_t launch_gemv_gateup(const LaunchCtx& c, int T, const float* x, const bf16* norm_w,
+                               float eps, const bf16* Wg, const bf16* Wu, int inter, int K, bf16* act) {
+    GemvP p = {};
+    p.x = x; p.norm_w = norm_w; p.eps = eps; p.W = Wg; p.W2 = Wu; p.n_out = inter; p.K = K; p.T = T;
+    p.out_bf16 = act;
+    return gemv_dispatch<G_GATEUP>(c, p, 0);
+}
+
+cudaError_t launch_gemv_resid(const LaunchCtx& c, int T, const bf16* act, const bf16* W, int n_out,
+                              int K, float* x) {
+    GemvP p = {};
+    p.act = act; p.W = W; p.n_out = n_out; p.K = K; p.T = T; p.out = x;
+    return gemv_dispatch<G_RESID>(c, p, 0);
+}
+
+cudaError_t launch_gemv_lmhead(const LaunchCtx& c, int B, const float* x, const int* rows,
+                               const bf16* norm_w, float eps, const bf16* E, int vocab, int K,
+                               float* logits, unsigned long long* best) {
+    GemvP p = {};
+    p.x = x; p.rows = rows; p.norm_w = norm_w; p.eps = eps; p.W = E; p.n_out = vocab; p.K = K;
+    p.T = B; p.out = logits; p.best = best;
+    return gemv_dispatch<G_LMHEAD>(c, p, num_sms() * 8);
+}
+
+// =======================================================================================
+// Finalize: unpack the argmax keys into next ids (lowest index wins ties), clear the keys
+// for the next call and advance each sequence's length by its token count (Paso 9).
+// =======================================================================================
+__global__ void k_finalize(StepDesc sd, unsigned long long* best, int32_t* next_ids, KVView kv) {
+    pdl_wait();
+    for (int b = threadIdx.x; b < sd.B; b += blockDim.x) {
+        const unsigned long long key = best[b];
+        next_ids[b] = (int32_t)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
+        best[b] = 0ull;
+        kv.len[sd.seq[b]] += sd.start[b + 1] - sd.start[b];
+    }
+    pdl_launch();
+}
+
+cudaError_t launch_finalize(const LaunchCtx& c, const StepDesc& sd, unsigned long long* best,
+                            int32_t* next_ids, KVView kv) {
+    return launch_k(c, k_finalize, dim3(1), dim3(256), 0, sd, best, next_ids, kv);
+}
+
+// =======================================================================================
+// QK-norm + RoPE + KV append (Paso 5; Paso 4 for the rotation).
+// One warp per (token, head) over the fp32 q|k|v projection row; lane l holds dims
+// [4l, 4l+4), so dim i and its rotate-half partner i+64 sit in lanes l and l^16.
+//   q, k heads: per-head RMSNorm over head_dim with the shared [head_dim] weight, then the
+//               rotation by pos * theta^(-i/64) (cos/sin from the fp32 table).
+//   v heads   : copied.
+// q is written as bf16 [T][n_heads][128]; k and v go to the page slot
+// page_table[seq][pos / 16] * 16 + pos % 16 of this layer, and to a contiguous bf16
+// [T][2][n_kv][128] copy that the prefill attention reads.
+// =======================================================================================
+__global__ void __launch_bounds__(256) k_qknorm_rope_append(
+    int T, int layer, const float* __restrict__ qkv, const bf16* __restrict__ q_norm,
+    const bf16* __restrict__ k_norm, float eps, const float* __restrict__ rope_cos,
+    const float* __restrict__ rope_sin, int n_heads, int n_kv, TokView tv, KVView kv,
+    bf16* __restrict__ q_out, bf16* __restrict__ kv_new, int32_t* dbg_pos, int32_t* dbg_slot,
+    int* status) {
+    pdl_wait();
+    const int NH = n_heads + 2 * n_kv;
+    const int w = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    const int t = w / NH, hh = w % NH;
+    if (t < T) {
+        const float4 xv = *reinterpret_cast<const float4*>(qkv + ((size_t)t * NH + hh) * 128 + lane * 4);
+        float y[4] = {xv.x, xv.y, xv.z, xv.w};
+        const int pos = tv.pos[t];
+        if (hh < n_heads + n_kv) {
+            const bf16* nw = (hh < n_heads) ? q_norm : k_norm;
+            const float ss = warp_sum(y[0] * y[0] + y[1] * y[1] + y[2] * y[2] + y[3] * y[3]);
+            const float r = rsqrtf(ss * (1.0f / 128.0f) + eps);
+            const uint2 wb = *reinterpret_cast<const uint2*>(nw + lane * 4);
+            y[0] *= r * bf_lo(wb.x);
+            y[1] *= r * bf_hi(wb.x);
+            y[2] *= r * bf_lo(wb.y);
+            y[3] *= r * bf_hi(wb.y);
+            const int i0 = (lane & 15) * 4;
+            const float4 cs = *reinterpret_cast<const float4*>(rope_cos + (size_t)pos * 64 + i0);
+            const float4 sn = *reinterpret_cast<const float4*>(rope_sin + (size_t)pos * 64 + i0);
+            const float c[4] = {cs.x, cs.y, cs.z, cs.w}, s[4] = {sn.x, sn.y, sn.z, sn.w};
+            float o[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float pj = __shfl_xor_sync(0xffffffffu, y[j], 16);
+                o[j] = (lane < 16) ? (y[j] * c[j] - pj * s[j]) : (pj * s[j] + y[j] * c[j]);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) y[j] = o[j];
+        }
+        uint2 packed;
+        packed.x = pack_bf2(y[0], y[1]);
+        packed.y = pack_bf2(y[2], y[3]);
+        if (hh < n_heads) {
+            *reinterpret_cast<uint2*>(q_out + ((size_t)t * n_heads + hh) * 128 + lane * 4) = packed;
+        } else {
+            const int which = (hh - n_heads) / n_kv;  // 0 = K, 1 = V
+            const int g = (hh - n_heads) % n_kv;
+            *reinterpret_cast<uint2*>(kv_new + (((size_t)t * 2 + which) * n_kv + g) * 128 + lane * 4) = packed;
+            const int seq = tv.seq[t];
+            const int pi = pos >> 4;
+            const int page = (pi < kv.max_pages_per_seq) ? kv.page_table[(size_t)seq * kv.max_pages_per_seq + pi] : -1;
+            if (page < 0 || page >= kv.n_pages) {
+                if (lane == 0) atomicOr(status, QW_DEV_BAD_POS);
+            } else {
+                bf16* pool = (which == 0 ? kv.k : kv.v) + (size_t)layer * kv.layer_stride;
+                bf16* dst = pool + (((size_t)page * n_kv + g) * 16 + (pos & 15)) * 128 + lane * 4;
+                *reinterpret_cast<uint2*>(dst) = packed;
+                if (dbg_pos && which == 0 && g == 0 && lane == 0) {
+                    dbg_pos[t] = pos;
+                    dbg_slot[t] = page * 16 + (pos & 15);
+                }
+            }
+        }
+    }
+    pdl_launch();
+}
+
+cudaError_t launch_qknorm_rope_append(const LaunchCtx& c, int T, int layer, const float* qkv,
+                                      const bf16* q_norm, const bf16* k_norm, float eps,
+                                      const float* rope_cos, const float* rope_sin, int n_heads,
+                                      int n_kv, TokView tv, KVView kv, bf16* q_out, bf16* kv_new,
+                                      int32_t* dbg_pos, int32_t* dbg_slot, int* status) {
+    const int warps = T * (n_heads + 2 * n_kv);
+    return launch_k(c, k_qknorm_rope_append, dim3((warps + 7) / 8), dim3(256), 0, T, layer, qkv,
+                    q_norm, k_norm, eps, rope_cos, rope_sin, n_heads, n_kv, tv, kv, q_out, kv_new,
+                    dbg_pos, dbg_slot, status);
+}
+
+// =======================================================================================
+// Synthetic KV fill with the counter-based SplitMix64 generator (Steele, Lea, Flood 2014):
+// element idx -> z = mix(seed + (idx + 1) * golden); b = (int8)(z >> 56); K = b/64, V = b/128.
+// =======================================================================================
+__device__ __forceinline__ unsigned long long splitmix64_at(unsigned long long seed,
+                                                            unsigned long long idx) {
+    unsigned long long z = seed + (idx + 1ull) * 0x9E3779B97F4A7C15ull;
+    z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+    z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+    return z ^ (z >> 31);
+}
+
+__global__ void k_kv_fill(KVView kv, int n_layers, int n_kv, int seq, int n_tokens,
+                          unsigned long long seed) {
+    // grid: (pages of the sequence, n_layers * 2); block: n_kv * 16 * ... threads loop
+    const int pi = blockIdx.x;
+    const int layer = blockIdx.y >> 1, which = blockIdx.y & 1;
+    const int page = kv.page_table[(size_t)seq * kv.max_pages_per_seq + pi];
+    if (page < 0) return;
+    bf16* pool = (which == 0 ? kv.k : kv.v) + (size_t)layer * kv.layer_stride;
+    const float scale = which == 0 ? (1.0f / 64.0f) : (1.0f / 128.0f);
+    for (int e = threadIdx.x; e < n_kv * 16 * 128; e += blockDim.x) {
+        const int g = e / (16 * 128), o = (e / 128) % 16, d = e % 128;
+        const int pos = pi * 16 + o;
+        float val = 0.f;
+        if (pos < n_tokens) {
+            const unsigned long long idx =
+                (((((unsigned long long)(layer * 2 + which)) << 22 | (unsigned long long)pos) * n_kv + g) * 128 + d);
+            const int8_t b = (int8_t)(splitmix64_at(seed, idx) >> 56);
+            val = (float)b * scale;
+        }
+        pool[(((size_t)page * n_kv + g) * 16 + o) * 128 + d] = __float2bfloat16_rn(val);
+    }
+    (void)n_layers;
+}
+
+cudaError_t launch_kv_fill(const LaunchCtx& c, KVView kv, int n_layers, int n_kv, int seq,
+                           int n_tokens, unsigned long long seed) {
+    const int pages = (n_tokens + 15) / 16;
+    if (pages == 0) return cudaSuccess;
+    return launch_k(c, k_kv_fill, dim3(pages, n_layers * 2), dim3(256), 0, kv, n_layers, n_kv, seq,
+                    n_tokens, seed);
+}

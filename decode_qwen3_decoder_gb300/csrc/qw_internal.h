@@ -1,0 +1,150 @@
+// Internal declarations shared by the libqw translation units (host runtime + kernels).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/qw.h"
+
+typedef __nv_bfloat16 bf16;
+
+// Device status bits (ORed into the workspace status word; read by qw_sync_status).
+enum : int {
+    QW_DEV_BAD_TOKEN = 1,
+    QW_DEV_TIMEOUT = 2,
+    QW_DEV_BAD_POS = 4,
+};
+
+// Per-call batch description, passed by value to the step-begin kernel.
+struct StepDesc {
+    int B;                       // sequences in the call
+    int T;                       // tokens in the call
+    int seq[QW_MAX_BATCH];       // sequence id of batch entry b
+    int start[QW_MAX_BATCH + 1]; // token offsets: tokens of entry b are [start[b], start[b+1])
+};
+
+// Device view of the paged KV cache.
+struct KVView {
+    int* len;            // [max_seqs] current length of each sequence
+    int* page_table;     // [max_seqs][max_pages_per_seq], -1 = no page
+    bf16* k;             // [n_layers][n_pages][n_kv][page][head_dim]
+    bf16* v;
+    int max_pages_per_seq;
+    int n_pages;
+    long long layer_stride; // elements per layer of the K (or V) pool
+};
+
+// Per-token bookkeeping written by the step-begin kernel.
+struct TokView {
+    int* seq;  // [T]
+    int* pos;  // [T]
+    int* last; // [B] row of each entry's last token
+};
+
+// ---------------------------------------------------------------------------------------
+// Small device helpers
+// ---------------------------------------------------------------------------------------
+#ifdef __CUDACC__
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float bf2f(bf16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+// Key that orders like the float value, with the lowest index winning ties under max.
+__device__ __forceinline__ unsigned long long argmax_key(float v, int idx) {
+    uint32_t u = __float_as_uint(v);
+    uint32_t k = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return ((unsigned long long)k << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)idx);
+}
+__device__ __forceinline__ unsigned long long u64_max(unsigned long long a, unsigned long long b) {
+    return a > b ? a : b;
+}
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = u64_max(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+// Programmatic dependent launch: wait for the upstream grid's memory / let dependents start.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch() { asm volatile("griddepcontrol.launch_dependents;"); }
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+#endif
+
+// ---------------------------------------------------------------------------------------
+// Launchers (defined in the kernel translation units). All return cudaGetLastError().
+// ---------------------------------------------------------------------------------------
+struct LaunchCtx {
+    cudaStream_t stream;
+    bool pdl;     // launch with programmatic stream serialization
+    int* counter; // incremented per launch (kernel count bookkeeping)
+};
+
+cudaError_t launch_step_begin(const LaunchCtx& c, const StepDesc& sd, const int32_t* ids,
+                              const bf16* embed, int vocab, int hidden, float* x, TokView tv,
+                              KVView kv, int* status);
+cudaError_t launch_rmsnorm(const LaunchCtx& c, const float* x, const int* rows, int n_rows,
+                           int hidden, const bf16* w, float eps, bf16* h);
+// GEMV family (T <= 8 token rows).
+cudaError_t launch_gemv_qkv(const LaunchCtx& c, int T, const float* x, const bf16* norm_w, float eps,
+                            const bf16* W, int n_out, int K, float* out);
+cudaError_t launch_gemv_gateup(const LaunchCtx& c, int T, const float* x, const bf16* norm_w,
+                               float eps, const bf16* Wg, const bf16* Wu, int inter, int K, bf16* act);
+cudaError_t launch_gemv_resid(const LaunchCtx& c, int T, const bf16* act, const bf16* W, int n_out,
+                              int K, float* x);
+cudaError_t launch_gemv_lmhead(const LaunchCtx& c, int B, const float* x, const int* rows,
+                               const bf16* norm_w, float eps, const bf16* E, int vocab, int K,
+                               float* logits, unsigned long long* best);
+cudaError_t launch_finalize(const LaunchCtx& c, const StepDesc& sd, unsigned long long* best,
+                            int32_t* next_ids, KVView kv);
+cudaError_t launch_qknorm_rope_append(const LaunchCtx& c, int T, int layer, const float* qkv,
+                                      const bf16* q_norm, const bf16* k_norm, float eps,
+                                      const float* rope_cos, const float* rope_sin, int n_heads,
+                                      int n_kv, TokView tv, KVView kv, bf16* q_out, bf16* kv_new,
+                                      int32_t* dbg_pos, int32_t* dbg_slot, int* status);
+cudaError_t launch_attn_paged(const LaunchCtx& c, int T, int layer, const bf16* q, int n_heads,
+                              int n_kv, TokView tv, KVView kv, int chunk, int n_splits,
+                              float* part_o, float* part_ml, int* counters, bf16* out);
+cudaError_t launch_attn_prefill(const LaunchCtx& c, const StepDesc& sd, int max_len, const bf16* q,
+                                const bf16* kv_new, int n_heads, int n_kv, bf16* out);
+cudaError_t launch_kv_fill(const LaunchCtx& c, KVView kv, int n_layers, int n_kv, int seq,
+                           int n_tokens, unsigned long long seed);
+
+// tcgen05 GEMM (T > 8 token rows). Epilogue kinds:
+enum GemmEpi : int { EPI_STORE_F32 = 0, EPI_RESID_F32 = 1, EPI_SILU_MUL = 2, EPI_ARGMAX = 3 };
+struct GemmArgs {
+    const CUtensorMap* tmA;   // weights [rows_total, K] bf16, box 128 x 64
+    const CUtensorMap* tmA2;  // second weight (up) for EPI_SILU_MUL, else same as tmA
+    const CUtensorMap* tmB;   // activations [T_cap, K] bf16, box BN x 64
+    int a_row0;               // first weight row of this matrix (layer offset)
+    int a2_row0;
+    int M;                    // output features (multiple of 128)
+    int K;                    // reduction length (multiple of 64)
+    int T;                    // token rows (columns of the transposed product)
+    float* out_f32;           // EPI_STORE_F32: out[t][m]; EPI_RESID_F32: x[t][m] +=
+    int ld_out;
+    bf16* out_bf16;           // EPI_SILU_MUL: act[t][m]
+    float* logits;            // EPI_ARGMAX: optional logits[t][m]
+    unsigned long long* best; // EPI_ARGMAX: per-token packed argmax keys
+    int* status;
+};
+cudaError_t launch_gemm_tc(const LaunchCtx& c, int epi, const GemmArgs& a);
+bool gemm_tc_encode_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                        uint32_t box_rows);

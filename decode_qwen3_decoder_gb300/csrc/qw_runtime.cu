@@ -1,0 +1,849 @@
+// Host runtime of libqw: the C ABI of include/qw.h.
+//
+// Holds the model configuration, packs the weights into the caller's workspace, builds
+// the RoPE table, runs the paged KV allocator, orchestrates the kernels of one prefill or
+// decode step, and captures decode steps into CUDA graphs. Everything here is host code;
+// all arithmetic of the forward pass runs in the kernels of k_*.cu.
+//
+// Page: "Dentro de un LLM: Inferencia en Python puro para Qwen3-0.6B en MLX".
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <set>
+#include <string>
+#include <vector>
+
+#include "qw_internal.h"
+
+// ---------------------------------------------------------------------------------------
+// Errors
+// ---------------------------------------------------------------------------------------
+static thread_local std::string g_err;
+
+static qw_status fail(qw_status s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return s;
+}
+
+#define CUDA_TRY(expr)                                                                        \
+    do {                                                                                      \
+        cudaError_t _e = (expr);                                                              \
+        if (_e != cudaSuccess)                                                                \
+            return fail(QW_ERR_CUDA, "%s failed: %s (%s:%d)", #expr, cudaGetErrorString(_e), \
+                        __FILE__, __LINE__);                                                  \
+    } while (0)
+
+#define QW_TRY(expr)                   \
+    do {                               \
+        qw_status _s = (expr);         \
+        if (_s != QW_OK) return _s;    \
+    } while (0)
+
+extern "C" const char* qw_last_error(void) { return g_err.c_str(); }
+
+// ---------------------------------------------------------------------------------------
+// Configuration and workspace layout
+// ---------------------------------------------------------------------------------------
+static constexpr int kMaxSplits = 128;   // split-KV partial slots per (token, head)
+static constexpr int kSmallT = 8;        // token rows handled by the GEMV family
+
+static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+static bool config_ok(const qw_config* c, std::string* why) {
+    auto bad = [&](const char* m) {
+        if (why) *why = m;
+        return false;
+    };
+    if (!c) return bad("config is NULL");
+    if (c->n_layers < 1) return bad("n_layers must be >= 1");
+    if (c->head_dim != 128) return bad("head_dim must be 128");
+    if (c->n_kv_heads < 1 || c->n_heads != 2 * c->n_kv_heads) return bad("need n_heads == 2 * n_kv_heads");
+    if (c->hidden <= 0 || c->hidden % 256) return bad("hidden must be a positive multiple of 256");
+    if (c->inter <= 0 || c->inter % 256) return bad("inter must be a positive multiple of 256");
+    if ((c->n_heads * c->head_dim) % 256) return bad("n_heads * head_dim must be a multiple of 256");
+    if (c->hidden > 4096 || c->inter > 4096 || c->n_heads * c->head_dim > 4096)
+        return bad("GEMV rows are limited to 4096 columns");
+    if (c->vocab <= 0 || c->vocab % 128) return bad("vocab must be a positive multiple of 128");
+    if (c->page_size != 16) return bad("page_size must be 16");
+    if (c->tie_embed != 1) return bad("only the tied LM head is supported");
+    if (!(c->rms_eps > 0.f)) return bad("rms_eps must be > 0");
+    if (!(c->rope_theta > 1.0)) return bad("rope_theta must be > 1");
+    if (c->max_tokens < 1 || c->max_tokens > (1 << 20)) return bad("max_tokens out of range");
+    if (c->max_batch < 1 || c->max_batch > QW_MAX_BATCH) return bad("max_batch out of range");
+    if (c->max_context < 1 || c->max_context > (1 << 22)) return bad("max_context out of range");
+    return true;
+}
+
+struct WsLayout {
+    size_t wqkv, wo, wg, wu, wd, norms, fnorm, rcos, rsin;
+    size_t x, h, qkv, q, kvnew, attn, act, part_o, part_ml, counters;
+    size_t tok_seq, tok_pos, last, best, status, gen_tok, gen_cur, gen_out;
+    size_t total;
+    int part_T;
+};
+
+static WsLayout layout_for(const qw_config& c) {
+    WsLayout L = {};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t o = off;
+        off = align_up(off + bytes, 256);
+        return o;
+    };
+    const size_t D = c.hidden, I = c.inter, QD = (size_t)c.n_heads * c.head_dim;
+    const size_t KD = (size_t)c.n_kv_heads * c.head_dim, NL = c.n_layers;
+    const size_t QKV = QD + 2 * KD;
+    const size_t T = c.max_tokens;
+    L.wqkv = take(NL * QKV * D * 2);
+    L.wo = take(NL * D * QD * 2);
+    L.wg = take(NL * I * D * 2);
+    L.wu = take(NL * I * D * 2);
+    L.wd = take(NL * D * I * 2);
+    L.norms = take(NL * (2 * D + 2 * c.head_dim) * 2);
+    L.fnorm = take(D * 2);
+    L.rcos = take((size_t)c.max_context * 64 * 4);
+    L.rsin = take((size_t)c.max_context * 64 * 4);
+    L.x = take(T * D * 4);
+    L.h = take(std::max(T, (size_t)c.max_batch) * D * 2);
+    L.qkv = take(T * QKV * 4);
+    L.q = take(T * QD * 2);
+    L.kvnew = take(T * 2 * KD * 2);
+    L.attn = take(T * QD * 2);
+    L.act = take(T * I * 2);
+    L.part_T = std::min<int>(c.max_tokens, std::max(c.max_batch, kSmallT));
+    L.part_o = take((size_t)L.part_T * c.n_heads * kMaxSplits * 128 * 4);
+    L.part_ml = take((size_t)L.part_T * c.n_heads * kMaxSplits * 2 * 4);
+    L.counters = take((size_t)L.part_T * c.n_kv_heads * 4);
+    L.tok_seq = take(T * 4);
+    L.tok_pos = take(T * 4);
+    L.last = take((size_t)c.max_batch * 4);
+    L.best = take((size_t)c.max_batch * 8);
+    L.status = take(4);
+    L.gen_tok = take(T * 4);
+    L.gen_cur = take((size_t)c.max_batch * 4);
+    L.gen_out = take((size_t)c.max_batch * ((size_t)c.max_context + 1) * 4);
+    L.total = off;
+    return L;
+}
+
+// ---------------------------------------------------------------------------------------
+// Model and KV objects
+// ---------------------------------------------------------------------------------------
+struct GraphEntry {
+    cudaGraphExec_t exec;
+    int launches;
+    unsigned long long last_use;
+};
+
+struct qw_model {
+    qw_config cfg;
+    WsLayout L;
+    char* ws;
+    int qkv_rows;
+    bf16 *wqkv, *wo, *wg, *wu, *wd, *norms, *fnorm;
+    const bf16* embed;
+    float *rcos, *rsin, *x, *qkv, *part_o, *part_ml;
+    bf16 *h, *q, *kvnew, *attn, *act;
+    int *counters, *tok_seq, *tok_pos, *last, *status;
+    unsigned long long* best;
+    int32_t *gen_tok, *gen_cur, *gen_out;
+    float* dbg_hidden;
+    int32_t *dbg_pos, *dbg_slot;
+    cudaStream_t cap_stream;
+    std::map<std::vector<long long>, GraphEntry> graphs;
+    unsigned long long use_clock;
+    int last_launches;
+    int num_sms;
+    bool pdl;
+    // profiling: events around launches of one kernel kind
+    int prof_kind;
+    std::vector<cudaEvent_t> prof_events;
+    unsigned long long prof_gen;
+    // TMA descriptors of the tensor-core GEMM operands
+    CUtensorMap tm_wqkv, tm_wo, tm_wg, tm_wu, tm_wd, tm_embed;
+    CUtensorMap tm_h[3], tm_attn[3], tm_act[3];  // token boxes of 64, 128, 256 rows
+};
+
+struct qw_kv {
+    qw_model* m;
+    char* pool;
+    int max_seqs, n_pages, maxp;
+    int* d_len;
+    int* d_pt;
+    bf16* k;
+    bf16* v;
+    long long layer_stride;
+    std::vector<int> len;
+    std::vector<std::vector<int>> pt;
+    std::set<int> free_pages;
+
+    KVView view() const {
+        KVView v_;
+        v_.len = d_len;
+        v_.page_table = d_pt;
+        v_.k = k;
+        v_.v = v;
+        v_.max_pages_per_seq = maxp;
+        v_.n_pages = n_pages;
+        v_.layer_stride = layer_stride;
+        return v_;
+    }
+};
+
+// ---------------------------------------------------------------------------------------
+// Weights
+// ---------------------------------------------------------------------------------------
+extern "C" size_t qw_model_workspace_bytes(const qw_config* cfg) {
+    if (!config_ok(cfg, nullptr)) return 0;
+    return layout_for(*cfg).total;
+}
+
+static bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+extern "C" qw_status qw_init_weights(const qw_config* cfg, const qw_weight_ptrs* w, void* dev_workspace,
+                                     size_t ws_bytes, void* stream_, qw_model** out) {
+    std::string why;
+    if (!out) return fail(QW_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    if (!config_ok(cfg, &why)) return fail(QW_ERR_INVALID_ARG, "invalid config: %s", why.c_str());
+    if (!w || !w->embed_tokens || !w->norm || !w->layers) return fail(QW_ERR_INVALID_ARG, "weight pointers missing");
+    const WsLayout L = layout_for(*cfg);
+    if (!dev_workspace || !aligned(dev_workspace, 256)) return fail(QW_ERR_INVALID_ARG, "workspace NULL or not 256-byte aligned");
+    if (ws_bytes < L.total) return fail(QW_ERR_INVALID_ARG, "workspace too small: %zu < %zu", ws_bytes, L.total);
+    if (!aligned(w->embed_tokens, 16)) return fail(QW_ERR_INVALID_ARG, "embed_tokens not 16-byte aligned");
+    for (int l = 0; l < cfg->n_layers; ++l) {
+        const qw_layer_ptrs& lp = w->layers[l];
+        const void* ps[11] = {lp.input_layernorm, lp.q_proj, lp.k_proj, lp.v_proj, lp.o_proj, lp.q_norm,
+                              lp.k_norm, lp.post_attention_layernorm, lp.gate_proj, lp.up_proj, lp.down_proj};
+        for (const void* p : ps)
+            if (!p) return fail(QW_ERR_INVALID_ARG, "layer %d has a NULL tensor", l);
+    }
+    cudaStream_t st = (cudaStream_t)stream_;
+    qw_model* m = new qw_model();
+    m->cfg = *cfg;
+    m->L = L;
+    m->ws = (char*)dev_workspace;
+    const size_t D = cfg->hidden, I = cfg->inter, d = cfg->head_dim;
+    const size_t QD = (size_t)cfg->n_heads * d, KD = (size_t)cfg->n_kv_heads * d;
+    m->qkv_rows = (int)(QD + 2 * KD);
+    char* b = m->ws;
+    m->wqkv = (bf16*)(b + L.wqkv);
+    m->wo = (bf16*)(b + L.wo);
+    m->wg = (bf16*)(b + L.wg);
+    m->wu = (bf16*)(b + L.wu);
+    m->wd = (bf16*)(b + L.wd);
+    m->norms = (bf16*)(b + L.norms);
+    m->fnorm = (bf16*)(b + L.fnorm);
+    m->embed = (const bf16*)w->embed_tokens;
+    m->rcos = (float*)(b + L.rcos);
+    m->rsin = (float*)(b + L.rsin);
+    m->x = (float*)(b + L.x);
+    m->h = (bf16*)(b + L.h);
+    m->qkv = (float*)(b + L.qkv);
+    m->q = (bf16*)(b + L.q);
+    m->kvnew = (bf16*)(b + L.kvnew);
+    m->attn = (bf16*)(b + L.attn);
+    m->act = (bf16*)(b + L.act);
+    m->part_o = (float*)(b + L.part_o);
+    m->part_ml = (float*)(b + L.part_ml);
+    m->counters = (int*)(b + L.counters);
+    m->tok_seq = (int*)(b + L.tok_seq);
+    m->tok_pos = (int*)(b + L.tok_pos);
+    m->last = (int*)(b + L.last);
+    m->best = (unsigned long long*)(b + L.best);
+    m->status = (int*)(b + L.status);
+    m->gen_tok = (int32_t*)(b + L.gen_tok);
+    m->gen_cur = (int32_t*)(b + L.gen_cur);
+    m->gen_out = (int32_t*)(b + L.gen_out);
+    m->use_clock = 0;
+    m->last_launches = 0;
+    m->pdl = false;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (m->num_sms <= 0) m->num_sms = 148;
+
+    auto fail_free = [&](qw_status s) {
+        delete m;
+        return s;
+    };
+    auto cp = [&](void* dst, const void* src, size_t bytes) {
+        return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, st);
+    };
+    // Pack: per layer q|k|v rows concatenated (one [qkv_rows, hidden] matrix), the other
+    // matrices copied as they are; norms as [in D][post D][q_norm d][k_norm d].
+    for (int l = 0; l < cfg->n_layers; ++l) {
+        const qw_layer_ptrs& lp = w->layers[l];
+        bf16* q0 = m->wqkv + (size_t)l * m->qkv_rows * D;
+        cudaError_t e = cudaSuccess;
+        if (e == cudaSuccess) e = cp(q0, lp.q_proj, QD * D * 2);
+        if (e == cudaSuccess) e = cp(q0 + QD * D, lp.k_proj, KD * D * 2);
+        if (e == cudaSuccess) e = cp(q0 + (QD + KD) * D, lp.v_proj, KD * D * 2);
+        if (e == cudaSuccess) e = cp(m->wo + (size_t)l * D * QD, lp.o_proj, D * QD * 2);
+        if (e == cudaSuccess) e = cp(m->wg + (size_t)l * I * D, lp.gate_proj, I * D * 2);
+        if (e == cudaSuccess) e = cp(m->wu + (size_t)l * I * D, lp.up_proj, I * D * 2);
+        if (e == cudaSuccess) e = cp(m->wd + (size_t)l * D * I, lp.down_proj, D * I * 2);
+        bf16* nb = m->norms + (size_t)l * (2 * D + 2 * d);
+        if (e == cudaSuccess) e = cp(nb, lp.input_layernorm, D * 2);
+        if (e == cudaSuccess) e = cp(nb + D, lp.post_attention_layernorm, D * 2);
+        if (e == cudaSuccess) e = cp(nb + 2 * D, lp.q_norm, d * 2);
+        if (e == cudaSuccess) e = cp(nb + 2 * D + d, lp.k_norm, d * 2);
+        if (e != cudaSuccess) {
+            fail(QW_ERR_CUDA, "weight packing failed: %s", cudaGetErrorString(e));
+            return fail_free(QW_ERR_CUDA);
+        }
+    }
+    if (cp(m->fnorm, w->norm, D * 2) != cudaSuccess) {
+        fail(QW_ERR_CUDA, "final norm copy failed");
+        return fail_free(QW_ERR_CUDA);
+    }
+    // RoPE table (Paso 4): angle = pos * theta^(-i/64), evaluated in fp64, stored as fp32.
+    {
+        const size_t n = (size_t)cfg->max_context * 64;
+        std::vector<float> c(n), s(n);
+        for (int i = 0; i < 64; ++i) {
+            const double inv = 1.0 / std::pow(cfg->rope_theta, (double)i / 64.0);
+            for (int p = 0; p < cfg->max_context; ++p) {
+                const double a = (double)p * inv;
+                c[(size_t)p * 64 + i] = (float)std::cos(a);
+                s[(size_t)p * 64 + i] = (float)std::sin(a);
+            }
+        }
+        if (cudaMemcpyAsync(m->rcos, c.data(), n * 4, cudaMemcpyHostToDevice, st) != cudaSuccess ||
+            cudaMemcpyAsync(m->rsin, s.data(), n * 4, cudaMemcpyHostToDevice, st) != cudaSuccess) {
+            fail(QW_ERR_CUDA, "RoPE table upload failed");
+            return fail_free(QW_ERR_CUDA);
+        }
+        // pageable sources: keep them alive until the copies are done
+        if (cudaStreamSynchronize(st) != cudaSuccess) {
+            fail(QW_ERR_CUDA, "stream sync failed");
+            return fail_free(QW_ERR_CUDA);
+        }
+    }
+    if (cudaMemsetAsync(m->counters, 0, (size_t)L.part_T * cfg->n_kv_heads * 4, st) != cudaSuccess ||
+        cudaMemsetAsync(m->best, 0, (size_t)cfg->max_batch * 8, st) != cudaSuccess ||
+        cudaMemsetAsync(m->status, 0, 4, st) != cudaSuccess) {
+        fail(QW_ERR_CUDA, "workspace clear failed");
+        return fail_free(QW_ERR_CUDA);
+    }
+    // Tensor maps for the tcgen05 GEMMs: weights as [rows, K] (box 128 x 64) and the
+    // activation operands as [rows, K] (box up to 256 x 64).
+    const uint64_t NL = cfg->n_layers, TT = std::max<uint64_t>(cfg->max_tokens, cfg->max_batch);
+    bool ok = true;
+    ok = ok && gemm_tc_encode_map(&m->tm_wqkv, m->wqkv, NL * m->qkv_rows, D, 128);
+    ok = ok && gemm_tc_encode_map(&m->tm_wo, m->wo, NL * D, QD, 128);
+    ok = ok && gemm_tc_encode_map(&m->tm_wg, m->wg, NL * I, D, 128);
+    ok = ok && gemm_tc_encode_map(&m->tm_wu, m->wu, NL * I, D, 128);
+    ok = ok && gemm_tc_encode_map(&m->tm_wd, m->wd, NL * D, I, 128);
+    ok = ok && gemm_tc_encode_map(&m->tm_embed, m->embed, cfg->vocab, D, 128);
+    ok = ok && gemm_tc_encode_map(m->tm_h, m->h, TT, D, 0);
+    ok = ok && gemm_tc_encode_map(m->tm_attn, m->attn, cfg->max_tokens, QD, 0);
+    ok = ok && gemm_tc_encode_map(m->tm_act, m->act, cfg->max_tokens, I, 0);
+    if (!ok) {
+        fail(QW_ERR_CUDA, "cuTensorMapEncodeTiled failed");
+        return fail_free(QW_ERR_CUDA);
+    }
+    if (cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking) != cudaSuccess) {
+        fail(QW_ERR_CUDA, "capture stream creation failed");
+        return fail_free(QW_ERR_CUDA);
+    }
+    m->dbg_hidden = nullptr;
+    m->dbg_pos = m->dbg_slot = nullptr;
+    m->prof_kind = QW_PROF_OFF;
+    m->prof_gen = 0;
+    *out = m;
+    return QW_OK;
+}
+
+extern "C" void qw_free_model(qw_model* m) {
+    if (!m) return;
+    for (auto& kv : m->graphs) cudaGraphExecDestroy(kv.second.exec);
+    if (m->cap_stream) cudaStreamDestroy(m->cap_stream);
+    delete m;
+}
+
+extern "C" qw_status qw_debug_set(qw_model* m, float* dev_hidden, int32_t* dev_positions, int32_t* dev_slots) {
+    if (!m) return fail(QW_ERR_INVALID_ARG, "model is NULL");
+    if (dev_hidden && (!dev_positions || !dev_slots)) return fail(QW_ERR_INVALID_ARG, "debug buffers incomplete");
+    m->dbg_hidden = dev_hidden;
+    m->dbg_pos = dev_hidden ? dev_positions : nullptr;
+    m->dbg_slot = dev_hidden ? dev_slots : nullptr;
+    return QW_OK;
+}
+
+extern "C" int qw_last_launch_count(const qw_model* m) { return m ? m->last_launches : 0; }
+
+extern "C" qw_status qw_profile_set(qw_model* m, int kind, void* const* events, int n_events) {
+    if (!m) return fail(QW_ERR_INVALID_ARG, "model is NULL");
+    if (kind < QW_PROF_OFF || kind > QW_PROF_RMSNORM) return fail(QW_ERR_INVALID_ARG, "unknown kernel kind %d", kind);
+    m->prof_events.clear();
+    if (kind == QW_PROF_OFF || !events || n_events < 2) {
+        m->prof_kind = QW_PROF_OFF;
+        return QW_OK;
+    }
+    for (int i = 0; i < n_events; ++i) m->prof_events.push_back((cudaEvent_t)events[i]);
+    m->prof_kind = kind;
+    ++m->prof_gen;
+    return QW_OK;
+}
+
+// Records the profiling events around one launch of `kind` (j-th of the step).
+struct ProfScope {
+    qw_model* m;
+    cudaStream_t st;
+    int idx;
+    ProfScope(qw_model* m_, int kind, int* counts, cudaStream_t st_) : m(m_), st(st_), idx(-1) {
+        if (m->prof_kind != kind) return;
+        const int j = counts[kind]++;
+        if (2 * j + 1 < (int)m->prof_events.size()) {
+            idx = 2 * j;
+            cudaEventRecordWithFlags(m->prof_events[idx], st, cudaEventRecordExternal);
+        }
+    }
+    ~ProfScope() {
+        if (idx >= 0) cudaEventRecordWithFlags(m->prof_events[idx + 1], st, cudaEventRecordExternal);
+    }
+};
+
+// ---------------------------------------------------------------------------------------
+// Paged KV cache
+// ---------------------------------------------------------------------------------------
+static size_t kv_meta_bytes(const qw_model* m, int max_seqs) {
+    const int maxp = (m->cfg.max_context + 15) / 16;
+    return align_up((size_t)max_seqs * 4, 256) + align_up((size_t)max_seqs * maxp * 4, 256);
+}
+
+static size_t kv_page_bytes(const qw_model* m) {  // K + V, all layers, one page
+    return (size_t)m->cfg.n_layers * 2 * m->cfg.n_kv_heads * 16 * m->cfg.head_dim * 2;
+}
+
+extern "C" size_t qw_kv_pool_bytes(const qw_model* m, int n_pages, int max_seqs) {
+    if (!m || n_pages < 1 || max_seqs < 1) return 0;
+    return kv_meta_bytes(m, max_seqs) + kv_page_bytes(m) * (size_t)n_pages;
+}
+
+extern "C" qw_status qw_kv_alloc(qw_model* m, void* dev_pool, size_t pool_bytes, int max_seqs, void* stream_,
+                                 qw_kv** out) {
+    if (!out) return fail(QW_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    if (!m || !dev_pool || !aligned(dev_pool, 256)) return fail(QW_ERR_INVALID_ARG, "model/pool NULL or pool not 256-byte aligned");
+    if (max_seqs < 1 || max_seqs > (1 << 20)) return fail(QW_ERR_INVALID_ARG, "max_seqs out of range");
+    const size_t meta = kv_meta_bytes(m, max_seqs);
+    if (pool_bytes < meta + kv_page_bytes(m)) return fail(QW_ERR_INVALID_ARG, "pool too small for one page");
+    const long long n_pages = (long long)((pool_bytes - meta) / kv_page_bytes(m));
+    if (n_pages > (1ll << 30)) return fail(QW_ERR_INVALID_ARG, "pool too large");
+    cudaStream_t st = (cudaStream_t)stream_;
+    qw_kv* kv = new qw_kv();
+    kv->m = m;
+    kv->pool = (char*)dev_pool;
+    kv->max_seqs = max_seqs;
+    kv->n_pages = (int)n_pages;
+    kv->maxp = (m->cfg.max_context + 15) / 16;
+    kv->d_len = (int*)kv->pool;
+    kv->d_pt = (int*)(kv->pool + align_up((size_t)max_seqs * 4, 256));
+    kv->layer_stride = (long long)n_pages * m->cfg.n_kv_heads * 16 * m->cfg.head_dim;
+    kv->k = (bf16*)(kv->pool + meta);
+    kv->v = kv->k + (size_t)m->cfg.n_layers * kv->layer_stride;
+    kv->len.assign(max_seqs, 0);
+    kv->pt.assign(max_seqs, std::vector<int>());
+    for (int i = 0; i < kv->n_pages; ++i) kv->free_pages.insert(i);
+    if (cudaMemsetAsync(kv->d_len, 0, (size_t)max_seqs * 4, st) != cudaSuccess ||
+        cudaMemsetAsync(kv->d_pt, 0xFF, (size_t)max_seqs * kv->maxp * 4, st) != cudaSuccess) {
+        delete kv;
+        return fail(QW_ERR_CUDA, "KV metadata clear failed");
+    }
+    *out = kv;
+    return QW_OK;
+}
+
+extern "C" void qw_free_kv(qw_kv* kv) { delete kv; }
+
+extern "C" qw_status qw_kv_reserve(qw_kv* kv, int seq, int total_tokens, void* stream_) {
+    if (!kv) return fail(QW_ERR_INVALID_ARG, "kv is NULL");
+    if (seq < 0 || seq >= kv->max_seqs) return fail(QW_ERR_INVALID_ARG, "seq id %d out of range", seq);
+    if (total_tokens < 0 || total_tokens > kv->m->cfg.max_context)
+        return fail(QW_ERR_INVALID_ARG, "total_tokens %d outside [0, max_context]", total_tokens);
+    std::vector<int>& t = kv->pt[seq];
+    const int need = (total_tokens + 15) / 16 - (int)t.size();
+    if (need <= 0) return QW_OK;
+    if (need > (int)kv->free_pages.size())
+        return fail(QW_ERR_KV_FULL, "KV cache full: %d pages needed, %zu free", need, kv->free_pages.size());
+    const int old = (int)t.size();
+    for (int i = 0; i < need; ++i) {
+        t.push_back(*kv->free_pages.begin());
+        kv->free_pages.erase(kv->free_pages.begin());
+    }
+    CUDA_TRY(cudaMemcpyAsync(kv->d_pt + (size_t)seq * kv->maxp + old, t.data() + old, (size_t)need * 4,
+                             cudaMemcpyHostToDevice, (cudaStream_t)stream_));
+    return QW_OK;
+}
+
+extern "C" qw_status qw_kv_reset(qw_kv* kv, int seq, void* stream_) {
+    if (!kv) return fail(QW_ERR_INVALID_ARG, "kv is NULL");
+    if (seq < -1 || seq >= kv->max_seqs) return fail(QW_ERR_INVALID_ARG, "seq id %d out of range", seq);
+    cudaStream_t st = (cudaStream_t)stream_;
+    const int a = seq < 0 ? 0 : seq, b = seq < 0 ? kv->max_seqs : seq + 1;
+    for (int s = a; s < b; ++s) {
+        for (int p : kv->pt[s]) kv->free_pages.insert(p);
+        kv->pt[s].clear();
+        kv->len[s] = 0;
+    }
+    CUDA_TRY(cudaMemsetAsync(kv->d_len + a, 0, (size_t)(b - a) * 4, st));
+    CUDA_TRY(cudaMemsetAsync(kv->d_pt + (size_t)a * kv->maxp, 0xFF, (size_t)(b - a) * kv->maxp * 4, st));
+    return QW_OK;
+}
+
+extern "C" int qw_kv_free_pages(const qw_kv* kv) { return kv ? (int)kv->free_pages.size() : -1; }
+
+extern "C" int qw_kv_length(const qw_kv* kv, int seq) {
+    if (!kv || seq < 0 || seq >= kv->max_seqs) return -1;
+    return kv->len[seq];
+}
+
+extern "C" int qw_kv_page_table(const qw_kv* kv, int seq, int32_t* host_out, int max_pages) {
+    if (!kv || seq < 0 || seq >= kv->max_seqs) return fail(QW_ERR_INVALID_ARG, "bad kv or seq id");
+    const std::vector<int>& t = kv->pt[seq];
+    if (host_out)
+        for (int i = 0; i < (int)t.size() && i < max_pages; ++i) host_out[i] = t[i];
+    return (int)t.size();
+}
+
+extern "C" qw_status qw_kv_pool_ptrs(const qw_kv* kv, void** dev_k, void** dev_v, int* n_pages) {
+    if (!kv) return fail(QW_ERR_INVALID_ARG, "kv is NULL");
+    if (dev_k) *dev_k = kv->k;
+    if (dev_v) *dev_v = kv->v;
+    if (n_pages) *n_pages = kv->n_pages;
+    return QW_OK;
+}
+
+extern "C" qw_status qw_kv_fill_synthetic(qw_kv* kv, int seq, int n_tokens, uint64_t seed, void* stream_) {
+    if (!kv) return fail(QW_ERR_INVALID_ARG, "kv is NULL");
+    if (seq < 0 || seq >= kv->max_seqs) return fail(QW_ERR_INVALID_ARG, "seq id out of range");
+    if (n_tokens < 0 || n_tokens > (1 << 22)) return fail(QW_ERR_INVALID_ARG, "n_tokens out of range");
+    if (kv->len[seq] != 0) return fail(QW_ERR_BAD_STATE, "sequence %d is not empty", seq);
+    if ((int)kv->pt[seq].size() * 16 < n_tokens) return fail(QW_ERR_KV_FULL, "sequence %d reserved for fewer tokens", seq);
+    cudaStream_t st = (cudaStream_t)stream_;
+    LaunchCtx c = {st, false, nullptr};
+    CUDA_TRY(launch_kv_fill(c, kv->view(), kv->m->cfg.n_layers, kv->m->cfg.n_kv_heads, seq, n_tokens, seed));
+    const int n = n_tokens;
+    CUDA_TRY(cudaMemcpyAsync(kv->d_len + seq, &n, 4, cudaMemcpyHostToDevice, st));
+    kv->len[seq] = n_tokens;
+    return QW_OK;
+}
+
+// ---------------------------------------------------------------------------------------
+// One step of the forward pass (prefill or decode)
+// ---------------------------------------------------------------------------------------
+struct SplitPlan {
+    int chunk, n_splits;
+};
+
+static SplitPlan plan_splits(const qw_model* m, int T, int max_keys) {
+    // aim for ~4 CTAs per SM over T * n_kv (token, KV head) pairs; chunks are whole pages
+    const int pairs = T * m->cfg.n_kv_heads;
+    int want = (4 * m->num_sms + pairs - 1) / pairs;
+    want = std::max(1, std::min(want, kMaxSplits));
+    int chunk = (max_keys + want - 1) / want;
+    chunk = std::max(64, (chunk + 15) / 16 * 16);
+    int n = (max_keys + chunk - 1) / chunk;
+    while (n > kMaxSplits) {
+        chunk += 16;
+        n = (max_keys + chunk - 1) / chunk;
+    }
+    return {chunk, std::max(n, 1)};
+}
+
+static qw_status run_step(qw_model* m, qw_kv* kv, const StepDesc& sd, bool prefill, int max_keys,
+                          const int32_t* tokens, float* logits, int32_t* next, cudaStream_t st,
+                          bool allow_debug, int* launches) {
+    const qw_config& c = m->cfg;
+    LaunchCtx lc = {st, m->pdl, launches};
+    const int T = sd.T, B = sd.B;
+    const int D = c.hidden, I = c.inter, QD = c.n_heads * c.head_dim, d = c.head_dim;
+    const KVView kvv = kv->view();
+    TokView tv = {m->tok_seq, m->tok_pos, m->last};
+    const bool dbg = allow_debug && m->dbg_hidden;
+    const bool small = T <= kSmallT;
+    const SplitPlan sp = plan_splits(m, T, max_keys);
+    if (!small && !prefill && T > m->L.part_T) return fail(QW_ERR_UNSUPPORTED, "decode batch beyond partial buffers");
+
+    int pc[16] = {0};
+#define PROF(kind) ProfScope prof_scope_(m, kind, pc, st)
+    CUDA_TRY(launch_step_begin(lc, sd, tokens, m->embed, c.vocab, D, m->x, tv, kvv, m->status));
+    for (int l = 0; l < c.n_layers; ++l) {
+        const bf16* nb = m->norms + (size_t)l * (2 * D + 2 * d);
+        const bf16* w_in = nb;
+        const bf16* w_post = nb + D;
+        const bf16* w_qn = nb + 2 * D;
+        const bf16* w_kn = nb + 2 * D + d;
+        // --- attention sublayer (Paso 5) ---
+        if (small) {
+            PROF(QW_PROF_QKV);
+            CUDA_TRY(launch_gemv_qkv(lc, T, m->x, w_in, c.rms_eps, m->wqkv + (size_t)l * m->qkv_rows * D,
+                                     m->qkv_rows, D, m->qkv));
+        } else {
+            {
+                PROF(QW_PROF_RMSNORM);
+                CUDA_TRY(launch_rmsnorm(lc, m->x, nullptr, T, D, w_in, c.rms_eps, m->h));
+            }
+            PROF(QW_PROF_QKV);
+            GemmArgs g = {};
+            g.tmA = &m->tm_wqkv; g.tmA2 = &m->tm_wqkv; g.tmB = m->tm_h;
+            g.a_row0 = l * m->qkv_rows; g.a2_row0 = g.a_row0; g.M = m->qkv_rows; g.K = D; g.T = T;
+            g.out_f32 = m->qkv; g.ld_out = m->qkv_rows; g.status = m->status;
+            CUDA_TRY(launch_gemm_tc(lc, EPI_STORE_F32, g));
+        }
+        {
+        PROF(QW_PROF_ROPE);
+        CUDA_TRY(launch_qknorm_rope_append(lc, T, l, m->qkv, w_qn, w_kn, c.rms_eps, m->rcos, m->rsin,
+                                           c.n_heads, c.n_kv_heads, tv, kvv, m->q, m->kvnew,
+                                           (dbg && l == 0) ? m->dbg_pos : nullptr,
+                                           (dbg && l == 0) ? m->dbg_slot : nullptr, m->status));
+        }
+        {
+        PROF(QW_PROF_ATTN);
+        CUDA_TRY(launch_attn_paged(lc, T, l, m->q, c.n_heads, c.n_kv_heads, tv, kvv, sp.chunk, sp.n_splits,
+                                   m->part_o, m->part_ml, m->counters, m->attn));
+        }
+        if (small) {
+            PROF(QW_PROF_OPROJ);
+            CUDA_TRY(launch_gemv_resid(lc, T, m->attn, m->wo + (size_t)l * D * QD, D, QD, m->x));
+        } else {
+            PROF(QW_PROF_OPROJ);
+            GemmArgs g = {};
+            g.tmA = &m->tm_wo; g.tmA2 = &m->tm_wo; g.tmB = m->tm_attn;
+            g.a_row0 = l * D; g.a2_row0 = g.a_row0; g.M = D; g.K = QD; g.T = T;
+            g.out_f32 = m->x; g.ld_out = D; g.status = m->status;
+            CUDA_TRY(launch_gemm_tc(lc, EPI_RESID_F32, g));
+        }
+        // --- feed-forward sublayer (Paso 6) ---
+        if (small) {
+            {
+                PROF(QW_PROF_GATEUP);
+                CUDA_TRY(launch_gemv_gateup(lc, T, m->x, w_post, c.rms_eps, m->wg + (size_t)l * I * D,
+                                            m->wu + (size_t)l * I * D, I, D, m->act));
+            }
+            PROF(QW_PROF_DOWN);
+            CUDA_TRY(launch_gemv_resid(lc, T, m->act, m->wd + (size_t)l * D * I, D, I, m->x));
+        } else {
+            {
+                PROF(QW_PROF_RMSNORM);
+                CUDA_TRY(launch_rmsnorm(lc, m->x, nullptr, T, D, w_post, c.rms_eps, m->h));
+            }
+            GemmArgs g = {};
+            g.tmA = &m->tm_wg; g.tmA2 = &m->tm_wu; g.tmB = m->tm_h;
+            g.a_row0 = l * I; g.a2_row0 = l * I; g.M = I; g.K = D; g.T = T;
+            g.out_bf16 = m->act; g.ld_out = I; g.status = m->status;
+            {
+                PROF(QW_PROF_GATEUP);
+                CUDA_TRY(launch_gemm_tc(lc, EPI_SILU_MUL, g));
+            }
+            GemmArgs g2 = {};
+            g2.tmA = &m->tm_wd; g2.tmA2 = &m->tm_wd; g2.tmB = m->tm_act;
+            g2.a_row0 = l * D; g2.a2_row0 = g2.a_row0; g2.M = D; g2.K = I; g2.T = T;
+            g2.out_f32 = m->x; g2.ld_out = D; g2.status = m->status;
+            PROF(QW_PROF_DOWN);
+            CUDA_TRY(launch_gemm_tc(lc, EPI_RESID_F32, g2));
+        }
+        if (dbg)
+            CUDA_TRY(cudaMemcpyAsync(m->dbg_hidden + (size_t)l * T * D, m->x, (size_t)T * D * 4,
+                                     cudaMemcpyDeviceToDevice, st));
+    }
+    // --- final norm + tied LM head + greedy argmax (Paso 8) ---
+    if (B <= kSmallT) {
+        PROF(QW_PROF_LMHEAD);
+        CUDA_TRY(launch_gemv_lmhead(lc, B, m->x, m->last, m->fnorm, c.rms_eps, m->embed, c.vocab, D, logits,
+                                    m->best));
+    } else {
+        {
+            PROF(QW_PROF_RMSNORM);
+            CUDA_TRY(launch_rmsnorm(lc, m->x, m->last, B, D, m->fnorm, c.rms_eps, m->h));
+        }
+        PROF(QW_PROF_LMHEAD);
+        GemmArgs g = {};
+        g.tmA = &m->tm_embed; g.tmA2 = &m->tm_embed; g.tmB = m->tm_h;
+        g.a_row0 = 0; g.a2_row0 = 0; g.M = c.vocab; g.K = D; g.T = B;
+        g.logits = logits; g.ld_out = c.vocab; g.best = m->best; g.status = m->status;
+        CUDA_TRY(launch_gemm_tc(lc, EPI_ARGMAX, g));
+    }
+    CUDA_TRY(launch_finalize(lc, sd, m->best, next, kvv));
+#undef PROF
+    return QW_OK;
+}
+
+static qw_status check_batch(const qw_model* m, const qw_kv* kv, int B, const int* seq_ids) {
+    if (!m || !kv) return fail(QW_ERR_INVALID_ARG, "model or kv is NULL");
+    if (kv->m != m) return fail(QW_ERR_INVALID_ARG, "kv belongs to another model");
+    if (B < 1 || B > m->cfg.max_batch) return fail(QW_ERR_INVALID_ARG, "B=%d outside [1, max_batch]", B);
+    if (!seq_ids) return fail(QW_ERR_INVALID_ARG, "seq_ids is NULL");
+    std::set<int> seen;
+    for (int b = 0; b < B; ++b) {
+        const int s = seq_ids[b];
+        if (s < 0 || s >= kv->max_seqs) return fail(QW_ERR_INVALID_ARG, "seq id %d out of range", s);
+        if (!seen.insert(s).second) return fail(QW_ERR_INVALID_ARG, "seq id %d repeated", s);
+    }
+    return QW_OK;
+}
+
+extern "C" qw_status qw_prefill(qw_model* m, qw_kv* kv, int B, const int* seq_ids, const int* lens,
+                                const int32_t* dev_token_ids, float* dev_logits, int32_t* dev_next_ids,
+                                void* stream_) {
+    QW_TRY(check_batch(m, kv, B, seq_ids));
+    if (!lens || !dev_token_ids || !dev_next_ids) return fail(QW_ERR_INVALID_ARG, "NULL argument");
+    StepDesc sd = {};
+    sd.B = B;
+    long long total = 0;
+    int max_len = 0;
+    for (int b = 0; b < B; ++b) {
+        const int s = seq_ids[b];
+        if (lens[b] < 1) return fail(QW_ERR_INVALID_ARG, "lens[%d] = %d < 1", b, lens[b]);
+        if (kv->len[s] != 0) return fail(QW_ERR_BAD_STATE, "prefill into non-empty sequence %d", s);
+        if (lens[b] > m->cfg.max_context) return fail(QW_ERR_INVALID_ARG, "prompt longer than max_context");
+        if ((long long)kv->pt[s].size() * 16 < lens[b])
+            return fail(QW_ERR_KV_FULL, "sequence %d reserved for %zu tokens < %d", s, kv->pt[s].size() * 16, lens[b]);
+        sd.seq[b] = s;
+        sd.start[b] = (int)total;
+        total += lens[b];
+        max_len = std::max(max_len, lens[b]);
+    }
+    if (total > m->cfg.max_tokens) return fail(QW_ERR_INVALID_ARG, "%lld tokens > max_tokens", total);
+    sd.start[B] = (int)total;
+    sd.T = (int)total;
+    int launches = 0;
+    QW_TRY(run_step(m, kv, sd, true, max_len, dev_token_ids, dev_logits, dev_next_ids, (cudaStream_t)stream_,
+                    true, &launches));
+    m->last_launches = launches;
+    for (int b = 0; b < B; ++b) kv->len[seq_ids[b]] += lens[b];
+    return QW_OK;
+}
+
+extern "C" qw_status qw_decode_step(qw_model* m, qw_kv* kv, int B, const int* seq_ids,
+                                    const int32_t* dev_token_ids, float* dev_logits, int32_t* dev_next_ids,
+                                    void* stream_) {
+    QW_TRY(check_batch(m, kv, B, seq_ids));
+    if (!dev_token_ids || !dev_next_ids) return fail(QW_ERR_INVALID_ARG, "NULL argument");
+    if (B > m->cfg.max_tokens) return fail(QW_ERR_INVALID_ARG, "B > max_tokens");
+    StepDesc sd = {};
+    sd.B = B;
+    sd.T = B;
+    int cap = 0;
+    for (int b = 0; b < B; ++b) {
+        const int s = seq_ids[b];
+        const int capacity = std::min((int)kv->pt[s].size() * 16, m->cfg.max_context);
+        if (kv->len[s] + 1 > capacity)
+            return fail(QW_ERR_KV_FULL, "sequence %d has no reserved slot for position %d", s, kv->len[s]);
+        sd.seq[b] = s;
+        sd.start[b] = b;
+        cap = std::max(cap, capacity);
+    }
+    sd.start[B] = B;
+    cudaStream_t st = (cudaStream_t)stream_;
+    if (m->dbg_hidden) {
+        int launches = 0;
+        int max_keys = 0;
+        for (int b = 0; b < B; ++b) max_keys = std::max(max_keys, kv->len[seq_ids[b]] + 1);
+        QW_TRY(run_step(m, kv, sd, false, max_keys, dev_token_ids, dev_logits, dev_next_ids, st, true, &launches));
+        m->last_launches = launches;
+    } else {
+        // graph key: everything baked into the captured kernels
+        const SplitPlan sp = plan_splits(m, B, cap);
+        std::vector<long long> key;
+        key.reserve(B + 8);
+        key.push_back(B);
+        key.push_back(cap);
+        key.push_back((long long)(uintptr_t)dev_token_ids);
+        key.push_back((long long)(uintptr_t)dev_logits);
+        key.push_back((long long)(uintptr_t)dev_next_ids);
+        key.push_back((long long)(uintptr_t)kv);
+        key.push_back(sp.chunk);
+        key.push_back(m->prof_kind);
+        key.push_back(m->prof_kind ? (long long)m->prof_gen : 0);
+        for (int b = 0; b < B; ++b) key.push_back(seq_ids[b]);
+        auto it = m->graphs.find(key);
+        if (it == m->graphs.end()) {
+            if (m->graphs.size() >= 64) {  // evict the least recently used entry
+                auto lru = m->graphs.begin();
+                for (auto jt = m->graphs.begin(); jt != m->graphs.end(); ++jt)
+                    if (jt->second.last_use < lru->second.last_use) lru = jt;
+                cudaGraphExecDestroy(lru->second.exec);
+                m->graphs.erase(lru);
+            }
+            int launches = 0;
+            cudaGraph_t graph = nullptr;
+            CUDA_TRY(cudaStreamBeginCapture(m->cap_stream, cudaStreamCaptureModeThreadLocal));
+            qw_status s = run_step(m, kv, sd, false, cap, dev_token_ids, dev_logits, dev_next_ids, m->cap_stream,
+                                   false, &launches);
+            cudaError_t e = cudaStreamEndCapture(m->cap_stream, &graph);
+            if (s != QW_OK) {
+                if (graph) cudaGraphDestroy(graph);
+                return s;
+            }
+            if (e != cudaSuccess) return fail(QW_ERR_CUDA, "graph capture failed: %s", cudaGetErrorString(e));
+            cudaGraphExec_t exec = nullptr;
+            e = cudaGraphInstantiate(&exec, graph, 0);
+            cudaGraphDestroy(graph);
+            if (e != cudaSuccess) return fail(QW_ERR_CUDA, "graph instantiate failed: %s", cudaGetErrorString(e));
+            it = m->graphs.emplace(key, GraphEntry{exec, launches, 0}).first;
+        }
+        it->second.last_use = ++m->use_clock;
+        CUDA_TRY(cudaGraphLaunch(it->second.exec, st));
+        m->last_launches = it->second.launches;
+    }
+    for (int b = 0; b < B; ++b) kv->len[seq_ids[b]] += 1;
+    return QW_OK;
+}
+
+extern "C" qw_status qw_generate(qw_model* m, qw_kv* kv, int B, const int* seq_ids, const int* lens,
+                                 const int32_t* host_prompt_ids, int n_decode, int32_t* host_out_ids,
+                                 void* stream_) {
+    QW_TRY(check_batch(m, kv, B, seq_ids));
+    if (!lens || !host_prompt_ids || !host_out_ids) return fail(QW_ERR_INVALID_ARG, "NULL argument");
+    if (n_decode < 0 || n_decode + 1 > m->cfg.max_context) return fail(QW_ERR_INVALID_ARG, "n_decode out of range");
+    long long total = 0;
+    for (int b = 0; b < B; ++b) {
+        if (lens[b] < 1) return fail(QW_ERR_INVALID_ARG, "lens[%d] < 1", b);
+        const int s = seq_ids[b];
+        if ((long long)kv->pt[s].size() * 16 < (long long)lens[b] + n_decode)
+            return fail(QW_ERR_KV_FULL, "sequence %d not reserved for prompt + %d decode tokens", s, n_decode);
+        total += lens[b];
+    }
+    if (total > m->cfg.max_tokens) return fail(QW_ERR_INVALID_ARG, "prompts exceed max_tokens");
+    cudaStream_t st = (cudaStream_t)stream_;
+    CUDA_TRY(cudaMemcpyAsync(m->gen_tok, host_prompt_ids, (size_t)total * 4, cudaMemcpyHostToDevice, st));
+    QW_TRY(qw_prefill(m, kv, B, seq_ids, lens, m->gen_tok, nullptr, m->gen_cur, st));
+    int launches = m->last_launches;
+    CUDA_TRY(cudaMemcpyAsync(m->gen_out, m->gen_cur, (size_t)B * 4, cudaMemcpyDeviceToDevice, st));
+    for (int i = 1; i <= n_decode; ++i) {
+        QW_TRY(qw_decode_step(m, kv, B, seq_ids, m->gen_cur, nullptr, m->gen_cur, st));
+        launches += m->last_launches;
+        CUDA_TRY(cudaMemcpyAsync(m->gen_out + (size_t)i * B, m->gen_cur, (size_t)B * 4, cudaMemcpyDeviceToDevice, st));
+    }
+    std::vector<int32_t> tmp((size_t)(n_decode + 1) * B);
+    CUDA_TRY(cudaMemcpyAsync(tmp.data(), m->gen_out, tmp.size() * 4, cudaMemcpyDeviceToHost, st));
+    CUDA_TRY(cudaStreamSynchronize(st));
+    for (int i = 0; i <= n_decode; ++i)
+        for (int b = 0; b < B; ++b) host_out_ids[(size_t)b * (n_decode + 1) + i] = tmp[(size_t)i * B + b];
+    m->last_launches = launches;
+    return QW_OK;
+}
+
+extern "C" qw_status qw_sync_status(qw_model* m, void* stream_) {
+    if (!m) return fail(QW_ERR_INVALID_ARG, "model is NULL");
+    cudaStream_t st = (cudaStream_t)stream_;
+    CUDA_TRY(cudaStreamSynchronize(st));
+    int word = 0;
+    CUDA_TRY(cudaMemcpy(&word, m->status, 4, cudaMemcpyDeviceToHost));
+    CUDA_TRY(cudaMemset(m->status, 0, 4));
+    if (word & QW_DEV_BAD_TOKEN) return fail(QW_ERR_BAD_TOKEN, "a token id was outside [0, vocab)");
+    if (word & QW_DEV_BAD_POS) return fail(QW_ERR_BAD_POS, "a position had no reserved page");
+    if (word & QW_DEV_TIMEOUT) return fail(QW_ERR_TIMEOUT, "a bounded wait in a kernel timed out");
+    return QW_OK;
+}

@@ -1,0 +1,219 @@
+/*
+ * qw.h - C ABI of the GB300 (sm_103a) Qwen3-style decoder library (libqw.so).
+ *
+ * The library runs the decoder forward pass walked through on the page "Dentro de un LLM:
+ * Inferencia en Python puro para Qwen3-0.6B en MLX": embedding gather (Paso 2), RMSNorm
+ * (Paso 3), Q/K/V projections with per-head QK-norm and rotate-half RoPE (Pasos 4-5), KV
+ * cache append and grouped-query causal attention (Paso 5), o_proj, SwiGLU (Paso 6), the
+ * residual block (Paso 7), final norm + tied LM head + greedy argmax (Paso 8), and the
+ * prefill / decode loop (Paso 9).
+ *
+ * Conventions shared by every entry point:
+ *  - Device pointers are CUDA device addresses owned by the CALLER. The library never
+ *    allocates device memory; it carves what it needs from the workspace and KV pool the
+ *    caller hands it. Borrowed buffers must outlive the object that borrows them.
+ *  - Host pointers are plain host memory, read during the call only (never retained).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream). Work is
+ *    enqueued asynchronously on it unless the function says it synchronises.
+ *  - Every call returns QW_OK (0) or a negative qw_status. An error found on the host is
+ *    reported before anything is enqueued and leaves all state unchanged. qw_last_error()
+ *    returns a message for the calling thread's last error.
+ *  - Errors found on the device (a token id out of range, a position without a reserved
+ *    page, a wait that timed out) set bits in a device status word; the affected rows are
+ *    written as zeros and nothing traps. qw_sync_status() reads and clears that word.
+ *  - Weights are bf16 in the HF [out_features, in_features] row-major layout (x @ W^T).
+ */
+#ifndef QW_H
+#define QW_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    QW_OK = 0,
+    QW_ERR_INVALID_ARG = -1, /* a null/misaligned pointer, a size or id out of range          */
+    QW_ERR_KV_FULL = -2,     /* not enough free pages, or a sequence past its reservation      */
+    QW_ERR_BAD_STATE = -3,   /* e.g. prefill into a sequence that already holds tokens        */
+    QW_ERR_CUDA = -4,        /* a CUDA runtime call failed (message has the CUDA error)        */
+    QW_ERR_BAD_TOKEN = -5,   /* device status: a token id outside [0, vocab)                  */
+    QW_ERR_TIMEOUT = -6,     /* device status: a bounded wait inside a kernel gave up          */
+    QW_ERR_UNSUPPORTED = -7, /* a shape this build has no kernel for                          */
+    QW_ERR_BAD_POS = -8      /* device status: a position with no page in the page table      */
+} qw_status;
+
+/* Model shape. Per-layer dims of Qwen3-0.6B: hidden 1024, 16 query / 8 KV heads of 128,
+ * SwiGLU 3072, vocab 151936, 28 layers, eps 1e-6, theta 1e6 (Pasos 2-7). This build
+ * supports head_dim 128, n_heads == 2 * n_kv_heads, hidden % 256 == 0, inter % 256 == 0,
+ * (n_heads * head_dim) % 256 == 0, vocab % 128 == 0, page_size 16, tie_embed 1. */
+typedef struct {
+    int n_layers;
+    int hidden;
+    int n_heads;
+    int n_kv_heads;
+    int head_dim;
+    int inter;
+    int vocab;
+    int page_size;   /* tokens per KV page; 16                                            */
+    int tie_embed;   /* 1: the LM head is model.embed_tokens.weight (Paso 8, tied)        */
+    float rms_eps;   /* 1e-6 (Paso 3)                                                     */
+    double rope_theta; /* 1e6 (Paso 4)                                                    */
+    int max_tokens;  /* most tokens one prefill/decode call may carry (sizes workspace)   */
+    int max_batch;   /* most sequences in one call (<= QW_MAX_BATCH)                      */
+    int max_context; /* longest sequence in tokens (RoPE table and page-table rows)       */
+} qw_config;
+
+#define QW_MAX_BATCH 256
+
+/* Device pointers of one decoder layer's bf16 tensors, HF names. */
+typedef struct {
+    const void* input_layernorm;          /* [hidden]                        */
+    const void* q_proj;                   /* [n_heads*head_dim, hidden]      */
+    const void* k_proj;                   /* [n_kv_heads*head_dim, hidden]   */
+    const void* v_proj;                   /* [n_kv_heads*head_dim, hidden]   */
+    const void* o_proj;                   /* [hidden, n_heads*head_dim]      */
+    const void* q_norm;                   /* [head_dim], shared by all heads */
+    const void* k_norm;                   /* [head_dim]                      */
+    const void* post_attention_layernorm; /* [hidden]                        */
+    const void* gate_proj;                /* [inter, hidden]                 */
+    const void* up_proj;                  /* [inter, hidden]                 */
+    const void* down_proj;                /* [hidden, inter]                 */
+} qw_layer_ptrs;
+
+typedef struct {
+    const void* embed_tokens;     /* [vocab, hidden]; BORROWED for the model's lifetime   */
+    const void* norm;             /* [hidden] final norm                                  */
+    const qw_layer_ptrs* layers;  /* host array of n_layers entries                       */
+} qw_weight_ptrs;
+
+typedef struct qw_model qw_model;
+typedef struct qw_kv qw_kv;
+
+/* Bytes of device workspace qw_init_weights needs for `cfg` (packed weights, RoPE table,
+ * activations for max_tokens, split-KV partials, status word). 0 if cfg is invalid. */
+size_t qw_model_workspace_bytes(const qw_config* cfg);
+
+/* Validate cfg, pack the per-layer weights into `dev_workspace` (bit-identical copies:
+ * q|k|v rows concatenated, the rest copied as is), build the fp32 RoPE cos/sin table (host
+ * fp64, Paso 4) and carve the activation buffers. Copies are enqueued on `stream`; the
+ * source layer tensors may be freed once the stream has passed them. embed_tokens is NOT
+ * copied and must outlive the model. ws_bytes >= qw_model_workspace_bytes(cfg), workspace
+ * 256-byte aligned. On success *out owns host state only. */
+qw_status qw_init_weights(const qw_config* cfg, const qw_weight_ptrs* w, void* dev_workspace,
+                          size_t ws_bytes, void* stream, qw_model** out);
+
+/* Bytes of device pool for a paged KV cache of `n_pages` pages of page_size tokens for
+ * `max_seqs` sequences: per-sequence lengths and page tables, then K and V pools laid out
+ * [n_layers][n_pages][n_kv_heads][page_size][head_dim] bf16. */
+size_t qw_kv_pool_bytes(const qw_model* m, int n_pages, int max_seqs);
+
+/* Bind a caller-owned pool (256-byte aligned) as the KV cache (Paso 5, "KV cache"). The page
+ * count is the largest that fits pool_bytes. Zeroes lengths and page tables on `stream`. */
+qw_status qw_kv_alloc(qw_model* m, void* dev_pool, size_t pool_bytes, int max_seqs, void* stream,
+                      qw_kv** out);
+
+/* Make sure sequence `seq_id` owns pages for `total_tokens` positions, taking free pages
+ * lowest id first (QW_ERR_KV_FULL, nothing taken, if too few are free). Page-table rows are
+ * written on `stream`. */
+qw_status qw_kv_reserve(qw_kv* kv, int seq_id, int total_tokens, void* stream);
+
+/* Free the pages of `seq_id` (-1: every sequence) and set its length to 0, on `stream`. */
+qw_status qw_kv_reset(qw_kv* kv, int seq_id, void* stream);
+
+int qw_kv_free_pages(const qw_kv* kv);
+int qw_kv_length(const qw_kv* kv, int seq_id); /* host mirror of the device length */
+
+/* Prefill (Paso 9, first forward): run B empty sequences' prompts through the model.
+ * seq_ids[B], lens[B] (host): sequence ids and prompt lengths (each >= 1, each sequence
+ * empty and reserved for at least lens[b] tokens). dev_token_ids: the prompts
+ * concatenated, sum(lens) int32. dev_logits: [B, vocab] fp32 logits of each prompt's last
+ * position, or NULL. dev_next_ids: [B] int32 greedy picks (argmax, lowest index on ties).
+ * Appends every prompt token's K/V to the cache and advances the lengths. */
+qw_status qw_prefill(qw_model* m, qw_kv* kv, int B, const int* seq_ids, const int* lens,
+                     const int32_t* dev_token_ids, float* dev_logits, int32_t* dev_next_ids,
+                     void* stream);
+
+/* One decode step (Paso 9 loop body): each of the B sequences takes one new token at
+ * position = its current length. dev_token_ids [B] may alias the previous step's
+ * dev_next_ids. Outputs as in qw_prefill. The step is replayed from a CUDA graph cached per
+ * (B, seq_ids, pointers); the first call with a new key captures it. */
+qw_status qw_decode_step(qw_model* m, qw_kv* kv, int B, const int* seq_ids,
+                         const int32_t* dev_token_ids, float* dev_logits, int32_t* dev_next_ids,
+                         void* stream);
+
+/* Greedy generation from HOST buffers (Paso 9 at temperature 0, no EOS stop): copies the
+ * concatenated prompts (host_prompt_ids, sum(lens) int32) to the device, prefills, runs
+ * n_decode decode steps feeding each pick back on the device, copies the picks to
+ * host_out_ids ([B, n_decode + 1] int32, row b = sequence b) and synchronises `stream`.
+ * Sequences must be empty and reserved for lens[b] + n_decode tokens. */
+qw_status qw_generate(qw_model* m, qw_kv* kv, int B, const int* seq_ids, const int* lens,
+                      const int32_t* host_prompt_ids, int n_decode, int32_t* host_out_ids,
+                      void* stream);
+
+/* Synchronise `stream`, read and clear the device status word. Returns QW_OK or the first
+ * of QW_ERR_BAD_TOKEN, QW_ERR_BAD_POS, QW_ERR_TIMEOUT that the word records. */
+qw_status qw_sync_status(qw_model* m, void* stream);
+
+/* Message for the calling thread's last error ("" if none). Valid until the next call. */
+const char* qw_last_error(void);
+
+void qw_free_model(qw_model* m); /* frees host state and cached graphs; not the workspace */
+void qw_free_kv(qw_kv* kv);
+
+/* ---- Test and inspection hooks (not on the hot path) -------------------------------- */
+
+/* When dev_hidden is non-NULL, every following prefill/decode call copies the residual
+ * stream after each layer to dev_hidden[layer][t][hidden] (fp32, t < that call's token
+ * count) and writes each token's position and KV slot (page * page_size + offset) to
+ * dev_positions[t] / dev_slots[t]. Pass NULLs to turn it off. Calls made while it is on are
+ * not graph-captured. */
+qw_status qw_debug_set(qw_model* m, float* dev_hidden, int32_t* dev_positions, int32_t* dev_slots);
+
+/* Copy sequence seq_id's page table (host mirror) into host_out[0..max_pages); returns the
+ * number of pages it owns, or a negative qw_status. */
+int qw_kv_page_table(const qw_kv* kv, int seq_id, int32_t* host_out, int max_pages);
+
+/* Device addresses of the K and V pools ([n_layers][n_pages][n_kv_heads][page][head_dim]
+ * bf16) and the page count. */
+qw_status qw_kv_pool_ptrs(const qw_kv* kv, void** dev_k, void** dev_v, int* n_pages);
+
+/* Fill positions [0, n_tokens) of sequence seq_id (reserved, empty) with synthetic K/V from
+ * the counter-based SplitMix64 generator: element index
+ *   idx = (((layer*2 + which) << 22 | pos) * n_kv_heads + head) * head_dim + dim,
+ *   z = splitmix64(seed + (idx + 1) * 0x9E3779B97F4A7C15), b = (int8)(z >> 56),
+ *   K = b / 64, V = b / 128 (exact in bf16),
+ * and set the sequence's length to n_tokens. Stands in for a long prefill. */
+qw_status qw_kv_fill_synthetic(qw_kv* kv, int seq_id, int n_tokens, uint64_t seed, void* stream);
+
+/* Number of kernels the last prefill / decode call enqueued (graph replays count the
+ * kernels inside the graph). */
+int qw_last_launch_count(const qw_model* m);
+
+/* Kernel kinds for qw_profile_set. */
+enum {
+    QW_PROF_OFF = 0,
+    QW_PROF_QKV = 1,      /* q|k|v projection (RMSNorm fused on the small-batch path)    */
+    QW_PROF_ROPE = 2,     /* QK-norm + RoPE + KV append                                   */
+    QW_PROF_ATTN = 3,     /* attention                                                    */
+    QW_PROF_OPROJ = 4,    /* o_proj + residual                                            */
+    QW_PROF_GATEUP = 5,   /* gate/up + SiLU*mul (RMSNorm fused on the small-batch path)   */
+    QW_PROF_DOWN = 6,     /* down_proj + residual                                         */
+    QW_PROF_LMHEAD = 7,   /* final norm + tied LM head + argmax                           */
+    QW_PROF_RMSNORM = 8   /* stand-alone RMSNorm (tensor-core path)                       */
+};
+
+/* Bracket the j-th launch of kernel kind `kind` in every following prefill/decode call with
+ * cudaEventRecord(events[2j]) before and cudaEventRecord(events[2j+1]) after it, on the
+ * launching stream (captured as event-record nodes in decode graphs), for 2j+1 < n_events.
+ * `events` are caller-owned cudaEvent_t handles (timing enabled) that must outlive every
+ * graph captured while they are set; kind QW_PROF_OFF (or events NULL) turns it off. */
+qw_status qw_profile_set(qw_model* m, int kind, void* const* events, int n_events);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QW_H */

@@ -101,12 +101,33 @@ def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
     return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
 
 
+_CHUNK = 1 << 22
+
+
 def _draw(seed: int, group: int, index: int, shape, is_norm: bool) -> np.ndarray:
+    """Draws the tensor's normals in consecutive chunks of one stream (identical to a single
+    draw of the whole tensor) into reused buffers, then rounds each chunk to bf16."""
     rng = np.random.default_rng(np.random.SeedSequence([seed, group, index]))
-    z = rng.standard_normal(shape, dtype=np.float32) * np.float32(0.02)
-    if is_norm:
-        z = z + np.float32(1.0)
-    return f32_to_bf16_bits(z)
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.uint16)
+    buf = np.empty(min(n, _CHUNK), dtype=np.float32)
+    u = buf.view(np.uint32)
+    tmp = np.empty_like(u)
+    for a in range(0, n, _CHUNK):
+        m = min(_CHUNK, n - a)
+        z, uu, tt = buf[:m], u[:m], tmp[:m]
+        rng.standard_normal(out=z, dtype=np.float32)
+        z *= np.float32(0.02)
+        if is_norm:
+            z += np.float32(1.0)
+        # round to nearest even on the upper 16 bits
+        np.right_shift(uu, np.uint32(16), out=tt)
+        tt &= np.uint32(1)
+        tt += np.uint32(0x7FFF)
+        uu += tt
+        uu >>= np.uint32(16)
+        out[a:a + m] = uu
+    return out.reshape(shape)
 
 
 def make_layer(s: Shape, layer: int, seed: int = 0) -> Dict[str, np.ndarray]:

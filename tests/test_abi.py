@@ -1,0 +1,61 @@
+"""The C-ABI library builds for sm_103a, loads, and exports every entry point the header
+declares; the binding's signature table covers the same set. No GPU needed (no compute)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "qw.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = set(re.findall(r"\b(qw_[a-z0-9_]+)\s*\(", src))
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import decode_qwen3_decoder_gb300 as pkg
+    path = pkg._build_lib()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for fn in ("qw_init_weights", "qw_prefill", "qw_decode_step", "qw_kv_alloc", "qw_kv_reset",
+               "qw_kv_reserve", "qw_generate", "qw_sync_status", "qw_last_error"):
+        assert fn in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in sorted(_declared()) if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_covers_header():
+    from decode_qwen3_decoder_gb300 import qw
+    assert set(qw.SIGNATURES) == _declared()
+
+
+def test_host_only_calls_without_gpu(lib):
+    """Entry points that touch no device: config validation and error strings."""
+    from decode_qwen3_decoder_gb300 import qw
+    import synth
+    qw.load()
+    cfg = qw.make_config(synth.QWEN3_0_6B, max_tokens=64, max_batch=8, max_context=2048)
+    assert qw.qw_model_workspace_bytes(cfg) > 0
+    bad = qw.make_config(synth.QWEN3_0_6B, max_tokens=64, max_batch=8, max_context=2048)
+    bad.head_dim = 64
+    assert qw.qw_model_workspace_bytes(bad) == 0
+    bad2 = qw.make_config(synth.TINY, max_tokens=64, max_batch=8, max_context=64)
+    assert qw.qw_model_workspace_bytes(bad2) == 0   # head_dim 16 is not built
+    out = ctypes.c_void_p()
+    st = qw.load().qw_init_weights(ctypes.byref(cfg), None, None, 0, None, ctypes.byref(out))
+    assert st == -1 and out.value is None
+    assert "weight pointers" in qw.qw_last_error() or "NULL" in qw.qw_last_error()
+    assert qw.qw_kv_length(None, 0) == -1
+    assert qw.qw_kv_free_pages(None) == -1

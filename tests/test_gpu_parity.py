@@ -1,0 +1,197 @@
+"""GPU parity, small-batch path (<= 8 token rows per call: the GEMV family + paged attention).
+
+Each test drives libqw through its C ABI and compares with the fp64 oracle on the same
+seeded bf16 weights: positions and KV slots bit-exact, hidden state per layer and token
+within 5e-3 normwise, logits within 5e-2, greedy ids equal when the oracle's top-2 gap
+exceeds 1e-2.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_util import Run, check_hidden, check_logits, check_token, engine, weights
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def one_block(qw):
+    eng = engine(qw, synth.ONE_BLOCK, max_tokens=64, max_batch=16, max_context=512, kv_pages=256,
+                 max_seqs=16)
+    yield Run(qw, eng), oracle.Model(weights(synth.ONE_BLOCK))
+    eng.close()
+
+
+def _n_pages(run):
+    return run.qw.qw_kv_pool_ptrs(run.eng.kv)[2]
+
+
+def _greedy_parity(run, om, prompt, n_decode, graph_steps=()):
+    """Prefill + n_decode greedy steps on sequence 0; the oracle runs its own greedy loop.
+    Comparison stops at the first legitimate divergence (ids differ where the top-2 gap is
+    within tolerance)."""
+    s = run.s
+    qw, eng = run.qw, run.eng
+    qw.qw_kv_reset(eng.kv, -1, eng.stream)
+    mirror = oracle.PagedKVMirror(_n_pages(run), 16, 16)
+    mirror.reserve(0, len(prompt) + n_decode)
+    cache = oracle.SeqCache(s.n_layers)
+    o = oracle.forward(om, prompt, cache)
+    g = run.prefill([0], [prompt], reserve_extra=n_decode)
+    assert g["status"] == 0
+    np.testing.assert_array_equal(g["pos"], np.arange(len(prompt)))
+    np.testing.assert_array_equal(g["slot"], mirror.slots(0, range(len(prompt))))
+    np.testing.assert_array_equal(qw.qw_kv_page_table(eng.kv, 0), mirror.tables[0])
+    check_hidden(g["hidden"], o["hidden"])
+    check_logits(g["logits"][0], o["logits"])
+    same = check_token(g["next"][0], o["logits"])
+    tok = int(g["next"][0])
+    compared = 0
+    for step in range(n_decode):
+        if not same:
+            break
+        pos = len(prompt) + step
+        o = oracle.forward(om, [tok], cache)
+        dbg = step not in graph_steps
+        g = run.decode([0], [tok], debug=dbg)
+        assert g["status"] == 0
+        if dbg:
+            assert g["pos"][0] == pos
+            assert g["slot"][0] == mirror.slots(0, [pos])[0]
+            check_hidden(g["hidden"], o["hidden"])
+        check_logits(g["logits"][0], o["logits"])
+        same = check_token(g["next"][0], o["logits"])
+        tok = int(g["next"][0])
+        compared += 1
+    return compared
+
+
+def test_config0_random_prompt_greedy(one_block):
+    run, om = one_block
+    prompt = synth.make_tokens(synth.ONE_BLOCK.vocab, 5, 1000).tolist()
+    n = _greedy_parity(run, om, prompt, 16, graph_steps=range(8, 16))
+    assert n >= 8
+
+
+def test_config0_page_prompt_greedy(one_block):
+    run, om = one_block
+    n = _greedy_parity(run, om, list(synth.PAGE_PROMPT), 16)
+    assert n >= 8
+
+
+def test_graph_replay_bit_identical_to_direct(one_block):
+    run, _ = one_block
+    qw, eng = run.qw, run.eng
+    prompt = synth.make_tokens(synth.ONE_BLOCK.vocab, 7, 77).tolist()
+    outs = []
+    for dbg in (True, False, False):
+        qw.qw_kv_reset(eng.kv, -1, eng.stream)
+        g = run.prefill([3], [prompt], debug=False, reserve_extra=4)
+        tok = int(g["next"][0])
+        steps = []
+        for _ in range(3):
+            d = run.decode([3], [tok], debug=dbg)
+            steps.append(d["logits"][0])
+            tok = int(d["next"][0])
+        outs.append(np.stack(steps))
+    np.testing.assert_array_equal(outs[0], outs[1])
+    np.testing.assert_array_equal(outs[1], outs[2])
+
+
+def test_ragged_small_batch_slots_and_values(one_block):
+    """Three sequences with interleaved reservations, prefilled together (6 tokens)."""
+    run, om = one_block
+    s = synth.ONE_BLOCK
+    qw, eng = run.qw, run.eng
+    qw.qw_kv_reset(eng.kv, -1, eng.stream)
+    mirror = oracle.PagedKVMirror(_n_pages(run), 16, 16)
+    for seq, n in ((2, 20), (0, 7), (2, 40), (5, 3)):
+        qw.qw_kv_reserve(eng.kv, seq, n, eng.stream)
+        mirror.reserve(seq, n)
+    seqs = [2, 0, 5]
+    prompts = [synth.make_tokens(s.vocab, n, 300 + i).tolist() for i, n in enumerate((3, 2, 1))]
+    g = run.prefill(seqs, prompts)
+    assert g["status"] == 0
+    want_pos = np.concatenate([np.arange(len(p)) for p in prompts])
+    want_slot = np.concatenate([mirror.slots(sq, range(len(p))) for sq, p in zip(seqs, prompts)])
+    np.testing.assert_array_equal(g["pos"], want_pos)
+    np.testing.assert_array_equal(g["slot"], want_slot)
+    for sq in (0, 2, 5):
+        np.testing.assert_array_equal(qw.qw_kv_page_table(eng.kv, sq), mirror.tables[sq])
+    # per-sequence oracle: hidden states and last-position logits; K rows at their slots
+    kptr, _, n_pages = qw.qw_kv_pool_ptrs(eng.kv)
+    import torch
+    off = kptr - eng.pool.data_ptr()
+    nk = n_pages * s.n_kv_heads * 16 * s.head_dim
+    k0 = eng.pool[off:off + 2 * nk].view(torch.bfloat16).float().cpu().numpy()
+    k0 = k0.reshape(n_pages, s.n_kv_heads, 16, s.head_dim)
+    row = 0
+    for b, (sq, p) in enumerate(zip(seqs, prompts)):
+        taps = {}
+        o = oracle.forward(om, p, oracle.SeqCache(1), taps=taps)
+        check_hidden(g["hidden"][:, row:row + len(p)], o["hidden"])
+        check_logits(g["logits"][b], o["logits"])
+        check_token(g["next"][b], o["logits"])
+        for j in range(len(p)):
+            slot = int(want_slot[row + j])
+            got = k0[slot // 16, :, slot % 16, :]            # [n_kv, head_dim]
+            want = taps["k"][0][:, j, :]                      # layer 0, after QK-norm + RoPE
+            err = np.linalg.norm(got - want) / np.linalg.norm(want)
+            assert err < 1e-2, (sq, j, err)
+        row += len(p)
+
+
+def test_error_paths_leave_state(one_block):
+    run, _ = one_block
+    qw, eng = run.qw, run.eng
+    qw.qw_kv_reset(eng.kv, -1, eng.stream)
+    free = qw.qw_kv_free_pages(eng.kv)
+    per_seq = 512 // 16
+    n_full = free // per_seq
+    for sq in range(n_full):
+        qw.qw_kv_reserve(eng.kv, sq, 512, eng.stream)
+    left = qw.qw_kv_free_pages(eng.kv)
+    with pytest.raises(qw.QwError) as e:
+        qw.qw_kv_reserve(eng.kv, n_full, 16 * (left + 1), eng.stream)
+    assert e.value.status == -2
+    assert qw.qw_kv_free_pages(eng.kv) == left       # nothing was taken
+    qw.qw_kv_reset(eng.kv, -1, eng.stream)
+    assert qw.qw_kv_free_pages(eng.kv) == free
+    # prefill beyond the reservation
+    qw.qw_kv_reserve(eng.kv, 1, 4, eng.stream)
+    with pytest.raises(qw.QwError) as e:
+        run.prefill([1], [[1] * 20], debug=False, reserve=False)
+    assert e.value.status == -2
+    assert qw.qw_kv_length(eng.kv, 1) == 0
+    # prefill into a non-empty sequence
+    g = run.prefill([1], [[1, 2, 3]], debug=False)
+    assert g["status"] == 0
+    with pytest.raises(qw.QwError) as e:
+        run.prefill([1], [[4]], debug=False, reserve=False)
+    assert e.value.status == -3
+    assert qw.qw_kv_length(eng.kv, 1) == 3
+    # a token id outside the vocabulary is reported through the status word
+    qw.qw_kv_reserve(eng.kv, 4, 8, eng.stream)
+    g = run.prefill([4], [[5, synth.ONE_BLOCK.vocab + 3]], debug=False)
+    assert g["status"] == -5
+    assert qw.qw_sync_status(eng.model, eng.stream) == 0  # the word was cleared
+
+
+@pytest.fixture(scope="module")
+def full_model(qw):
+    eng = engine(qw, synth.QWEN3_0_6B, max_tokens=64, max_batch=8, max_context=256, kv_pages=64,
+                 max_seqs=8)
+    yield Run(qw, eng), oracle.Model(weights(synth.QWEN3_0_6B))
+    eng.close()
+
+
+def test_config1_greedy_28_layers(full_model):
+    """28 layers, batch 1, 5-token prompt, 64 greedy decode steps (graph replays except a few
+    steps that also dump hidden states)."""
+    run, om = full_model
+    prompt = synth.make_tokens(synth.QWEN3_0_6B.vocab, 5, 1001).tolist()
+    graph = [i for i in range(64) if i not in (0, 31, 63)]
+    n = _greedy_parity(run, om, prompt, 64, graph_steps=graph)
+    assert n >= 32
