@@ -241,6 +241,8 @@ def run_ours(args, cfg, rank, world):
     n_launch_per_step = {1: s.n_layers, 4: s.n_layers, 5: s.n_layers, 6: s.n_layers, 7: 1}
     for kind, nl in n_launch_per_step.items():
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * nl)]
+        for ev in evs:          # torch creates the CUDA event on its first record
+            ev.record(st)
         handles = (qw.ctypes.c_void_p * (2 * nl))(*[ev.cuda_event for ev in evs])
         durs = []
         qw.qw_kv_reset(eng.kv, -1, st)

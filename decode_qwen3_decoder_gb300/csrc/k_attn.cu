@@ -44,14 +44,14 @@ __device__ __forceinline__ uint4 ldg_nc(const void* p) {
 }
 
 __device__ __forceinline__ float dot8q(const float* q, const uint4 k) {
-    float a = q[0] * bf_lo(k.x);
-    a = fmaf(q[1], bf_hi(k.x), a);
-    a = fmaf(q[2], bf_lo(k.y), a);
-    a = fmaf(q[3], bf_hi(k.y), a);
-    a = fmaf(q[4], bf_lo(k.z), a);
-    a = fmaf(q[5], bf_hi(k.z), a);
-    a = fmaf(q[6], bf_lo(k.w), a);
-    a = fmaf(q[7], bf_hi(k.w), a);
+    float a = q[0] * h_lo(k.x);
+    a = fmaf(q[1], h_hi(k.x), a);
+    a = fmaf(q[2], h_lo(k.y), a);
+    a = fmaf(q[3], h_hi(k.y), a);
+    a = fmaf(q[4], h_lo(k.z), a);
+    a = fmaf(q[5], h_hi(k.z), a);
+    a = fmaf(q[6], h_lo(k.w), a);
+    a = fmaf(q[7], h_hi(k.w), a);
     return a;
 }
 
@@ -66,7 +66,7 @@ __device__ __forceinline__ float half_warp_sum(float v) {
 }  // namespace
 
 struct AttnP {
-    const bf16* q;      // [T][n_heads][128]
+    const f16* q;       // [T][n_heads][128]
     int n_heads, n_kv;
     TokView tv;
     KVView kv;
@@ -76,7 +76,7 @@ struct AttnP {
     float* part_o;      // [T][n_heads][n_splits][128]
     float* part_ml;     // [T][n_heads][n_splits][2]
     int* counters;      // [T][n_kv]
-    bf16* out;          // [T][n_heads * 128]
+    f16* out;           // [T][n_heads * 128]
     float scale_log2;   // head_dim^-0.5 * log2(e)
 };
 
@@ -95,16 +95,16 @@ __global__ void __launch_bounds__(AW * 32) k_attn_paged(AttnP p) {
 
     float q0[8], q1[8];
     {
-        const bf16* qp = p.q + ((size_t)t * p.n_heads + 2 * g) * 128 + dl;
+        const f16* qp = p.q + ((size_t)t * p.n_heads + 2 * g) * 128 + dl;
         const uint4 a = *reinterpret_cast<const uint4*>(qp);
         const uint4 b = *reinterpret_cast<const uint4*>(qp + 128);
         const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            q0[2 * i] = bf_lo(aw[i]) * p.scale_log2;
-            q0[2 * i + 1] = bf_hi(aw[i]) * p.scale_log2;
-            q1[2 * i] = bf_lo(bw[i]) * p.scale_log2;
-            q1[2 * i + 1] = bf_hi(bw[i]) * p.scale_log2;
+            q0[2 * i] = h_lo(aw[i]) * p.scale_log2;
+            q0[2 * i + 1] = h_hi(aw[i]) * p.scale_log2;
+            q1[2 * i] = h_lo(bw[i]) * p.scale_log2;
+            q1[2 * i + 1] = h_hi(bw[i]) * p.scale_log2;
         }
     }
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
@@ -112,8 +112,8 @@ __global__ void __launch_bounds__(AW * 32) k_attn_paged(AttnP p) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) o0[i] = o1[i] = 0.f;
 
-    const bf16* Kl = p.kv.k + (size_t)p.layer * p.kv.layer_stride;
-    const bf16* Vl = p.kv.v + (size_t)p.layer * p.kv.layer_stride;
+    const f16* Kl = p.kv.k + (size_t)p.layer * p.kv.layer_stride;
+    const f16* Vl = p.kv.v + (size_t)p.layer * p.kv.layer_stride;
     const int* pt = p.kv.page_table + (size_t)seq * p.kv.max_pages_per_seq;
     const int p0 = k0 >> 4, p1 = (k1 + 15) >> 4;
 
@@ -160,7 +160,7 @@ __global__ void __launch_bounds__(AW * 32) k_attn_paged(AttnP p) {
             const uint32_t vw[4] = {vr[i].x, vr[i].y, vr[i].z, vr[i].w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const float va = bf_lo(vw[j]), vb = bf_hi(vw[j]);
+                const float va = h_lo(vw[j]), vb = h_hi(vw[j]);
                 o0[2 * j] = fmaf(e0, va, o0[2 * j]);
                 o0[2 * j + 1] = fmaf(e0, vb, o0[2 * j + 1]);
                 o1[2 * j] = fmaf(e1, va, o1[2 * j]);
@@ -209,9 +209,9 @@ __global__ void __launch_bounds__(AW * 32) k_attn_paged(AttnP p) {
         O1 += sm_o[w][hh][d2 + 1] * f;
     }
     const int head = 2 * g + hh;
-    bf16* outp = p.out + ((size_t)t * p.n_heads + head) * 128 + d2;
+    f16* outp = p.out + ((size_t)t * p.n_heads + head) * 128 + d2;
     if (n_act == 1) {
-        *reinterpret_cast<uint32_t*>(outp) = pack_bf2(O0 / L, O1 / L);
+        *reinterpret_cast<uint32_t*>(outp) = pack_h2(O0 / L, O1 / L);
         pdl_launch();
         return;
     }
@@ -239,14 +239,14 @@ __global__ void __launch_bounds__(AW * 32) k_attn_paged(AttnP p) {
         A0 += ov.x * f;
         A1 += ov.y * f;
     }
-    *reinterpret_cast<uint32_t*>(outp) = pack_bf2(A0 / LL, A1 / LL);
+    *reinterpret_cast<uint32_t*>(outp) = pack_h2(A0 / LL, A1 / LL);
     if (threadIdx.x == 0) p.counters[(size_t)t * p.n_kv + g] = 0;
     pdl_launch();
 }
 
-cudaError_t launch_attn_paged(const LaunchCtx& c, int T, int layer, const bf16* q, int n_heads,
+cudaError_t launch_attn_paged(const LaunchCtx& c, int T, int layer, const f16* q, int n_heads,
                               int n_kv, TokView tv, KVView kv, int chunk, int n_splits,
-                              float* part_o, float* part_ml, int* counters, bf16* out) {
+                              float* part_o, float* part_ml, int* counters, f16* out) {
     AttnP p;
     p.q = q;
     p.n_heads = n_heads;

@@ -4,9 +4,10 @@
 //
 // The product is computed transposed, D^T[m][t] = sum_k W[m][k] * H[t][k]: the weight tile
 // (128 output features) is the A operand and the token tile (BN = 64/128/256 rows) the B
-// operand, both K-major bf16 in shared memory with the 128-byte swizzle, fed by TMA
+// operand, both K-major fp16 in shared memory with the 128-byte swizzle, fed by TMA
 // (cp.async.bulk.tensor) through an mbarrier ring. One elected thread issues
-// tcgen05.mma.cta_group::1.kind::f16 (M=128, N=BN, K=16) into an fp32 accumulator in TMEM;
+// tcgen05.mma.cta_group::1.kind::f16 (M=128, N=BN, K=16, fp16 x fp16) into an fp32
+// accumulator in TMEM;
 // the four epilogue warps read it back with tcgen05.ld.32x32b (thread = output feature,
 // registers = tokens), so every store of a token row is a coalesced 32-feature run.
 // Epilogues: plain fp32 store (q|k|v), residual add into the fp32 stream (o_proj,
@@ -22,7 +23,7 @@
 namespace {
 
 constexpr int BM = 128;
-constexpr int BK = 64;  // 64 bf16 = 128 bytes = one swizzle row
+constexpr int BK = 64;  // 64 fp16 = 128 bytes = one swizzle row
 constexpr int GEMM_THREADS = 192;
 constexpr unsigned long long kWaitNs = 2000000000ull;
 
@@ -88,12 +89,14 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
     return d;
 }
 
-// Instruction descriptor of kind::f16: fp32 accumulate, bf16 A and B, both K-major.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+// Instruction descriptor of kind::f16: fp32 accumulate (bits 4-5 = 1), fp16 A and B (format
+// 0 in bits 7-9 and 10-12), both K-major (bits 15, 16 clear), N >> 3 at bit 17, M >> 4 at
+// bit 24.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
+    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
@@ -138,7 +141,7 @@ struct GemmCfg {
 struct GemmKParams {
     int a_row0, a2_row0, K, T, ld_out;
     float* out_f32;
-    bf16* out_bf16;
+    f16* out_h;
     float* logits;
     unsigned long long* best;
     int* status;
@@ -213,7 +216,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     } else if (warp == 5) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16(BM, BN);
+            constexpr uint32_t idesc = idesc_f16(BM, BN);
             bool ok = true;
             for (int kb = 0; kb < nk; ++kb) {
                 const int s = kb % C::STAGES;
@@ -230,10 +233,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 #pragma unroll
                 for (int k = 0; k < BK / 16; ++k) {
                     const uint32_t acc = (kb > 0 || k > 0) ? 1u : 0u;
-                    umma_bf16(tmem, ad + 2 * k, bd + 2 * k, idesc, acc);
+                    umma_f16(tmem, ad + 2 * k, bd + 2 * k, idesc, acc);
                     if (NA == 2) {
                         const uint64_t a2 = sw128_desc(st + C::A_BYTES);
-                        umma_bf16(tmem + BN, a2 + 2 * k, bd + 2 * k, idesc, acc);
+                        umma_f16(tmem + BN, a2 + 2 * k, bd + 2 * k, idesc, acc);
                     }
                 }
                 umma_commit(smem_u32(empty + s));  // frees the stage once these MMAs finish
@@ -261,7 +264,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         const int tok = n0 + c0 + j;
                         if (tok < p.T) {
                             const float g = __uint_as_float(r[j]), uu = __uint_as_float(u[j]);
-                            p.out_bf16[(size_t)tok * p.ld_out + f] = __float2bfloat16_rn(g / (1.0f + expf(-g)) * uu);
+                            p.out_h[(size_t)tok * p.ld_out + f] = __float2half_rn(g / (1.0f + expf(-g)) * uu);
                         }
                     }
                 } else {
@@ -335,7 +338,7 @@ cudaError_t gemm_go(const LaunchCtx& c, const GemmArgs& a, int bn_idx) {
     p.T = a.T;
     p.ld_out = a.ld_out;
     p.out_f32 = a.out_f32;
-    p.out_bf16 = a.out_bf16;
+    p.out_h = a.out_h;
     p.logits = a.logits;
     p.best = a.best;
     p.status = a.status;
@@ -388,7 +391,7 @@ bool encode_one(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols
     cuuint64_t strides[1] = {cols * 2};
     cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
     cuuint32_t estr[2] = {1, 1};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

@@ -37,16 +37,16 @@ __device__ __forceinline__ uint4 ldg_stream(const void* p) {
     return r;
 }
 
-// 8 bf16 weights (one 16-byte chunk) against 8 fp32 activations.
+// 8 fp16 weights (one 16-byte chunk) against 8 fp32 activations.
 __device__ __forceinline__ float dot8(const uint4 w, const float4 a0, const float4 a1, float acc) {
-    acc = fmaf(bf_lo(w.x), a0.x, acc);
-    acc = fmaf(bf_hi(w.x), a0.y, acc);
-    acc = fmaf(bf_lo(w.y), a0.z, acc);
-    acc = fmaf(bf_hi(w.y), a0.w, acc);
-    acc = fmaf(bf_lo(w.z), a1.x, acc);
-    acc = fmaf(bf_hi(w.z), a1.y, acc);
-    acc = fmaf(bf_lo(w.w), a1.z, acc);
-    acc = fmaf(bf_hi(w.w), a1.w, acc);
+    acc = fmaf(h_lo(w.x), a0.x, acc);
+    acc = fmaf(h_hi(w.x), a0.y, acc);
+    acc = fmaf(h_lo(w.y), a0.z, acc);
+    acc = fmaf(h_hi(w.y), a0.w, acc);
+    acc = fmaf(h_lo(w.z), a1.x, acc);
+    acc = fmaf(h_hi(w.z), a1.y, acc);
+    acc = fmaf(h_lo(w.w), a1.z, acc);
+    acc = fmaf(h_hi(w.w), a1.w, acc);
     return acc;
 }
 
@@ -94,12 +94,12 @@ cudaError_t launch_step_begin(const LaunchCtx& c, const StepDesc& sd, const int3
 }
 
 // =======================================================================================
-// RMSNorm (Paso 3) of fp32 rows into bf16 GEMM operands: h = x * rsqrt(mean(x^2) + eps) * w.
+// RMSNorm (Paso 3) of fp32 rows into fp16 GEMM operands: h = x * rsqrt(mean(x^2) + eps) * w.
 // One warp per row; `rows` optionally gathers (the LM head reads each sequence's last row).
 // =======================================================================================
 __global__ void __launch_bounds__(256) k_rmsnorm(const float* __restrict__ x, const int* __restrict__ rows,
                                                  int n_rows, int hidden, const bf16* __restrict__ w,
-                                                 float eps, bf16* __restrict__ h) {
+                                                 float eps, f16* __restrict__ h) {
     pdl_wait();
     const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
@@ -111,13 +111,13 @@ __global__ void __launch_bounds__(256) k_rmsnorm(const float* __restrict__ x, co
             ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
         }
         const float rs = rsqrtf(warp_sum(ss) / (float)hidden + eps);
-        bf16* hr = h + (size_t)r * hidden;
+        f16* hr = h + (size_t)r * hidden;
         for (int k = lane * 4; k < hidden; k += 128) {
             float4 v = *reinterpret_cast<const float4*>(xr + k);
             uint2 wb = *reinterpret_cast<const uint2*>(w + k);
             uint2 o;
-            o.x = pack_bf2(v.x * rs * bf_lo(wb.x), v.y * rs * bf_hi(wb.x));
-            o.y = pack_bf2(v.z * rs * bf_lo(wb.y), v.w * rs * bf_hi(wb.y));
+            o.x = pack_h2(v.x * rs * bf_lo(wb.x), v.y * rs * bf_hi(wb.x));
+            o.y = pack_h2(v.z * rs * bf_lo(wb.y), v.w * rs * bf_hi(wb.y));
             *reinterpret_cast<uint2*>(hr + k) = o;
         }
     }
@@ -125,7 +125,7 @@ __global__ void __launch_bounds__(256) k_rmsnorm(const float* __restrict__ x, co
 }
 
 cudaError_t launch_rmsnorm(const LaunchCtx& c, const float* x, const int* rows, int n_rows,
-                           int hidden, const bf16* w, float eps, bf16* h) {
+                           int hidden, const bf16* w, float eps, f16* h) {
     return launch_k(c, k_rmsnorm, dim3((n_rows + 7) / 8), dim3(256), 0, x, rows, n_rows, hidden, w,
                     eps, h);
 }
@@ -136,11 +136,11 @@ cudaError_t launch_rmsnorm(const LaunchCtx& c, const float* x, const int* rows, 
 // Each warp owns RPW output rows at a time; every lane streams one 16-byte chunk of each
 // row per 256 columns, so a warp reads whole rows with coalesced 512-byte requests, in
 // passes of 1024 columns that keep RPW*4 16-byte loads per lane in flight. The activations sit in
-// shared memory as fp32. MODE selects the prologue/epilogue:
-//   G_QKV    : a = bf16(rms_norm(x) * w_in)  (Paso 3 fused), out fp32 (Paso 5 projections)
-//   G_GATEUP : a = bf16(rms_norm(x) * w_post), act = bf16(silu(Wg a) * (Wu a))  (Paso 6)
-//   G_RESID  : a = bf16 activations, x += W a  (o_proj / down_proj + residual, Paso 7)
-//   G_LMHEAD : a = bf16(rms_norm(x[last]) * w_final), logits, packed argmax (Paso 8)
+// shared memory as fp32; weights are fp16. MODE selects the prologue/epilogue:
+//   G_QKV    : a = rms_norm(x) * w_in  (Paso 3 fused), out fp32 (Paso 5 projections)
+//   G_GATEUP : a = rms_norm(x) * w_post, act = fp16(silu(Wg a) * (Wu a))  (Paso 6)
+//   G_RESID  : a = fp16 activations, x += W a  (o_proj / down_proj + residual, Paso 7)
+//   G_LMHEAD : a = rms_norm(x[last]) * w_final, logits, packed argmax (Paso 8)
 // =======================================================================================
 enum { G_QKV = 0, G_GATEUP = 1, G_RESID = 2, G_LMHEAD = 3 };
 
@@ -149,14 +149,14 @@ struct GemvP {
     const int* rows;
     const bf16* norm_w;
     float eps;
-    const bf16* act;
-    const bf16* W;
-    const bf16* W2;
+    const f16* act;
+    const f16* W;
+    const f16* W2;
     int n_out;
     int K;
     int T;
     float* out;
-    bf16* out_bf16;
+    f16* out_h;
     unsigned long long* best;
 };
 
@@ -178,8 +178,8 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) k_gemv(GemvP p) {
             float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
             if (t < p.T) {
                 uint4 w = *reinterpret_cast<const uint4*>(p.act + (size_t)t * K + k8);
-                a0 = make_float4(bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y));
-                a1 = make_float4(bf_lo(w.z), bf_hi(w.z), bf_lo(w.w), bf_hi(w.w));
+                a0 = make_float4(h_lo(w.x), h_hi(w.x), h_lo(w.y), h_hi(w.y));
+                a1 = make_float4(h_lo(w.z), h_hi(w.z), h_lo(w.w), h_hi(w.w));
             }
             *reinterpret_cast<float4*>(hs + t * K + k8) = a0;
             *reinterpret_cast<float4*>(hs + t * K + k8 + 4) = a1;
@@ -207,10 +207,8 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) k_gemv(GemvP p) {
                 float4 v = *reinterpret_cast<const float4*>(xr + k4);
                 uint2 wb = *reinterpret_cast<const uint2*>(p.norm_w + k4);
                 const float r = rs[t];
-                // round to bf16: the projection operand precision of the tensor-core path
-                uint32_t lo = pack_bf2(v.x * r * bf_lo(wb.x), v.y * r * bf_hi(wb.x));
-                uint32_t hi = pack_bf2(v.z * r * bf_lo(wb.y), v.w * r * bf_hi(wb.y));
-                o = make_float4(bf_lo(lo), bf_hi(lo), bf_lo(hi), bf_hi(hi));
+                o = make_float4(v.x * r * bf_lo(wb.x), v.y * r * bf_hi(wb.x), v.z * r * bf_lo(wb.y),
+                                v.w * r * bf_hi(wb.y));
             }
             *reinterpret_cast<float4*>(hs + t * K + k4) = o;
         }
@@ -277,7 +275,7 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) k_gemv(GemvP p) {
                             p.out[(size_t)t * p.n_out + row] += acc[rr][0][t];
                         } else if (MODE == G_GATEUP) {
                             const float g = acc[rr][0][t], u = acc[rr][NW - 1][t];
-                            p.out_bf16[(size_t)t * p.n_out + row] = __float2bfloat16_rn(silu_f(g) * u);
+                            p.out_h[(size_t)t * p.n_out + row] = __float2half_rn(silu_f(g) * u);
                         } else {
                             if (p.out) p.out[(size_t)t * p.n_out + row] = acc[rr][0][t];
                             best[t] = u64_max(best[t], argmax_key(acc[rr][0][t], row));
@@ -361,21 +359,21 @@ cudaError_t gemv_dispatch(const LaunchCtx& c, const GemvP& p, int max_ctas) {
 }  // namespace
 
 cudaError_t launch_gemv_qkv(const LaunchCtx& c, int T, const float* x, const bf16* norm_w, float eps,
-                            const bf16* W, int n_out, int K, float* out) {
+                            const f16* W, int n_out, int K, float* out) {
     GemvP p = {};
     p.x = x; p.norm_w = norm_w; p.eps = eps; p.W = W; p.n_out = n_out; p.K = K; p.T = T; p.out = out;
     return gemv_dispatch<G_QKV>(c, p, 0);
 }
 
 cudaError_t launch_gemv_gateup(const LaunchCtx& c, int T, const float* x, const bf16* norm_w,
-                               float eps, const bf16* Wg, const bf16* Wu, int inter, int K, bf16* act) {
+                               float eps, const f16* Wg, const f16* Wu, int inter, int K, f16* act) {
     GemvP p = {};
     p.x = x; p.norm_w = norm_w; p.eps = eps; p.W = Wg; p.W2 = Wu; p.n_out = inter; p.K = K; p.T = T;
-    p.out_bf16 = act;
+    p.out_h = act;
     return gemv_dispatch<G_GATEUP>(c, p, 0);
 }
 
-cudaError_t launch_gemv_resid(const LaunchCtx& c, int T, const bf16* act, const bf16* W, int n_out,
+cudaError_t launch_gemv_resid(const LaunchCtx& c, int T, const f16* act, const f16* W, int n_out,
                               int K, float* x) {
     GemvP p = {};
     p.act = act; p.W = W; p.n_out = n_out; p.K = K; p.T = T; p.out = x;
@@ -383,7 +381,7 @@ cudaError_t launch_gemv_resid(const LaunchCtx& c, int T, const bf16* act, const 
 }
 
 cudaError_t launch_gemv_lmhead(const LaunchCtx& c, int B, const float* x, const int* rows,
-                               const bf16* norm_w, float eps, const bf16* E, int vocab, int K,
+                               const bf16* norm_w, float eps, const f16* E, int vocab, int K,
                                float* logits, unsigned long long* best) {
     GemvP p = {};
     p.x = x; p.rows = rows; p.norm_w = norm_w; p.eps = eps; p.W = E; p.n_out = vocab; p.K = K;
@@ -418,15 +416,15 @@ cudaError_t launch_finalize(const LaunchCtx& c, const StepDesc& sd, unsigned lon
 //   q, k heads: per-head RMSNorm over head_dim with the shared [head_dim] weight, then the
 //               rotation by pos * theta^(-i/64) (cos/sin from the fp32 table).
 //   v heads   : copied.
-// q is written as bf16 [T][n_heads][128]; k and v go to the page slot
-// page_table[seq][pos / 16] * 16 + pos % 16 of this layer, and to a contiguous bf16
+// q is written as fp16 [T][n_heads][128]; k and v go (fp16) to the page slot
+// page_table[seq][pos / 16] * 16 + pos % 16 of this layer, and to a contiguous fp16
 // [T][2][n_kv][128] copy that the prefill attention reads.
 // =======================================================================================
 __global__ void __launch_bounds__(256) k_qknorm_rope_append(
     int T, int layer, const float* __restrict__ qkv, const bf16* __restrict__ q_norm,
     const bf16* __restrict__ k_norm, float eps, const float* __restrict__ rope_cos,
     const float* __restrict__ rope_sin, int n_heads, int n_kv, TokView tv, KVView kv,
-    bf16* __restrict__ q_out, bf16* __restrict__ kv_new, int32_t* dbg_pos, int32_t* dbg_slot,
+    f16* __restrict__ q_out, f16* __restrict__ kv_new, int32_t* dbg_pos, int32_t* dbg_slot,
     int* status) {
     pdl_wait();
     const int NH = n_heads + 2 * n_kv;
@@ -460,8 +458,8 @@ __global__ void __launch_bounds__(256) k_qknorm_rope_append(
             for (int j = 0; j < 4; ++j) y[j] = o[j];
         }
         uint2 packed;
-        packed.x = pack_bf2(y[0], y[1]);
-        packed.y = pack_bf2(y[2], y[3]);
+        packed.x = pack_h2(y[0], y[1]);
+        packed.y = pack_h2(y[2], y[3]);
         if (hh < n_heads) {
             *reinterpret_cast<uint2*>(q_out + ((size_t)t * n_heads + hh) * 128 + lane * 4) = packed;
         } else {
@@ -474,8 +472,8 @@ __global__ void __launch_bounds__(256) k_qknorm_rope_append(
             if (page < 0 || page >= kv.n_pages) {
                 if (lane == 0) atomicOr(status, QW_DEV_BAD_POS);
             } else {
-                bf16* pool = (which == 0 ? kv.k : kv.v) + (size_t)layer * kv.layer_stride;
-                bf16* dst = pool + (((size_t)page * n_kv + g) * 16 + (pos & 15)) * 128 + lane * 4;
+                f16* pool = (which == 0 ? kv.k : kv.v) + (size_t)layer * kv.layer_stride;
+                f16* dst = pool + (((size_t)page * n_kv + g) * 16 + (pos & 15)) * 128 + lane * 4;
                 *reinterpret_cast<uint2*>(dst) = packed;
                 if (dbg_pos && which == 0 && g == 0 && lane == 0) {
                     dbg_pos[t] = pos;
@@ -490,7 +488,7 @@ __global__ void __launch_bounds__(256) k_qknorm_rope_append(
 cudaError_t launch_qknorm_rope_append(const LaunchCtx& c, int T, int layer, const float* qkv,
                                       const bf16* q_norm, const bf16* k_norm, float eps,
                                       const float* rope_cos, const float* rope_sin, int n_heads,
-                                      int n_kv, TokView tv, KVView kv, bf16* q_out, bf16* kv_new,
+                                      int n_kv, TokView tv, KVView kv, f16* q_out, f16* kv_new,
                                       int32_t* dbg_pos, int32_t* dbg_slot, int* status) {
     const int warps = T * (n_heads + 2 * n_kv);
     return launch_k(c, k_qknorm_rope_append, dim3((warps + 7) / 8), dim3(256), 0, T, layer, qkv,
@@ -500,7 +498,8 @@ cudaError_t launch_qknorm_rope_append(const LaunchCtx& c, int T, int layer, cons
 
 // =======================================================================================
 // Synthetic KV fill with the counter-based SplitMix64 generator (Steele, Lea, Flood 2014):
-// element idx -> z = mix(seed + (idx + 1) * golden); b = (int8)(z >> 56); K = b/64, V = b/128.
+// element idx -> z = mix(seed + (idx + 1) * golden); b = (int8)(z >> 56); K = b/64, V = b/128
+// (exact in fp16).
 // =======================================================================================
 __device__ __forceinline__ unsigned long long splitmix64_at(unsigned long long seed,
                                                             unsigned long long idx) {
@@ -517,7 +516,7 @@ __global__ void k_kv_fill(KVView kv, int n_layers, int n_kv, int seq, int n_toke
     const int layer = blockIdx.y >> 1, which = blockIdx.y & 1;
     const int page = kv.page_table[(size_t)seq * kv.max_pages_per_seq + pi];
     if (page < 0) return;
-    bf16* pool = (which == 0 ? kv.k : kv.v) + (size_t)layer * kv.layer_stride;
+    f16* pool = (which == 0 ? kv.k : kv.v) + (size_t)layer * kv.layer_stride;
     const float scale = which == 0 ? (1.0f / 64.0f) : (1.0f / 128.0f);
     for (int e = threadIdx.x; e < n_kv * 16 * 128; e += blockDim.x) {
         const int g = e / (16 * 128), o = (e / 128) % 16, d = e % 128;
@@ -529,7 +528,7 @@ __global__ void k_kv_fill(KVView kv, int n_layers, int n_kv, int seq, int n_toke
             const int8_t b = (int8_t)(splitmix64_at(seed, idx) >> 56);
             val = (float)b * scale;
         }
-        pool[(((size_t)page * n_kv + g) * 16 + o) * 128 + d] = __float2bfloat16_rn(val);
+        pool[(((size_t)page * n_kv + g) * 16 + o) * 128 + d] = __float2half_rn(val);
     }
     (void)n_layers;
 }
@@ -540,4 +539,45 @@ cudaError_t launch_kv_fill(const LaunchCtx& c, KVView kv, int n_layers, int n_kv
     if (pages == 0) return cudaSuccess;
     return launch_k(c, k_kv_fill, dim3(pages, n_layers * 2), dim3(256), 0, kv, n_layers, n_kv, seq,
                     n_tokens, seed);
+}
+
+// =======================================================================================
+// Weight conversion bf16 -> fp16 for the packed copies (done once at load). fp16 carries
+// every bf16 value of magnitude in [2^-14, 65504] exactly; smaller magnitudes round to the
+// fp16 subnormal grid (absolute error <= 2^-25). Values beyond the fp16 range set
+// QW_DEV_RANGE in the status word.
+// =======================================================================================
+__global__ void k_convert_bf16_f16(const bf16* __restrict__ src, f16* __restrict__ dst, size_t n, int* status) {
+    const size_t i0 = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 8;
+    const size_t stride = (size_t)gridDim.x * blockDim.x * 8;
+    for (size_t i = i0; i < n; i += stride) {
+        if (i + 8 <= n) {
+            const uint4 w = *reinterpret_cast<const uint4*>(src + i);
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+            uint32_t o[4];
+            bool bad = false;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float a = bf_lo(ws[j]), b = bf_hi(ws[j]);
+                bad |= fabsf(a) > 65504.f || fabsf(b) > 65504.f;
+                o[j] = pack_h2(a, b);
+            }
+            *reinterpret_cast<uint4*>(dst + i) = make_uint4(o[0], o[1], o[2], o[3]);
+            if (bad) atomicOr(status, QW_DEV_RANGE);
+        } else {
+            for (size_t j = i; j < n; ++j) {
+                const float a = __bfloat162float(src[j]);
+                if (fabsf(a) > 65504.f) atomicOr(status, QW_DEV_RANGE);
+                dst[j] = __float2half_rn(a);
+            }
+        }
+    }
+}
+
+cudaError_t launch_convert_bf16_f16(const LaunchCtx& c, const bf16* src, f16* dst, size_t n, int* status) {
+    if (n == 0) return cudaSuccess;
+    size_t blocks = (n / 8 + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    if (blocks < 1) blocks = 1;
+    return launch_k(c, k_convert_bf16_f16, dim3((unsigned)blocks), dim3(256), 0, src, dst, n, status);
 }

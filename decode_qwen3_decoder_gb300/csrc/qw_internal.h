@@ -3,18 +3,21 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "../../include/qw.h"
 
 typedef __nv_bfloat16 bf16;
+typedef __half f16;
 
 // Device status bits (ORed into the workspace status word; read by qw_sync_status).
 enum : int {
     QW_DEV_BAD_TOKEN = 1,
     QW_DEV_TIMEOUT = 2,
     QW_DEV_BAD_POS = 4,
+    QW_DEV_RANGE = 8,
 };
 
 // Per-call batch description, passed by value to the step-begin kernel.
@@ -29,8 +32,8 @@ struct StepDesc {
 struct KVView {
     int* len;            // [max_seqs] current length of each sequence
     int* page_table;     // [max_seqs][max_pages_per_seq], -1 = no page
-    bf16* k;             // [n_layers][n_pages][n_kv][page][head_dim]
-    bf16* v;
+    f16* k;              // [n_layers][n_pages][n_kv][page][head_dim]
+    f16* v;
     int max_pages_per_seq;
     int n_pages;
     long long layer_stride; // elements per layer of the K (or V) pool
@@ -50,6 +53,16 @@ struct TokView {
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 __device__ __forceinline__ float bf2f(bf16 v) { return __bfloat162float(v); }
+__device__ __forceinline__ float h_lo(uint32_t w) {
+    return __half2float(__ushort_as_half((unsigned short)(w & 0xFFFFu)));
+}
+__device__ __forceinline__ float h_hi(uint32_t w) {
+    return __half2float(__ushort_as_half((unsigned short)(w >> 16)));
+}
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
 __device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
@@ -101,38 +114,37 @@ cudaError_t launch_step_begin(const LaunchCtx& c, const StepDesc& sd, const int3
                               const bf16* embed, int vocab, int hidden, float* x, TokView tv,
                               KVView kv, int* status);
 cudaError_t launch_rmsnorm(const LaunchCtx& c, const float* x, const int* rows, int n_rows,
-                           int hidden, const bf16* w, float eps, bf16* h);
+                           int hidden, const bf16* w, float eps, f16* h);
+cudaError_t launch_convert_bf16_f16(const LaunchCtx& c, const bf16* src, f16* dst, size_t n, int* status);
 // GEMV family (T <= 8 token rows).
 cudaError_t launch_gemv_qkv(const LaunchCtx& c, int T, const float* x, const bf16* norm_w, float eps,
-                            const bf16* W, int n_out, int K, float* out);
+                            const f16* W, int n_out, int K, float* out);
 cudaError_t launch_gemv_gateup(const LaunchCtx& c, int T, const float* x, const bf16* norm_w,
-                               float eps, const bf16* Wg, const bf16* Wu, int inter, int K, bf16* act);
-cudaError_t launch_gemv_resid(const LaunchCtx& c, int T, const bf16* act, const bf16* W, int n_out,
+                               float eps, const f16* Wg, const f16* Wu, int inter, int K, f16* act);
+cudaError_t launch_gemv_resid(const LaunchCtx& c, int T, const f16* act, const f16* W, int n_out,
                               int K, float* x);
 cudaError_t launch_gemv_lmhead(const LaunchCtx& c, int B, const float* x, const int* rows,
-                               const bf16* norm_w, float eps, const bf16* E, int vocab, int K,
+                               const bf16* norm_w, float eps, const f16* E, int vocab, int K,
                                float* logits, unsigned long long* best);
 cudaError_t launch_finalize(const LaunchCtx& c, const StepDesc& sd, unsigned long long* best,
                             int32_t* next_ids, KVView kv);
 cudaError_t launch_qknorm_rope_append(const LaunchCtx& c, int T, int layer, const float* qkv,
                                       const bf16* q_norm, const bf16* k_norm, float eps,
                                       const float* rope_cos, const float* rope_sin, int n_heads,
-                                      int n_kv, TokView tv, KVView kv, bf16* q_out, bf16* kv_new,
+                                      int n_kv, TokView tv, KVView kv, f16* q_out, f16* kv_new,
                                       int32_t* dbg_pos, int32_t* dbg_slot, int* status);
-cudaError_t launch_attn_paged(const LaunchCtx& c, int T, int layer, const bf16* q, int n_heads,
+cudaError_t launch_attn_paged(const LaunchCtx& c, int T, int layer, const f16* q, int n_heads,
                               int n_kv, TokView tv, KVView kv, int chunk, int n_splits,
-                              float* part_o, float* part_ml, int* counters, bf16* out);
-cudaError_t launch_attn_prefill(const LaunchCtx& c, const StepDesc& sd, int max_len, const bf16* q,
-                                const bf16* kv_new, int n_heads, int n_kv, bf16* out);
+                              float* part_o, float* part_ml, int* counters, f16* out);
 cudaError_t launch_kv_fill(const LaunchCtx& c, KVView kv, int n_layers, int n_kv, int seq,
                            int n_tokens, unsigned long long seed);
 
 // tcgen05 GEMM (T > 8 token rows). Epilogue kinds:
 enum GemmEpi : int { EPI_STORE_F32 = 0, EPI_RESID_F32 = 1, EPI_SILU_MUL = 2, EPI_ARGMAX = 3 };
 struct GemmArgs {
-    const CUtensorMap* tmA;   // weights [rows_total, K] bf16, box 128 x 64
+    const CUtensorMap* tmA;   // weights [rows_total, K] fp16, box 128 x 64
     const CUtensorMap* tmA2;  // second weight (up) for EPI_SILU_MUL, else same as tmA
-    const CUtensorMap* tmB;   // activations [T_cap, K] bf16, box BN x 64
+    const CUtensorMap* tmB;   // activations [T_cap, K] fp16, box BN x 64
     int a_row0;               // first weight row of this matrix (layer offset)
     int a2_row0;
     int M;                    // output features (multiple of 128)
@@ -140,7 +152,7 @@ struct GemmArgs {
     int T;                    // token rows (columns of the transposed product)
     float* out_f32;           // EPI_STORE_F32: out[t][m]; EPI_RESID_F32: x[t][m] +=
     int ld_out;
-    bf16* out_bf16;           // EPI_SILU_MUL: act[t][m]
+    f16* out_h;               // EPI_SILU_MUL: act[t][m]
     float* logits;            // EPI_ARGMAX: optional logits[t][m]
     unsigned long long* best; // EPI_ARGMAX: per-token packed argmax keys
     int* status;

@@ -83,7 +83,7 @@ static bool config_ok(const qw_config* c, std::string* why) {
 }
 
 struct WsLayout {
-    size_t wqkv, wo, wg, wu, wd, norms, fnorm, rcos, rsin;
+    size_t wqkv, wo, wg, wu, wd, embed16, norms, fnorm, rcos, rsin;
     size_t x, h, qkv, q, kvnew, attn, act, part_o, part_ml, counters;
     size_t tok_seq, tok_pos, last, best, status, gen_tok, gen_cur, gen_out;
     size_t total;
@@ -107,6 +107,7 @@ static WsLayout layout_for(const qw_config& c) {
     L.wg = take(NL * I * D * 2);
     L.wu = take(NL * I * D * 2);
     L.wd = take(NL * D * I * 2);
+    L.embed16 = take((size_t)c.vocab * D * 2);
     L.norms = take(NL * (2 * D + 2 * c.head_dim) * 2);
     L.fnorm = take(D * 2);
     L.rcos = take((size_t)c.max_context * 64 * 4);
@@ -148,10 +149,11 @@ struct qw_model {
     WsLayout L;
     char* ws;
     int qkv_rows;
-    bf16 *wqkv, *wo, *wg, *wu, *wd, *norms, *fnorm;
+    f16 *wqkv, *wo, *wg, *wu, *wd, *embed16;  // fp16 copies of the bf16 weights
+    bf16 *norms, *fnorm;
     const bf16* embed;
     float *rcos, *rsin, *x, *qkv, *part_o, *part_ml;
-    bf16 *h, *q, *kvnew, *attn, *act;
+    f16 *h, *q, *kvnew, *attn, *act;
     int *counters, *tok_seq, *tok_pos, *last, *status;
     unsigned long long* best;
     int32_t *gen_tok, *gen_cur, *gen_out;
@@ -178,8 +180,8 @@ struct qw_kv {
     int max_seqs, n_pages, maxp;
     int* d_len;
     int* d_pt;
-    bf16* k;
-    bf16* v;
+    f16* k;
+    f16* v;
     long long layer_stride;
     std::vector<int> len;
     std::vector<std::vector<int>> pt;
@@ -235,23 +237,24 @@ extern "C" qw_status qw_init_weights(const qw_config* cfg, const qw_weight_ptrs*
     const size_t QD = (size_t)cfg->n_heads * d, KD = (size_t)cfg->n_kv_heads * d;
     m->qkv_rows = (int)(QD + 2 * KD);
     char* b = m->ws;
-    m->wqkv = (bf16*)(b + L.wqkv);
-    m->wo = (bf16*)(b + L.wo);
-    m->wg = (bf16*)(b + L.wg);
-    m->wu = (bf16*)(b + L.wu);
-    m->wd = (bf16*)(b + L.wd);
+    m->wqkv = (f16*)(b + L.wqkv);
+    m->wo = (f16*)(b + L.wo);
+    m->wg = (f16*)(b + L.wg);
+    m->wu = (f16*)(b + L.wu);
+    m->wd = (f16*)(b + L.wd);
+    m->embed16 = (f16*)(b + L.embed16);
     m->norms = (bf16*)(b + L.norms);
     m->fnorm = (bf16*)(b + L.fnorm);
     m->embed = (const bf16*)w->embed_tokens;
     m->rcos = (float*)(b + L.rcos);
     m->rsin = (float*)(b + L.rsin);
     m->x = (float*)(b + L.x);
-    m->h = (bf16*)(b + L.h);
+    m->h = (f16*)(b + L.h);
     m->qkv = (float*)(b + L.qkv);
-    m->q = (bf16*)(b + L.q);
-    m->kvnew = (bf16*)(b + L.kvnew);
-    m->attn = (bf16*)(b + L.attn);
-    m->act = (bf16*)(b + L.act);
+    m->q = (f16*)(b + L.q);
+    m->kvnew = (f16*)(b + L.kvnew);
+    m->attn = (f16*)(b + L.attn);
+    m->act = (f16*)(b + L.act);
     m->part_o = (float*)(b + L.part_o);
     m->part_ml = (float*)(b + L.part_ml);
     m->counters = (int*)(b + L.counters);
@@ -278,19 +281,29 @@ extern "C" qw_status qw_init_weights(const qw_config* cfg, const qw_weight_ptrs*
     auto cp = [&](void* dst, const void* src, size_t bytes) {
         return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, st);
     };
-    // Pack: per layer q|k|v rows concatenated (one [qkv_rows, hidden] matrix), the other
-    // matrices copied as they are; norms as [in D][post D][q_norm d][k_norm d].
+    if (cudaMemsetAsync(m->status, 0, 4, st) != cudaSuccess) {
+        fail(QW_ERR_CUDA, "status clear failed");
+        return fail_free(QW_ERR_CUDA);
+    }
+    // Pack: the projection matrices become fp16 (the tensor-core operand type; exact for
+    // every bf16 magnitude in [2^-14, 65504]); per layer q|k|v rows are concatenated into one
+    // [qkv_rows, hidden] matrix. Norm weights stay bf16, copied as
+    // [input D][post-attention D][q_norm d][k_norm d].
+    LaunchCtx pc = {st, false, nullptr};
+    auto cv = [&](f16* dst, const void* src, size_t n) {
+        return launch_convert_bf16_f16(pc, (const bf16*)src, dst, n, m->status);
+    };
     for (int l = 0; l < cfg->n_layers; ++l) {
         const qw_layer_ptrs& lp = w->layers[l];
-        bf16* q0 = m->wqkv + (size_t)l * m->qkv_rows * D;
+        f16* q0 = m->wqkv + (size_t)l * m->qkv_rows * D;
         cudaError_t e = cudaSuccess;
-        if (e == cudaSuccess) e = cp(q0, lp.q_proj, QD * D * 2);
-        if (e == cudaSuccess) e = cp(q0 + QD * D, lp.k_proj, KD * D * 2);
-        if (e == cudaSuccess) e = cp(q0 + (QD + KD) * D, lp.v_proj, KD * D * 2);
-        if (e == cudaSuccess) e = cp(m->wo + (size_t)l * D * QD, lp.o_proj, D * QD * 2);
-        if (e == cudaSuccess) e = cp(m->wg + (size_t)l * I * D, lp.gate_proj, I * D * 2);
-        if (e == cudaSuccess) e = cp(m->wu + (size_t)l * I * D, lp.up_proj, I * D * 2);
-        if (e == cudaSuccess) e = cp(m->wd + (size_t)l * D * I, lp.down_proj, D * I * 2);
+        if (e == cudaSuccess) e = cv(q0, lp.q_proj, QD * D);
+        if (e == cudaSuccess) e = cv(q0 + QD * D, lp.k_proj, KD * D);
+        if (e == cudaSuccess) e = cv(q0 + (QD + KD) * D, lp.v_proj, KD * D);
+        if (e == cudaSuccess) e = cv(m->wo + (size_t)l * D * QD, lp.o_proj, D * QD);
+        if (e == cudaSuccess) e = cv(m->wg + (size_t)l * I * D, lp.gate_proj, I * D);
+        if (e == cudaSuccess) e = cv(m->wu + (size_t)l * I * D, lp.up_proj, I * D);
+        if (e == cudaSuccess) e = cv(m->wd + (size_t)l * D * I, lp.down_proj, D * I);
         bf16* nb = m->norms + (size_t)l * (2 * D + 2 * d);
         if (e == cudaSuccess) e = cp(nb, lp.input_layernorm, D * 2);
         if (e == cudaSuccess) e = cp(nb + D, lp.post_attention_layernorm, D * 2);
@@ -301,8 +314,9 @@ extern "C" qw_status qw_init_weights(const qw_config* cfg, const qw_weight_ptrs*
             return fail_free(QW_ERR_CUDA);
         }
     }
-    if (cp(m->fnorm, w->norm, D * 2) != cudaSuccess) {
-        fail(QW_ERR_CUDA, "final norm copy failed");
+    if (cp(m->fnorm, w->norm, D * 2) != cudaSuccess ||
+        cv(m->embed16, w->embed_tokens, (size_t)cfg->vocab * D) != cudaSuccess) {
+        fail(QW_ERR_CUDA, "final norm / embedding copy failed");
         return fail_free(QW_ERR_CUDA);
     }
     // RoPE table (Paso 4): angle = pos * theta^(-i/64), evaluated in fp64, stored as fp32.
@@ -329,10 +343,21 @@ extern "C" qw_status qw_init_weights(const qw_config* cfg, const qw_weight_ptrs*
         }
     }
     if (cudaMemsetAsync(m->counters, 0, (size_t)L.part_T * cfg->n_kv_heads * 4, st) != cudaSuccess ||
-        cudaMemsetAsync(m->best, 0, (size_t)cfg->max_batch * 8, st) != cudaSuccess ||
-        cudaMemsetAsync(m->status, 0, 4, st) != cudaSuccess) {
+        cudaMemsetAsync(m->best, 0, (size_t)cfg->max_batch * 8, st) != cudaSuccess) {
         fail(QW_ERR_CUDA, "workspace clear failed");
         return fail_free(QW_ERR_CUDA);
+    }
+    {
+        int word = 0;
+        if (cudaStreamSynchronize(st) != cudaSuccess ||
+            cudaMemcpy(&word, m->status, 4, cudaMemcpyDeviceToHost) != cudaSuccess) {
+            fail(QW_ERR_CUDA, "weight conversion failed");
+            return fail_free(QW_ERR_CUDA);
+        }
+        if (word & QW_DEV_RANGE) {
+            fail(QW_ERR_INVALID_ARG, "a weight is outside the fp16 range (|w| > 65504)");
+            return fail_free(QW_ERR_INVALID_ARG);
+        }
     }
     // Tensor maps for the tcgen05 GEMMs: weights as [rows, K] (box 128 x 64) and the
     // activation operands as [rows, K] (box up to 256 x 64).
@@ -343,7 +368,7 @@ extern "C" qw_status qw_init_weights(const qw_config* cfg, const qw_weight_ptrs*
     ok = ok && gemm_tc_encode_map(&m->tm_wg, m->wg, NL * I, D, 128);
     ok = ok && gemm_tc_encode_map(&m->tm_wu, m->wu, NL * I, D, 128);
     ok = ok && gemm_tc_encode_map(&m->tm_wd, m->wd, NL * D, I, 128);
-    ok = ok && gemm_tc_encode_map(&m->tm_embed, m->embed, cfg->vocab, D, 128);
+    ok = ok && gemm_tc_encode_map(&m->tm_embed, m->embed16, cfg->vocab, D, 128);
     ok = ok && gemm_tc_encode_map(m->tm_h, m->h, TT, D, 0);
     ok = ok && gemm_tc_encode_map(m->tm_attn, m->attn, cfg->max_tokens, QD, 0);
     ok = ok && gemm_tc_encode_map(m->tm_act, m->act, cfg->max_tokens, I, 0);
@@ -450,7 +475,7 @@ extern "C" qw_status qw_kv_alloc(qw_model* m, void* dev_pool, size_t pool_bytes,
     kv->d_len = (int*)kv->pool;
     kv->d_pt = (int*)(kv->pool + align_up((size_t)max_seqs * 4, 256));
     kv->layer_stride = (long long)n_pages * m->cfg.n_kv_heads * 16 * m->cfg.head_dim;
-    kv->k = (bf16*)(kv->pool + meta);
+    kv->k = (f16*)(kv->pool + meta);
     kv->v = kv->k + (size_t)m->cfg.n_layers * kv->layer_stride;
     kv->len.assign(max_seqs, 0);
     kv->pt.assign(max_seqs, std::vector<int>());
@@ -641,7 +666,7 @@ static qw_status run_step(qw_model* m, qw_kv* kv, const StepDesc& sd, bool prefi
             GemmArgs g = {};
             g.tmA = &m->tm_wg; g.tmA2 = &m->tm_wu; g.tmB = m->tm_h;
             g.a_row0 = l * I; g.a2_row0 = l * I; g.M = I; g.K = D; g.T = T;
-            g.out_bf16 = m->act; g.ld_out = I; g.status = m->status;
+            g.out_h = m->act; g.ld_out = I; g.status = m->status;
             {
                 PROF(QW_PROF_GATEUP);
                 CUDA_TRY(launch_gemm_tc(lc, EPI_SILU_MUL, g));
@@ -660,7 +685,7 @@ static qw_status run_step(qw_model* m, qw_kv* kv, const StepDesc& sd, bool prefi
     // --- final norm + tied LM head + greedy argmax (Paso 8) ---
     if (B <= kSmallT) {
         PROF(QW_PROF_LMHEAD);
-        CUDA_TRY(launch_gemv_lmhead(lc, B, m->x, m->last, m->fnorm, c.rms_eps, m->embed, c.vocab, D, logits,
+        CUDA_TRY(launch_gemv_lmhead(lc, B, m->x, m->last, m->fnorm, c.rms_eps, m->embed16, c.vocab, D, logits,
                                     m->best));
     } else {
         {
@@ -845,5 +870,6 @@ extern "C" qw_status qw_sync_status(qw_model* m, void* stream_) {
     if (word & QW_DEV_BAD_TOKEN) return fail(QW_ERR_BAD_TOKEN, "a token id was outside [0, vocab)");
     if (word & QW_DEV_BAD_POS) return fail(QW_ERR_BAD_POS, "a position had no reserved page");
     if (word & QW_DEV_TIMEOUT) return fail(QW_ERR_TIMEOUT, "a bounded wait in a kernel timed out");
+    if (word & QW_DEV_RANGE) return fail(QW_ERR_INVALID_ARG, "a value was outside the fp16 range");
     return QW_OK;
 }

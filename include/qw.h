@@ -21,7 +21,12 @@
  *  - Errors found on the device (a token id out of range, a position without a reserved
  *    page, a wait that timed out) set bits in a device status word; the affected rows are
  *    written as zeros and nothing traps. qw_sync_status() reads and clears that word.
- *  - Weights are bf16 in the HF [out_features, in_features] row-major layout (x @ W^T).
+ *  - Weights are given as bf16 in the HF [out_features, in_features] row-major layout
+ *    (x @ W^T). The projection matrices are packed as fp16 copies, the operand type of the
+ *    tensor cores here: fp16 holds every bf16 value of magnitude in [2^-14, 65504] exactly
+ *    and rounds smaller ones to its subnormal grid (error <= 2^-25). Activations that feed
+ *    a matrix product and the KV cache are fp16; the residual stream, accumulators,
+ *    norms, softmax and logits are fp32.
  */
 #ifndef QW_H
 #define QW_H
@@ -92,22 +97,24 @@ typedef struct {
 typedef struct qw_model qw_model;
 typedef struct qw_kv qw_kv;
 
-/* Bytes of device workspace qw_init_weights needs for `cfg` (packed weights, RoPE table,
- * activations for max_tokens, split-KV partials, status word). 0 if cfg is invalid. */
+/* Bytes of device workspace qw_init_weights needs for `cfg` (fp16 packed weights and an
+ * fp16 copy of the embedding for the LM head, RoPE table, activations for max_tokens,
+ * split-KV partials, status word). 0 if cfg is invalid. */
 size_t qw_model_workspace_bytes(const qw_config* cfg);
 
-/* Validate cfg, pack the per-layer weights into `dev_workspace` (bit-identical copies:
- * q|k|v rows concatenated, the rest copied as is), build the fp32 RoPE cos/sin table (host
- * fp64, Paso 4) and carve the activation buffers. Copies are enqueued on `stream`; the
- * source layer tensors may be freed once the stream has passed them. embed_tokens is NOT
- * copied and must outlive the model. ws_bytes >= qw_model_workspace_bytes(cfg), workspace
- * 256-byte aligned. On success *out owns host state only. */
+/* Validate cfg, pack the weights into `dev_workspace` (fp16 copies of the matrices with
+ * q|k|v rows concatenated per layer, norm weights copied as bf16), build the fp32 RoPE
+ * cos/sin table (host fp64, Paso 4) and carve the activation buffers. Synchronises
+ * `stream`; the source tensors may be freed afterwards except embed_tokens, which the
+ * embedding gather keeps reading and must outlive the model. A weight beyond the fp16 range
+ * gives QW_ERR_INVALID_ARG. ws_bytes >= qw_model_workspace_bytes(cfg), workspace 256-byte
+ * aligned. On success *out owns host state only. */
 qw_status qw_init_weights(const qw_config* cfg, const qw_weight_ptrs* w, void* dev_workspace,
                           size_t ws_bytes, void* stream, qw_model** out);
 
 /* Bytes of device pool for a paged KV cache of `n_pages` pages of page_size tokens for
  * `max_seqs` sequences: per-sequence lengths and page tables, then K and V pools laid out
- * [n_layers][n_pages][n_kv_heads][page_size][head_dim] bf16. */
+ * [n_layers][n_pages][n_kv_heads][page_size][head_dim] fp16. */
 size_t qw_kv_pool_bytes(const qw_model* m, int n_pages, int max_seqs);
 
 /* Bind a caller-owned pool (256-byte aligned) as the KV cache (Paso 5, "KV cache"). The page
@@ -177,14 +184,14 @@ qw_status qw_debug_set(qw_model* m, float* dev_hidden, int32_t* dev_positions, i
 int qw_kv_page_table(const qw_kv* kv, int seq_id, int32_t* host_out, int max_pages);
 
 /* Device addresses of the K and V pools ([n_layers][n_pages][n_kv_heads][page][head_dim]
- * bf16) and the page count. */
+ * fp16) and the page count. */
 qw_status qw_kv_pool_ptrs(const qw_kv* kv, void** dev_k, void** dev_v, int* n_pages);
 
 /* Fill positions [0, n_tokens) of sequence seq_id (reserved, empty) with synthetic K/V from
  * the counter-based SplitMix64 generator: element index
  *   idx = (((layer*2 + which) << 22 | pos) * n_kv_heads + head) * head_dim + dim,
  *   z = splitmix64(seed + (idx + 1) * 0x9E3779B97F4A7C15), b = (int8)(z >> 56),
- *   K = b / 64, V = b / 128 (exact in bf16),
+ *   K = b / 64, V = b / 128 (exact in fp16),
  * and set the sequence's length to n_tokens. Stands in for a long prefill. */
 qw_status qw_kv_fill_synthetic(qw_kv* kv, int seq_id, int n_tokens, uint64_t seed, void* stream);
 

@@ -16,7 +16,7 @@ Recipes (all seeded, all reproducible):
 * Injected KV-cache contents: the counter-based SplitMix64 generator (Steele, Lea and Flood,
   "Fast splittable pseudorandom number generators", OOPSLA 2014) hashed over the element
   index. The top byte of each 64-bit output, read as a signed int8 ``b``, gives
-  ``K = b / 64`` and ``V = b / 128``. Both are exact in bf16, so a device-side fill that
+  ``K = b / 64`` and ``V = b / 128``. Both are exact in fp16 (and bf16), so a device-side fill that
   implements the same published generator produces bit-identical values.
 """
 

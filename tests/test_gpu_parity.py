@@ -125,7 +125,7 @@ def test_ragged_small_batch_slots_and_values(one_block):
     import torch
     off = kptr - eng.pool.data_ptr()
     nk = n_pages * s.n_kv_heads * 16 * s.head_dim
-    k0 = eng.pool[off:off + 2 * nk].view(torch.bfloat16).float().cpu().numpy()
+    k0 = eng.pool[off:off + 2 * nk].view(torch.float16).float().cpu().numpy()
     k0 = k0.reshape(n_pages, s.n_kv_heads, 16, s.head_dim)
     row = 0
     for b, (sq, p) in enumerate(zip(seqs, prompts)):
