@@ -127,6 +127,11 @@ __global__ void __launch_bounds__(AW * 32) k_attn_paged(AttnP p) {
         for (int i = 0; i < 8; ++i) kr[i] = ldg_nc(Kl + off + (size_t)(2 * i + half) * 128);
 #pragma unroll
         for (int i = 0; i < 8; ++i) vr[i] = ldg_nc(Vl + off + (size_t)(2 * i + half) * 128);
+        // slots past the last valid key hold whatever the pool held before: give them zero
+        // values as well as zero weight (0 * NaN would poison the sum)
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (2 * i + half >= nvalid) vr[i] = make_uint4(0u, 0u, 0u, 0u);
         float s0[8], s1[8];
         float pm0 = -INFINITY, pm1 = -INFINITY;
 #pragma unroll
