@@ -139,6 +139,18 @@ cudaError_t launch_attn_paged(const LaunchCtx& c, int T, int layer, const f16* q
 cudaError_t launch_kv_fill(const LaunchCtx& c, KVView kv, int n_layers, int n_kv, int seq,
                            int n_tokens, unsigned long long seed);
 
+// What the LM head needs from a model (read-only view for entry points in other files).
+struct LmHeadView {
+    const bf16* final_norm;
+    const f16* embed16;
+    float eps;
+    int vocab;
+    int hidden;
+};
+bool qw_model_lmhead_view(const qw_model* m, LmHeadView* v);
+// Records `fmt` as the calling thread's last error and returns s.
+qw_status qw_fail(qw_status s, const char* fmt, ...);
+
 // tcgen05 GEMM (T > 8 token rows). Epilogue kinds:
 enum GemmEpi : int { EPI_STORE_F32 = 0, EPI_RESID_F32 = 1, EPI_SILU_MUL = 2, EPI_ARGMAX = 3 };
 struct GemmArgs {

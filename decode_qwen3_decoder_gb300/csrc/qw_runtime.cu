@@ -406,6 +406,26 @@ extern "C" qw_status qw_debug_set(qw_model* m, float* dev_hidden, int32_t* dev_p
 
 extern "C" int qw_last_launch_count(const qw_model* m) { return m ? m->last_launches : 0; }
 
+bool qw_model_lmhead_view(const qw_model* m, LmHeadView* v) {
+    if (!m || !v) return false;
+    v->final_norm = m->fnorm;
+    v->embed16 = m->embed16;
+    v->eps = m->cfg.rms_eps;
+    v->vocab = m->cfg.vocab;
+    v->hidden = m->cfg.hidden;
+    return true;
+}
+
+qw_status qw_fail(qw_status s, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return s;
+}
+
 extern "C" qw_status qw_profile_set(qw_model* m, int kind, void* const* events, int n_events) {
     if (!m) return fail(QW_ERR_INVALID_ARG, "model is NULL");
     if (kind < QW_PROF_OFF || kind > QW_PROF_RMSNORM) return fail(QW_ERR_INVALID_ARG, "unknown kernel kind %d", kind);

@@ -77,6 +77,7 @@ SIGNATURES = {
     "qw_kv_fill_synthetic": (_I, [_VP, _I, _I, ctypes.c_uint64, _VP]),
     "qw_last_launch_count": (_I, [_VP]),
     "qw_profile_set": (_I, [_VP, _I, _P(_VP), _I]),
+    "qw_lm_head_argmax_noalloc": (_I, [_VP, _I, _VP, _VP, _VP, _VP]),
 }
 
 
@@ -219,6 +220,13 @@ def qw_kv_fill_synthetic(kv: int, seq_id: int, n_tokens: int, seed: int, stream=
 
 def qw_last_launch_count(model: int) -> int:
     return load().qw_last_launch_count(model)
+
+
+def qw_lm_head_argmax_noalloc(model: int, B: int, x_ptr: int, logits_ptr: int, next_ptr: int,
+                              stream=None) -> None:
+    """LM head + argmax over B residual rows with no device allocation (scratch is a static
+    device array of QW_NOALLOC_MAX_ROWS keys); see include/qw.h."""
+    _check(load().qw_lm_head_argmax_noalloc(model, B, x_ptr, logits_ptr or None, next_ptr, _stream(stream)))
 
 
 def qw_profile_set(model: int, kind: int, events, n_events: int) -> None:

@@ -219,6 +219,28 @@ enum {
  * graph captured while they are set; kind QW_PROF_OFF (or events NULL) turns it off. */
 qw_status qw_profile_set(qw_model* m, int kind, void* const* events, int n_events);
 
+/* ---- For callers that cannot allocate device memory ---------------------------------- */
+
+/* The page has no counterpart to this entry point; it serves callers that must not call
+ * cudaMalloc at the point of use: code running under another framework's fixed device
+ * budget, serving loops that never touch the allocator after start-up, or code that
+ * prepares work while a stream is being captured.
+ *
+ * Final RMSNorm + tied LM head + greedy argmax (the same kernel as the small-batch path of
+ * qw_prefill / qw_decode_step) over B caller-provided fp32 residual rows dev_x [B, hidden]
+ * (16-byte aligned): writes dev_logits [B, vocab] fp32 (or skips it when NULL) and
+ * dev_next_ids [B] (lowest index on ties), asynchronously on `stream`. It allocates
+ * nothing (no cudaMalloc, cudaFree or allocating library call): its only scratch, B
+ * packed 64-bit argmax keys, is a file-scope device array of QW_NOALLOC_MAX_ROWS entries
+ * that every GPU loading the library holds until exit. B > QW_NOALLOC_MAX_ROWS gives
+ * QW_ERR_INVALID_ARG. The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before any stream
+ * capture. All calls share the array and each clears the keys it uses, so calls whose work
+ * overlaps on the GPU race: issue them on one stream. */
+#define QW_NOALLOC_MAX_ROWS 8
+qw_status qw_lm_head_argmax_noalloc(const qw_model* m, int B, const float* dev_x, float* dev_logits,
+                                    int32_t* dev_next_ids, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
