@@ -8,7 +8,13 @@
 // chunks and the two half-warps take alternate keys. Warps merge through shared memory;
 // splits merge with log-sum-exp weights in the CTA that finishes last (an atomic ticket,
 // no waiting). The query at position p sees keys 0..p of its sequence (the causal rule by
-// position; the new token's own K/V were appended before this kernel runs).
+// position).
+//
+// Two modes. Prefill: the new tokens' K/V were appended by k_qknorm_rope_append and q is
+// read as fp16. Decode (one new token per sequence, FUSED): the CTA itself applies the
+// per-head QK-norm and rotate-half RoPE (Paso 5, Paso 4) to its two query heads and its KV
+// head from the fp32 q|k|v projection row, keeps q in fp32, and the CTA whose split holds
+// the new position appends the new K/V to its page slot before reading it back.
 #include <utility>
 
 #include "qw_internal.h"
@@ -66,7 +72,16 @@ __device__ __forceinline__ float half_warp_sum(float v) {
 }  // namespace
 
 struct AttnP {
-    const f16* q;       // [T][n_heads][128]
+    const f16* q;       // [T][n_heads][128] (prefill mode)
+    const float* qkv;   // [T][(n_heads + 2 n_kv) * 128] fp32 (decode mode)
+    const bf16* q_norm; // [128]
+    const bf16* k_norm; // [128]
+    float eps;
+    const float* rope_cos;  // [max_context][64]
+    const float* rope_sin;
+    int32_t* dbg_pos;
+    int32_t* dbg_slot;
+    int* status;
     int n_heads, n_kv;
     TokView tv;
     KVView kv;
@@ -82,7 +97,9 @@ struct AttnP {
 
 constexpr int AW = 4;  // warps per CTA
 
+template <bool FUSED>
 __global__ void __launch_bounds__(AW * 32) k_attn_paged(AttnP p) {
+    pdl_launch();
     pdl_wait();
     const int t = blockIdx.z, g = blockIdx.y, s = blockIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -93,8 +110,68 @@ __global__ void __launch_bounds__(AW * 32) k_attn_paged(AttnP p) {
     const int k0 = s * p.chunk, k1 = min(k0 + p.chunk, n_keys);
     const int half = lane >> 4, dl = (lane & 15) * 8;
 
+    const int* pt = p.kv.page_table + (size_t)seq * p.kv.max_pages_per_seq;
+    const bool writer = FUSED && (s == n_act - 1);  // this split holds the new position
+    __shared__ float sq[2][128];
+    if (FUSED) {
+        // warp 0, 1: query heads 2g, 2g+1; warp 2: KV head g's key; warp 3: its value
+        const int NH = p.n_heads + 2 * p.n_kv;
+        const int hh = warp < 2 ? 2 * g + warp : (warp == 2 ? p.n_heads + g : p.n_heads + p.n_kv + g);
+        const float4 xv = *reinterpret_cast<const float4*>(p.qkv + ((size_t)t * NH + hh) * 128 + lane * 4);
+        float y[4] = {xv.x, xv.y, xv.z, xv.w};
+        if (warp < 3) {
+            const bf16* nw = warp < 2 ? p.q_norm : p.k_norm;
+            const float ss = warp_sum(y[0] * y[0] + y[1] * y[1] + y[2] * y[2] + y[3] * y[3]);
+            const float r = rsqrtf(ss * (1.0f / 128.0f) + p.eps);
+            const uint2 wb = *reinterpret_cast<const uint2*>(nw + lane * 4);
+            y[0] *= r * bf_lo(wb.x);
+            y[1] *= r * bf_hi(wb.x);
+            y[2] *= r * bf_lo(wb.y);
+            y[3] *= r * bf_hi(wb.y);
+            const int i0 = (lane & 15) * 4;
+            const float4 cs = *reinterpret_cast<const float4*>(p.rope_cos + (size_t)pos * 64 + i0);
+            const float4 sn = *reinterpret_cast<const float4*>(p.rope_sin + (size_t)pos * 64 + i0);
+            const float c[4] = {cs.x, cs.y, cs.z, cs.w}, sv[4] = {sn.x, sn.y, sn.z, sn.w};
+            float o[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float pj = __shfl_xor_sync(0xffffffffu, y[j], 16);
+                o[j] = (lane < 16) ? (y[j] * c[j] - pj * sv[j]) : (pj * sv[j] + y[j] * c[j]);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) y[j] = o[j];
+        }
+        if (warp < 2) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) sq[warp][lane * 4 + j] = y[j];
+        } else if (writer) {
+            const int pi = pos >> 4;
+            const int page = (pi < p.kv.max_pages_per_seq) ? pt[pi] : -1;
+            if (page < 0 || page >= p.kv.n_pages) {
+                if (lane == 0) atomicOr(p.status, QW_DEV_BAD_POS);
+            } else {
+                f16* pool = (warp == 2 ? p.kv.k : p.kv.v) + (size_t)p.layer * p.kv.layer_stride;
+                uint2 packed;
+                packed.x = pack_h2(y[0], y[1]);
+                packed.y = pack_h2(y[2], y[3]);
+                *reinterpret_cast<uint2*>(pool + (((size_t)page * p.n_kv + g) * 16 + (pos & 15)) * 128 + lane * 4) =
+                    packed;
+                if (p.dbg_pos && warp == 2 && g == 0 && lane == 0) {
+                    p.dbg_pos[t] = pos;
+                    p.dbg_slot[t] = page * 16 + (pos & 15);
+                }
+            }
+        }
+        __syncthreads();
+    }
     float q0[8], q1[8];
-    {
+    if (FUSED) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            q0[i] = sq[0][dl + i] * p.scale_log2;
+            q1[i] = sq[1][dl + i] * p.scale_log2;
+        }
+    } else {
         const f16* qp = p.q + ((size_t)t * p.n_heads + 2 * g) * 128 + dl;
         const uint4 a = *reinterpret_cast<const uint4*>(qp);
         const uint4 b = *reinterpret_cast<const uint4*>(qp + 128);
@@ -114,7 +191,6 @@ __global__ void __launch_bounds__(AW * 32) k_attn_paged(AttnP p) {
 
     const f16* Kl = p.kv.k + (size_t)p.layer * p.kv.layer_stride;
     const f16* Vl = p.kv.v + (size_t)p.layer * p.kv.layer_stride;
-    const int* pt = p.kv.page_table + (size_t)seq * p.kv.max_pages_per_seq;
     const int p0 = k0 >> 4, p1 = (k1 + 15) >> 4;
 
     for (int pg = p0 + warp; pg < p1; pg += AW) {
@@ -123,10 +199,18 @@ __global__ void __launch_bounds__(AW * 32) k_attn_paged(AttnP p) {
         const int nvalid = min(16, k1 - pg * 16);
         const size_t off = ((size_t)page * p.n_kv + g) * 16 * 128 + dl;
         uint4 kr[8], vr[8];
+        if (writer && pg == p1 - 1) {
+            // the page this CTA just wrote: coherent loads (not the read-only path)
 #pragma unroll
-        for (int i = 0; i < 8; ++i) kr[i] = ldg_nc(Kl + off + (size_t)(2 * i + half) * 128);
+            for (int i = 0; i < 8; ++i) kr[i] = *reinterpret_cast<const uint4*>(Kl + off + (size_t)(2 * i + half) * 128);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) vr[i] = ldg_nc(Vl + off + (size_t)(2 * i + half) * 128);
+            for (int i = 0; i < 8; ++i) vr[i] = *reinterpret_cast<const uint4*>(Vl + off + (size_t)(2 * i + half) * 128);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) kr[i] = ldg_nc(Kl + off + (size_t)(2 * i + half) * 128);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) vr[i] = ldg_nc(Vl + off + (size_t)(2 * i + half) * 128);
+        }
         // slots past the last valid key hold whatever the pool held before: give them zero
         // values as well as zero weight (0 * NaN would poison the sum)
 #pragma unroll
@@ -217,7 +301,6 @@ __global__ void __launch_bounds__(AW * 32) k_attn_paged(AttnP p) {
     f16* outp = p.out + ((size_t)t * p.n_heads + head) * 128 + d2;
     if (n_act == 1) {
         *reinterpret_cast<uint32_t*>(outp) = pack_h2(O0 / L, O1 / L);
-        pdl_launch();
         return;
     }
     const size_t slot = ((size_t)t * p.n_heads + head) * p.n_splits + s;
@@ -246,13 +329,13 @@ __global__ void __launch_bounds__(AW * 32) k_attn_paged(AttnP p) {
     }
     *reinterpret_cast<uint32_t*>(outp) = pack_h2(A0 / LL, A1 / LL);
     if (threadIdx.x == 0) p.counters[(size_t)t * p.n_kv + g] = 0;
-    pdl_launch();
 }
 
 cudaError_t launch_attn_paged(const LaunchCtx& c, int T, int layer, const f16* q, int n_heads,
                               int n_kv, TokView tv, KVView kv, int chunk, int n_splits,
-                              float* part_o, float* part_ml, int* counters, f16* out) {
-    AttnP p;
+                              float* part_o, float* part_ml, int* counters, f16* out,
+                              const AttnFuse* fuse) {
+    AttnP p = {};
     p.q = q;
     p.n_heads = n_heads;
     p.n_kv = n_kv;
@@ -266,5 +349,17 @@ cudaError_t launch_attn_paged(const LaunchCtx& c, int T, int layer, const f16* q
     p.counters = counters;
     p.out = out;
     p.scale_log2 = 0.08838834764831845f * 1.4426950408889634f;  // 128^-0.5 * log2(e)
-    return launch_k(c, k_attn_paged, dim3(n_splits, n_kv, T), dim3(AW * 32), 0, p);
+    if (fuse) {
+        p.qkv = fuse->qkv;
+        p.q_norm = fuse->q_norm;
+        p.k_norm = fuse->k_norm;
+        p.eps = fuse->eps;
+        p.rope_cos = fuse->rope_cos;
+        p.rope_sin = fuse->rope_sin;
+        p.dbg_pos = fuse->dbg_pos;
+        p.dbg_slot = fuse->dbg_slot;
+        p.status = fuse->status;
+        return launch_k(c, k_attn_paged<true>, dim3(n_splits, n_kv, T), dim3(AW * 32), 0, p);
+    }
+    return launch_k(c, k_attn_paged<false>, dim3(n_splits, n_kv, T), dim3(AW * 32), 0, p);
 }

@@ -62,6 +62,7 @@ __global__ void __launch_bounds__(256) k_step_begin(StepDesc sd, const int32_t* 
                                                     const bf16* __restrict__ embed, int vocab,
                                                     int hidden, float* __restrict__ x, TokView tv,
                                                     KVView kv, int* status) {
+    pdl_launch();
     pdl_wait();
     const int t = blockIdx.x;
     int b = 0;
@@ -83,7 +84,6 @@ __global__ void __launch_bounds__(256) k_step_begin(StepDesc sd, const int32_t* 
         if (t == sd.start[b + 1] - 1) tv.last[b] = t;
         if (bad) atomicOr(status, QW_DEV_BAD_TOKEN);
     }
-    pdl_launch();
 }
 
 cudaError_t launch_step_begin(const LaunchCtx& c, const StepDesc& sd, const int32_t* ids,
@@ -100,6 +100,7 @@ cudaError_t launch_step_begin(const LaunchCtx& c, const StepDesc& sd, const int3
 __global__ void __launch_bounds__(256) k_rmsnorm(const float* __restrict__ x, const int* __restrict__ rows,
                                                  int n_rows, int hidden, const bf16* __restrict__ w,
                                                  float eps, f16* __restrict__ h) {
+    pdl_launch();
     pdl_wait();
     const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
@@ -121,7 +122,6 @@ __global__ void __launch_bounds__(256) k_rmsnorm(const float* __restrict__ x, co
             *reinterpret_cast<uint2*>(hr + k) = o;
         }
     }
-    pdl_launch();
 }
 
 cudaError_t launch_rmsnorm(const LaunchCtx& c, const float* x, const int* rows, int n_rows,
@@ -162,13 +162,46 @@ struct GemvP {
 
 constexpr int GEMV_WARPS = 4;
 
+// Streaming 16-byte load issued in program order (volatile), so the weight fetches of a
+// launch stay ahead of its griddepcontrol.wait.
+__device__ __forceinline__ uint4 ldg_stream_v(const void* ptr) {
+    uint4 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(ptr));
+    return r;
+}
+
+// Programmatic dependent launch: the kernel lets its dependents launch at entry and issues
+// the weight loads of its first row group before griddepcontrol.wait, so the weights (which
+// no earlier kernel writes) stream from HBM while the upstream kernel is still finishing.
+// Everything that reads upstream outputs, or writes anything, comes after the wait.
 template <int TT, int MODE, int KC, int RPW>
 __global__ void __launch_bounds__(GEMV_WARPS * 32) k_gemv(GemvP p) {
     extern __shared__ float4 smem_f4[];
     float* hs = reinterpret_cast<float*>(smem_f4);  // [TT][K] fp32
     constexpr int K = KC * 256;
     constexpr int NW = (MODE == G_GATEUP) ? 2 : 1;
+    constexpr int PC = (KC <= 12) ? KC : 4;  // 16-byte chunks per lane held per pass
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int gw = blockIdx.x * GEMV_WARPS + warp;
+    const int nw = gridDim.x * GEMV_WARPS;
+    pdl_launch();
+
+    uint4 wv[RPW][NW][PC];
+    auto load_pass = [&](int r0, int c0) {
+#pragma unroll
+        for (int rr = 0; rr < RPW; ++rr) {
+            const int row = min(r0 + rr, p.n_out - 1);
+#pragma unroll
+            for (int c = 0; c < PC; ++c) {
+                const size_t off = (size_t)row * K + (c0 + c) * 256 + lane * 8;
+                wv[rr][0][c] = ldg_stream_v(p.W + off);
+                if (NW == 2) wv[rr][NW - 1][c] = ldg_stream_v(p.W2 + off);
+            }
+        }
+    };
+    if (gw * RPW < p.n_out) load_pass(gw * RPW, 0);
     pdl_wait();
 
     // ---- prologue: activations into shared memory --------------------------------------
@@ -216,12 +249,11 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) k_gemv(GemvP p) {
     __syncthreads();
 
     // ---- main loop ---------------------------------------------------------------------
-    const int gw = blockIdx.x * GEMV_WARPS + warp;
-    const int nw = gridDim.x * GEMV_WARPS;
     unsigned long long best[TT];
 #pragma unroll
     for (int t = 0; t < TT; ++t) best[t] = 0ull;
 
+    bool first = true;
     for (int r0 = gw * RPW; r0 < p.n_out; r0 += nw * RPW) {
         float acc[RPW][NW][TT];
 #pragma unroll
@@ -230,22 +262,12 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) k_gemv(GemvP p) {
             for (int n = 0; n < NW; ++n)
 #pragma unroll
                 for (int t = 0; t < TT; ++t) acc[rr][n][t] = 0.f;
-        // passes of 4 chunks (1024 columns): RPW*NW*4 16-byte loads in flight per lane
 #pragma unroll 1
-        for (int c0 = 0; c0 < KC; c0 += 4) {
-            uint4 wv[RPW][NW][4];
+        for (int c0 = 0; c0 < KC; c0 += PC) {
+            if (!first) load_pass(r0, c0);
+            first = false;
 #pragma unroll
-            for (int rr = 0; rr < RPW; ++rr) {
-                const int row = min(r0 + rr, p.n_out - 1);
-#pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    const size_t off = (size_t)row * K + (c0 + c) * 256 + lane * 8;
-                    wv[rr][0][c] = ldg_stream(p.W + off);
-                    if (NW == 2) wv[rr][NW - 1][c] = ldg_stream(p.W2 + off);
-                }
-            }
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
+            for (int c = 0; c < PC; ++c) {
 #pragma unroll
                 for (int t = 0; t < TT; ++t) {
                     const float* a = hs + t * K + (c0 + c) * 256 + lane * 8;
@@ -298,7 +320,6 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) k_gemv(GemvP p) {
             atomicMax(p.best + tid, b);
         }
     }
-    pdl_launch();
 }
 
 namespace {
@@ -331,16 +352,17 @@ cudaError_t gemv_go(const LaunchCtx& c, const GemvP& p, int max_ctas) {
     return launch_k(c, k_gemv<TT, MODE, KC, RPW>, dim3(grid), dim3(GEMV_WARPS * 32), smem, p);
 }
 
-// Rows per warp iteration: 4 rows x 4 chunks = 256 bytes in flight per lane for 1-2 tokens;
-// fewer rows for more tokens to bound the fp32 accumulators and activation registers.
+// Rows per warp: a lane holds whole rows (K <= 3072) of RPW rows in registers; 4 rows of
+// K=1024 (64 registers) for 1-2 tokens, fewer for more tokens or longer rows, so that the
+// narrow long-K matrices (o_proj, down_proj: 1024 rows) still spread over >= 256 CTAs.
 template <int MODE, int KC>
 cudaError_t gemv_kc(const LaunchCtx& c, const GemvP& p, int max_ctas) {
     constexpr int NW = (MODE == G_GATEUP) ? 2 : 1;
-    // the long-K matrices (o_proj, down_proj) have few rows: fewer rows per warp, more CTAs
-    constexpr int R12 = (KC >= 8 ? 2 : 4) / NW;
+    constexpr int R12 = (KC >= 8 ? 1 : 4 / NW);
+    constexpr int R4 = (KC >= 8 ? 1 : 2 / NW);
     if (p.T <= 1) return gemv_go<1, MODE, KC, R12>(c, p, max_ctas);
     if (p.T <= 2) return gemv_go<2, MODE, KC, R12>(c, p, max_ctas);
-    if (p.T <= 4) return gemv_go<4, MODE, KC, 2 / NW>(c, p, max_ctas);
+    if (p.T <= 4) return gemv_go<4, MODE, KC, R4>(c, p, max_ctas);
     return gemv_go<8, MODE, KC, 1>(c, p, max_ctas);
 }
 
@@ -394,6 +416,7 @@ cudaError_t launch_gemv_lmhead(const LaunchCtx& c, int B, const float* x, const 
 // for the next call and advance each sequence's length by its token count (Paso 9).
 // =======================================================================================
 __global__ void k_finalize(StepDesc sd, unsigned long long* best, int32_t* next_ids, KVView kv) {
+    pdl_launch();
     pdl_wait();
     for (int b = threadIdx.x; b < sd.B; b += blockDim.x) {
         const unsigned long long key = best[b];
@@ -401,7 +424,6 @@ __global__ void k_finalize(StepDesc sd, unsigned long long* best, int32_t* next_
         best[b] = 0ull;
         kv.len[sd.seq[b]] += sd.start[b + 1] - sd.start[b];
     }
-    pdl_launch();
 }
 
 cudaError_t launch_finalize(const LaunchCtx& c, const StepDesc& sd, unsigned long long* best,
@@ -426,6 +448,7 @@ __global__ void __launch_bounds__(256) k_qknorm_rope_append(
     const float* __restrict__ rope_sin, int n_heads, int n_kv, TokView tv, KVView kv,
     f16* __restrict__ q_out, f16* __restrict__ kv_new, int32_t* dbg_pos, int32_t* dbg_slot,
     int* status) {
+    pdl_launch();
     pdl_wait();
     const int NH = n_heads + 2 * n_kv;
     const int w = blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -482,7 +505,6 @@ __global__ void __launch_bounds__(256) k_qknorm_rope_append(
             }
         }
     }
-    pdl_launch();
 }
 
 cudaError_t launch_qknorm_rope_append(const LaunchCtx& c, int T, int layer, const float* qkv,

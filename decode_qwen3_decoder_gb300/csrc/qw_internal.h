@@ -133,9 +133,22 @@ cudaError_t launch_qknorm_rope_append(const LaunchCtx& c, int T, int layer, cons
                                       const float* rope_cos, const float* rope_sin, int n_heads,
                                       int n_kv, TokView tv, KVView kv, f16* q_out, f16* kv_new,
                                       int32_t* dbg_pos, int32_t* dbg_slot, int* status);
+// Decode mode of the paged attention: QK-norm + RoPE + KV append done inside the kernel.
+struct AttnFuse {
+    const float* qkv;
+    const bf16* q_norm;
+    const bf16* k_norm;
+    float eps;
+    const float* rope_cos;
+    const float* rope_sin;
+    int32_t* dbg_pos;
+    int32_t* dbg_slot;
+    int* status;
+};
 cudaError_t launch_attn_paged(const LaunchCtx& c, int T, int layer, const f16* q, int n_heads,
                               int n_kv, TokView tv, KVView kv, int chunk, int n_splits,
-                              float* part_o, float* part_ml, int* counters, f16* out);
+                              float* part_o, float* part_ml, int* counters, f16* out,
+                              const AttnFuse* fuse);
 cudaError_t launch_kv_fill(const LaunchCtx& c, KVView kv, int n_layers, int n_kv, int seq,
                            int n_tokens, unsigned long long seed);
 

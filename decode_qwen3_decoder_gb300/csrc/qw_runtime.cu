@@ -268,7 +268,7 @@ extern "C" qw_status qw_init_weights(const qw_config* cfg, const qw_weight_ptrs*
     m->gen_out = (int32_t*)(b + L.gen_out);
     m->use_clock = 0;
     m->last_launches = 0;
-    m->pdl = false;
+    m->pdl = true;
     int dev = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, dev);
@@ -646,17 +646,25 @@ static qw_status run_step(qw_model* m, qw_kv* kv, const StepDesc& sd, bool prefi
             g.out_f32 = m->qkv; g.ld_out = m->qkv_rows; g.status = m->status;
             CUDA_TRY(launch_gemm_tc(lc, EPI_STORE_F32, g));
         }
-        {
-        PROF(QW_PROF_ROPE);
-        CUDA_TRY(launch_qknorm_rope_append(lc, T, l, m->qkv, w_qn, w_kn, c.rms_eps, m->rcos, m->rsin,
-                                           c.n_heads, c.n_kv_heads, tv, kvv, m->q, m->kvnew,
-                                           (dbg && l == 0) ? m->dbg_pos : nullptr,
-                                           (dbg && l == 0) ? m->dbg_slot : nullptr, m->status));
-        }
-        {
-        PROF(QW_PROF_ATTN);
-        CUDA_TRY(launch_attn_paged(lc, T, l, m->q, c.n_heads, c.n_kv_heads, tv, kvv, sp.chunk, sp.n_splits,
-                                   m->part_o, m->part_ml, m->counters, m->attn));
+        if (prefill) {
+            {
+                PROF(QW_PROF_ROPE);
+                CUDA_TRY(launch_qknorm_rope_append(lc, T, l, m->qkv, w_qn, w_kn, c.rms_eps, m->rcos, m->rsin,
+                                                   c.n_heads, c.n_kv_heads, tv, kvv, m->q, m->kvnew,
+                                                   (dbg && l == 0) ? m->dbg_pos : nullptr,
+                                                   (dbg && l == 0) ? m->dbg_slot : nullptr, m->status));
+            }
+            PROF(QW_PROF_ATTN);
+            CUDA_TRY(launch_attn_paged(lc, T, l, m->q, c.n_heads, c.n_kv_heads, tv, kvv, sp.chunk, sp.n_splits,
+                                       m->part_o, m->part_ml, m->counters, m->attn, nullptr));
+        } else {
+            // decode: one new token per sequence; QK-norm, RoPE and the KV append run inside
+            AttnFuse fz = {m->qkv, w_qn, w_kn, c.rms_eps, m->rcos, m->rsin,
+                           (dbg && l == 0) ? m->dbg_pos : nullptr, (dbg && l == 0) ? m->dbg_slot : nullptr,
+                           m->status};
+            PROF(QW_PROF_ATTN);
+            CUDA_TRY(launch_attn_paged(lc, T, l, m->q, c.n_heads, c.n_kv_heads, tv, kvv, sp.chunk, sp.n_splits,
+                                       m->part_o, m->part_ml, m->counters, m->attn, &fz));
         }
         if (small) {
             PROF(QW_PROF_OPROJ);
