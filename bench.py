@@ -146,8 +146,19 @@ def kernel_bytes(kind: int, s, T: int, B: int) -> float:
     return float("nan")
 
 
+def step_bytes(s, B: int, ctx: float) -> float:
+    """Algorithmic bytes of one whole decode step: every weight once (fp16), the KV cache of
+    each sequence once (ctx keys, fp16 K and V, all layers), the new K/V written, and the
+    embedding rows, logits-free."""
+    D, I, QD, KD, V, L = s.hidden, s.inter, s.n_heads * s.head_dim, s.n_kv_heads * s.head_dim, s.vocab, s.n_layers
+    weights = L * ((QD + 2 * KD) * D + D * QD + 2 * I * D + D * I) * 2 + V * D * 2
+    kv = B * ctx * L * 2 * KD * 2
+    return weights + kv + B * L * 2 * KD * 2 + B * D * 2
+
+
 KIND_NAMES = {1: "qkv_proj(rmsnorm fused)", 2: "qknorm_rope_append", 3: "attention", 4: "o_proj+residual",
-              5: "gate_up+silu_mul(rmsnorm fused)", 6: "down_proj+residual", 7: "lm_head+argmax"}
+              5: "gate_up+silu_mul(rmsnorm fused)", 6: "down_proj+residual", 7: "lm_head+argmax",
+              9: "k_decode_mk (persistent decode step)"}
 
 
 def run_ours(args, cfg, rank, world):
@@ -168,6 +179,8 @@ def run_ours(args, cfg, rank, world):
                     kv_pages=B * ((max_ctx + 15) // 16) + 8, max_seqs=max(B, 8))
     del named, w
     st = eng.stream
+    if args.persistent:
+        qw.qw_set_option(eng.model, qw.QW_OPT_PERSISTENT_DECODE, 1)
     seqs = list(range(B))
     prompt = synth.make_tokens(s.vocab, B * P, 1000 + args.config + 17 * rank)
     d_prompt = torch.tensor(prompt, dtype=torch.int32, device="cuda")
@@ -236,15 +249,18 @@ def run_ours(args, cfg, rank, world):
     decode_us = a.elapsed_time(b) * 1e3 / ND
 
     # ---- per-kernel timing with CUDA events around each launch of one kernel kind ----
+    # (events bracket the launches inside the captured decode graphs; measured on the
+    # same workload right after the timed region)
     hbm, bf16_burst, bf16_sust, peak_src = peaks()
+    persistent = args.persistent and B <= 4
+    n_launch_per_step = {9: 1} if persistent else {1: s.n_layers, 4: s.n_layers, 5: s.n_layers, 6: s.n_layers, 7: 1}
     kinds = {}
-    n_launch_per_step = {1: s.n_layers, 4: s.n_layers, 5: s.n_layers, 6: s.n_layers, 7: 1}
     for kind, nl in n_launch_per_step.items():
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * nl)]
         for ev in evs:          # torch creates the CUDA event on its first record
             ev.record(st)
         handles = (qw.ctypes.c_void_p * (2 * nl))(*[ev.cuda_event for ev in evs])
-        durs = []
+        durs, ctxs = [], []
         qw.qw_kv_reset(eng.kv, -1, st)
         for sq in seqs:
             qw.qw_kv_reserve(eng.kv, sq, P + ND, st)
@@ -255,11 +271,13 @@ def run_ours(args, cfg, rank, world):
             st.synchronize()
             if i >= 2:
                 durs.extend(evs[2 * j].elapsed_time(evs[2 * j + 1]) for j in range(nl))
+                ctxs.append(P + i + 1)
         qw.qw_profile_set(eng.model, 0, None, 0)
         st.synchronize()
         avg_us = statistics.mean(durs) * 1e3
+        nbytes = step_bytes(s, B, statistics.mean(ctxs)) if kind == 9 else kernel_bytes(kind, s, B, B)
         kinds[kind] = dict(name=KIND_NAMES[kind], launches_per_step=nl, avg_us=avg_us,
-                           total_us_per_step=avg_us * nl, bytes=kernel_bytes(kind, s, B, B))
+                           total_us_per_step=avg_us * nl, bytes=nbytes)
     dom = max(kinds, key=lambda k: kinds[k]["total_us_per_step"])
     dk = kinds[dom]
     achieved = dk["bytes"] / (dk["avg_us"] * 1e-6) / 1e9
@@ -267,7 +285,7 @@ def run_ours(args, cfg, rank, world):
                 "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / hbm, 4),
                 "traffic": None, "algorithmic_bytes_per_launch": dk["bytes"],
                 "avg_launch_us": round(dk["avg_us"], 3)}
-    step_bytes = sum(kernel_bytes(k, s, B, B) * n for k, n in n_launch_per_step.items())
+    step_b = step_bytes(s, B, P + ND / 2)
     # ---- end to end through qw_generate with pinned host buffers ----
     h_prompt = torch.empty(B * P, dtype=torch.int32, pin_memory=True).numpy()
     h_prompt[:] = prompt
@@ -295,8 +313,8 @@ def run_ours(args, cfg, rank, world):
                    "tokens_per_step": tokens_per_step, "parallelism": f"replicas x{world} (no collective)",
                    "l2": "weights (1.19 GB per decode step) exceed L2; no flush",
                    "decode_step_us": round(decode_us, 2),
-                   "decode_step_bytes": step_bytes,
-                   "decode_step_hbm_frac": round(step_bytes / (decode_us * 1e-6) / 1e9 / hbm, 4)},
+                   "decode_step_bytes": step_b,
+                   "decode_step_hbm_frac": round(step_b / (decode_us * 1e-6) / 1e9 / hbm, 4)},
         "roofline": roofline,
         "kernels": {KIND_NAMES[k]: {"avg_us": round(v["avg_us"], 3), "per_step_us": round(v["total_us_per_step"], 2),
                                     "GB/s": round(v["bytes"] / (v["avg_us"] * 1e-6) / 1e9, 1)}
@@ -306,6 +324,179 @@ def run_ours(args, cfg, rank, world):
         "gpu_launches": gpu_launches,
         "clocks": clk.summary(),
     }
+    eng.close()
+    return out
+
+
+def attn_bytes_layer(s, ctx_total: float) -> float:
+    """KV bytes one attention launch reads: every cached key and value once (fp16)."""
+    return ctx_total * s.n_kv_heads * s.head_dim * 2 * 2
+
+
+def run_other(args, cfg, rank, world):
+    """Batched decode (2), prefill (3) and long-context decode (4)."""
+    import torch
+    import decode_qwen3_decoder_gb300 as pkg
+    pkg.build()
+    qw = pkg.qw
+    dev = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(dev)
+    s = cfg["shape"]
+    B, ND = cfg["B"], cfg["n_decode"]
+    kind = cfg["kind"]
+    if kind == "decode_long":
+        lens = synth.make_lengths(B, 1024, 32768, 2000)
+    else:
+        lens = np.full(B, cfg["prompt"], dtype=np.int64)
+    max_ctx = int(lens.max()) + ND + 16
+    chunk_seqs = 16 if kind != "decode_long" else B            # prefill 16 sequences per call
+    max_tokens = max(int(lens[:chunk_seqs].sum()), B, 8) if kind != "decode_long" else max(B, 8)
+    pages = int(sum((l + ND + 15) // 16 + 1 for l in lens)) + 8
+    w = synth.Weights(s, seed=0)
+    eng = qw.Engine(s, dict(w.named()), max_tokens=max_tokens, max_batch=max(B, 8), max_context=max_ctx,
+                    kv_pages=pages, max_seqs=max(B, 8))
+    del w
+    st = eng.stream
+    seqs = list(range(B))
+    rng_seed = 1000 + args.config + 17 * rank
+    d_cur = torch.zeros(B, dtype=torch.int32, device="cuda")
+    hbm, bf16_burst, bf16_sust, peak_src = peaks()
+
+    def fill_cache():
+        qw.qw_kv_reset(eng.kv, -1, st)
+        for sq in seqs:
+            qw.qw_kv_reserve(eng.kv, sq, int(lens[sq]) + ND, st)
+        if kind == "decode_long":
+            for sq in seqs:
+                qw.qw_kv_fill_synthetic(eng.kv, sq, int(lens[sq]), 77, st)
+        else:
+            toks = synth.make_tokens(s.vocab, int(lens.sum()), rng_seed)
+            d_t = torch.tensor(toks, dtype=torch.int32, device="cuda")
+            off = 0
+            for a in range(0, B, chunk_seqs):
+                grp = seqs[a:a + chunk_seqs]
+                n = int(lens[a:a + chunk_seqs].sum())
+                qw.qw_prefill(eng.model, eng.kv, grp, [int(lens[q]) for q in grp], d_t.data_ptr() + 4 * off, 0,
+                              d_cur.data_ptr() + 4 * a, st)
+                off += n
+        st.synchronize()
+
+    launches = [0]
+    if kind == "prefill":
+        toks = torch.tensor(synth.make_tokens(s.vocab, int(lens.sum()), rng_seed), dtype=torch.int32, device="cuda")
+
+        def one_step():
+            qw.qw_kv_reset(eng.kv, -1, st)
+            for sq in seqs:
+                qw.qw_kv_reserve(eng.kv, sq, int(lens[sq]), st)
+            qw.qw_prefill(eng.model, eng.kv, seqs, [int(x) for x in lens], toks.data_ptr(), 0, d_cur.data_ptr(), st)
+            launches[0] += qw.qw_last_launch_count(eng.model)
+        units_per_step = int(lens.sum())
+    else:
+        fill_cache()
+
+        def one_step():
+            for sq in seqs:
+                qw.qw_kv_truncate(eng.kv, sq, int(lens[sq]), st)
+            for i in range(ND):
+                qw.qw_decode_step(eng.model, eng.kv, seqs, d_cur.data_ptr(), 0, d_cur.data_ptr(), st)
+                launches[0] += qw.qw_last_launch_count(eng.model)
+        units_per_step = B * ND
+
+    for _ in range(args.warmup):
+        one_step()
+    st.synchronize()
+    if qw.qw_sync_status(eng.model, st) != 0:
+        raise RuntimeError(f"device status after warm-up: {qw.qw_last_error()}")
+    gpu_uuid = str(dev)
+    try:
+        gpu_uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        gpu_uuid = gpu_uuid if gpu_uuid.startswith("GPU-") else "GPU-" + gpu_uuid
+    except Exception:
+        pass
+    barrier(world)
+    launches[0] = 0
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(gpu_uuid) as clk:
+        torch.cuda.synchronize()
+        e0.record(st)
+        for _ in range(args.steps):
+            one_step()
+        e1.record(st)
+        torch.cuda.synchronize()
+    barrier(world)
+    ms_max = reduce_max(e0.elapsed_time(e1), world)
+    value = units_per_step * args.steps * world / (ms_max / 1e3)
+    if qw.qw_sync_status(eng.model, st) != 0:
+        raise RuntimeError(f"device status in the timed region: {qw.qw_last_error()}")
+
+    # per-kernel timing (events around each launch of a kind, one step after the timed region)
+    L = s.n_layers
+    kinds_n = {1: L, 3: L, 4: L, 5: L, 6: L, 7: 1}
+    if kind == "prefill":
+        kinds_n.update({2: L, 8: 2 * L + 1})
+    kinds = {}
+    for kd, nl in kinds_n.items():
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * nl)]
+        for ev in evs:
+            ev.record(st)
+        handles = (qw.ctypes.c_void_p * (2 * nl))(*[ev.cuda_event for ev in evs])
+        if kind != "prefill":
+            for sq in seqs:
+                qw.qw_kv_truncate(eng.kv, sq, int(lens[sq]), st)
+        qw.qw_profile_set(eng.model, kd, handles, 2 * nl)
+        if kind == "prefill":
+            one_step()
+        else:
+            qw.qw_decode_step(eng.model, eng.kv, seqs, d_cur.data_ptr(), 0, d_cur.data_ptr(), st)
+        st.synchronize()
+        qw.qw_profile_set(eng.model, 0, None, 0)
+        d = [evs[2 * j].elapsed_time(evs[2 * j + 1]) * 1e3 for j in range(nl)]
+        kinds[kd] = dict(name=KIND_NAMES.get(kd, "rmsnorm" if kd == 8 else str(kd)), avg_us=statistics.mean(d),
+                         per_step_us=sum(d), launches=nl)
+    T = int(lens.sum()) if kind == "prefill" else B
+    D, I, QD, KD, V = s.hidden, s.inter, s.n_heads * s.head_dim, s.n_kv_heads * s.head_dim, s.vocab
+    if kind == "prefill":
+        flops = {1: 2 * T * (QD + 2 * KD) * D, 4: 2 * T * D * QD, 5: 2 * T * 2 * I * D, 6: 2 * T * D * I,
+                 7: 2 * B * V * D}
+        for kd, f in flops.items():
+            kinds[kd]["TFLOP/s"] = round(f / (kinds[kd]["avg_us"] * 1e-6) / 1e12, 1)
+        gemm_kinds = [1, 4, 5, 6]
+        dom = max(gemm_kinds, key=lambda k: kinds[k]["per_step_us"])
+        ach = flops[dom] / (kinds[dom]["avg_us"] * 1e-6) / 1e12
+        roofline = {"bound": "tensor", "kernel": kinds[dom]["name"] + " (tcgen05 GEMM)", "achieved": round(ach, 1),
+                    "peak": bf16_sust, "peak_source": peak_src + " bf16 sustained (fp16 operands run at the bf16 rate)",
+                    "unit": "TFLOP/s", "frac": round(ach / bf16_sust, 4), "traffic": None,
+                    "algorithmic_flops_per_launch": flops[dom], "avg_launch_us": round(kinds[dom]["avg_us"], 2)}
+        attn_pairs = sum(int(l) * (int(l) + 1) // 2 for l in lens)
+        total_flops = L * sum(flops[k] for k in gemm_kinds) + flops[7] + L * attn_pairs * 4 * s.head_dim * s.n_heads
+        extra = {"step_tflop": total_flops / 1e12,
+                 "step_tc_frac": round(total_flops / (ms_max / args.steps * 1e-3) / 1e12 / bf16_burst, 4)}
+    else:
+        ctx = float(np.mean(lens)) + ND / 2
+        kv_bytes = attn_bytes_layer(s, float(np.sum(lens)) + B * ND / 2)
+        byts = {1: (QD + 2 * KD) * D * 2, 3: kv_bytes, 4: D * QD * 2, 5: 2 * I * D * 2, 6: D * I * 2, 7: V * D * 2}
+        for kd, b in byts.items():
+            kinds[kd]["GB/s"] = round(b / (kinds[kd]["avg_us"] * 1e-6) / 1e9, 1)
+        dom = max(byts, key=lambda k: kinds[k]["per_step_us"])
+        ach = byts[dom] / (kinds[dom]["avg_us"] * 1e-6) / 1e9
+        roofline = {"bound": "hbm", "kernel": kinds[dom]["name"], "achieved": round(ach, 1), "peak": hbm,
+                    "peak_source": peak_src, "unit": "GB/s", "frac": round(ach / hbm, 4), "traffic": None,
+                    "algorithmic_bytes_per_launch": byts[dom], "avg_launch_us": round(kinds[dom]["avg_us"], 2)}
+        step_b = step_bytes(s, B, ctx)
+        step_us = ms_max / args.steps / ND * 1e3
+        extra = {"decode_step_us": round(step_us, 2), "decode_step_bytes": step_b,
+                 "decode_step_hbm_frac": round(step_b / (step_us * 1e-6) / 1e9 / hbm, 4),
+                 "mean_cached_len": float(np.mean(lens))}
+    out = {"metric": METRIC, "value": round(value, 2), "unit": cfg["unit"], "n_gpus": world, "steps": args.steps,
+           "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f16 operands / f32 accumulate (bf16 weights)",
+           "data": "synthetic (seeded random-init bf16 weights N(0,0.02), uniform-random token ids)",
+           "config": dict({"workload": cfg["workload"], "batch": B, "l2": "working set exceeds L2; no flush"}, **extra),
+           "roofline": roofline,
+           "kernels": {v["name"]: {k: (round(x, 2) if isinstance(x, float) else x) for k, x in v.items() if k != "name"}
+                       for v in kinds.values()},
+           "gpu_launches": launches[0], "clocks": clk.summary()}
     eng.close()
     return out
 
@@ -394,7 +585,9 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=1, choices=[0, 1])
+    ap.add_argument("--config", type=int, default=1, choices=[0, 1, 2, 3, 4])
+    ap.add_argument("--persistent", action="store_true",
+                    help="decode steps of <= 4 sequences as one persistent kernel")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -409,9 +602,9 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("gloo")
-    out = run_ours(args, cfg, rank, world)
+    out = run_ours(args, cfg, rank, world) if args.config in (0, 1) else run_other(args, cfg, rank, world)
     if rank == 0:
-        if not args.no_cpu_baseline:
+        if not args.no_cpu_baseline and args.config in (0, 1):
             out["cpu_baseline"] = cpu_baseline(cfg)
         print(json.dumps(out), flush=True)
     if world > 1:

@@ -68,7 +68,7 @@ extern "C" qw_status qw_lm_head_argmax_noalloc(const qw_model* m, int B, const f
     e = cudaMemsetAsync(keys, 0, (size_t)B * sizeof(unsigned long long), st);
     if (e != cudaSuccess) return qw_fail(QW_ERR_CUDA, "clearing the keys failed: %s", cudaGetErrorString(e));
     LaunchCtx c = {st, false, nullptr};
-    e = launch_gemv_lmhead(c, B, dev_x, nullptr, v.final_norm, v.eps, v.embed16, v.vocab, v.hidden, dev_logits,
+    e = launch_gemv_lmhead(c, B, dev_x, nullptr, v.final_norm, v.eps, v.embed, v.vocab, v.hidden, dev_logits,
                            (unsigned long long*)keys);
     if (e != cudaSuccess) return qw_fail(QW_ERR_CUDA, "LM-head launch failed: %s", cudaGetErrorString(e));
     k_noalloc_unpack<<<1, 32, 0, st>>>((unsigned long long*)keys, B, dev_next_ids);

@@ -37,16 +37,16 @@ __device__ __forceinline__ uint4 ldg_stream(const void* p) {
     return r;
 }
 
-// 8 fp16 weights (one 16-byte chunk) against 8 fp32 activations.
+// 8 bf16 weights (one 16-byte chunk, widened exactly by a shift) against 8 fp32 activations.
 __device__ __forceinline__ float dot8(const uint4 w, const float4 a0, const float4 a1, float acc) {
-    acc = fmaf(h_lo(w.x), a0.x, acc);
-    acc = fmaf(h_hi(w.x), a0.y, acc);
-    acc = fmaf(h_lo(w.y), a0.z, acc);
-    acc = fmaf(h_hi(w.y), a0.w, acc);
-    acc = fmaf(h_lo(w.z), a1.x, acc);
-    acc = fmaf(h_hi(w.z), a1.y, acc);
-    acc = fmaf(h_lo(w.w), a1.z, acc);
-    acc = fmaf(h_hi(w.w), a1.w, acc);
+    acc = fmaf(bf_lo(w.x), a0.x, acc);
+    acc = fmaf(bf_hi(w.x), a0.y, acc);
+    acc = fmaf(bf_lo(w.y), a0.z, acc);
+    acc = fmaf(bf_hi(w.y), a0.w, acc);
+    acc = fmaf(bf_lo(w.z), a1.x, acc);
+    acc = fmaf(bf_hi(w.z), a1.y, acc);
+    acc = fmaf(bf_lo(w.w), a1.z, acc);
+    acc = fmaf(bf_hi(w.w), a1.w, acc);
     return acc;
 }
 
@@ -136,7 +136,7 @@ cudaError_t launch_rmsnorm(const LaunchCtx& c, const float* x, const int* rows, 
 // Each warp owns RPW output rows at a time; every lane streams one 16-byte chunk of each
 // row per 256 columns, so a warp reads whole rows with coalesced 512-byte requests, in
 // passes of 1024 columns that keep RPW*4 16-byte loads per lane in flight. The activations sit in
-// shared memory as fp32; weights are fp16. MODE selects the prologue/epilogue:
+// shared memory as fp32; weights are the bf16 originals. MODE selects the prologue/epilogue:
 //   G_QKV    : a = rms_norm(x) * w_in  (Paso 3 fused), out fp32 (Paso 5 projections)
 //   G_GATEUP : a = rms_norm(x) * w_post, act = fp16(silu(Wg a) * (Wu a))  (Paso 6)
 //   G_RESID  : a = fp16 activations, x += W a  (o_proj / down_proj + residual, Paso 7)
@@ -150,8 +150,8 @@ struct GemvP {
     const bf16* norm_w;
     float eps;
     const f16* act;
-    const f16* W;
-    const f16* W2;
+    const bf16* W;
+    const bf16* W2;
     int n_out;
     int K;
     int T;
@@ -381,21 +381,21 @@ cudaError_t gemv_dispatch(const LaunchCtx& c, const GemvP& p, int max_ctas) {
 }  // namespace
 
 cudaError_t launch_gemv_qkv(const LaunchCtx& c, int T, const float* x, const bf16* norm_w, float eps,
-                            const f16* W, int n_out, int K, float* out) {
+                            const bf16* W, int n_out, int K, float* out) {
     GemvP p = {};
     p.x = x; p.norm_w = norm_w; p.eps = eps; p.W = W; p.n_out = n_out; p.K = K; p.T = T; p.out = out;
     return gemv_dispatch<G_QKV>(c, p, 0);
 }
 
 cudaError_t launch_gemv_gateup(const LaunchCtx& c, int T, const float* x, const bf16* norm_w,
-                               float eps, const f16* Wg, const f16* Wu, int inter, int K, f16* act) {
+                               float eps, const bf16* Wg, const bf16* Wu, int inter, int K, f16* act) {
     GemvP p = {};
     p.x = x; p.norm_w = norm_w; p.eps = eps; p.W = Wg; p.W2 = Wu; p.n_out = inter; p.K = K; p.T = T;
     p.out_h = act;
     return gemv_dispatch<G_GATEUP>(c, p, 0);
 }
 
-cudaError_t launch_gemv_resid(const LaunchCtx& c, int T, const f16* act, const f16* W, int n_out,
+cudaError_t launch_gemv_resid(const LaunchCtx& c, int T, const f16* act, const bf16* W, int n_out,
                               int K, float* x) {
     GemvP p = {};
     p.act = act; p.W = W; p.n_out = n_out; p.K = K; p.T = T; p.out = x;
@@ -403,7 +403,7 @@ cudaError_t launch_gemv_resid(const LaunchCtx& c, int T, const f16* act, const f
 }
 
 cudaError_t launch_gemv_lmhead(const LaunchCtx& c, int B, const float* x, const int* rows,
-                               const bf16* norm_w, float eps, const f16* E, int vocab, int K,
+                               const bf16* norm_w, float eps, const bf16* E, int vocab, int K,
                                float* logits, unsigned long long* best) {
     GemvP p = {};
     p.x = x; p.rows = rows; p.norm_w = norm_w; p.eps = eps; p.W = E; p.n_out = vocab; p.K = K;

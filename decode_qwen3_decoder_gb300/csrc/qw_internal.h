@@ -118,13 +118,13 @@ cudaError_t launch_rmsnorm(const LaunchCtx& c, const float* x, const int* rows, 
 cudaError_t launch_convert_bf16_f16(const LaunchCtx& c, const bf16* src, f16* dst, size_t n, int* status);
 // GEMV family (T <= 8 token rows).
 cudaError_t launch_gemv_qkv(const LaunchCtx& c, int T, const float* x, const bf16* norm_w, float eps,
-                            const f16* W, int n_out, int K, float* out);
+                            const bf16* W, int n_out, int K, float* out);
 cudaError_t launch_gemv_gateup(const LaunchCtx& c, int T, const float* x, const bf16* norm_w,
-                               float eps, const f16* Wg, const f16* Wu, int inter, int K, f16* act);
-cudaError_t launch_gemv_resid(const LaunchCtx& c, int T, const f16* act, const f16* W, int n_out,
+                               float eps, const bf16* Wg, const bf16* Wu, int inter, int K, f16* act);
+cudaError_t launch_gemv_resid(const LaunchCtx& c, int T, const f16* act, const bf16* W, int n_out,
                               int K, float* x);
 cudaError_t launch_gemv_lmhead(const LaunchCtx& c, int B, const float* x, const int* rows,
-                               const bf16* norm_w, float eps, const f16* E, int vocab, int K,
+                               const bf16* norm_w, float eps, const bf16* E, int vocab, int K,
                                float* logits, unsigned long long* best);
 cudaError_t launch_finalize(const LaunchCtx& c, const StepDesc& sd, unsigned long long* best,
                             int32_t* next_ids, KVView kv);
@@ -149,13 +149,16 @@ cudaError_t launch_attn_paged(const LaunchCtx& c, int T, int layer, const f16* q
                               int n_kv, TokView tv, KVView kv, int chunk, int n_splits,
                               float* part_o, float* part_ml, int* counters, f16* out,
                               const AttnFuse* fuse);
+// Causal flash attention of a prefill over the contiguous new K/V (sequences start empty).
+cudaError_t launch_attn_prefill(const LaunchCtx& c, const StepDesc& sd, int max_len, const f16* q,
+                                const f16* kv_new, int n_heads, int n_kv, f16* out);
 cudaError_t launch_kv_fill(const LaunchCtx& c, KVView kv, int n_layers, int n_kv, int seq,
                            int n_tokens, unsigned long long seed);
 
 // What the LM head needs from a model (read-only view for entry points in other files).
 struct LmHeadView {
     const bf16* final_norm;
-    const f16* embed16;
+    const bf16* embed;
     float eps;
     int vocab;
     int hidden;
@@ -181,7 +184,59 @@ struct GemmArgs {
     float* logits;            // EPI_ARGMAX: optional logits[t][m]
     unsigned long long* best; // EPI_ARGMAX: per-token packed argmax keys
     int* status;
+    float* part;              // split-K partial tiles (NULL: never split)
+    size_t part_bytes;
+    int* tickets;             // split-K per-tile counters (zeroed; left zeroed)
+    int max_tiles;
+    int num_sms;
 };
 cudaError_t launch_gemm_tc(const LaunchCtx& c, int epi, const GemmArgs& a);
 bool gemm_tc_encode_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                         uint32_t box_rows);
+
+// Persistent decode kernel (k_mk.cu): one cooperative launch per decode step of <= 8 tokens.
+struct MkParams {
+    // model
+    const bf16* wqkv;  // bf16 packed weights
+    const bf16* wo;
+    const bf16* wg;
+    const bf16* wu;
+    const bf16* wd;
+    const bf16* embed;
+    const bf16* norms;  // per layer [in D][post D][q_norm 128][k_norm 128]
+    const bf16* fnorm;
+    const float* rcos;
+    const float* rsin;
+    int n_layers, D, I, QD, QKV, V, n_heads, n_kv;
+    float eps;
+    float scale_log2;
+    // step
+    int T;
+    int seq[8];
+    const int32_t* ids;
+    int32_t* next_ids;
+    float* logits;
+    KVView kv;
+    int chunk, n_splits;
+    // workspace
+    float* x;
+    float* qkv;
+    f16* o;
+    f16* act;
+    float* part_o;
+    float* part_ml;
+    int* counters;
+    unsigned long long* best;
+    int* status;
+    unsigned* sync;  // [0] arrivals, [1] generation, [2] LM-head ticket
+    int* abort_g;
+    float* dbg_hidden;
+    int32_t* dbg_pos;
+    int32_t* dbg_slot;
+    unsigned long long* trace;  // optional: [grid][trace_n][2] barrier arrival / release times
+    int trace_n;
+};
+int mk_smem_bytes();
+int mk_max_tokens(int D, int I, int QD);
+int mk_grid_size();
+cudaError_t launch_decode_mk(const LaunchCtx& c, const MkParams& p, int grid);

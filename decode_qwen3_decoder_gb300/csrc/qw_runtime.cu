@@ -54,6 +54,8 @@ extern "C" const char* qw_last_error(void) { return g_err.c_str(); }
 // ---------------------------------------------------------------------------------------
 static constexpr int kMaxSplits = 128;   // split-KV partial slots per (token, head)
 static constexpr int kSmallT = 8;        // token rows handled by the GEMV family
+static constexpr size_t kGemmPartBytes = 48u << 20;
+static constexpr int kGemmMaxTiles = 4096;
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -83,9 +85,9 @@ static bool config_ok(const qw_config* c, std::string* why) {
 }
 
 struct WsLayout {
-    size_t wqkv, wo, wg, wu, wd, embed16, norms, fnorm, rcos, rsin;
+    size_t wqkv, wo, wg, wu, wd, embed16, bqkv, bo, bg, bu, bd, norms, fnorm, rcos, rsin;
     size_t x, h, qkv, q, kvnew, attn, act, part_o, part_ml, counters;
-    size_t tok_seq, tok_pos, last, best, status, gen_tok, gen_cur, gen_out;
+    size_t tok_seq, tok_pos, last, best, status, gen_tok, gen_cur, gen_out, mk_sync, gpart, gtick;
     size_t total;
     int part_T;
 };
@@ -108,6 +110,11 @@ static WsLayout layout_for(const qw_config& c) {
     L.wu = take(NL * I * D * 2);
     L.wd = take(NL * D * I * 2);
     L.embed16 = take((size_t)c.vocab * D * 2);
+    L.bqkv = take(NL * QKV * D * 2);
+    L.bo = take(NL * D * QD * 2);
+    L.bg = take(NL * I * D * 2);
+    L.bu = take(NL * I * D * 2);
+    L.bd = take(NL * D * I * 2);
     L.norms = take(NL * (2 * D + 2 * c.head_dim) * 2);
     L.fnorm = take(D * 2);
     L.rcos = take((size_t)c.max_context * 64 * 4);
@@ -128,6 +135,9 @@ static WsLayout layout_for(const qw_config& c) {
     L.last = take((size_t)c.max_batch * 4);
     L.best = take((size_t)c.max_batch * 8);
     L.status = take(4);
+    L.mk_sync = take(16);  // persistent decode kernel: arrivals, generation, ticket, abort
+    L.gpart = take(kGemmPartBytes);          // split-K partial tiles
+    L.gtick = take(kGemmMaxTiles * 4);       // split-K tickets
     L.gen_tok = take(T * 4);
     L.gen_cur = take((size_t)c.max_batch * 4);
     L.gen_out = take((size_t)c.max_batch * ((size_t)c.max_context + 1) * 4);
@@ -149,12 +159,19 @@ struct qw_model {
     WsLayout L;
     char* ws;
     int qkv_rows;
-    f16 *wqkv, *wo, *wg, *wu, *wd, *embed16;  // fp16 copies of the bf16 weights
+    f16 *wqkv, *wo, *wg, *wu, *wd, *embed16;  // fp16 copies of the bf16 weights (tensor cores)
+    bf16 *bqkv, *bo, *bg, *bu, *bd;           // bf16 packed copies (small-batch decode paths)
     bf16 *norms, *fnorm;
     const bf16* embed;
     float *rcos, *rsin, *x, *qkv, *part_o, *part_ml;
     f16 *h, *q, *kvnew, *attn, *act;
     int *counters, *tok_seq, *tok_pos, *last, *status;
+    unsigned* mk_sync;
+    float* gpart;
+    int* gtick;
+    int mk_grid;       // CTAs of the persistent decode kernel (0: not available)
+    int mk_max_t;      // most tokens it takes
+    bool use_mk;       // decode steps of <= mk_max_t tokens run as one persistent kernel
     unsigned long long* best;
     int32_t *gen_tok, *gen_cur, *gen_out;
     float* dbg_hidden;
@@ -167,6 +184,8 @@ struct qw_model {
     bool pdl;
     // profiling: events around launches of one kernel kind
     int prof_kind;
+    unsigned long long* trace;
+    int trace_n;
     std::vector<cudaEvent_t> prof_events;
     unsigned long long prof_gen;
     // TMA descriptors of the tensor-core GEMM operands
@@ -243,6 +262,11 @@ extern "C" qw_status qw_init_weights(const qw_config* cfg, const qw_weight_ptrs*
     m->wu = (f16*)(b + L.wu);
     m->wd = (f16*)(b + L.wd);
     m->embed16 = (f16*)(b + L.embed16);
+    m->bqkv = (bf16*)(b + L.bqkv);
+    m->bo = (bf16*)(b + L.bo);
+    m->bg = (bf16*)(b + L.bg);
+    m->bu = (bf16*)(b + L.bu);
+    m->bd = (bf16*)(b + L.bd);
     m->norms = (bf16*)(b + L.norms);
     m->fnorm = (bf16*)(b + L.fnorm);
     m->embed = (const bf16*)w->embed_tokens;
@@ -263,6 +287,9 @@ extern "C" qw_status qw_init_weights(const qw_config* cfg, const qw_weight_ptrs*
     m->last = (int*)(b + L.last);
     m->best = (unsigned long long*)(b + L.best);
     m->status = (int*)(b + L.status);
+    m->mk_sync = (unsigned*)(b + L.mk_sync);
+    m->gpart = (float*)(b + L.gpart);
+    m->gtick = (int*)(b + L.gtick);
     m->gen_tok = (int32_t*)(b + L.gen_tok);
     m->gen_cur = (int32_t*)(b + L.gen_cur);
     m->gen_out = (int32_t*)(b + L.gen_out);
@@ -304,6 +331,15 @@ extern "C" qw_status qw_init_weights(const qw_config* cfg, const qw_weight_ptrs*
         if (e == cudaSuccess) e = cv(m->wg + (size_t)l * I * D, lp.gate_proj, I * D);
         if (e == cudaSuccess) e = cv(m->wu + (size_t)l * I * D, lp.up_proj, I * D);
         if (e == cudaSuccess) e = cv(m->wd + (size_t)l * D * I, lp.down_proj, D * I);
+        // bf16 packed copies (bit-identical) for the bandwidth-bound small-batch paths
+        bf16* b0 = m->bqkv + (size_t)l * m->qkv_rows * D;
+        if (e == cudaSuccess) e = cp(b0, lp.q_proj, QD * D * 2);
+        if (e == cudaSuccess) e = cp(b0 + QD * D, lp.k_proj, KD * D * 2);
+        if (e == cudaSuccess) e = cp(b0 + (QD + KD) * D, lp.v_proj, KD * D * 2);
+        if (e == cudaSuccess) e = cp(m->bo + (size_t)l * D * QD, lp.o_proj, D * QD * 2);
+        if (e == cudaSuccess) e = cp(m->bg + (size_t)l * I * D, lp.gate_proj, I * D * 2);
+        if (e == cudaSuccess) e = cp(m->bu + (size_t)l * I * D, lp.up_proj, I * D * 2);
+        if (e == cudaSuccess) e = cp(m->bd + (size_t)l * D * I, lp.down_proj, D * I * 2);
         bf16* nb = m->norms + (size_t)l * (2 * D + 2 * d);
         if (e == cudaSuccess) e = cp(nb, lp.input_layernorm, D * 2);
         if (e == cudaSuccess) e = cp(nb + D, lp.post_attention_layernorm, D * 2);
@@ -343,7 +379,9 @@ extern "C" qw_status qw_init_weights(const qw_config* cfg, const qw_weight_ptrs*
         }
     }
     if (cudaMemsetAsync(m->counters, 0, (size_t)L.part_T * cfg->n_kv_heads * 4, st) != cudaSuccess ||
-        cudaMemsetAsync(m->best, 0, (size_t)cfg->max_batch * 8, st) != cudaSuccess) {
+        cudaMemsetAsync(m->best, 0, (size_t)cfg->max_batch * 8, st) != cudaSuccess ||
+        cudaMemsetAsync(m->mk_sync, 0, 16, st) != cudaSuccess ||
+        cudaMemsetAsync(m->gtick, 0, kGemmMaxTiles * 4, st) != cudaSuccess) {
         fail(QW_ERR_CUDA, "workspace clear failed");
         return fail_free(QW_ERR_CUDA);
     }
@@ -384,6 +422,11 @@ extern "C" qw_status qw_init_weights(const qw_config* cfg, const qw_weight_ptrs*
     m->dbg_pos = m->dbg_slot = nullptr;
     m->prof_kind = QW_PROF_OFF;
     m->prof_gen = 0;
+    m->trace = nullptr;
+    m->trace_n = 0;
+    m->mk_grid = mk_grid_size();
+    m->mk_max_t = m->mk_grid > 0 ? std::min(mk_max_tokens(cfg->hidden, cfg->inter, cfg->n_heads * cfg->head_dim), 8) : 0;
+    m->use_mk = false;  // opt in with QW_OPT_PERSISTENT_DECODE
     *out = m;
     return QW_OK;
 }
@@ -406,10 +449,35 @@ extern "C" qw_status qw_debug_set(qw_model* m, float* dev_hidden, int32_t* dev_p
 
 extern "C" int qw_last_launch_count(const qw_model* m) { return m ? m->last_launches : 0; }
 
+extern "C" qw_status qw_trace_set(qw_model* m, unsigned long long* dev_buf, int per_cta) {
+    if (!m) return fail(QW_ERR_INVALID_ARG, "model is NULL");
+    m->trace = per_cta > 0 ? dev_buf : nullptr;
+    m->trace_n = dev_buf ? per_cta : 0;
+    ++m->prof_gen;
+    return QW_OK;
+}
+
+extern "C" int qw_persistent_grid(const qw_model* m) { return m ? m->mk_grid : 0; }
+
+extern "C" qw_status qw_set_option(qw_model* m, int option, int value) {
+    if (!m) return fail(QW_ERR_INVALID_ARG, "model is NULL");
+    switch (option) {
+        case QW_OPT_PERSISTENT_DECODE:
+            if (value && m->mk_max_t == 0) return fail(QW_ERR_UNSUPPORTED, "persistent decode kernel unavailable");
+            m->use_mk = value != 0;
+            return QW_OK;
+        case QW_OPT_PDL:
+            m->pdl = value != 0;
+            return QW_OK;
+        default:
+            return fail(QW_ERR_INVALID_ARG, "unknown option %d", option);
+    }
+}
+
 bool qw_model_lmhead_view(const qw_model* m, LmHeadView* v) {
     if (!m || !v) return false;
     v->final_norm = m->fnorm;
-    v->embed16 = m->embed16;
+    v->embed = m->embed;
     v->eps = m->cfg.rms_eps;
     v->vocab = m->cfg.vocab;
     v->hidden = m->cfg.hidden;
@@ -428,7 +496,7 @@ qw_status qw_fail(qw_status s, const char* fmt, ...) {
 
 extern "C" qw_status qw_profile_set(qw_model* m, int kind, void* const* events, int n_events) {
     if (!m) return fail(QW_ERR_INVALID_ARG, "model is NULL");
-    if (kind < QW_PROF_OFF || kind > QW_PROF_RMSNORM) return fail(QW_ERR_INVALID_ARG, "unknown kernel kind %d", kind);
+    if (kind < QW_PROF_OFF || kind > QW_PROF_STEP) return fail(QW_ERR_INVALID_ARG, "unknown kernel kind %d", kind);
     m->prof_events.clear();
     if (kind == QW_PROF_OFF || !events || n_events < 2) {
         m->prof_kind = QW_PROF_OFF;
@@ -450,11 +518,20 @@ struct ProfScope {
         const int j = counts[kind]++;
         if (2 * j + 1 < (int)m->prof_events.size()) {
             idx = 2 * j;
-            cudaEventRecordWithFlags(m->prof_events[idx], st, cudaEventRecordExternal);
+            record(m->prof_events[idx]);
         }
     }
+    // inside stream capture the records become event-record nodes of the graph
+    void record(cudaEvent_t ev) {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        cudaStreamIsCapturing(st, &cs);
+        if (cs == cudaStreamCaptureStatusActive)
+            cudaEventRecordWithFlags(ev, st, cudaEventRecordExternal);
+        else
+            cudaEventRecord(ev, st);
+    }
     ~ProfScope() {
-        if (idx >= 0) cudaEventRecordWithFlags(m->prof_events[idx + 1], st, cudaEventRecordExternal);
+        if (idx >= 0) record(m->prof_events[idx + 1]);
     }
 };
 
@@ -546,6 +623,17 @@ extern "C" qw_status qw_kv_reset(qw_kv* kv, int seq, void* stream_) {
     return QW_OK;
 }
 
+extern "C" qw_status qw_kv_truncate(qw_kv* kv, int seq, int n_tokens, void* stream_) {
+    if (!kv) return fail(QW_ERR_INVALID_ARG, "kv is NULL");
+    if (seq < 0 || seq >= kv->max_seqs) return fail(QW_ERR_INVALID_ARG, "seq id %d out of range", seq);
+    if (n_tokens < 0 || n_tokens > kv->len[seq])
+        return fail(QW_ERR_INVALID_ARG, "n_tokens %d outside [0, length %d]", n_tokens, kv->len[seq]);
+    const int n = n_tokens;
+    CUDA_TRY(cudaMemcpyAsync(kv->d_len + seq, &n, 4, cudaMemcpyHostToDevice, (cudaStream_t)stream_));
+    kv->len[seq] = n_tokens;
+    return QW_OK;
+}
+
 extern "C" int qw_kv_free_pages(const qw_kv* kv) { return kv ? (int)kv->free_pages.size() : -1; }
 
 extern "C" int qw_kv_length(const qw_kv* kv, int seq) {
@@ -610,7 +698,7 @@ static qw_status run_step(qw_model* m, qw_kv* kv, const StepDesc& sd, bool prefi
                           const int32_t* tokens, float* logits, int32_t* next, cudaStream_t st,
                           bool allow_debug, int* launches) {
     const qw_config& c = m->cfg;
-    LaunchCtx lc = {st, m->pdl, launches};
+    LaunchCtx lc = {st, m->pdl && m->prof_kind == QW_PROF_OFF, launches};  // events must bracket launches
     const int T = sd.T, B = sd.B;
     const int D = c.hidden, I = c.inter, QD = c.n_heads * c.head_dim, d = c.head_dim;
     const KVView kvv = kv->view();
@@ -622,6 +710,42 @@ static qw_status run_step(qw_model* m, qw_kv* kv, const StepDesc& sd, bool prefi
 
     int pc[16] = {0};
 #define PROF(kind) ProfScope prof_scope_(m, kind, pc, st)
+    if (!prefill && m->use_mk && T <= m->mk_max_t) {
+        // one cooperative launch for the whole decode step
+        const int units_teams = 3 * m->mk_grid;
+        const int pairs = T * c.n_kv_heads;
+        int want = std::max(1, std::min((units_teams + pairs - 1) / pairs, kMaxSplits));
+        int chunk = std::max(64, ((max_keys + want - 1) / want + 15) / 16 * 16);
+        int nspl = (max_keys + chunk - 1) / chunk;
+        while (nspl > kMaxSplits) {
+            chunk += 16;
+            nspl = (max_keys + chunk - 1) / chunk;
+        }
+        MkParams mp = {};
+        mp.wqkv = m->bqkv; mp.wo = m->bo; mp.wg = m->bg; mp.wu = m->bu; mp.wd = m->bd;
+        mp.embed = m->embed; mp.norms = m->norms; mp.fnorm = m->fnorm;
+        mp.rcos = m->rcos; mp.rsin = m->rsin;
+        mp.n_layers = c.n_layers; mp.D = D; mp.I = I; mp.QD = QD; mp.QKV = m->qkv_rows; mp.V = c.vocab;
+        mp.n_heads = c.n_heads; mp.n_kv = c.n_kv_heads; mp.eps = c.rms_eps;
+        mp.scale_log2 = 0.08838834764831845f * 1.4426950408889634f;
+        mp.T = T;
+        for (int b = 0; b < T; ++b) mp.seq[b] = sd.seq[b];
+        mp.ids = tokens; mp.next_ids = next; mp.logits = logits;
+        mp.kv = kvv; mp.chunk = chunk; mp.n_splits = std::max(nspl, 1);
+        mp.x = m->x; mp.qkv = m->qkv; mp.o = m->attn; mp.act = m->act;
+        mp.part_o = m->part_o; mp.part_ml = m->part_ml; mp.counters = m->counters; mp.best = m->best;
+        mp.status = m->status; mp.sync = m->mk_sync; mp.abort_g = (int*)(m->mk_sync + 3);
+        mp.dbg_hidden = dbg ? m->dbg_hidden : nullptr;
+        mp.dbg_pos = dbg ? m->dbg_pos : nullptr;
+        mp.dbg_slot = dbg ? m->dbg_slot : nullptr;
+        mp.trace = m->trace;
+        mp.trace_n = m->trace_n;
+        int pc0[16] = {0};
+        ProfScope prof_scope_(m, QW_PROF_STEP, pc0, st);
+        LaunchCtx lc1 = {st, false, launches};
+        CUDA_TRY(launch_decode_mk(lc1, mp, m->mk_grid));
+        return QW_OK;
+    }
     CUDA_TRY(launch_step_begin(lc, sd, tokens, m->embed, c.vocab, D, m->x, tv, kvv, m->status));
     for (int l = 0; l < c.n_layers; ++l) {
         const bf16* nb = m->norms + (size_t)l * (2 * D + 2 * d);
@@ -632,7 +756,7 @@ static qw_status run_step(qw_model* m, qw_kv* kv, const StepDesc& sd, bool prefi
         // --- attention sublayer (Paso 5) ---
         if (small) {
             PROF(QW_PROF_QKV);
-            CUDA_TRY(launch_gemv_qkv(lc, T, m->x, w_in, c.rms_eps, m->wqkv + (size_t)l * m->qkv_rows * D,
+            CUDA_TRY(launch_gemv_qkv(lc, T, m->x, w_in, c.rms_eps, m->bqkv + (size_t)l * m->qkv_rows * D,
                                      m->qkv_rows, D, m->qkv));
         } else {
             {
@@ -643,7 +767,7 @@ static qw_status run_step(qw_model* m, qw_kv* kv, const StepDesc& sd, bool prefi
             GemmArgs g = {};
             g.tmA = &m->tm_wqkv; g.tmA2 = &m->tm_wqkv; g.tmB = m->tm_h;
             g.a_row0 = l * m->qkv_rows; g.a2_row0 = g.a_row0; g.M = m->qkv_rows; g.K = D; g.T = T;
-            g.out_f32 = m->qkv; g.ld_out = m->qkv_rows; g.status = m->status;
+            g.out_f32 = m->qkv; g.ld_out = m->qkv_rows; g.status = m->status; g.part = m->gpart; g.part_bytes = kGemmPartBytes; g.tickets = m->gtick; g.max_tiles = kGemmMaxTiles; g.num_sms = m->num_sms;
             CUDA_TRY(launch_gemm_tc(lc, EPI_STORE_F32, g));
         }
         if (prefill) {
@@ -655,8 +779,11 @@ static qw_status run_step(qw_model* m, qw_kv* kv, const StepDesc& sd, bool prefi
                                                    (dbg && l == 0) ? m->dbg_slot : nullptr, m->status));
             }
             PROF(QW_PROF_ATTN);
-            CUDA_TRY(launch_attn_paged(lc, T, l, m->q, c.n_heads, c.n_kv_heads, tv, kvv, sp.chunk, sp.n_splits,
-                                       m->part_o, m->part_ml, m->counters, m->attn, nullptr));
+            if (small)
+                CUDA_TRY(launch_attn_paged(lc, T, l, m->q, c.n_heads, c.n_kv_heads, tv, kvv, sp.chunk, sp.n_splits,
+                                           m->part_o, m->part_ml, m->counters, m->attn, nullptr));
+            else
+                CUDA_TRY(launch_attn_prefill(lc, sd, max_keys, m->q, m->kvnew, c.n_heads, c.n_kv_heads, m->attn));
         } else {
             // decode: one new token per sequence; QK-norm, RoPE and the KV append run inside
             AttnFuse fz = {m->qkv, w_qn, w_kn, c.rms_eps, m->rcos, m->rsin,
@@ -668,24 +795,24 @@ static qw_status run_step(qw_model* m, qw_kv* kv, const StepDesc& sd, bool prefi
         }
         if (small) {
             PROF(QW_PROF_OPROJ);
-            CUDA_TRY(launch_gemv_resid(lc, T, m->attn, m->wo + (size_t)l * D * QD, D, QD, m->x));
+            CUDA_TRY(launch_gemv_resid(lc, T, m->attn, m->bo + (size_t)l * D * QD, D, QD, m->x));
         } else {
             PROF(QW_PROF_OPROJ);
             GemmArgs g = {};
             g.tmA = &m->tm_wo; g.tmA2 = &m->tm_wo; g.tmB = m->tm_attn;
             g.a_row0 = l * D; g.a2_row0 = g.a_row0; g.M = D; g.K = QD; g.T = T;
-            g.out_f32 = m->x; g.ld_out = D; g.status = m->status;
+            g.out_f32 = m->x; g.ld_out = D; g.status = m->status; g.part = m->gpart; g.part_bytes = kGemmPartBytes; g.tickets = m->gtick; g.max_tiles = kGemmMaxTiles; g.num_sms = m->num_sms;
             CUDA_TRY(launch_gemm_tc(lc, EPI_RESID_F32, g));
         }
         // --- feed-forward sublayer (Paso 6) ---
         if (small) {
             {
                 PROF(QW_PROF_GATEUP);
-                CUDA_TRY(launch_gemv_gateup(lc, T, m->x, w_post, c.rms_eps, m->wg + (size_t)l * I * D,
-                                            m->wu + (size_t)l * I * D, I, D, m->act));
+                CUDA_TRY(launch_gemv_gateup(lc, T, m->x, w_post, c.rms_eps, m->bg + (size_t)l * I * D,
+                                            m->bu + (size_t)l * I * D, I, D, m->act));
             }
             PROF(QW_PROF_DOWN);
-            CUDA_TRY(launch_gemv_resid(lc, T, m->act, m->wd + (size_t)l * D * I, D, I, m->x));
+            CUDA_TRY(launch_gemv_resid(lc, T, m->act, m->bd + (size_t)l * D * I, D, I, m->x));
         } else {
             {
                 PROF(QW_PROF_RMSNORM);
@@ -694,7 +821,7 @@ static qw_status run_step(qw_model* m, qw_kv* kv, const StepDesc& sd, bool prefi
             GemmArgs g = {};
             g.tmA = &m->tm_wg; g.tmA2 = &m->tm_wu; g.tmB = m->tm_h;
             g.a_row0 = l * I; g.a2_row0 = l * I; g.M = I; g.K = D; g.T = T;
-            g.out_h = m->act; g.ld_out = I; g.status = m->status;
+            g.out_h = m->act; g.ld_out = I; g.status = m->status; g.part = m->gpart; g.part_bytes = kGemmPartBytes; g.tickets = m->gtick; g.max_tiles = kGemmMaxTiles; g.num_sms = m->num_sms;
             {
                 PROF(QW_PROF_GATEUP);
                 CUDA_TRY(launch_gemm_tc(lc, EPI_SILU_MUL, g));
@@ -702,7 +829,7 @@ static qw_status run_step(qw_model* m, qw_kv* kv, const StepDesc& sd, bool prefi
             GemmArgs g2 = {};
             g2.tmA = &m->tm_wd; g2.tmA2 = &m->tm_wd; g2.tmB = m->tm_act;
             g2.a_row0 = l * D; g2.a2_row0 = g2.a_row0; g2.M = D; g2.K = I; g2.T = T;
-            g2.out_f32 = m->x; g2.ld_out = D; g2.status = m->status;
+            g2.out_f32 = m->x; g2.ld_out = D; g2.status = m->status; g2.part = m->gpart; g2.part_bytes = kGemmPartBytes; g2.tickets = m->gtick; g2.max_tiles = kGemmMaxTiles; g2.num_sms = m->num_sms;
             PROF(QW_PROF_DOWN);
             CUDA_TRY(launch_gemm_tc(lc, EPI_RESID_F32, g2));
         }
@@ -713,7 +840,7 @@ static qw_status run_step(qw_model* m, qw_kv* kv, const StepDesc& sd, bool prefi
     // --- final norm + tied LM head + greedy argmax (Paso 8) ---
     if (B <= kSmallT) {
         PROF(QW_PROF_LMHEAD);
-        CUDA_TRY(launch_gemv_lmhead(lc, B, m->x, m->last, m->fnorm, c.rms_eps, m->embed16, c.vocab, D, logits,
+        CUDA_TRY(launch_gemv_lmhead(lc, B, m->x, m->last, m->fnorm, c.rms_eps, m->embed, c.vocab, D, logits,
                                     m->best));
     } else {
         {
@@ -724,7 +851,7 @@ static qw_status run_step(qw_model* m, qw_kv* kv, const StepDesc& sd, bool prefi
         GemmArgs g = {};
         g.tmA = &m->tm_embed; g.tmA2 = &m->tm_embed; g.tmB = m->tm_h;
         g.a_row0 = 0; g.a2_row0 = 0; g.M = c.vocab; g.K = D; g.T = B;
-        g.logits = logits; g.ld_out = c.vocab; g.best = m->best; g.status = m->status;
+        g.logits = logits; g.ld_out = c.vocab; g.best = m->best; g.status = m->status; g.part = m->gpart; g.part_bytes = kGemmPartBytes; g.tickets = m->gtick; g.max_tiles = kGemmMaxTiles; g.num_sms = m->num_sms;
         CUDA_TRY(launch_gemm_tc(lc, EPI_ARGMAX, g));
     }
     CUDA_TRY(launch_finalize(lc, sd, m->best, next, kvv));
@@ -818,7 +945,9 @@ extern "C" qw_status qw_decode_step(qw_model* m, qw_kv* kv, int B, const int* se
         key.push_back((long long)(uintptr_t)kv);
         key.push_back(sp.chunk);
         key.push_back(m->prof_kind);
-        key.push_back(m->prof_kind ? (long long)m->prof_gen : 0);
+        key.push_back(m->use_mk ? 1 : 0);
+        key.push_back(m->pdl ? 1 : 0);
+        key.push_back(m->prof_kind || m->trace ? (long long)m->prof_gen : 0);
         for (int b = 0; b < B; ++b) key.push_back(seq_ids[b]);
         auto it = m->graphs.find(key);
         if (it == m->graphs.end()) {
@@ -895,6 +1024,7 @@ extern "C" qw_status qw_sync_status(qw_model* m, void* stream_) {
     int word = 0;
     CUDA_TRY(cudaMemcpy(&word, m->status, 4, cudaMemcpyDeviceToHost));
     CUDA_TRY(cudaMemset(m->status, 0, 4));
+    CUDA_TRY(cudaMemset(m->mk_sync, 0, 16));
     if (word & QW_DEV_BAD_TOKEN) return fail(QW_ERR_BAD_TOKEN, "a token id was outside [0, vocab)");
     if (word & QW_DEV_BAD_POS) return fail(QW_ERR_BAD_POS, "a position had no reserved page");
     if (word & QW_DEV_TIMEOUT) return fail(QW_ERR_TIMEOUT, "a bounded wait in a kernel timed out");

@@ -62,6 +62,7 @@ SIGNATURES = {
     "qw_kv_reserve": (_I, [_VP, _I, _I, _VP]),
     "qw_kv_reset": (_I, [_VP, _I, _VP]),
     "qw_kv_free_pages": (_I, [_VP]),
+    "qw_kv_truncate": (_I, [_VP, _I, _I, _VP]),
     "qw_kv_length": (_I, [_VP, _I]),
     "qw_prefill": (_I, [_VP, _VP, _I, _P(_I), _P(_I), _VP, _VP, _VP, _VP]),
     "qw_decode_step": (_I, [_VP, _VP, _I, _P(_I), _VP, _VP, _VP, _VP]),
@@ -77,6 +78,9 @@ SIGNATURES = {
     "qw_kv_fill_synthetic": (_I, [_VP, _I, _I, ctypes.c_uint64, _VP]),
     "qw_last_launch_count": (_I, [_VP]),
     "qw_profile_set": (_I, [_VP, _I, _P(_VP), _I]),
+    "qw_set_option": (_I, [_VP, _I, _I]),
+    "qw_trace_set": (_I, [_VP, _VP, _I]),
+    "qw_persistent_grid": (_I, [_VP]),
     "qw_lm_head_argmax_noalloc": (_I, [_VP, _I, _VP, _VP, _VP, _VP]),
 }
 
@@ -146,6 +150,10 @@ def qw_kv_reserve(kv: int, seq_id: int, total_tokens: int, stream=None) -> None:
 
 def qw_kv_reset(kv: int, seq_id: int, stream=None) -> None:
     _check(load().qw_kv_reset(kv, seq_id, _stream(stream)))
+
+
+def qw_kv_truncate(kv: int, seq_id: int, n_tokens: int, stream=None) -> None:
+    _check(load().qw_kv_truncate(kv, seq_id, n_tokens, _stream(stream)))
 
 
 def qw_kv_free_pages(kv: int) -> int:
@@ -227,6 +235,22 @@ def qw_lm_head_argmax_noalloc(model: int, B: int, x_ptr: int, logits_ptr: int, n
     """LM head + argmax over B residual rows with no device allocation (scratch is a static
     device array of QW_NOALLOC_MAX_ROWS keys); see include/qw.h."""
     _check(load().qw_lm_head_argmax_noalloc(model, B, x_ptr, logits_ptr or None, next_ptr, _stream(stream)))
+
+
+QW_OPT_PERSISTENT_DECODE = 1
+QW_OPT_PDL = 2
+
+
+def qw_set_option(model: int, option: int, value: int) -> None:
+    _check(load().qw_set_option(model, option, value))
+
+
+def qw_trace_set(model: int, buf_ptr: int, per_cta: int) -> None:
+    _check(load().qw_trace_set(model, buf_ptr or None, per_cta))
+
+
+def qw_persistent_grid(model: int) -> int:
+    return load().qw_persistent_grid(model)
 
 
 def qw_profile_set(model: int, kind: int, events, n_events: int) -> None:

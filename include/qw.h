@@ -130,6 +130,11 @@ qw_status qw_kv_reserve(qw_kv* kv, int seq_id, int total_tokens, void* stream);
 /* Free the pages of `seq_id` (-1: every sequence) and set its length to 0, on `stream`. */
 qw_status qw_kv_reset(qw_kv* kv, int seq_id, void* stream);
 
+/* Keep only the first n_tokens positions of sequence seq_id (n_tokens <= its length): the
+ * length goes back to n_tokens, the pages stay reserved, and later steps overwrite the
+ * dropped positions. Written on `stream`. */
+qw_status qw_kv_truncate(qw_kv* kv, int seq_id, int n_tokens, void* stream);
+
 int qw_kv_free_pages(const qw_kv* kv);
 int qw_kv_length(const qw_kv* kv, int seq_id); /* host mirror of the device length */
 
@@ -209,8 +214,31 @@ enum {
     QW_PROF_GATEUP = 5,   /* gate/up + SiLU*mul (RMSNorm fused on the small-batch path)   */
     QW_PROF_DOWN = 6,     /* down_proj + residual                                         */
     QW_PROF_LMHEAD = 7,   /* final norm + tied LM head + argmax                           */
-    QW_PROF_RMSNORM = 8   /* stand-alone RMSNorm (tensor-core path)                       */
+    QW_PROF_RMSNORM = 8,  /* stand-alone RMSNorm (tensor-core path)                       */
+    QW_PROF_STEP = 9      /* the persistent decode kernel (a whole decode step)           */
 };
+
+/* Options for qw_set_option. */
+enum {
+    /* 1: decode steps of <= 4 tokens run as one persistent cooperative kernel (needs one
+     * 416-thread CTA per SM); 0 (default): as one launch per layer phase. Both compute the
+     * same operations. */
+    QW_OPT_PERSISTENT_DECODE = 1,
+    /* 1 (default): consecutive launches use programmatic dependent launch. */
+    QW_OPT_PDL = 2
+};
+qw_status qw_set_option(qw_model* m, int option, int value);
+
+/* Inspection of the persistent decode kernel: when dev_buf is non-NULL (per_cta = n), every
+ * following persistent decode step writes %globaltimer values (ns, uint64) into the block
+ * B_c = dev_buf + c * 8n of each CTA c: B_c[2k], B_c[2k+1] = arrival / release of grid
+ * barrier k < n; B_c[2n + 2j], B_c[2n + 2j + 1] = start / end of the first consumer warp's
+ * wait for weight stage j < 2n; B_c[6n + j] = when the producer issued stage j < 2n.
+ * NULL turns it off. */
+qw_status qw_trace_set(qw_model* m, unsigned long long* dev_buf, int per_cta);
+
+/* CTAs of the persistent decode kernel (one per SM), 0 if unavailable. */
+int qw_persistent_grid(const qw_model* m);
 
 /* Bracket the j-th launch of kernel kind `kind` in every following prefill/decode call with
  * cudaEventRecord(events[2j]) before and cudaEventRecord(events[2j+1]) after it, on the

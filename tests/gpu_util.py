@@ -43,7 +43,7 @@ class Run:
     def _t(self, arr, dtype):
         return self.torch.tensor(np.asarray(arr), dtype=dtype, device="cuda")
 
-    def prefill(self, seq_ids, prompts, debug=True, logits=True, reserve_extra=0, reserve=True):
+    def prefill(self, seq_ids, prompts, debug=True, logits=True, reserve_extra=0, reserve=True, check=True):
         torch, qw, eng = self.torch, self.qw, self.eng
         lens = [len(p) for p in prompts]
         if reserve:
@@ -52,15 +52,16 @@ class Run:
         T = sum(lens)
         toks = self._t(np.concatenate([np.asarray(p, np.int32) for p in prompts]), torch.int32)
         return self._step(lambda lg, nx: qw.qw_prefill(eng.model, eng.kv, seq_ids, lens, toks.data_ptr(), lg, nx,
-                                                        eng.stream), len(seq_ids), T, debug, logits)
+                                                        eng.stream), len(seq_ids), T, debug, logits, check)
 
-    def decode(self, seq_ids, tokens, debug=True, logits=True):
+    def decode(self, seq_ids, tokens, debug=True, logits=True, check=True):
         torch, qw, eng = self.torch, self.qw, self.eng
         toks = self._t(np.asarray(tokens, np.int32), torch.int32)
         return self._step(lambda lg, nx: qw.qw_decode_step(eng.model, eng.kv, seq_ids, toks.data_ptr(), lg, nx,
-                                                            eng.stream), len(seq_ids), len(seq_ids), debug, logits)
+                                                            eng.stream), len(seq_ids), len(seq_ids), debug, logits,
+                          check)
 
-    def _step(self, call, B, T, debug, logits):
+    def _step(self, call, B, T, debug, logits, check=True):
         torch, qw, eng, s = self.torch, self.qw, self.eng, self.s
         lg = torch.empty((B, s.vocab), dtype=torch.float32, device="cuda") if logits else None
         nx = torch.full((B,), -7, dtype=torch.int32, device="cuda")
@@ -76,6 +77,8 @@ class Run:
             if debug:
                 qw.qw_debug_set(eng.model, 0, 0, 0)
         st = qw.qw_sync_status(eng.model, eng.stream)
+        if check:
+            assert st == 0, f"device status {st}: {qw.qw_last_error()}"
         out["status"] = st
         out["next"] = nx.cpu().numpy()
         if lg is not None:
