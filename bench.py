@@ -159,6 +159,9 @@ def step_bytes(s, B: int, ctx: float) -> float:
 KIND_NAMES = {1: "qkv_proj(rmsnorm fused)", 2: "qknorm_rope_append", 3: "attention", 4: "o_proj+residual",
               5: "gate_up+silu_mul(rmsnorm fused)", 6: "down_proj+residual", 7: "lm_head+argmax",
               9: "k_decode_mk (persistent decode step)"}
+# names on the tensor-core path (more than 8 token rows)
+TC_KIND_NAMES = {1: "qkv_proj+qk_norm+rope+kv_append", 3: "attention", 4: "o_proj+residual",
+                 5: "gate_up+silu_mul", 6: "down_proj+residual", 7: "lm_head+argmax", 8: "rmsnorm"}
 
 
 def run_ours(args, cfg, rank, world):
@@ -433,8 +436,8 @@ def run_other(args, cfg, rank, world):
     # per-kernel timing (events around each launch of a kind, one step after the timed region)
     L = s.n_layers
     kinds_n = {1: L, 3: L, 4: L, 5: L, 6: L, 7: 1}
-    if kind == "prefill":
-        kinds_n.update({2: L, 8: 2 * L + 1})
+    if (int(lens.sum()) if kind == "prefill" else B) > 8:
+        kinds_n[8] = 2 * L + 1  # tensor-core path: RMSNorm runs as its own kernel
     kinds = {}
     for kd, nl in kinds_n.items():
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * nl)]
@@ -452,7 +455,8 @@ def run_other(args, cfg, rank, world):
         st.synchronize()
         qw.qw_profile_set(eng.model, 0, None, 0)
         d = [evs[2 * j].elapsed_time(evs[2 * j + 1]) * 1e3 for j in range(nl)]
-        kinds[kd] = dict(name=KIND_NAMES.get(kd, "rmsnorm" if kd == 8 else str(kd)), avg_us=statistics.mean(d),
+        names = TC_KIND_NAMES if 8 in kinds_n else KIND_NAMES
+        kinds[kd] = dict(name=names.get(kd, str(kd)), avg_us=statistics.mean(d),
                          per_step_us=sum(d), launches=nl)
     T = int(lens.sum()) if kind == "prefill" else B
     D, I, QD, KD, V = s.hidden, s.inter, s.n_heads * s.head_dim, s.n_kv_heads * s.head_dim, s.vocab
@@ -589,10 +593,20 @@ def main():
     ap.add_argument("--persistent", action="store_true",
                     help="decode steps of <= 4 sequences as one persistent kernel")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--prompt-len", type=int, default=0,
+                    help="configs 2/3: tokens per sequence instead of the configured length (smaller case for profiling)")
+    ap.add_argument("--decode-steps", type=int, default=0,
+                    help="configs 2/4: decode steps per timed step instead of the configured count")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    cfg = CONFIGS[args.config]
+    cfg = dict(CONFIGS[args.config])
+    if args.prompt_len > 0 and args.config in (2, 3):
+        cfg["prompt"] = args.prompt_len
+        cfg["workload"] += f" [reduced: {args.prompt_len} tokens per sequence]"
+    if args.decode_steps > 0 and args.config in (2, 4):
+        cfg["n_decode"] = args.decode_steps
+        cfg["workload"] += f" [reduced: {args.decode_steps} decode steps]"
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":

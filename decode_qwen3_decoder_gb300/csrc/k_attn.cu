@@ -371,7 +371,9 @@ cudaError_t launch_attn_paged(const LaunchCtx& c, int T, int layer, const f16* q
 // of 16 rows) stream the sequence's K/V tiles of 64 keys through shared memory once.
 // S = Q K^T and O += P V use mma.sync m16n8k16 (fp16 operands, fp32 accumulation); the
 // online softmax runs in fp32 in the exp2 domain; P goes from the S accumulators straight
-// into the A fragments of P V. K/V tiles are double-buffered with cp.async; shared rows of
+// into the A fragments of P V. K/V tiles (the new keys were just appended to the paged
+// cache: key j sits at page_table[seq][j / 16], slot j % 16) are double-buffered with
+// cp.async; shared rows of
 // 256 bytes are XOR-swizzled by 16-byte chunk so ldmatrix is conflict-free. Key tiles past
 // the query tile are skipped; the diagonal tile is masked key > query.
 // =======================================================================================
@@ -414,7 +416,10 @@ __device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b
 struct PrefillP {
     StepDesc sd;
     const f16* q;       // [T][n_heads][128]
-    const f16* kv_new;  // [T][2][n_kv][128]
+    const f16* k;       // this layer's K pool [n_pages][n_kv][16][128]
+    const f16* v;
+    const int* page_table;
+    int max_pages_per_seq, n_pages;
     f16* out;           // [T][n_heads * 128]
     int n_heads, n_kv;
     float scale_log2;
@@ -434,7 +439,7 @@ __global__ void __launch_bounds__(PF_WARPS * 32) k_attn_prefill(const __grid_con
     if (q0 >= len) return;
     const int base = p.sd.start[b];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int KVD = p.n_kv * 128;
+    const int* pt = p.page_table + (size_t)p.sd.seq[b] * p.max_pages_per_seq;
 
     // ---- Q tile: rows 0..63 head 2g, rows 64..127 head 2g+1 ---------------------------
     for (int i = tid; i < 128 * 16; i += PF_WARPS * 32) {
@@ -446,13 +451,22 @@ __global__ void __launch_bounds__(PF_WARPS * 32) k_attn_prefill(const __grid_con
     }
     auto load_kv = [&](int kt, int buf) {
         const int k0 = kt * PF_KV;
-        for (int i = tid; i < PF_KV * 16; i += PF_WARPS * 32) {
-            const int row = i >> 4, ch = i & 15;
-            const int kj = k0 + row;
-            const bool v = kj < len;
-            const size_t tok = (size_t)(base + (v ? kj : 0));
-            cp_async16(sK + buf * PF_KV * 256 + swz(row, ch), p.kv_new + (tok * 2 + 0) * KVD + g * 128 + ch * 8, v);
-            cp_async16(sV + buf * PF_KV * 256 + swz(row, ch), p.kv_new + (tok * 2 + 1) * KVD + g * 128 + ch * 8, v);
+        // 256 threads x 4: pass j copies rows 16 j .. 16 j + 15 = page j of the tile
+        static_assert(PF_KV == 64 && PF_WARPS * 32 == 256, "one page per pass");
+        int page[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int pi = (k0 >> 4) + j;
+            page[j] = (pi * 16 < len && pi < p.max_pages_per_seq) ? pt[pi] : -1;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int row = (tid >> 4) + 16 * j, ch = tid & 15;
+            const int kj = k0 + row;  // key position (the sequence started empty)
+            const bool v = kj < len && page[j] >= 0 && page[j] < p.n_pages;  // bad pages were reported
+            const size_t off = (((size_t)(v ? page[j] : 0) * p.n_kv + g) * 16 + (kj & 15)) * 128 + ch * 8;
+            cp_async16(sK + buf * PF_KV * 256 + swz(row, ch), p.k + off, v);
+            cp_async16(sV + buf * PF_KV * 256 + swz(row, ch), p.v + off, v);
         }
     };
     const int n_kt = (min(len, q0 + PF_Q) + PF_KV - 1) / PF_KV;  // causal: keys < q0 + 64
@@ -583,12 +597,16 @@ __global__ void __launch_bounds__(PF_WARPS * 32) k_attn_prefill(const __grid_con
     }
 }
 
-cudaError_t launch_attn_prefill(const LaunchCtx& c, const StepDesc& sd, int max_len, const f16* q,
-                                const f16* kv_new, int n_heads, int n_kv, f16* out) {
+cudaError_t launch_attn_prefill(const LaunchCtx& c, const StepDesc& sd, int max_len, int layer, const f16* q,
+                                KVView kv, int n_heads, int n_kv, f16* out) {
     PrefillP p;
     p.sd = sd;
     p.q = q;
-    p.kv_new = kv_new;
+    p.k = kv.k + (size_t)layer * kv.layer_stride;
+    p.v = kv.v + (size_t)layer * kv.layer_stride;
+    p.page_table = kv.page_table;
+    p.max_pages_per_seq = kv.max_pages_per_seq;
+    p.n_pages = kv.n_pages;
     p.out = out;
     p.n_heads = n_heads;
     p.n_kv = n_kv;

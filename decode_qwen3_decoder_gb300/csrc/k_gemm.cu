@@ -3,21 +3,40 @@
 // token rows: prefill and batched decode.
 //
 // The product is computed transposed, D^T[m][t] = sum_k W[m][k] * H[t][k]: the weight tile
-// (128 output features) is the A operand and the token tile (BN = 64/128/256 rows) the B
+// (128 output rows) is the A operand and the token tile (BN = 64/128/256 rows) the B
 // operand, both K-major fp16 in shared memory with the 128-byte swizzle, fed by TMA
 // (cp.async.bulk.tensor) through an mbarrier ring. One elected thread issues
 // tcgen05.mma.cta_group::1.kind::f16 (M=128, N=BN, K=16, fp16 x fp16) into an fp32
-// accumulator in TMEM;
-// the four epilogue warps read it back with tcgen05.ld.32x32b (thread = output feature,
-// registers = tokens), so every store of a token row is a coalesced 32-feature run.
-// Epilogues: plain fp32 store (q|k|v), residual add into the fp32 stream (o_proj,
-// down_proj), SiLU(gate) * up from two accumulators fed by the gate and up tiles (SwiGLU),
-// and the LM head's per-token argmax (+ optional logits).
+// accumulator in TMEM; the four epilogue warps read it back with tcgen05.ld.32x32b
+// (thread = output row, registers = tokens).
 //
-// Split-K (gridDim.z > 1, used when the tiles alone would leave most SMs idle, e.g. batched
-// decode): each split accumulates a K range and writes its fp32 partial tile to a workspace;
-// the CTA that finishes last for the tile (an atomic ticket, no waiting) sums the splits in
-// fixed order, so results do not depend on timing, and applies the epilogue.
+// Epilogues:
+//   EPI_QKV_HEADS  one 128-row tile of the q|k|v projection is exactly one head: the tile
+//                  is staged through shared memory as [token][128] and each token's head
+//                  gets the per-head RMSNorm and the rotate-half RoPE (q and k heads, Pasos 4
+//                  and 5), then q is stored as fp16 [T][n_heads][128] and k / v are appended
+//                  (fp16) at the token's page slot of the KV cache.
+//   EPI_RESID_F32  x = x + W h (o_proj, down_proj): the residual rows of the next 32 tokens
+//                  are loaded while the current ones are added and stored.
+//   EPI_SILU_MUL   gate and up rows are packed interleaved, 64 gate rows then the same 64 up
+//                  rows per tile, so one M=128 MMA yields both; the epilogue stores
+//                  SiLU(gate) * up as fp16 (Paso 6).
+//   EPI_ARGMAX     the tied LM head: per-token packed argmax keys (+ optional logits).
+//
+// Two kernels share this machinery:
+//   k_gemm_tc  persistent (one CTA per SM walks the output tiles; the TMA ring runs across
+//              tiles; two TMEM accumulators let one tile's epilogue overlap the next tile's
+//              MMAs). Used when the tiles fill the GPU (prefill, LM head).
+//   k_gemm_cl  split-K over a thread-block cluster, one tile per cluster (batched decode,
+//              where a layer has too few tiles to occupy the SMs): CTA z of the cluster
+//              accumulates K range z, writes its fp32 partial for the token columns owned by
+//              CTA o straight into o's shared memory (distributed shared memory), and each
+//              CTA sums the partials of its own columns and applies the epilogue. Only the
+//              two cluster barriers order it; nothing goes through global memory.
+//
+// Programmatic dependent launch: weights never change during a step, so the producer
+// issues the weight tiles of the first ring stages before waiting for the previous kernel
+// (griddepcontrol.wait); activations, residuals and outputs are touched only after it.
 //
 // Every mbarrier wait is bounded: after ~2 s it sets QW_DEV_TIMEOUT in the status word and
 // the CTA skips the rest of its work, frees its TMEM and exits.
@@ -143,64 +162,251 @@ __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.
         "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])                \
         : "memory")
 
-template <int BN, int NA>
+
+__device__ __forceinline__ void named_bar_epi() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+}
+// address of the same shared variable in cluster CTA `rank`
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+constexpr int EP = 132;                   // pitch (floats) of the [token][128] staging tile
+constexpr int E_BYTES = 32 * EP * 4;      // 32 tokens
+constexpr int SMEM_BUDGET = 227 * 1024;
+
+template <int BN, int EPI>
 struct GemmCfg {
     static constexpr int A_BYTES = BM * BK * 2;  // 16 KB
     static constexpr int B_BYTES = BN * BK * 2;
-    static constexpr int STAGE_BYTES = NA * A_BYTES + B_BYTES;
-    static constexpr int ACC_COLS = NA * BN;                 // one accumulator buffer
-    static constexpr int NBUF = (2 * ACC_COLS <= 512) ? 2 : 1;
-    static constexpr int TMEM_RAW = NBUF * ACC_COLS;
-    static constexpr int TMEM_COLS = TMEM_RAW <= 32 ? 32 : TMEM_RAW <= 64 ? 64 : TMEM_RAW <= 128 ? 128
-                                   : TMEM_RAW <= 256 ? 256 : 512;
-    static constexpr int SBEST_BYTES = 4 * BN * 8;
-    static constexpr int STAGES_RAW = (200 * 1024 - SBEST_BYTES) / STAGE_BYTES;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int NBUF = (2 * BN <= 512) ? 2 : 1;
+    static constexpr int TMEM_COLS = NBUF * BN < 32 ? 32 : NBUF * BN;
+    static constexpr int SBEST_BYTES = (EPI == EPI_ARGMAX) ? 4 * BN * 8 : 0;
+    static constexpr int STAGE_E_BYTES = (EPI == EPI_QKV_HEADS || EPI == EPI_SILU_MUL) ? E_BYTES : 0;
+    static constexpr int NW_BYTES = (EPI == EPI_QKV_HEADS) ? 256 * 4 : 0;
+    static constexpr int META_BYTES = (EPI == EPI_QKV_HEADS) ? 2 * BN * 4 + 512 : 0;  // tpos, tdst, ssx
+    static constexpr int EXTRA = SBEST_BYTES + STAGE_E_BYTES + NW_BYTES + META_BYTES;
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int STAGES_RAW = (SMEM_BUDGET - 1024 - BAR_BYTES - EXTRA) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
-    static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + SBEST_BYTES + 512;
+    static constexpr int SMEM = 1024 + STAGES * STAGE_BYTES + EXTRA + BAR_BYTES;
 };
 
 struct GemmKParams {
-    int a_row0, a2_row0, K, T, ld_out;
-    int tiles_m, tiles_n, splits, units;
-    float* out_f32;
-    f16* out_h;
-    float* logits;
+    int a_row0, b_row0, K, T, ld_out;
+    int tiles_m, tiles_n, units, splits;
+    float* out_f32;  // EPI_RESID_F32: x [T][ld_out]
+    f16* out_h;      // EPI_SILU_MUL: act [T][ld_out]
+    float* logits;   // EPI_ARGMAX: optional [T][ld_out]
     unsigned long long* best;
     int* status;
-    float* part;   // split-K partial tiles [tile][split][NA*BN][128]
-    int* tickets;  // split-K arrival counter per tile
+    // EPI_QKV_HEADS
+    f16* q_out;
+    const bf16* q_norm;
+    const bf16* k_norm;
+    float eps;
+    const float* rope_cos;
+    const float* rope_sin;
+    TokView tv;
+    KVView kv;
+    int layer, n_heads, n_kv;
+    int32_t* dbg_pos;
+    int32_t* dbg_slot;
 };
+
+// ---- epilogues over a staged [token][EP] fp32 tile (128 epilogue threads) -------------
+
+// Token metadata of a q|k|v tile, filled while its MMAs run: tpos[c] = position of token
+// n0 + c, tdst[c] = its KV slot row page * 16 + pos % 16 (-1: no page; reported).
+template <int BN>
+__device__ void fill_tok_meta(const GemmKParams& p, int n0, int hd, int* tpos, int* tdst) {
+    for (int c = threadIdx.x; c < BN; c += 128) {
+        const int tok = n0 + c;
+        int pos = 0, dst = -1;
+        if (tok < p.T) {
+            pos = p.tv.pos[tok];
+            const int seq = p.tv.seq[tok];
+            const int pi = pos >> 4;
+            const int page = (pi < p.kv.max_pages_per_seq) ? p.kv.page_table[(size_t)seq * p.kv.max_pages_per_seq + pi] : -1;
+            if (page >= 0 && page < p.kv.n_pages) {
+                dst = page * 16 + (pos & 15);
+            } else if (hd >= p.n_heads) {
+                atomicOr(p.status, QW_DEV_BAD_POS);
+            }
+            if (p.dbg_pos && hd == p.n_heads) {
+                p.dbg_pos[tok] = pos;
+                p.dbg_slot[tok] = dst;
+            }
+        }
+        tpos[c] = pos;
+        tdst[c] = dst;
+    }
+}
+
+// Epilogue thread layout over a staged chunk of 32 tokens: lane = token t of the chunk,
+// warp q = the dims [16q, 16q + 16) of the head and their rotate-half partners 64 + 16q ..
+// (for SwiGLU: gate features [16q, 16q + 16) and the matching up rows). Shared-memory rows
+// have a pitch of 132 floats, so the 16-byte reads of 8 consecutive lanes hit distinct banks;
+// every store is a whole 32-byte sector.
+
+// RoPE cos/sin of this thread's 16 dims for its token (tpos[cbase + lane]).
+struct RopeRegs {
+    float4 c[4], s[4];
+};
+__device__ __forceinline__ void load_rope(const GemmKParams& p, const int* tpos, int cbase, int ntok, RopeRegs& rr) {
+    const int lane = threadIdx.x & 31, q = threadIdx.x >> 5;
+    const int pos = lane < ntok ? tpos[cbase + lane] : 0;
+    const float4* cs = reinterpret_cast<const float4*>(p.rope_cos + (size_t)pos * 64 + 16 * q);
+    const float4* sn = reinterpret_cast<const float4*>(p.rope_sin + (size_t)pos * 64 + 16 * q);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        rr.c[k] = __ldg(cs + k);
+        rr.s[k] = __ldg(sn + k);
+    }
+}
+
+__device__ __forceinline__ void store16h(f16* dst, const float* v) {  // 16 values -> 32 bytes
+    uint4 a, b;
+    a.x = pack_h2(v[0], v[1]);
+    a.y = pack_h2(v[2], v[3]);
+    a.z = pack_h2(v[4], v[5]);
+    a.w = pack_h2(v[6], v[7]);
+    b.x = pack_h2(v[8], v[9]);
+    b.y = pack_h2(v[10], v[11]);
+    b.z = pack_h2(v[12], v[13]);
+    b.w = pack_h2(v[14], v[15]);
+    reinterpret_cast<uint4*>(dst)[0] = a;
+    reinterpret_cast<uint4*>(dst)[1] = b;
+}
+
+// q|k|v head tile `hd`, tokens tok0 .. tok0 + ntok - 1 (tile columns cbase ..). q and k
+// heads: RMSNorm over the head's 128 dims with the shared weight (partial sums of the four
+// quarters meet in ssx), then the rotation by pos * theta^(-i/64); v heads: copied.
+__device__ void epi_heads(const GemmKParams& p, const float* E, const float* nws, const int* tdst, float* ssx,
+                          const RopeRegs& rr, int tok0, int cbase, int ntok, int hd) {
+    const int t = threadIdx.x & 31, q = threadIdx.x >> 5;
+    const bool isq = hd < p.n_heads;
+    const bool isv = hd >= p.n_heads + p.n_kv;
+    const float* row = E + t * EP;
+    float a[16], b[16];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float4 va = *reinterpret_cast<const float4*>(row + 16 * q + 4 * k);
+        const float4 vb = *reinterpret_cast<const float4*>(row + 64 + 16 * q + 4 * k);
+        a[4 * k] = va.x; a[4 * k + 1] = va.y; a[4 * k + 2] = va.z; a[4 * k + 3] = va.w;
+        b[4 * k] = vb.x; b[4 * k + 1] = vb.y; b[4 * k + 2] = vb.z; b[4 * k + 3] = vb.w;
+    }
+    if (!isv) {
+        float ss = 0.f;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) ss = fmaf(a[k], a[k], fmaf(b[k], b[k], ss));
+        ssx[q * 32 + t] = ss;
+        named_bar_epi();
+        ss = ssx[t] + ssx[32 + t] + ssx[64 + t] + ssx[96 + t];
+        const float r = rsqrtf(ss * (1.0f / 128.0f) + p.eps);
+        const float* w = nws + (isq ? 0 : 128) + 16 * q;
+        const float c[16] = {rr.c[0].x, rr.c[0].y, rr.c[0].z, rr.c[0].w, rr.c[1].x, rr.c[1].y, rr.c[1].z, rr.c[1].w,
+                             rr.c[2].x, rr.c[2].y, rr.c[2].z, rr.c[2].w, rr.c[3].x, rr.c[3].y, rr.c[3].z, rr.c[3].w};
+        const float sn[16] = {rr.s[0].x, rr.s[0].y, rr.s[0].z, rr.s[0].w, rr.s[1].x, rr.s[1].y, rr.s[1].z, rr.s[1].w,
+                              rr.s[2].x, rr.s[2].y, rr.s[2].z, rr.s[2].w, rr.s[3].x, rr.s[3].y, rr.s[3].z, rr.s[3].w};
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const float ya = a[k] * r * w[k], yb = b[k] * r * w[64 + k];
+            a[k] = ya * c[k] - yb * sn[k];
+            b[k] = yb * c[k] + ya * sn[k];
+        }
+    }
+    if (t >= ntok) return;
+    f16* dst;
+    if (isq) {
+        dst = p.q_out + ((size_t)(tok0 + t) * p.n_heads + hd) * 128;
+    } else {
+        const int slot = tdst[cbase + t];
+        if (slot < 0) return;
+        const int g = hd - p.n_heads - (isv ? p.n_kv : 0);
+        dst = (isv ? p.kv.v : p.kv.k) + (size_t)p.layer * p.kv.layer_stride +
+              (((size_t)(slot >> 4) * p.n_kv + g) * 16 + (slot & 15)) * 128;
+    }
+    store16h(dst + 16 * q, a);
+    store16h(dst + 64 + 16 * q, b);
+}
+
+// interleaved gate/up tile `tile` (gate rows 0..63, up rows 64..127 of output features
+// 64 tile .. 64 tile + 63): act = SiLU(gate) * up.
+__device__ void epi_silu(const GemmKParams& p, const float* E, int tok0, int ntok, int tile) {
+    const int t = threadIdx.x & 31, q = threadIdx.x >> 5;
+    if (t >= ntok) return;
+    const float* row = E + t * EP;
+    float v[16];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float4 g = *reinterpret_cast<const float4*>(row + 16 * q + 4 * k);
+        const float4 u = *reinterpret_cast<const float4*>(row + 64 + 16 * q + 4 * k);
+        v[4 * k] = g.x / (1.0f + expf(-g.x)) * u.x;
+        v[4 * k + 1] = g.y / (1.0f + expf(-g.y)) * u.y;
+        v[4 * k + 2] = g.z / (1.0f + expf(-g.z)) * u.z;
+        v[4 * k + 3] = g.w / (1.0f + expf(-g.w)) * u.w;
+    }
+    store16h(p.out_h + (size_t)(tok0 + t) * p.ld_out + tile * 64 + 16 * q, v);
+}
+
+// fp32 residual x[tok0 + j][f], j < 32 (0 past the last token)
+__device__ __forceinline__ void load_resid(const GemmKParams& p, int tok0, int f, float* xr) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) xr[j] = (tok0 + j < p.T) ? __ldcg(p.out_f32 + (size_t)(tok0 + j) * p.ld_out + f) : 0.f;
+}
+
+__device__ __forceinline__ void load_norm_weights(const GemmKParams& p, float* nws) {
+    for (int i = threadIdx.x; i < 256; i += 128) nws[i] = __bfloat162float(i < 128 ? p.q_norm[i] : p.k_norm[i - 128]);
+}
 
 }  // namespace
 
-// Persistent: CTA b processes work units u = b, b + gridDim.x, ...; a unit is an output tile
-// (128 features x BN tokens) and, with split-K, one K range of it. The TMA ring runs across
-// units without draining; two TMEM accumulator buffers let the epilogue of one unit overlap
-// the MMAs of the next. The epilogue warps hand a buffer to the MMA warp (barrier acce) only
-// when it is ready for the unit that will use it: for the residual epilogue that means the
-// fp32 residual tile x was loaded into it (tcgen05.st), so the MMAs compute x + W h and the
-// epilogue only stores; the loads of x overlap the other buffer's MMAs.
+// =======================================================================================
+// Persistent kernel: CTA b processes tiles u = b, b + gridDim.x, ...
+// =======================================================================================
 template <int BN, int EPI>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
-    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
-              const __grid_constant__ CUtensorMap tmB, GemmKParams p) {
-    constexpr int NA = (EPI == EPI_SILU_MUL) ? 2 : 1;
-    using C = GemmCfg<BN, NA>;
+    k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmKParams p) {
+    using C = GemmCfg<BN, EPI>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    unsigned long long* sbest = reinterpret_cast<unsigned long long*>(smem + C::STAGES * C::STAGE_BYTES);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES + C::SBEST_BYTES);
+    uint8_t* extra = smem + C::STAGES * C::STAGE_BYTES;
+    unsigned long long* sbest = reinterpret_cast<unsigned long long*>(extra);
+    float* E = reinterpret_cast<float*>(extra + C::SBEST_BYTES);
+    float* nws = reinterpret_cast<float*>(extra + C::SBEST_BYTES + C::STAGE_E_BYTES);
+    int* tpos = reinterpret_cast<int*>(extra + C::SBEST_BYTES + C::STAGE_E_BYTES + C::NW_BYTES);
+    int* tdst = tpos + BN;
+    float* ssx = reinterpret_cast<float*>(tdst + BN);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(extra + C::EXTRA);
     uint64_t* full = bars;
     uint64_t* empty = bars + C::STAGES;
     uint64_t* accf = bars + 2 * C::STAGES;      // [2] accumulator ready
-    uint64_t* acce = bars + 2 * C::STAGES + 2;  // [2] accumulator drained
+    uint64_t* acce = bars + 2 * C::STAGES + 2;  // [2] accumulator free
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 4);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
-    volatile int* ep_fail = reinterpret_cast<volatile int*>(tmem_slot + 3);
+    volatile int* ep_fail = reinterpret_cast<volatile int*>(tmem_slot + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int nk_all = p.K / BK;
+    const int nk = p.K / BK;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
@@ -209,7 +415,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(accf + b), 1);
-            mbar_init(smem_u32(acce + b), 4);  // one arrival per epilogue warp: buffer ready
+            mbar_init(smem_u32(acce + b), 4);  // one arrival per epilogue warp
         }
         *abort_flag = 0;
         *ep_fail = 0;
@@ -218,7 +424,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
     if (warp == 4 && lane == 0) {
         tma_prefetch_desc(&tmA);
-        if (NA == 2) tma_prefetch_desc(&tmA2);
         tma_prefetch_desc(&tmB);
     }
     if (warp == 5) {
@@ -231,35 +436,53 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    pdl_wait();
+    pdl_launch();
 
-    auto unit_of = [&](int u, int& tm, int& tn, int& kb0, int& kb1) {
-        const int z = u % p.splits, rest = u / p.splits;
-        tm = rest % p.tiles_m;
-        tn = rest / p.tiles_m;
-        kb0 = (nk_all * z) / p.splits;
-        kb1 = (nk_all * (z + 1)) / p.splits;
+    auto tile_of = [&](int u, int& tm, int& tn) {
+        tm = u % p.tiles_m;
+        tn = u / p.tiles_m;
     };
 
     if (warp == 4) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
+            // weight tiles of the first ring stages before the dependency wait
+            int pre = 0;
+            {
+                int u = blockIdx.x, kb = 0;
+                while (pre < C::STAGES && u < p.units) {
+                    int tm, tn;
+                    tile_of(u, tm, tn);
+                    const uint32_t st = smem_u32(smem + pre * C::STAGE_BYTES);
+                    mbar_expect_tx(smem_u32(full + pre), C::STAGE_BYTES);
+                    tma_load_2d(st, &tmA, smem_u32(full + pre), kb * BK, p.a_row0 + tm * BM);
+                    ++pre;
+                    if (++kb == nk) {
+                        kb = 0;
+                        u += gridDim.x;
+                    }
+                }
+            }
+            pdl_wait();
             uint32_t g = 0;
             for (int u = blockIdx.x; u < p.units && !*abort_flag; u += gridDim.x) {
-                int tm, tn, kb0, kb1;
-                unit_of(u, tm, tn, kb0, kb1);
-                for (int kb = kb0; kb < kb1; ++kb, ++g) {
+                int tm, tn;
+                tile_of(u, tm, tn);
+                for (int kb = 0; kb < nk; ++kb, ++g) {
                     const int s = g % C::STAGES;
+                    const uint32_t st = smem_u32(smem + s * C::STAGE_BYTES);
+                    if ((int)g < pre) {  // weights already in flight
+                        tma_load_2d(st + C::A_BYTES, &tmB, smem_u32(full + s), kb * BK, p.b_row0 + tn * BN);
+                        continue;
+                    }
                     const uint32_t ph = (g / C::STAGES) & 1u;
                     if (!mbar_wait(smem_u32(empty + s), ph ^ 1u, abort_flag)) {
                         *abort_flag = 1;
                         break;
                     }
-                    const uint32_t st = smem_u32(smem + s * C::STAGE_BYTES);
                     mbar_expect_tx(smem_u32(full + s), C::STAGE_BYTES);
                     tma_load_2d(st, &tmA, smem_u32(full + s), kb * BK, p.a_row0 + tm * BM);
-                    if (NA == 2) tma_load_2d(st + C::A_BYTES, &tmA2, smem_u32(full + s), kb * BK, p.a2_row0 + tm * BM);
-                    tma_load_2d(st + NA * C::A_BYTES, &tmB, smem_u32(full + s), kb * BK, tn * BN);
+                    tma_load_2d(st + C::A_BYTES, &tmB, smem_u32(full + s), kb * BK, p.b_row0 + tn * BN);
                 }
             }
         }
@@ -270,8 +493,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             uint32_t g = 0;
             int i = 0;
             for (int u = blockIdx.x; u < p.units && !*abort_flag; u += gridDim.x, ++i) {
-                int tm, tn, kb0, kb1;
-                unit_of(u, tm, tn, kb0, kb1);
                 const int buf = i % C::NBUF;
                 const uint32_t use = (uint32_t)(i / C::NBUF);
                 if (!mbar_wait(smem_u32(acce + buf), use & 1u, abort_flag)) {
@@ -279,11 +500,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d = tmem + buf * C::ACC_COLS;
-                // the residual tile already sits in the accumulator of split 0
-                const bool from_c = (EPI == EPI_RESID_F32) && (u % p.splits == 0);
+                const uint32_t d = tmem + buf * BN;
                 bool ok = true;
-                for (int kb = kb0; kb < kb1; ++kb, ++g) {
+                for (int kb = 0; kb < nk; ++kb, ++g) {
                     const int s = g % C::STAGES;
                     const uint32_t ph = (g / C::STAGES) & 1u;
                     if (!mbar_wait(smem_u32(full + s), ph, abort_flag)) {
@@ -294,16 +513,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     tc_fence_after();
                     const uint32_t st = smem_u32(smem + s * C::STAGE_BYTES);
                     const uint64_t ad = sw128_desc(st);
-                    const uint64_t bd = sw128_desc(st + NA * C::A_BYTES);
+                    const uint64_t bd = sw128_desc(st + C::A_BYTES);
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k) {
-                        const uint32_t acc = (kb > kb0 || k > 0 || from_c) ? 1u : 0u;
-                        umma_f16(d, ad + 2 * k, bd + 2 * k, idesc, acc);
-                        if (NA == 2) {
-                            const uint64_t a2 = sw128_desc(st + C::A_BYTES);
-                            umma_f16(d + BN, a2 + 2 * k, bd + 2 * k, idesc, acc);
-                        }
-                    }
+                    for (int k = 0; k < BK / 16; ++k)
+                        umma_f16(d, ad + 2 * k, bd + 2 * k, idesc, (kb > 0 || k > 0) ? 1u : 0u);
                     umma_commit(smem_u32(empty + s));  // frees the stage once these MMAs finish
                 }
                 if (!ok) break;
@@ -312,44 +525,32 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         }
     } else {
         // ---------------- epilogue warps 0-3: TMEM lanes 32w .. 32w+31 ----------------
-        // Make buffer (i % NBUF) ready for this CTA's i-th unit and hand it to the MMA warp.
+        if (EPI == EPI_QKV_HEADS) load_norm_weights(p, nws);  // weights: before the wait
+        // hand buffer (i2 % NBUF) to the MMA warp for this CTA's i2-th tile
         auto prepare = [&](int i2) {
             const int u2 = blockIdx.x + i2 * gridDim.x;
             if (u2 >= p.units) return;
-            const int buf2 = i2 % C::NBUF;
-            if (EPI == EPI_RESID_F32 && u2 % p.splits == 0) {
-                int tm2, tn2, a0, a1;
-                unit_of(u2, tm2, tn2, a0, a1);
-                const int n02 = tn2 * BN;
-                const int f2 = tm2 * BM + warp * 32 + lane;
-                const uint32_t trow2 = tmem + buf2 * C::ACC_COLS + ((uint32_t)(warp * 32) << 16);
-                for (int c0 = 0; c0 < BN; c0 += 32) {
-                    uint32_t r[32];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int tok = n02 + c0 + j;
-                        r[j] = tok < p.T ? __float_as_uint(__ldcg(p.out_f32 + (size_t)tok * p.ld_out + f2)) : 0u;
-                    }
-                    TMEM_ST32(trow2 + c0, r);
-                }
-                tmem_wait_st();
-            }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(acce + buf2)) : "memory");
+            if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(acce + (i2 % C::NBUF))) : "memory");
         };
-        for (int i2 = 0; i2 < C::NBUF; ++i2) prepare(i2);
+        for (int i2 = 0; i2 < C::NBUF; ++i2) prepare(i2);  // nothing to read: before the wait
+        pdl_wait();
+        if (EPI == EPI_QKV_HEADS) named_bar_epi();  // norm weights visible
         int i = 0;
         for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++i) {
-            int tm, tn, kb0, kb1;
-            unit_of(u, tm, tn, kb0, kb1);
+            int tm, tn;
+            tile_of(u, tm, tn);
             const int buf = i % C::NBUF;
             const uint32_t use = (uint32_t)(i / C::NBUF);
+            if (EPI == EPI_QKV_HEADS) fill_tok_meta<BN>(p, tn * BN, tm, tpos, tdst);  // overlaps the MMAs
+            float xr[32];  // EPI_RESID_F32: residual rows of the current 32 tokens
+            if (EPI == EPI_RESID_F32) load_resid(p, tn * BN, tm * BM + warp * 32 + lane, xr);
             // all four epilogue warps take the same decision (they meet at named barriers)
             if (!mbar_wait(smem_u32(accf + buf), use & 1u, abort_flag)) *ep_fail = 1;
-            asm volatile("bar.sync 1, 128;" ::: "memory");
+            named_bar_epi();
             const bool ok = (*ep_fail == 0);
-            asm volatile("bar.sync 1, 128;" ::: "memory");
+            named_bar_epi();
             tc_fence_after();
             if (!ok) {
                 if (threadIdx.x == 0) atomicOr(p.status, QW_DEV_TIMEOUT);
@@ -357,106 +558,64 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
             const int n0 = tn * BN;
             const int ncols = min(BN, ((p.T - n0) + 31) / 32 * 32);  // token columns holding data
-            const int f = tm * BM + warp * 32 + lane;  // output feature of this thread
-            const uint32_t trow = tmem + buf * C::ACC_COLS + ((uint32_t)(warp * 32) << 16);
-            auto release_tmem = [&]() { prepare(i + C::NBUF); };  // this buffer's next unit
-            // epilogue of 32 token columns c0.. for this thread's feature: v = accumulator,
-            // u = second accumulator (up projection) for SiLU * mul
-            auto apply = [&](int c0, const float* v, const float* w) {
-                if (EPI == EPI_SILU_MUL) {
+            const int fl = warp * 32 + lane;                           // tile row of this thread
+            const uint32_t trow = tmem + buf * BN + ((uint32_t)(warp * 32) << 16);
+            const bool rope = (EPI == EPI_QKV_HEADS) && tm < p.n_heads + p.n_kv;
+            RopeRegs rr_cur, rr_nxt;
+            if (rope) load_rope(p, tpos, 0, min(32, p.T - n0), rr_cur);
+            for (int c0 = 0; c0 < ncols; c0 += 32) {
+                uint32_t r[32];
+                TMEM_LD32(trow + c0, r);
+                tmem_wait_ld();
+                if (c0 + 32 >= ncols) prepare(i + C::NBUF);  // this buffer's next tile
+                if (EPI == EPI_QKV_HEADS || EPI == EPI_SILU_MUL) {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int tok = n0 + c0 + j;
-                        if (tok < p.T) p.out_h[(size_t)tok * p.ld_out + f] = __float2half_rn(v[j] / (1.0f + expf(-v[j])) * w[j]);
+                    for (int j = 0; j < 32; ++j) E[j * EP + fl] = __uint_as_float(r[j]);
+                    named_bar_epi();
+                    const int ntok = min(32, p.T - (n0 + c0));
+                    if (EPI == EPI_QKV_HEADS) {
+                        // the next chunk's RoPE rows are in flight while this chunk is processed
+                        if (rope && c0 + 32 < ncols) load_rope(p, tpos, c0 + 32, min(32, p.T - (n0 + c0 + 32)), rr_nxt);
+                        epi_heads(p, E, nws, tdst, ssx, rr_cur, n0 + c0, c0, ntok, tm);
+                        rr_cur = rr_nxt;
+                    } else {
+                        epi_silu(p, E, n0 + c0, ntok, tm);
                     }
-                } else if (EPI == EPI_STORE_F32) {
+                    named_bar_epi();  // E is refilled by the next chunk
+                } else if (EPI == EPI_RESID_F32) {
+                    const int f = tm * BM + fl;
+                    float xn[32];
+                    if (c0 + 32 < ncols) load_resid(p, n0 + c0 + 32, f, xn);
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const int tok = n0 + c0 + j;
-                        if (tok < p.T) p.out_f32[(size_t)tok * p.ld_out + f] = v[j];
+                        if (tok < p.T) p.out_f32[(size_t)tok * p.ld_out + f] = __uint_as_float(r[j]) + xr[j];
                     }
-                } else if (EPI == EPI_RESID_F32) {  // the accumulator already includes x
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) xr[j] = xn[j];
+                } else {  // EPI_ARGMAX
+                    const int f = tm * BM + fl;
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const int tok = n0 + c0 + j;
-                        if (tok < p.T) p.out_f32[(size_t)tok * p.ld_out + f] = v[j];
-                    }
-                } else {  // EPI_ARGMAX (never split)
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int tok = n0 + c0 + j;
-                        if (p.logits && tok < p.T) p.logits[(size_t)tok * p.ld_out + f] = v[j];
-                        const unsigned long long key = warp_max_u64(argmax_key(v[j], f));
+                        const float v = __uint_as_float(r[j]);
+                        if (p.logits && tok < p.T) p.logits[(size_t)tok * p.ld_out + f] = v;
+                        const unsigned long long key = warp_max_u64(argmax_key(v, f));
                         if (lane == 0) sbest[warp * BN + c0 + j] = key;
                     }
                 }
-            };
-            if (p.splits == 1) {
-                for (int c0 = 0; c0 < ncols; c0 += 32) {
-                    uint32_t r[32], uu[32];
-                    TMEM_LD32(trow + c0, r);
-                    if (NA == 2) TMEM_LD32(trow + BN + c0, uu);
-                    tmem_wait_ld();
-                    if (c0 + 32 >= ncols) release_tmem();
-                    float v[32], w[32];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        v[j] = __uint_as_float(r[j]);
-                        w[j] = NA == 2 ? __uint_as_float(uu[j]) : 0.f;
-                    }
-                    apply(c0, v, w);
-                }
-                if (EPI == EPI_ARGMAX) {
-                    asm volatile("bar.sync 1, 128;" ::: "memory");
-                    for (int cc = threadIdx.x; cc < ncols; cc += 128) {
-                        const int tok = n0 + cc;
-                        if (tok < p.T) {
-                            unsigned long long bb = sbest[cc];
-                            for (int w2 = 1; w2 < 4; ++w2) bb = u64_max(bb, sbest[w2 * BN + cc]);
-                            atomicMax(p.best + tok, bb);
-                        }
-                    }
-                    asm volatile("bar.sync 1, 128;" ::: "memory");
-                }
-            } else {
-                const int z = u % p.splits;
-                const int tile = tn * p.tiles_m + tm;
-                float* mine = p.part + ((size_t)tile * p.splits + z) * (NA * BN) * BM;
-                for (int h = 0; h < NA; ++h) {
-                    for (int c0 = 0; c0 < ncols; c0 += 32) {
-                        uint32_t r[32];
-                        TMEM_LD32(trow + h * BN + c0, r);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int j = 0; j < 32; ++j)
-                            __stcg(mine + (size_t)(h * BN + c0 + j) * BM + warp * 32 + lane, __uint_as_float(r[j]));
+            }
+            if (EPI == EPI_ARGMAX) {
+                named_bar_epi();
+                for (int cc = threadIdx.x; cc < ncols; cc += 128) {
+                    const int tok = n0 + cc;
+                    if (tok < p.T) {
+                        unsigned long long bb = sbest[cc];
+                        for (int w2 = 1; w2 < 4; ++w2) bb = u64_max(bb, sbest[w2 * BN + cc]);
+                        atomicMax(p.best + tok, bb);
                     }
                 }
-                release_tmem();
-                __threadfence();
-                asm volatile("bar.sync 1, 128;" ::: "memory");
-                if (threadIdx.x == 0) *last_flag = (atomicAdd(p.tickets + tile, 1) == p.splits - 1);
-                asm volatile("bar.sync 1, 128;" ::: "memory");
-                if (*last_flag) {
-                    __threadfence();
-                    const float* base = p.part + (size_t)tile * p.splits * (NA * BN) * BM + warp * 32 + lane;
-                    for (int c0 = 0; c0 < ncols; c0 += 32) {
-                        float v[32], w[32];
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] = w[j] = 0.f;
-                        for (int zz = 0; zz < p.splits; ++zz) {
-                            const float* src = base + (size_t)zz * (NA * BN) * BM;
-#pragma unroll
-                            for (int j = 0; j < 32; ++j) {
-                                v[j] += __ldcg(src + (size_t)(c0 + j) * BM);
-                                if (NA == 2) w[j] += __ldcg(src + (size_t)(BN + c0 + j) * BM);
-                            }
-                        }
-                        apply(c0, v, w);
-                    }
-                    if (threadIdx.x == 0) p.tickets[tile] = 0;
-                }
-                asm volatile("bar.sync 1, 128;" ::: "memory");  // last_flag is reused by the next unit
+                named_bar_epi();
             }
         }
     }
@@ -469,28 +628,218 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS)
                      : "memory");
     }
+}
+
+// =======================================================================================
+// Cluster split-K kernel: cluster c = one output tile, CTA rank z = K range z.
+// =======================================================================================
+template <int BN, int EPI>
+__global__ void __launch_bounds__(GEMM_THREADS, 1)
+    k_gemm_cl(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmKParams p) {
+    using C = GemmCfg<BN, EPI>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t* extra = smem + C::STAGES * C::STAGE_BYTES;
+    float* E = reinterpret_cast<float*>(extra + C::SBEST_BYTES);
+    float* nws = reinterpret_cast<float*>(extra + C::SBEST_BYTES + C::STAGE_E_BYTES);
+    int* tpos = reinterpret_cast<int*>(extra + C::SBEST_BYTES + C::STAGE_E_BYTES + C::NW_BYTES);
+    int* tdst = tpos + BN;
+    float* ssx = reinterpret_cast<float*>(tdst + BN);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(extra + C::EXTRA);
+    uint64_t* full = bars;
+    uint64_t* empty = bars + C::STAGES;
+    uint64_t* accf = bars + 2 * C::STAGES;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 2);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* ep_fail = reinterpret_cast<volatile int*>(tmem_slot + 2);
+    // partial sums received from the cluster: [split][owned column][128 rows] fp32, over the
+    // stage ring (free once every CTA of the cluster has finished its MMAs)
+    float* red = reinterpret_cast<float*>(smem);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int S = p.splits;
+    const int z = (int)cluster_rank();
+    const int tile = (int)cluster_id_x();
+    const int tm = tile % p.tiles_m, tn = tile / p.tiles_m;
+    const int nk_all = p.K / BK;
+    const int kb0 = (nk_all * z) / S, kb1 = (nk_all * (z + 1)) / S;
+    const int nk = kb1 - kb0;
+    const int WMAX = (BN + S - 1) / S;
+    const int n0 = tn * BN;
+    float xr0[32];  // EPI_RESID_F32: residual rows of the first 32 owned columns (epilogue warps)
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(smem_u32(full + s), 1);
+            mbar_init(smem_u32(empty + s), 1);
+        }
+        mbar_init(smem_u32(accf), 1);
+        *abort_flag = 0;
+        *ep_fail = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 4 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 5) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(C::TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
     pdl_launch();
+
+    if (warp == 4) {
+        if (lane == 0) {
+            const int pre = min(nk, C::STAGES);
+            for (int j = 0; j < pre; ++j) {  // weights first: they do not depend on the previous kernel
+                mbar_expect_tx(smem_u32(full + j), C::STAGE_BYTES);
+                tma_load_2d(smem_u32(smem + j * C::STAGE_BYTES), &tmA, smem_u32(full + j), (kb0 + j) * BK,
+                            p.a_row0 + tm * BM);
+            }
+            pdl_wait();
+            for (int j = 0; j < pre; ++j)
+                tma_load_2d(smem_u32(smem + j * C::STAGE_BYTES) + C::A_BYTES, &tmB, smem_u32(full + j), (kb0 + j) * BK,
+                            p.b_row0 + n0);
+            for (int j = pre; j < nk; ++j) {
+                const int s = j % C::STAGES;
+                const uint32_t ph = (j / C::STAGES) & 1u;
+                if (!mbar_wait(smem_u32(empty + s), ph ^ 1u, abort_flag)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                const uint32_t st = smem_u32(smem + s * C::STAGE_BYTES);
+                mbar_expect_tx(smem_u32(full + s), C::STAGE_BYTES);
+                tma_load_2d(st, &tmA, smem_u32(full + s), (kb0 + j) * BK, p.a_row0 + tm * BM);
+                tma_load_2d(st + C::A_BYTES, &tmB, smem_u32(full + s), (kb0 + j) * BK, p.b_row0 + n0);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 5) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_f16(BM, BN);
+            bool ok = true;
+            for (int j = 0; j < nk && ok; ++j) {
+                const int s = j % C::STAGES;
+                const uint32_t ph = (j / C::STAGES) & 1u;
+                if (!mbar_wait(smem_u32(full + s), ph, abort_flag)) {
+                    ok = false;
+                    *abort_flag = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t st = smem_u32(smem + s * C::STAGE_BYTES);
+                const uint64_t ad = sw128_desc(st);
+                const uint64_t bd = sw128_desc(st + C::A_BYTES);
+#pragma unroll
+                for (int k = 0; k < BK / 16; ++k)
+                    umma_f16(tmem, ad + 2 * k, bd + 2 * k, idesc, (j > 0 || k > 0) ? 1u : 0u);
+                umma_commit(smem_u32(empty + s));
+            }
+            if (ok) umma_commit(smem_u32(accf));
+        }
+        __syncwarp();
+    } else {
+        if (EPI == EPI_QKV_HEADS) load_norm_weights(p, nws);
+        pdl_wait();
+        if (EPI == EPI_QKV_HEADS) fill_tok_meta<BN>(p, n0, tm, tpos, tdst);
+        const int fl = warp * 32 + lane;
+        if (EPI == EPI_RESID_F32) {  // residual rows of this CTA's first owned columns
+            const int lo = (z * BN) / S;
+            load_resid(p, n0 + lo, tm * BM + fl, xr0);
+        }
+        if (!mbar_wait(smem_u32(accf), 0u, abort_flag)) *ep_fail = 1;
+        tc_fence_after();
+    }
+
+    // phase 0: every CTA of the cluster has finished its MMAs (stage rings are free)
+    cluster_sync_all();
+    if (warp < 4) {
+        const bool ok = (*ep_fail == 0) && !*abort_flag;
+        if (ok) {
+            const int fl = warp * 32 + lane;
+            const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);
+            const uint32_t red_s = smem_u32(red);
+            const int ncols = min(BN, ((p.T - n0) + 31) / 32 * 32);
+            for (int c0 = 0; c0 < ncols; c0 += 32) {
+                uint32_t r[32];
+                TMEM_LD32(trow + c0, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int c = c0 + j;
+                    const int o = ((c + 1) * S - 1) / BN;  // owner: columns [o BN / S, (o+1) BN / S)
+                    const int lo = (o * BN) / S;
+                    const uint32_t dst = mapa_shared(red_s + (uint32_t)(((z * WMAX + (c - lo)) * 128 + fl) * 4), (uint32_t)o);
+                    st_cluster_f32(dst, __uint_as_float(r[j]));
+                }
+            }
+        }
+    }
+    // phase 1: all partials have landed in their owners' shared memory
+    cluster_sync_all();
+    if (warp < 4) {
+        const bool ok = (*ep_fail == 0) && !*abort_flag;
+        if (!ok) {
+            if (threadIdx.x == 0) atomicOr(p.status, QW_DEV_TIMEOUT);
+        } else {
+            const int fl = warp * 32 + lane;
+            const int lo = (z * BN) / S, hi = ((z + 1) * BN) / S;
+            for (int cc = lo; cc < hi; cc += 32) {
+                const int w = min(32, hi - cc);
+                const int tok0 = n0 + cc;
+                if (tok0 >= p.T) break;
+                const int ntok = min(w, p.T - tok0);
+                if (EPI == EPI_RESID_F32) {
+                    if (cc > lo) load_resid(p, tok0, tm * BM + fl, xr0);
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        if (j >= ntok) break;
+                        float v = xr0[j];
+                        for (int s = 0; s < S; ++s) v += red[(s * WMAX + (cc - lo) + j) * 128 + fl];
+                        p.out_f32[(size_t)(tok0 + j) * p.ld_out + tm * BM + fl] = v;
+                    }
+                } else {
+                    RopeRegs rr;
+                    if (EPI == EPI_QKV_HEADS && tm < p.n_heads + p.n_kv) load_rope(p, tpos, cc, ntok, rr);
+                    for (int j = 0; j < w; ++j) {
+                        float v = 0.f;
+                        for (int s = 0; s < S; ++s) v += red[(s * WMAX + (cc - lo) + j) * 128 + fl];
+                        E[j * EP + fl] = v;
+                    }
+                    named_bar_epi();
+                    if (EPI == EPI_QKV_HEADS)
+                        epi_heads(p, E, nws, tdst, ssx, rr, tok0, cc, ntok, tm);
+                    else
+                        epi_silu(p, E, tok0, ntok, tm);
+                    named_bar_epi();
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag && threadIdx.x == 0) atomicOr(p.status, QW_DEV_TIMEOUT);
+    if (warp == 5) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS)
+                     : "memory");
+    }
 }
 
 namespace {
 
-int g_gemm_sms = 0;
-
 template <int BN, int EPI>
-cudaError_t gemm_go(const LaunchCtx& c, const GemmArgs& a, int bn_idx) {
-    constexpr int NA = (EPI == EPI_SILU_MUL) ? 2 : 1;
-    using C = GemmCfg<BN, NA>;
-    static_assert(C::SMEM <= 227 * 1024, "shared memory budget");
-    static_assert(C::STAGES >= 3, "pipeline depth");
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<BN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
-    GemmKParams p;
+void fill_params(GemmKParams& p, const GemmArgs& a) {
+    p = GemmKParams{};
     p.a_row0 = a.a_row0;
-    p.a2_row0 = a.a2_row0;
+    p.b_row0 = a.b_row0;
     p.K = a.K;
     p.T = a.T;
     p.ld_out = a.ld_out;
@@ -499,42 +848,130 @@ cudaError_t gemm_go(const LaunchCtx& c, const GemmArgs& a, int bn_idx) {
     p.logits = a.logits;
     p.best = a.best;
     p.status = a.status;
-    p.part = a.part;
-    p.tickets = a.tickets;
+    p.q_out = a.q_out;
+    p.q_norm = a.q_norm;
+    p.k_norm = a.k_norm;
+    p.eps = a.eps;
+    p.rope_cos = a.rope_cos;
+    p.rope_sin = a.rope_sin;
+    p.tv = a.tv;
+    p.kv = a.kv;
+    p.layer = a.layer;
+    p.n_heads = a.n_heads;
+    p.n_kv = a.n_kv;
+    p.dbg_pos = a.dbg_pos;
+    p.dbg_slot = a.dbg_slot;
     p.tiles_m = a.M / BM;
     p.tiles_n = (a.T + BN - 1) / BN;
+}
+
+template <typename K>
+cudaError_t set_smem(K kern, int bytes, bool& done) {
+    if (done) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done = true;
+    return e;
+}
+
+// Largest cluster size <= want for which all `clusters` clusters are co-resident (the
+// device's count of simultaneously active clusters per size is probed once and cached);
+// 1 when none is.
+template <int BN, int EPI>
+int cluster_fit(int want, int clusters, int smem, cudaStream_t st) {
+    static int max_active[9] = {0};  // by cluster size; 0: not probed
+    static bool probed = false;
+    if (!probed) {
+        probed = true;
+        for (int s = 2; s <= 8; ++s) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(s);
+            cfg.blockDim = dim3(GEMM_THREADS);
+            cfg.dynamicSmemBytes = smem;
+            cfg.stream = st;
+            cudaLaunchAttribute at[1];
+            at[0].id = cudaLaunchAttributeClusterDimension;
+            at[0].val.clusterDim.x = s;
+            at[0].val.clusterDim.y = 1;
+            at[0].val.clusterDim.z = 1;
+            cfg.attrs = at;
+            cfg.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, k_gemm_cl<BN, EPI>, &cfg) != cudaSuccess) {
+                cudaGetLastError();
+                n = 0;
+            }
+            max_active[s] = n;
+        }
+    }
+    for (int s = std::min(want, 8); s >= 2; --s)
+        if (max_active[s] >= clusters) return s;
+    return 1;
+}
+
+template <int BN, int EPI>
+cudaError_t gemm_go(const LaunchCtx& c, const GemmArgs& a, int bn_idx) {
+    using C = GemmCfg<BN, EPI>;
+    static_assert(C::SMEM <= SMEM_BUDGET, "shared memory budget");
+    static_assert(C::STAGES >= 3, "pipeline depth");
+    GemmKParams p;
+    fill_params<BN, EPI>(p, a);
     const int tiles = p.tiles_m * p.tiles_n;
     const int sms = a.num_sms > 0 ? a.num_sms : 148;
-    int splits = 1;
-    if (EPI != EPI_ARGMAX && a.part && tiles * 2 <= sms && tiles <= a.max_tiles) {
-        const int nk_all = a.K / BK;
-        splits = std::min(std::min(sms / tiles, 8), std::max(nk_all / 4, 1));
-        while (splits > 1 && (size_t)tiles * splits * NA * BN * BM * 4 > a.part_bytes) --splits;
-        splits = std::max(splits, 1);
-    }
-    p.splits = splits;
-    p.units = tiles * splits;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(std::min(p.units, sms));
     cfg.blockDim = dim3(GEMM_THREADS);
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = c.stream;
-    cudaLaunchAttribute attr[1];
-    cfg.numAttrs = 0;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
     if (c.pdl) {
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
     }
     if (c.counter) ++*c.counter;
-    return cudaLaunchKernelEx(&cfg, k_gemm_tc<BN, EPI>, *a.tmA, *a.tmA2, a.tmB[bn_idx], p);
+    if constexpr (EPI != EPI_ARGMAX) {
+        int splits = 1;
+        if (tiles * 2 <= sms) {
+            splits = std::min(std::min(sms / tiles, 8), std::max((a.K / BK) / 4, 1));
+            // the partials of all splits must fit in one CTA's stage ring
+            while (splits > 1 && splits * 128 * ((BN + splits - 1) / splits) * 4 > C::STAGES * C::STAGE_BYTES)
+                --splits;
+        }
+        if (splits > 1) {
+            static bool done = false;
+            cudaError_t e = set_smem(k_gemm_cl<BN, EPI>, C::SMEM, done);
+            if (e != cudaSuccess) return e;
+            splits = cluster_fit<BN, EPI>(splits, tiles, C::SMEM, c.stream);
+        }
+        if (splits > 1) {
+            p.splits = splits;
+            p.units = tiles;
+            attr[na].id = cudaLaunchAttributeClusterDimension;
+            attr[na].val.clusterDim.x = splits;
+            attr[na].val.clusterDim.y = 1;
+            attr[na].val.clusterDim.z = 1;
+            ++na;
+            cfg.gridDim = dim3(tiles * splits);
+            cfg.attrs = attr;
+            cfg.numAttrs = na;
+            return cudaLaunchKernelEx(&cfg, k_gemm_cl<BN, EPI>, *a.tmA, a.tmB[bn_idx], p);
+        }
+    }
+    static bool done = false;
+    cudaError_t e = set_smem(k_gemm_tc<BN, EPI>, C::SMEM, done);
+    if (e != cudaSuccess) return e;
+    p.splits = 1;
+    p.units = tiles;
+    cfg.gridDim = dim3(std::min(tiles, sms));
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, k_gemm_tc<BN, EPI>, *a.tmA, a.tmB[bn_idx], p);
 }
 
 template <int EPI>
 cudaError_t gemm_bn(const LaunchCtx& c, const GemmArgs& a) {
     if (a.T <= 64) return gemm_go<64, EPI>(c, a, 0);
-    if (a.T <= 128 || EPI == EPI_SILU_MUL) return gemm_go<128, EPI>(c, a, 1);
+    if (a.T <= 128) return gemm_go<128, EPI>(c, a, 1);
     return gemm_go<256, EPI>(c, a, 2);
 }
 
@@ -580,7 +1017,7 @@ bool gemm_tc_encode_map(CUtensorMap* map, const void* base, uint64_t rows, uint6
 cudaError_t launch_gemm_tc(const LaunchCtx& c, int epi, const GemmArgs& a) {
     if (a.M % BM || a.K % BK || a.T < 1) return cudaErrorInvalidValue;
     switch (epi) {
-        case EPI_STORE_F32: return gemm_bn<EPI_STORE_F32>(c, a);
+        case EPI_QKV_HEADS: return gemm_bn<EPI_QKV_HEADS>(c, a);
         case EPI_RESID_F32: return gemm_bn<EPI_RESID_F32>(c, a);
         case EPI_SILU_MUL: return gemm_bn<EPI_SILU_MUL>(c, a);
         case EPI_ARGMAX: return gemm_bn<EPI_ARGMAX>(c, a);

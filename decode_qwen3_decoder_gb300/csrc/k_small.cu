@@ -439,14 +439,13 @@ cudaError_t launch_finalize(const LaunchCtx& c, const StepDesc& sd, unsigned lon
 //               rotation by pos * theta^(-i/64) (cos/sin from the fp32 table).
 //   v heads   : copied.
 // q is written as fp16 [T][n_heads][128]; k and v go (fp16) to the page slot
-// page_table[seq][pos / 16] * 16 + pos % 16 of this layer, and to a contiguous fp16
-// [T][2][n_kv][128] copy that the prefill attention reads.
+// page_table[seq][pos / 16] * 16 + pos % 16 of this layer.
 // =======================================================================================
 __global__ void __launch_bounds__(256) k_qknorm_rope_append(
     int T, int layer, const float* __restrict__ qkv, const bf16* __restrict__ q_norm,
     const bf16* __restrict__ k_norm, float eps, const float* __restrict__ rope_cos,
     const float* __restrict__ rope_sin, int n_heads, int n_kv, TokView tv, KVView kv,
-    f16* __restrict__ q_out, f16* __restrict__ kv_new, int32_t* dbg_pos, int32_t* dbg_slot,
+    f16* __restrict__ q_out, int32_t* dbg_pos, int32_t* dbg_slot,
     int* status) {
     pdl_launch();
     pdl_wait();
@@ -488,7 +487,6 @@ __global__ void __launch_bounds__(256) k_qknorm_rope_append(
         } else {
             const int which = (hh - n_heads) / n_kv;  // 0 = K, 1 = V
             const int g = (hh - n_heads) % n_kv;
-            *reinterpret_cast<uint2*>(kv_new + (((size_t)t * 2 + which) * n_kv + g) * 128 + lane * 4) = packed;
             const int seq = tv.seq[t];
             const int pi = pos >> 4;
             const int page = (pi < kv.max_pages_per_seq) ? kv.page_table[(size_t)seq * kv.max_pages_per_seq + pi] : -1;
@@ -510,11 +508,11 @@ __global__ void __launch_bounds__(256) k_qknorm_rope_append(
 cudaError_t launch_qknorm_rope_append(const LaunchCtx& c, int T, int layer, const float* qkv,
                                       const bf16* q_norm, const bf16* k_norm, float eps,
                                       const float* rope_cos, const float* rope_sin, int n_heads,
-                                      int n_kv, TokView tv, KVView kv, f16* q_out, f16* kv_new,
+                                      int n_kv, TokView tv, KVView kv, f16* q_out,
                                       int32_t* dbg_pos, int32_t* dbg_slot, int* status) {
     const int warps = T * (n_heads + 2 * n_kv);
     return launch_k(c, k_qknorm_rope_append, dim3((warps + 7) / 8), dim3(256), 0, T, layer, qkv,
-                    q_norm, k_norm, eps, rope_cos, rope_sin, n_heads, n_kv, tv, kv, q_out, kv_new,
+                    q_norm, k_norm, eps, rope_cos, rope_sin, n_heads, n_kv, tv, kv, q_out,
                     dbg_pos, dbg_slot, status);
 }
 
@@ -602,4 +600,25 @@ cudaError_t launch_convert_bf16_f16(const LaunchCtx& c, const bf16* src, f16* ds
     if (blocks > 4096) blocks = 4096;
     if (blocks < 1) blocks = 1;
     return launch_k(c, k_convert_bf16_f16, dim3((unsigned)blocks), dim3(256), 0, src, dst, n, status);
+}
+
+// gate/up interleave for the tensor-core SwiGLU: output row r of block b = r / 128 is gate row
+// 64 b + r % 128 for r % 128 < 64, else up row 64 b + r % 128 - 64.
+__global__ void k_convert_gateup(const bf16* __restrict__ gate, const bf16* __restrict__ up, f16* __restrict__ dst,
+                                 int inter, int K, int* status) {
+    const int r = blockIdx.x;  // destination row
+    const int b = r >> 7, w = r & 127;
+    const bf16* src = (w < 64 ? gate : up) + (size_t)(b * 64 + (w & 63)) * K;
+    bool big = false;
+    for (int k = threadIdx.x; k < K; k += blockDim.x) {
+        const float v = __bfloat162float(src[k]);
+        big |= fabsf(v) > 65504.f;
+        dst[(size_t)r * K + k] = __float2half_rn(v);
+    }
+    if (big) atomicOr(status, QW_DEV_RANGE);
+}
+
+cudaError_t launch_convert_gateup(const LaunchCtx& c, const bf16* gate, const bf16* up, f16* dst, int inter, int K,
+                                  int* status) {
+    return launch_k(c, k_convert_gateup, dim3(2 * inter), dim3(256), 0, gate, up, dst, inter, K, status);
 }

@@ -131,7 +131,7 @@ cudaError_t launch_finalize(const LaunchCtx& c, const StepDesc& sd, unsigned lon
 cudaError_t launch_qknorm_rope_append(const LaunchCtx& c, int T, int layer, const float* qkv,
                                       const bf16* q_norm, const bf16* k_norm, float eps,
                                       const float* rope_cos, const float* rope_sin, int n_heads,
-                                      int n_kv, TokView tv, KVView kv, f16* q_out, f16* kv_new,
+                                      int n_kv, TokView tv, KVView kv, f16* q_out,
                                       int32_t* dbg_pos, int32_t* dbg_slot, int* status);
 // Decode mode of the paged attention: QK-norm + RoPE + KV append done inside the kernel.
 struct AttnFuse {
@@ -149,9 +149,13 @@ cudaError_t launch_attn_paged(const LaunchCtx& c, int T, int layer, const f16* q
                               int n_kv, TokView tv, KVView kv, int chunk, int n_splits,
                               float* part_o, float* part_ml, int* counters, f16* out,
                               const AttnFuse* fuse);
-// Causal flash attention of a prefill over the contiguous new K/V (sequences start empty).
-cudaError_t launch_attn_prefill(const LaunchCtx& c, const StepDesc& sd, int max_len, const f16* q,
-                                const f16* kv_new, int n_heads, int n_kv, f16* out);
+// Causal flash attention of a prefill (sequences start empty) over the K/V just appended to
+// the paged cache.
+cudaError_t launch_attn_prefill(const LaunchCtx& c, const StepDesc& sd, int max_len, int layer, const f16* q,
+                                KVView kv, int n_heads, int n_kv, f16* out);
+// bf16 gate/up [inter][K] -> fp16 rows interleaved per 64: [gate 64b..64b+63][up 64b..64b+63]...
+cudaError_t launch_convert_gateup(const LaunchCtx& c, const bf16* gate, const bf16* up, f16* dst, int inter,
+                                  int K, int* status);
 cudaError_t launch_kv_fill(const LaunchCtx& c, KVView kv, int n_layers, int n_kv, int seq,
                            int n_tokens, unsigned long long seed);
 
@@ -168,26 +172,33 @@ bool qw_model_lmhead_view(const qw_model* m, LmHeadView* v);
 qw_status qw_fail(qw_status s, const char* fmt, ...);
 
 // tcgen05 GEMM (T > 8 token rows). Epilogue kinds:
-enum GemmEpi : int { EPI_STORE_F32 = 0, EPI_RESID_F32 = 1, EPI_SILU_MUL = 2, EPI_ARGMAX = 3 };
+enum GemmEpi : int { EPI_QKV_HEADS = 0, EPI_RESID_F32 = 1, EPI_SILU_MUL = 2, EPI_ARGMAX = 3 };
 struct GemmArgs {
     const CUtensorMap* tmA;   // weights [rows_total, K] fp16, box 128 x 64
-    const CUtensorMap* tmA2;  // second weight (up) for EPI_SILU_MUL, else same as tmA
-    const CUtensorMap* tmB;   // activations [T_cap, K] fp16, box BN x 64
+    const CUtensorMap* tmB;   // activations [T_cap, K] fp16: three maps, boxes of 64/128/256 rows
     int a_row0;               // first weight row of this matrix (layer offset)
-    int a2_row0;
-    int M;                    // output features (multiple of 128)
+    int b_row0;               // first activation row (token offset of the tmB maps)
+    int M;                    // weight rows (multiple of 128)
     int K;                    // reduction length (multiple of 64)
     int T;                    // token rows (columns of the transposed product)
-    float* out_f32;           // EPI_STORE_F32: out[t][m]; EPI_RESID_F32: x[t][m] +=
+    float* out_f32;           // EPI_RESID_F32: x[t][m] (read and written)
     int ld_out;
-    f16* out_h;               // EPI_SILU_MUL: act[t][m]
+    f16* out_h;               // EPI_SILU_MUL: act[t][m] (rows interleaved 64 gate / 64 up per tile)
     float* logits;            // EPI_ARGMAX: optional logits[t][m]
     unsigned long long* best; // EPI_ARGMAX: per-token packed argmax keys
     int* status;
-    float* part;              // split-K partial tiles (NULL: never split)
-    size_t part_bytes;
-    int* tickets;             // split-K per-tile counters (zeroed; left zeroed)
-    int max_tiles;
+    // EPI_QKV_HEADS: per-head QK-norm + RoPE, q out, k/v appended to the paged cache
+    f16* q_out;               // [T][n_heads][128]
+    const bf16* q_norm;
+    const bf16* k_norm;
+    float eps;
+    const float* rope_cos;
+    const float* rope_sin;
+    TokView tv;
+    KVView kv;
+    int layer, n_heads, n_kv;
+    int32_t* dbg_pos;
+    int32_t* dbg_slot;
     int num_sms;
 };
 cudaError_t launch_gemm_tc(const LaunchCtx& c, int epi, const GemmArgs& a);

@@ -54,8 +54,6 @@ extern "C" const char* qw_last_error(void) { return g_err.c_str(); }
 // ---------------------------------------------------------------------------------------
 static constexpr int kMaxSplits = 128;   // split-KV partial slots per (token, head)
 static constexpr int kSmallT = 8;        // token rows handled by the GEMV family
-static constexpr size_t kGemmPartBytes = 48u << 20;
-static constexpr int kGemmMaxTiles = 4096;
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -85,9 +83,9 @@ static bool config_ok(const qw_config* c, std::string* why) {
 }
 
 struct WsLayout {
-    size_t wqkv, wo, wg, wu, wd, embed16, bqkv, bo, bg, bu, bd, norms, fnorm, rcos, rsin;
-    size_t x, h, qkv, q, kvnew, attn, act, part_o, part_ml, counters;
-    size_t tok_seq, tok_pos, last, best, status, gen_tok, gen_cur, gen_out, mk_sync, gpart, gtick;
+    size_t wqkv, wo, wgu, wd, embed16, bqkv, bo, bg, bu, bd, norms, fnorm, rcos, rsin;
+    size_t x, h, qkv, q, attn, act, part_o, part_ml, counters;
+    size_t tok_seq, tok_pos, last, best, status, gen_tok, gen_cur, gen_out, mk_sync;
     size_t total;
     int part_T;
 };
@@ -106,8 +104,7 @@ static WsLayout layout_for(const qw_config& c) {
     const size_t T = c.max_tokens;
     L.wqkv = take(NL * QKV * D * 2);
     L.wo = take(NL * D * QD * 2);
-    L.wg = take(NL * I * D * 2);
-    L.wu = take(NL * I * D * 2);
+    L.wgu = take(NL * 2 * I * D * 2);
     L.wd = take(NL * D * I * 2);
     L.embed16 = take((size_t)c.vocab * D * 2);
     L.bqkv = take(NL * QKV * D * 2);
@@ -121,9 +118,8 @@ static WsLayout layout_for(const qw_config& c) {
     L.rsin = take((size_t)c.max_context * 64 * 4);
     L.x = take(T * D * 4);
     L.h = take(std::max(T, (size_t)c.max_batch) * D * 2);
-    L.qkv = take(T * QKV * 4);
+    L.qkv = take(std::min<size_t>(T, kSmallT) * QKV * 4);  // fp32 q|k|v of the small-batch path
     L.q = take(T * QD * 2);
-    L.kvnew = take(T * 2 * KD * 2);
     L.attn = take(T * QD * 2);
     L.act = take(T * I * 2);
     L.part_T = std::min<int>(c.max_tokens, std::max(c.max_batch, kSmallT));
@@ -136,8 +132,6 @@ static WsLayout layout_for(const qw_config& c) {
     L.best = take((size_t)c.max_batch * 8);
     L.status = take(4);
     L.mk_sync = take(16);  // persistent decode kernel: arrivals, generation, ticket, abort
-    L.gpart = take(kGemmPartBytes);          // split-K partial tiles
-    L.gtick = take(kGemmMaxTiles * 4);       // split-K tickets
     L.gen_tok = take(T * 4);
     L.gen_cur = take((size_t)c.max_batch * 4);
     L.gen_out = take((size_t)c.max_batch * ((size_t)c.max_context + 1) * 4);
@@ -159,16 +153,14 @@ struct qw_model {
     WsLayout L;
     char* ws;
     int qkv_rows;
-    f16 *wqkv, *wo, *wg, *wu, *wd, *embed16;  // fp16 copies of the bf16 weights (tensor cores)
+    f16 *wqkv, *wo, *wgu, *wd, *embed16;  // fp16 copies of the bf16 weights (tensor cores)
     bf16 *bqkv, *bo, *bg, *bu, *bd;           // bf16 packed copies (small-batch decode paths)
     bf16 *norms, *fnorm;
     const bf16* embed;
     float *rcos, *rsin, *x, *qkv, *part_o, *part_ml;
-    f16 *h, *q, *kvnew, *attn, *act;
+    f16 *h, *q, *attn, *act;
     int *counters, *tok_seq, *tok_pos, *last, *status;
     unsigned* mk_sync;
-    float* gpart;
-    int* gtick;
     int mk_grid;       // CTAs of the persistent decode kernel (0: not available)
     int mk_max_t;      // most tokens it takes
     bool use_mk;       // decode steps of <= mk_max_t tokens run as one persistent kernel
@@ -177,6 +169,9 @@ struct qw_model {
     float* dbg_hidden;
     int32_t *dbg_pos, *dbg_slot;
     cudaStream_t cap_stream;
+    cudaStream_t aux_stream;   // second half of a split decode batch
+    cudaEvent_t ev_fork, ev_join;
+    bool split_decode;         // decode batches of >= 16 run as two overlapping halves
     std::map<std::vector<long long>, GraphEntry> graphs;
     unsigned long long use_clock;
     int last_launches;
@@ -189,7 +184,7 @@ struct qw_model {
     std::vector<cudaEvent_t> prof_events;
     unsigned long long prof_gen;
     // TMA descriptors of the tensor-core GEMM operands
-    CUtensorMap tm_wqkv, tm_wo, tm_wg, tm_wu, tm_wd, tm_embed;
+    CUtensorMap tm_wqkv, tm_wo, tm_wgu, tm_wd, tm_embed;
     CUtensorMap tm_h[3], tm_attn[3], tm_act[3];  // token boxes of 64, 128, 256 rows
 };
 
@@ -258,8 +253,7 @@ extern "C" qw_status qw_init_weights(const qw_config* cfg, const qw_weight_ptrs*
     char* b = m->ws;
     m->wqkv = (f16*)(b + L.wqkv);
     m->wo = (f16*)(b + L.wo);
-    m->wg = (f16*)(b + L.wg);
-    m->wu = (f16*)(b + L.wu);
+    m->wgu = (f16*)(b + L.wgu);
     m->wd = (f16*)(b + L.wd);
     m->embed16 = (f16*)(b + L.embed16);
     m->bqkv = (bf16*)(b + L.bqkv);
@@ -276,7 +270,6 @@ extern "C" qw_status qw_init_weights(const qw_config* cfg, const qw_weight_ptrs*
     m->h = (f16*)(b + L.h);
     m->qkv = (float*)(b + L.qkv);
     m->q = (f16*)(b + L.q);
-    m->kvnew = (f16*)(b + L.kvnew);
     m->attn = (f16*)(b + L.attn);
     m->act = (f16*)(b + L.act);
     m->part_o = (float*)(b + L.part_o);
@@ -288,8 +281,6 @@ extern "C" qw_status qw_init_weights(const qw_config* cfg, const qw_weight_ptrs*
     m->best = (unsigned long long*)(b + L.best);
     m->status = (int*)(b + L.status);
     m->mk_sync = (unsigned*)(b + L.mk_sync);
-    m->gpart = (float*)(b + L.gpart);
-    m->gtick = (int*)(b + L.gtick);
     m->gen_tok = (int32_t*)(b + L.gen_tok);
     m->gen_cur = (int32_t*)(b + L.gen_cur);
     m->gen_out = (int32_t*)(b + L.gen_out);
@@ -314,8 +305,9 @@ extern "C" qw_status qw_init_weights(const qw_config* cfg, const qw_weight_ptrs*
     }
     // Pack: the projection matrices become fp16 (the tensor-core operand type; exact for
     // every bf16 magnitude in [2^-14, 65504]); per layer q|k|v rows are concatenated into one
-    // [qkv_rows, hidden] matrix. Norm weights stay bf16, copied as
-    // [input D][post-attention D][q_norm d][k_norm d].
+    // [qkv_rows, hidden] matrix; gate and up rows are interleaved in blocks of 64 (64 gate
+    // rows, then the same 64 up rows) so one 128-row tile holds both halves of SwiGLU. Norm
+    // weights stay bf16, copied as [input D][post-attention D][q_norm d][k_norm d].
     LaunchCtx pc = {st, false, nullptr};
     auto cv = [&](f16* dst, const void* src, size_t n) {
         return launch_convert_bf16_f16(pc, (const bf16*)src, dst, n, m->status);
@@ -328,8 +320,9 @@ extern "C" qw_status qw_init_weights(const qw_config* cfg, const qw_weight_ptrs*
         if (e == cudaSuccess) e = cv(q0 + QD * D, lp.k_proj, KD * D);
         if (e == cudaSuccess) e = cv(q0 + (QD + KD) * D, lp.v_proj, KD * D);
         if (e == cudaSuccess) e = cv(m->wo + (size_t)l * D * QD, lp.o_proj, D * QD);
-        if (e == cudaSuccess) e = cv(m->wg + (size_t)l * I * D, lp.gate_proj, I * D);
-        if (e == cudaSuccess) e = cv(m->wu + (size_t)l * I * D, lp.up_proj, I * D);
+        if (e == cudaSuccess)
+            e = launch_convert_gateup(pc, (const bf16*)lp.gate_proj, (const bf16*)lp.up_proj,
+                                      m->wgu + (size_t)l * 2 * I * D, (int)I, (int)D, m->status);
         if (e == cudaSuccess) e = cv(m->wd + (size_t)l * D * I, lp.down_proj, D * I);
         // bf16 packed copies (bit-identical) for the bandwidth-bound small-batch paths
         bf16* b0 = m->bqkv + (size_t)l * m->qkv_rows * D;
@@ -380,8 +373,7 @@ extern "C" qw_status qw_init_weights(const qw_config* cfg, const qw_weight_ptrs*
     }
     if (cudaMemsetAsync(m->counters, 0, (size_t)L.part_T * cfg->n_kv_heads * 4, st) != cudaSuccess ||
         cudaMemsetAsync(m->best, 0, (size_t)cfg->max_batch * 8, st) != cudaSuccess ||
-        cudaMemsetAsync(m->mk_sync, 0, 16, st) != cudaSuccess ||
-        cudaMemsetAsync(m->gtick, 0, kGemmMaxTiles * 4, st) != cudaSuccess) {
+        cudaMemsetAsync(m->mk_sync, 0, 16, st) != cudaSuccess) {
         fail(QW_ERR_CUDA, "workspace clear failed");
         return fail_free(QW_ERR_CUDA);
     }
@@ -403,8 +395,7 @@ extern "C" qw_status qw_init_weights(const qw_config* cfg, const qw_weight_ptrs*
     bool ok = true;
     ok = ok && gemm_tc_encode_map(&m->tm_wqkv, m->wqkv, NL * m->qkv_rows, D, 128);
     ok = ok && gemm_tc_encode_map(&m->tm_wo, m->wo, NL * D, QD, 128);
-    ok = ok && gemm_tc_encode_map(&m->tm_wg, m->wg, NL * I, D, 128);
-    ok = ok && gemm_tc_encode_map(&m->tm_wu, m->wu, NL * I, D, 128);
+    ok = ok && gemm_tc_encode_map(&m->tm_wgu, m->wgu, NL * 2 * I, D, 128);
     ok = ok && gemm_tc_encode_map(&m->tm_wd, m->wd, NL * D, I, 128);
     ok = ok && gemm_tc_encode_map(&m->tm_embed, m->embed16, cfg->vocab, D, 128);
     ok = ok && gemm_tc_encode_map(m->tm_h, m->h, TT, D, 0);
@@ -414,10 +405,14 @@ extern "C" qw_status qw_init_weights(const qw_config* cfg, const qw_weight_ptrs*
         fail(QW_ERR_CUDA, "cuTensorMapEncodeTiled failed");
         return fail_free(QW_ERR_CUDA);
     }
-    if (cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking) != cudaSuccess) {
-        fail(QW_ERR_CUDA, "capture stream creation failed");
+    if (cudaStreamCreateWithFlags(&m->cap_stream, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&m->aux_stream, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&m->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&m->ev_join, cudaEventDisableTiming) != cudaSuccess) {
+        fail(QW_ERR_CUDA, "stream/event creation failed");
         return fail_free(QW_ERR_CUDA);
     }
+    m->split_decode = true;
     m->dbg_hidden = nullptr;
     m->dbg_pos = m->dbg_slot = nullptr;
     m->prof_kind = QW_PROF_OFF;
@@ -435,6 +430,9 @@ extern "C" void qw_free_model(qw_model* m) {
     if (!m) return;
     for (auto& kv : m->graphs) cudaGraphExecDestroy(kv.second.exec);
     if (m->cap_stream) cudaStreamDestroy(m->cap_stream);
+    if (m->aux_stream) cudaStreamDestroy(m->aux_stream);
+    if (m->ev_fork) cudaEventDestroy(m->ev_fork);
+    if (m->ev_join) cudaEventDestroy(m->ev_join);
     delete m;
 }
 
@@ -468,6 +466,9 @@ extern "C" qw_status qw_set_option(qw_model* m, int option, int value) {
             return QW_OK;
         case QW_OPT_PDL:
             m->pdl = value != 0;
+            return QW_OK;
+        case QW_OPT_SPLIT_DECODE:
+            m->split_decode = value != 0;
             return QW_OK;
         default:
             return fail(QW_ERR_INVALID_ARG, "unknown option %d", option);
@@ -694,22 +695,156 @@ static SplitPlan plan_splits(const qw_model* m, int T, int max_keys) {
     return {chunk, std::max(n, 1)};
 }
 
+// Token rows [t0, t0 + n) of a step through every layer, on stream st. The rows of a
+// decode step are independent sequences, so a batch can run as several such ranges on
+// different streams; every buffer is addressed at row t0 (the tensor-core operands through
+// the TMA row offset).
+static qw_status run_layers(qw_model* m, qw_kv* kv, const StepDesc& sd, bool prefill, int max_keys, int t0, int n,
+                            cudaStream_t st, bool dbg, int* launches, int* pc) {
+    const qw_config& c = m->cfg;
+    const bool pdl_on = m->pdl && m->prof_kind == QW_PROF_OFF;  // events must bracket launches
+    LaunchCtx lc = {st, false, launches};  // the first launch of a range follows a full dependency
+#define LAUNCH(expr)        \
+    do {                    \
+        CUDA_TRY(expr);     \
+        lc.pdl = pdl_on;    \
+    } while (0)
+#define PROF(kind) ProfScope prof_scope_(m, kind, pc, st)
+    const int T = n;
+    const int D = c.hidden, I = c.inter, QD = c.n_heads * c.head_dim, d = c.head_dim;
+    const KVView kvv = kv->view();
+    const TokView tv = {m->tok_seq + t0, m->tok_pos + t0, m->last};
+    const bool small = sd.T <= kSmallT;
+    const SplitPlan sp = plan_splits(m, T, max_keys);
+    float* x = m->x + (size_t)t0 * D;
+    f16* h = m->h + (size_t)t0 * D;
+    f16* q = m->q + (size_t)t0 * QD;
+    f16* attn = m->attn + (size_t)t0 * QD;
+    f16* act = m->act + (size_t)t0 * I;
+    float* qkv = m->qkv + (size_t)t0 * m->qkv_rows;
+    float* part_o = m->part_o + (size_t)t0 * c.n_heads * kMaxSplits * 128;
+    float* part_ml = m->part_ml + (size_t)t0 * c.n_heads * kMaxSplits * 2;
+    int* counters = m->counters + (size_t)t0 * c.n_kv_heads;
+    int32_t* dbg_pos = dbg ? m->dbg_pos + t0 : nullptr;
+    int32_t* dbg_slot = dbg ? m->dbg_slot + t0 : nullptr;
+    for (int l = 0; l < c.n_layers; ++l) {
+        const bf16* nb = m->norms + (size_t)l * (2 * D + 2 * d);
+        const bf16* w_in = nb;
+        const bf16* w_post = nb + D;
+        const bf16* w_qn = nb + 2 * D;
+        const bf16* w_kn = nb + 2 * D + d;
+        int32_t* lpos = l == 0 ? dbg_pos : nullptr;
+        int32_t* lslot = l == 0 ? dbg_slot : nullptr;
+        // --- attention sublayer (Paso 5) ---
+        if (small) {
+            PROF(QW_PROF_QKV);
+            LAUNCH(launch_gemv_qkv(lc, T, x, w_in, c.rms_eps, m->bqkv + (size_t)l * m->qkv_rows * D, m->qkv_rows, D,
+                                   qkv));
+        } else {
+            {
+                PROF(QW_PROF_RMSNORM);
+                LAUNCH(launch_rmsnorm(lc, x, nullptr, T, D, w_in, c.rms_eps, h));
+            }
+            PROF(QW_PROF_QKV);
+            // q|k|v projection with the per-head QK-norm, RoPE and the KV append in its epilogue
+            GemmArgs g = {};
+            g.tmA = &m->tm_wqkv; g.tmB = m->tm_h; g.b_row0 = t0;
+            g.a_row0 = l * m->qkv_rows; g.M = m->qkv_rows; g.K = D; g.T = T;
+            g.status = m->status; g.num_sms = m->num_sms;
+            g.q_out = q; g.q_norm = w_qn; g.k_norm = w_kn; g.eps = c.rms_eps;
+            g.rope_cos = m->rcos; g.rope_sin = m->rsin; g.tv = tv; g.kv = kvv; g.layer = l;
+            g.n_heads = c.n_heads; g.n_kv = c.n_kv_heads;
+            g.dbg_pos = lpos; g.dbg_slot = lslot;
+            LAUNCH(launch_gemm_tc(lc, EPI_QKV_HEADS, g));
+        }
+        if (small) {
+            if (prefill) {
+                {
+                    PROF(QW_PROF_ROPE);
+                    LAUNCH(launch_qknorm_rope_append(lc, T, l, qkv, w_qn, w_kn, c.rms_eps, m->rcos, m->rsin,
+                                                     c.n_heads, c.n_kv_heads, tv, kvv, q, lpos, lslot, m->status));
+                }
+                PROF(QW_PROF_ATTN);
+                LAUNCH(launch_attn_paged(lc, T, l, q, c.n_heads, c.n_kv_heads, tv, kvv, sp.chunk, sp.n_splits,
+                                         part_o, part_ml, counters, attn, nullptr));
+            } else {
+                // decode: one new token per sequence; QK-norm, RoPE and the KV append run inside
+                AttnFuse fz = {qkv, w_qn, w_kn, c.rms_eps, m->rcos, m->rsin, lpos, lslot, m->status};
+                PROF(QW_PROF_ATTN);
+                LAUNCH(launch_attn_paged(lc, T, l, q, c.n_heads, c.n_kv_heads, tv, kvv, sp.chunk, sp.n_splits,
+                                         part_o, part_ml, counters, attn, &fz));
+            }
+        } else {
+            // q, k, v were normalised, rotated and appended by the projection's epilogue
+            PROF(QW_PROF_ATTN);
+            if (prefill)
+                LAUNCH(launch_attn_prefill(lc, sd, max_keys, l, q, kvv, c.n_heads, c.n_kv_heads, attn));
+            else
+                LAUNCH(launch_attn_paged(lc, T, l, q, c.n_heads, c.n_kv_heads, tv, kvv, sp.chunk, sp.n_splits,
+                                         part_o, part_ml, counters, attn, nullptr));
+        }
+        if (small) {
+            PROF(QW_PROF_OPROJ);
+            LAUNCH(launch_gemv_resid(lc, T, attn, m->bo + (size_t)l * D * QD, D, QD, x));
+        } else {
+            PROF(QW_PROF_OPROJ);
+            GemmArgs g = {};
+            g.tmA = &m->tm_wo; g.tmB = m->tm_attn; g.b_row0 = t0;
+            g.a_row0 = l * D; g.M = D; g.K = QD; g.T = T;
+            g.out_f32 = x; g.ld_out = D; g.status = m->status; g.num_sms = m->num_sms;
+            LAUNCH(launch_gemm_tc(lc, EPI_RESID_F32, g));
+        }
+        // --- feed-forward sublayer (Paso 6) ---
+        if (small) {
+            {
+                PROF(QW_PROF_GATEUP);
+                LAUNCH(launch_gemv_gateup(lc, T, x, w_post, c.rms_eps, m->bg + (size_t)l * I * D,
+                                          m->bu + (size_t)l * I * D, I, D, act));
+            }
+            PROF(QW_PROF_DOWN);
+            LAUNCH(launch_gemv_resid(lc, T, act, m->bd + (size_t)l * D * I, D, I, x));
+        } else {
+            {
+                PROF(QW_PROF_RMSNORM);
+                LAUNCH(launch_rmsnorm(lc, x, nullptr, T, D, w_post, c.rms_eps, h));
+            }
+            GemmArgs g = {};
+            g.tmA = &m->tm_wgu; g.tmB = m->tm_h; g.b_row0 = t0;
+            g.a_row0 = l * 2 * I; g.M = 2 * I; g.K = D; g.T = T;
+            g.out_h = act; g.ld_out = I; g.status = m->status; g.num_sms = m->num_sms;
+            {
+                PROF(QW_PROF_GATEUP);
+                LAUNCH(launch_gemm_tc(lc, EPI_SILU_MUL, g));
+            }
+            GemmArgs g2 = {};
+            g2.tmA = &m->tm_wd; g2.tmB = m->tm_act; g2.b_row0 = t0;
+            g2.a_row0 = l * D; g2.M = D; g2.K = I; g2.T = T;
+            g2.out_f32 = x; g2.ld_out = D; g2.status = m->status; g2.num_sms = m->num_sms;
+            PROF(QW_PROF_DOWN);
+            LAUNCH(launch_gemm_tc(lc, EPI_RESID_F32, g2));
+        }
+        if (dbg)
+            CUDA_TRY(cudaMemcpyAsync(m->dbg_hidden + ((size_t)l * sd.T + t0) * D, x, (size_t)T * D * 4,
+                                     cudaMemcpyDeviceToDevice, st));
+    }
+#undef PROF
+#undef LAUNCH
+    return QW_OK;
+}
+
 static qw_status run_step(qw_model* m, qw_kv* kv, const StepDesc& sd, bool prefill, int max_keys,
                           const int32_t* tokens, float* logits, int32_t* next, cudaStream_t st,
                           bool allow_debug, int* launches) {
     const qw_config& c = m->cfg;
-    LaunchCtx lc = {st, m->pdl && m->prof_kind == QW_PROF_OFF, launches};  // events must bracket launches
     const int T = sd.T, B = sd.B;
-    const int D = c.hidden, I = c.inter, QD = c.n_heads * c.head_dim, d = c.head_dim;
+    const int D = c.hidden, I = c.inter, QD = c.n_heads * c.head_dim;
     const KVView kvv = kv->view();
     TokView tv = {m->tok_seq, m->tok_pos, m->last};
     const bool dbg = allow_debug && m->dbg_hidden;
     const bool small = T <= kSmallT;
-    const SplitPlan sp = plan_splits(m, T, max_keys);
     if (!small && !prefill && T > m->L.part_T) return fail(QW_ERR_UNSUPPORTED, "decode batch beyond partial buffers");
 
     int pc[16] = {0};
-#define PROF(kind) ProfScope prof_scope_(m, kind, pc, st)
     if (!prefill && m->use_mk && T <= m->mk_max_t) {
         // one cooperative launch for the whole decode step
         const int units_teams = 3 * m->mk_grid;
@@ -746,97 +881,27 @@ static qw_status run_step(qw_model* m, qw_kv* kv, const StepDesc& sd, bool prefi
         CUDA_TRY(launch_decode_mk(lc1, mp, m->mk_grid));
         return QW_OK;
     }
-    CUDA_TRY(launch_step_begin(lc, sd, tokens, m->embed, c.vocab, D, m->x, tv, kvv, m->status));
-    for (int l = 0; l < c.n_layers; ++l) {
-        const bf16* nb = m->norms + (size_t)l * (2 * D + 2 * d);
-        const bf16* w_in = nb;
-        const bf16* w_post = nb + D;
-        const bf16* w_qn = nb + 2 * D;
-        const bf16* w_kn = nb + 2 * D + d;
-        // --- attention sublayer (Paso 5) ---
-        if (small) {
-            PROF(QW_PROF_QKV);
-            CUDA_TRY(launch_gemv_qkv(lc, T, m->x, w_in, c.rms_eps, m->bqkv + (size_t)l * m->qkv_rows * D,
-                                     m->qkv_rows, D, m->qkv));
-        } else {
-            {
-                PROF(QW_PROF_RMSNORM);
-                CUDA_TRY(launch_rmsnorm(lc, m->x, nullptr, T, D, w_in, c.rms_eps, m->h));
-            }
-            PROF(QW_PROF_QKV);
-            GemmArgs g = {};
-            g.tmA = &m->tm_wqkv; g.tmA2 = &m->tm_wqkv; g.tmB = m->tm_h;
-            g.a_row0 = l * m->qkv_rows; g.a2_row0 = g.a_row0; g.M = m->qkv_rows; g.K = D; g.T = T;
-            g.out_f32 = m->qkv; g.ld_out = m->qkv_rows; g.status = m->status; g.part = m->gpart; g.part_bytes = kGemmPartBytes; g.tickets = m->gtick; g.max_tiles = kGemmMaxTiles; g.num_sms = m->num_sms;
-            CUDA_TRY(launch_gemm_tc(lc, EPI_STORE_F32, g));
-        }
-        if (prefill) {
-            {
-                PROF(QW_PROF_ROPE);
-                CUDA_TRY(launch_qknorm_rope_append(lc, T, l, m->qkv, w_qn, w_kn, c.rms_eps, m->rcos, m->rsin,
-                                                   c.n_heads, c.n_kv_heads, tv, kvv, m->q, m->kvnew,
-                                                   (dbg && l == 0) ? m->dbg_pos : nullptr,
-                                                   (dbg && l == 0) ? m->dbg_slot : nullptr, m->status));
-            }
-            PROF(QW_PROF_ATTN);
-            if (small)
-                CUDA_TRY(launch_attn_paged(lc, T, l, m->q, c.n_heads, c.n_kv_heads, tv, kvv, sp.chunk, sp.n_splits,
-                                           m->part_o, m->part_ml, m->counters, m->attn, nullptr));
-            else
-                CUDA_TRY(launch_attn_prefill(lc, sd, max_keys, m->q, m->kvnew, c.n_heads, c.n_kv_heads, m->attn));
-        } else {
-            // decode: one new token per sequence; QK-norm, RoPE and the KV append run inside
-            AttnFuse fz = {m->qkv, w_qn, w_kn, c.rms_eps, m->rcos, m->rsin,
-                           (dbg && l == 0) ? m->dbg_pos : nullptr, (dbg && l == 0) ? m->dbg_slot : nullptr,
-                           m->status};
-            PROF(QW_PROF_ATTN);
-            CUDA_TRY(launch_attn_paged(lc, T, l, m->q, c.n_heads, c.n_kv_heads, tv, kvv, sp.chunk, sp.n_splits,
-                                       m->part_o, m->part_ml, m->counters, m->attn, &fz));
-        }
-        if (small) {
-            PROF(QW_PROF_OPROJ);
-            CUDA_TRY(launch_gemv_resid(lc, T, m->attn, m->bo + (size_t)l * D * QD, D, QD, m->x));
-        } else {
-            PROF(QW_PROF_OPROJ);
-            GemmArgs g = {};
-            g.tmA = &m->tm_wo; g.tmA2 = &m->tm_wo; g.tmB = m->tm_attn;
-            g.a_row0 = l * D; g.a2_row0 = g.a_row0; g.M = D; g.K = QD; g.T = T;
-            g.out_f32 = m->x; g.ld_out = D; g.status = m->status; g.part = m->gpart; g.part_bytes = kGemmPartBytes; g.tickets = m->gtick; g.max_tiles = kGemmMaxTiles; g.num_sms = m->num_sms;
-            CUDA_TRY(launch_gemm_tc(lc, EPI_RESID_F32, g));
-        }
-        // --- feed-forward sublayer (Paso 6) ---
-        if (small) {
-            {
-                PROF(QW_PROF_GATEUP);
-                CUDA_TRY(launch_gemv_gateup(lc, T, m->x, w_post, c.rms_eps, m->bg + (size_t)l * I * D,
-                                            m->bu + (size_t)l * I * D, I, D, m->act));
-            }
-            PROF(QW_PROF_DOWN);
-            CUDA_TRY(launch_gemv_resid(lc, T, m->act, m->bd + (size_t)l * D * I, D, I, m->x));
-        } else {
-            {
-                PROF(QW_PROF_RMSNORM);
-                CUDA_TRY(launch_rmsnorm(lc, m->x, nullptr, T, D, w_post, c.rms_eps, m->h));
-            }
-            GemmArgs g = {};
-            g.tmA = &m->tm_wg; g.tmA2 = &m->tm_wu; g.tmB = m->tm_h;
-            g.a_row0 = l * I; g.a2_row0 = l * I; g.M = I; g.K = D; g.T = T;
-            g.out_h = m->act; g.ld_out = I; g.status = m->status; g.part = m->gpart; g.part_bytes = kGemmPartBytes; g.tickets = m->gtick; g.max_tiles = kGemmMaxTiles; g.num_sms = m->num_sms;
-            {
-                PROF(QW_PROF_GATEUP);
-                CUDA_TRY(launch_gemm_tc(lc, EPI_SILU_MUL, g));
-            }
-            GemmArgs g2 = {};
-            g2.tmA = &m->tm_wd; g2.tmA2 = &m->tm_wd; g2.tmB = m->tm_act;
-            g2.a_row0 = l * D; g2.a2_row0 = g2.a_row0; g2.M = D; g2.K = I; g2.T = T;
-            g2.out_f32 = m->x; g2.ld_out = D; g2.status = m->status; g2.part = m->gpart; g2.part_bytes = kGemmPartBytes; g2.tickets = m->gtick; g2.max_tiles = kGemmMaxTiles; g2.num_sms = m->num_sms;
-            PROF(QW_PROF_DOWN);
-            CUDA_TRY(launch_gemm_tc(lc, EPI_RESID_F32, g2));
-        }
-        if (dbg)
-            CUDA_TRY(cudaMemcpyAsync(m->dbg_hidden + (size_t)l * T * D, m->x, (size_t)T * D * 4,
-                                     cudaMemcpyDeviceToDevice, st));
+    // The first kernel of a step waits for everything before it (no programmatic overlap), so
+    // kernels of this step may read state written by earlier steps before their own wait.
+    const LaunchCtx lc0 = {st, false, launches};
+    CUDA_TRY(launch_step_begin(lc0, sd, tokens, m->embed, c.vocab, D, m->x, tv, kvv, m->status));
+    // A decode batch of >= 16 sequences runs as two halves on two streams, so that one
+    // half's latency-bound projections overlap the other half's HBM-bound attention.
+    const bool two = !prefill && !small && !dbg && m->prof_kind == QW_PROF_OFF && m->split_decode && T >= 16;
+    if (two) {
+        const int h0 = T / 2;
+        CUDA_TRY(cudaEventRecord(m->ev_fork, st));
+        CUDA_TRY(cudaStreamWaitEvent(m->aux_stream, m->ev_fork, 0));
+        QW_TRY(run_layers(m, kv, sd, prefill, max_keys, 0, h0, st, false, launches, pc));
+        QW_TRY(run_layers(m, kv, sd, prefill, max_keys, h0, T - h0, m->aux_stream, false, launches, pc));
+        CUDA_TRY(cudaEventRecord(m->ev_join, m->aux_stream));
+        CUDA_TRY(cudaStreamWaitEvent(st, m->ev_join, 0));
+    } else {
+        QW_TRY(run_layers(m, kv, sd, prefill, max_keys, 0, T, st, dbg, launches, pc));
     }
+    LaunchCtx lc = {st, false, launches};  // the head follows a full dependency on the layers
+    const bool pdl_on = m->pdl && m->prof_kind == QW_PROF_OFF;
+#define PROF(kind) ProfScope prof_scope_(m, kind, pc, st)
     // --- final norm + tied LM head + greedy argmax (Paso 8) ---
     if (B <= kSmallT) {
         PROF(QW_PROF_LMHEAD);
@@ -847,13 +912,15 @@ static qw_status run_step(qw_model* m, qw_kv* kv, const StepDesc& sd, bool prefi
             PROF(QW_PROF_RMSNORM);
             CUDA_TRY(launch_rmsnorm(lc, m->x, m->last, B, D, m->fnorm, c.rms_eps, m->h));
         }
+        lc.pdl = pdl_on;
         PROF(QW_PROF_LMHEAD);
         GemmArgs g = {};
-        g.tmA = &m->tm_embed; g.tmA2 = &m->tm_embed; g.tmB = m->tm_h;
-        g.a_row0 = 0; g.a2_row0 = 0; g.M = c.vocab; g.K = D; g.T = B;
-        g.logits = logits; g.ld_out = c.vocab; g.best = m->best; g.status = m->status; g.part = m->gpart; g.part_bytes = kGemmPartBytes; g.tickets = m->gtick; g.max_tiles = kGemmMaxTiles; g.num_sms = m->num_sms;
+        g.tmA = &m->tm_embed; g.tmB = m->tm_h;
+        g.a_row0 = 0; g.M = c.vocab; g.K = D; g.T = B;
+        g.logits = logits; g.ld_out = c.vocab; g.best = m->best; g.status = m->status; g.num_sms = m->num_sms;
         CUDA_TRY(launch_gemm_tc(lc, EPI_ARGMAX, g));
     }
+    lc.pdl = pdl_on;
     CUDA_TRY(launch_finalize(lc, sd, m->best, next, kvv));
 #undef PROF
     return QW_OK;
@@ -947,6 +1014,7 @@ extern "C" qw_status qw_decode_step(qw_model* m, qw_kv* kv, int B, const int* se
         key.push_back(m->prof_kind);
         key.push_back(m->use_mk ? 1 : 0);
         key.push_back(m->pdl ? 1 : 0);
+        key.push_back(m->split_decode ? 1 : 0);
         key.push_back(m->prof_kind || m->trace ? (long long)m->prof_gen : 0);
         for (int b = 0; b < B; ++b) key.push_back(seq_ids[b]);
         auto it = m->graphs.find(key);

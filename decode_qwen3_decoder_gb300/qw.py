@@ -239,6 +239,7 @@ def qw_lm_head_argmax_noalloc(model: int, B: int, x_ptr: int, logits_ptr: int, n
 
 QW_OPT_PERSISTENT_DECODE = 1
 QW_OPT_PDL = 2
+QW_OPT_SPLIT_DECODE = 3
 
 
 def qw_set_option(model: int, option: int, value: int) -> None:

@@ -225,7 +225,12 @@ enum {
      * same operations. */
     QW_OPT_PERSISTENT_DECODE = 1,
     /* 1 (default): consecutive launches use programmatic dependent launch. */
-    QW_OPT_PDL = 2
+    QW_OPT_PDL = 2,
+    /* 1 (default): a decode step of >= 16 sequences runs as two halves on two streams whose
+     * kernels overlap (each half's projections run while the other half's attention reads
+     * the KV cache); 0: one chain. Results agree within rounding (the attention's key split
+     * depends on the batch size). */
+    QW_OPT_SPLIT_DECODE = 3
 };
 qw_status qw_set_option(qw_model* m, int option, int value);
 

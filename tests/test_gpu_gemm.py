@@ -86,3 +86,38 @@ def test_batch_invariance_and_determinism(blk):
     g1 = run.prefill([5], [prompts[5]], debug=False, reserve_extra=2)
     d1 = run.decode([5], g1["next"].tolist(), debug=False)
     check_logits(d1["logits"][0], res[0][5], tol=2e-2)
+
+
+@pytest.mark.parametrize("B", [17, 32])
+def test_two_stream_decode(blk, B):
+    """A decode batch of >= 16 sequences runs as two halves on two streams (ragged halves for
+    odd B); every sequence still matches the oracle, and the one-chain run agrees within
+    rounding."""
+    run, om = blk
+    qw, eng = run.qw, run.eng
+    seqs = list(range(B))
+    prompts = [synth.make_tokens(S1.vocab, 2 + (i % 5), 1100 + i).tolist() for i in range(B)]
+    forced = synth.make_tokens(S1.vocab, 2 * B, 1177).reshape(2, B)
+    out = {}
+    for split in (1, 0):
+        qw.qw_set_option(eng.model, qw.QW_OPT_SPLIT_DECODE, split)
+        qw.qw_kv_reset(eng.kv, -1, eng.stream)
+        g = run.prefill(seqs, prompts, debug=False, reserve_extra=3)
+        caches = []
+        for b, p in enumerate(prompts):
+            c = oracle.SeqCache(1)
+            oracle.forward(om, p, c)
+            caches.append(c)
+        logits = []
+        for step in range(2):
+            d = run.decode(seqs, forced[step].tolist(), debug=False)
+            assert d["status"] == 0
+            for b in range(B):
+                o = oracle.forward(om, [int(forced[step, b])], caches[b])
+                check_logits(d["logits"][b], o["logits"])
+                check_token(d["next"][b], o["logits"])
+            logits.append(d["logits"])
+        out[split] = logits
+    qw.qw_set_option(eng.model, qw.QW_OPT_SPLIT_DECODE, 1)
+    for a, b in zip(out[1], out[0]):
+        check_logits(a, b, tol=2e-2)
