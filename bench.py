@@ -310,7 +310,8 @@ def run_ours(args, cfg, rank, world):
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": cfg["unit"], "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16 weights x f32 activations, f32 accumulate, f16 KV cache",
         "data": "synthetic (seeded random-init bf16 weights N(0,0.02), uniform-random token ids)",
         "config": {"workload": cfg["workload"], "batch": B, "prompt_tokens": P, "decode_steps": ND,
                    "tokens_per_step": tokens_per_step, "parallelism": f"replicas x{world} (no collective)",
@@ -494,7 +495,9 @@ def run_other(args, cfg, rank, world):
                  "mean_cached_len": float(np.mean(lens))}
     out = {"metric": METRIC, "value": round(value, 2), "unit": cfg["unit"], "n_gpus": world, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4), "higher_is_better": True,
-           "scaling": "weak", "vs_baseline": None, "dtype": "f16 operands / f32 accumulate (bf16 weights)",
+           "scaling": "weak", "vs_baseline": None, "dtype": "f16 tensor-core operands (bf16 weights converted), f32 accumulate, f16 KV cache"
+           if (int(lens.sum()) if kind == "prefill" else B) > 8 else
+           "bf16 weights x f32 activations, f32 accumulate, f16 KV cache",
            "data": "synthetic (seeded random-init bf16 weights N(0,0.02), uniform-random token ids)",
            "config": dict({"workload": cfg["workload"], "batch": B, "l2": "working set exceeds L2; no flush"}, **extra),
            "roofline": roofline,
