@@ -93,13 +93,42 @@ struct AttnP {
     int* counters;      // [T][n_kv]
     f16* out;           // [T][n_heads * 128]
     float scale_log2;   // head_dim^-0.5 * log2(e)
+    // decode: sequence of each token (kernel parameter), so that the pages cached by earlier
+    // steps can be prefetched into L2 before the dependency wait; prefetch = 0 turns it off
+    int prefetch;
+    int seqp[QW_MAX_BATCH];
 };
 
 constexpr int AW = 4;  // warps per CTA
 
+__device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
+}
+
 template <bool FUSED>
-__global__ void __launch_bounds__(AW * 32) k_attn_paged(AttnP p) {
+__global__ void __launch_bounds__(AW * 32) k_attn_paged(const __grid_constant__ AttnP p) {
     pdl_launch();
+    if (p.prefetch) {
+        // the sequence length and page table were written before this step began (the step's
+        // first kernel waits for everything earlier), so the first cached page of each warp
+        // (the warps take pages round-robin) can be requested into L2 while the projection is
+        // still running; only the first, so that a large batch does not overflow L2
+        const int t = blockIdx.z, g = blockIdx.y, s = blockIdx.x;
+        const int seq = p.seqp[t];
+        const int len = p.kv.len[seq];
+        const int k0 = s * p.chunk, k1 = min(k0 + p.chunk, len);
+        const int* pt = p.kv.page_table + (size_t)seq * p.kv.max_pages_per_seq;
+        const size_t lay = (size_t)p.layer * p.kv.layer_stride;
+        const int pg = (k0 >> 4) + threadIdx.x;
+        if (threadIdx.x < AW && pg < ((k1 + 15) >> 4)) {
+            const int page = pt[pg];
+            if (page >= 0 && page < p.kv.n_pages) {
+                const size_t off = lay + ((size_t)page * p.n_kv + g) * 16 * 128;
+                prefetch_l2(p.kv.k + off, 16 * 128 * 2);
+                prefetch_l2(p.kv.v + off, 16 * 128 * 2);
+            }
+        }
+    }
     pdl_wait();
     const int t = blockIdx.z, g = blockIdx.y, s = blockIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -334,8 +363,12 @@ __global__ void __launch_bounds__(AW * 32) k_attn_paged(AttnP p) {
 cudaError_t launch_attn_paged(const LaunchCtx& c, int T, int layer, const f16* q, int n_heads,
                               int n_kv, TokView tv, KVView kv, int chunk, int n_splits,
                               float* part_o, float* part_ml, int* counters, f16* out,
-                              const AttnFuse* fuse) {
+                              const AttnFuse* fuse, const int* decode_seqs) {
     AttnP p = {};
+    if (decode_seqs) {
+        p.prefetch = 1;
+        for (int t = 0; t < T; ++t) p.seqp[t] = decode_seqs[t];
+    }
     p.q = q;
     p.n_heads = n_heads;
     p.n_kv = n_kv;

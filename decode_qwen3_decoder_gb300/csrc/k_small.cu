@@ -202,10 +202,23 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) k_gemv(GemvP p) {
         }
     };
     if (gw * RPW < p.n_out) load_pass(gw * RPW, 0);
+    // the RMSNorm weight slice of this thread is constant too: also before the wait
+    constexpr int NCH = K / 512;  // float4 chunks of a row per thread (norm prologue)
+    uint2 nwv[NCH > 0 ? NCH : 1];
+    if (MODE != G_RESID) {
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) nwv[c] = *reinterpret_cast<const uint2*>(p.norm_w + (tid + c * 128) * 4);
+    }
     pdl_wait();
 
     // ---- prologue: activations into shared memory --------------------------------------
+    float xres[RPW];  // G_RESID: residual x[token = lane][row] of this warp's first rows
     if (MODE == G_RESID) {
+#pragma unroll
+        for (int rr = 0; rr < RPW; ++rr) {
+            const int row = gw * RPW + rr;
+            xres[rr] = (lane < p.T && row < p.n_out) ? p.out[(size_t)lane * p.n_out + row] : 0.f;
+        }
         for (int i = tid; i < TT * K / 8; i += blockDim.x) {
             const int t = i / (K / 8), k8 = (i % (K / 8)) * 8;
             float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
@@ -218,32 +231,41 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) k_gemv(GemvP p) {
             *reinterpret_cast<float4*>(hs + t * K + k8 + 4) = a1;
         }
     } else {
-        __shared__ float rs[TT];
-        for (int t = warp; t < TT; t += GEMV_WARPS) {
-            float ss = 0.f;
-            if (t < p.T) {
-                const float* xr = p.x + (size_t)(p.rows ? p.rows[t] : t) * K;
-                for (int k = lane * 4; k < K; k += 128) {
-                    float4 v = *reinterpret_cast<const float4*>(xr + k);
-                    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-                }
+        // one read of x: each thread stores its chunks of every token row raw into shared
+        // memory while summing their squares; the sums meet in shared memory, then each
+        // thread rescales its own chunks to h = x * rsqrt(mean(x^2) + eps) * w
+        static_assert(K % 512 == 0, "norm prologue: 128 threads x float4 chunks");
+        __shared__ float red[GEMV_WARPS][TT];
+#pragma unroll
+        for (int t = 0; t < TT; ++t) {
+            float part = 0.f;
+            const bool live = t < p.T;
+            const float* xr = p.x + (size_t)(live ? (p.rows ? p.rows[t] : t) : 0) * K;
+#pragma unroll
+            for (int c = 0; c < NCH; ++c) {
+                const float4 v = live ? *reinterpret_cast<const float4*>(xr + (tid + c * 128) * 4)
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+                *reinterpret_cast<float4*>(hs + t * K + (tid + c * 128) * 4) = v;
+                part += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
             }
-            ss = warp_sum(ss);
-            if (lane == 0) rs[t] = rsqrtf(ss / (float)K + p.eps);
+            part = warp_sum(part);
+            if (lane == 0) red[warp][t] = part;
         }
         __syncthreads();
-        for (int i = tid; i < TT * K / 4; i += blockDim.x) {
-            const int t = i / (K / 4), k4 = (i % (K / 4)) * 4;
-            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (t < p.T) {
-                const float* xr = p.x + (size_t)(p.rows ? p.rows[t] : t) * K;
-                float4 v = *reinterpret_cast<const float4*>(xr + k4);
-                uint2 wb = *reinterpret_cast<const uint2*>(p.norm_w + k4);
-                const float r = rs[t];
-                o = make_float4(v.x * r * bf_lo(wb.x), v.y * r * bf_hi(wb.x), v.z * r * bf_lo(wb.y),
-                                v.w * r * bf_hi(wb.y));
+#pragma unroll
+        for (int t = 0; t < TT; ++t) {
+            float ss = 0.f;
+#pragma unroll
+            for (int w = 0; w < GEMV_WARPS; ++w) ss += red[w][t];
+            const float r = rsqrtf(ss / (float)K + p.eps);
+#pragma unroll
+            for (int c = 0; c < NCH; ++c) {
+                float4* hp = reinterpret_cast<float4*>(hs + t * K + (tid + c * 128) * 4);
+                const float4 v = *hp;
+                const uint2 wb = nwv[c];
+                *hp = make_float4(v.x * r * bf_lo(wb.x), v.y * r * bf_hi(wb.x), v.z * r * bf_lo(wb.y),
+                                  v.w * r * bf_hi(wb.y));
             }
-            *reinterpret_cast<float4*>(hs + t * K + k4) = o;
         }
     }
     __syncthreads();
@@ -253,7 +275,7 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) k_gemv(GemvP p) {
 #pragma unroll
     for (int t = 0; t < TT; ++t) best[t] = 0ull;
 
-    bool first = true;
+    bool first = true, first_rows = true;
     for (int r0 = gw * RPW; r0 < p.n_out; r0 += nw * RPW) {
         float acc[RPW][NW][TT];
 #pragma unroll
@@ -294,7 +316,8 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) k_gemv(GemvP p) {
                         if (MODE == G_QKV) {
                             p.out[(size_t)t * p.n_out + row] = acc[rr][0][t];
                         } else if (MODE == G_RESID) {
-                            p.out[(size_t)t * p.n_out + row] += acc[rr][0][t];
+                            float* o = p.out + (size_t)t * p.n_out + row;
+                            *o = (first_rows ? xres[rr] : *o) + acc[rr][0][t];
                         } else if (MODE == G_GATEUP) {
                             const float g = acc[rr][0][t], u = acc[rr][NW - 1][t];
                             p.out_h[(size_t)t * p.n_out + row] = __float2half_rn(silu_f(g) * u);
@@ -306,6 +329,7 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) k_gemv(GemvP p) {
                 }
             }
         }
+        first_rows = false;
     }
 
     if (MODE == G_LMHEAD) {

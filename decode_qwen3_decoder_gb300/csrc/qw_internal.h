@@ -148,7 +148,7 @@ struct AttnFuse {
 cudaError_t launch_attn_paged(const LaunchCtx& c, int T, int layer, const f16* q, int n_heads,
                               int n_kv, TokView tv, KVView kv, int chunk, int n_splits,
                               float* part_o, float* part_ml, int* counters, f16* out,
-                              const AttnFuse* fuse);
+                              const AttnFuse* fuse, const int* decode_seqs);  // host ids (decode) or NULL
 // Causal flash attention of a prefill (sequences start empty) over the K/V just appended to
 // the paged cache.
 cudaError_t launch_attn_prefill(const LaunchCtx& c, const StepDesc& sd, int max_len, int layer, const f16* q,

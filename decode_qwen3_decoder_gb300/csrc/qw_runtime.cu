@@ -766,13 +766,13 @@ static qw_status run_layers(qw_model* m, qw_kv* kv, const StepDesc& sd, bool pre
                 }
                 PROF(QW_PROF_ATTN);
                 LAUNCH(launch_attn_paged(lc, T, l, q, c.n_heads, c.n_kv_heads, tv, kvv, sp.chunk, sp.n_splits,
-                                         part_o, part_ml, counters, attn, nullptr));
+                                         part_o, part_ml, counters, attn, nullptr, nullptr));
             } else {
                 // decode: one new token per sequence; QK-norm, RoPE and the KV append run inside
                 AttnFuse fz = {qkv, w_qn, w_kn, c.rms_eps, m->rcos, m->rsin, lpos, lslot, m->status};
                 PROF(QW_PROF_ATTN);
                 LAUNCH(launch_attn_paged(lc, T, l, q, c.n_heads, c.n_kv_heads, tv, kvv, sp.chunk, sp.n_splits,
-                                         part_o, part_ml, counters, attn, &fz));
+                                         part_o, part_ml, counters, attn, &fz, sd.seq + t0));
             }
         } else {
             // q, k, v were normalised, rotated and appended by the projection's epilogue
@@ -781,7 +781,7 @@ static qw_status run_layers(qw_model* m, qw_kv* kv, const StepDesc& sd, bool pre
                 LAUNCH(launch_attn_prefill(lc, sd, max_keys, l, q, kvv, c.n_heads, c.n_kv_heads, attn));
             else
                 LAUNCH(launch_attn_paged(lc, T, l, q, c.n_heads, c.n_kv_heads, tv, kvv, sp.chunk, sp.n_splits,
-                                         part_o, part_ml, counters, attn, nullptr));
+                                         part_o, part_ml, counters, attn, nullptr, sd.seq + t0));
         }
         if (small) {
             PROF(QW_PROF_OPROJ);
