@@ -15,6 +15,7 @@
 // per-head QK-norm and rotate-half RoPE (Paso 5, Paso 4) to its two query heads and its KV
 // head from the fp32 q|k|v projection row, keeps q in fp32, and the CTA whose split holds
 // the new position appends the new K/V to its page slot before reading it back.
+#include <algorithm>
 #include <utility>
 
 #include "qw_internal.h"
@@ -653,4 +654,466 @@ cudaError_t launch_attn_prefill(const LaunchCtx& c, const StepDesc& sd, int max_
     }
     const int qtiles = (max_len + PF_Q - 1) / PF_Q;
     return launch_k(c, k_attn_prefill, dim3(qtiles, n_kv, sd.B), dim3(PF_WARPS * 32), (size_t)smem, p);
+}
+
+// =======================================================================================
+// k_attn_decode: decode attention over long or many caches (Paso 5), one new token per
+// sequence, q already normalised and rotated (fp16) and its K/V already in the cache.
+//
+// The work items (token t, KV head g, page i) are laid out token-major, then head, then page,
+// and split into equal contiguous ranges over a fixed grid (2 CTAs per SM), so ragged cache
+// lengths cost no load imbalance and no wave tail. A CTA walks its range as segments (the
+// pages of one (t, g) pair inside the range). A producer warp streams each page's K and V
+// blocks with TMA tensor copies (the pools seen as [rows, 128] fp16, boxes of 16 rows x 64
+// dims with the 128-byte swizzle) into a 12-stage shared-memory ring; four consumer warps take
+// the pages of a segment round-robin. Per page a warp computes S = Q K^T and O += P V with
+// mma.sync m16n8k16 (fp16 operands, fp32 accumulation; the two query heads 2g, 2g+1 are rows
+// 0 and 1 of a 16-row tile), keeping the online softmax in fp32 in the exp2 domain. A segment
+// that covers its whole pair writes the output; otherwise the partial (m, l, o) goes to its
+// slot and the CTA that finishes the pair last (atomic ticket, no waiting) merges the slots
+// in order. Cache lengths and page tables were written before the step began, so the ring is
+// filled before the dependency wait, except a pair's newest page, which the kernel that
+// precedes this one writes.
+// =======================================================================================
+namespace {
+
+constexpr int AD_CW = 4;                      // consumer warps
+constexpr int AD_THREADS = (AD_CW + 1) * 32;  // + producer warp
+constexpr int AD_NST = 12;                    // ring stages
+// Within a segment consumer warp w takes items k = k_base + w, + CW, ...; it waits for a
+// stage by phase parity, which is sound only if the previous use of the same stage (item
+// k - NST) was its own (or belongs to an earlier segment, closed by the merge barrier).
+static_assert(AD_NST % AD_CW == 0, "ring depth must be a multiple of the consumer warps");
+constexpr int AD_BOX = 16 * 128;              // bytes of one 16-row x 64-dim box
+constexpr int AD_STAGE = 4 * AD_BOX;          // K dims 0-63, K 64-127, V 0-63, V 64-127
+constexpr unsigned long long AD_WAIT_NS = 2000000000ull;
+
+__device__ __forceinline__ uint32_t ad_smem(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ bool ad_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// bounded wait; false after ~2 s or when another role gave up
+__device__ __forceinline__ bool ad_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    if (ad_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    uint32_t n = 0;
+    while (true) {
+        if (ad_try_wait(bar, parity)) return true;
+        if ((++n & 255u) == 0) {
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > AD_WAIT_NS) return false;
+        }
+    }
+}
+
+// the CTA whose item range [c N / G, (c + 1) N / G) holds item j
+__device__ __forceinline__ int ad_cta_of(long long j, long long N, int G) {
+    return (int)(((j + 1) * G - 1) / N);
+}
+
+// byte offset of 16-byte chunk `ch` (0..7) of row r inside a 128-byte-swizzled box
+__device__ __forceinline__ uint32_t ad_swz(int r, int ch) { return (uint32_t)(r * 128 + ((ch ^ (r & 7)) << 4)); }
+
+__device__ __forceinline__ void ad_tma_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+}  // namespace
+
+struct AttnDP {
+    CUtensorMap tmK;     // K pool [n_layers * n_pages * n_kv * 16, 128] fp16
+    CUtensorMap tmV;
+    const f16* q;        // [T][n_heads][128]
+    f16* out;            // [T][n_heads][128]
+    KVView kv;
+    int layer, n_heads, n_kv, T;
+    float* part_o;       // [T][n_heads][max_slots][128]
+    float* part_ml;      // [T][n_heads][max_slots][2]
+    int* counters;       // [T][n_kv], zero between launches
+    int max_slots;
+    int* status;
+    float scale_log2;
+    int seqp[QW_MAX_BATCH];  // sequence of each token
+};
+
+// shared-memory layout of k_attn_decode (byte offsets from a 1024-aligned base)
+constexpr int AD_OFF_FULL = AD_NST * AD_STAGE;                 // ring first
+constexpr int AD_OFF_EMPTY = AD_OFF_FULL + AD_NST * 8;
+constexpr int AD_OFF_FLAGS = AD_OFF_EMPTY + AD_NST * 8;
+constexpr int AD_OFF_PREF = AD_OFF_FLAGS + 16;                 // [T + 1] page prefix
+constexpr int AD_OFF_NKEY = AD_OFF_PREF + ((QW_MAX_BATCH + 1) * 4 + 15) / 16 * 16;  // [T] keys
+constexpr int AD_OFF_SMO = AD_OFF_NKEY + QW_MAX_BATCH * 4;     // [CW][2][128]
+constexpr int AD_OFF_SMM = AD_OFF_SMO + AD_CW * 2 * 128 * 4;   // [CW][2]
+constexpr int AD_OFF_SML = AD_OFF_SMM + AD_CW * 2 * 4;         // [CW][2]
+constexpr int AD_SMEM = 1024 + AD_OFF_SML + AD_CW * 2 * 4;     // + alignment slack
+static_assert(AD_OFF_FULL % 8 == 0 && AD_OFF_PREF % 16 == 0, "alignment");
+
+__global__ void __launch_bounds__(AD_THREADS) k_attn_decode(const __grid_constant__ AttnDP p) {
+    extern __shared__ uint8_t ad_raw_[];
+    uint8_t* ad_raw = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(ad_raw_) + 1023) & ~(uintptr_t)1023);
+    uint8_t* ring = ad_raw;
+    uint64_t* full = reinterpret_cast<uint64_t*>(ad_raw + AD_OFF_FULL);
+    uint64_t* empty = reinterpret_cast<uint64_t*>(ad_raw + AD_OFF_EMPTY);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(ad_raw + AD_OFF_FLAGS);
+    volatile int* last_flag = abort_flag + 1;
+    int* pref = reinterpret_cast<int*>(ad_raw + AD_OFF_PREF);
+    int* nkey = reinterpret_cast<int*>(ad_raw + AD_OFF_NKEY);
+    float* sm_o = reinterpret_cast<float*>(ad_raw + AD_OFF_SMO);
+    float* sm_m = reinterpret_cast<float*>(ad_raw + AD_OFF_SMM);
+    float* sm_l = reinterpret_cast<float*>(ad_raw + AD_OFF_SML);
+
+    pdl_launch();
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int T = p.T, G = gridDim.x, c = blockIdx.x;
+    // ---- work layout (cache lengths are stable during the step: before the wait) ----------
+    for (int t = tid; t < T; t += AD_THREADS) nkey[t] = p.kv.len[p.seqp[t]] + 1;
+    if (tid == 0) {
+        for (int s = 0; s < AD_NST; ++s) {
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(ad_smem(full + s)) : "memory");
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(ad_smem(empty + s)) : "memory");
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == AD_CW && lane == 0) {
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&p.tmK) : "memory");
+        asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&p.tmV) : "memory");
+    }
+    __syncthreads();
+    if (warp == 0) {  // exclusive prefix of pages per token
+        int run = 0;
+        for (int t0 = 0; t0 < T; t0 += 32) {
+            const int t = t0 + lane;
+            const int v = t < T ? (nkey[t] + 15) >> 4 : 0;
+            int x = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += y;
+            }
+            if (t < T) pref[t] = run + x - v;
+            run += __shfl_sync(0xffffffffu, x, 31);
+        }
+        if (lane == 0) pref[T] = run;
+    }
+    __syncthreads();
+    const long long N = (long long)p.n_kv * pref[T];
+    const long long i_begin = (long long)c * N / G, i_end = (long long)(c + 1) * N / G;
+
+    // segment iterator: item j -> token t (largest with n_kv * pref[t] <= j), head, page
+    auto segment = [&](long long j, int& t, int& g, int& i0, int& n) {
+        int lo = 0, hi = T - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if ((long long)p.n_kv * pref[mid] <= j) lo = mid; else hi = mid - 1;
+        }
+        t = lo;
+        const int np = pref[t + 1] - pref[t];
+        const long long rel = j - (long long)p.n_kv * pref[t];
+        g = (int)(rel / np);
+        i0 = (int)(rel % np);
+        const long long seg_end = min(i_end, (long long)p.n_kv * pref[t] + (long long)(g + 1) * np);
+        n = (int)(seg_end - j);
+    };
+
+    if (warp == AD_CW) {
+        // ---------------- producer (the whole warp; lane 0 issues) ----------------
+        // page ids are fetched 32 at a time, one per lane, so the issue loop does not wait
+        // on a page-table load per page
+        bool waited = false;
+        int k = 0;
+        const long long layer_rows = (long long)p.layer * p.kv.n_pages;
+        for (long long j = i_begin; j < i_end && !*abort_flag;) {
+            int t, g, i0, n;
+            segment(j, t, g, i0, n);
+            const int* pt = p.kv.page_table + (size_t)p.seqp[t] * p.kv.max_pages_per_seq;
+            const int newest = ((nkey[t] + 15) >> 4) - 1;
+            bool stop = false;
+            for (int c0 = 0; c0 < n && !stop; c0 += 32) {
+                const int il = i0 + c0 + lane;
+                int pid = (c0 + lane < n && il < p.kv.max_pages_per_seq) ? pt[il] : -1;
+                if (c0 + lane < n && (pid < 0 || pid >= p.kv.n_pages)) {
+                    atomicOr(p.status, QW_DEV_BAD_POS);
+                    pid = 0;  // any valid block; the result is flagged
+                }
+                const int cn = min(32, n - c0);
+                for (int jj = 0; jj < cn; ++jj, ++k) {
+                    const int page = __shfl_sync(0xffffffffu, pid, jj);
+                    const int i = i0 + c0 + jj;
+                    if (!waited && i == newest) {  // written by the preceding kernel
+                        pdl_wait();
+                        waited = true;
+                    }
+                    const int s = k % AD_NST;
+                    int ok = 1;
+                    if (lane == 0 && k >= AD_NST && !ad_wait(ad_smem(empty + s), ((k / AD_NST) & 1) ^ 1, abort_flag)) {
+                        *abort_flag = 1;
+                        ok = 0;
+                    }
+                    if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                        stop = true;
+                        break;
+                    }
+                    if (lane == 0) {
+                        const int row = (int)(((layer_rows + page) * p.n_kv + g) * 16);
+                        const uint32_t dst = ad_smem(ring + s * AD_STAGE), bar = ad_smem(full + s);
+                        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(AD_STAGE)
+                                     : "memory");
+                        ad_tma_2d(dst, &p.tmK, bar, 0, row);
+                        ad_tma_2d(dst + AD_BOX, &p.tmK, bar, 64, row);
+                        ad_tma_2d(dst + 2 * AD_BOX, &p.tmV, bar, 0, row);
+                        ad_tma_2d(dst + 3 * AD_BOX, &p.tmV, bar, 64, row);
+                    }
+                }
+            }
+            j += n;
+        }
+        if (!waited) pdl_wait();
+        // before the CTA can retire, every copy issued must have landed (at once on the
+        // normal path; bounded when the consumers gave up)
+        if (lane == 0) {
+            for (int kk = max(0, k - AD_NST); kk < k; ++kk) {
+                const uint32_t bar = ad_smem(full + kk % AD_NST), par = (kk / AD_NST) & 1;
+                const uint64_t t0 = globaltimer_ns();
+                while (!ad_try_wait(bar, par) && globaltimer_ns() - t0 < AD_WAIT_NS) {
+                }
+            }
+        }
+        return;  // the producer takes no part in the consumers' named barriers
+    }
+
+    // ---------------- consumers ----------------
+    pdl_wait();  // q is written by the preceding kernel
+    const int gq = lane >> 2, tq = lane & 3;  // mma fragment row group / column pair
+    int k_base = 0;
+    for (long long j = i_begin; j < i_end;) {
+        int t, g, i0, n;
+        segment(j, t, g, i0, n);
+        // Q as the A operand: rows 0 and 1 = heads 2g, 2g+1 (lanes 0-7); rows 2-15 are zero
+        uint32_t qa[8][2];  // per k-step: (row gq, dims 16ks + 2tq..) and (row gq, dims +8)
+        {
+            const bool live = gq < 2;
+            const f16* qp = p.q + ((size_t)t * p.n_heads + 2 * g + (live ? gq : 0)) * 128 + 2 * tq;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                qa[ks][0] = live ? *reinterpret_cast<const uint32_t*>(qp + 16 * ks) : 0u;
+                qa[ks][1] = live ? *reinterpret_cast<const uint32_t*>(qp + 16 * ks + 8) : 0u;
+            }
+        }
+        float m_r = -INFINITY, l_r = 0.f;  // this lane's row (head gq for lanes 0-7)
+        float o[16][4];
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+        const int nk = nkey[t];
+        for (int jj = warp; jj < n; jj += AD_CW) {
+            const int k = k_base + jj, s = k % AD_NST;
+            if (*abort_flag) continue;
+            if (!ad_wait(ad_smem(full + s), (k / AD_NST) & 1, abort_flag)) {
+                *abort_flag = 1;
+                atomicOr(p.status, QW_DEV_TIMEOUT);
+                continue;
+            }
+            uint8_t* st = ring + s * AD_STAGE;
+            const uint32_t sa = ad_smem(st);
+            const int nvalid = min(16, nk - (i0 + jj) * 16);
+            if (nvalid < 16) {
+                // slots past the last key hold stale pool data (possibly not finite): zero
+                // their V rows so that 0-weight keys add exactly nothing
+                for (int e = lane; e < (16 - nvalid) * 16; e += 32) {
+                    const int r = nvalid + (e >> 4), box = 2 + ((e >> 3) & 1), ch = e & 7;
+                    *reinterpret_cast<uint4*>(st + box * AD_BOX + ad_swz(r, ch)) = make_uint4(0u, 0u, 0u, 0u);
+                }
+                __syncwarp();
+            }
+            // ---- S = Q K^T: 16 rows x 16 keys (two 8-key tiles), 8 k-steps of 16 dims ----
+            float sc[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) {
+                // matrices: (keys 0-7 | 8-15) x (dims 16ks..+7 | +8..+15)
+                const int key = (lane & 7) + ((lane >> 4) & 1) * 8;
+                const int chg = 2 * ks + ((lane >> 3) & 1);  // 16-byte chunk of the 128 dims
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4(sa + (chg >> 3) * AD_BOX + ad_swz(key, chg & 7), b0, b1, b2, b3);
+                const uint32_t a[4] = {qa[ks][0], 0u, qa[ks][1], 0u};
+                mma16816(sc[0], a, b0, b1);
+                mma16816(sc[1], a, b2, b3);
+            }
+            // ---- online softmax (exp2 domain) on this lane's row ----
+            float mx = -INFINITY;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int key = nt * 8 + 2 * tq + e;
+                    sc[nt][e] = key < nvalid ? sc[nt][e] * p.scale_log2 : -INFINITY;
+                    mx = fmaxf(mx, sc[nt][e]);
+                }
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            const float mn = fmaxf(m_r, mx);
+            const float alpha = (m_r == -INFINITY) ? 0.f : exp2f(m_r - mn);
+            m_r = mn;
+            float pv[2][2];
+            float ls = 0.f;
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    pv[nt][e] = exp2f(sc[nt][e] - mn);
+                    ls += pv[nt][e];
+                }
+            l_r = l_r * alpha + ls;
+#pragma unroll
+            for (int nt = 0; nt < 16; ++nt) {
+                o[nt][0] *= alpha;
+                o[nt][1] *= alpha;
+            }
+            // P as the A operand of P V (rows 8-15 zero)
+            const uint32_t pa[4] = {pack_h2(pv[0][0], pv[0][1]), 0u, pack_h2(pv[1][0], pv[1][1]), 0u};
+            // ---- O += P V: 16 dims tiles of 8, keys 0-15 in one k-step ----
+#pragma unroll
+            for (int np = 0; np < 8; ++np) {
+                const int key = (lane & 7) + ((lane >> 3) & 1) * 8;
+                const int chg = 2 * np + (lane >> 4);
+                uint32_t b0, b1, b2, b3;
+                ldsm_x4_t(sa + 2 * AD_BOX + (chg >> 3) * AD_BOX + ad_swz(key, chg & 7), b0, b1, b2, b3);
+                mma16816(o[2 * np], pa, b0, b1);
+                mma16816(o[2 * np + 1], pa, b2, b3);
+            }
+            __syncwarp();
+            if (lane == 0) {
+                // generic writes (the zeroed rows) before the next asynchronous refill
+                if (nvalid < 16) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(ad_smem(empty + s)) : "memory");
+            }
+        }
+        k_base += n;
+        // row sums over the four lanes of a row group
+        l_r += __shfl_xor_sync(0xffffffffu, l_r, 1);
+        l_r += __shfl_xor_sync(0xffffffffu, l_r, 2);
+        if (lane < 8) {
+#pragma unroll
+            for (int nt = 0; nt < 16; ++nt) {
+                sm_o[(warp * 2 + gq) * 128 + nt * 8 + 2 * tq] = o[nt][0];
+                sm_o[(warp * 2 + gq) * 128 + nt * 8 + 2 * tq + 1] = o[nt][1];
+            }
+            if (tq == 0) {
+                sm_m[warp * 2 + gq] = m_r;
+                sm_l[warp * 2 + gq] = l_r;
+            }
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(AD_CW * 32) : "memory");
+        // threads 0..127 merge: (head hh, dims d2, d2 + 1)
+        const int hh = (tid >> 6) & 1, d2 = (tid & 63) * 2;
+        const bool merger = tid < 128;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < AD_CW; ++w) M = fmaxf(M, sm_m[w * 2 + hh]);
+        float L = 0.f, O0 = 0.f, O1 = 0.f;
+#pragma unroll
+        for (int w = 0; w < AD_CW; ++w) {
+            const float f = (sm_m[w * 2 + hh] == -INFINITY) ? 0.f : exp2f(sm_m[w * 2 + hh] - M);
+            L += sm_l[w * 2 + hh] * f;
+            O0 += sm_o[(w * 2 + hh) * 128 + d2] * f;
+            O1 += sm_o[(w * 2 + hh) * 128 + d2 + 1] * f;
+        }
+        const int head = 2 * g + hh;
+        f16* outp = p.out + ((size_t)t * p.n_heads + head) * 128 + d2;
+        const int np = pref[t + 1] - pref[t];
+        const long long pair0 = (long long)p.n_kv * pref[t] + (long long)g * np;
+        if (i0 == 0 && n == np) {  // the whole pair is in this CTA
+            if (merger) *reinterpret_cast<uint32_t*>(outp) = pack_h2(O0 / L, O1 / L);
+        } else {
+            const int cf = ad_cta_of(pair0, N, G);
+            const int n_slots = ad_cta_of(pair0 + np - 1, N, G) - cf + 1;
+            const size_t slot = ((size_t)t * p.n_heads + head) * p.max_slots + (c - cf);
+            if (merger) {
+                *reinterpret_cast<float2*>(p.part_o + slot * 128 + d2) = make_float2(O0, O1);
+                if ((tid & 63) == 0) *reinterpret_cast<float2*>(p.part_ml + slot * 2) = make_float2(M, L);
+            }
+            // the CTA barrier orders every thread's partial before thread 0's fence, which
+            // releases them (cumulatively) ahead of the ticket; the last CTA's thread 0
+            // fences after the ticket (acquire) before the barrier that lets the merge read
+            asm volatile("bar.sync 1, %0;" ::"n"(AD_CW * 32) : "memory");
+            if (tid == 0) {
+                __threadfence();
+                const bool last = atomicAdd(p.counters + (size_t)t * p.n_kv + g, 1) == n_slots - 1;
+                __threadfence();
+                *last_flag = last;
+            }
+            asm volatile("bar.sync 1, %0;" ::"n"(AD_CW * 32) : "memory");
+            if (*last_flag && merger) {
+                const size_t base = ((size_t)t * p.n_heads + head) * p.max_slots;
+                float MM = -INFINITY;
+                for (int z = 0; z < n_slots; ++z) MM = fmaxf(MM, __ldcg(p.part_ml + (base + z) * 2));
+                float LL = 0.f, A0 = 0.f, A1 = 0.f;
+                for (int z = 0; z < n_slots; ++z) {
+                    const float2 ml = __ldcg(reinterpret_cast<const float2*>(p.part_ml + (base + z) * 2));
+                    const float f = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - MM);
+                    const float2 ov = __ldcg(reinterpret_cast<const float2*>(p.part_o + (base + z) * 128 + d2));
+                    LL += ml.y * f;
+                    A0 += ov.x * f;
+                    A1 += ov.y * f;
+                }
+                *reinterpret_cast<uint32_t*>(outp) = pack_h2(A0 / LL, A1 / LL);
+                if (tid == 0) p.counters[(size_t)t * p.n_kv + g] = 0;
+            }
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(AD_CW * 32) : "memory");  // shared merge buffers are reused
+        j += n;
+    }
+}
+
+int attn_decode_smem_bytes() { return AD_SMEM; }
+
+cudaError_t launch_attn_decode(const LaunchCtx& c, int T, int layer, const f16* q, int n_heads, int n_kv, KVView kv,
+                               const CUtensorMap* tmK, const CUtensorMap* tmV, const int* seqs, int max_keys,
+                               int max_slots, float* part_o, float* part_ml, int* counters, f16* out, int* status,
+                               int num_sms) {
+    AttnDP p;
+    memset(&p, 0, sizeof p);
+    p.tmK = *tmK;
+    p.tmV = *tmV;
+    p.q = q;
+    p.out = out;
+    p.kv = kv;
+    p.layer = layer;
+    p.n_heads = n_heads;
+    p.n_kv = n_kv;
+    p.T = T;
+    p.part_o = part_o;
+    p.part_ml = part_ml;
+    p.counters = counters;
+    p.max_slots = max_slots;
+    p.status = status;
+    p.scale_log2 = 0.08838834764831845f * 1.4426950408889634f;  // 128^-0.5 * log2(e)
+    for (int t = 0; t < T; ++t) p.seqp[t] = seqs[t];
+    const int smem = attn_decode_smem_bytes();
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(k_attn_decode, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    // at most one CTA per item; a pair spans at most G / n_kv + 2 CTAs (<= max_slots)
+    const long long items = (long long)T * n_kv * ((max_keys + 15) / 16);
+    int G = (int)std::min<long long>(2LL * num_sms, std::max(items, 1LL));
+    G = std::min(G, (max_slots - 2) * n_kv);
+    return launch_k(c, k_attn_decode, dim3(G), dim3(AD_THREADS), (size_t)smem, p);
 }

@@ -149,6 +149,15 @@ cudaError_t launch_attn_paged(const LaunchCtx& c, int T, int layer, const f16* q
                               int n_kv, TokView tv, KVView kv, int chunk, int n_splits,
                               float* part_o, float* part_ml, int* counters, f16* out,
                               const AttnFuse* fuse, const int* decode_seqs);  // host ids (decode) or NULL
+// Decode attention split evenly over (token, KV head, page) items for long or many caches;
+// q (fp16, normalised and rotated) and the new K/V must already be in place. seqs: host ids
+// of the T tokens' sequences; max_keys bounds every cached length + 1.
+// tmK / tmV: the K and V pools as [n_layers * n_pages * n_kv * 16, 128] fp16 maps (box 64 x 16,
+// 128-byte swizzle).
+cudaError_t launch_attn_decode(const LaunchCtx& c, int T, int layer, const f16* q, int n_heads, int n_kv, KVView kv,
+                               const CUtensorMap* tmK, const CUtensorMap* tmV, const int* seqs, int max_keys,
+                               int max_slots, float* part_o, float* part_ml, int* counters, f16* out, int* status,
+                               int num_sms);
 // Causal flash attention of a prefill (sequences start empty) over the K/V just appended to
 // the paged cache.
 cudaError_t launch_attn_prefill(const LaunchCtx& c, const StepDesc& sd, int max_len, int layer, const f16* q,

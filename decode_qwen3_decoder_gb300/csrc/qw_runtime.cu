@@ -54,6 +54,9 @@ extern "C" const char* qw_last_error(void) { return g_err.c_str(); }
 // ---------------------------------------------------------------------------------------
 static constexpr int kMaxSplits = 128;   // split-KV partial slots per (token, head)
 static constexpr int kSmallT = 8;        // token rows handled by the GEMV family
+static constexpr int kLmGemmMinRows = 4; // LM head rows from which the tensor-core GEMM runs
+static constexpr long long kLongDecodeKeys = 16384;  // tokens x keys from which decode attention splits evenly
+static constexpr int kShortCacheKeys = 4096;  // batched decode: longest cache served by the per-pair kernel
 
 static size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -197,6 +200,7 @@ struct qw_kv {
     f16* k;
     f16* v;
     long long layer_stride;
+    CUtensorMap tm_k, tm_v;  // K / V pools as [rows, 128] fp16 (box 64 x 16, 128-byte swizzle)
     std::vector<int> len;
     std::vector<std::vector<int>> pt;
     std::set<int> free_pages;
@@ -575,6 +579,14 @@ extern "C" qw_status qw_kv_alloc(qw_model* m, void* dev_pool, size_t pool_bytes,
     kv->layer_stride = (long long)n_pages * m->cfg.n_kv_heads * 16 * m->cfg.head_dim;
     kv->k = (f16*)(kv->pool + meta);
     kv->v = kv->k + (size_t)m->cfg.n_layers * kv->layer_stride;
+    {
+        const unsigned long long rows = (unsigned long long)m->cfg.n_layers * n_pages * m->cfg.n_kv_heads * 16;
+        if (rows >= (1ull << 31) || !gemm_tc_encode_map(&kv->tm_k, kv->k, rows, m->cfg.head_dim, 16) ||
+            !gemm_tc_encode_map(&kv->tm_v, kv->v, rows, m->cfg.head_dim, 16)) {
+            delete kv;
+            return fail(QW_ERR_INVALID_ARG, "KV pool too large for tensor-map row coordinates");
+        }
+    }
     kv->len.assign(max_seqs, 0);
     kv->pt.assign(max_seqs, std::vector<int>());
     for (int i = 0; i < kv->n_pages; ++i) kv->free_pages.insert(i);
@@ -716,6 +728,9 @@ static qw_status run_layers(qw_model* m, qw_kv* kv, const StepDesc& sd, bool pre
     const TokView tv = {m->tok_seq + t0, m->tok_pos + t0, m->last};
     const bool small = sd.T <= kSmallT;
     const SplitPlan sp = plan_splits(m, T, max_keys);
+    // small decode batches over long caches: separate QK-norm/RoPE/append, then the
+    // evenly split decode attention (short caches keep the fused per-pair kernel)
+    const bool long_decode = !prefill && small && (long long)T * max_keys >= kLongDecodeKeys;
     float* x = m->x + (size_t)t0 * D;
     f16* h = m->h + (size_t)t0 * D;
     f16* q = m->q + (size_t)t0 * QD;
@@ -767,6 +782,16 @@ static qw_status run_layers(qw_model* m, qw_kv* kv, const StepDesc& sd, bool pre
                 PROF(QW_PROF_ATTN);
                 LAUNCH(launch_attn_paged(lc, T, l, q, c.n_heads, c.n_kv_heads, tv, kvv, sp.chunk, sp.n_splits,
                                          part_o, part_ml, counters, attn, nullptr, nullptr));
+            } else if (long_decode) {
+                {
+                    PROF(QW_PROF_ROPE);
+                    LAUNCH(launch_qknorm_rope_append(lc, T, l, qkv, w_qn, w_kn, c.rms_eps, m->rcos, m->rsin,
+                                                     c.n_heads, c.n_kv_heads, tv, kvv, q, lpos, lslot, m->status));
+                }
+                PROF(QW_PROF_ATTN);
+                LAUNCH(launch_attn_decode(lc, T, l, q, c.n_heads, c.n_kv_heads, kvv, &kv->tm_k, &kv->tm_v, sd.seq + t0,
+                                          max_keys, kMaxSplits,
+                                          part_o, part_ml, counters, attn, m->status, m->num_sms));
             } else {
                 // decode: one new token per sequence; QK-norm, RoPE and the KV append run inside
                 AttnFuse fz = {qkv, w_qn, w_kn, c.rms_eps, m->rcos, m->rsin, lpos, lslot, m->status};
@@ -779,9 +804,13 @@ static qw_status run_layers(qw_model* m, qw_kv* kv, const StepDesc& sd, bool pre
             PROF(QW_PROF_ATTN);
             if (prefill)
                 LAUNCH(launch_attn_prefill(lc, sd, max_keys, l, q, kvv, c.n_heads, c.n_kv_heads, attn));
-            else
+            else if (max_keys <= kShortCacheKeys)  // light per-pair kernel: overlaps the other half's GEMMs
                 LAUNCH(launch_attn_paged(lc, T, l, q, c.n_heads, c.n_kv_heads, tv, kvv, sp.chunk, sp.n_splits,
                                          part_o, part_ml, counters, attn, nullptr, sd.seq + t0));
+            else
+                LAUNCH(launch_attn_decode(lc, T, l, q, c.n_heads, c.n_kv_heads, kvv, &kv->tm_k, &kv->tm_v, sd.seq + t0,
+                                          max_keys, kMaxSplits,
+                                          part_o, part_ml, counters, attn, m->status, m->num_sms));
         }
         if (small) {
             PROF(QW_PROF_OPROJ);
@@ -903,7 +932,9 @@ static qw_status run_step(qw_model* m, qw_kv* kv, const StepDesc& sd, bool prefi
     const bool pdl_on = m->pdl && m->prof_kind == QW_PROF_OFF;
 #define PROF(kind) ProfScope prof_scope_(m, kind, pc, st)
     // --- final norm + tied LM head + greedy argmax (Paso 8) ---
-    if (B <= kSmallT) {
+    // The GEMV reads the 311 MB head at full bandwidth for 1-3 rows; from 4 rows on its dot
+    // products cost more than the tensor-core GEMM, which streams the head once for any B.
+    if (B < kLmGemmMinRows) {
         PROF(QW_PROF_LMHEAD);
         CUDA_TRY(launch_gemv_lmhead(lc, B, m->x, m->last, m->fnorm, c.rms_eps, m->embed, c.vocab, D, logits,
                                     m->best));

@@ -224,16 +224,31 @@ def test_persistent_decode_matches_per_phase_launches(one_block):
 
 @pytest.fixture(scope="module")
 def one_block_long(qw):
-    eng = engine(qw, synth.ONE_BLOCK, max_tokens=64, max_batch=8, max_context=4096, kv_pages=600,
+    eng = engine(qw, synth.ONE_BLOCK, max_tokens=64, max_batch=8, max_context=8192, kv_pages=1300,
                  max_seqs=8)
     yield Run(qw, eng), oracle.Model(weights(synth.ONE_BLOCK))
     eng.close()
 
 
-@pytest.mark.parametrize("lens", [(2047, 3001), (1, 300, 4000)])
+@pytest.fixture(scope="module")
+def one_block_long_batch(qw):
+    eng = engine(qw, synth.ONE_BLOCK, max_tokens=64, max_batch=16, max_context=8192, kv_pages=3000,
+                 max_seqs=16)
+    yield Run(qw, eng), oracle.Model(weights(synth.ONE_BLOCK))
+    eng.close()
+
+
+def test_injected_long_cache_batched_decode(one_block_long_batch):
+    """More than 8 sequences (tensor-core projections) with caches longer than 4096 keys: the
+    evenly split decode attention behind the q|k|v epilogue."""
+    test_injected_long_cache_forced_decode(one_block_long_batch, (5000, 17, 4100, 300, 6001, 2, 4097, 900, 33, 5555))
+
+
+@pytest.mark.parametrize("lens", [(2047, 3001), (1, 300, 4000), (5000, 700, 6100)])
 def test_injected_long_cache_forced_decode(one_block_long, lens):
     """KV caches filled by the counter-based generator (bit-identical on both sides), then
-    forced decode steps; the oracle reads the same injected prefix."""
+    forced decode steps; the oracle reads the same injected prefix. The last case is long
+    enough (tokens x keys) for the evenly split decode attention."""
     run, om = one_block_long
     s = synth.ONE_BLOCK
     qw, eng = run.qw, run.eng
@@ -244,6 +259,7 @@ def test_injected_long_cache_forced_decode(one_block_long, lens):
         qw.qw_kv_reserve(eng.kv, sq, n + 3, eng.stream)
         qw.qw_kv_fill_synthetic(eng.kv, sq, n, seed, eng.stream)
     # the pool holds exactly the generator's values at the reserved slots
+    eng.stream.synchronize()  # the fills ran on the engine's stream
     kptr, vptr, n_pages = qw.qw_kv_pool_ptrs(eng.kv)
     import torch
     off = kptr - eng.pool.data_ptr()
