@@ -49,7 +49,8 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;  // 64 fp16 = 128 bytes = one swizzle row
-constexpr int GEMM_THREADS = 192;
+constexpr int GEMM_THREADS = 192;     // cluster kernel: 4 epilogue warps, producer, MMA
+constexpr int GEMM_TC_THREADS = 320;  // persistent kernel: 8 epilogue warps, producer, MMA
 constexpr unsigned long long kWaitNs = 2000000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -163,7 +164,12 @@ __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.
         : "memory")
 
 
-__device__ __forceinline__ void named_bar_epi() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Epilogue warpgroups: threads 0-127 (barrier 1) and, in the persistent kernel, 128-255
+// (barrier 2); helpers index threads within their warpgroup.
+__device__ __forceinline__ int epi_tid() { return threadIdx.x & 127; }
+__device__ __forceinline__ void named_bar_epi() {
+    asm volatile("bar.sync %0, 128;" ::"r"(1 + (threadIdx.x >> 7)) : "memory");
+}
 
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
@@ -192,17 +198,20 @@ constexpr int EP = 132;                   // pitch (floats) of the [token][128] 
 constexpr int E_BYTES = 32 * EP * 4;      // 32 tokens
 constexpr int SMEM_BUDGET = 227 * 1024;
 
-template <int BN, int EPI>
+template <int BN, int EPI, int NWG>  // NWG: epilogue warpgroups
 struct GemmCfg {
     static constexpr int A_BYTES = BM * BK * 2;  // 16 KB
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int NBUF = (2 * BN <= 512) ? 2 : 1;
     static constexpr int TMEM_COLS = NBUF * BN < 32 ? 32 : NBUF * BN;
-    static constexpr int SBEST_BYTES = (EPI == EPI_ARGMAX) ? 4 * BN * 8 : 0;
-    static constexpr int STAGE_E_BYTES = (EPI == EPI_QKV_HEADS || EPI == EPI_SILU_MUL) ? E_BYTES : 0;
+    static constexpr int SBEST_WG = (EPI == EPI_ARGMAX) ? 4 * BN * 8 : 0;
+    static constexpr int E_WG = (EPI == EPI_QKV_HEADS || EPI == EPI_SILU_MUL) ? E_BYTES : 0;
+    static constexpr int META_WG = (EPI == EPI_QKV_HEADS) ? 2 * BN * 4 + 512 : 0;  // tpos, tdst, ssx
+    static constexpr int SBEST_BYTES = NWG * SBEST_WG;
+    static constexpr int STAGE_E_BYTES = NWG * E_WG;
     static constexpr int NW_BYTES = (EPI == EPI_QKV_HEADS) ? 256 * 4 : 0;
-    static constexpr int META_BYTES = (EPI == EPI_QKV_HEADS) ? 2 * BN * 4 + 512 : 0;  // tpos, tdst, ssx
+    static constexpr int META_BYTES = NWG * META_WG;
     static constexpr int EXTRA = SBEST_BYTES + STAGE_E_BYTES + NW_BYTES + META_BYTES;
     static constexpr int BAR_BYTES = 256;
     static constexpr int STAGES_RAW = (SMEM_BUDGET - 1024 - BAR_BYTES - EXTRA) / STAGE_BYTES;
@@ -238,7 +247,7 @@ struct GemmKParams {
 // n0 + c, tdst[c] = its KV slot row page * 16 + pos % 16 (-1: no page; reported).
 template <int BN>
 __device__ void fill_tok_meta(const GemmKParams& p, int n0, int hd, int* tpos, int* tdst) {
-    for (int c = threadIdx.x; c < BN; c += 128) {
+    for (int c = epi_tid(); c < BN; c += 128) {
         const int tok = n0 + c;
         int pos = 0, dst = -1;
         if (tok < p.T) {
@@ -272,7 +281,7 @@ struct RopeRegs {
     float4 c[4], s[4];
 };
 __device__ __forceinline__ void load_rope(const GemmKParams& p, const int* tpos, int cbase, int ntok, RopeRegs& rr) {
-    const int lane = threadIdx.x & 31, q = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31, q = epi_tid() >> 5;
     const int pos = lane < ntok ? tpos[cbase + lane] : 0;
     const float4* cs = reinterpret_cast<const float4*>(p.rope_cos + (size_t)pos * 64 + 16 * q);
     const float4* sn = reinterpret_cast<const float4*>(p.rope_sin + (size_t)pos * 64 + 16 * q);
@@ -302,7 +311,7 @@ __device__ __forceinline__ void store16h(f16* dst, const float* v) {  // 16 valu
 // quarters meet in ssx), then the rotation by pos * theta^(-i/64); v heads: copied.
 __device__ void epi_heads(const GemmKParams& p, const float* E, const float* nws, const int* tdst, float* ssx,
                           const RopeRegs& rr, int tok0, int cbase, int ntok, int hd) {
-    const int t = threadIdx.x & 31, q = threadIdx.x >> 5;
+    const int t = threadIdx.x & 31, q = epi_tid() >> 5;
     const bool isq = hd < p.n_heads;
     const bool isv = hd >= p.n_heads + p.n_kv;
     const float* row = E + t * EP;
@@ -352,7 +361,7 @@ __device__ void epi_heads(const GemmKParams& p, const float* E, const float* nws
 // interleaved gate/up tile `tile` (gate rows 0..63, up rows 64..127 of output features
 // 64 tile .. 64 tile + 63): act = SiLU(gate) * up.
 __device__ void epi_silu(const GemmKParams& p, const float* E, int tok0, int ntok, int tile) {
-    const int t = threadIdx.x & 31, q = threadIdx.x >> 5;
+    const int t = threadIdx.x & 31, q = epi_tid() >> 5;
     if (t >= ntok) return;
     const float* row = E + t * EP;
     float v[16];
@@ -375,7 +384,7 @@ __device__ __forceinline__ void load_resid(const GemmKParams& p, int tok0, int f
 }
 
 __device__ __forceinline__ void load_norm_weights(const GemmKParams& p, float* nws) {
-    for (int i = threadIdx.x; i < 256; i += 128) nws[i] = __bfloat162float(i < 128 ? p.q_norm[i] : p.k_norm[i - 128]);
+    for (int i = epi_tid(); i < 256; i += 128) nws[i] = __bfloat162float(i < 128 ? p.q_norm[i] : p.k_norm[i - 128]);
 }
 
 }  // namespace
@@ -384,28 +393,30 @@ __device__ __forceinline__ void load_norm_weights(const GemmKParams& p, float* n
 // Persistent kernel: CTA b processes tiles u = b, b + gridDim.x, ...
 // =======================================================================================
 template <int BN, int EPI>
-__global__ void __launch_bounds__(GEMM_THREADS, 1)
+__global__ void __launch_bounds__(GEMM_TC_THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmKParams p) {
-    using C = GemmCfg<BN, EPI>;
+    using C = GemmCfg<BN, EPI, 2>;
+    static_assert(C::NBUF == 2, "one accumulator buffer per epilogue warpgroup");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t* extra = smem + C::STAGES * C::STAGE_BYTES;
-    unsigned long long* sbest = reinterpret_cast<unsigned long long*>(extra);
-    float* E = reinterpret_cast<float*>(extra + C::SBEST_BYTES);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int wg = (warp < 8) ? (warp >> 2) : 0;  // epilogue warpgroup of this thread
+    unsigned long long* sbest = reinterpret_cast<unsigned long long*>(extra + wg * C::SBEST_WG);
+    float* E = reinterpret_cast<float*>(extra + C::SBEST_BYTES + wg * C::E_WG);
     float* nws = reinterpret_cast<float*>(extra + C::SBEST_BYTES + C::STAGE_E_BYTES);
-    int* tpos = reinterpret_cast<int*>(extra + C::SBEST_BYTES + C::STAGE_E_BYTES + C::NW_BYTES);
+    int* tpos = reinterpret_cast<int*>(extra + C::SBEST_BYTES + C::STAGE_E_BYTES + C::NW_BYTES + wg * C::META_WG);
     int* tdst = tpos + BN;
     float* ssx = reinterpret_cast<float*>(tdst + BN);
     uint64_t* bars = reinterpret_cast<uint64_t*>(extra + C::EXTRA);
     uint64_t* full = bars;
     uint64_t* empty = bars + C::STAGES;
-    uint64_t* accf = bars + 2 * C::STAGES;      // [2] accumulator ready
+    uint64_t* accf = bars + 2 * C::STAGES;      // [2] accumulator ready (buffer b: warpgroup b)
     uint64_t* acce = bars + 2 * C::STAGES + 2;  // [2] accumulator free
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::STAGES + 4);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    volatile int* ep_fail = reinterpret_cast<volatile int*>(tmem_slot + 2);
+    volatile int* ep_fail = reinterpret_cast<volatile int*>(tmem_slot + 2) + wg;  // [2]
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nk = p.K / BK;
 
     if (threadIdx.x == 0) {
@@ -418,20 +429,22 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             mbar_init(smem_u32(acce + b), 4);  // one arrival per epilogue warp
         }
         *abort_flag = 0;
-        *ep_fail = 0;
+        ep_fail[0] = 0;
+        ep_fail[1] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
-    if (warp == 4 && lane == 0) {
+    if (warp == 8 && lane == 0) {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
     }
-    if (warp == 5) {
+    if (warp == 9) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                      "r"(C::TMEM_COLS)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
+    if (EPI == EPI_QKV_HEADS && threadIdx.x < 128) load_norm_weights(p, nws);  // weights: before the wait
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -443,7 +456,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
         tn = u / p.tiles_m;
     };
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
             // weight tiles of the first ring stages before the dependency wait
@@ -486,7 +499,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                 }
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // ---------------- MMA issuer ----------------
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_f16(BM, BN);
@@ -524,8 +537,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             }
         }
     } else {
-        // ---------------- epilogue warps 0-3: TMEM lanes 32w .. 32w+31 ----------------
-        if (EPI == EPI_QKV_HEADS) load_norm_weights(p, nws);  // weights: before the wait
+        // ---------------- epilogue warpgroups: warp w reads TMEM lanes 32 (w % 4) .. ----------
+        // warpgroup wg takes this CTA's tiles i = wg, wg + 2, ... in accumulator buffer wg
+        const int ew = warp & 3;  // warp within the warpgroup
         // hand buffer (i2 % NBUF) to the MMA warp for this CTA's i2-th tile
         auto prepare = [&](int i2) {
             const int u2 = blockIdx.x + i2 * gridDim.x;
@@ -534,18 +548,17 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             __syncwarp();
             if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(acce + (i2 % C::NBUF))) : "memory");
         };
-        for (int i2 = 0; i2 < C::NBUF; ++i2) prepare(i2);  // nothing to read: before the wait
+        prepare(wg);  // nothing to read: before the wait
         pdl_wait();
-        if (EPI == EPI_QKV_HEADS) named_bar_epi();  // norm weights visible
-        int i = 0;
-        for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++i) {
+        int i = wg;
+        for (int u = blockIdx.x + wg * gridDim.x; u < p.units; u += 2 * gridDim.x, i += 2) {
             int tm, tn;
             tile_of(u, tm, tn);
             const int buf = i % C::NBUF;
             const uint32_t use = (uint32_t)(i / C::NBUF);
             if (EPI == EPI_QKV_HEADS) fill_tok_meta<BN>(p, tn * BN, tm, tpos, tdst);  // overlaps the MMAs
             float xr[32];  // EPI_RESID_F32: residual rows of the current 32 tokens
-            if (EPI == EPI_RESID_F32) load_resid(p, tn * BN, tm * BM + warp * 32 + lane, xr);
+            if (EPI == EPI_RESID_F32) load_resid(p, tn * BN, tm * BM + ew * 32 + lane, xr);
             // all four epilogue warps take the same decision (they meet at named barriers)
             if (!mbar_wait(smem_u32(accf + buf), use & 1u, abort_flag)) *ep_fail = 1;
             named_bar_epi();
@@ -553,31 +566,28 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
             named_bar_epi();
             tc_fence_after();
             if (!ok) {
-                if (threadIdx.x == 0) atomicOr(p.status, QW_DEV_TIMEOUT);
+                if (epi_tid() == 0) atomicOr(p.status, QW_DEV_TIMEOUT);
                 break;
             }
             const int n0 = tn * BN;
             const int ncols = min(BN, ((p.T - n0) + 31) / 32 * 32);  // token columns holding data
-            const int fl = warp * 32 + lane;                           // tile row of this thread
-            const uint32_t trow = tmem + buf * BN + ((uint32_t)(warp * 32) << 16);
+            const int fl = ew * 32 + lane;                             // tile row of this thread
+            const uint32_t trow = tmem + buf * BN + ((uint32_t)(ew * 32) << 16);
             const bool rope = (EPI == EPI_QKV_HEADS) && tm < p.n_heads + p.n_kv;
-            RopeRegs rr_cur, rr_nxt;
-            if (rope) load_rope(p, tpos, 0, min(32, p.T - n0), rr_cur);
             for (int c0 = 0; c0 < ncols; c0 += 32) {
                 uint32_t r[32];
                 TMEM_LD32(trow + c0, r);
+                RopeRegs rr;  // this chunk's RoPE rows, in flight during the staging below
+                if (rope) load_rope(p, tpos, c0, min(32, p.T - (n0 + c0)), rr);
                 tmem_wait_ld();
-                if (c0 + 32 >= ncols) prepare(i + C::NBUF);  // this buffer's next tile
+                if (c0 + 32 >= ncols) prepare(i + 2);  // this buffer's next tile
                 if (EPI == EPI_QKV_HEADS || EPI == EPI_SILU_MUL) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) E[j * EP + fl] = __uint_as_float(r[j]);
                     named_bar_epi();
                     const int ntok = min(32, p.T - (n0 + c0));
                     if (EPI == EPI_QKV_HEADS) {
-                        // the next chunk's RoPE rows are in flight while this chunk is processed
-                        if (rope && c0 + 32 < ncols) load_rope(p, tpos, c0 + 32, min(32, p.T - (n0 + c0 + 32)), rr_nxt);
-                        epi_heads(p, E, nws, tdst, ssx, rr_cur, n0 + c0, c0, ntok, tm);
-                        rr_cur = rr_nxt;
+                        epi_heads(p, E, nws, tdst, ssx, rr, n0 + c0, c0, ntok, tm);
                     } else {
                         epi_silu(p, E, n0 + c0, ntok, tm);
                     }
@@ -601,13 +611,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                         const float v = __uint_as_float(r[j]);
                         if (p.logits && tok < p.T) p.logits[(size_t)tok * p.ld_out + f] = v;
                         const unsigned long long key = warp_max_u64(argmax_key(v, f));
-                        if (lane == 0) sbest[warp * BN + c0 + j] = key;
+                        if (lane == 0) sbest[ew * BN + c0 + j] = key;
                     }
                 }
             }
             if (EPI == EPI_ARGMAX) {
                 named_bar_epi();
-                for (int cc = threadIdx.x; cc < ncols; cc += 128) {
+                for (int cc = epi_tid(); cc < ncols; cc += 128) {
                     const int tok = n0 + cc;
                     if (tok < p.T) {
                         unsigned long long bb = sbest[cc];
@@ -623,7 +633,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     tc_fence_before();
     __syncthreads();
     if (*abort_flag && threadIdx.x == 0) atomicOr(p.status, QW_DEV_TIMEOUT);
-    if (warp == 5) {
+    if (warp == 9) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS)
                      : "memory");
@@ -636,7 +646,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
 template <int BN, int EPI>
 __global__ void __launch_bounds__(GEMM_THREADS, 1)
     k_gemm_cl(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmKParams p) {
-    using C = GemmCfg<BN, EPI>;
+    using C = GemmCfg<BN, EPI, 1>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
     uint8_t* extra = smem + C::STAGES * C::STAGE_BYTES;
@@ -910,16 +920,15 @@ int cluster_fit(int want, int clusters, int smem, cudaStream_t st) {
 
 template <int BN, int EPI>
 cudaError_t gemm_go(const LaunchCtx& c, const GemmArgs& a, int bn_idx) {
-    using C = GemmCfg<BN, EPI>;
-    static_assert(C::SMEM <= SMEM_BUDGET, "shared memory budget");
-    static_assert(C::STAGES >= 3, "pipeline depth");
+    using CC = GemmCfg<BN, EPI, 1>;  // cluster split-K kernel
+    using CT = GemmCfg<BN, EPI, 2>;  // persistent kernel
+    static_assert(CC::SMEM <= SMEM_BUDGET && CT::SMEM <= SMEM_BUDGET, "shared memory budget");
+    static_assert(CC::STAGES >= 3 && CT::STAGES >= 3, "pipeline depth");
     GemmKParams p;
     fill_params<BN, EPI>(p, a);
     const int tiles = p.tiles_m * p.tiles_n;
     const int sms = a.num_sms > 0 ? a.num_sms : 148;
     cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(GEMM_THREADS);
-    cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = c.stream;
     cudaLaunchAttribute attr[2];
     int na = 0;
@@ -934,14 +943,14 @@ cudaError_t gemm_go(const LaunchCtx& c, const GemmArgs& a, int bn_idx) {
         if (tiles * 2 <= sms) {
             splits = std::min(std::min(sms / tiles, 8), std::max((a.K / BK) / 4, 1));
             // the partials of all splits must fit in one CTA's stage ring
-            while (splits > 1 && splits * 128 * ((BN + splits - 1) / splits) * 4 > C::STAGES * C::STAGE_BYTES)
+            while (splits > 1 && splits * 128 * ((BN + splits - 1) / splits) * 4 > CC::STAGES * CC::STAGE_BYTES)
                 --splits;
         }
         if (splits > 1) {
             static bool done = false;
-            cudaError_t e = set_smem(k_gemm_cl<BN, EPI>, C::SMEM, done);
+            cudaError_t e = set_smem(k_gemm_cl<BN, EPI>, CC::SMEM, done);
             if (e != cudaSuccess) return e;
-            splits = cluster_fit<BN, EPI>(splits, tiles, C::SMEM, c.stream);
+            splits = cluster_fit<BN, EPI>(splits, tiles, CC::SMEM, c.stream);
         }
         if (splits > 1) {
             p.splits = splits;
@@ -952,17 +961,21 @@ cudaError_t gemm_go(const LaunchCtx& c, const GemmArgs& a, int bn_idx) {
             attr[na].val.clusterDim.z = 1;
             ++na;
             cfg.gridDim = dim3(tiles * splits);
+            cfg.blockDim = dim3(GEMM_THREADS);
+            cfg.dynamicSmemBytes = CC::SMEM;
             cfg.attrs = attr;
             cfg.numAttrs = na;
             return cudaLaunchKernelEx(&cfg, k_gemm_cl<BN, EPI>, *a.tmA, a.tmB[bn_idx], p);
         }
     }
     static bool done = false;
-    cudaError_t e = set_smem(k_gemm_tc<BN, EPI>, C::SMEM, done);
+    cudaError_t e = set_smem(k_gemm_tc<BN, EPI>, CT::SMEM, done);
     if (e != cudaSuccess) return e;
     p.splits = 1;
     p.units = tiles;
     cfg.gridDim = dim3(std::min(tiles, sms));
+    cfg.blockDim = dim3(GEMM_TC_THREADS);
+    cfg.dynamicSmemBytes = CT::SMEM;
     cfg.attrs = attr;
     cfg.numAttrs = na;
     return cudaLaunchKernelEx(&cfg, k_gemm_tc<BN, EPI>, *a.tmA, a.tmB[bn_idx], p);
