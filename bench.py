@@ -25,6 +25,7 @@ workload (the only other program this bench runs).
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -55,6 +56,32 @@ CONFIGS = {
                      "32 greedy decode steps",
             shape=synth.QWEN3_0_6B, B=8, prompt=None, n_decode=32, unit="tok/s", kind="decode_long"),
 }
+
+
+# DRAM bytes per launch of a kernel from one ncu capture (summaries under profiles/), reported
+# as roofline.traffic only while the kernel's source file is byte-identical to the capture's.
+NCU_TRAFFIC = {
+    (1, "gate_up+silu_mul(rmsnorm fused)"): (12606720, "decode_qwen3_decoder_gb300/csrc/k_small.cu",
+                                             "0eca842ea9e3d616dc7a649c7eefeedf777de9b09921357bd6f4f5fcf25f82c9"),
+    (1, "qkv_proj(rmsnorm fused)"): (8409856, "decode_qwen3_decoder_gb300/csrc/k_small.cu",
+                                     "0eca842ea9e3d616dc7a649c7eefeedf777de9b09921357bd6f4f5fcf25f82c9"),
+    (3, "gate_up+silu_mul"): (29390080 + 446976, "decode_qwen3_decoder_gb300/csrc/k_gemm.cu", "f566e7ddb93c954624b5befc4d82bd0bade5d8f7fc9471aab3688c52dbee812b"),
+    (3, "qkv_proj+qk_norm+rope+kv_append"): (25536256 + 9972736, "decode_qwen3_decoder_gb300/csrc/k_gemm.cu",
+                                             "f566e7ddb93c954624b5befc4d82bd0bade5d8f7fc9471aab3688c52dbee812b"),
+}
+
+
+def ncu_traffic(config: int, kernel: str):
+    ent = NCU_TRAFFIC.get((config, kernel))
+    if ent is None:
+        return None
+    nbytes, src, sha = ent
+    try:
+        with open(os.path.join(os.path.dirname(os.path.abspath(__file__)), src), "rb") as fh:
+            cur = hashlib.sha256(fh.read()).hexdigest()
+    except OSError:
+        return None
+    return nbytes if cur == sha else None
 
 
 def log(*a):
@@ -286,7 +313,7 @@ def run_ours(args, cfg, rank, world):
     achieved = dk["bytes"] / (dk["avg_us"] * 1e-6) / 1e9
     roofline = {"bound": "hbm", "kernel": dk["name"], "achieved": round(achieved, 1), "peak": hbm,
                 "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / hbm, 4),
-                "traffic": None, "algorithmic_bytes_per_launch": dk["bytes"],
+                "traffic": ncu_traffic(args.config, dk["name"]), "algorithmic_bytes_per_launch": dk["bytes"],
                 "avg_launch_us": round(dk["avg_us"], 3)}
     step_b = step_bytes(s, B, P + ND / 2)
     # ---- end to end through qw_generate with pinned host buffers ----
@@ -471,7 +498,8 @@ def run_other(args, cfg, rank, world):
         ach = flops[dom] / (kinds[dom]["avg_us"] * 1e-6) / 1e12
         roofline = {"bound": "tensor", "kernel": kinds[dom]["name"] + " (tcgen05 GEMM)", "achieved": round(ach, 1),
                     "peak": bf16_sust, "peak_source": peak_src + " bf16 sustained (fp16 operands run at the bf16 rate)",
-                    "unit": "TFLOP/s", "frac": round(ach / bf16_sust, 4), "traffic": None,
+                    "unit": "TFLOP/s", "frac": round(ach / bf16_sust, 4),
+                    "traffic": ncu_traffic(args.config, kinds[dom]["name"]),
                     "algorithmic_flops_per_launch": flops[dom], "avg_launch_us": round(kinds[dom]["avg_us"], 2)}
         attn_pairs = sum(int(l) * (int(l) + 1) // 2 for l in lens)
         total_flops = L * sum(flops[k] for k in gemm_kinds) + flops[7] + L * attn_pairs * 4 * s.head_dim * s.n_heads

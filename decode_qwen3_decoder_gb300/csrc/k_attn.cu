@@ -402,7 +402,8 @@ cudaError_t launch_attn_paged(const LaunchCtx& c, int T, int layer, const f16* q
 // k_attn_prefill: causal GQA attention of a prefill (sequences start empty, so position =
 // index in the prompt) on the tensor cores, flash style (Paso 5): for each tile of 64
 // queries of one sequence and one KV head, both query heads 2g and 2g+1 (128 rows, 8 warps
-// of 16 rows) stream the sequence's K/V tiles of 64 keys through shared memory once.
+// of 16 rows) stream the sequence's K/V tiles of 64 keys through shared memory once; each
+// tile is processed as two halves of 32 keys (fewer live registers, two CTAs per SM).
 // S = Q K^T and O += P V use mma.sync m16n8k16 (fp16 operands, fp32 accumulation); the
 // online softmax runs in fp32 in the exp2 domain; P goes from the S accumulators straight
 // into the A fragments of P V. K/V tiles (the new keys were just appended to the paged
@@ -459,7 +460,7 @@ struct PrefillP {
     float scale_log2;
 };
 
-__global__ void __launch_bounds__(PF_WARPS * 32) k_attn_prefill(const __grid_constant__ PrefillP p) {
+__global__ void __launch_bounds__(PF_WARPS * 32, 2) k_attn_prefill(const __grid_constant__ PrefillP p) {
     extern __shared__ __align__(128) uint8_t pf_smem[];
     const uint32_t sQ = (uint32_t)__cvta_generic_to_shared(pf_smem);  // [128 rows][256 B]
     const uint32_t sK = sQ + 128 * 256;                               // [2][64][256 B]
@@ -512,7 +513,6 @@ __global__ void __launch_bounds__(PF_WARPS * 32) k_attn_prefill(const __grid_con
     const int gq = lane >> 2, tq = lane & 3;
     const int qpos0 = q0 + (r0 & 63) + gq;      // positions of this thread's two rows
     const int qpos1 = qpos0 + 8;
-    uint32_t qa[8][4];
     float o[16][4];
 #pragma unroll
     for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
@@ -524,89 +524,92 @@ __global__ void __launch_bounds__(PF_WARPS * 32) k_attn_prefill(const __grid_con
         cp_commit();
         cp_wait<1>();
         __syncthreads();
-        if (kt == 0) {
+        const uint32_t kb = sK + buf * PF_KV * 256;
+        const uint32_t vb = sV + buf * PF_KV * 256;
+        const int k0 = kt * PF_KV;
+        // two halves of 32 keys, each with its own online-softmax update (fewer live
+        // registers: two CTAs fit on an SM); Q fragments are re-read from shared memory
+#pragma unroll
+        for (int hk = 0; hk < 2; ++hk) {
+            // ---- S = Q K^T (16 rows x 32 keys) -------------------------------------------
+            float s[4][4];
+#pragma unroll
+            for (int n = 0; n < 4; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks) {
-                const int row = r0 + (lane & 7) + ((lane >> 3) & 1) * 8;
-                const int ch = 2 * ks + (lane >> 4);
-                ldsm_x4(sQ + swz(row, ch), qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3]);
+                uint32_t qa[4];
+                {
+                    const int row = r0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+                    const int ch = 2 * ks + (lane >> 4);
+                    ldsm_x4(sQ + swz(row, ch), qa[0], qa[1], qa[2], qa[3]);
+                }
+#pragma unroll
+                for (int np = 0; np < 2; ++np) {  // pairs of 8-key n-tiles
+                    const int key = hk * 32 + np * 16 + (lane & 7) + ((lane >> 4) & 1) * 8;
+                    const int ch = 2 * ks + ((lane >> 3) & 1);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(kb + swz(key, ch), b0, b1, b2, b3);
+                    mma16816(s[2 * np], qa, b0, b1);
+                    mma16816(s[2 * np + 1], qa, b2, b3);
+                }
             }
-        }
-        // ---- S = Q K^T (16 rows x 64 keys) ---------------------------------------------
-        float s[8][4];
+            // ---- online softmax (exp2 domain), causal mask on the diagonal tile -----------
+            float tm0 = -INFINITY, tm1 = -INFINITY;
 #pragma unroll
-        for (int n = 0; n < 8; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
-        const uint32_t kb = sK + buf * PF_KV * 256;
+            for (int n = 0; n < 4; ++n) {
+                const int kp = k0 + hk * 32 + n * 8 + 2 * tq;
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-#pragma unroll
-            for (int np = 0; np < 4; ++np) {  // pairs of 8-key n-tiles
-                const int key = np * 16 + (lane & 7) + ((lane >> 4) & 1) * 8;
-                const int ch = 2 * ks + ((lane >> 3) & 1);
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4(kb + swz(key, ch), b0, b1, b2, b3);
-                mma16816(s[2 * np], qa[ks], b0, b1);
-                mma16816(s[2 * np + 1], qa[ks], b2, b3);
+                for (int e = 0; e < 2; ++e) {
+                    const bool in = (kp + e) < len;
+                    s[n][e] = (in && kp + e <= qpos0) ? s[n][e] * p.scale_log2 : -INFINITY;
+                    s[n][2 + e] = (in && kp + e <= qpos1) ? s[n][2 + e] * p.scale_log2 : -INFINITY;
+                    tm0 = fmaxf(tm0, s[n][e]);
+                    tm1 = fmaxf(tm1, s[n][2 + e]);
+                }
             }
-        }
-        // ---- online softmax (exp2 domain), causal mask on the diagonal tile ---------------
-        const int k0 = kt * PF_KV;
-        float tm0 = -INFINITY, tm1 = -INFINITY;
+            tm0 = fmaxf(tm0, __shfl_xor_sync(0xffffffffu, tm0, 1));
+            tm0 = fmaxf(tm0, __shfl_xor_sync(0xffffffffu, tm0, 2));
+            tm1 = fmaxf(tm1, __shfl_xor_sync(0xffffffffu, tm1, 1));
+            tm1 = fmaxf(tm1, __shfl_xor_sync(0xffffffffu, tm1, 2));
+            const float nm0 = fmaxf(m0, tm0), nm1 = fmaxf(m1, tm1);
+            // rows with no visible key yet keep m = -inf; guard the rescale against inf - inf
+            const float a0 = (nm0 == -INFINITY) ? 1.f : exp2f(m0 - nm0);
+            const float a1 = (nm1 == -INFINITY) ? 1.f : exp2f(m1 - nm1);
+            m0 = nm0;
+            m1 = nm1;
+            l0 *= a0;
+            l1 *= a1;
 #pragma unroll
-        for (int n = 0; n < 8; ++n) {
-            const int kp = k0 + n * 8 + 2 * tq;
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const bool in = (kp + e) < len;
-                s[n][e] = (in && kp + e <= qpos0) ? s[n][e] * p.scale_log2 : -INFINITY;
-                s[n][2 + e] = (in && kp + e <= qpos1) ? s[n][2 + e] * p.scale_log2 : -INFINITY;
-                tm0 = fmaxf(tm0, s[n][e]);
-                tm1 = fmaxf(tm1, s[n][2 + e]);
+            for (int n = 0; n < 16; ++n) {
+                o[n][0] *= a0;
+                o[n][1] *= a0;
+                o[n][2] *= a1;
+                o[n][3] *= a1;
             }
-        }
-        tm0 = fmaxf(tm0, __shfl_xor_sync(0xffffffffu, tm0, 1));
-        tm0 = fmaxf(tm0, __shfl_xor_sync(0xffffffffu, tm0, 2));
-        tm1 = fmaxf(tm1, __shfl_xor_sync(0xffffffffu, tm1, 1));
-        tm1 = fmaxf(tm1, __shfl_xor_sync(0xffffffffu, tm1, 2));
-        const float nm0 = fmaxf(m0, tm0), nm1 = fmaxf(m1, tm1);
-        // rows with no visible key yet keep m = -inf; guard the rescale against inf - inf
-        const float a0 = (nm0 == -INFINITY) ? 1.f : exp2f(m0 - nm0);
-        const float a1 = (nm1 == -INFINITY) ? 1.f : exp2f(m1 - nm1);
-        m0 = nm0;
-        m1 = nm1;
-        l0 *= a0;
-        l1 *= a1;
+            uint32_t pa[2][4];  // P as A fragments of P V, 2 k-steps of 16 keys
 #pragma unroll
-        for (int n = 0; n < 16; ++n) {
-            o[n][0] *= a0;
-            o[n][1] *= a0;
-            o[n][2] *= a1;
-            o[n][3] *= a1;
-        }
-        uint32_t pa[4][4];  // P as A fragments of P V, 4 k-steps of 16 keys
+            for (int n = 0; n < 4; ++n) {
+                const float e0 = (m0 == -INFINITY) ? 0.f : exp2f(s[n][0] - m0);
+                const float e1 = (m0 == -INFINITY) ? 0.f : exp2f(s[n][1] - m0);
+                const float e2 = (m1 == -INFINITY) ? 0.f : exp2f(s[n][2] - m1);
+                const float e3 = (m1 == -INFINITY) ? 0.f : exp2f(s[n][3] - m1);
+                l0 += e0 + e1;
+                l1 += e2 + e3;
+                pa[n >> 1][(n & 1) * 2 + 0] = pack_h2(e0, e1);
+                pa[n >> 1][(n & 1) * 2 + 1] = pack_h2(e2, e3);
+            }
+            // ---- O += P V ----------------------------------------------------------------
 #pragma unroll
-        for (int n = 0; n < 8; ++n) {
-            const float e0 = (m0 == -INFINITY) ? 0.f : exp2f(s[n][0] - m0);
-            const float e1 = (m0 == -INFINITY) ? 0.f : exp2f(s[n][1] - m0);
-            const float e2 = (m1 == -INFINITY) ? 0.f : exp2f(s[n][2] - m1);
-            const float e3 = (m1 == -INFINITY) ? 0.f : exp2f(s[n][3] - m1);
-            l0 += e0 + e1;
-            l1 += e2 + e3;
-            pa[n >> 1][(n & 1) * 2 + 0] = pack_h2(e0, e1);
-            pa[n >> 1][(n & 1) * 2 + 1] = pack_h2(e2, e3);
-        }
-        // ---- O += P V ------------------------------------------------------------------------
-        const uint32_t vb = sV + buf * PF_KV * 256;
+            for (int ks = 0; ks < 2; ++ks) {
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-#pragma unroll
-            for (int np = 0; np < 8; ++np) {  // pairs of 8-dim n-tiles
-                const int key = ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-                const int ch = 2 * np + (lane >> 4);
-                uint32_t b0, b1, b2, b3;
-                ldsm_x4_t(vb + swz(key, ch), b0, b1, b2, b3);
-                mma16816(o[2 * np], pa[ks], b0, b1);
-                mma16816(o[2 * np + 1], pa[ks], b2, b3);
+                for (int np = 0; np < 8; ++np) {  // pairs of 8-dim n-tiles
+                    const int key = hk * 32 + ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+                    const int ch = 2 * np + (lane >> 4);
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(vb + swz(key, ch), b0, b1, b2, b3);
+                    mma16816(o[2 * np], pa[ks], b0, b1);
+                    mma16816(o[2 * np + 1], pa[ks], b2, b3);
+                }
             }
         }
         __syncthreads();  // the buffer is refilled two iterations later
