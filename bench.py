@@ -84,6 +84,16 @@ def ncu_traffic(config: int, kernel: str):
     return nbytes if cur == sha else None
 
 
+def rank_token_seed(config: int, rank: int) -> int:
+    """Seed of the token ids of one replica: each rank decodes its own synthetic prompts."""
+    return 1000 + config + 17 * rank
+
+
+def whole_job_rate(units_per_rank_step: float, steps: int, world: int, ms_max: float) -> float:
+    """Units per second over all ranks: every rank processed the same work in at most ms_max."""
+    return units_per_rank_step * steps * world / (ms_max / 1e3)
+
+
 def log(*a):
     print(*a, file=sys.stderr, flush=True)
 
@@ -212,7 +222,7 @@ def run_ours(args, cfg, rank, world):
     if args.persistent:
         qw.qw_set_option(eng.model, qw.QW_OPT_PERSISTENT_DECODE, 1)
     seqs = list(range(B))
-    prompt = synth.make_tokens(s.vocab, B * P, 1000 + args.config + 17 * rank)
+    prompt = synth.make_tokens(s.vocab, B * P, rank_token_seed(args.config, rank))
     d_prompt = torch.tensor(prompt, dtype=torch.int32, device="cuda")
     d_cur = torch.zeros(B, dtype=torch.int32, device="cuda")
     d_out = torch.zeros((ND + 1, B), dtype=torch.int32, device="cuda")
@@ -260,7 +270,7 @@ def run_ours(args, cfg, rank, world):
     ms_max = reduce_max(ms, world)
     gpu_launches = launches[0]
     tokens_per_step = B * (ND + 1)
-    value = tokens_per_step * args.steps * world / (ms_max / 1e3)
+    value = whole_job_rate(tokens_per_step, args.steps, world, ms_max)
     status = qw.qw_sync_status(eng.model, st)
     if status != 0:
         raise RuntimeError(f"device status {status} in the timed region: {qw.qw_last_error()}")
@@ -389,7 +399,7 @@ def run_other(args, cfg, rank, world):
     del w
     st = eng.stream
     seqs = list(range(B))
-    rng_seed = 1000 + args.config + 17 * rank
+    rng_seed = rank_token_seed(args.config, rank)
     d_cur = torch.zeros(B, dtype=torch.int32, device="cuda")
     hbm, bf16_burst, bf16_sust, peak_src = peaks()
 
@@ -457,7 +467,7 @@ def run_other(args, cfg, rank, world):
         torch.cuda.synchronize()
     barrier(world)
     ms_max = reduce_max(e0.elapsed_time(e1), world)
-    value = units_per_step * args.steps * world / (ms_max / 1e3)
+    value = whole_job_rate(units_per_step, args.steps, world, ms_max)
     if qw.qw_sync_status(eng.model, st) != 0:
         raise RuntimeError(f"device status in the timed region: {qw.qw_last_error()}")
 
