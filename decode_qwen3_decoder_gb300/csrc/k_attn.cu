@@ -448,6 +448,14 @@ __device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b
 
 }  // namespace
 
+// 2^x with the hardware approximation (PTX ex2.approx.ftz; 2^-inf = +0), for the softmax
+// weights of the prefill attention
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 struct PrefillP {
     StepDesc sd;
     const f16* q;       // [T][n_heads][128]
@@ -553,18 +561,31 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 2) k_attn_prefill(const __grid_
                     mma16816(s[2 * np + 1], qa, b2, b3);
                 }
             }
-            // ---- online softmax (exp2 domain), causal mask on the diagonal tile -----------
+            // ---- online softmax (exp2 domain), causal mask on the diagonal / tail keys -----
             float tm0 = -INFINITY, tm1 = -INFINITY;
+            const int kh0 = k0 + hk * 32;  // first key of this half
+            if (kh0 + 31 <= q0 && kh0 + 32 <= len) {  // every key visible to every row
 #pragma unroll
-            for (int n = 0; n < 4; ++n) {
-                const int kp = k0 + hk * 32 + n * 8 + 2 * tq;
+                for (int n = 0; n < 4; ++n)
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const bool in = (kp + e) < len;
-                    s[n][e] = (in && kp + e <= qpos0) ? s[n][e] * p.scale_log2 : -INFINITY;
-                    s[n][2 + e] = (in && kp + e <= qpos1) ? s[n][2 + e] * p.scale_log2 : -INFINITY;
-                    tm0 = fmaxf(tm0, s[n][e]);
-                    tm1 = fmaxf(tm1, s[n][2 + e]);
+                    for (int e = 0; e < 2; ++e) {
+                        s[n][e] *= p.scale_log2;
+                        s[n][2 + e] *= p.scale_log2;
+                        tm0 = fmaxf(tm0, s[n][e]);
+                        tm1 = fmaxf(tm1, s[n][2 + e]);
+                    }
+            } else {
+#pragma unroll
+                for (int n = 0; n < 4; ++n) {
+                    const int kp = kh0 + n * 8 + 2 * tq;
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const bool in = (kp + e) < len;
+                        s[n][e] = (in && kp + e <= qpos0) ? s[n][e] * p.scale_log2 : -INFINITY;
+                        s[n][2 + e] = (in && kp + e <= qpos1) ? s[n][2 + e] * p.scale_log2 : -INFINITY;
+                        tm0 = fmaxf(tm0, s[n][e]);
+                        tm1 = fmaxf(tm1, s[n][2 + e]);
+                    }
                 }
             }
             tm0 = fmaxf(tm0, __shfl_xor_sync(0xffffffffu, tm0, 1));
@@ -573,8 +594,8 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 2) k_attn_prefill(const __grid_
             tm1 = fmaxf(tm1, __shfl_xor_sync(0xffffffffu, tm1, 2));
             const float nm0 = fmaxf(m0, tm0), nm1 = fmaxf(m1, tm1);
             // rows with no visible key yet keep m = -inf; guard the rescale against inf - inf
-            const float a0 = (nm0 == -INFINITY) ? 1.f : exp2f(m0 - nm0);
-            const float a1 = (nm1 == -INFINITY) ? 1.f : exp2f(m1 - nm1);
+            const float a0 = (nm0 == -INFINITY) ? 1.f : ex2_approx(m0 - nm0);
+            const float a1 = (nm1 == -INFINITY) ? 1.f : ex2_approx(m1 - nm1);
             m0 = nm0;
             m1 = nm1;
             l0 *= a0;
@@ -587,12 +608,15 @@ __global__ void __launch_bounds__(PF_WARPS * 32, 2) k_attn_prefill(const __grid_
                 o[n][3] *= a1;
             }
             uint32_t pa[2][4];  // P as A fragments of P V, 2 k-steps of 16 keys
+            // a row with no visible key yet has m = -inf: use 0 as its reference (all its
+            // scores are -inf, so every weight is 2^-inf = 0)
+            const float r0 = (m0 == -INFINITY) ? 0.f : m0, r1 = (m1 == -INFINITY) ? 0.f : m1;
 #pragma unroll
             for (int n = 0; n < 4; ++n) {
-                const float e0 = (m0 == -INFINITY) ? 0.f : exp2f(s[n][0] - m0);
-                const float e1 = (m0 == -INFINITY) ? 0.f : exp2f(s[n][1] - m0);
-                const float e2 = (m1 == -INFINITY) ? 0.f : exp2f(s[n][2] - m1);
-                const float e3 = (m1 == -INFINITY) ? 0.f : exp2f(s[n][3] - m1);
+                const float e0 = ex2_approx(s[n][0] - r0);
+                const float e1 = ex2_approx(s[n][1] - r0);
+                const float e2 = ex2_approx(s[n][2] - r1);
+                const float e3 = ex2_approx(s[n][3] - r1);
                 l0 += e0 + e1;
                 l1 += e2 + e3;
                 pa[n >> 1][(n & 1) * 2 + 0] = pack_h2(e0, e1);

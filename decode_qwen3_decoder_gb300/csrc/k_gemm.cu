@@ -12,7 +12,7 @@
 //
 // Epilogues:
 //   EPI_QKV_HEADS  one 128-row tile of the q|k|v projection is exactly one head: the tile
-//                  is staged through shared memory as [token][128] and each token's head
+//                  is staged through shared memory as fp16 [token][128] and each token's head
 //                  gets the per-head RMSNorm and the rotate-half RoPE (q and k heads, Pasos 4
 //                  and 5), then q is stored as fp16 [T][n_heads][128] and k / v are appended
 //                  (fp16) at the token's page slot of the KV cache.
@@ -196,6 +196,8 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
 
 constexpr int EP = 132;                   // pitch (floats) of the [token][128] staging tile
 constexpr int E_BYTES = 32 * EP * 4;      // 32 tokens
+constexpr int EPH = 136;                  // pitch (halves) of the fp16 staging tile (q|k|v heads)
+constexpr int EH_BYTES = 32 * EPH * 2;
 constexpr int SMEM_BUDGET = 227 * 1024;
 
 template <int BN, int EPI, int NWG>  // NWG: epilogue warpgroups
@@ -206,7 +208,7 @@ struct GemmCfg {
     static constexpr int NBUF = (2 * BN <= 512) ? 2 : 1;
     static constexpr int TMEM_COLS = NBUF * BN < 32 ? 32 : NBUF * BN;
     static constexpr int SBEST_WG = (EPI == EPI_ARGMAX) ? 4 * BN * 8 : 0;
-    static constexpr int E_WG = (EPI == EPI_QKV_HEADS || EPI == EPI_SILU_MUL) ? E_BYTES : 0;
+    static constexpr int E_WG = (EPI == EPI_QKV_HEADS) ? EH_BYTES : (EPI == EPI_SILU_MUL) ? E_BYTES : 0;
     static constexpr int META_WG = (EPI == EPI_QKV_HEADS) ? 2 * BN * 4 + 512 : 0;  // tpos, tdst, ssx
     static constexpr int SBEST_BYTES = NWG * SBEST_WG;
     static constexpr int STAGE_E_BYTES = NWG * E_WG;
@@ -309,19 +311,25 @@ __device__ __forceinline__ void store16h(f16* dst, const float* v) {  // 16 valu
 // q|k|v head tile `hd`, tokens tok0 .. tok0 + ntok - 1 (tile columns cbase ..). q and k
 // heads: RMSNorm over the head's 128 dims with the shared weight (partial sums of the four
 // quarters meet in ssx), then the rotation by pos * theta^(-i/64); v heads: copied.
-__device__ void epi_heads(const GemmKParams& p, const float* E, const float* nws, const int* tdst, float* ssx,
+__device__ void epi_heads(const GemmKParams& p, const f16* EH, const float* nws, const int* tdst, float* ssx,
                           const RopeRegs& rr, int tok0, int cbase, int ntok, int hd) {
     const int t = threadIdx.x & 31, q = epi_tid() >> 5;
     const bool isq = hd < p.n_heads;
     const bool isv = hd >= p.n_heads + p.n_kv;
-    const float* row = E + t * EP;
+    const f16* row = EH + t * EPH;  // the tile staged as fp16 [token][EPH]
     float a[16], b[16];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const float4 va = *reinterpret_cast<const float4*>(row + 16 * q + 4 * k);
-        const float4 vb = *reinterpret_cast<const float4*>(row + 64 + 16 * q + 4 * k);
-        a[4 * k] = va.x; a[4 * k + 1] = va.y; a[4 * k + 2] = va.z; a[4 * k + 3] = va.w;
-        b[4 * k] = vb.x; b[4 * k + 1] = vb.y; b[4 * k + 2] = vb.z; b[4 * k + 3] = vb.w;
+    for (int k = 0; k < 2; ++k) {
+        const uint4 va = *reinterpret_cast<const uint4*>(row + 16 * q + 8 * k);
+        const uint4 vb = *reinterpret_cast<const uint4*>(row + 64 + 16 * q + 8 * k);
+        const uint32_t wa[4] = {va.x, va.y, va.z, va.w}, wb[4] = {vb.x, vb.y, vb.z, vb.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            a[8 * k + 2 * i] = h_lo(wa[i]);
+            a[8 * k + 2 * i + 1] = h_hi(wa[i]);
+            b[8 * k + 2 * i] = h_lo(wb[i]);
+            b[8 * k + 2 * i + 1] = h_hi(wb[i]);
+        }
     }
     if (!isv) {
         float ss = 0.f;
@@ -582,12 +590,18 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1)
                 tmem_wait_ld();
                 if (c0 + 32 >= ncols) prepare(i + 2);  // this buffer's next tile
                 if (EPI == EPI_QKV_HEADS || EPI == EPI_SILU_MUL) {
+                    if (EPI == EPI_QKV_HEADS) {
+                        f16* EH = reinterpret_cast<f16*>(E);
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) E[j * EP + fl] = __uint_as_float(r[j]);
+                        for (int j = 0; j < 32; ++j) EH[j * EPH + fl] = __float2half_rn(__uint_as_float(r[j]));
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) E[j * EP + fl] = __uint_as_float(r[j]);
+                    }
                     named_bar_epi();
                     const int ntok = min(32, p.T - (n0 + c0));
                     if (EPI == EPI_QKV_HEADS) {
-                        epi_heads(p, E, nws, tdst, ssx, rr, n0 + c0, c0, ntok, tm);
+                        epi_heads(p, reinterpret_cast<const f16*>(E), nws, tdst, ssx, rr, n0 + c0, c0, ntok, tm);
                     } else {
                         epi_silu(p, E, n0 + c0, ntok, tm);
                     }
@@ -821,11 +835,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     for (int j = 0; j < w; ++j) {
                         float v = 0.f;
                         for (int s = 0; s < S; ++s) v += red[(s * WMAX + (cc - lo) + j) * 128 + fl];
-                        E[j * EP + fl] = v;
+                        if (EPI == EPI_QKV_HEADS)
+                            reinterpret_cast<f16*>(E)[j * EPH + fl] = __float2half_rn(v);
+                        else
+                            E[j * EP + fl] = v;
                     }
                     named_bar_epi();
                     if (EPI == EPI_QKV_HEADS)
-                        epi_heads(p, E, nws, tdst, ssx, rr, tok0, cc, ntok, tm);
+                        epi_heads(p, reinterpret_cast<const f16*>(E), nws, tdst, ssx, rr, tok0, cc, ntok, tm);
                     else
                         epi_silu(p, E, tok0, ntok, tm);
                     named_bar_epi();
