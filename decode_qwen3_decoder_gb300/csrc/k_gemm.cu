@@ -209,7 +209,7 @@ struct GemmCfg {
     static constexpr int TMEM_COLS = NBUF * BN < 32 ? 32 : NBUF * BN;
     static constexpr int SBEST_WG = (EPI == EPI_ARGMAX) ? 4 * BN * 8 : 0;
     static constexpr int E_WG = (EPI == EPI_QKV_HEADS) ? EH_BYTES : (EPI == EPI_SILU_MUL) ? E_BYTES : 0;
-    static constexpr int META_WG = (EPI == EPI_QKV_HEADS) ? 2 * BN * 4 + 512 : 0;  // tpos, tdst, ssx
+    static constexpr int META_WG = (EPI == EPI_QKV_HEADS) ? 2 * BN * 4 : 0;  // tpos, tdst
     static constexpr int SBEST_BYTES = NWG * SBEST_WG;
     static constexpr int STAGE_E_BYTES = NWG * E_WG;
     static constexpr int NW_BYTES = (EPI == EPI_QKV_HEADS) ? 256 * 4 : 0;
@@ -272,19 +272,22 @@ __device__ void fill_tok_meta(const GemmKParams& p, int n0, int hd, int* tpos, i
     }
 }
 
-// Epilogue thread layout over a staged chunk of 32 tokens: lane = token t of the chunk,
-// warp q = the dims [16q, 16q + 16) of the head and their rotate-half partners 64 + 16q ..
-// (for SwiGLU: gate features [16q, 16q + 16) and the matching up rows). Shared-memory rows
-// have a pitch of 132 floats, so the 16-byte reads of 8 consecutive lanes hit distinct banks;
-// every store is a whole 32-byte sector.
+// Head-epilogue thread layout over a staged chunk of 32 tokens: warp w of the warpgroup takes
+// tokens 8w .. 8w + 7; lane l holds token t = 8w + l / 4 and quarter q = l % 4, i.e. the dims
+// [16q, 16q + 16) of the head and their rotate-half partners 64 + 16q .. (the four quarters of
+// a token are adjacent lanes, so the head's sum of squares needs two shuffles). The fp16
+// staging rows have a pitch of 136 halves, so the 16-byte reads of 8 consecutive lanes hit
+// distinct banks; every store is a whole 32-byte sector.
+__device__ __forceinline__ int head_tok() { return ((epi_tid() >> 5) << 3) + ((threadIdx.x & 31) >> 2); }
+__device__ __forceinline__ int head_qtr() { return threadIdx.x & 3; }
 
-// RoPE cos/sin of this thread's 16 dims for its token (tpos[cbase + lane]).
+// RoPE cos/sin of this thread's 16 dims for its token (tpos[cbase + t]).
 struct RopeRegs {
     float4 c[4], s[4];
 };
 __device__ __forceinline__ void load_rope(const GemmKParams& p, const int* tpos, int cbase, int ntok, RopeRegs& rr) {
-    const int lane = threadIdx.x & 31, q = epi_tid() >> 5;
-    const int pos = lane < ntok ? tpos[cbase + lane] : 0;
+    const int t = head_tok(), q = head_qtr();
+    const int pos = t < ntok ? tpos[cbase + t] : 0;
     const float4* cs = reinterpret_cast<const float4*>(p.rope_cos + (size_t)pos * 64 + 16 * q);
     const float4* sn = reinterpret_cast<const float4*>(p.rope_sin + (size_t)pos * 64 + 16 * q);
 #pragma unroll
@@ -309,11 +312,11 @@ __device__ __forceinline__ void store16h(f16* dst, const float* v) {  // 16 valu
 }
 
 // q|k|v head tile `hd`, tokens tok0 .. tok0 + ntok - 1 (tile columns cbase ..). q and k
-// heads: RMSNorm over the head's 128 dims with the shared weight (partial sums of the four
-// quarters meet in ssx), then the rotation by pos * theta^(-i/64); v heads: copied.
-__device__ void epi_heads(const GemmKParams& p, const f16* EH, const float* nws, const int* tdst, float* ssx,
+// heads: RMSNorm over the head's 128 dims with the shared weight, then the rotation by
+// pos * theta^(-i/64); v heads: copied.
+__device__ void epi_heads(const GemmKParams& p, const f16* EH, const float* nws, const int* tdst,
                           const RopeRegs& rr, int tok0, int cbase, int ntok, int hd) {
-    const int t = threadIdx.x & 31, q = epi_tid() >> 5;
+    const int t = head_tok(), q = head_qtr();
     const bool isq = hd < p.n_heads;
     const bool isv = hd >= p.n_heads + p.n_kv;
     const f16* row = EH + t * EPH;  // the tile staged as fp16 [token][EPH]
@@ -335,18 +338,24 @@ __device__ void epi_heads(const GemmKParams& p, const f16* EH, const float* nws,
         float ss = 0.f;
 #pragma unroll
         for (int k = 0; k < 16; ++k) ss = fmaf(a[k], a[k], fmaf(b[k], b[k], ss));
-        ssx[q * 32 + t] = ss;
-        named_bar_epi();
-        ss = ssx[t] + ssx[32 + t] + ssx[64 + t] + ssx[96 + t];
+        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+        ss += __shfl_xor_sync(0xffffffffu, ss, 2);
         const float r = rsqrtf(ss * (1.0f / 128.0f) + p.eps);
-        const float* w = nws + (isq ? 0 : 128) + 16 * q;
+        const float4* w4 = reinterpret_cast<const float4*>(nws + (isq ? 0 : 128) + 16 * q);
+        float wa[16], wb[16];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float4 x = w4[k], y = w4[16 + k];  // dims 16q + 4k .. and 64 + 16q + 4k ..
+            wa[4 * k] = x.x; wa[4 * k + 1] = x.y; wa[4 * k + 2] = x.z; wa[4 * k + 3] = x.w;
+            wb[4 * k] = y.x; wb[4 * k + 1] = y.y; wb[4 * k + 2] = y.z; wb[4 * k + 3] = y.w;
+        }
         const float c[16] = {rr.c[0].x, rr.c[0].y, rr.c[0].z, rr.c[0].w, rr.c[1].x, rr.c[1].y, rr.c[1].z, rr.c[1].w,
                              rr.c[2].x, rr.c[2].y, rr.c[2].z, rr.c[2].w, rr.c[3].x, rr.c[3].y, rr.c[3].z, rr.c[3].w};
         const float sn[16] = {rr.s[0].x, rr.s[0].y, rr.s[0].z, rr.s[0].w, rr.s[1].x, rr.s[1].y, rr.s[1].z, rr.s[1].w,
                               rr.s[2].x, rr.s[2].y, rr.s[2].z, rr.s[2].w, rr.s[3].x, rr.s[3].y, rr.s[3].z, rr.s[3].w};
 #pragma unroll
         for (int k = 0; k < 16; ++k) {
-            const float ya = a[k] * r * w[k], yb = b[k] * r * w[64 + k];
+            const float ya = a[k] * r * wa[k], yb = b[k] * r * wb[k];
             a[k] = ya * c[k] - yb * sn[k];
             b[k] = yb * c[k] + ya * sn[k];
         }
@@ -366,6 +375,8 @@ __device__ void epi_heads(const GemmKParams& p, const f16* EH, const float* nws,
     store16h(dst + 64 + 16 * q, b);
 }
 
+// SwiGLU thread layout: lane = token t of the chunk, warp q of the warpgroup = gate features
+// [16q, 16q + 16) and the matching up rows.
 // interleaved gate/up tile `tile` (gate rows 0..63, up rows 64..127 of output features
 // 64 tile .. 64 tile + 63): act = SiLU(gate) * up.
 __device__ void epi_silu(const GemmKParams& p, const float* E, int tok0, int ntok, int tile) {
@@ -415,7 +426,6 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1)
     float* nws = reinterpret_cast<float*>(extra + C::SBEST_BYTES + C::STAGE_E_BYTES);
     int* tpos = reinterpret_cast<int*>(extra + C::SBEST_BYTES + C::STAGE_E_BYTES + C::NW_BYTES + wg * C::META_WG);
     int* tdst = tpos + BN;
-    float* ssx = reinterpret_cast<float*>(tdst + BN);
     uint64_t* bars = reinterpret_cast<uint64_t*>(extra + C::EXTRA);
     uint64_t* full = bars;
     uint64_t* empty = bars + C::STAGES;
@@ -601,7 +611,7 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1)
                     named_bar_epi();
                     const int ntok = min(32, p.T - (n0 + c0));
                     if (EPI == EPI_QKV_HEADS) {
-                        epi_heads(p, reinterpret_cast<const f16*>(E), nws, tdst, ssx, rr, n0 + c0, c0, ntok, tm);
+                        epi_heads(p, reinterpret_cast<const f16*>(E), nws, tdst, rr, n0 + c0, c0, ntok, tm);
                     } else {
                         epi_silu(p, E, n0 + c0, ntok, tm);
                     }
@@ -668,7 +678,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     float* nws = reinterpret_cast<float*>(extra + C::SBEST_BYTES + C::STAGE_E_BYTES);
     int* tpos = reinterpret_cast<int*>(extra + C::SBEST_BYTES + C::STAGE_E_BYTES + C::NW_BYTES);
     int* tdst = tpos + BN;
-    float* ssx = reinterpret_cast<float*>(tdst + BN);
     uint64_t* bars = reinterpret_cast<uint64_t*>(extra + C::EXTRA);
     uint64_t* full = bars;
     uint64_t* empty = bars + C::STAGES;
@@ -842,7 +851,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
                     }
                     named_bar_epi();
                     if (EPI == EPI_QKV_HEADS)
-                        epi_heads(p, reinterpret_cast<const f16*>(E), nws, tdst, ssx, rr, tok0, cc, ntok, tm);
+                        epi_heads(p, reinterpret_cast<const f16*>(E), nws, tdst, rr, tok0, cc, ntok, tm);
                     else
                         epi_silu(p, E, tok0, ntok, tm);
                     named_bar_epi();
