@@ -19,6 +19,7 @@
 #include <utility>
 
 #include "qw_internal.h"
+#include "tc_sm103.cuh"
 
 namespace {
 
@@ -1143,4 +1144,363 @@ cudaError_t launch_attn_decode(const LaunchCtx& c, int T, int layer, const f16* 
     int G = (int)std::min<long long>(2LL * num_sms, std::max(items, 1LL));
     G = std::min(G, (max_slots - 2) * n_kv);
     return launch_k(c, k_attn_decode, dim3(G), dim3(AD_THREADS), (size_t)smem, p);
+}
+
+// =======================================================================================
+// k_attn_prefill_tc: causal GQA attention of a prefill on tcgen05 (Paso 5). A CTA takes 64
+// queries of one sequence for both query heads 2g, 2g+1 of KV head g: the 128 rows of the MMA
+// (rows 0-63 head 2g, 64-127 head 2g+1), so every K/V tile read from the cache serves both
+// heads. Per tile of 64 keys, read from the sequence's cache pages with TMA (128-byte swizzle):
+//   S = Q K^T     -> TMEM, two buffers, so the next tile's S overlaps this tile's softmax;
+//   softmax       -> four warps, thread = row = TMEM lane, running max and sum in fp32 in the
+//                    exp2 domain; P (fp16) goes back into the first half of its S buffer;
+//   O += P V      -> A = P from TMEM, B = V as loaded ([key][dim], MN-major), O in TMEM.
+// A row's running max moves only when a tile's max exceeds it by more than 2^8 (then O and
+// the sum are rescaled), so most tiles skip the rescale and P stays <= 256; the final
+// normalisation by the sum is exact either way. One thread issues the MMAs, one streams K/V;
+// 96 KB of shared memory and 256 TMEM columns let two CTAs share an SM; every wait is bounded.
+// =======================================================================================
+namespace {
+
+constexpr int FA_BQ = 64;               // queries per head (128 MMA rows for the head pair)
+constexpr int FA_BK = 64;               // keys per tile
+constexpr int FA_THREADS = 192;         // warps 0-3 softmax/output, 4 producer, 5 MMA
+constexpr int FA_QSUB = 128 * 128;      // Q: [128 rows][64 dims] swizzled subtile (16 KB)
+constexpr int FA_KSUB = FA_BK * 128;    // K, V: [64 keys][64 dims] swizzled subtile (8 KB)
+constexpr int FA_KV = 2 * FA_KSUB;      // one K or V tile, all 128 dims
+constexpr int FA_OFF_K = 2 * FA_QSUB;   // [2] stages
+constexpr int FA_OFF_V = FA_OFF_K + 2 * FA_KV;
+constexpr int FA_OFF_BAR = FA_OFF_V + 2 * FA_KV;
+constexpr int FA_SMEM = 1024 + FA_OFF_BAR + 128;
+constexpr int FA_TMEM_COLS = 256;       // S[0] 0-63, S[1] 64-127, O 128-255
+constexpr int FA_O = 128;
+constexpr float FA_RESCALE_LOG2 = 8.f;  // the running max moves only past 2^8
+
+__device__ __forceinline__ void fa_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+}  // namespace
+
+struct PrefillTcP {
+    CUtensorMap tmK;  // K pool as [n_layers * n_pages * n_kv * 16, 128] fp16
+    CUtensorMap tmV;
+    StepDesc sd;
+    const f16* q;     // [T][n_heads][128]
+    f16* out;         // [T][n_heads][128]
+    const int* page_table;
+    int max_pages_per_seq, n_pages, layer, n_heads, n_kv;
+    int* status;
+    float scale_log2;
+};
+
+__global__ void __launch_bounds__(FA_THREADS, 2) k_attn_prefill_tc(const __grid_constant__ PrefillTcP p) {
+    extern __shared__ uint8_t fa_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(fa_raw) + 1023) & ~(uintptr_t)1023);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + FA_OFF_BAR);
+    uint64_t* k_full = bars;        // [2] K of a stage landed
+    uint64_t* v_full = bars + 2;    // [2] V of a stage landed
+    uint64_t* kv_empty = bars + 4;  // [2] the stage's S and P V MMAs finished
+    uint64_t* s_full = bars + 6;    // [2] S buffer written
+    uint64_t* p_full = bars + 8;    // [2] P written into the S buffer, O rescaled
+    uint64_t* pv_done = bars + 10;  // O += P V finished
+    uint64_t* q_ready = bars + 11;
+    uint64_t* mma_fin = bars + 12;  // every MMA of the CTA finished (before TMEM is freed)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int b = blockIdx.z, g = blockIdx.y;
+    const int len = p.sd.start[b + 1] - p.sd.start[b];
+    const int q0 = ((int)gridDim.x - 1 - (int)blockIdx.x) * FA_BQ;  // heavy (late) query tiles first
+    pdl_launch();
+    if (q0 >= len) return;  // uniform over the CTA
+    const int base = p.sd.start[b];
+    // causal: keys < min(len, q0 + 64); only the last tile holds keys after some query
+    const int n_kt = (min(len, q0 + FA_BQ) + FA_BK - 1) / FA_BK;
+    auto wait = [&](uint64_t* bar, int parity) { return mbar_wait(smem_u32(bar), (uint32_t)parity & 1u, abort_flag); };
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(smem_u32(k_full + i), 1);
+            mbar_init(smem_u32(v_full + i), 1);
+            mbar_init(smem_u32(kv_empty + i), 1);
+            mbar_init(smem_u32(s_full + i), 1);
+            mbar_init(smem_u32(p_full + i), 4);
+        }
+        mbar_init(smem_u32(pv_done), 1);
+        mbar_init(smem_u32(q_ready), 4);
+        mbar_init(smem_u32(mma_fin), 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 4 && lane == 0) {
+        tma_prefetch_desc(&p.tmK);
+        tma_prefetch_desc(&p.tmV);
+    }
+    if (warp == 5) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(FA_TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    pdl_wait();  // q and this layer's K/V come from the projection
+
+    if (warp == 4) {
+        // ---------------- K/V producer ----------------
+        if (lane == 0) {
+            const int* pt = p.page_table + (size_t)p.sd.seq[b] * p.max_pages_per_seq;
+            const long long layer_rows = (long long)p.layer * p.n_pages;
+            int issued = 0;
+            for (int j = 0; j < n_kt && !*abort_flag; ++j, ++issued) {
+                const int st = j & 1;
+                if (j >= 2 && !wait(kv_empty + st, (j >> 1) - 1)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                const int k0 = j * FA_BK;
+                const int npg = (min(k0 + FA_BK, len) - k0 + 15) >> 4;
+                int row[FA_BK / 16];
+#pragma unroll
+                for (int pg = 0; pg < FA_BK / 16; ++pg) {
+                    const int pi = (k0 >> 4) + pg;
+                    int page = (pg < npg && pi < p.max_pages_per_seq) ? pt[pi] : 0;
+                    if (page < 0 || page >= p.n_pages) page = 0;  // bad pages were reported by the append
+                    row[pg] = (int)(((layer_rows + page) * p.n_kv + g) * 16);
+                }
+                const uint32_t kd = smem_u32(sm + FA_OFF_K + st * FA_KV), vd = smem_u32(sm + FA_OFF_V + st * FA_KV);
+                const uint32_t kb = smem_u32(k_full + st), vb = smem_u32(v_full + st);
+                mbar_expect_tx(kb, (uint32_t)npg * 2 * 2048);
+                for (int pg = 0; pg < npg; ++pg) {
+                    tma_load_2d(kd + pg * 2048, &p.tmK, kb, 0, row[pg]);
+                    tma_load_2d(kd + FA_KSUB + pg * 2048, &p.tmK, kb, 64, row[pg]);
+                }
+                mbar_expect_tx(vb, (uint32_t)npg * 2 * 2048);
+                for (int pg = 0; pg < npg; ++pg) {
+                    tma_load_2d(vd + pg * 2048, &p.tmV, vb, 0, row[pg]);
+                    tma_load_2d(vd + FA_KSUB + pg * 2048, &p.tmV, vb, 64, row[pg]);
+                }
+            }
+            // the copies issued must have landed before the CTA retires (at once on the normal
+            // path; bounded when another role gave up)
+            for (int jj = max(0, issued - 2); jj < issued; ++jj) {
+                const uint64_t t0 = globaltimer_ns();
+                while (!mbar_try_wait(smem_u32(k_full + (jj & 1)), (jj >> 1) & 1) && globaltimer_ns() - t0 < kTcWaitNs) {
+                }
+                while (!mbar_try_wait(smem_u32(v_full + (jj & 1)), (jj >> 1) & 1) && globaltimer_ns() - t0 < kTcWaitNs) {
+                }
+            }
+        }
+    } else if (warp == 5) {
+        // ---------------- MMA issuer: S_0, S_1, PV_0, S_2, PV_1, ... ----------------
+        // S_{j+2} reuses the TMEM columns of S_j / P_j; it is issued after PV_j, and the MMAs
+        // of a CTA run in issue order.
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = idesc_f16(128, FA_BK);
+            constexpr uint32_t idesc_o = idesc_f16(128, 128) | kIdescBMajorMN;
+            const uint32_t qa = smem_u32(sm);
+            bool ok = wait(q_ready, 0);
+            for (int j = 0; j <= n_kt && ok; ++j) {
+                if (j < n_kt) {
+                    const int st = j & 1;
+                    if (!wait(k_full + st, j >> 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t ka = smem_u32(sm + FA_OFF_K + st * FA_KV);
+#pragma unroll
+                    for (int sub = 0; sub < 2; ++sub)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            umma_f16(tmem + st * FA_BK, sw128_desc(qa + sub * FA_QSUB) + 2 * kk,
+                                     sw128_desc(ka + sub * FA_KSUB) + 2 * kk, idesc_s, (sub | kk) ? 1u : 0u);
+                    umma_commit(smem_u32(s_full + st));
+                }
+                if (j >= 1) {
+                    const int jj = j - 1, sp = jj & 1;
+                    if (!wait(p_full + sp, jj >> 1) || !wait(v_full + sp, jj >> 1)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t va = smem_u32(sm + FA_OFF_V + sp * FA_KV);
+#pragma unroll
+                    for (int kk = 0; kk < FA_BK / 16; ++kk)
+                        umma_f16_ts(tmem + FA_O, tmem + sp * FA_BK + kk * 8, sw128_desc_mn(va + kk * 16 * 128, FA_KSUB),
+                                    idesc_o, (jj | kk) ? 1u : 0u);
+                    umma_commit(smem_u32(pv_done));
+                    umma_commit(smem_u32(kv_empty + sp));
+                }
+            }
+            if (!ok) *abort_flag = 1;
+            umma_commit(smem_u32(mma_fin));
+            const uint64_t t0 = globaltimer_ns();
+            while (!mbar_try_wait(smem_u32(mma_fin), 0) && globaltimer_ns() - t0 < kTcWaitNs) {
+            }
+        }
+    } else {
+        // ---------------- softmax / output: thread = row = TMEM lane ----------------
+        const int r = threadIdx.x;
+        const int hq = 2 * g + (r >> 6), qpos = q0 + (r & 63);
+        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+        // warp-uniform outcome of a bounded wait
+        auto wwait = [&](uint64_t* bar, int parity) { return __all_sync(0xffffffffu, wait(bar, parity)); };
+        {
+            // Q row into the swizzled operand (zeros past the sequence)
+            const bool v = qpos < len;
+            const f16* src = p.q + ((size_t)(base + (v ? qpos : 0)) * p.n_heads + hq) * 128;
+            const uint32_t qd = smem_u32(sm) + r * 128;
+#pragma unroll
+            for (int ch = 0; ch < 16; ++ch) cp_async16(qd + (ch >> 3) * FA_QSUB + (((ch & 7) ^ (r & 7)) << 4), src + ch * 8, v);
+            cp_commit();
+            cp_wait<0>();
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) fa_arrive(smem_u32(q_ready));
+        }
+        float m = -INFINITY, l = 0.f;
+        bool good = true;
+        for (int j = 0; j < n_kt; ++j) {
+            const int st = j & 1, k0 = j * FA_BK;
+            if (!wwait(s_full + st, j >> 1)) {
+                good = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t xa[32], xb[32];
+            TMEM_LD32(lane_base + st * FA_BK, xa);
+            TMEM_LD32(lane_base + st * FA_BK + 32, xb);
+            tmem_wait_ld();
+            float s[FA_BK];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                s[i] = __uint_as_float(xa[i]) * p.scale_log2;
+                s[32 + i] = __uint_as_float(xb[i]) * p.scale_log2;
+            }
+            const bool last = j == n_kt - 1;
+            if (last) {
+#pragma unroll
+                for (int i = 0; i < FA_BK; ++i)
+                    if (k0 + i > qpos || k0 + i >= len) s[i] = -INFINITY;
+            }
+            float mt = s[0];
+#pragma unroll
+            for (int i = 1; i < FA_BK; ++i) mt = fmaxf(mt, s[i]);
+            const bool move = mt > m + FA_RESCALE_LOG2;  // always on the first tile (m = -inf)
+            const float mn = move ? mt : m;
+            const float alpha = move ? ex2_approx(m - mn) : 1.f;  // 2^-inf = 0 on the first tile
+            if (j > 0 && __any_sync(0xffffffffu, move)) {
+                // O holds tiles < j at the old max: once P V of tile j-1 is done, rescale it
+                if (!wwait(pv_done, j - 1)) {
+                    good = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    uint32_t x[32];
+                    TMEM_LD32(lane_base + FA_O + c * 32, x);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) x[i] = __float_as_uint(__uint_as_float(x[i]) * alpha);
+                    TMEM_ST32(lane_base + FA_O + c * 32, x);
+                }
+            }
+            float ls = 0.f;
+            uint32_t h[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float e0 = ex2_approx(s[2 * i] - mn), e1 = ex2_approx(s[2 * i + 1] - mn);
+                ls += e0 + e1;
+                h[i] = pack_h2(e0, e1);
+            }
+            l = l * alpha + ls;
+            m = mn;
+            TMEM_ST32(lane_base + st * FA_BK, h);
+            if (last && k0 + FA_BK > len) {
+                // V rows of keys past the sequence hold stale data; weight 0 must add exactly 0
+                if (!wwait(v_full + st, j >> 1)) {
+                    tmem_wait_st();
+                    good = false;
+                    break;
+                }
+                uint8_t* vs = sm + FA_OFF_V + st * FA_KV;
+                const int kv0 = len - k0;  // first row past the sequence
+                for (int e = lane; e < 16 * 16; e += 32) {
+                    const int row = warp * 16 + (e >> 4), ch = e & 15;
+                    if (row >= kv0)
+                        *reinterpret_cast<uint4*>(vs + (ch >> 3) * FA_KSUB + row * 128 + ((ch & 7) << 4)) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) fa_arrive(smem_u32(p_full + st));
+        }
+        // ---- normalise and store the rows ----
+        if (good && wwait(pv_done, n_kt - 1)) {
+            tc_fence_after();
+            const float inv = 1.f / l;
+            f16* orow = p.out + ((size_t)(base + qpos) * p.n_heads + hq) * 128;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                uint32_t x[32];
+                TMEM_LD32(lane_base + FA_O + c * 32, x);
+                tmem_wait_ld();
+                if (qpos < len) {
+                    uint32_t h[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        h[i] = pack_h2(__uint_as_float(x[2 * i]) * inv, __uint_as_float(x[2 * i + 1]) * inv);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        *reinterpret_cast<uint4*>(orow + c * 32 + u * 8) = make_uint4(h[4 * u], h[4 * u + 1], h[4 * u + 2], h[4 * u + 3]);
+                }
+            }
+        } else {
+            *abort_flag = 1;
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag && threadIdx.x == 0) atomicOr(p.status, QW_DEV_TIMEOUT);
+    if (warp == 5) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(FA_TMEM_COLS) : "memory");
+    }
+}
+
+cudaError_t launch_attn_prefill_tc(const LaunchCtx& c, const StepDesc& sd, int max_len, int layer, const f16* q,
+                                   KVView kv, const CUtensorMap* tmK, const CUtensorMap* tmV, int n_heads, int n_kv,
+                                   f16* out, int* status) {
+    PrefillTcP p;
+    memset(&p, 0, sizeof p);
+    p.tmK = *tmK;
+    p.tmV = *tmV;
+    p.sd = sd;
+    p.q = q;
+    p.out = out;
+    p.page_table = kv.page_table;
+    p.max_pages_per_seq = kv.max_pages_per_seq;
+    p.n_pages = kv.n_pages;
+    p.layer = layer;
+    p.n_heads = n_heads;
+    p.n_kv = n_kv;
+    p.status = status;
+    p.scale_log2 = 0.08838834764831845f * 1.4426950408889634f;  // 128^-0.5 * log2(e)
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(k_attn_prefill_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, FA_SMEM);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    const int qtiles = (max_len + FA_BQ - 1) / FA_BQ;
+    return launch_k(c, k_attn_prefill_tc, dim3(qtiles, n_kv, sd.B), dim3(FA_THREADS), (size_t)FA_SMEM, p);
 }

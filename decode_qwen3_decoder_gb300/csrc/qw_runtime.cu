@@ -803,7 +803,8 @@ static qw_status run_layers(qw_model* m, qw_kv* kv, const StepDesc& sd, bool pre
             // q, k, v were normalised, rotated and appended by the projection's epilogue
             PROF(QW_PROF_ATTN);
             if (prefill)
-                LAUNCH(launch_attn_prefill(lc, sd, max_keys, l, q, kvv, c.n_heads, c.n_kv_heads, attn));
+                LAUNCH(launch_attn_prefill_tc(lc, sd, max_keys, l, q, kvv, &kv->tm_k, &kv->tm_v, c.n_heads,
+                                              c.n_kv_heads, attn, m->status));
             else if (max_keys <= kShortCacheKeys)  // light per-pair kernel: overlaps the other half's GEMMs
                 LAUNCH(launch_attn_paged(lc, T, l, q, c.n_heads, c.n_kv_heads, tv, kvv, sp.chunk, sp.n_splits,
                                          part_o, part_ml, counters, attn, nullptr, sd.seq + t0));
