@@ -1157,21 +1157,23 @@ cudaError_t launch_attn_decode(const LaunchCtx& c, int T, int layer, const f16* 
 //   O += P V      -> A = P from TMEM, B = V as loaded ([key][dim], MN-major), O in TMEM.
 // A row's running max moves only when a tile's max exceeds it by more than 2^8 (then O and
 // the sum are rescaled), so most tiles skip the rescale and P stays <= 256; the final
-// normalisation by the sum is exact either way. One thread issues the MMAs, one streams K/V;
+// normalisation by the sum is exact either way. One thread issues the MMAs; one streams K and
+// one V, each in a ring of two tiles that is released as soon as its MMA finished (K after
+// S = Q K^T, V after O += P V), so the next K tile loads while this tile's softmax runs.
 // 96 KB of shared memory and 256 TMEM columns let two CTAs share an SM; every wait is bounded.
 // =======================================================================================
 namespace {
 
 constexpr int FA_BQ = 64;               // queries per head (128 MMA rows for the head pair)
 constexpr int FA_BK = 64;               // keys per tile
-constexpr int FA_THREADS = 192;         // warps 0-3 softmax/output, 4 producer, 5 MMA
+constexpr int FA_THREADS = 224;         // warps 0-3 softmax/output, 4 K producer, 5 MMA, 6 V producer
 constexpr int FA_QSUB = 128 * 128;      // Q: [128 rows][64 dims] swizzled subtile (16 KB)
 constexpr int FA_KSUB = FA_BK * 128;    // K, V: [64 keys][64 dims] swizzled subtile (8 KB)
 constexpr int FA_KV = 2 * FA_KSUB;      // one K or V tile, all 128 dims
 constexpr int FA_OFF_K = 2 * FA_QSUB;   // [2] stages
 constexpr int FA_OFF_V = FA_OFF_K + 2 * FA_KV;
 constexpr int FA_OFF_BAR = FA_OFF_V + 2 * FA_KV;
-constexpr int FA_SMEM = 1024 + FA_OFF_BAR + 128;
+constexpr int FA_SMEM = 1024 + FA_OFF_BAR + 256;
 constexpr int FA_TMEM_COLS = 256;       // S[0] 0-63, S[1] 64-127, O 128-255
 constexpr int FA_O = 128;
 constexpr float FA_RESCALE_LOG2 = 8.f;  // the running max moves only past 2^8
@@ -1200,13 +1202,17 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_attn_prefill_tc(const __grid_
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + FA_OFF_BAR);
     uint64_t* k_full = bars;        // [2] K of a stage landed
     uint64_t* v_full = bars + 2;    // [2] V of a stage landed
-    uint64_t* kv_empty = bars + 4;  // [2] the stage's S and P V MMAs finished
-    uint64_t* s_full = bars + 6;    // [2] S buffer written
-    uint64_t* p_full = bars + 8;    // [2] P written into the S buffer, O rescaled
-    uint64_t* pv_done = bars + 10;  // O += P V finished
-    uint64_t* q_ready = bars + 11;
-    uint64_t* mma_fin = bars + 12;  // every MMA of the CTA finished (before TMEM is freed)
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
+    uint64_t* k_empty = bars + 4;   // [2] S = Q K^T of the stage finished
+    uint64_t* v_empty = bars + 6;   // [2] O += P V of the stage finished
+    uint64_t* s_full = bars + 8;    // [2] S buffer written
+    uint64_t* p_full = bars + 10;   // [2] P written into the S buffer, O rescaled
+    // [2] O += P V of the even / odd tiles finished. One barrier per tile parity: when a
+    // softmax warp finishes its last tile, P V of the two previous tiles may still be pending,
+    // and a single barrier's parity could not tell those three states apart.
+    uint64_t* pv_done = bars + 12;
+    uint64_t* q_ready = bars + 14;
+    uint64_t* mma_fin = bars + 15;  // every MMA of the CTA finished (before TMEM is freed)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int b = blockIdx.z, g = blockIdx.y;
@@ -1223,21 +1229,20 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_attn_prefill_tc(const __grid_
         for (int i = 0; i < 2; ++i) {
             mbar_init(smem_u32(k_full + i), 1);
             mbar_init(smem_u32(v_full + i), 1);
-            mbar_init(smem_u32(kv_empty + i), 1);
+            mbar_init(smem_u32(k_empty + i), 1);
+            mbar_init(smem_u32(v_empty + i), 1);
             mbar_init(smem_u32(s_full + i), 1);
             mbar_init(smem_u32(p_full + i), 4);
+            mbar_init(smem_u32(pv_done + i), 1);
         }
-        mbar_init(smem_u32(pv_done), 1);
         mbar_init(smem_u32(q_ready), 4);
         mbar_init(smem_u32(mma_fin), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
-    if (warp == 4 && lane == 0) {
-        tma_prefetch_desc(&p.tmK);
-        tma_prefetch_desc(&p.tmV);
-    }
+    if (warp == 4 && lane == 0) tma_prefetch_desc(&p.tmK);
+    if (warp == 6 && lane == 0) tma_prefetch_desc(&p.tmV);
     if (warp == 5) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
                      "r"(FA_TMEM_COLS)
@@ -1250,55 +1255,55 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_attn_prefill_tc(const __grid_
     const uint32_t tmem = *tmem_slot;
     pdl_wait();  // q and this layer's K/V come from the projection
 
-    if (warp == 4) {
-        // ---------------- K/V producer ----------------
+    if (warp == 4 || warp == 6) {
+        // ---------------- producers: warp 4 streams K, warp 6 streams V ----------------
         if (lane == 0) {
+            const bool is_k = warp == 4;
+            const CUtensorMap* tm = is_k ? &p.tmK : &p.tmV;
+            uint64_t* full = is_k ? k_full : v_full;
+            uint64_t* empty = is_k ? k_empty : v_empty;
+            uint8_t* ring = sm + (is_k ? FA_OFF_K : FA_OFF_V);
             const int* pt = p.page_table + (size_t)p.sd.seq[b] * p.max_pages_per_seq;
             const long long layer_rows = (long long)p.layer * p.n_pages;
             int issued = 0;
             for (int j = 0; j < n_kt && !*abort_flag; ++j, ++issued) {
                 const int st = j & 1;
-                if (j >= 2 && !wait(kv_empty + st, (j >> 1) - 1)) {
+                if (j >= 2 && !wait(empty + st, (j >> 1) - 1)) {
                     *abort_flag = 1;
                     break;
                 }
                 const int k0 = j * FA_BK;
                 const int npg = (min(k0 + FA_BK, len) - k0 + 15) >> 4;
-                int row[FA_BK / 16];
-#pragma unroll
-                for (int pg = 0; pg < FA_BK / 16; ++pg) {
+                const uint32_t dst = smem_u32(ring + st * FA_KV), bar = smem_u32(full + st);
+                mbar_expect_tx(bar, (uint32_t)npg * 2 * 2048);
+                for (int pg = 0; pg < npg; ++pg) {
                     const int pi = (k0 >> 4) + pg;
-                    int page = (pg < npg && pi < p.max_pages_per_seq) ? pt[pi] : 0;
+                    int page = pi < p.max_pages_per_seq ? pt[pi] : 0;
                     if (page < 0 || page >= p.n_pages) page = 0;  // bad pages were reported by the append
-                    row[pg] = (int)(((layer_rows + page) * p.n_kv + g) * 16);
-                }
-                const uint32_t kd = smem_u32(sm + FA_OFF_K + st * FA_KV), vd = smem_u32(sm + FA_OFF_V + st * FA_KV);
-                const uint32_t kb = smem_u32(k_full + st), vb = smem_u32(v_full + st);
-                mbar_expect_tx(kb, (uint32_t)npg * 2 * 2048);
-                for (int pg = 0; pg < npg; ++pg) {
-                    tma_load_2d(kd + pg * 2048, &p.tmK, kb, 0, row[pg]);
-                    tma_load_2d(kd + FA_KSUB + pg * 2048, &p.tmK, kb, 64, row[pg]);
-                }
-                mbar_expect_tx(vb, (uint32_t)npg * 2 * 2048);
-                for (int pg = 0; pg < npg; ++pg) {
-                    tma_load_2d(vd + pg * 2048, &p.tmV, vb, 0, row[pg]);
-                    tma_load_2d(vd + FA_KSUB + pg * 2048, &p.tmV, vb, 64, row[pg]);
+                    const int row = (int)(((layer_rows + page) * p.n_kv + g) * 16);
+                    tma_load_2d(dst + pg * 2048, tm, bar, 0, row);
+                    tma_load_2d(dst + FA_KSUB + pg * 2048, tm, bar, 64, row);
                 }
             }
-            // the copies issued must have landed before the CTA retires (at once on the normal
-            // path; bounded when another role gave up)
+            // Before the CTA retires, the copies issued must have landed and the MMA thread's
+            // releases of the last two tiles (asynchronous arrivals from tcgen05.commit) must have
+            // reached this ring's barriers: an arrival still in flight would land in the shared
+            // memory of the next CTA on this SM. At once on the normal path; bounded when another
+            // role gave up.
             for (int jj = max(0, issued - 2); jj < issued; ++jj) {
                 const uint64_t t0 = globaltimer_ns();
-                while (!mbar_try_wait(smem_u32(k_full + (jj & 1)), (jj >> 1) & 1) && globaltimer_ns() - t0 < kTcWaitNs) {
+                while (!mbar_try_wait(smem_u32(full + (jj & 1)), (jj >> 1) & 1) && globaltimer_ns() - t0 < kTcWaitNs) {
                 }
-                while (!mbar_try_wait(smem_u32(v_full + (jj & 1)), (jj >> 1) & 1) && globaltimer_ns() - t0 < kTcWaitNs) {
+                while (!*abort_flag && !mbar_try_wait(smem_u32(empty + (jj & 1)), (jj >> 1) & 1) &&
+                       globaltimer_ns() - t0 < kTcWaitNs) {
                 }
             }
         }
     } else if (warp == 5) {
         // ---------------- MMA issuer: S_0, S_1, PV_0, S_2, PV_1, ... ----------------
-        // S_{j+2} reuses the TMEM columns of S_j / P_j; it is issued after PV_j, and the MMAs
-        // of a CTA run in issue order.
+        // S_{j+2} reuses the TMEM columns of S_j / P_j: it is issued only once PV_j, which
+        // reads P_j from those columns, has finished (issue order alone does not keep a later
+        // MMA's accumulator writes behind an earlier MMA's reads of A from tensor memory).
         if (lane == 0) {
             constexpr uint32_t idesc_s = idesc_f16(128, FA_BK);
             constexpr uint32_t idesc_o = idesc_f16(128, 128) | kIdescBMajorMN;
@@ -1307,7 +1312,7 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_attn_prefill_tc(const __grid_
             for (int j = 0; j <= n_kt && ok; ++j) {
                 if (j < n_kt) {
                     const int st = j & 1;
-                    if (!wait(k_full + st, j >> 1)) {
+                    if (!wait(k_full + st, j >> 1) || (j >= 2 && !wait(pv_done + st, (j - 2) >> 1))) {
                         ok = false;
                         break;
                     }
@@ -1320,6 +1325,7 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_attn_prefill_tc(const __grid_
                             umma_f16(tmem + st * FA_BK, sw128_desc(qa + sub * FA_QSUB) + 2 * kk,
                                      sw128_desc(ka + sub * FA_KSUB) + 2 * kk, idesc_s, (sub | kk) ? 1u : 0u);
                     umma_commit(smem_u32(s_full + st));
+                    umma_commit(smem_u32(k_empty + st));
                 }
                 if (j >= 1) {
                     const int jj = j - 1, sp = jj & 1;
@@ -1333,8 +1339,8 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_attn_prefill_tc(const __grid_
                     for (int kk = 0; kk < FA_BK / 16; ++kk)
                         umma_f16_ts(tmem + FA_O, tmem + sp * FA_BK + kk * 8, sw128_desc_mn(va + kk * 16 * 128, FA_KSUB),
                                     idesc_o, (jj | kk) ? 1u : 0u);
-                    umma_commit(smem_u32(pv_done));
-                    umma_commit(smem_u32(kv_empty + sp));
+                    umma_commit(smem_u32(pv_done + sp));
+                    umma_commit(smem_u32(v_empty + sp));
                 }
             }
             if (!ok) *abort_flag = 1;
@@ -1396,7 +1402,7 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_attn_prefill_tc(const __grid_
             const float alpha = move ? ex2_approx(m - mn) : 1.f;  // 2^-inf = 0 on the first tile
             if (j > 0 && __any_sync(0xffffffffu, move)) {
                 // O holds tiles < j at the old max: once P V of tile j-1 is done, rescale it
-                if (!wwait(pv_done, j - 1)) {
+                if (!wwait(pv_done + ((j - 1) & 1), (j - 1) >> 1)) {
                     good = false;
                     break;
                 }
@@ -1445,7 +1451,7 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_attn_prefill_tc(const __grid_
             if (lane == 0) fa_arrive(smem_u32(p_full + st));
         }
         // ---- normalise and store the rows ----
-        if (good && wwait(pv_done, n_kt - 1)) {
+        if (good && wwait(pv_done + ((n_kt - 1) & 1), (n_kt - 1) >> 1)) {
             tc_fence_after();
             const float inv = 1.f / l;
             f16* orow = p.out + ((size_t)(base + qpos) * p.n_heads + hq) * 128;

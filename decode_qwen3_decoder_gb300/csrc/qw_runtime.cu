@@ -171,6 +171,7 @@ struct qw_model {
     int32_t *gen_tok, *gen_cur, *gen_out;
     float* dbg_hidden;
     int32_t *dbg_pos, *dbg_slot;
+    f16* dbg_attn;
     cudaStream_t cap_stream;
     cudaStream_t aux_stream;   // second half of a split decode batch
     cudaEvent_t ev_fork, ev_join;
@@ -419,6 +420,7 @@ extern "C" qw_status qw_init_weights(const qw_config* cfg, const qw_weight_ptrs*
     m->split_decode = true;
     m->dbg_hidden = nullptr;
     m->dbg_pos = m->dbg_slot = nullptr;
+    m->dbg_attn = nullptr;
     m->prof_kind = QW_PROF_OFF;
     m->prof_gen = 0;
     m->trace = nullptr;
@@ -446,6 +448,12 @@ extern "C" qw_status qw_debug_set(qw_model* m, float* dev_hidden, int32_t* dev_p
     m->dbg_hidden = dev_hidden;
     m->dbg_pos = dev_hidden ? dev_positions : nullptr;
     m->dbg_slot = dev_hidden ? dev_slots : nullptr;
+    return QW_OK;
+}
+
+extern "C" qw_status qw_debug_set_attn(qw_model* m, void* dev_attn) {
+    if (!m) return fail(QW_ERR_INVALID_ARG, "model is NULL");
+    m->dbg_attn = reinterpret_cast<f16*>(dev_attn);
     return QW_OK;
 }
 
@@ -813,6 +821,9 @@ static qw_status run_layers(qw_model* m, qw_kv* kv, const StepDesc& sd, bool pre
                                           max_keys, kMaxSplits,
                                           part_o, part_ml, counters, attn, m->status, m->num_sms));
         }
+        if (dbg && m->dbg_attn)
+            CUDA_TRY(cudaMemcpyAsync(m->dbg_attn + ((size_t)l * sd.T + t0) * QD, attn, (size_t)T * QD * sizeof(f16),
+                                     cudaMemcpyDeviceToDevice, st));
         if (small) {
             PROF(QW_PROF_OPROJ);
             LAUNCH(launch_gemv_resid(lc, T, attn, m->bo + (size_t)l * D * QD, D, QD, x));

@@ -73,6 +73,7 @@ SIGNATURES = {
     "qw_free_model": (None, [_VP]),
     "qw_free_kv": (None, [_VP]),
     "qw_debug_set": (_I, [_VP, _VP, _VP, _VP]),
+    "qw_debug_set_attn": (_I, [_VP, _VP]),
     "qw_kv_page_table": (_I, [_VP, _I, _P(ctypes.c_int32), _I]),
     "qw_kv_pool_ptrs": (_I, [_VP, _P(_VP), _P(_VP), _P(_I)]),
     "qw_kv_fill_synthetic": (_I, [_VP, _I, _I, ctypes.c_uint64, _VP]),
@@ -205,6 +206,10 @@ def qw_free_kv(kv: int) -> None:
 
 def qw_debug_set(model: int, hidden_ptr: int, pos_ptr: int, slot_ptr: int) -> None:
     _check(load().qw_debug_set(model, hidden_ptr or None, pos_ptr or None, slot_ptr or None))
+
+
+def qw_debug_set_attn(model: int, attn_ptr: int) -> None:
+    _check(load().qw_debug_set_attn(model, attn_ptr or None))
 
 
 def qw_kv_page_table(kv: int, seq_id: int, max_pages: int = 1 << 16):

@@ -184,6 +184,12 @@ void qw_free_kv(qw_kv* kv);
  * not graph-captured. */
 qw_status qw_debug_set(qw_model* m, float* dev_hidden, int32_t* dev_positions, int32_t* dev_slots);
 
+/* While qw_debug_set is on and dev_attn is non-NULL, prefill calls and decode calls that run
+ * layer by layer (more than the persistent decode kernel's batch) also copy each layer's
+ * attention output, the input of o_proj, to dev_attn[layer][t][n_heads * head_dim] (fp16,
+ * t < that call's token count). NULL turns it off. */
+qw_status qw_debug_set_attn(qw_model* m, void* dev_attn);
+
 /* Copy sequence seq_id's page table (host mirror) into host_out[0..max_pages); returns the
  * number of pages it owns, or a negative qw_status. */
 int qw_kv_page_table(const qw_kv* kv, int seq_id, int32_t* host_out, int max_pages);

@@ -121,3 +121,77 @@ def test_two_stream_decode(blk, B):
     qw.qw_set_option(eng.model, qw.QW_OPT_SPLIT_DECODE, 1)
     for a, b in zip(out[1], out[0]):
         check_logits(a, b, tol=2e-2)
+
+
+class _PeakyQK:
+    """The seeded weights with every QK-norm weight set to 2.0. Normalised q and k then have
+    RMS 2 per component, the attention logits q.k / sqrt(128) a standard deviation near 4, and
+    each query's softmax mass sits on a few keys: a stale or wrong key/value tile changes the
+    attention output by O(1) instead of averaging out as it does with near-uniform weights."""
+
+    def __init__(self, base):
+        self.base = base
+        self.shape = base.shape
+
+    @property
+    def embed(self):
+        return self.base.embed
+
+    @property
+    def final_norm(self):
+        return self.base.final_norm
+
+    def layer(self, i):
+        d = dict(self.base.layer(i))
+        for name in ("self_attn.q_norm.weight", "self_attn.k_norm.weight"):
+            d[name] = np.full_like(d[name], 0x4000)  # bf16 bits of 2.0
+        return d
+
+    def named(self):
+        yield "model.embed_tokens.weight", self.embed
+        for i in range(self.shape.n_layers):
+            for name, arr in self.layer(i).items():
+                yield f"model.layers.{i}.{name}", arr
+        yield "model.norm.weight", self.final_norm
+
+
+ATTN_REL = 2e-2  # ||o_gpu - o_oracle|| / ||o_oracle|| per token (fp16 q, k, v, P; peaky softmax)
+
+
+@pytest.mark.parametrize("lens", [(300, 129, 64, 17), (1000,)])
+def test_prefill_attention_peaky(qw, lens):
+    """Prefill attention output of every token against the oracle's, with sharply peaked
+    softmax rows; sequences span many 64-key tiles and end mid-tile and mid-page."""
+    import torch
+    w = _PeakyQK(weights(S1))
+    om = oracle.Model(w)
+    names = [n for n, _ in synth.Weights(S1).named()]
+    wd = dict(w.named())
+    assert sorted(wd) == sorted(names)
+    eng = qw.qw.Engine(S1, wd, max_tokens=1024, max_batch=8, max_context=1024, kv_pages=256, max_seqs=8)
+    try:
+        run = Run(qw, eng)
+        prompts = [synth.make_tokens(S1.vocab, n, 900 + i).tolist() for i, n in enumerate(lens)]
+        T = sum(lens)
+        attn = torch.zeros((S1.n_layers, T, S1.n_heads * S1.head_dim), dtype=torch.float16, device="cuda")
+        qw.qw.qw_debug_set_attn(eng.model, attn.data_ptr())
+        try:
+            g = run.prefill(list(range(len(lens))), prompts)
+        finally:
+            qw.qw.qw_debug_set_attn(eng.model, 0)
+        assert g["status"] == 0
+        a = attn.float().cpu().numpy()
+        row = 0
+        for b, p in enumerate(prompts):
+            taps = {}
+            o = oracle.forward(om, p, oracle.SeqCache(S1.n_layers), taps=taps)
+            want = taps["attn"][0]
+            got = a[0, row:row + len(p)]
+            err = np.linalg.norm(got - want, axis=1) / np.linalg.norm(want, axis=1)
+            worst = int(np.argmax(err))
+            assert err[worst] <= ATTN_REL, f"sequence {b}, token {worst}: {err[worst]:.3e}"
+            check_hidden(g["hidden"][:, row:row + len(p)], o["hidden"])
+            check_logits(g["logits"][b], o["logits"])
+            row += len(p)
+    finally:
+        eng.close()
