@@ -400,28 +400,11 @@ cudaError_t launch_attn_paged(const LaunchCtx& c, int T, int layer, const f16* q
 }
 
 // =======================================================================================
-// k_attn_prefill: causal GQA attention of a prefill (sequences start empty, so position =
-// index in the prompt) on the tensor cores, flash style (Paso 5): for each tile of 64
-// queries of one sequence and one KV head, both query heads 2g and 2g+1 (128 rows, 8 warps
-// of 16 rows) stream the sequence's K/V tiles of 64 keys through shared memory once; each
-// tile is processed as two halves of 32 keys (fewer live registers, two CTAs per SM).
-// S = Q K^T and O += P V use mma.sync m16n8k16 (fp16 operands, fp32 accumulation); the
-// online softmax runs in fp32 in the exp2 domain; P goes from the S accumulators straight
-// into the A fragments of P V. K/V tiles (the new keys were just appended to the paged
-// cache: key j sits at page_table[seq][j / 16], slot j % 16) are double-buffered with
-// cp.async; shared rows of
-// 256 bytes are XOR-swizzled by 16-byte chunk so ldmatrix is conflict-free. Key tiles past
-// the query tile are skipped; the diagonal tile is masked key > query.
+// Warp-level helpers of the mma.sync paths (decode attention) and of the prefill kernel's
+// Q staging: cp.async copies, ldmatrix, m16n8k16 MMA.
 // =======================================================================================
 namespace {
 
-constexpr int PF_Q = 64;      // queries per CTA (per head)
-constexpr int PF_KV = 64;     // keys per tile
-constexpr int PF_WARPS = 8;
-
-__device__ __forceinline__ uint32_t swz(int row, int chunk) {  // byte offset in a 256-byte-row tile
-    return (uint32_t)(row * 256 + ((chunk ^ (row & 7)) << 4));
-}
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
     const int n = valid ? 16 : 0;
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(n) : "memory");
@@ -455,233 +438,6 @@ __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
-}
-
-struct PrefillP {
-    StepDesc sd;
-    const f16* q;       // [T][n_heads][128]
-    const f16* k;       // this layer's K pool [n_pages][n_kv][16][128]
-    const f16* v;
-    const int* page_table;
-    int max_pages_per_seq, n_pages;
-    f16* out;           // [T][n_heads * 128]
-    int n_heads, n_kv;
-    float scale_log2;
-};
-
-__global__ void __launch_bounds__(PF_WARPS * 32, 2) k_attn_prefill(const __grid_constant__ PrefillP p) {
-    extern __shared__ __align__(128) uint8_t pf_smem[];
-    const uint32_t sQ = (uint32_t)__cvta_generic_to_shared(pf_smem);  // [128 rows][256 B]
-    const uint32_t sK = sQ + 128 * 256;                               // [2][64][256 B]
-    const uint32_t sV = sK + 2 * PF_KV * 256;                         // [2][64][256 B]
-    pdl_launch();
-    pdl_wait();
-    const int b = blockIdx.z, g = blockIdx.y;
-    const int len = p.sd.start[b + 1] - p.sd.start[b];
-    const int qt = (int)gridDim.x - 1 - (int)blockIdx.x;  // heavy (late) query tiles first
-    const int q0 = qt * PF_Q;
-    if (q0 >= len) return;
-    const int base = p.sd.start[b];
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int* pt = p.page_table + (size_t)p.sd.seq[b] * p.max_pages_per_seq;
-
-    // ---- Q tile: rows 0..63 head 2g, rows 64..127 head 2g+1 ---------------------------
-    for (int i = tid; i < 128 * 16; i += PF_WARPS * 32) {
-        const int row = i >> 4, ch = i & 15;
-        const int hq = 2 * g + (row >> 6), qi = q0 + (row & 63);
-        const bool v = qi < len;
-        const f16* src = p.q + ((size_t)(base + (v ? qi : 0)) * p.n_heads + hq) * 128 + ch * 8;
-        cp_async16(sQ + swz(row, ch), src, v);
-    }
-    auto load_kv = [&](int kt, int buf) {
-        const int k0 = kt * PF_KV;
-        // 256 threads x 4: pass j copies rows 16 j .. 16 j + 15 = page j of the tile
-        static_assert(PF_KV == 64 && PF_WARPS * 32 == 256, "one page per pass");
-        int page[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int pi = (k0 >> 4) + j;
-            page[j] = (pi * 16 < len && pi < p.max_pages_per_seq) ? pt[pi] : -1;
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int row = (tid >> 4) + 16 * j, ch = tid & 15;
-            const int kj = k0 + row;  // key position (the sequence started empty)
-            const bool v = kj < len && page[j] >= 0 && page[j] < p.n_pages;  // bad pages were reported
-            const size_t off = (((size_t)(v ? page[j] : 0) * p.n_kv + g) * 16 + (kj & 15)) * 128 + ch * 8;
-            cp_async16(sK + buf * PF_KV * 256 + swz(row, ch), p.k + off, v);
-            cp_async16(sV + buf * PF_KV * 256 + swz(row, ch), p.v + off, v);
-        }
-    };
-    const int n_kt = (min(len, q0 + PF_Q) + PF_KV - 1) / PF_KV;  // causal: keys < q0 + 64
-    load_kv(0, 0);
-    cp_commit();
-
-    // this warp: 16 query rows of one head
-    const int r0 = warp * 16;                   // row in the Q tile
-    const int gq = lane >> 2, tq = lane & 3;
-    const int qpos0 = q0 + (r0 & 63) + gq;      // positions of this thread's two rows
-    const int qpos1 = qpos0 + 8;
-    float o[16][4];
-#pragma unroll
-    for (int n = 0; n < 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-
-    for (int kt = 0; kt < n_kt; ++kt) {
-        const int buf = kt & 1;
-        if (kt + 1 < n_kt) load_kv(kt + 1, buf ^ 1);
-        cp_commit();
-        cp_wait<1>();
-        __syncthreads();
-        const uint32_t kb = sK + buf * PF_KV * 256;
-        const uint32_t vb = sV + buf * PF_KV * 256;
-        const int k0 = kt * PF_KV;
-        // two halves of 32 keys, each with its own online-softmax update (fewer live
-        // registers: two CTAs fit on an SM); Q fragments are re-read from shared memory
-#pragma unroll
-        for (int hk = 0; hk < 2; ++hk) {
-            // ---- S = Q K^T (16 rows x 32 keys) -------------------------------------------
-            float s[4][4];
-#pragma unroll
-            for (int n = 0; n < 4; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) {
-                uint32_t qa[4];
-                {
-                    const int row = r0 + (lane & 7) + ((lane >> 3) & 1) * 8;
-                    const int ch = 2 * ks + (lane >> 4);
-                    ldsm_x4(sQ + swz(row, ch), qa[0], qa[1], qa[2], qa[3]);
-                }
-#pragma unroll
-                for (int np = 0; np < 2; ++np) {  // pairs of 8-key n-tiles
-                    const int key = hk * 32 + np * 16 + (lane & 7) + ((lane >> 4) & 1) * 8;
-                    const int ch = 2 * ks + ((lane >> 3) & 1);
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(kb + swz(key, ch), b0, b1, b2, b3);
-                    mma16816(s[2 * np], qa, b0, b1);
-                    mma16816(s[2 * np + 1], qa, b2, b3);
-                }
-            }
-            // ---- online softmax (exp2 domain), causal mask on the diagonal / tail keys -----
-            float tm0 = -INFINITY, tm1 = -INFINITY;
-            const int kh0 = k0 + hk * 32;  // first key of this half
-            if (kh0 + 31 <= q0 && kh0 + 32 <= len) {  // every key visible to every row
-#pragma unroll
-                for (int n = 0; n < 4; ++n)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        s[n][e] *= p.scale_log2;
-                        s[n][2 + e] *= p.scale_log2;
-                        tm0 = fmaxf(tm0, s[n][e]);
-                        tm1 = fmaxf(tm1, s[n][2 + e]);
-                    }
-            } else {
-#pragma unroll
-                for (int n = 0; n < 4; ++n) {
-                    const int kp = kh0 + n * 8 + 2 * tq;
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const bool in = (kp + e) < len;
-                        s[n][e] = (in && kp + e <= qpos0) ? s[n][e] * p.scale_log2 : -INFINITY;
-                        s[n][2 + e] = (in && kp + e <= qpos1) ? s[n][2 + e] * p.scale_log2 : -INFINITY;
-                        tm0 = fmaxf(tm0, s[n][e]);
-                        tm1 = fmaxf(tm1, s[n][2 + e]);
-                    }
-                }
-            }
-            tm0 = fmaxf(tm0, __shfl_xor_sync(0xffffffffu, tm0, 1));
-            tm0 = fmaxf(tm0, __shfl_xor_sync(0xffffffffu, tm0, 2));
-            tm1 = fmaxf(tm1, __shfl_xor_sync(0xffffffffu, tm1, 1));
-            tm1 = fmaxf(tm1, __shfl_xor_sync(0xffffffffu, tm1, 2));
-            const float nm0 = fmaxf(m0, tm0), nm1 = fmaxf(m1, tm1);
-            // rows with no visible key yet keep m = -inf; guard the rescale against inf - inf
-            const float a0 = (nm0 == -INFINITY) ? 1.f : ex2_approx(m0 - nm0);
-            const float a1 = (nm1 == -INFINITY) ? 1.f : ex2_approx(m1 - nm1);
-            m0 = nm0;
-            m1 = nm1;
-            l0 *= a0;
-            l1 *= a1;
-#pragma unroll
-            for (int n = 0; n < 16; ++n) {
-                o[n][0] *= a0;
-                o[n][1] *= a0;
-                o[n][2] *= a1;
-                o[n][3] *= a1;
-            }
-            uint32_t pa[2][4];  // P as A fragments of P V, 2 k-steps of 16 keys
-            // a row with no visible key yet has m = -inf: use 0 as its reference (all its
-            // scores are -inf, so every weight is 2^-inf = 0)
-            const float r0 = (m0 == -INFINITY) ? 0.f : m0, r1 = (m1 == -INFINITY) ? 0.f : m1;
-#pragma unroll
-            for (int n = 0; n < 4; ++n) {
-                const float e0 = ex2_approx(s[n][0] - r0);
-                const float e1 = ex2_approx(s[n][1] - r0);
-                const float e2 = ex2_approx(s[n][2] - r1);
-                const float e3 = ex2_approx(s[n][3] - r1);
-                l0 += e0 + e1;
-                l1 += e2 + e3;
-                pa[n >> 1][(n & 1) * 2 + 0] = pack_h2(e0, e1);
-                pa[n >> 1][(n & 1) * 2 + 1] = pack_h2(e2, e3);
-            }
-            // ---- O += P V ----------------------------------------------------------------
-#pragma unroll
-            for (int ks = 0; ks < 2; ++ks) {
-#pragma unroll
-                for (int np = 0; np < 8; ++np) {  // pairs of 8-dim n-tiles
-                    const int key = hk * 32 + ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
-                    const int ch = 2 * np + (lane >> 4);
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(vb + swz(key, ch), b0, b1, b2, b3);
-                    mma16816(o[2 * np], pa[ks], b0, b1);
-                    mma16816(o[2 * np + 1], pa[ks], b2, b3);
-                }
-            }
-        }
-        __syncthreads();  // the buffer is refilled two iterations later
-    }
-    cp_wait<0>();
-    // ---- normalise and store -------------------------------------------------------------
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-    const float i0 = 1.f / l0, i1 = 1.f / l1;
-    const int hq = 2 * g + (r0 >> 6);
-#pragma unroll
-    for (int n = 0; n < 16; ++n) {
-        const int d = n * 8 + 2 * tq;
-        if (qpos0 < len)
-            *reinterpret_cast<uint32_t*>(p.out + ((size_t)(base + qpos0) * p.n_heads + hq) * 128 + d) =
-                pack_h2(o[n][0] * i0, o[n][1] * i0);
-        if (qpos1 < len)
-            *reinterpret_cast<uint32_t*>(p.out + ((size_t)(base + qpos1) * p.n_heads + hq) * 128 + d) =
-                pack_h2(o[n][2] * i1, o[n][3] * i1);
-    }
-}
-
-cudaError_t launch_attn_prefill(const LaunchCtx& c, const StepDesc& sd, int max_len, int layer, const f16* q,
-                                KVView kv, int n_heads, int n_kv, f16* out) {
-    PrefillP p;
-    p.sd = sd;
-    p.q = q;
-    p.k = kv.k + (size_t)layer * kv.layer_stride;
-    p.v = kv.v + (size_t)layer * kv.layer_stride;
-    p.page_table = kv.page_table;
-    p.max_pages_per_seq = kv.max_pages_per_seq;
-    p.n_pages = kv.n_pages;
-    p.out = out;
-    p.n_heads = n_heads;
-    p.n_kv = n_kv;
-    p.scale_log2 = 0.08838834764831845f * 1.4426950408889634f;
-    const int smem = 128 * 256 + 4 * PF_KV * 256;  // 96 KB
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(k_attn_prefill, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
-    const int qtiles = (max_len + PF_Q - 1) / PF_Q;
-    return launch_k(c, k_attn_prefill, dim3(qtiles, n_kv, sd.B), dim3(PF_WARPS * 32), (size_t)smem, p);
 }
 
 // =======================================================================================

@@ -160,8 +160,6 @@ cudaError_t launch_attn_decode(const LaunchCtx& c, int T, int layer, const f16* 
                                int num_sms);
 // Causal flash attention of a prefill (sequences start empty) over the K/V just appended to
 // the paged cache.
-cudaError_t launch_attn_prefill(const LaunchCtx& c, const StepDesc& sd, int max_len, int layer, const f16* q,
-                                KVView kv, int n_heads, int n_kv, f16* out);
 // Causal flash attention of a prefill on tcgen05 (S and O in TMEM), K/V from the cache pages
 // through the pools' tensor maps.
 cudaError_t launch_attn_prefill_tc(const LaunchCtx& c, const StepDesc& sd, int max_len, int layer, const f16* q,
