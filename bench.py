@@ -597,7 +597,7 @@ def cores():
         return os.cpu_count()
 
 
-def cpu_baseline(cfg, n_decode=8):
+def cpu_baseline(cfg, n_decode=96):
     v, dt = oracle_sample(cfg, n_decode, 4242)
     return {"value": round(v, 4), "unit": cfg["unit"], "cores": cores(), "kind": "oracle",
             "sample": f"fp64 NumPy oracle, {cfg['prompt']}-token prompt prefill + {n_decode} greedy decode steps "
