@@ -65,9 +65,15 @@ NCU_TRAFFIC = {
                                              "0eca842ea9e3d616dc7a649c7eefeedf777de9b09921357bd6f4f5fcf25f82c9"),
     (1, "qkv_proj(rmsnorm fused)"): (8409856, "decode_qwen3_decoder_gb300/csrc/k_small.cu",
                                      "0eca842ea9e3d616dc7a649c7eefeedf777de9b09921357bd6f4f5fcf25f82c9"),
-    (3, "gate_up+silu_mul"): (29390080 + 446976, "decode_qwen3_decoder_gb300/csrc/k_gemm.cu", "f566e7ddb93c954624b5befc4d82bd0bade5d8f7fc9471aab3688c52dbee812b"),
-    (3, "qkv_proj+qk_norm+rope+kv_append"): (25536256 + 9972736, "decode_qwen3_decoder_gb300/csrc/k_gemm.cu",
-                                             "f566e7ddb93c954624b5befc4d82bd0bade5d8f7fc9471aab3688c52dbee812b"),
+    (3, "gate_up+silu_mul"): (29389056 + 523264, "decode_qwen3_decoder_gb300/csrc/k_gemm.cu",
+                              "453fe4f107647e6c90c4e837a33290347795cddcaebe25046108888fe16f4382"),
+    (3, "qkv_proj+qk_norm+rope+kv_append"): (25540096 + 11586048, "decode_qwen3_decoder_gb300/csrc/k_gemm.cu",
+                                             "453fe4f107647e6c90c4e837a33290347795cddcaebe25046108888fe16f4382"),
+    # batched decode attention: measured on 256-token caches (two 32-token launches, 35.83 MB
+    # each, 1.064 x their algorithmic bytes) and scaled by the key count to one 64-token launch
+    # of the full workload (285.2 MB algorithmic); the traffic grows with the keys read
+    (2, "attention"): (303361426, "decode_qwen3_decoder_gb300/csrc/k_attn.cu",
+                       "61af91e223391560db436f3e9959056499064c92da6d764574cc549d568fe58c"),
 }
 
 
