@@ -1,4 +1,5 @@
-"""CPU oracle for the Qwen3-style decoder forward pass (prefill + greedy decode).
+"""CPU oracle for the Qwen3-style decoder forward pass (prefill + greedy decode) and for
+temperature + top-p sampling.
 
 TEST INFRASTRUCTURE ONLY. This package is a plain, slow, fp64 NumPy restatement of the
 computation described on the page "Dentro de un LLM: Inferencia en Python puro para
@@ -22,4 +23,10 @@ from .qwen3 import (  # noqa: F401
     forward,
     generate,
     argmax_lowest,
+)
+from .sampling import (  # noqa: F401
+    softmax_t,
+    nucleus,
+    kept_cdf,
+    sample as sample_top_p,
 )
