@@ -213,6 +213,8 @@ struct GemmArgs {
     int32_t* dbg_slot;
     int num_sms;
 };
+cudaError_t launch_sample_top_p(cudaStream_t st, int B, int V, const float* logits, size_t ld, float inv_t,
+                                unsigned long long tp_fix, const float* uniform, int32_t* next);
 cudaError_t launch_gemm_tc(const LaunchCtx& c, int epi, const GemmArgs& a);
 bool gemm_tc_encode_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                         uint32_t box_rows);

@@ -457,6 +457,22 @@ extern "C" qw_status qw_debug_set_attn(qw_model* m, void* dev_attn) {
     return QW_OK;
 }
 
+extern "C" qw_status qw_sample_top_p(int B, int vocab, const float* dev_logits, size_t ld, float temperature,
+                                     float top_p, const float* dev_uniform, int32_t* dev_next_ids, void* stream) {
+    if (B < 1 || B > 65535) return fail(QW_ERR_INVALID_ARG, "B out of range");
+    if (vocab < 1 || ld < (size_t)vocab) return fail(QW_ERR_INVALID_ARG, "vocab < 1 or ld < vocab");
+    if (!dev_logits || !dev_next_ids) return fail(QW_ERR_INVALID_ARG, "NULL buffer");
+    if (!std::isfinite(temperature) || temperature < 0.f) return fail(QW_ERR_INVALID_ARG, "bad temperature");
+    if (temperature > 0.f && !dev_uniform) return fail(QW_ERR_INVALID_ARG, "NULL uniforms");
+    if (!std::isfinite(top_p) || !(top_p > 0.f) || top_p > 1.f) return fail(QW_ERR_INVALID_ARG, "top_p outside (0, 1]");
+    // probabilities are summed as integers of 2^-40 (see k_sample.cu)
+    const unsigned long long tp_fix = (unsigned long long)std::llround((double)top_p * 1099511627776.0);
+    const float inv_t = temperature > 0.f ? 1.f / temperature : 0.f;
+    CUDA_TRY(launch_sample_top_p((cudaStream_t)stream, B, vocab, dev_logits, ld, inv_t, tp_fix, dev_uniform,
+                                 dev_next_ids));
+    return QW_OK;
+}
+
 extern "C" int qw_last_launch_count(const qw_model* m) { return m ? m->last_launches : 0; }
 
 extern "C" qw_status qw_trace_set(qw_model* m, unsigned long long* dev_buf, int per_cta) {

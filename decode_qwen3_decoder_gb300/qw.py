@@ -73,6 +73,7 @@ SIGNATURES = {
     "qw_free_model": (None, [_VP]),
     "qw_free_kv": (None, [_VP]),
     "qw_debug_set": (_I, [_VP, _VP, _VP, _VP]),
+    "qw_sample_top_p": (_I, [_I, _I, _VP, _SZ, ctypes.c_float, ctypes.c_float, _VP, _VP, _VP]),
     "qw_debug_set_attn": (_I, [_VP, _VP]),
     "qw_kv_page_table": (_I, [_VP, _I, _P(ctypes.c_int32), _I]),
     "qw_kv_pool_ptrs": (_I, [_VP, _P(_VP), _P(_VP), _P(_I)]),
@@ -210,6 +211,12 @@ def qw_debug_set(model: int, hidden_ptr: int, pos_ptr: int, slot_ptr: int) -> No
 
 def qw_debug_set_attn(model: int, attn_ptr: int) -> None:
     _check(load().qw_debug_set_attn(model, attn_ptr or None))
+
+
+def qw_sample_top_p(B: int, vocab: int, logits_ptr: int, ld: int, temperature: float, top_p: float,
+                    uniform_ptr: int, next_ptr: int, stream=None) -> None:
+    _check(load().qw_sample_top_p(B, vocab, logits_ptr, ld, temperature, top_p, uniform_ptr or None, next_ptr,
+                                  _stream(stream)))
 
 
 def qw_kv_page_table(kv: int, seq_id: int, max_pages: int = 1 << 16):

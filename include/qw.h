@@ -258,6 +258,25 @@ int qw_persistent_grid(const qw_model* m);
  * graph captured while they are set; kind QW_PROF_OFF (or events NULL) turns it off. */
 qw_status qw_profile_set(qw_model* m, int kind, void* const* events, int n_events);
 
+/* ---- Sampling (Paso 8) ------------------------------------------------------------------ */
+
+/* Temperature + top-p sampling of B rows of logits, one token per row: row b is
+ * dev_logits[b * ld + v], v < vocab (fp32; e.g. the logits a prefill or decode call wrote),
+ * and its token goes to dev_next_ids[b].
+ * temperature == 0: greedy argmax, lowest index on ties (dev_uniform may be NULL).
+ * temperature > 0: p = softmax(logits / temperature); the nucleus is the shortest prefix of
+ * the probabilities in descending order (equal values by ascending token id) whose running
+ * sum reaches top_p, i.e. one more token than the running sums below top_p; the token is
+ * drawn by inverse CDF from dev_uniform[b] in [0, 1) (values outside are clamped): the kept
+ * tokens are enumerated by ascending token id and the first whose running kept probability
+ * exceeds u times the kept total is chosen. The running sums are exact sums of the fp32
+ * probabilities rounded to multiples of 2^-40, so the result is deterministic.
+ * Asynchronous on `stream`; every buffer belongs to the caller; one cluster of 8 CTAs per
+ * row. Errors (nothing enqueued): QW_ERR_INVALID_ARG for B outside [1, 65535], vocab < 1,
+ * ld < vocab, a NULL buffer, a negative or non-finite temperature, top_p outside (0, 1]. */
+qw_status qw_sample_top_p(int B, int vocab, const float* dev_logits, size_t ld, float temperature, float top_p,
+                          const float* dev_uniform, int32_t* dev_next_ids, void* stream);
+
 /* ---- For callers that cannot allocate device memory ---------------------------------- */
 
 /* The page has no counterpart to this entry point; it serves callers that must not call
