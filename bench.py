@@ -370,9 +370,38 @@ def run_ours(args, cfg, rank, world):
                 "d2h_bytes_per_step": B * (ND + 1) * 4},
         "gpu_launches": gpu_launches,
         "clocks": clk.summary(),
+        "sampling": time_sampling(qw, s.vocab, st),
     }
     eng.close()
     return out
+
+
+def time_sampling(qw, vocab: int, st, reps: int = 20):
+    """qw_sample_top_p (temperature 0.7, top_p 0.9) on B rows of seeded N(0, 2) logits, for
+    B = 1 and 64: microseconds per call (CUDA events on the launching stream, after 3 warm-up
+    calls) and the rate at which the logits are read once (B * vocab * 4 bytes per call)."""
+    import torch
+    res = {}
+    g = torch.Generator(device="cuda")
+    g.manual_seed(1234)
+    for B in (1, 64):
+        lg = torch.randn((B, vocab), device="cuda", generator=g) * 2.0
+        u = torch.rand(B, device="cuda", generator=g)
+        nx = torch.empty(B, dtype=torch.int32, device="cuda")
+        call = lambda: qw.qw_sample_top_p(B, vocab, lg.data_ptr(), vocab, 0.7, 0.9, u.data_ptr(), nx.data_ptr(), st)
+        for _ in range(3):
+            call()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        st.synchronize()
+        e0.record(st)
+        for _ in range(reps):
+            call()
+        e1.record(st)
+        st.synchronize()
+        us = e0.elapsed_time(e1) * 1e3 / reps
+        res[f"B{B}"] = {"us_per_call": round(us, 2), "logits_GB/s": round(B * vocab * 4 / (us * 1e-6) / 1e9, 1)}
+    res["note"] = "temperature 0.7, top_p 0.9; one cluster of 8 CTAs per row, latency-bound"
+    return res
 
 
 def attn_bytes_layer(s, ctx_total: float) -> float:

@@ -7,24 +7,29 @@
 // argmax (lowest index on ties).
 //
 // k_sample_top_p: one cluster of 8 CTAs (1024 threads each) per row of logits; CTA r owns a
-// contiguous eighth of the vocabulary. Nothing is sorted: the k-th largest probability that
-// closes the nucleus is found by a radix select over the fp32 bit patterns of p (three
-// digits of 10 bits; p >= 0, so the bit patterns order like the values): per digit, each CTA
-// builds a histogram of counts and probability sums over its slice, the eight histograms are
-// summed through distributed shared memory, and a suffix scan over the digits finds the one
-// where the running sum from the top reaches top_p. Every probability sum is taken in fixed
-// point (p * 2^40 rounded to an integer), so the sums, the nucleus and the drawn token do not
-// depend on the order of the atomic additions: the result is deterministic.
+// contiguous eighth of the vocabulary and keeps the bit patterns of its probabilities in
+// shared memory (p >= 0, so the bit patterns order like the values). Nothing is sorted: the
+// probability that closes the nucleus is found by a radix select over those bit patterns
+// (digits of 8, 8, 8 and 6 bits): per digit, each CTA sums the probabilities of its slice
+// into lane-private histograms (no two lanes of a warp touch the same address), the eight
+// CTAs' histograms are added through distributed shared memory, and a suffix scan over the
+// digits finds the one where the running sum from the top reaches top_p. Every probability
+// sum is taken in fixed point (p * 2^40 rounded to an integer), so the sums, the nucleus and
+// the drawn token do not depend on the order of the atomic additions: the result is
+// deterministic.
 #include <cstdint>
 
 #include "qw_internal.h"
 
 namespace {
 
-constexpr int SP_CL = 8;           // CTAs per row (cluster)
-constexpr int SP_T = 1024;         // threads per CTA
-constexpr int SP_BINS = 1024;      // one radix digit (10 bits)
-constexpr float SP_FIX = 1099511627776.0f;  // 2^40: fixed-point scale of probabilities
+constexpr int SP_CL = 8;                     // CTAs per row (cluster)
+constexpr int SP_T = 1024;                   // threads per CTA
+constexpr int SP_BINS = 256;                 // histogram bins (digits of up to 8 bits)
+constexpr int SP_HP = SP_BINS + 1;           // padded pitch of a lane's histogram (bank spread)
+constexpr int SP_MAX_SLICE = 24576;          // vocabulary entries per CTA held in shared memory
+constexpr float SP_FIX = 1099511627776.0f;   // 2^40: fixed-point scale of probabilities
+constexpr int SP_SMEM = SP_MAX_SLICE * 4 + 32 * SP_HP * 8 + 2 * SP_BINS * 8;
 
 __device__ __forceinline__ uint32_t sp_rank() {
     uint32_t r;
@@ -60,14 +65,8 @@ struct SampleP {
     int32_t* next;                // [B]
 };
 
-// One element: its probability's bit pattern (the sort key) and fixed-point value.
-struct Elem {
-    uint32_t key;
-    unsigned long long q;
-};
-__device__ __forceinline__ Elem sp_elem(float l, float m, float inv_t, float inv_z) {
-    const float p = expf((l - m) * inv_t) * inv_z;
-    return {__float_as_uint(p), __float2ull_rn(p * SP_FIX)};
+__device__ __forceinline__ unsigned long long sp_fix(uint32_t key) {
+    return __float2ull_rn(__uint_as_float(key) * SP_FIX);
 }
 
 // Block-wide inclusive scan of one u64 per thread (1024 threads); `ws` holds 32 entries.
@@ -106,35 +105,25 @@ __device__ __forceinline__ unsigned long long sp_sum(unsigned long long v, unsig
     return r;
 }
 
-// Add (count 1, q) to digit d of the histogram for every lane with valid d; lanes of a warp
-// with the same digit are combined first (one pair of shared atomics per distinct digit).
-__device__ __forceinline__ void sp_hist_add(uint32_t d, unsigned long long q, uint32_t* cnt,
-                                            unsigned long long* sum) {
-    const unsigned peers = __match_any_sync(0xffffffffu, d);
-    const uint32_t hi = (uint32_t)(q >> 20), lo = (uint32_t)(q & 0xFFFFFu);
-    const uint32_t hs = __reduce_add_sync(peers, hi), ls = __reduce_add_sync(peers, lo);
-    const int lane = threadIdx.x & 31;
-    if (d < SP_BINS && lane == __ffs(peers) - 1) {
-        atomicAdd(cnt + d, (uint32_t)__popc(peers));
-        atomicAdd(sum + d, ((unsigned long long)hs << 20) + ls);
-    }
-}
-
 }  // namespace
 
+
+// Keys are the fp32 bit patterns of probabilities in [0, 1]: 30 significant bits, taken as
+// digits of 8, 8, 8 and 6 bits (shifts 22, 14, 6, 0).
 __global__ void __launch_bounds__(SP_T, 1) k_sample_top_p(const __grid_constant__ SampleP p) {
-    __shared__ uint32_t hcnt[2][SP_BINS];            // digit histograms (two: a level is written
-    __shared__ unsigned long long hsum[2][SP_BINS];  // while the previous may still be read)
+    extern __shared__ __align__(16) uint8_t sp_smem[];
+    uint32_t* keys = reinterpret_cast<uint32_t*>(sp_smem);                                 // [slice]
+    unsigned long long* hist = reinterpret_cast<unsigned long long*>(sp_smem + SP_MAX_SLICE * 4);  // [32][SP_HP]
+    unsigned long long* msum = hist + 32 * SP_HP;  // [2][SP_BINS] this CTA's histogram (two levels deep)
     __shared__ unsigned long long ws[32];
-    __shared__ unsigned long long pub64[3];          // published per-CTA totals (Z, ties, kept)
-    __shared__ float pub_m;                          // published CTA max and its lowest index
+    __shared__ unsigned long long pub64[3];  // published per-CTA totals (Z, ties, kept)
+    __shared__ float pub_m;                  // published CTA max and its lowest index
     __shared__ int pub_i;
     __shared__ float wm[32];
     __shared__ int wi[32];
     __shared__ float s_m, s_inv_z;
     __shared__ int s_mi, s_digit, s_keep_all;
-    __shared__ uint32_t s_cnt;
-    __shared__ unsigned long long s_g, s_off;
+    __shared__ unsigned long long s_g, s_off, s_ties;
 
     const int rank = (int)sp_rank(), b = blockIdx.y, tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
     const int slice = (p.V + SP_CL - 1) / SP_CL;
@@ -182,9 +171,14 @@ __global__ void __launch_bounds__(SP_T, 1) k_sample_top_p(const __grid_constant_
         return;
     }
 
-    // ---- 2. softmax normaliser, in fixed point ----------------------------------------
+    // ---- 2. exp((l - max) / T) into shared memory; the normaliser in fixed point ------
+    float* ev = reinterpret_cast<float*>(keys);
     unsigned long long z = 0;
-    for (int i = lo + tid; i < hi; i += SP_T) z += __float2ull_rn(expf((row[i] - M) * p.inv_t) * SP_FIX);
+    for (int j = tid; j < n; j += SP_T) {
+        const float e = expf((row[lo + j] - M) * p.inv_t);
+        ev[j] = e;
+        z += __float2ull_rn(e * SP_FIX);
+    }
     z = sp_sum(z, ws);
     if (tid == 0) pub64[0] = z;
     sp_cluster_sync();
@@ -195,105 +189,98 @@ __global__ void __launch_bounds__(SP_T, 1) k_sample_top_p(const __grid_constant_
     }
     __syncthreads();
     const float inv_z = s_inv_z;
+    for (int j = tid; j < n; j += SP_T) keys[j] = __float_as_uint(ev[j] * inv_z);
+    __syncthreads();
 
     // ---- 3. radix select of the probability that closes the nucleus --------------------
-    // After level l, `prefix` holds the top 10 (l + 1) bits of that probability's key and G
-    // the fixed-point sum of all probabilities with a larger key.
-    uint32_t prefix = 0, tie_cnt = 0;
+    // After a level, `prefix` holds the key bits fixed so far and G the fixed-point sum of
+    // every probability with a larger key.
+    uint32_t prefix = 0;
     unsigned long long G = 0;
     bool keep_all = false;
-    for (int level = 0; level < 3 && !keep_all; ++level) {
-        const int shift = 20 - 10 * level;
-        uint32_t* cnt = hcnt[level & 1];
-        unsigned long long* sum = hsum[level & 1];
-        cnt[tid] = 0;
-        sum[tid] = 0;
+    for (int level = 0; level < 4 && !keep_all; ++level) {
+        const int bits = level == 3 ? 6 : 8, shift = level == 3 ? 0 : 22 - 8 * level, above = shift + bits;
+        const uint32_t mask = (1u << bits) - 1u;
+        for (int i = tid; i < 32 * SP_HP; i += SP_T) hist[i] = 0;
         __syncthreads();
-        for (int base = 0; base < n; base += SP_T) {  // the same trip count in every warp
-            uint32_t d = 0xFFFFFFFFu;
-            unsigned long long q = 0;
-            if (base + tid < n) {
-                const Elem e = sp_elem(row[lo + base + tid], M, p.inv_t, inv_z);
-                if (level == 0 || (e.key >> (shift + 10)) == prefix) {
-                    d = (e.key >> shift) & (SP_BINS - 1);
-                    q = e.q;
-                }
-            }
-            sp_hist_add(d, q, cnt, sum);
+        unsigned long long* mine = hist + lane * SP_HP;  // lane-private: no two lanes of a warp collide
+        for (int j = tid; j < n; j += SP_T) {
+            const uint32_t k = keys[j];
+            if (level == 0 || (k >> above) == prefix) atomicAdd(mine + ((k >> shift) & mask), sp_fix(k));
+        }
+        __syncthreads();
+        unsigned long long* ms = msum + (level & 1) * SP_BINS;
+        if (tid < SP_BINS) {
+            unsigned long long t = 0;
+            for (int l = 0; l < 32; ++l) t += hist[l * SP_HP + tid];
+            ms[tid] = t;
         }
         sp_cluster_sync();
-        // thread t holds digit 1023 - t of the merged histogram: an inclusive scan gives the
-        // sum over this digit and every larger one
+        // thread t < 256 holds digit 255 - t of the cluster's histogram; the inclusive scan
+        // gives the sum over that digit and every larger one
         const int dr = SP_BINS - 1 - tid;
-        uint32_t c = 0;
         unsigned long long s = 0;
-        for (int r = 0; r < SP_CL; ++r) {
-            c += sp_ld32(cnt + dr, r);
-            s += sp_ld64(sum + dr, r);
-        }
+        if (tid < SP_BINS)
+            for (int r = 0; r < SP_CL; ++r) s += sp_ld64(ms + dr, r);
         const unsigned long long incl = sp_scan_incl(s, ws);
         if (tid == 0) s_keep_all = 0;
         __syncthreads();
-        if (tid == SP_T - 1 && G + incl < p.tp_fix) s_keep_all = 1;  // rounding kept every sum below top_p
-        if (G + incl >= p.tp_fix && G + incl - s < p.tp_fix) {
+        if (tid == SP_T - 1 && G + incl < p.tp_fix) {  // rounding kept every running sum below top_p
+            s_keep_all = 1;
+            s_g = G + incl;
+        }
+        if (tid < SP_BINS && G + incl >= p.tp_fix && G + incl - s < p.tp_fix) {
             s_digit = dr;
             s_g = G + incl - s;
-            s_cnt = c;
         }
         __syncthreads();
         keep_all = s_keep_all != 0;
-        if (!keep_all) {
-            prefix = (prefix << 10) | (uint32_t)s_digit;
-            G = s_g;
-            tie_cnt = s_cnt;
-        } else {
-            G = G + incl;  // (thread 1023's value is the total; broadcast below)
-        }
+        G = s_g;
+        if (!keep_all) prefix = (prefix << bits) | (uint32_t)s_digit;
         __syncthreads();
     }
 
-    // ---- 4. the kept set and its total -------------------------------------------------
-    uint32_t tstar;
-    unsigned long long keep_ties, S;
-    if (!keep_all) {
-        tstar = prefix;
-        const unsigned long long qt = __float2ull_rn(__uint_as_float(tstar) * SP_FIX);
-        keep_ties = qt == 0 ? tie_cnt : min((unsigned long long)tie_cnt, (p.tp_fix - G + qt - 1) / qt);
-        S = G + keep_ties * qt;
-    } else {
-        if (tid == SP_T - 1) s_g = G;
-        __syncthreads();
-        S = s_g;
-        tstar = 0;
-        keep_ties = ~0ull;
-    }
-
-    // ---- 5. inverse-CDF draw over the kept tokens by ascending id ----------------------
-    const float uf = fminf(fmaxf(p.uniform[b], 0.f), 0.99999994f);
-    const unsigned long long R = min(S - 1, (unsigned long long)((double)uf * (double)S));
-    const int cw = (n + SP_T - 1) / SP_T;
-    const int c0 = lo + min(n, tid * cw), c1 = lo + min(n, tid * cw + cw);
-    // ties below this thread's ids, cluster-wide (the nucleus keeps the lowest ids among them)
+    // ---- 4. ties at the closing value (the nucleus keeps the lowest ids among them) ----
+    const uint32_t tstar = keep_all ? 0u : prefix;
+    const int cw = (n + SP_T - 1) / SP_T, j0 = min(n, tid * cw), j1 = min(n, j0 + cw);
     unsigned long long tl = 0;
-    for (int i = c0; i < c1; ++i) tl += sp_elem(row[i], M, p.inv_t, inv_z).key == tstar;
+    for (int j = j0; j < j1; ++j) tl += keys[j] == tstar;
     const unsigned long long tincl = sp_scan_incl(tl, ws);
     if (tid == SP_T - 1) pub64[1] = tincl;
     sp_cluster_sync();
     if (tid == 0) {
-        unsigned long long off = 0;
-        for (int r = 0; r < rank; ++r) off += sp_ld64(&pub64[1], r);
+        unsigned long long off = 0, all = 0;
+        for (int r = 0; r < SP_CL; ++r) {
+            const unsigned long long v = sp_ld64(&pub64[1], r);
+            if (r < rank) off += v;
+            all += v;
+        }
         s_off = off;
+        s_ties = all;
     }
     __syncthreads();
     const unsigned long long tie0 = s_off + tincl - tl;
+    unsigned long long keep_ties, S;
+    if (!keep_all) {
+        const unsigned long long qt = sp_fix(tstar), c = s_ties;
+        keep_ties = qt == 0 ? c : min(c, (p.tp_fix - G + qt - 1) / qt);
+        S = G + keep_ties * qt;
+    } else {
+        keep_ties = ~0ull;
+        S = G;  // every token is kept: G is the total
+    }
     __syncthreads();
+
+    // ---- 5. inverse-CDF draw over the kept tokens by ascending id ----------------------
+    const float uf = fminf(fmaxf(p.uniform[b], 0.f), 0.99999994f);
+    const unsigned long long R = min(S - 1, (unsigned long long)((double)uf * (double)S));
     unsigned long long ks = 0, tr = tie0;
-    for (int i = c0; i < c1; ++i) {
-        const Elem e = sp_elem(row[i], M, p.inv_t, inv_z);
-        if (e.key > tstar) {
-            ks += e.q;
-        } else if (e.key == tstar) {
-            if (tr < keep_ties) ks += e.q;
+    for (int j = j0; j < j1; ++j) {
+        const uint32_t k = keys[j];
+        if (k > tstar) {
+            ks += sp_fix(k);
+        } else if (k == tstar) {
+            if (tr < keep_ties) ks += sp_fix(k);
             ++tr;
         }
     }
@@ -310,17 +297,17 @@ __global__ void __launch_bounds__(SP_T, 1) k_sample_top_p(const __grid_constant_
     if (R >= base && R < base + ks) {  // exactly one thread of the cluster
         unsigned long long acc = base;
         tr = tie0;
-        for (int i = c0; i < c1; ++i) {
-            const Elem e = sp_elem(row[i], M, p.inv_t, inv_z);
+        for (int j = j0; j < j1; ++j) {
+            const uint32_t k = keys[j];
             unsigned long long wq = 0;
-            if (e.key > tstar) {
-                wq = e.q;
-            } else if (e.key == tstar) {
-                if (tr < keep_ties) wq = e.q;
+            if (k > tstar) {
+                wq = sp_fix(k);
+            } else if (k == tstar) {
+                if (tr < keep_ties) wq = sp_fix(k);
                 ++tr;
             }
             if (R < acc + wq) {
-                p.next[b] = i;
+                p.next[b] = lo + j;
                 break;
             }
             acc += wq;
@@ -329,8 +316,17 @@ __global__ void __launch_bounds__(SP_T, 1) k_sample_top_p(const __grid_constant_
     sp_cluster_sync();  // no CTA leaves while another may read its shared memory
 }
 
+int sample_max_vocab() { return SP_CL * SP_MAX_SLICE; }
+
 cudaError_t launch_sample_top_p(cudaStream_t st, int B, int V, const float* logits, size_t ld, float inv_t,
                                 unsigned long long tp_fix, const float* uniform, int32_t* next) {
+    if (V > SP_CL * SP_MAX_SLICE) return cudaErrorInvalidValue;
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(k_sample_top_p, cudaFuncAttributeMaxDynamicSharedMemorySize, SP_SMEM);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
     SampleP p;
     p.logits = logits;
     p.ld = ld;
@@ -342,7 +338,7 @@ cudaError_t launch_sample_top_p(cudaStream_t st, int B, int V, const float* logi
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(SP_CL, B);
     cfg.blockDim = dim3(SP_T);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = SP_SMEM;
     cfg.stream = st;
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;

@@ -213,6 +213,7 @@ struct GemmArgs {
     int32_t* dbg_slot;
     int num_sms;
 };
+int sample_max_vocab();  // largest vocabulary qw_sample_top_p takes (8 slices in shared memory)
 cudaError_t launch_sample_top_p(cudaStream_t st, int B, int V, const float* logits, size_t ld, float inv_t,
                                 unsigned long long tp_fix, const float* uniform, int32_t* next);
 cudaError_t launch_gemm_tc(const LaunchCtx& c, int epi, const GemmArgs& a);

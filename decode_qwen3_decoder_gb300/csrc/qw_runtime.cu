@@ -461,6 +461,7 @@ extern "C" qw_status qw_sample_top_p(int B, int vocab, const float* dev_logits, 
                                      float top_p, const float* dev_uniform, int32_t* dev_next_ids, void* stream) {
     if (B < 1 || B > 65535) return fail(QW_ERR_INVALID_ARG, "B out of range");
     if (vocab < 1 || ld < (size_t)vocab) return fail(QW_ERR_INVALID_ARG, "vocab < 1 or ld < vocab");
+    if (vocab > sample_max_vocab()) return fail(QW_ERR_INVALID_ARG, "vocab above %d", sample_max_vocab());
     if (!dev_logits || !dev_next_ids) return fail(QW_ERR_INVALID_ARG, "NULL buffer");
     if (!std::isfinite(temperature) || temperature < 0.f) return fail(QW_ERR_INVALID_ARG, "bad temperature");
     if (temperature > 0.f && !dev_uniform) return fail(QW_ERR_INVALID_ARG, "NULL uniforms");

@@ -272,8 +272,9 @@ qw_status qw_profile_set(qw_model* m, int kind, void* const* events, int n_event
  * exceeds u times the kept total is chosen. The running sums are exact sums of the fp32
  * probabilities rounded to multiples of 2^-40, so the result is deterministic.
  * Asynchronous on `stream`; every buffer belongs to the caller; one cluster of 8 CTAs per
- * row. Errors (nothing enqueued): QW_ERR_INVALID_ARG for B outside [1, 65535], vocab < 1,
- * ld < vocab, a NULL buffer, a negative or non-finite temperature, top_p outside (0, 1]. */
+ * row, each CTA holding an eighth of the row in shared memory. Errors (nothing enqueued):
+ * QW_ERR_INVALID_ARG for B outside [1, 65535], vocab outside [1, 196608], ld < vocab, a NULL
+ * buffer, a negative or non-finite temperature, top_p outside (0, 1]. */
 qw_status qw_sample_top_p(int B, int vocab, const float* dev_logits, size_t ld, float temperature, float top_p,
                           const float* dev_uniform, int32_t* dev_next_ids, void* stream);
 
