@@ -947,6 +947,7 @@ struct PrefillTcP {
     const f16* q;     // [T][n_heads][128]
     f16* out;         // [T][n_heads][128]
     const int* page_table;
+    const int* tok_pos;  // [T] position of each token (a sequence's tokens continue its cache)
     int max_pages_per_seq, n_pages, layer, n_heads, n_kv;
     int* status;
     float scale_log2;
@@ -977,8 +978,6 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_attn_prefill_tc(const __grid_
     pdl_launch();
     if (q0 >= len) return;  // uniform over the CTA
     const int base = p.sd.start[b];
-    // causal: keys < min(len, q0 + 64); only the last tile holds keys after some query
-    const int n_kt = (min(len, q0 + FA_BQ) + FA_BK - 1) / FA_BK;
     auto wait = [&](uint64_t* bar, int parity) { return mbar_wait(smem_u32(bar), (uint32_t)parity & 1u, abort_flag); };
 
     if (threadIdx.x == 0) {
@@ -1010,6 +1009,12 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_attn_prefill_tc(const __grid_
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     pdl_wait();  // q and this layer's K/V come from the projection
+    // The call's tokens of this sequence sit at positions L0 .. L0 + len - 1 after a cached
+    // prefix of L0 tokens (0 for a first prompt); the keys are every position < L0 + len, and
+    // query L0 + i sees keys <= L0 + i. This tile's queries need keys < L0 + min(len, q0 + 64).
+    const int L0 = p.tok_pos[base];
+    const int kend = L0 + len;
+    const int n_kt = (L0 + min(len, q0 + FA_BQ) + FA_BK - 1) / FA_BK;
 
     if (warp == 4 || warp == 6) {
         // ---------------- producers: warp 4 streams K, warp 6 streams V ----------------
@@ -1029,7 +1034,7 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_attn_prefill_tc(const __grid_
                     break;
                 }
                 const int k0 = j * FA_BK;
-                const int npg = (min(k0 + FA_BK, len) - k0 + 15) >> 4;
+                const int npg = (min(k0 + FA_BK, kend) - k0 + 15) >> 4;
                 const uint32_t dst = smem_u32(ring + st * FA_KV), bar = smem_u32(full + st);
                 mbar_expect_tx(bar, (uint32_t)npg * 2 * 2048);
                 for (int pg = 0; pg < npg; ++pg) {
@@ -1108,14 +1113,14 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_attn_prefill_tc(const __grid_
     } else {
         // ---------------- softmax / output: thread = row = TMEM lane ----------------
         const int r = threadIdx.x;
-        const int hq = 2 * g + (r >> 6), qpos = q0 + (r & 63);
+        const int hq = 2 * g + (r >> 6), qi = q0 + (r & 63), qpos = L0 + qi;  // index in the call, position
         const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
         // warp-uniform outcome of a bounded wait
         auto wwait = [&](uint64_t* bar, int parity) { return __all_sync(0xffffffffu, wait(bar, parity)); };
         {
             // Q row into the swizzled operand (zeros past the sequence)
-            const bool v = qpos < len;
-            const f16* src = p.q + ((size_t)(base + (v ? qpos : 0)) * p.n_heads + hq) * 128;
+            const bool v = qi < len;
+            const f16* src = p.q + ((size_t)(base + (v ? qi : 0)) * p.n_heads + hq) * 128;
             const uint32_t qd = smem_u32(sm) + r * 128;
 #pragma unroll
             for (int ch = 0; ch < 16; ++ch) cp_async16(qd + (ch >> 3) * FA_QSUB + (((ch & 7) ^ (r & 7)) << 4), src + ch * 8, v);
@@ -1144,11 +1149,11 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_attn_prefill_tc(const __grid_
                 s[i] = __uint_as_float(xa[i]) * p.scale_log2;
                 s[32 + i] = __uint_as_float(xb[i]) * p.scale_log2;
             }
-            const bool last = j == n_kt - 1;
-            if (last) {
+            // mask keys after the query or past the sequence, on the tiles that hold any
+            if (k0 + FA_BK - 1 > L0 + q0 || k0 + FA_BK > kend) {
 #pragma unroll
                 for (int i = 0; i < FA_BK; ++i)
-                    if (k0 + i > qpos || k0 + i >= len) s[i] = -INFINITY;
+                    if (k0 + i > qpos || k0 + i >= kend) s[i] = -INFINITY;
             }
             float mt = s[0];
 #pragma unroll
@@ -1184,7 +1189,7 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_attn_prefill_tc(const __grid_
             l = l * alpha + ls;
             m = mn;
             TMEM_ST32(lane_base + st * FA_BK, h);
-            if (last && k0 + FA_BK > len) {
+            if (j == n_kt - 1 && k0 + FA_BK > kend) {
                 // V rows of keys past the sequence hold stale data; weight 0 must add exactly 0
                 if (!wwait(v_full + st, j >> 1)) {
                     tmem_wait_st();
@@ -1192,7 +1197,7 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_attn_prefill_tc(const __grid_
                     break;
                 }
                 uint8_t* vs = sm + FA_OFF_V + st * FA_KV;
-                const int kv0 = len - k0;  // first row past the sequence
+                const int kv0 = kend - k0;  // first row past the sequence
                 for (int e = lane; e < 16 * 16; e += 32) {
                     const int row = warp * 16 + (e >> 4), ch = e & 15;
                     if (row >= kv0)
@@ -1210,13 +1215,13 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_attn_prefill_tc(const __grid_
         if (good && wwait(pv_done + ((n_kt - 1) & 1), (n_kt - 1) >> 1)) {
             tc_fence_after();
             const float inv = 1.f / l;
-            f16* orow = p.out + ((size_t)(base + qpos) * p.n_heads + hq) * 128;
+            f16* orow = p.out + ((size_t)(base + qi) * p.n_heads + hq) * 128;
 #pragma unroll 1
             for (int c = 0; c < 4; ++c) {
                 uint32_t x[32];
                 TMEM_LD32(lane_base + FA_O + c * 32, x);
                 tmem_wait_ld();
-                if (qpos < len) {
+                if (qi < len) {
                     uint32_t h[16];
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
@@ -1239,7 +1244,7 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_attn_prefill_tc(const __grid_
     }
 }
 
-cudaError_t launch_attn_prefill_tc(const LaunchCtx& c, const StepDesc& sd, int max_len, int layer, const f16* q,
+cudaError_t launch_attn_prefill_tc(const LaunchCtx& c, const StepDesc& sd, const int* tok_pos, int layer, const f16* q,
                                    KVView kv, const CUtensorMap* tmK, const CUtensorMap* tmV, int n_heads, int n_kv,
                                    f16* out, int* status) {
     PrefillTcP p;
@@ -1250,6 +1255,7 @@ cudaError_t launch_attn_prefill_tc(const LaunchCtx& c, const StepDesc& sd, int m
     p.q = q;
     p.out = out;
     p.page_table = kv.page_table;
+    p.tok_pos = tok_pos;
     p.max_pages_per_seq = kv.max_pages_per_seq;
     p.n_pages = kv.n_pages;
     p.layer = layer;
@@ -1263,6 +1269,8 @@ cudaError_t launch_attn_prefill_tc(const LaunchCtx& c, const StepDesc& sd, int m
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
+    int max_len = 1;
+    for (int b = 0; b < sd.B; ++b) max_len = std::max(max_len, sd.start[b + 1] - sd.start[b]);
     const int qtiles = (max_len + FA_BQ - 1) / FA_BQ;
     return launch_k(c, k_attn_prefill_tc, dim3(qtiles, n_kv, sd.B), dim3(FA_THREADS), (size_t)FA_SMEM, p);
 }

@@ -162,7 +162,7 @@ cudaError_t launch_attn_decode(const LaunchCtx& c, int T, int layer, const f16* 
 // the paged cache.
 // Causal flash attention of a prefill on tcgen05 (S and O in TMEM), K/V from the cache pages
 // through the pools' tensor maps.
-cudaError_t launch_attn_prefill_tc(const LaunchCtx& c, const StepDesc& sd, int max_len, int layer, const f16* q,
+cudaError_t launch_attn_prefill_tc(const LaunchCtx& c, const StepDesc& sd, const int* tok_pos, int layer, const f16* q,
                                    KVView kv, const CUtensorMap* tmK, const CUtensorMap* tmV, int n_heads, int n_kv,
                                    f16* out, int* status);
 // bf16 gate/up [inter][K] -> fp16 rows interleaved per 64: [gate 64b..64b+63][up 64b..64b+63]...

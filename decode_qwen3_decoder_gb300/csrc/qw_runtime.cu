@@ -828,7 +828,7 @@ static qw_status run_layers(qw_model* m, qw_kv* kv, const StepDesc& sd, bool pre
             // q, k, v were normalised, rotated and appended by the projection's epilogue
             PROF(QW_PROF_ATTN);
             if (prefill)
-                LAUNCH(launch_attn_prefill_tc(lc, sd, max_keys, l, q, kvv, &kv->tm_k, &kv->tm_v, c.n_heads,
+                LAUNCH(launch_attn_prefill_tc(lc, sd, m->tok_pos, l, q, kvv, &kv->tm_k, &kv->tm_v, c.n_heads,
                                               c.n_kv_heads, attn, m->status));
             else if (max_keys <= kShortCacheKeys)  // light per-pair kernel: overlaps the other half's GEMMs
                 LAUNCH(launch_attn_paged(lc, T, l, q, c.n_heads, c.n_kv_heads, tv, kvv, sp.chunk, sp.n_splits,
@@ -1008,24 +1008,25 @@ extern "C" qw_status qw_prefill(qw_model* m, qw_kv* kv, int B, const int* seq_id
     StepDesc sd = {};
     sd.B = B;
     long long total = 0;
-    int max_len = 0;
+    int max_keys = 0;
     for (int b = 0; b < B; ++b) {
         const int s = seq_ids[b];
         if (lens[b] < 1) return fail(QW_ERR_INVALID_ARG, "lens[%d] = %d < 1", b, lens[b]);
-        if (kv->len[s] != 0) return fail(QW_ERR_BAD_STATE, "prefill into non-empty sequence %d", s);
-        if (lens[b] > m->cfg.max_context) return fail(QW_ERR_INVALID_ARG, "prompt longer than max_context");
-        if ((long long)kv->pt[s].size() * 16 < lens[b])
-            return fail(QW_ERR_KV_FULL, "sequence %d reserved for %zu tokens < %d", s, kv->pt[s].size() * 16, lens[b]);
+        // the prompt continues the sequence's cache (chunked prefill): positions kv->len[s] ..
+        const long long keys = (long long)kv->len[s] + lens[b];
+        if (keys > m->cfg.max_context) return fail(QW_ERR_INVALID_ARG, "cache + prompt longer than max_context");
+        if ((long long)kv->pt[s].size() * 16 < keys)
+            return fail(QW_ERR_KV_FULL, "sequence %d reserved for %zu tokens < %lld", s, kv->pt[s].size() * 16, keys);
         sd.seq[b] = s;
         sd.start[b] = (int)total;
         total += lens[b];
-        max_len = std::max(max_len, lens[b]);
+        max_keys = std::max(max_keys, (int)keys);
     }
     if (total > m->cfg.max_tokens) return fail(QW_ERR_INVALID_ARG, "%lld tokens > max_tokens", total);
     sd.start[B] = (int)total;
     sd.T = (int)total;
     int launches = 0;
-    QW_TRY(run_step(m, kv, sd, true, max_len, dev_token_ids, dev_logits, dev_next_ids, (cudaStream_t)stream_,
+    QW_TRY(run_step(m, kv, sd, true, max_keys, dev_token_ids, dev_logits, dev_next_ids, (cudaStream_t)stream_,
                     true, &launches));
     m->last_launches = launches;
     for (int b = 0; b < B; ++b) kv->len[seq_ids[b]] += lens[b];

@@ -138,12 +138,15 @@ qw_status qw_kv_truncate(qw_kv* kv, int seq_id, int n_tokens, void* stream);
 int qw_kv_free_pages(const qw_kv* kv);
 int qw_kv_length(const qw_kv* kv, int seq_id); /* host mirror of the device length */
 
-/* Prefill (Paso 9, first forward): run B empty sequences' prompts through the model.
- * seq_ids[B], lens[B] (host): sequence ids and prompt lengths (each >= 1, each sequence
- * empty and reserved for at least lens[b] tokens). dev_token_ids: the prompts
- * concatenated, sum(lens) int32. dev_logits: [B, vocab] fp32 logits of each prompt's last
- * position, or NULL. dev_next_ids: [B] int32 greedy picks (argmax, lowest index on ties).
- * Appends every prompt token's K/V to the cache and advances the lengths. */
+/* Prefill (Paso 9, first forward): run B sequences' prompts through the model. A prompt
+ * continues its sequence's cache (chunked prefill): its tokens take positions len .. len +
+ * lens[b] - 1 after the sequence's current length len (0 for a first prompt) and attend to the
+ * cached prefix and to the earlier prompt tokens (causal by position).
+ * seq_ids[B], lens[B] (host): sequence ids and prompt lengths (each >= 1; each sequence
+ * reserved for at least len + lens[b] tokens, at most max_context). dev_token_ids: the
+ * prompts concatenated, sum(lens) int32. dev_logits: [B, vocab] fp32 logits of each prompt's
+ * last position, or NULL. dev_next_ids: [B] int32 greedy picks (argmax, lowest index on
+ * ties). Appends every prompt token's K/V to the cache and advances the lengths. */
 qw_status qw_prefill(qw_model* m, qw_kv* kv, int B, const int* seq_ids, const int* lens,
                      const int32_t* dev_token_ids, float* dev_logits, int32_t* dev_next_ids,
                      void* stream);

@@ -195,3 +195,76 @@ def test_prefill_attention_peaky(qw, lens):
             row += len(p)
     finally:
         eng.close()
+
+
+def _chunked_run(om, run, plan, s, taps_check=None):
+    """plan: list of calls, each a list of (seq, n_tokens). Every call's hidden states, last
+    logits, positions and slots against the oracle continuing each sequence's own cache."""
+    caches, fed = {}, {}
+    mirror = oracle.PagedKVMirror(run.qw.qw_kv_pool_ptrs(run.eng.kv)[2], 16, 16)
+    total = {}
+    for call in plan:
+        for sq, n in call:
+            total[sq] = total.get(sq, 0) + n
+    run.qw.qw_kv_reset(run.eng.kv, -1, run.eng.stream)
+    for sq in sorted(total):
+        run.qw.qw_kv_reserve(run.eng.kv, sq, total[sq], run.eng.stream)
+        mirror.reserve(sq, total[sq])
+    for ci, call in enumerate(plan):
+        seqs = [sq for sq, _ in call]
+        prompts = [synth.make_tokens(s.vocab, n, 3000 + 31 * ci + sq).tolist() for sq, n in call]
+        T = sum(len(p) for p in prompts)
+        attn = None
+        if taps_check is not None:
+            import torch
+            attn = torch.zeros((s.n_layers, T, s.n_heads * s.head_dim), dtype=torch.float16, device="cuda")
+            run.qw.qw_debug_set_attn(run.eng.model, attn.data_ptr())
+        try:
+            g = run.prefill(seqs, prompts, reserve=False)
+        finally:
+            if attn is not None:
+                run.qw.qw_debug_set_attn(run.eng.model, 0)
+        assert g["status"] == 0
+        row = 0
+        for b, (sq, p) in enumerate(zip(seqs, prompts)):
+            c = caches.setdefault(sq, oracle.SeqCache(s.n_layers))
+            start = fed.get(sq, 0)
+            np.testing.assert_array_equal(g["pos"][row:row + len(p)], np.arange(start, start + len(p)))
+            np.testing.assert_array_equal(g["slot"][row:row + len(p)], mirror.slots(sq, range(start, start + len(p))))
+            taps = {}
+            o = oracle.forward(om, p, c, taps=taps)
+            check_hidden(g["hidden"][:, row:row + len(p)], o["hidden"])
+            check_logits(g["logits"][b], o["logits"])
+            check_token(g["next"][b], o["logits"])
+            if taps_check is not None:
+                taps_check(attn.float().cpu().numpy()[0, row:row + len(p)], taps["attn"][0], (ci, sq))
+            fed[sq] = start + len(p)
+            row += len(p)
+
+
+def test_chunked_prefill_tensor_core_path(blk):
+    """Prompts fed in chunks that continue each sequence's cache (positions after the cached
+    prefix, attention over it): chunks of several sequences share calls, start and end
+    mid-page and mid-tile, and one call is small enough for the small-batch path."""
+    run, om = blk
+    plan = [[(0, 300), (1, 77)], [(0, 200), (1, 50), (2, 9)], [(1, 129), (2, 140)], [(2, 5), (0, 3)]]
+    _chunked_run(om, run, plan, S1)
+
+
+def test_chunked_prefill_peaked_attention(qw):
+    """The same with sharply peaked attention (QK-norm weights 2.0): every token's attention
+    output over the cached prefix within 2e-2 of the oracle's."""
+    w = _PeakyQK(weights(S1))
+    om = oracle.Model(w)
+    eng = qw.qw.Engine(S1, dict(w.named()), max_tokens=1024, max_batch=8, max_context=1024, kv_pages=256,
+                       max_seqs=8)
+
+    def check(got, want, where):
+        err = np.linalg.norm(got - want, axis=1) / np.linalg.norm(want, axis=1)
+        assert err.max() <= ATTN_REL, f"{where}: token {int(np.argmax(err))}: {err.max():.3e}"
+
+    try:
+        plan = [[(0, 333), (1, 64)], [(0, 420), (1, 191)], [(1, 17)]]
+        _chunked_run(om, Run(qw, eng), plan, S1, taps_check=check)
+    finally:
+        eng.close()

@@ -165,13 +165,17 @@ def test_error_paths_leave_state(one_block):
         run.prefill([1], [[1] * 20], debug=False, reserve=False)
     assert e.value.status == -2
     assert qw.qw_kv_length(eng.kv, 1) == 0
-    # prefill into a non-empty sequence
+    # a prompt continues a non-empty sequence (chunked prefill) within its reservation only
     g = run.prefill([1], [[1, 2, 3]], debug=False)
     assert g["status"] == 0
+    g = run.prefill([1], [[4]], debug=False, reserve=False)
+    assert g["status"] == 0
+    assert qw.qw_kv_length(eng.kv, 1) == 4
+    pages = len(qw.qw_kv_page_table(eng.kv, 1))
     with pytest.raises(qw.QwError) as e:
-        run.prefill([1], [[4]], debug=False, reserve=False)
-    assert e.value.status == -3
-    assert qw.qw_kv_length(eng.kv, 1) == 3
+        run.prefill([1], [[5] * (16 * pages - 3)], debug=False, reserve=False)
+    assert e.value.status == -2
+    assert qw.qw_kv_length(eng.kv, 1) == 4
     # a token id outside the vocabulary is reported through the status word
     qw.qw_kv_reserve(eng.kv, 4, 8, eng.stream)
     g = run.prefill([4], [[5, synth.ONE_BLOCK.vocab + 3]], debug=False, check=False)
