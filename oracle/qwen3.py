@@ -279,11 +279,13 @@ def forward(model: Model, ids: Sequence[int], cache: SeqCache, all_logits: bool 
 
 
 def generate(model: Model, prompt: Sequence[int], n_decode: int, cache: Optional[SeqCache] = None,
-             keep_hidden: bool = True) -> dict:
-    """Paso 9 at temperature 0: prefill the prompt, then ``n_decode`` single-token steps,
-    each fed the previous greedy pick. No EOS stop (the page never gives EOS_ID).
+             keep_hidden: bool = True, eos_id: Optional[int] = None) -> dict:
+    """Paso 9 at temperature 0: prefill the prompt, then up to ``n_decode`` single-token
+    steps, each fed the previous greedy pick. With ``eos_id`` (the page leaves EOS_ID
+    undefined, so it is the caller's): as in the page's loop, a pick equal to it is kept as
+    the last output and never fed, so the cache ends with the picks before it.
 
-    Returns ``ids`` (n_decode + 1 generated ids), ``logits`` per step ([n_decode + 1, V]) and,
+    Returns ``ids`` (the generated ids: n_decode + 1 without a stop), ``logits`` per step and,
     with ``keep_hidden``, per-step hidden states."""
     cache = cache if cache is not None else SeqCache(model.s.n_layers)
     out = forward(model, list(prompt), cache)
@@ -291,6 +293,8 @@ def generate(model: Model, prompt: Sequence[int], n_decode: int, cache: Optional
     logits = [out["logits"]]
     hidden = [out["hidden"]] if keep_hidden else None
     for _ in range(n_decode):
+        if eos_id is not None and ids[-1] == eos_id:
+            break
         out = forward(model, [ids[-1]], cache)
         ids.append(argmax_lowest(out["logits"]))
         logits.append(out["logits"])

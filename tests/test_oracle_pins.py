@@ -354,6 +354,24 @@ def test_generate_deterministic(tiny_model):
     np.testing.assert_array_equal(a["logits"], b["logits"])
 
 
+def test_generate_eos_stop_follows_the_page_loop(tiny_model):
+    """Paso 9: a pick equal to EOS_ID ends the output (kept as its last id) and is never fed:
+    the output is the no-stop run cut after the first EOS, and the cache holds the prompt and
+    the picks before it."""
+    s = synth.TINY
+    p = synth.make_tokens(s.vocab, 5, 12).tolist()
+    full = oracle.generate(tiny_model, p, 8, keep_hidden=False)["ids"]
+    eos = full[3]
+    k = full.index(eos)
+    c = SeqCache(s.n_layers)
+    got = oracle.generate(tiny_model, p, 8, cache=c, keep_hidden=False, eos_id=eos)["ids"]
+    assert got == full[:k + 1]
+    assert c.length == len(p) + k
+    c2 = SeqCache(s.n_layers)
+    never = oracle.generate(tiny_model, p, 8, cache=c2, keep_hidden=False, eos_id=s.vocab + 1)["ids"]
+    assert never == full and c2.length == len(p) + 8
+
+
 # ------------------------------------------------------------------- paged KV mirror ---
 
 def test_paged_mirror_slots_and_lowest_first():
