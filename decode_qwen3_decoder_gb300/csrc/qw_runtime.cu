@@ -1112,9 +1112,15 @@ extern "C" qw_status qw_decode_step(qw_model* m, qw_kv* kv, int B, const int* se
     return QW_OK;
 }
 
-extern "C" qw_status qw_generate(qw_model* m, qw_kv* kv, int B, const int* seq_ids, const int* lens,
-                                 const int32_t* host_prompt_ids, int n_decode, int32_t* host_out_ids,
-                                 void* stream_) {
+// Paso 9 over a batch: prefill, then decode steps feeding each pick back on the device. With
+// eos_id >= 0 a sequence stops after its first pick equal to eos_id (the pick is kept, never
+// fed). Stopped sequences keep stepping with the rest of the batch (one graph for the whole
+// batch); their extra positions are dropped from the cache at the end. The host looks at the
+// picks every kEosCheck steps and ends the loop once every sequence has stopped.
+static qw_status generate_impl(qw_model* m, qw_kv* kv, int B, const int* seq_ids, const int* lens,
+                               const int32_t* host_prompt_ids, int n_decode, int eos_id, int32_t* host_out_ids,
+                               int32_t* host_out_counts, cudaStream_t st) {
+    constexpr int kEosCheck = 8;
     QW_TRY(check_batch(m, kv, B, seq_ids));
     if (!lens || !host_prompt_ids || !host_out_ids) return fail(QW_ERR_INVALID_ARG, "NULL argument");
     if (n_decode < 0 || n_decode + 1 > m->cfg.max_context) return fail(QW_ERR_INVALID_ARG, "n_decode out of range");
@@ -1122,28 +1128,70 @@ extern "C" qw_status qw_generate(qw_model* m, qw_kv* kv, int B, const int* seq_i
     for (int b = 0; b < B; ++b) {
         if (lens[b] < 1) return fail(QW_ERR_INVALID_ARG, "lens[%d] < 1", b);
         const int s = seq_ids[b];
+        if (kv->len[s] != 0) return fail(QW_ERR_BAD_STATE, "generate needs empty sequences (%d is not)", s);
         if ((long long)kv->pt[s].size() * 16 < (long long)lens[b] + n_decode)
             return fail(QW_ERR_KV_FULL, "sequence %d not reserved for prompt + %d decode tokens", s, n_decode);
         total += lens[b];
     }
     if (total > m->cfg.max_tokens) return fail(QW_ERR_INVALID_ARG, "prompts exceed max_tokens");
-    cudaStream_t st = (cudaStream_t)stream_;
     CUDA_TRY(cudaMemcpyAsync(m->gen_tok, host_prompt_ids, (size_t)total * 4, cudaMemcpyHostToDevice, st));
     QW_TRY(qw_prefill(m, kv, B, seq_ids, lens, m->gen_tok, nullptr, m->gen_cur, st));
     int launches = m->last_launches;
     CUDA_TRY(cudaMemcpyAsync(m->gen_out, m->gen_cur, (size_t)B * 4, cudaMemcpyDeviceToDevice, st));
-    for (int i = 1; i <= n_decode; ++i) {
+    std::vector<int32_t> tmp((size_t)(n_decode + 1) * B);
+    std::vector<int> stop_at(B, -1);  // index of a sequence's first EOS pick
+    int n_stopped = 0, seen = 0;      // picks [0, seen) were read on the host
+    auto look = [&](int upto) -> qw_status {  // read picks [seen, upto] and note the stops
+        if (upto < seen) return QW_OK;
+        CUDA_TRY(cudaMemcpyAsync(tmp.data() + (size_t)seen * B, m->gen_out + (size_t)seen * B,
+                                 (size_t)(upto + 1 - seen) * B * 4, cudaMemcpyDeviceToHost, st));
+        CUDA_TRY(cudaStreamSynchronize(st));
+        for (int i = seen; i <= upto; ++i)
+            for (int b = 0; b < B; ++b)
+                if (eos_id >= 0 && stop_at[b] < 0 && tmp[(size_t)i * B + b] == eos_id) {
+                    stop_at[b] = i;
+                    ++n_stopped;
+                }
+        seen = upto + 1;
+        return QW_OK;
+    };
+    if (eos_id >= 0) QW_TRY(look(0));
+    int last = 0;
+    for (int i = 1; i <= n_decode && n_stopped < B; ++i) {
         QW_TRY(qw_decode_step(m, kv, B, seq_ids, m->gen_cur, nullptr, m->gen_cur, st));
         launches += m->last_launches;
         CUDA_TRY(cudaMemcpyAsync(m->gen_out + (size_t)i * B, m->gen_cur, (size_t)B * 4, cudaMemcpyDeviceToDevice, st));
+        last = i;
+        if (eos_id >= 0 && i % kEosCheck == 0) QW_TRY(look(i));
     }
-    std::vector<int32_t> tmp((size_t)(n_decode + 1) * B);
-    CUDA_TRY(cudaMemcpyAsync(tmp.data(), m->gen_out, tmp.size() * 4, cudaMemcpyDeviceToHost, st));
+    QW_TRY(look(last));
+    for (int b = 0; b < B; ++b) {
+        const int n = stop_at[b] >= 0 ? stop_at[b] + 1 : last + 1;
+        for (int i = 0; i <= n_decode; ++i)
+            host_out_ids[(size_t)b * (n_decode + 1) + i] = i < n ? tmp[(size_t)i * B + b] : -1;
+        if (host_out_counts) host_out_counts[b] = n;
+        // fed: the prompt and the picks before the stop; the cache advanced once per step
+        if (stop_at[b] >= 0 && stop_at[b] < last) QW_TRY(qw_kv_truncate(kv, seq_ids[b], lens[b] + stop_at[b], st));
+    }
     CUDA_TRY(cudaStreamSynchronize(st));
-    for (int i = 0; i <= n_decode; ++i)
-        for (int b = 0; b < B; ++b) host_out_ids[(size_t)b * (n_decode + 1) + i] = tmp[(size_t)i * B + b];
     m->last_launches = launches;
     return QW_OK;
+}
+
+extern "C" qw_status qw_generate(qw_model* m, qw_kv* kv, int B, const int* seq_ids, const int* lens,
+                                 const int32_t* host_prompt_ids, int n_decode, int32_t* host_out_ids,
+                                 void* stream_) {
+    return generate_impl(m, kv, B, seq_ids, lens, host_prompt_ids, n_decode, -1, host_out_ids, nullptr,
+                         (cudaStream_t)stream_);
+}
+
+extern "C" qw_status qw_generate_eos(qw_model* m, qw_kv* kv, int B, const int* seq_ids, const int* lens,
+                                     const int32_t* host_prompt_ids, int n_decode, int eos_id,
+                                     int32_t* host_out_ids, int32_t* host_out_counts, void* stream_) {
+    if (eos_id < 0 || (m && eos_id >= m->cfg.vocab)) return fail(QW_ERR_INVALID_ARG, "eos_id outside [0, vocab)");
+    if (!host_out_counts) return fail(QW_ERR_INVALID_ARG, "NULL argument");
+    return generate_impl(m, kv, B, seq_ids, lens, host_prompt_ids, n_decode, eos_id, host_out_ids, host_out_counts,
+                         (cudaStream_t)stream_);
 }
 
 extern "C" qw_status qw_sync_status(qw_model* m, void* stream_) {

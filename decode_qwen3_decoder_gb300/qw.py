@@ -68,6 +68,8 @@ SIGNATURES = {
     "qw_decode_step": (_I, [_VP, _VP, _I, _P(_I), _VP, _VP, _VP, _VP]),
     "qw_generate": (_I, [_VP, _VP, _I, _P(_I), _P(_I), _P(ctypes.c_int32), _I,
                          _P(ctypes.c_int32), _VP]),
+    "qw_generate_eos": (_I, [_VP, _VP, _I, _P(_I), _P(_I), _P(ctypes.c_int32), _I, _I,
+                             _P(ctypes.c_int32), _P(ctypes.c_int32), _VP]),
     "qw_sync_status": (_I, [_VP, _VP]),
     "qw_last_error": (ctypes.c_char_p, []),
     "qw_free_model": (None, [_VP]),
@@ -187,6 +189,18 @@ def qw_generate(model: int, kv: int, seq_ids: Sequence[int], lens: Sequence[int]
     _check(load().qw_generate(model, kv, len(seq_ids), _ints(seq_ids), _ints(lens),
                               host_prompt.ctypes.data_as(_P(ctypes.c_int32)), n_decode,
                               host_out.ctypes.data_as(_P(ctypes.c_int32)), _stream(stream)))
+
+
+def qw_generate_eos(model: int, kv: int, seq_ids: Sequence[int], lens: Sequence[int], host_prompt,
+                    n_decode: int, eos_id: int, host_out, host_counts, stream=None) -> None:
+    """As qw_generate with an EOS stop; host_counts: int32 numpy array (B)."""
+    import numpy as np
+    for a in (host_prompt, host_out, host_counts):
+        assert a.dtype == np.int32 and a.flags.c_contiguous
+    _check(load().qw_generate_eos(model, kv, len(seq_ids), _ints(seq_ids), _ints(lens),
+                                  host_prompt.ctypes.data_as(_P(ctypes.c_int32)), n_decode, eos_id,
+                                  host_out.ctypes.data_as(_P(ctypes.c_int32)),
+                                  host_counts.ctypes.data_as(_P(ctypes.c_int32)), _stream(stream)))
 
 
 def qw_sync_status(model: int, stream=None) -> int:

@@ -168,6 +168,20 @@ qw_status qw_generate(qw_model* m, qw_kv* kv, int B, const int* seq_ids, const i
                       const int32_t* host_prompt_ids, int n_decode, int32_t* host_out_ids,
                       void* stream);
 
+/* Greedy generation with an EOS stop (Paso 9: the page's loop ends when a pick equals
+ * EOS_ID; the page leaves the id undefined, so the caller gives it). As qw_generate, except:
+ * a sequence stops after its first pick equal to eos_id, which is kept as its last output and
+ * never fed to the model. Row b of host_out_ids ([B, n_decode + 1]) holds host_out_counts[b]
+ * picks (up to and including that EOS; n_decode + 1 without one) followed by -1, and the
+ * sequence's cache ends with the prompt and the picks it fed. The batch steps until every
+ * sequence has stopped (the host reads the picks every 8 steps) or n_decode steps ran;
+ * stopped sequences keep stepping with the batch meanwhile and their extra positions are
+ * dropped from the cache at the end. Errors as qw_generate, plus QW_ERR_INVALID_ARG for
+ * eos_id outside [0, vocab) or a NULL host_out_counts. */
+qw_status qw_generate_eos(qw_model* m, qw_kv* kv, int B, const int* seq_ids, const int* lens,
+                          const int32_t* host_prompt_ids, int n_decode, int eos_id, int32_t* host_out_ids,
+                          int32_t* host_out_counts, void* stream);
+
 /* Synchronise `stream`, read and clear the device status word. Returns QW_OK or the first
  * of QW_ERR_BAD_TOKEN, QW_ERR_BAD_POS, QW_ERR_TIMEOUT that the word records. */
 qw_status qw_sync_status(qw_model* m, void* stream);

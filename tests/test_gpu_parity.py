@@ -291,3 +291,58 @@ def test_injected_long_cache_forced_decode(one_block_long, lens):
             check_hidden(d["hidden"][:, b:b + 1], o["hidden"])
             check_logits(d["logits"][b], o["logits"])
             check_token(d["next"][b], o["logits"])
+
+
+def test_generate_eos_stop(one_block):
+    """Paso 9's EOS stop over a batch: each row equals the no-stop run cut after its first EOS
+    (then -1), each cache holds exactly the tokens fed (the EOS is never fed), and a stopped
+    sequence continues from its cache as the oracle's does."""
+    run, om = one_block
+    qw, eng = run.qw, run.eng
+    s = synth.ONE_BLOCK
+    lens, nd = [5, 9, 3, 7], 20
+    prompts = [synth.make_tokens(s.vocab, n, 600 + n).tolist() for n in lens]
+    flat = np.ascontiguousarray(np.concatenate(prompts).astype(np.int32))
+    seqs = [0, 1, 2, 3]
+
+    def fresh():
+        qw.qw_kv_reset(eng.kv, -1, eng.stream)
+        for sq, n in zip(seqs, lens):
+            qw.qw_kv_reserve(eng.kv, sq, n + nd, eng.stream)
+
+    fresh()
+    full = np.zeros((4, nd + 1), np.int32)
+    qw.qw_generate(eng.model, eng.kv, seqs, lens, flat, nd, full, eng.stream)
+    eos = int(full[1, 4])  # appears in row 1 by index 4; maybe elsewhere, maybe not
+    fresh()
+    out = np.zeros((4, nd + 1), np.int32)
+    counts = np.zeros(4, np.int32)
+    qw.qw_generate_eos(eng.model, eng.kv, seqs, lens, flat, nd, eos, out, counts, eng.stream)
+    stopped = []
+    for b in range(4):
+        hits = np.flatnonzero(full[b] == eos)
+        n = int(hits[0]) + 1 if hits.size else nd + 1
+        assert counts[b] == n, (b, counts[b], n)
+        np.testing.assert_array_equal(out[b, :n], full[b, :n])
+        assert np.all(out[b, n:] == -1)
+        if hits.size:
+            stopped.append(b)
+            assert qw.qw_kv_length(eng.kv, seqs[b]) == lens[b] + n - 1
+    assert 1 in stopped
+    if len(stopped) == 4:  # every row stopped: the loop ended at the last stop
+        last = max(int(counts[b]) for b in range(4)) - 1
+    else:
+        last = nd
+    for b in range(4):
+        if b not in stopped:
+            assert qw.qw_kv_length(eng.kv, seqs[b]) == lens[b] + last
+    # row 1 continues from its cache, fed token 17: the oracle is given the same tokens the
+    # GPU fed (the prompt and the picks before the EOS; greedy paths of the two may part on
+    # near ties, so the GPU's picks are forced)
+    c = oracle.SeqCache(s.n_layers)
+    oracle.forward(om, prompts[1] + out[1, :counts[1] - 1].tolist(), c)
+    assert c.length == qw.qw_kv_length(eng.kv, 1)
+    o = oracle.forward(om, [17], c)
+    d = run.decode([1], [17], debug=False)
+    check_logits(d["logits"][0], o["logits"])
+    check_token(d["next"][0], o["logits"])
