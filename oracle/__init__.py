@@ -30,3 +30,4 @@ from .sampling import (  # noqa: F401
     kept_cdf,
     sample as sample_top_p,
 )
+from . import quant  # noqa: F401

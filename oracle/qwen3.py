@@ -33,7 +33,10 @@ import numpy as np
 
 
 def _widen(bits: np.ndarray) -> np.ndarray:
-    """bf16 bit patterns (uint16) -> float64, exactly."""
+    """bf16 bit patterns (uint16) -> float64, exactly; float arrays (e.g. dequantized
+    weights) are taken as they are."""
+    if np.asarray(bits).dtype.kind == "f":
+        return np.asarray(bits, dtype=np.float64)
     u = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
     return u.view(np.float32).astype(np.float64)
 
