@@ -152,6 +152,11 @@ struct GemvP {
     const f16* act;
     const bf16* W;
     const bf16* W2;
+    // quantized weights (QB = 8 or 4): codes and per-group (scale, bias) half2 words
+    const uint8_t* qw;
+    const uint8_t* qw2;
+    const uint32_t* sb;
+    const uint32_t* sb2;
     int n_out;
     int K;
     int T;
@@ -171,12 +176,51 @@ __device__ __forceinline__ uint4 ldg_stream_v(const void* ptr) {
                  : "l"(ptr));
     return r;
 }
+__device__ __forceinline__ uint2 ldg_stream_v2(const void* ptr) {
+    uint2 r;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(ptr));
+    return r;
+}
+__device__ __forceinline__ uint32_t ldg_stream_u32(const void* ptr) {
+    uint32_t r;
+    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(r) : "l"(ptr));
+    return r;
+}
+
+// Eight dequantized weights (scale * q + bias) times eight activations: w.x (and w.y for
+// 8-bit codes) hold the codes, w.z the group's (scale, bias) half2 word.
+template <int QB>
+__device__ __forceinline__ float dot8q(const uint4 w, const float4 a0, const float4 a1, float acc) {
+    float q[8];
+    if (QB == 8) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            q[i] = (float)((w.x >> (8 * i)) & 0xFFu);
+            q[4 + i] = (float)((w.y >> (8 * i)) & 0xFFu);
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) q[i] = (float)((w.x >> (4 * i)) & 0xFu);
+    }
+    const float s = h_lo(w.z), b = h_hi(w.z);
+    float dq = q[0] * a0.x;
+    dq = fmaf(q[1], a0.y, dq);
+    dq = fmaf(q[2], a0.z, dq);
+    dq = fmaf(q[3], a0.w, dq);
+    dq = fmaf(q[4], a1.x, dq);
+    dq = fmaf(q[5], a1.y, dq);
+    dq = fmaf(q[6], a1.z, dq);
+    dq = fmaf(q[7], a1.w, dq);
+    const float sa = ((a0.x + a0.y) + (a0.z + a0.w)) + ((a1.x + a1.y) + (a1.z + a1.w));
+    return fmaf(s, dq, fmaf(b, sa, acc));
+}
 
 // Programmatic dependent launch: the kernel lets its dependents launch at entry and issues
 // the weight loads of its first row group before griddepcontrol.wait, so the weights (which
 // no earlier kernel writes) stream from HBM while the upstream kernel is still finishing.
 // Everything that reads upstream outputs, or writes anything, comes after the wait.
-template <int TT, int MODE, int KC, int RPW>
+// QB: weight format, 16 = the bf16 originals, 8 / 4 = grouped affine codes (groups of 64).
+template <int TT, int MODE, int KC, int RPW, int QB>
 __global__ void __launch_bounds__(GEMV_WARPS * 32) k_gemv(GemvP p) {
     extern __shared__ float4 smem_f4[];
     float* hs = reinterpret_cast<float*>(smem_f4);  // [TT][K] fp32
@@ -196,8 +240,29 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) k_gemv(GemvP p) {
 #pragma unroll
             for (int c = 0; c < PC; ++c) {
                 const size_t off = (size_t)row * K + (c0 + c) * 256 + lane * 8;
-                wv[rr][0][c] = ldg_stream_v(p.W + off);
-                if (NW == 2) wv[rr][NW - 1][c] = ldg_stream_v(p.W2 + off);
+                if (QB == 16) {
+                    wv[rr][0][c] = ldg_stream_v(p.W + off);
+                    if (NW == 2) wv[rr][NW - 1][c] = ldg_stream_v(p.W2 + off);
+                } else {
+                    const size_t gi = off / 64;  // group of these 8 inputs
+#pragma unroll
+                    for (int n = 0; n < NW; ++n) {
+                        const uint8_t* cw = n ? p.qw2 : p.qw;
+                        const uint32_t* sw = n ? p.sb2 : p.sb;
+                        uint4 v;
+                        if (QB == 8) {
+                            const uint2 t = ldg_stream_v2(cw + off);
+                            v.x = t.x;
+                            v.y = t.y;
+                        } else {
+                            v.x = ldg_stream_u32(cw + off / 2);
+                            v.y = 0u;
+                        }
+                        v.z = ldg_stream_u32(sw + gi);
+                        v.w = 0u;
+                        wv[rr][n][c] = v;
+                    }
+                }
             }
         }
     };
@@ -298,7 +363,9 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) k_gemv(GemvP p) {
 #pragma unroll
                     for (int rr = 0; rr < RPW; ++rr)
 #pragma unroll
-                        for (int n = 0; n < NW; ++n) acc[rr][n][t] = dot8(wv[rr][n][c], a0, a1, acc[rr][n][t]);
+                        for (int n = 0; n < NW; ++n)
+                            acc[rr][n][t] = QB == 16 ? dot8(wv[rr][n][c], a0, a1, acc[rr][n][t])
+                                                     : dot8q<QB>(wv[rr][n][c], a0, a1, acc[rr][n][t]);
                 }
             }
         }
@@ -360,12 +427,12 @@ int num_sms() {
     return g_num_sms;
 }
 
-template <int TT, int MODE, int KC, int RPW>
+template <int TT, int MODE, int KC, int RPW, int QB>
 cudaError_t gemv_go(const LaunchCtx& c, const GemvP& p, int max_ctas) {
     const size_t smem = (size_t)TT * KC * 256 * sizeof(float);
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(k_gemv<TT, MODE, KC, RPW>,
+        cudaError_t e = cudaFuncSetAttribute(k_gemv<TT, MODE, KC, RPW, QB>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         attr_set = true;
@@ -373,57 +440,80 @@ cudaError_t gemv_go(const LaunchCtx& c, const GemvP& p, int max_ctas) {
     const int per_cta = GEMV_WARPS * RPW;
     int grid = (p.n_out + per_cta - 1) / per_cta;
     if (max_ctas > 0 && grid > max_ctas) grid = max_ctas;
-    return launch_k(c, k_gemv<TT, MODE, KC, RPW>, dim3(grid), dim3(GEMV_WARPS * 32), smem, p);
+    return launch_k(c, k_gemv<TT, MODE, KC, RPW, QB>, dim3(grid), dim3(GEMV_WARPS * 32), smem, p);
 }
 
 // Rows per warp: a lane holds whole rows (K <= 3072) of RPW rows in registers; 4 rows of
 // K=1024 (64 registers) for 1-2 tokens, fewer for more tokens or longer rows, so that the
 // narrow long-K matrices (o_proj, down_proj: 1024 rows) still spread over >= 256 CTAs.
-template <int MODE, int KC>
+template <int MODE, int KC, int QB>
 cudaError_t gemv_kc(const LaunchCtx& c, const GemvP& p, int max_ctas) {
     constexpr int NW = (MODE == G_GATEUP) ? 2 : 1;
     constexpr int R12 = (KC >= 8 ? 1 : 4 / NW);
     constexpr int R4 = (KC >= 8 ? 1 : 2 / NW);
-    if (p.T <= 1) return gemv_go<1, MODE, KC, R12>(c, p, max_ctas);
-    if (p.T <= 2) return gemv_go<2, MODE, KC, R12>(c, p, max_ctas);
-    if (p.T <= 4) return gemv_go<4, MODE, KC, R4>(c, p, max_ctas);
-    return gemv_go<8, MODE, KC, 1>(c, p, max_ctas);
+    if (p.T <= 1) return gemv_go<1, MODE, KC, R12, QB>(c, p, max_ctas);
+    if (p.T <= 2) return gemv_go<2, MODE, KC, R12, QB>(c, p, max_ctas);
+    if (p.T <= 4) return gemv_go<4, MODE, KC, R4, QB>(c, p, max_ctas);
+    return gemv_go<8, MODE, KC, 1, QB>(c, p, max_ctas);
+}
+
+// Quantized weights exist only for the projections of the layers (q|k|v and gate/up over the
+// hidden size 1024, o_proj and down_proj over 2048 and 3072 inputs).
+template <int MODE, int QB>
+cudaError_t gemv_dispatch(const LaunchCtx& c, const GemvP& p, int max_ctas) {
+    if (p.T < 1 || p.T > 8) return cudaErrorInvalidValue;
+    if constexpr (QB == 16) {
+        switch (p.K) {
+            case 1024: return gemv_kc<MODE, 4, 16>(c, p, max_ctas);
+            case 2048: return gemv_kc<MODE, 8, 16>(c, p, max_ctas);
+            case 3072: return gemv_kc<MODE, 12, 16>(c, p, max_ctas);
+            case 4096: return gemv_kc<MODE, 16, 16>(c, p, max_ctas);
+            default: return cudaErrorInvalidValue;
+        }
+    } else if constexpr (MODE == G_QKV || MODE == G_GATEUP) {
+        return p.K == 1024 ? gemv_kc<MODE, 4, QB>(c, p, max_ctas) : cudaErrorInvalidValue;
+    } else if constexpr (MODE == G_RESID) {
+        if (p.K == 2048) return gemv_kc<MODE, 8, QB>(c, p, max_ctas);
+        if (p.K == 3072) return gemv_kc<MODE, 12, QB>(c, p, max_ctas);
+        return cudaErrorInvalidValue;
+    } else {
+        return cudaErrorInvalidValue;
+    }
 }
 
 template <int MODE>
-cudaError_t gemv_dispatch(const LaunchCtx& c, const GemvP& p, int max_ctas) {
-    if (p.T < 1 || p.T > 8) return cudaErrorInvalidValue;
-    switch (p.K) {
-        case 1024: return gemv_kc<MODE, 4>(c, p, max_ctas);
-        case 2048: return gemv_kc<MODE, 8>(c, p, max_ctas);
-        case 3072: return gemv_kc<MODE, 12>(c, p, max_ctas);
-        case 4096: return gemv_kc<MODE, 16>(c, p, max_ctas);
-        default: return cudaErrorInvalidValue;
-    }
+cudaError_t gemv_any(const LaunchCtx& c, const GemvP& p, int qbits, int max_ctas) {
+    if (qbits == 8) return gemv_dispatch<MODE, 8>(c, p, max_ctas);
+    if (qbits == 4) return gemv_dispatch<MODE, 4>(c, p, max_ctas);
+    return gemv_dispatch<MODE, 16>(c, p, max_ctas);
 }
 
 }  // namespace
 
 cudaError_t launch_gemv_qkv(const LaunchCtx& c, int T, const float* x, const bf16* norm_w, float eps,
-                            const bf16* W, int n_out, int K, float* out) {
+                            const bf16* W, int n_out, int K, float* out, const QWeights* qw) {
     GemvP p = {};
     p.x = x; p.norm_w = norm_w; p.eps = eps; p.W = W; p.n_out = n_out; p.K = K; p.T = T; p.out = out;
-    return gemv_dispatch<G_QKV>(c, p, 0);
+    if (qw) { p.qw = qw->codes; p.sb = qw->sb; }
+    return gemv_any<G_QKV>(c, p, qw ? qw->bits : 16, 0);
 }
 
 cudaError_t launch_gemv_gateup(const LaunchCtx& c, int T, const float* x, const bf16* norm_w,
-                               float eps, const bf16* Wg, const bf16* Wu, int inter, int K, f16* act) {
+                               float eps, const bf16* Wg, const bf16* Wu, int inter, int K, f16* act,
+                               const QWeights* qg, const QWeights* qu) {
     GemvP p = {};
     p.x = x; p.norm_w = norm_w; p.eps = eps; p.W = Wg; p.W2 = Wu; p.n_out = inter; p.K = K; p.T = T;
     p.out_h = act;
-    return gemv_dispatch<G_GATEUP>(c, p, 0);
+    if (qg) { p.qw = qg->codes; p.sb = qg->sb; p.qw2 = qu->codes; p.sb2 = qu->sb; }
+    return gemv_any<G_GATEUP>(c, p, qg ? qg->bits : 16, 0);
 }
 
 cudaError_t launch_gemv_resid(const LaunchCtx& c, int T, const f16* act, const bf16* W, int n_out,
-                              int K, float* x) {
+                              int K, float* x, const QWeights* qw) {
     GemvP p = {};
     p.act = act; p.W = W; p.n_out = n_out; p.K = K; p.T = T; p.out = x;
-    return gemv_dispatch<G_RESID>(c, p, 0);
+    if (qw) { p.qw = qw->codes; p.sb = qw->sb; }
+    return gemv_any<G_RESID>(c, p, qw ? qw->bits : 16, 0);
 }
 
 cudaError_t launch_gemv_lmhead(const LaunchCtx& c, int B, const float* x, const int* rows,
@@ -432,7 +522,7 @@ cudaError_t launch_gemv_lmhead(const LaunchCtx& c, int B, const float* x, const 
     GemvP p = {};
     p.x = x; p.rows = rows; p.norm_w = norm_w; p.eps = eps; p.W = E; p.n_out = vocab; p.K = K;
     p.T = B; p.out = logits; p.best = best;
-    return gemv_dispatch<G_LMHEAD>(c, p, num_sms() * 8);
+    return gemv_dispatch<G_LMHEAD, 16>(c, p, num_sms() * 8);
 }
 
 // =======================================================================================
@@ -645,4 +735,80 @@ __global__ void k_convert_gateup(const bf16* __restrict__ gate, const bf16* __re
 cudaError_t launch_convert_gateup(const LaunchCtx& c, const bf16* gate, const bf16* up, f16* dst, int inter, int K,
                                   int* status) {
     return launch_k(c, k_convert_gateup, dim3(2 * inter), dim3(256), 0, gate, up, dst, inter, K, status);
+}
+
+// =======================================================================================
+// Weight-only grouped affine quantization ("Lo que omite el script": 4- and 8-bit weights):
+// each row of a [rows, K] bf16 matrix is cut into groups of 64 inputs; per group, in fp32,
+// scale = (max - min) / (2^bits - 1) and bias = min, both rounded to fp16 (how they are
+// stored, as one half2 word: scale low, bias high); code q = clamp(rint((w - bias) / scale),
+// 0, 2^bits - 1) (q = 0 where the fp16 scale is 0), with IEEE division. Codes are stored one
+// per byte (8 bits) or two per byte, the even input in the low nibble (4 bits). The thread of
+// a group also writes the dequantized weights scale * q + bias (fp16) into the tensor-core
+// copy of the matrix, at row deq_row(r): r, or r's place among interleaved gate/up rows.
+// =======================================================================================
+__global__ void k_quantize(const bf16* __restrict__ W, int rows, int K, int nbits, uint8_t* __restrict__ codes,
+                           uint32_t* __restrict__ sb, f16* __restrict__ deq, int deq_mode) {
+    const int G = K / 64;
+    const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (gid >= (long long)rows * G) return;
+    const int r = (int)(gid / G), g = (int)(gid % G);
+    const bf16* src = W + (size_t)r * K + g * 64;
+    float w[64];
+    float lo = INFINITY, hi = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 64; i += 8) {
+        const uint4 v = *reinterpret_cast<const uint4*>(src + i);
+        const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            w[i + 2 * j] = bf_lo(u[j]);
+            w[i + 2 * j + 1] = bf_hi(u[j]);
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < 64; ++i) {
+        lo = fminf(lo, w[i]);
+        hi = fmaxf(hi, w[i]);
+    }
+    const float levels = (float)((1 << nbits) - 1);
+    const __half s16 = __float2half_rn(__fdiv_rn(hi - lo, levels));
+    const __half b16 = __float2half_rn(lo);
+    const float s = __half2float(s16), b = __half2float(b16);
+    sb[(size_t)r * G + g] = (uint32_t)__half_as_ushort(s16) | ((uint32_t)__half_as_ushort(b16) << 16);
+    int dr = r;
+    if (deq_mode == 1) dr = (r / 64) * 128 + r % 64;       // gate row among interleaved gate/up rows
+    else if (deq_mode == 2) dr = (r / 64) * 128 + 64 + r % 64;  // up row
+    f16* drow = deq + (size_t)dr * K + g * 64;
+    uint32_t pack = 0;
+#pragma unroll
+    for (int i = 0; i < 64; ++i) {
+        float q = s == 0.f ? 0.f : rintf(__fdiv_rn(w[i] - b, s));
+        q = fminf(fmaxf(q, 0.f), levels);
+        const uint32_t qi = (uint32_t)q;
+        drow[i] = __float2half_rn(fmaf(s, q, b));
+        if (nbits == 8) {
+            pack |= qi << (8 * (i & 3));
+            if ((i & 3) == 3) {
+                *reinterpret_cast<uint32_t*>(codes + (size_t)r * K + g * 64 + i - 3) = pack;
+                pack = 0;
+            }
+        } else {
+            pack |= qi << (4 * (i & 7));
+            if ((i & 7) == 7) {
+                *reinterpret_cast<uint32_t*>(codes + ((size_t)r * K + g * 64 + i - 7) / 2) = pack;
+                pack = 0;
+            }
+        }
+    }
+}
+
+cudaError_t launch_quantize(cudaStream_t st, const bf16* W, int rows, int K, int nbits, uint8_t* codes, uint32_t* sb,
+                            f16* deq, int deq_mode) {
+    if (K % 64 || (nbits != 8 && nbits != 4)) return cudaErrorInvalidValue;
+    const long long groups = (long long)rows * (K / 64);
+    const int threads = 128;
+    const unsigned blocks = (unsigned)((groups + threads - 1) / threads);
+    k_quantize<<<blocks, threads, 0, st>>>(W, rows, K, nbits, codes, sb, deq, deq_mode);
+    return cudaGetLastError();
 }

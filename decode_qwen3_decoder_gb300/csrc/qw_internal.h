@@ -116,13 +116,25 @@ cudaError_t launch_step_begin(const LaunchCtx& c, const StepDesc& sd, const int3
 cudaError_t launch_rmsnorm(const LaunchCtx& c, const float* x, const int* rows, int n_rows,
                            int hidden, const bf16* w, float eps, f16* h);
 cudaError_t launch_convert_bf16_f16(const LaunchCtx& c, const bf16* src, f16* dst, size_t n, int* status);
-// GEMV family (T <= 8 token rows).
+// Grouped affine weight codes of one matrix [rows, K]: codes (one per byte at 8 bits, two per
+// byte at 4, the even input in the low nibble) and one (scale, bias) half2 word per group of
+// 64 inputs, scale in the low half.
+struct QWeights {
+    const uint8_t* codes;
+    const uint32_t* sb;
+    int bits;
+};
+cudaError_t launch_quantize(cudaStream_t st, const bf16* W, int rows, int K, int nbits, uint8_t* codes, uint32_t* sb,
+                            f16* deq, int deq_mode);
+// GEMV family (T <= 8 token rows); with quantized weights (non-NULL QWeights) the bf16
+// pointers are not read.
 cudaError_t launch_gemv_qkv(const LaunchCtx& c, int T, const float* x, const bf16* norm_w, float eps,
-                            const bf16* W, int n_out, int K, float* out);
+                            const bf16* W, int n_out, int K, float* out, const QWeights* qw = nullptr);
 cudaError_t launch_gemv_gateup(const LaunchCtx& c, int T, const float* x, const bf16* norm_w,
-                               float eps, const bf16* Wg, const bf16* Wu, int inter, int K, f16* act);
+                               float eps, const bf16* Wg, const bf16* Wu, int inter, int K, f16* act,
+                               const QWeights* qg = nullptr, const QWeights* qu = nullptr);
 cudaError_t launch_gemv_resid(const LaunchCtx& c, int T, const f16* act, const bf16* W, int n_out,
-                              int K, float* x);
+                              int K, float* x, const QWeights* qw = nullptr);
 cudaError_t launch_gemv_lmhead(const LaunchCtx& c, int B, const float* x, const int* rows,
                                const bf16* norm_w, float eps, const bf16* E, int vocab, int K,
                                float* logits, unsigned long long* best);

@@ -7,6 +7,7 @@
 //
 // Page: "Dentro de un LLM: Inferencia en Python puro para Qwen3-0.6B en MLX".
 #include <algorithm>
+#include <array>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -177,6 +178,11 @@ struct qw_model {
     cudaEvent_t ev_fork, ev_join;
     bool split_decode;         // decode batches of >= 16 run as two overlapping halves
     std::map<std::vector<long long>, GraphEntry> graphs;
+    // 16: the small-batch GEMVs read the bf16 weights; 8 / 4: they read grouped affine codes of
+    // the layers' projections (per layer: q|k|v, o, gate, up, down), whose dequantized values
+    // also replaced the tensor-core fp16 copies
+    int qbits = 16;
+    std::vector<std::array<QWeights, 5>> qlay;
     unsigned long long use_clock;
     int last_launches;
     int num_sms;
@@ -474,6 +480,76 @@ extern "C" qw_status qw_sample_top_p(int B, int vocab, const float* dev_logits, 
     return QW_OK;
 }
 
+// ---------------------------------------------------------------------------------------
+// Weight-only quantization of the layers' projections
+// ---------------------------------------------------------------------------------------
+struct QuantMat {
+    const bf16* src;
+    f16* deq;
+    int rows, K, deq_mode;
+};
+
+static std::array<QuantMat, 5> quant_mats(const qw_model* m, int l) {
+    const qw_config& c = m->cfg;
+    const size_t D = c.hidden, I = c.inter, QD = (size_t)c.n_heads * c.head_dim, R = m->qkv_rows;
+    return {QuantMat{m->bqkv + l * R * D, m->wqkv + l * R * D, (int)R, (int)D, 0},
+            QuantMat{m->bo + l * D * QD, m->wo + l * D * QD, (int)D, (int)QD, 0},
+            QuantMat{m->bg + l * I * D, m->wgu + l * 2 * I * D, (int)I, (int)D, 1},
+            QuantMat{m->bu + l * I * D, m->wgu + l * 2 * I * D, (int)I, (int)D, 2},
+            QuantMat{m->bd + l * D * I, m->wd + l * D * I, (int)D, (int)I, 0}};
+}
+
+static size_t quant_bytes(const qw_model* m, int bits, std::vector<std::array<QWeights, 5>>* lay, char* base) {
+    size_t off = 0;
+    auto take = [&](size_t n) {
+        const size_t o = off;
+        off = align_up(off + n, 256);
+        return o;
+    };
+    if (lay) lay->assign(m->cfg.n_layers, {});
+    for (int l = 0; l < m->cfg.n_layers; ++l) {
+        const auto mats = quant_mats(m, l);
+        for (int i = 0; i < 5; ++i) {
+            const size_t codes = take((size_t)mats[i].rows * mats[i].K * bits / 8);
+            const size_t sb = take((size_t)mats[i].rows * (mats[i].K / 64) * 4);
+            if (lay) (*lay)[l][i] = QWeights{(const uint8_t*)(base + codes), (const uint32_t*)(base + sb), bits};
+        }
+    }
+    return off;
+}
+
+extern "C" size_t qw_quantize_bytes(const qw_model* m, int bits) {
+    if (!m || (bits != 8 && bits != 4)) return 0;
+    return quant_bytes(m, bits, nullptr, nullptr);
+}
+
+extern "C" qw_status qw_quantize_weights(qw_model* m, int bits, void* dev_buf, size_t bytes, void* stream_) {
+    if (!m) return fail(QW_ERR_INVALID_ARG, "model is NULL");
+    if (bits != 8 && bits != 4) return fail(QW_ERR_INVALID_ARG, "bits must be 8 or 4");
+    if (m->qbits != 16) return fail(QW_ERR_BAD_STATE, "the weights are already quantized");
+    if (m->use_mk) return fail(QW_ERR_BAD_STATE, "the persistent decode kernel reads bf16 weights; turn it off first");
+    const qw_config& c = m->cfg;
+    const int QD = c.n_heads * c.head_dim;
+    if (c.hidden != 1024 || (QD != 2048 && QD != 3072) || (c.inter != 2048 && c.inter != 3072))
+        return fail(QW_ERR_UNSUPPORTED, "quantized GEMVs cover hidden 1024 with 2048/3072-wide o_proj and down_proj");
+    if (!dev_buf || !aligned(dev_buf, 256)) return fail(QW_ERR_INVALID_ARG, "buffer NULL or not 256-byte aligned");
+    std::vector<std::array<QWeights, 5>> lay;
+    const size_t need = quant_bytes(m, bits, &lay, (char*)dev_buf);
+    if (bytes < need) return fail(QW_ERR_INVALID_ARG, "buffer too small: %zu < %zu", bytes, need);
+    cudaStream_t st = (cudaStream_t)stream_;
+    for (int l = 0; l < c.n_layers; ++l) {
+        const auto mats = quant_mats(m, l);
+        for (int i = 0; i < 5; ++i)
+            CUDA_TRY(launch_quantize(st, mats[i].src, mats[i].rows, mats[i].K, bits, (uint8_t*)lay[l][i].codes,
+                                     (uint32_t*)lay[l][i].sb, mats[i].deq, mats[i].deq_mode));
+    }
+    for (auto& g : m->graphs) cudaGraphExecDestroy(g.second.exec);  // they launch the bf16 GEMVs
+    m->graphs.clear();
+    m->qlay = std::move(lay);
+    m->qbits = bits;
+    return QW_OK;
+}
+
 extern "C" int qw_last_launch_count(const qw_model* m) { return m ? m->last_launches : 0; }
 
 extern "C" qw_status qw_trace_set(qw_model* m, unsigned long long* dev_buf, int per_cta) {
@@ -491,6 +567,7 @@ extern "C" qw_status qw_set_option(qw_model* m, int option, int value) {
     switch (option) {
         case QW_OPT_PERSISTENT_DECODE:
             if (value && m->mk_max_t == 0) return fail(QW_ERR_UNSUPPORTED, "persistent decode kernel unavailable");
+            if (value && m->qbits != 16) return fail(QW_ERR_UNSUPPORTED, "the persistent decode kernel reads bf16 weights");
             m->use_mk = value != 0;
             return QW_OK;
         case QW_OPT_PDL:
@@ -775,11 +852,12 @@ static qw_status run_layers(qw_model* m, qw_kv* kv, const StepDesc& sd, bool pre
         const bf16* w_kn = nb + 2 * D + d;
         int32_t* lpos = l == 0 ? dbg_pos : nullptr;
         int32_t* lslot = l == 0 ? dbg_slot : nullptr;
+        const QWeights* qq = m->qbits != 16 ? m->qlay[l].data() : nullptr;  // quantized projections
         // --- attention sublayer (Paso 5) ---
         if (small) {
             PROF(QW_PROF_QKV);
             LAUNCH(launch_gemv_qkv(lc, T, x, w_in, c.rms_eps, m->bqkv + (size_t)l * m->qkv_rows * D, m->qkv_rows, D,
-                                   qkv));
+                                   qkv, qq ? &qq[0] : nullptr));
         } else {
             {
                 PROF(QW_PROF_RMSNORM);
@@ -843,7 +921,7 @@ static qw_status run_layers(qw_model* m, qw_kv* kv, const StepDesc& sd, bool pre
                                      cudaMemcpyDeviceToDevice, st));
         if (small) {
             PROF(QW_PROF_OPROJ);
-            LAUNCH(launch_gemv_resid(lc, T, attn, m->bo + (size_t)l * D * QD, D, QD, x));
+            LAUNCH(launch_gemv_resid(lc, T, attn, m->bo + (size_t)l * D * QD, D, QD, x, qq ? &qq[1] : nullptr));
         } else {
             PROF(QW_PROF_OPROJ);
             GemmArgs g = {};
@@ -857,10 +935,11 @@ static qw_status run_layers(qw_model* m, qw_kv* kv, const StepDesc& sd, bool pre
             {
                 PROF(QW_PROF_GATEUP);
                 LAUNCH(launch_gemv_gateup(lc, T, x, w_post, c.rms_eps, m->bg + (size_t)l * I * D,
-                                          m->bu + (size_t)l * I * D, I, D, act));
+                                          m->bu + (size_t)l * I * D, I, D, act, qq ? &qq[2] : nullptr,
+                                          qq ? &qq[3] : nullptr));
             }
             PROF(QW_PROF_DOWN);
-            LAUNCH(launch_gemv_resid(lc, T, act, m->bd + (size_t)l * D * I, D, I, x));
+            LAUNCH(launch_gemv_resid(lc, T, act, m->bd + (size_t)l * D * I, D, I, x, qq ? &qq[4] : nullptr));
         } else {
             {
                 PROF(QW_PROF_RMSNORM);

@@ -75,6 +75,8 @@ SIGNATURES = {
     "qw_free_model": (None, [_VP]),
     "qw_free_kv": (None, [_VP]),
     "qw_debug_set": (_I, [_VP, _VP, _VP, _VP]),
+    "qw_quantize_bytes": (_SZ, [_VP, _I]),
+    "qw_quantize_weights": (_I, [_VP, _I, _VP, _SZ, _VP]),
     "qw_sample_top_p": (_I, [_I, _I, _VP, _SZ, ctypes.c_float, ctypes.c_float, _VP, _VP, _VP]),
     "qw_debug_set_attn": (_I, [_VP, _VP]),
     "qw_kv_page_table": (_I, [_VP, _I, _P(ctypes.c_int32), _I]),
@@ -227,6 +229,14 @@ def qw_debug_set_attn(model: int, attn_ptr: int) -> None:
     _check(load().qw_debug_set_attn(model, attn_ptr or None))
 
 
+def qw_quantize_bytes(model: int, bits: int) -> int:
+    return load().qw_quantize_bytes(model, bits)
+
+
+def qw_quantize_weights(model: int, bits: int, buf_ptr: int, nbytes: int, stream=None) -> None:
+    _check(load().qw_quantize_weights(model, bits, buf_ptr, nbytes, _stream(stream)))
+
+
 def qw_sample_top_p(B: int, vocab: int, logits_ptr: int, ld: int, temperature: float, top_p: float,
                     uniform_ptr: int, next_ptr: int, stream=None) -> None:
     _check(load().qw_sample_top_p(B, vocab, logits_ptr, ld, temperature, top_p, uniform_ptr or None, next_ptr,
@@ -345,6 +355,17 @@ class Engine:
         if field in ("q_proj", "k_proj", "v_proj", "o_proj", "q_norm", "k_norm"):
             return f"self_attn.{field}.weight"
         return f"mlp.{field}.weight"
+
+    def quantize(self, bits: int) -> None:
+        """Quantize the layers' projections (qw_quantize_weights) into a buffer this engine
+        keeps alive."""
+        import torch
+        n = qw_quantize_bytes(self.model, bits)
+        if n == 0:
+            raise ValueError("bits must be 8 or 4")
+        self.qbuf = torch.empty(n, dtype=torch.uint8, device=self.dev)
+        qw_quantize_weights(self.model, bits, self.qbuf.data_ptr(), n, self.stream)
+        self.stream.synchronize()
 
     def close(self) -> None:
         if getattr(self, "kv", None):

@@ -275,6 +275,26 @@ int qw_persistent_grid(const qw_model* m);
  * graph captured while they are set; kind QW_PROF_OFF (or events NULL) turns it off. */
 qw_status qw_profile_set(qw_model* m, int kind, void* const* events, int n_events);
 
+/* ---- Weight-only quantization ("Lo que omite el script": 4- and 8-bit weights) --------- */
+
+/* Bytes of the caller-owned device buffer that qw_quantize_weights needs for `bits` (8 or 4);
+ * 0 for other values. */
+size_t qw_quantize_bytes(const qw_model* m, int bits);
+
+/* Quantizes the projections of every layer (q|k|v, o_proj, gate, up, down; not the norms and
+ * not the tied embedding / LM head) to grouped affine codes: groups of 64 inputs, scale =
+ * (max - min) / (2^bits - 1) and bias = min per group computed in fp32 and stored as fp16,
+ * code = clamp(rint((w - bias) / scale), 0, 2^bits - 1) (0 where the fp16 scale is 0),
+ * weight = scale * code + bias. The codes and (scale, bias) words go to dev_buf (256-byte
+ * aligned, at least qw_quantize_bytes(m, bits), owned by the caller, kept alive as long as the
+ * model is used). From then on the small-batch paths (<= 8 token rows) read the codes, and
+ * the tensor-core paths use the dequantized weights (written over the model's fp16 copies),
+ * so every call computes with the same quantized model. Irreversible for this model handle.
+ * Asynchronous on `stream`. Errors: QW_ERR_INVALID_ARG (bits, buffer), QW_ERR_BAD_STATE
+ * (already quantized, or the persistent decode kernel is on), QW_ERR_UNSUPPORTED (a shape
+ * other than hidden 1024 with o_proj / down_proj inputs of 2048 or 3072). */
+qw_status qw_quantize_weights(qw_model* m, int bits, void* dev_buf, size_t bytes, void* stream);
+
 /* ---- Sampling (Paso 8) ------------------------------------------------------------------ */
 
 /* Temperature + top-p sampling of B rows of logits, one token per row: row b is
