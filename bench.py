@@ -373,7 +373,53 @@ def run_ours(args, cfg, rank, world):
         "sampling": time_sampling(qw, s.vocab, st),
     }
     eng.close()
+    if B == 1:
+        out["quantized_decode"] = time_quantized_decode(qw, s, P, ND, hbm)
     return out
+
+
+def time_quantized_decode(qw, s, P: int, ND: int, hbm: float):
+    """B=1 decode steps (graph replays) with the layers' projections quantized to 8 and 4 bits
+    (qw_quantize_weights; the tied LM head stays bf16), on the default workload's prompt
+    length and step count: microseconds per step and the HBM fraction of the bytes a step
+    reads (codes + scales, LM head, KV)."""
+    import torch
+    res = {}
+    for bits in (8, 4):
+        w = synth.Weights(s, seed=0)
+        eng = qw.Engine(s, dict(w.named()), max_tokens=8, max_batch=8, max_context=P + ND + 16,
+                        kv_pages=(P + ND + 15) // 16 + 8, max_seqs=8)
+        del w
+        eng.quantize(bits)
+        st = eng.stream
+        d_prompt = torch.tensor(synth.make_tokens(s.vocab, P, 4242).astype(np.int32), device="cuda")
+        d_cur = torch.zeros(1, dtype=torch.int32, device="cuda")
+
+        def steps(n):
+            qw.qw_kv_reset(eng.kv, -1, st)
+            qw.qw_kv_reserve(eng.kv, 0, P + ND, st)
+            qw.qw_prefill(eng.model, eng.kv, [0], [P], d_prompt.data_ptr(), 0, d_cur.data_ptr(), st)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(st)
+            for _ in range(n):
+                qw.qw_decode_step(eng.model, eng.kv, [0], d_cur.data_ptr(), 0, d_cur.data_ptr(), st)
+            b.record(st)
+            st.synchronize()
+            return a.elapsed_time(b) * 1e3 / n
+
+        steps(ND)  # warm-up: captures the graphs
+        us = steps(ND)
+        if qw.qw_sync_status(eng.model, st) != 0:
+            raise RuntimeError(f"device status after quantized decode: {qw.qw_last_error()}")
+        nbytes = qw.qw_quantize_bytes(eng.model, bits) + s.vocab * s.hidden * 2 + \
+            (P + ND / 2) * s.n_layers * 2 * s.n_kv_heads * s.head_dim * 2
+        res[f"{bits}bit"] = {"decode_step_us": round(us, 2), "tok_s": round(1e6 / us, 1),
+                             "bytes_per_step": int(nbytes),
+                             "hbm_frac": round(nbytes / (us * 1e-6) / 1e9 / hbm, 4)}
+        eng.close()
+    res["note"] = ("B=1 greedy decode, the layers' projections as grouped affine codes (groups of 64, "
+                   "fp16 scale and bias); not the headline number, which uses the bf16 weights")
+    return res
 
 
 def time_sampling(qw, vocab: int, st, reps: int = 20):

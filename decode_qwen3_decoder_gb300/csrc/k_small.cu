@@ -189,18 +189,23 @@ __device__ __forceinline__ uint32_t ldg_stream_u32(const void* ptr) {
 
 // Eight dequantized weights (scale * q + bias) times eight activations: w.x (and w.y for
 // 8-bit codes) hold the codes, w.z the group's (scale, bias) half2 word.
+// A code c < 2^23 becomes a float exactly as (the float with bits 0x4B000000 | c) - 2^23:
+// that float is 2^23 + c, so a logic op and one addition replace an int-to-float conversion.
+__device__ __forceinline__ float code_to_float(uint32_t c) { return __uint_as_float(0x4B000000u | c) - 8388608.0f; }
+
+// sa: the sum of the eight activations (the bias term's factor, shared by every row).
 template <int QB>
-__device__ __forceinline__ float dot8q(const uint4 w, const float4 a0, const float4 a1, float acc) {
+__device__ __forceinline__ float dot8q(const uint4 w, const float4 a0, const float4 a1, float sa, float acc) {
     float q[8];
     if (QB == 8) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            q[i] = (float)((w.x >> (8 * i)) & 0xFFu);
-            q[4 + i] = (float)((w.y >> (8 * i)) & 0xFFu);
+            q[i] = code_to_float((w.x >> (8 * i)) & 0xFFu);
+            q[4 + i] = code_to_float((w.y >> (8 * i)) & 0xFFu);
         }
     } else {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) q[i] = (float)((w.x >> (4 * i)) & 0xFu);
+        for (int i = 0; i < 8; ++i) q[i] = code_to_float((w.x >> (4 * i)) & 0xFu);
     }
     const float s = h_lo(w.z), b = h_hi(w.z);
     float dq = q[0] * a0.x;
@@ -211,7 +216,6 @@ __device__ __forceinline__ float dot8q(const uint4 w, const float4 a0, const flo
     dq = fmaf(q[5], a1.y, dq);
     dq = fmaf(q[6], a1.z, dq);
     dq = fmaf(q[7], a1.w, dq);
-    const float sa = ((a0.x + a0.y) + (a0.z + a0.w)) + ((a1.x + a1.y) + (a1.z + a1.w));
     return fmaf(s, dq, fmaf(b, sa, acc));
 }
 
@@ -360,12 +364,13 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) k_gemv(GemvP p) {
                     const float* a = hs + t * K + (c0 + c) * 256 + lane * 8;
                     const float4 a0 = *reinterpret_cast<const float4*>(a);
                     const float4 a1 = *reinterpret_cast<const float4*>(a + 4);
+                    const float sa = QB == 16 ? 0.f : ((a0.x + a0.y) + (a0.z + a0.w)) + ((a1.x + a1.y) + (a1.z + a1.w));
 #pragma unroll
                     for (int rr = 0; rr < RPW; ++rr)
 #pragma unroll
                         for (int n = 0; n < NW; ++n)
                             acc[rr][n][t] = QB == 16 ? dot8(wv[rr][n][c], a0, a1, acc[rr][n][t])
-                                                     : dot8q<QB>(wv[rr][n][c], a0, a1, acc[rr][n][t]);
+                                                     : dot8q<QB>(wv[rr][n][c], a0, a1, sa, acc[rr][n][t]);
                 }
             }
         }
