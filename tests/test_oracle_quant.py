@@ -76,3 +76,23 @@ def test_quantized_provider_feeds_the_model():
     np.testing.assert_array_equal(lw.in_norm, m.layer(0).in_norm)
     out = oracle.forward(m, [1, 2, 3], oracle.SeqCache(shape.n_layers))
     assert np.all(np.isfinite(out["logits"]))
+
+
+def test_halfway_values_round_to_even_code():
+    # min 0, max 15/128 (scale 1/128): w = k.5/128 lies exactly between codes k and k + 1, and
+    # rint sends it to the even one (round half up would give 1, 2, 3, 4 here)
+    w = np.zeros(64)
+    w[1] = 15 / 128
+    w[2:6] = np.array([0.5, 1.5, 2.5, 3.5]) / 128
+    codes, s, b = quant.quantize(_bf16(w).reshape(1, 64), 4)
+    assert s[0, 0] == np.float16(1 / 128) and b[0, 0] == 0
+    assert codes[0, 2:6].tolist() == [0, 2, 2, 4]
+
+
+def test_eight_bits_finer_than_four():
+    rng = np.random.default_rng(7)
+    w = _bf16(rng.normal(0, 0.02, (4, 128)))
+    wf = quant._bf16_to_f32(w).astype(np.float64)
+    err = {n: np.abs(quant.dequantize(*quant.quantize(w, n)) - wf).max() for n in (4, 8)}
+    # 255 levels instead of 15 over the same range: the step is 17x finer
+    assert err[8] < err[4] / 8
