@@ -89,11 +89,17 @@ constexpr int E_BYTES = 32 * EP * 4;      // 32 tokens
 constexpr int EPH = 136;                  // pitch (halves) of the fp16 staging tile (q|k|v heads)
 constexpr int EH_BYTES = 32 * EPH * 2;
 constexpr int SMEM_BUDGET = 227 * 1024;
+// 1: the persistent GEMM runs on CTA pairs (tcgen05.mma.cta_group::2) wherever the tiles allow
+#ifndef QW_GEMM_PAIR
+#define QW_GEMM_PAIR 1
+#endif
 
-template <int BN, int EPI, int NWG>  // NWG: epilogue warpgroups
+// NWG: epilogue warpgroups; BSPLIT: CTAs sharing the B tile (2 for the CTA-pair MMA, each
+// CTA holding BN / 2 of its rows)
+template <int BN, int EPI, int NWG, int BSPLIT = 1>
 struct GemmCfg {
     static constexpr int A_BYTES = BM * BK * 2;  // 16 KB
-    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int B_BYTES = BN / BSPLIT * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int NBUF = (2 * BN <= 512) ? 2 : 1;
     static constexpr int TMEM_COLS = NBUF * BN < 32 ? 32 : NBUF * BN;
@@ -300,11 +306,18 @@ __device__ __forceinline__ void load_norm_weights(const GemmKParams& p, float* n
 
 // =======================================================================================
 // Persistent kernel: CTA b processes tiles u = b, b + gridDim.x, ...
+// PAIR: clusters of two CTAs on a pair of SMs process 256-row tiles with the CTA-pair MMA
+// (tcgen05.mma.cta_group::2, M = 256): CTA rank r holds weight rows [128 r, 128 r + 128) and
+// token rows [r BN / 2, (r + 1) BN / 2) of each stage, so each SM loads and keeps half of the
+// token tile; the leader (rank 0) issues the MMAs into both CTAs' tensor memory, and each
+// CTA's epilogue reads its own 128 rows. The leader's stage barriers count both CTAs' copies;
+// its MMA completions are multicast to both CTAs; the peer's epilogue frees accumulators by
+// arriving on the leader's barriers.
 // =======================================================================================
-template <int BN, int EPI>
+template <int BN, int EPI, bool PAIR>
 __global__ void __launch_bounds__(GEMM_TC_THREADS, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmKParams p) {
-    using C = GemmCfg<BN, EPI, 2>;
+    using C = GemmCfg<BN, EPI, 2, PAIR ? 2 : 1>;
     static_assert(C::NBUF == 2, "one accumulator buffer per epilogue warpgroup");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -326,6 +339,14 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1)
     volatile int* ep_fail = reinterpret_cast<volatile int*>(tmem_slot + 2) + wg;  // [2]
 
     const int nk = p.K / BK;
+    const int rank = PAIR ? (int)cluster_rank() : 0;
+    const int pid = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;  // CTA (pair) index
+    const int npid = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+    const int tiles_mp = PAIR ? p.tiles_m / 2 : p.tiles_m;  // tile rows of 256 (pair) or 128
+    // stage barriers the copies complete on: the leader's for a pair
+    auto full_bar = [&](int s) -> uint32_t {
+        return PAIR ? mapa_shared(smem_u32(full + s), 0u) : smem_u32(full + s);
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
@@ -334,7 +355,7 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(accf + b), 1);
-            mbar_init(smem_u32(acce + b), 4);  // one arrival per epilogue warp
+            mbar_init(smem_u32(acce + b), PAIR ? 8 : 4);  // one arrival per epilogue warp (of both CTAs)
         }
         *abort_flag = 0;
         ep_fail[0] = 0;
@@ -347,53 +368,71 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1)
         tma_prefetch_desc(&tmB);
     }
     if (warp == 9) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                     "r"(C::TMEM_COLS)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        if (PAIR) {  // one warp of each CTA of the pair, collectively
+            asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                         "r"(C::TMEM_COLS)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+        } else {
+            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                         "r"(C::TMEM_COLS)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        }
     }
     if (EPI == EPI_QKV_HEADS && threadIdx.x < 128) load_norm_weights(p, nws);  // weights: before the wait
     tc_fence_before();
     __syncthreads();
+    if (PAIR) cluster_sync_all();  // the peer's copies signal the leader's barriers: both initialised
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     pdl_launch();
 
+    // tm: 128-row weight tile of this CTA; tn: token tile
     auto tile_of = [&](int u, int& tm, int& tn) {
-        tm = u % p.tiles_m;
-        tn = u / p.tiles_m;
+        tm = PAIR ? 2 * (u % tiles_mp) + rank : u % tiles_mp;
+        tn = u / tiles_mp;
     };
+    const int b_off = PAIR ? rank * (BN / 2) : 0;  // this CTA's token rows within a tile
 
     if (warp == 8) {
         // ---------------- TMA producer ----------------
         if (lane == 0) {
             // weight tiles of the first ring stages before the dependency wait
+            // the leader's stage barrier expects the bytes of both CTAs' copies
+            constexpr uint32_t kStageTx = (PAIR ? 2 : 1) * C::STAGE_BYTES;
+            auto load = [&](uint32_t dst, const CUtensorMap* map, int s, int x, int y) {
+                if (PAIR)
+                    tma_load_2d_pair(dst, map, full_bar(s), x, y);
+                else
+                    tma_load_2d(dst, map, full_bar(s), x, y);
+            };
             int pre = 0;
             {
-                int u = blockIdx.x, kb = 0;
+                int u = pid, kb = 0;
                 while (pre < C::STAGES && u < p.units) {
                     int tm, tn;
                     tile_of(u, tm, tn);
                     const uint32_t st = smem_u32(smem + pre * C::STAGE_BYTES);
-                    mbar_expect_tx(smem_u32(full + pre), C::STAGE_BYTES);
-                    tma_load_2d(st, &tmA, smem_u32(full + pre), kb * BK, p.a_row0 + tm * BM);
+                    if (rank == 0) mbar_expect_tx(smem_u32(full + pre), kStageTx);
+                    load(st, &tmA, pre, kb * BK, p.a_row0 + tm * BM);
                     ++pre;
                     if (++kb == nk) {
                         kb = 0;
-                        u += gridDim.x;
+                        u += npid;
                     }
                 }
             }
             pdl_wait();
             uint32_t g = 0;
-            for (int u = blockIdx.x; u < p.units && !*abort_flag; u += gridDim.x) {
+            for (int u = pid; u < p.units && !*abort_flag; u += npid) {
                 int tm, tn;
                 tile_of(u, tm, tn);
                 for (int kb = 0; kb < nk; ++kb, ++g) {
                     const int s = g % C::STAGES;
                     const uint32_t st = smem_u32(smem + s * C::STAGE_BYTES);
                     if ((int)g < pre) {  // weights already in flight
-                        tma_load_2d(st + C::A_BYTES, &tmB, smem_u32(full + s), kb * BK, p.b_row0 + tn * BN);
+                        load(st + C::A_BYTES, &tmB, s, kb * BK, p.b_row0 + tn * BN + b_off);
                         continue;
                     }
                     const uint32_t ph = (g / C::STAGES) & 1u;
@@ -401,19 +440,19 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1)
                         *abort_flag = 1;
                         break;
                     }
-                    mbar_expect_tx(smem_u32(full + s), C::STAGE_BYTES);
-                    tma_load_2d(st, &tmA, smem_u32(full + s), kb * BK, p.a_row0 + tm * BM);
-                    tma_load_2d(st + C::A_BYTES, &tmB, smem_u32(full + s), kb * BK, p.b_row0 + tn * BN);
+                    if (rank == 0) mbar_expect_tx(smem_u32(full + s), kStageTx);
+                    load(st, &tmA, s, kb * BK, p.a_row0 + tm * BM);
+                    load(st + C::A_BYTES, &tmB, s, kb * BK, p.b_row0 + tn * BN + b_off);
                 }
             }
         }
     } else if (warp == 9) {
-        // ---------------- MMA issuer ----------------
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_f16(BM, BN);
+        // ---------------- MMA issuer (the leader of a pair) ----------------
+        if (lane == 0 && rank == 0) {
+            constexpr uint32_t idesc = idesc_f16(PAIR ? 2 * BM : BM, BN);
             uint32_t g = 0;
             int i = 0;
-            for (int u = blockIdx.x; u < p.units && !*abort_flag; u += gridDim.x, ++i) {
+            for (int u = pid; u < p.units && !*abort_flag; u += npid, ++i) {
                 const int buf = i % C::NBUF;
                 const uint32_t use = (uint32_t)(i / C::NBUF);
                 if (!mbar_wait(smem_u32(acce + buf), use & 1u, abort_flag)) {
@@ -436,12 +475,23 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1)
                     const uint64_t ad = sw128_desc(st);
                     const uint64_t bd = sw128_desc(st + C::A_BYTES);
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k)
-                        umma_f16(d, ad + 2 * k, bd + 2 * k, idesc, (kb > 0 || k > 0) ? 1u : 0u);
-                    umma_commit(smem_u32(empty + s));  // frees the stage once these MMAs finish
+                    for (int k = 0; k < BK / 16; ++k) {
+                        if (PAIR)
+                            umma_f16_pair(d, ad + 2 * k, bd + 2 * k, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+                        else
+                            umma_f16(d, ad + 2 * k, bd + 2 * k, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+                    }
+                    // frees the stage (in both CTAs of a pair) once these MMAs finish
+                    if (PAIR)
+                        umma_commit_pair(smem_u32(empty + s));
+                    else
+                        umma_commit(smem_u32(empty + s));
                 }
                 if (!ok) break;
-                umma_commit(smem_u32(accf + buf));
+                if (PAIR)
+                    umma_commit_pair(smem_u32(accf + buf));
+                else
+                    umma_commit(smem_u32(accf + buf));
             }
         }
     } else {
@@ -450,16 +500,23 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1)
         const int ew = warp & 3;  // warp within the warpgroup
         // hand buffer (i2 % NBUF) to the MMA warp for this CTA's i2-th tile
         auto prepare = [&](int i2) {
-            const int u2 = blockIdx.x + i2 * gridDim.x;
+            const int u2 = pid + i2 * npid;
             if (u2 >= p.units) return;
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(acce + (i2 % C::NBUF))) : "memory");
+            if (lane == 0) {
+                const uint32_t bar = smem_u32(acce + (i2 % C::NBUF));
+                if (PAIR)  // the leader's MMA waits for both CTAs' epilogues
+                    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(mapa_shared(bar, 0u))
+                                 : "memory");
+                else
+                    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+            }
         };
         prepare(wg);  // nothing to read: before the wait
         pdl_wait();
         int i = wg;
-        for (int u = blockIdx.x + wg * gridDim.x; u < p.units; u += 2 * gridDim.x, i += 2) {
+        for (int u = pid + wg * npid; u < p.units; u += 2 * npid, i += 2) {
             int tm, tn;
             tile_of(u, tm, tn);
             const int buf = i % C::NBUF;
@@ -547,10 +604,15 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1)
     tc_fence_before();
     __syncthreads();
     if (*abort_flag && threadIdx.x == 0) atomicOr(p.status, QW_DEV_TIMEOUT);
+    if (PAIR) cluster_sync_all();  // no copy, MMA or arrival of the pair still targets this CTA
     if (warp == 9) {
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS)
-                     : "memory");
+        if (PAIR)
+            asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS)
+                         : "memory");
+        else
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::TMEM_COLS)
+                         : "memory");
     }
 }
 
@@ -838,8 +900,10 @@ template <int BN, int EPI>
 cudaError_t gemm_go(const LaunchCtx& c, const GemmArgs& a, int bn_idx) {
     using CC = GemmCfg<BN, EPI, 1>;  // cluster split-K kernel
     using CT = GemmCfg<BN, EPI, 2>;  // persistent kernel
-    static_assert(CC::SMEM <= SMEM_BUDGET && CT::SMEM <= SMEM_BUDGET, "shared memory budget");
-    static_assert(CC::STAGES >= 3 && CT::STAGES >= 3, "pipeline depth");
+    using CP = GemmCfg<BN, EPI, 2, 2>;  // persistent kernel on CTA pairs
+    static_assert(CC::SMEM <= SMEM_BUDGET && CT::SMEM <= SMEM_BUDGET && CP::SMEM <= SMEM_BUDGET,
+                  "shared memory budget");
+    static_assert(CC::STAGES >= 3 && CT::STAGES >= 3 && CP::STAGES >= 3, "pipeline depth");
     GemmKParams p;
     fill_params<BN, EPI>(p, a);
     const int tiles = p.tiles_m * p.tiles_n;
@@ -884,17 +948,38 @@ cudaError_t gemm_go(const LaunchCtx& c, const GemmArgs& a, int bn_idx) {
             return cudaLaunchKernelEx(&cfg, k_gemm_cl<BN, EPI>, *a.tmA, a.tmB[bn_idx], p);
         }
     }
-    static bool done = false;
-    cudaError_t e = set_smem(k_gemm_tc<BN, EPI>, CT::SMEM, done);
-    if (e != cudaSuccess) return e;
     p.splits = 1;
+    if constexpr (QW_GEMM_PAIR && BN >= 128 && EPI != EPI_ARGMAX) {
+        if (p.tiles_m % 2 == 0 && sms >= 2) {
+            // 256-row tiles on CTA pairs; each CTA loads half of the token tile (map bn_idx - 1
+            // has boxes of BN / 2 rows)
+            static bool done_p = false;
+            cudaError_t e = set_smem(k_gemm_tc<BN, EPI, true>, CP::SMEM, done_p);
+            if (e != cudaSuccess) return e;
+            p.units = tiles / 2;
+            attr[na].id = cudaLaunchAttributeClusterDimension;
+            attr[na].val.clusterDim.x = 2;
+            attr[na].val.clusterDim.y = 1;
+            attr[na].val.clusterDim.z = 1;
+            ++na;
+            cfg.gridDim = dim3(2 * std::min(p.units, sms / 2));
+            cfg.blockDim = dim3(GEMM_TC_THREADS);
+            cfg.dynamicSmemBytes = CP::SMEM;
+            cfg.attrs = attr;
+            cfg.numAttrs = na;
+            return cudaLaunchKernelEx(&cfg, k_gemm_tc<BN, EPI, true>, *a.tmA, a.tmB[bn_idx - 1], p);
+        }
+    }
+    static bool done = false;
+    cudaError_t e = set_smem(k_gemm_tc<BN, EPI, false>, CT::SMEM, done);
+    if (e != cudaSuccess) return e;
     p.units = tiles;
     cfg.gridDim = dim3(std::min(tiles, sms));
     cfg.blockDim = dim3(GEMM_TC_THREADS);
     cfg.dynamicSmemBytes = CT::SMEM;
     cfg.attrs = attr;
     cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, k_gemm_tc<BN, EPI>, *a.tmA, a.tmB[bn_idx], p);
+    return cudaLaunchKernelEx(&cfg, k_gemm_tc<BN, EPI, false>, *a.tmA, a.tmB[bn_idx], p);
 }
 
 template <int EPI>
