@@ -284,10 +284,11 @@ __device__ void epi_silu(const GemmKParams& p, const float* E, int tok0, int nto
     for (int k = 0; k < 4; ++k) {
         const float4 g = *reinterpret_cast<const float4*>(row + 16 * q + 4 * k);
         const float4 u = *reinterpret_cast<const float4*>(row + 64 + 16 * q + 4 * k);
-        v[4 * k] = g.x / (1.0f + expf(-g.x)) * u.x;
-        v[4 * k + 1] = g.y / (1.0f + expf(-g.y)) * u.y;
-        v[4 * k + 2] = g.z / (1.0f + expf(-g.z)) * u.z;
-        v[4 * k + 3] = g.w / (1.0f + expf(-g.w)) * u.w;
+        // fast exponential and division: their fp32 error is far below the fp16 rounding of act
+        v[4 * k] = __fdividef(g.x, 1.0f + __expf(-g.x)) * u.x;
+        v[4 * k + 1] = __fdividef(g.y, 1.0f + __expf(-g.y)) * u.y;
+        v[4 * k + 2] = __fdividef(g.z, 1.0f + __expf(-g.z)) * u.z;
+        v[4 * k + 3] = __fdividef(g.w, 1.0f + __expf(-g.w)) * u.w;
     }
     store16h(p.out_h + (size_t)(tok0 + t) * p.ld_out + tile * 64 + 16 * q, v);
 }
@@ -539,13 +540,29 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1)
             const int fl = ew * 32 + lane;                             // tile row of this thread
             const uint32_t trow = tmem + buf * BN + ((uint32_t)(ew * 32) << 16);
             const bool rope = (EPI == EPI_QKV_HEADS) && tm < p.n_heads + p.n_kv;
+            // q|k|v and gate/up (K = 1024: one tile of MMA time per epilogue): the next chunk's
+            // columns are read from tensor memory while this chunk is processed, and the
+            // accumulator is freed as soon as its last columns have landed in registers
+            constexpr bool kPipe = (EPI == EPI_QKV_HEADS || EPI == EPI_SILU_MUL);
+            uint32_t rnext[kPipe ? 32 : 1];
+            if (kPipe) {
+                TMEM_LD32(trow, rnext);
+                tmem_wait_ld();
+                if (ncols <= 32) prepare(i + 2);
+            }
             for (int c0 = 0; c0 < ncols; c0 += 32) {
                 uint32_t r[32];
-                TMEM_LD32(trow + c0, r);
                 RopeRegs rr;  // this chunk's RoPE rows, in flight during the staging below
-                if (rope) load_rope(p, tpos, c0, min(32, p.T - (n0 + c0)), rr);
-                tmem_wait_ld();
-                if (c0 + 32 >= ncols) prepare(i + 2);  // this buffer's next tile
+                if (kPipe) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) r[j] = rnext[j];
+                    if (c0 + 32 < ncols) TMEM_LD32(trow + c0 + 32, rnext);
+                    if (rope) load_rope(p, tpos, c0, min(32, p.T - (n0 + c0)), rr);
+                } else {
+                    TMEM_LD32(trow + c0, r);
+                    tmem_wait_ld();
+                    if (c0 + 32 >= ncols) prepare(i + 2);  // this buffer's next tile
+                }
                 if (EPI == EPI_QKV_HEADS || EPI == EPI_SILU_MUL) {
                     if (EPI == EPI_QKV_HEADS) {
                         f16* EH = reinterpret_cast<f16*>(E);
@@ -561,6 +578,10 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1)
                         epi_heads(p, reinterpret_cast<const f16*>(E), nws, tdst, rr, n0 + c0, c0, ntok, tm);
                     } else {
                         epi_silu(p, E, n0 + c0, ntok, tm);
+                    }
+                    if (c0 + 32 < ncols) {
+                        tmem_wait_ld();
+                        if (c0 + 64 >= ncols) prepare(i + 2);  // all columns read: this buffer's next tile
                     }
                     named_bar_epi();  // E is refilled by the next chunk
                 } else if (EPI == EPI_RESID_F32) {
