@@ -540,24 +540,31 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1)
             const int fl = ew * 32 + lane;                             // tile row of this thread
             const uint32_t trow = tmem + buf * BN + ((uint32_t)(ew * 32) << 16);
             const bool rope = (EPI == EPI_QKV_HEADS) && tm < p.n_heads + p.n_kv;
-            // q|k|v and gate/up (K = 1024: one tile of MMA time per epilogue): the next chunk's
-            // columns are read from tensor memory while this chunk is processed, and the
-            // accumulator is freed as soon as its last columns have landed in registers
-            constexpr bool kPipe = (EPI == EPI_QKV_HEADS || EPI == EPI_SILU_MUL);
+            // gate/up (K = 1024: one tile of MMA time per epilogue): the next chunk's columns are
+            // read from tensor memory while this chunk is processed, and the accumulator is
+            // freed as soon as its last columns have landed in registers. q|k|v instead requests
+            // the next chunk's RoPE rows (L2-resident table) one chunk ahead (registers allow
+            // one of the two).
+            constexpr bool kPipe = (EPI == EPI_SILU_MUL);
             uint32_t rnext[kPipe ? 32 : 1];
+            RopeRegs rrnext;
             if (kPipe) {
                 TMEM_LD32(trow, rnext);
                 tmem_wait_ld();
                 if (ncols <= 32) prepare(i + 2);
             }
+            if (rope) load_rope(p, tpos, 0, min(32, p.T - n0), rrnext);
             for (int c0 = 0; c0 < ncols; c0 += 32) {
                 uint32_t r[32];
-                RopeRegs rr;  // this chunk's RoPE rows, in flight during the staging below
+                RopeRegs rr;  // this chunk's RoPE rows
+                if (rope) {
+                    rr = rrnext;
+                    if (c0 + 32 < ncols) load_rope(p, tpos, c0 + 32, min(32, p.T - (n0 + c0 + 32)), rrnext);
+                }
                 if (kPipe) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) r[j] = rnext[j];
                     if (c0 + 32 < ncols) TMEM_LD32(trow + c0 + 32, rnext);
-                    if (rope) load_rope(p, tpos, c0, min(32, p.T - (n0 + c0)), rr);
                 } else {
                     TMEM_LD32(trow + c0, r);
                     tmem_wait_ld();
@@ -579,7 +586,7 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1)
                     } else {
                         epi_silu(p, E, n0 + c0, ntok, tm);
                     }
-                    if (c0 + 32 < ncols) {
+                    if (kPipe && c0 + 32 < ncols) {
                         tmem_wait_ld();
                         if (c0 + 64 >= ncols) prepare(i + 2);  // all columns read: this buffer's next tile
                     }
