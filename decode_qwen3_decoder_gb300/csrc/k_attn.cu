@@ -1143,11 +1143,12 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_attn_prefill_tc(const __grid_
             TMEM_LD32(lane_base + st * FA_BK, xa);
             TMEM_LD32(lane_base + st * FA_BK + 32, xb);
             tmem_wait_ld();
+            // raw scores q.k; the scale (> 0) is applied inside the exponent below
             float s[FA_BK];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-                s[i] = __uint_as_float(xa[i]) * p.scale_log2;
-                s[32 + i] = __uint_as_float(xb[i]) * p.scale_log2;
+                s[i] = __uint_as_float(xa[i]);
+                s[32 + i] = __uint_as_float(xb[i]);
             }
             // mask keys after the query or past the sequence, on the tiles that hold any
             if (k0 + FA_BK - 1 > L0 + q0 || k0 + FA_BK > kend) {
@@ -1155,9 +1156,14 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_attn_prefill_tc(const __grid_
                 for (int i = 0; i < FA_BK; ++i)
                     if (k0 + i > qpos || k0 + i >= kend) s[i] = -INFINITY;
             }
-            float mt = s[0];
+            // row max through 8 independent partial maxima (short dependency chains)
+            float pm[8];
 #pragma unroll
-            for (int i = 1; i < FA_BK; ++i) mt = fmaxf(mt, s[i]);
+            for (int u = 0; u < 8; ++u) pm[u] = s[u];
+#pragma unroll
+            for (int i = 8; i < FA_BK; ++i) pm[i & 7] = fmaxf(pm[i & 7], s[i]);
+            const float mt = fmaxf(fmaxf(fmaxf(pm[0], pm[1]), fmaxf(pm[2], pm[3])),
+                                   fmaxf(fmaxf(pm[4], pm[5]), fmaxf(pm[6], pm[7]))) * p.scale_log2;
             const bool move = mt > m + FA_RESCALE_LOG2;  // always on the first tile (m = -inf)
             const float mn = move ? mt : m;
             const float alpha = move ? ex2_approx(m - mn) : 1.f;  // 2^-inf = 0 on the first tile
@@ -1178,15 +1184,16 @@ __global__ void __launch_bounds__(FA_THREADS, 2) k_attn_prefill_tc(const __grid_
                     TMEM_ST32(lane_base + FA_O + c * 32, x);
                 }
             }
-            float ls = 0.f;
+            float lp[4] = {0.f, 0.f, 0.f, 0.f};  // partial sums (short dependency chains)
             uint32_t h[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-                const float e0 = ex2_approx(s[2 * i] - mn), e1 = ex2_approx(s[2 * i + 1] - mn);
-                ls += e0 + e1;
+                const float e0 = ex2_approx(fmaf(s[2 * i], p.scale_log2, -mn));
+                const float e1 = ex2_approx(fmaf(s[2 * i + 1], p.scale_log2, -mn));
+                lp[i & 3] += e0 + e1;
                 h[i] = pack_h2(e0, e1);
             }
-            l = l * alpha + ls;
+            l = l * alpha + ((lp[0] + lp[1]) + (lp[2] + lp[3]));
             m = mn;
             TMEM_ST32(lane_base + st * FA_BK, h);
             if (j == n_kt - 1 && k0 + FA_BK > kend) {

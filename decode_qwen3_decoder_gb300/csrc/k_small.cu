@@ -104,7 +104,28 @@ __global__ void __launch_bounds__(256) k_rmsnorm(const float* __restrict__ x, co
     pdl_wait();
     const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
-    if (r < n_rows) {
+    if (r < n_rows && hidden == 1024) {
+        // the model's width: the row's 8 float4 per lane are requested together and kept in
+        // registers (one round trip, no second read)
+        const float* xr = x + (size_t)(rows ? rows[r] : r) * 1024;
+        float4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) v[u] = *reinterpret_cast<const float4*>(xr + lane * 4 + u * 128);
+        float ss = 0.f;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) ss += v[u].x * v[u].x + v[u].y * v[u].y + v[u].z * v[u].z + v[u].w * v[u].w;
+        const float rs = rsqrtf(warp_sum(ss) / 1024.f + eps);
+        f16* hr = h + (size_t)r * 1024;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int k = lane * 4 + u * 128;
+            const uint2 wb = *reinterpret_cast<const uint2*>(w + k);
+            uint2 o;
+            o.x = pack_h2(v[u].x * rs * bf_lo(wb.x), v[u].y * rs * bf_hi(wb.x));
+            o.y = pack_h2(v[u].z * rs * bf_lo(wb.y), v[u].w * rs * bf_hi(wb.y));
+            *reinterpret_cast<uint2*>(hr + k) = o;
+        }
+    } else if (r < n_rows) {
         const float* xr = x + (size_t)(rows ? rows[r] : r) * hidden;
         float ss = 0.f;
         for (int k = lane * 4; k < hidden; k += 128) {
