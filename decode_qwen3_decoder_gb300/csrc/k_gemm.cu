@@ -356,7 +356,7 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(smem_u32(accf + b), 1);
-            mbar_init(smem_u32(acce + b), PAIR ? 8 : 4);  // one arrival per epilogue warp (of both CTAs)
+            mbar_init(smem_u32(acce + b), PAIR ? 16 : 8);  // one arrival per epilogue warp (of both CTAs)
         }
         *abort_flag = 0;
         ep_fail[0] = 0;
@@ -497,7 +497,9 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1)
         }
     } else {
         // ---------------- epilogue warpgroups: warp w reads TMEM lanes 32 (w % 4) .. ----------
-        // warpgroup wg takes this CTA's tiles i = wg, wg + 2, ... in accumulator buffer wg
+        // both warpgroups take every tile, warpgroup wg its token columns [wg BN / 2, (wg + 1)
+        // BN / 2): a tile's accumulator is read in half the time, so it is back with the MMA
+        // warp well within the next tile's MMAs
         const int ew = warp & 3;  // warp within the warpgroup
         // hand buffer (i2 % NBUF) to the MMA warp for this CTA's i2-th tile
         auto prepare = [&](int i2) {
@@ -514,17 +516,19 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1)
                     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
             }
         };
-        prepare(wg);  // nothing to read: before the wait
+        prepare(0);  // both buffers start free: nothing to read, before the wait
+        prepare(1);
         pdl_wait();
-        int i = wg;
-        for (int u = pid + wg * npid; u < p.units; u += 2 * npid, i += 2) {
+        int i = 0;
+        const int c_lo = wg * (BN / 2);  // this warpgroup's first token column of a tile
+        for (int u = pid; u < p.units; u += npid, ++i) {
             int tm, tn;
             tile_of(u, tm, tn);
             const int buf = i % C::NBUF;
             const uint32_t use = (uint32_t)(i / C::NBUF);
             if (EPI == EPI_QKV_HEADS) fill_tok_meta<BN>(p, tn * BN, tm, tpos, tdst);  // overlaps the MMAs
             float xr[32];  // EPI_RESID_F32: residual rows of the current 32 tokens
-            if (EPI == EPI_RESID_F32) load_resid(p, tn * BN, tm * BM + ew * 32 + lane, xr);
+            if (EPI == EPI_RESID_F32) load_resid(p, tn * BN + c_lo, tm * BM + ew * 32 + lane, xr);
             // all four epilogue warps take the same decision (they meet at named barriers)
             if (!mbar_wait(smem_u32(accf + buf), use & 1u, abort_flag)) *ep_fail = 1;
             named_bar_epi();
@@ -537,6 +541,7 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1)
             }
             const int n0 = tn * BN;
             const int ncols = min(BN, ((p.T - n0) + 31) / 32 * 32);  // token columns holding data
+            const int c_hi = min(c_lo + BN / 2, ncols);                // this warpgroup's columns end
             const int fl = ew * 32 + lane;                             // tile row of this thread
             const uint32_t trow = tmem + buf * BN + ((uint32_t)(ew * 32) << 16);
             const bool rope = (EPI == EPI_QKV_HEADS) && tm < p.n_heads + p.n_kv;
@@ -548,27 +553,28 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1)
             constexpr bool kPipe = (EPI == EPI_SILU_MUL);
             uint32_t rnext[kPipe ? 32 : 1];
             RopeRegs rrnext;
-            if (kPipe) {
-                TMEM_LD32(trow, rnext);
+            if (c_hi <= c_lo) prepare(i + 2);  // no columns of this tile here: free it at once
+            if (kPipe && c_lo < c_hi) {
+                TMEM_LD32(trow + c_lo, rnext);
                 tmem_wait_ld();
-                if (ncols <= 32) prepare(i + 2);
+                if (c_hi - c_lo <= 32) prepare(i + 2);
             }
-            if (rope) load_rope(p, tpos, 0, min(32, p.T - n0), rrnext);
-            for (int c0 = 0; c0 < ncols; c0 += 32) {
+            if (rope && c_lo < c_hi) load_rope(p, tpos, c_lo, min(32, p.T - (n0 + c_lo)), rrnext);
+            for (int c0 = c_lo; c0 < c_hi; c0 += 32) {
                 uint32_t r[32];
                 RopeRegs rr;  // this chunk's RoPE rows
                 if (rope) {
                     rr = rrnext;
-                    if (c0 + 32 < ncols) load_rope(p, tpos, c0 + 32, min(32, p.T - (n0 + c0 + 32)), rrnext);
+                    if (c0 + 32 < c_hi) load_rope(p, tpos, c0 + 32, min(32, p.T - (n0 + c0 + 32)), rrnext);
                 }
                 if (kPipe) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) r[j] = rnext[j];
-                    if (c0 + 32 < ncols) TMEM_LD32(trow + c0 + 32, rnext);
+                    if (c0 + 32 < c_hi) TMEM_LD32(trow + c0 + 32, rnext);
                 } else {
                     TMEM_LD32(trow + c0, r);
                     tmem_wait_ld();
-                    if (c0 + 32 >= ncols) prepare(i + 2);  // this buffer's next tile
+                    if (c0 + 32 >= c_hi) prepare(i + 2);  // this buffer's next tile
                 }
                 if (EPI == EPI_QKV_HEADS || EPI == EPI_SILU_MUL) {
                     if (EPI == EPI_QKV_HEADS) {
@@ -586,15 +592,15 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1)
                     } else {
                         epi_silu(p, E, n0 + c0, ntok, tm);
                     }
-                    if (kPipe && c0 + 32 < ncols) {
+                    if (kPipe && c0 + 32 < c_hi) {
                         tmem_wait_ld();
-                        if (c0 + 64 >= ncols) prepare(i + 2);  // all columns read: this buffer's next tile
+                        if (c0 + 64 >= c_hi) prepare(i + 2);  // all columns read: this buffer's next tile
                     }
                     named_bar_epi();  // E is refilled by the next chunk
                 } else if (EPI == EPI_RESID_F32) {
                     const int f = tm * BM + fl;
                     float xn[32];
-                    if (c0 + 32 < ncols) load_resid(p, n0 + c0 + 32, f, xn);
+                    if (c0 + 32 < c_hi) load_resid(p, n0 + c0 + 32, f, xn);
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const int tok = n0 + c0 + j;
@@ -616,7 +622,7 @@ __global__ void __launch_bounds__(GEMM_TC_THREADS, 1)
             }
             if (EPI == EPI_ARGMAX) {
                 named_bar_epi();
-                for (int cc = epi_tid(); cc < ncols; cc += 128) {
+                for (int cc = c_lo + epi_tid(); cc < c_hi; cc += 128) {
                     const int tok = n0 + cc;
                     if (tok < p.T) {
                         unsigned long long bb = sbest[cc];
