@@ -142,7 +142,8 @@ struct GemmKParams {
 // ---- epilogues over a staged [token][EP] fp32 tile (128 epilogue threads) -------------
 
 // Token metadata of a q|k|v tile, filled while its MMAs run: tpos[c] = position of token
-// n0 + c, tdst[c] = its KV slot row page * 16 + pos % 16 (-1: no page; reported).
+// n0 + c, tdst[c] = its KV slot row page * 16 + pos % 16 (-1: no page; reported), both
+// computed once per step by the step's first kernel.
 template <int BN>
 __device__ void fill_tok_meta(const GemmKParams& p, int n0, int hd, int* tpos, int* tdst) {
     for (int c = epi_tid(); c < BN; c += 128) {
@@ -150,14 +151,8 @@ __device__ void fill_tok_meta(const GemmKParams& p, int n0, int hd, int* tpos, i
         int pos = 0, dst = -1;
         if (tok < p.T) {
             pos = p.tv.pos[tok];
-            const int seq = p.tv.seq[tok];
-            const int pi = pos >> 4;
-            const int page = (pi < p.kv.max_pages_per_seq) ? p.kv.page_table[(size_t)seq * p.kv.max_pages_per_seq + pi] : -1;
-            if (page >= 0 && page < p.kv.n_pages) {
-                dst = page * 16 + (pos & 15);
-            } else if (hd >= p.n_heads) {
-                atomicOr(p.status, QW_DEV_BAD_POS);
-            }
+            dst = p.tv.slot[tok];
+            if (dst < 0 && hd >= p.n_heads) atomicOr(p.status, QW_DEV_BAD_POS);
             if (p.dbg_pos && hd == p.n_heads) {
                 p.dbg_pos[tok] = pos;
                 p.dbg_slot[tok] = dst;

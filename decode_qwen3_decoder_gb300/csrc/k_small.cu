@@ -79,8 +79,13 @@ __global__ void __launch_bounds__(256) k_step_begin(StepDesc sd, const int32_t* 
     }
     if (threadIdx.x == 0) {
         const int seq = sd.seq[b];
+        const int pos = kv.len[seq] + (t - sd.start[b]);
         tv.seq[t] = seq;
-        tv.pos[t] = kv.len[seq] + (t - sd.start[b]);
+        tv.pos[t] = pos;
+        // the token's KV slot, the same for every layer (kernels that append report a missing page)
+        const int pi = pos >> 4;
+        const int page = (pi < kv.max_pages_per_seq) ? kv.page_table[(size_t)seq * kv.max_pages_per_seq + pi] : -1;
+        tv.slot[t] = (page >= 0 && page < kv.n_pages) ? page * 16 + (pos & 15) : -1;
         if (t == sd.start[b + 1] - 1) tv.last[b] = t;
         if (bad) atomicOr(status, QW_DEV_BAD_TOKEN);
     }

@@ -44,6 +44,7 @@ struct TokView {
     int* seq;  // [T]
     int* pos;  // [T]
     int* last; // [B] row of each entry's last token
+    int* slot; // [T] KV slot row page * 16 + pos % 16 of the token (-1: no page reserved)
 };
 
 // ---------------------------------------------------------------------------------------

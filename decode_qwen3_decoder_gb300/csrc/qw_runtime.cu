@@ -89,7 +89,7 @@ static bool config_ok(const qw_config* c, std::string* why) {
 struct WsLayout {
     size_t wqkv, wo, wgu, wd, embed16, bqkv, bo, bg, bu, bd, norms, fnorm, rcos, rsin;
     size_t x, h, qkv, q, attn, act, part_o, part_ml, counters;
-    size_t tok_seq, tok_pos, last, best, status, gen_tok, gen_cur, gen_out, mk_sync;
+    size_t tok_seq, tok_pos, tok_slot, last, best, status, gen_tok, gen_cur, gen_out, mk_sync;
     size_t total;
     int part_T;
 };
@@ -132,6 +132,7 @@ static WsLayout layout_for(const qw_config& c) {
     L.counters = take((size_t)L.part_T * c.n_kv_heads * 4);
     L.tok_seq = take(T * 4);
     L.tok_pos = take(T * 4);
+    L.tok_slot = take(T * 4);
     L.last = take((size_t)c.max_batch * 4);
     L.best = take((size_t)c.max_batch * 8);
     L.status = take(4);
@@ -163,7 +164,7 @@ struct qw_model {
     const bf16* embed;
     float *rcos, *rsin, *x, *qkv, *part_o, *part_ml;
     f16 *h, *q, *attn, *act;
-    int *counters, *tok_seq, *tok_pos, *last, *status;
+    int *counters, *tok_seq, *tok_pos, *tok_slot, *last, *status;
     unsigned* mk_sync;
     int mk_grid;       // CTAs of the persistent decode kernel (0: not available)
     int mk_max_t;      // most tokens it takes
@@ -288,6 +289,7 @@ extern "C" qw_status qw_init_weights(const qw_config* cfg, const qw_weight_ptrs*
     m->counters = (int*)(b + L.counters);
     m->tok_seq = (int*)(b + L.tok_seq);
     m->tok_pos = (int*)(b + L.tok_pos);
+    m->tok_slot = (int*)(b + L.tok_slot);
     m->last = (int*)(b + L.last);
     m->best = (unsigned long long*)(b + L.best);
     m->status = (int*)(b + L.status);
@@ -827,7 +829,7 @@ static qw_status run_layers(qw_model* m, qw_kv* kv, const StepDesc& sd, bool pre
     const int T = n;
     const int D = c.hidden, I = c.inter, QD = c.n_heads * c.head_dim, d = c.head_dim;
     const KVView kvv = kv->view();
-    const TokView tv = {m->tok_seq + t0, m->tok_pos + t0, m->last};
+    const TokView tv = {m->tok_seq + t0, m->tok_pos + t0, m->last, m->tok_slot + t0};
     const bool small = sd.T <= kSmallT;
     const SplitPlan sp = plan_splits(m, T, max_keys);
     // small decode batches over long caches: separate QK-norm/RoPE/append, then the
@@ -976,7 +978,7 @@ static qw_status run_step(qw_model* m, qw_kv* kv, const StepDesc& sd, bool prefi
     const int T = sd.T, B = sd.B;
     const int D = c.hidden, I = c.inter, QD = c.n_heads * c.head_dim;
     const KVView kvv = kv->view();
-    TokView tv = {m->tok_seq, m->tok_pos, m->last};
+    TokView tv = {m->tok_seq, m->tok_pos, m->last, m->tok_slot};
     const bool dbg = allow_debug && m->dbg_hidden;
     const bool small = T <= kSmallT;
     if (!small && !prefill && T > m->L.part_T) return fail(QW_ERR_UNSUPPORTED, "decode batch beyond partial buffers");
