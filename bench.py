@@ -61,19 +61,19 @@ CONFIGS = {
 # DRAM bytes per launch of a kernel from one ncu capture (summaries under profiles/), reported
 # as roofline.traffic only while the kernel's source file is byte-identical to the capture's.
 NCU_TRAFFIC = {
-    (1, "gate_up+silu_mul(rmsnorm fused)"): (12606720, "decode_qwen3_decoder_gb300/csrc/k_small.cu",
-                                             "0eca842ea9e3d616dc7a649c7eefeedf777de9b09921357bd6f4f5fcf25f82c9"),
-    (1, "qkv_proj(rmsnorm fused)"): (8409856, "decode_qwen3_decoder_gb300/csrc/k_small.cu",
-                                     "0eca842ea9e3d616dc7a649c7eefeedf777de9b09921357bd6f4f5fcf25f82c9"),
-    (3, "gate_up+silu_mul"): (29389056 + 523264, "decode_qwen3_decoder_gb300/csrc/k_gemm.cu",
-                              "453fe4f107647e6c90c4e837a33290347795cddcaebe25046108888fe16f4382"),
-    (3, "qkv_proj+qk_norm+rope+kv_append"): (25540096 + 11586048, "decode_qwen3_decoder_gb300/csrc/k_gemm.cu",
-                                             "453fe4f107647e6c90c4e837a33290347795cddcaebe25046108888fe16f4382"),
+    (1, "gate_up+silu_mul(rmsnorm fused)"): (12606976, "decode_qwen3_decoder_gb300/csrc/k_small.cu",
+                                             "60ff501555a32c105747c8e175d3bbe27852b6a4931a769598a5ae541815842e"),
+    (1, "qkv_proj(rmsnorm fused)"): (8409344, "decode_qwen3_decoder_gb300/csrc/k_small.cu",
+                                     "60ff501555a32c105747c8e175d3bbe27852b6a4931a769598a5ae541815842e"),
+    (3, "gate_up+silu_mul"): (29395200 + 668160, "decode_qwen3_decoder_gb300/csrc/k_gemm.cu",
+                              "ac14bf4a7fabf4ebcb03ecc75dc46125c104e7ad15728ab9ed1e163b507579cc"),
+    (3, "qkv_proj+qk_norm+rope+kv_append"): (25560832 + 10699520, "decode_qwen3_decoder_gb300/csrc/k_gemm.cu",
+                                             "ac14bf4a7fabf4ebcb03ecc75dc46125c104e7ad15728ab9ed1e163b507579cc"),
     # batched decode attention: measured on 256-token caches (two 32-token launches, 35.83 MB
     # each, 1.064 x their algorithmic bytes) and scaled by the key count to one 64-token launch
     # of the full workload (285.2 MB algorithmic); the traffic grows with the keys read
     (2, "attention"): (303361426, "decode_qwen3_decoder_gb300/csrc/k_attn.cu",
-                       "61af91e223391560db436f3e9959056499064c92da6d764574cc549d568fe58c"),
+                       "0d66968b12b44735a08f408243699a895815c7cc6effd772c4a675a1e9d25935"),
 }
 
 
