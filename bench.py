@@ -27,6 +27,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -102,6 +103,14 @@ def whole_job_rate(units_per_rank_step: float, steps: int, world: int, ms_max: f
 
 def log(*a):
     print(*a, file=sys.stderr, flush=True)
+
+
+def step_stats(events):
+    """Median and 95th percentile (us) of the intervals between consecutive CUDA events
+    recorded on one stream (one interval per step)."""
+    d = sorted(events[i].elapsed_time(events[i + 1]) * 1e3 for i in range(len(events) - 1))
+    p95 = d[min(len(d) - 1, int(math.ceil(0.95 * len(d))) - 1)]
+    return {"median_us": round(statistics.median(d), 2), "p95_us": round(p95, 2), "n": len(d)}
 
 
 # ---------------------------------------------------------------------------------------
@@ -286,13 +295,14 @@ def run_ours(args, cfg, rank, world):
     for sq in seqs:
         qw.qw_kv_reserve(eng.kv, sq, P + ND, st)
     qw.qw_prefill(eng.model, eng.kv, seqs, [P] * B, d_prompt.data_ptr(), 0, d_cur.data_ptr(), st)
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(st)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(ND + 1)]
+    evs[0].record(st)
     for i in range(ND):
         qw.qw_decode_step(eng.model, eng.kv, seqs, d_cur.data_ptr(), 0, d_cur.data_ptr(), st)
-    b.record(st)
+        evs[i + 1].record(st)
     st.synchronize()
-    decode_us = a.elapsed_time(b) * 1e3 / ND
+    decode_us = evs[0].elapsed_time(evs[ND]) * 1e3 / ND
+    decode_stats = step_stats(evs)
 
     # ---- per-kernel timing with CUDA events around each launch of one kernel kind ----
     # (events bracket the launches inside the captured decode graphs; measured on the
@@ -360,6 +370,7 @@ def run_ours(args, cfg, rank, world):
                    "tokens_per_step": tokens_per_step, "parallelism": f"replicas x{world} (no collective)",
                    "l2": "weights (1.19 GB per decode step) exceed L2; no flush",
                    "decode_step_us": round(decode_us, 2),
+                   "decode_step_stats": decode_stats,
                    "decode_step_bytes": step_b,
                    "decode_step_hbm_frac": round(step_b / (decode_us * 1e-6) / 1e9 / hbm, 4)},
         "roofline": roofline,
@@ -539,11 +550,13 @@ def run_other(args, cfg, rank, world):
     barrier(world)
     launches[0] = 0
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    step_evs = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     with ClockSampler(gpu_uuid) as clk:
         torch.cuda.synchronize()
         e0.record(st)
-        for _ in range(args.steps):
+        for i in range(args.steps):
             one_step()
+            step_evs[i].record(st)
         e1.record(st)
         torch.cuda.synchronize()
     barrier(world)
@@ -551,6 +564,19 @@ def run_other(args, cfg, rank, world):
     value = whole_job_rate(units_per_step, args.steps, world, ms_max)
     if qw.qw_sync_status(eng.model, st) != 0:
         raise RuntimeError(f"device status in the timed region: {qw.qw_last_error()}")
+    if kind == "prefill":
+        step_lat = step_stats([e0] + step_evs)
+    else:
+        # decode-step latency, one interval per step (the same graphs, right after the timed region)
+        for sq in seqs:
+            qw.qw_kv_truncate(eng.kv, sq, int(lens[sq]), st)
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(ND + 1)]
+        evs[0].record(st)
+        for i in range(ND):
+            qw.qw_decode_step(eng.model, eng.kv, seqs, d_cur.data_ptr(), 0, d_cur.data_ptr(), st)
+            evs[i + 1].record(st)
+        st.synchronize()
+        step_lat = step_stats(evs)
 
     # per-kernel timing (events around each launch of a kind, one step after the timed region)
     L = s.n_layers
@@ -595,7 +621,8 @@ def run_other(args, cfg, rank, world):
         attn_pairs = sum(int(l) * (int(l) + 1) // 2 for l in lens)
         total_flops = L * sum(flops[k] for k in gemm_kinds) + flops[7] + L * attn_pairs * 4 * s.head_dim * s.n_heads
         extra = {"step_tflop": total_flops / 1e12,
-                 "step_tc_frac": round(total_flops / (ms_max / args.steps * 1e-3) / 1e12 / bf16_burst, 4)}
+                 "step_tc_frac": round(total_flops / (ms_max / args.steps * 1e-3) / 1e12 / bf16_burst, 4),
+                 "prefill_step_stats": step_lat}
     else:
         ctx = float(np.mean(lens)) + ND / 2
         kv_bytes = attn_bytes_layer(s, float(np.sum(lens)) + B * ND / 2)
@@ -605,11 +632,12 @@ def run_other(args, cfg, rank, world):
         dom = max(byts, key=lambda k: kinds[k]["per_step_us"])
         ach = byts[dom] / (kinds[dom]["avg_us"] * 1e-6) / 1e9
         roofline = {"bound": "hbm", "kernel": kinds[dom]["name"], "achieved": round(ach, 1), "peak": hbm,
-                    "peak_source": peak_src, "unit": "GB/s", "frac": round(ach / hbm, 4), "traffic": None,
+                    "peak_source": peak_src, "unit": "GB/s", "frac": round(ach / hbm, 4),
+                    "traffic": ncu_traffic(args.config, kinds[dom]["name"]),
                     "algorithmic_bytes_per_launch": byts[dom], "avg_launch_us": round(kinds[dom]["avg_us"], 2)}
         step_b = step_bytes(s, B, ctx)
         step_us = ms_max / args.steps / ND * 1e3
-        extra = {"decode_step_us": round(step_us, 2), "decode_step_bytes": step_b,
+        extra = {"decode_step_us": round(step_us, 2), "decode_step_stats": step_lat, "decode_step_bytes": step_b,
                  "decode_step_hbm_frac": round(step_b / (step_us * 1e-6) / 1e9 / hbm, 4),
                  "mean_cached_len": float(np.mean(lens))}
     out = {"metric": METRIC, "value": round(value, 2), "unit": cfg["unit"], "n_gpus": world, "steps": args.steps,
