@@ -58,3 +58,42 @@ def test_whole_job_rate():
     # 2 ranks x 65 tokens per step x 10 steps in at most 500 ms -> 2600 tok/s for the job
     assert bench.whole_job_rate(65, 10, 2, 500.0) == pytest.approx(2600.0)
     assert bench.whole_job_rate(65, 10, 1, 500.0) == pytest.approx(1300.0)
+
+
+class _Ev:
+    """Stand-in for a CUDA event: elapsed_time in ms between two recorded times."""
+
+    def __init__(self, t_ms):
+        self.t = t_ms
+
+    def elapsed_time(self, other):
+        return other.t - self.t
+
+
+def test_step_stats_median_and_nearest_rank_p95():
+    import bench
+    # 20 intervals: 18 of 0.5 ms, one of 0.4 ms, one of 2.0 ms
+    times = [0.0]
+    for d in [0.5] * 9 + [0.4] + [0.5] * 9 + [2.0]:
+        times.append(times[-1] + d)
+    st = bench.step_stats([_Ev(t) for t in times])
+    assert st["n"] == 20
+    assert st["median_us"] == pytest.approx(500.0)
+    assert st["p95_us"] == pytest.approx(500.0)  # nearest rank 19 of 20: the outlier is the 20th
+    times.append(times[-1] + 3.0)  # a 21st interval: rank ceil(0.95 * 21) = 20 -> 2.0 ms
+    assert bench.step_stats([_Ev(t) for t in times])["p95_us"] == pytest.approx(2000.0)
+
+
+def test_ncu_traffic_needs_the_captured_source():
+    import bench
+    # every entry names a tracked source; an unknown kernel or a stale hash gives no traffic
+    for (cfg, kernel), (nbytes, src, sha) in bench.NCU_TRAFFIC.items():
+        assert nbytes > 0 and len(sha) == 64
+    assert bench.ncu_traffic(1, "no such kernel") is None
+    key = next(iter(bench.NCU_TRAFFIC))
+    saved = bench.NCU_TRAFFIC[key]
+    try:
+        bench.NCU_TRAFFIC[key] = (saved[0], saved[1], "0" * 64)
+        assert bench.ncu_traffic(*key) is None
+    finally:
+        bench.NCU_TRAFFIC[key] = saved
