@@ -183,6 +183,39 @@ def test_error_paths_leave_state(one_block):
     assert qw.qw_sync_status(eng.model, eng.stream) == 0  # the word was cleared
 
 
+def test_degenerate_calls_are_rejected(one_block):
+    """Empty batches, empty prompts, repeated or unknown sequence ids and batches beyond
+    max_batch are refused on the host (QW_ERR_INVALID_ARG) before any launch, and leave the
+    cache untouched."""
+    import torch
+    run, _ = one_block
+    qw, eng = run.qw, run.eng
+    qw.qw_kv_reset(eng.kv, -1, eng.stream)
+    qw.qw_kv_reserve(eng.kv, 0, 32, eng.stream)
+    qw.qw_kv_reserve(eng.kv, 1, 32, eng.stream)
+    tok = torch.ones(64, dtype=torch.int32, device="cuda")
+    nxt = torch.zeros(32, dtype=torch.int32, device="cuda")
+    t, n = tok.data_ptr(), nxt.data_ptr()
+    calls = [
+        lambda: qw.qw_prefill(eng.model, eng.kv, [], [], t, 0, n, eng.stream),            # no sequence
+        lambda: qw.qw_prefill(eng.model, eng.kv, [0], [0], t, 0, n, eng.stream),          # empty prompt
+        lambda: qw.qw_prefill(eng.model, eng.kv, [0, 1], [2, 0], t, 0, n, eng.stream),   # one empty prompt
+        lambda: qw.qw_prefill(eng.model, eng.kv, [0, 0], [2, 2], t, 0, n, eng.stream),   # repeated id
+        lambda: qw.qw_prefill(eng.model, eng.kv, [10 ** 6], [2], t, 0, n, eng.stream),   # unknown id
+        lambda: qw.qw_prefill(eng.model, eng.kv, [-1], [2], t, 0, n, eng.stream),        # negative id
+        lambda: qw.qw_prefill(eng.model, eng.kv, list(range(17)), [1] * 17, t, 0, n, eng.stream),  # > max_batch
+        lambda: qw.qw_decode_step(eng.model, eng.kv, [], t, 0, n, eng.stream),           # no sequence
+        lambda: qw.qw_decode_step(eng.model, eng.kv, [1, 1], t, 0, n, eng.stream),       # repeated id
+        lambda: qw.qw_decode_step(eng.model, eng.kv, list(range(17)), t, 0, n, eng.stream),  # > max_batch
+    ]
+    for call in calls:
+        with pytest.raises(qw.QwError) as e:
+            call()
+        assert e.value.status == -1
+        assert qw.qw_kv_length(eng.kv, 0) == 0 and qw.qw_kv_length(eng.kv, 1) == 0
+    qw.qw_kv_reset(eng.kv, -1, eng.stream)
+
+
 @pytest.fixture(scope="module")
 def full_model(qw):
     eng = engine(qw, synth.QWEN3_0_6B, max_tokens=64, max_batch=8, max_context=256, kv_pages=64,
