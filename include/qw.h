@@ -42,7 +42,7 @@ typedef enum {
     QW_OK = 0,
     QW_ERR_INVALID_ARG = -1, /* a null/misaligned pointer, a size or id out of range          */
     QW_ERR_KV_FULL = -2,     /* not enough free pages, or a sequence past its reservation      */
-    QW_ERR_BAD_STATE = -3,   /* e.g. prefill into a sequence that already holds tokens        */
+    QW_ERR_BAD_STATE = -3,   /* e.g. generate into a non-empty sequence, quantize twice       */
     QW_ERR_CUDA = -4,        /* a CUDA runtime call failed (message has the CUDA error)        */
     QW_ERR_BAD_TOKEN = -5,   /* device status: a token id outside [0, vocab)                  */
     QW_ERR_TIMEOUT = -6,     /* device status: a bounded wait inside a kernel gave up          */
