@@ -1,34 +1,50 @@
 #!/usr/bin/env python3
 """Benchmark of the libqw decoder forward pass on GB300.
 
-Default workload (N=1): the 28-layer Qwen3-0.6B shape with seeded random bf16 weights,
-batch 1, a 5-token uniform-random prompt, prefill + 64 greedy decode steps. One bench step
-is one such generation (KV reset + reserve, prefill, 64 decode steps replayed from CUDA
-graphs, each step feeding its pick back on the device). ``value`` counts the generated
-tokens (65 per step: one from the prefill, one per decode step) per second of device
-time with inputs resident in HBM; ``e2e`` is the same metric through ``qw_generate`` from
-pinned host buffers (prompt copied in, picks copied out, every step).
+Default run (no --config): one JSON line whose headline is the 28-layer Qwen3-0.6B shape
+with seeded random bf16 weights, batch 1, a 5-token uniform-random prompt, prefill + 64
+greedy decode steps. One bench step is one such generation (KV reset + reserve, prefill, 64
+decode steps replayed from CUDA graphs, each step feeding its pick back on the device).
+``value`` counts the generated tokens (65 per step) per second of device time with inputs
+resident in HBM; ``e2e`` is the same metric through ``qw_generate`` from pinned host
+buffers (prompt copied in, picks copied out, every step). The same line carries one object
+per other workload, each timed the same way (K timed steps after W warm-up steps), with its
+own step-level roofline, ``e2e`` (host buffers, copies inside the timed region) and
+``cpu_baseline`` (the fp64 oracle on a bounded sample):
 
-Other workloads: ``--config 0`` (one block + tied head, 16 decode steps),
-``--config 2`` (batch 64, 1024-token prefill each, 128 decode steps; decode tokens/s),
-``--config 3`` (batch 16 x 512-token prefill; prefill tokens/s), ``--config 4`` (batch 8,
-cached lengths uniform in [1024, 32768] injected by the synthetic KV fill, 32 decode
-steps; decode tokens/s).
+  ``b64_decode``       batch 64, each sequence prefilled with 1024 tokens, then 128 greedy
+                       decode steps (decode tokens/s; one bench step = the 128 steps);
+  ``prefill_16x512``   batch 16 x 512-token prefill (prefill tokens/s);
+  ``one_block``        one decoder block + tied head, batch 1, 5 + 16 steps (generated tok/s);
+  ``long_context_b8``  batch 8, cached lengths uniform in [1024, 32768] injected by the
+                       synthetic KV fill, 32 decode steps (decode tokens/s).
 
-Multi-GPU: replicas only (independent sequences per GPU, no collective on the data path);
-``value`` is the sum over ranks of the units processed divided by the slowest rank's time.
+``--config N`` runs workload N alone as the headline (0: one block, 1: B=1, 2: B=64 decode,
+3: 16 x 512 prefill, 4: long context).
+
+Per-kernel times (``kernels``, and ``roofline`` of the headline) come from CUDA events around
+every launch of one kernel kind in one extra step run with programmatic dependent launch off,
+i.e. serialised; the timed steps overlap launches, so the step-level fractions
+(``step_roofline`` / each workload's ``roofline``) are the ones consistent with ``value``.
+
+Multi-GPU: replicas only (independent sequences per GPU, no collective on the data path).
+``--gpus N`` without a launcher re-executes itself under ``torch.distributed.run`` with N
+processes (one per GPU); ``value`` is the sum over ranks of the units processed divided by
+the slowest rank's time.
 
 ``--impl reference`` times the fp64 CPU oracle on this host on a bounded sample of the same
-workload (the only other program this bench runs).
+workload (the only other program this bench runs); under N processes rank 0 alone runs it.
 """
 
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
 import os
+import socket
 import statistics
 import subprocess
 import sys
@@ -208,12 +224,43 @@ def step_bytes(s, B: int, ctx: float) -> float:
     return weights + kv + B * L * 2 * KD * 2 + B * D * 2
 
 
+SERIAL_NOTE = ("CUDA events around each launch of the kind, in one extra step with programmatic dependent "
+               "launch off (serialised); the timed steps overlap launches")
+
 KIND_NAMES = {1: "qkv_proj(rmsnorm fused)", 2: "qknorm_rope_append", 3: "attention", 4: "o_proj+residual",
               5: "gate_up+silu_mul(rmsnorm fused)", 6: "down_proj+residual", 7: "lm_head+argmax",
               9: "k_decode_mk (persistent decode step)"}
 # names on the tensor-core path (more than 8 token rows)
 TC_KIND_NAMES = {1: "qkv_proj+qk_norm+rope+kv_append", 3: "attention", 4: "o_proj+residual",
                  5: "gate_up+silu_mul", 6: "down_proj+residual", 7: "lm_head+argmax", 8: "rmsnorm"}
+
+
+_WEIGHTS = {}
+
+
+def model_weights(s) -> dict:
+    """HF-named bf16 bit arrays of the seeded weights of shape `s`, drawn once per run. Every
+    tensor has its own seed, so a shape with fewer layers is a subset of the 28-layer draw."""
+    full = synth.QWEN3_0_6B
+    if s != full and "full" in _WEIGHTS and dataclasses.replace(full, n_layers=s.n_layers) == s:
+        keep = tuple(f"model.layers.{i}." for i in range(s.n_layers))
+        return {k: v for k, v in _WEIGHTS["full"].items()
+                if not k.startswith("model.layers.") or k.startswith(keep)}
+    key = "full" if s == full else s
+    if key not in _WEIGHTS:
+        t0 = time.time()
+        _WEIGHTS[key] = dict(synth.Weights(s, seed=0).named())
+        log(f"weights of {s.n_layers} layer(s) drawn in {time.time() - t0:.1f}s")
+    return _WEIGHTS[key]
+
+
+def gpu_uuid_of(dev: int) -> str:
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return str(dev)
 
 
 def run_ours(args, cfg, rank, world):
@@ -225,19 +272,14 @@ def run_ours(args, cfg, rank, world):
     torch.cuda.set_device(dev)
     s = cfg["shape"]
     B, P, ND = cfg["B"], cfg["prompt"], cfg["n_decode"]
-    t0 = time.time()
-    w = synth.Weights(s, seed=0)
-    named = dict(w.named())
-    log(f"[rank {rank}] weights drawn in {time.time() - t0:.1f}s")
     max_ctx = P + ND + 16
-    eng = qw.Engine(s, named, max_tokens=max(B * P, 8), max_batch=max(B, 8), max_context=max_ctx,
+    eng = qw.Engine(s, model_weights(s), max_tokens=max(B * P, 8), max_batch=max(B, 8), max_context=max_ctx,
                     kv_pages=B * ((max_ctx + 15) // 16) + 8, max_seqs=max(B, 8))
-    del named, w
     st = eng.stream
     if args.persistent:
         qw.qw_set_option(eng.model, qw.QW_OPT_PERSISTENT_DECODE, 1)
     seqs = list(range(B))
-    prompt = synth.make_tokens(s.vocab, B * P, rank_token_seed(args.config, rank))
+    prompt = synth.make_tokens(s.vocab, B * P, rank_token_seed(cfg["id"], rank))
     d_prompt = torch.tensor(prompt, dtype=torch.int32, device="cuda")
     d_cur = torch.zeros(B, dtype=torch.int32, device="cuda")
     d_out = torch.zeros((ND + 1, B), dtype=torch.int32, device="cuda")
@@ -263,13 +305,7 @@ def run_ours(args, cfg, rank, world):
     status = qw.qw_sync_status(eng.model, st)
     if status != 0:
         raise RuntimeError(f"device status {status} after warm-up: {qw.qw_last_error()}")
-    gpu_uuid = "0"
-    try:
-        gpu_uuid = str(torch.cuda.get_device_properties(dev).uuid)
-        if not gpu_uuid.startswith("GPU-"):
-            gpu_uuid = "GPU-" + gpu_uuid
-    except Exception:
-        gpu_uuid = str(dev)
+    gpu_uuid = gpu_uuid_of(dev)
     barrier(world)
     launches[0] = 0
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -339,8 +375,8 @@ def run_ours(args, cfg, rank, world):
     achieved = dk["bytes"] / (dk["avg_us"] * 1e-6) / 1e9
     roofline = {"bound": "hbm", "kernel": dk["name"], "achieved": round(achieved, 1), "peak": hbm,
                 "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / hbm, 4),
-                "traffic": ncu_traffic(args.config, dk["name"]), "algorithmic_bytes_per_launch": dk["bytes"],
-                "avg_launch_us": round(dk["avg_us"], 3)}
+                "traffic": ncu_traffic(cfg["id"], dk["name"]), "algorithmic_bytes_per_launch": dk["bytes"],
+                "avg_launch_us": round(dk["avg_us"], 3), "timing": SERIAL_NOTE}
     step_b = step_bytes(s, B, P + ND / 2)
     # ---- end to end through qw_generate with pinned host buffers ----
     h_prompt = torch.empty(B * P, dtype=torch.int32, pin_memory=True).numpy()
@@ -374,17 +410,23 @@ def run_ours(args, cfg, rank, world):
                    "decode_step_bytes": step_b,
                    "decode_step_hbm_frac": round(step_b / (decode_us * 1e-6) / 1e9 / hbm, 4)},
         "roofline": roofline,
+        "step_roofline": {"bound": "hbm", "achieved": round(step_b / (decode_us * 1e-6) / 1e9, 1), "peak": hbm,
+                          "unit": "GB/s", "frac": round(step_b / (decode_us * 1e-6) / 1e9 / hbm, 4),
+                          "bytes_per_step": step_b, "step_us": round(decode_us, 2),
+                          "note": "whole decode step (weights + KV read once) over the event-timed graph replay"},
         "kernels": {KIND_NAMES[k]: {"avg_us": round(v["avg_us"], 3), "per_step_us": round(v["total_us_per_step"], 2),
                                     "GB/s": round(v["bytes"] / (v["avg_us"] * 1e-6) / 1e9, 1)}
                     for k, v in kinds.items()},
+        "kernels_timing": SERIAL_NOTE,
         "e2e": {"value": round(e2e_val, 2), "unit": cfg["unit"], "h2d_bytes_per_step": B * P * 4,
                 "d2h_bytes_per_step": B * (ND + 1) * 4},
         "gpu_launches": gpu_launches,
         "clocks": clk.summary(),
-        "sampling": time_sampling(qw, s.vocab, st),
     }
+    if cfg["id"] == 1:
+        out["sampling"] = time_sampling(qw, s.vocab, st)
     eng.close()
-    if B == 1:
+    if cfg["id"] == 1:
         out["quantized_decode"] = time_quantized_decode(qw, s, P, ND, hbm)
     return out
 
@@ -397,10 +439,8 @@ def time_quantized_decode(qw, s, P: int, ND: int, hbm: float):
     import torch
     res = {}
     for bits in (8, 4):
-        w = synth.Weights(s, seed=0)
-        eng = qw.Engine(s, dict(w.named()), max_tokens=8, max_batch=8, max_context=P + ND + 16,
+        eng = qw.Engine(s, model_weights(s), max_tokens=8, max_batch=8, max_context=P + ND + 16,
                         kv_pages=(P + ND + 15) // 16 + 8, max_seqs=8)
-        del w
         eng.quantize(bits)
         st = eng.stream
         d_prompt = torch.tensor(synth.make_tokens(s.vocab, P, 4242).astype(np.int32), device="cuda")
@@ -485,13 +525,11 @@ def run_other(args, cfg, rank, world):
     chunk_seqs = 16 if kind != "decode_long" else B            # prefill 16 sequences per call
     max_tokens = max(int(lens[:chunk_seqs].sum()), B, 8) if kind != "decode_long" else max(B, 8)
     pages = int(sum((l + ND + 15) // 16 + 1 for l in lens)) + 8
-    w = synth.Weights(s, seed=0)
-    eng = qw.Engine(s, dict(w.named()), max_tokens=max_tokens, max_batch=max(B, 8), max_context=max_ctx,
+    eng = qw.Engine(s, model_weights(s), max_tokens=max_tokens, max_batch=max(B, 8), max_context=max_ctx,
                     kv_pages=pages, max_seqs=max(B, 8))
-    del w
     st = eng.stream
     seqs = list(range(B))
-    rng_seed = rank_token_seed(args.config, rank)
+    rng_seed = rank_token_seed(cfg["id"], rank)
     d_cur = torch.zeros(B, dtype=torch.int32, device="cuda")
     hbm, bf16_burst, bf16_sust, peak_src = peaks()
 
@@ -541,12 +579,7 @@ def run_other(args, cfg, rank, world):
     st.synchronize()
     if qw.qw_sync_status(eng.model, st) != 0:
         raise RuntimeError(f"device status after warm-up: {qw.qw_last_error()}")
-    gpu_uuid = str(dev)
-    try:
-        gpu_uuid = str(torch.cuda.get_device_properties(dev).uuid)
-        gpu_uuid = gpu_uuid if gpu_uuid.startswith("GPU-") else "GPU-" + gpu_uuid
-    except Exception:
-        pass
+    gpu_uuid = gpu_uuid_of(dev)
     barrier(world)
     launches[0] = 0
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -605,6 +638,7 @@ def run_other(args, cfg, rank, world):
                          per_step_us=sum(d), launches=nl)
     T = int(lens.sum()) if kind == "prefill" else B
     D, I, QD, KD, V = s.hidden, s.inter, s.n_heads * s.head_dim, s.n_kv_heads * s.head_dim, s.vocab
+    step_ms = ms_max / args.steps
     if kind == "prefill":
         flops = {1: 2 * T * (QD + 2 * KD) * D, 4: 2 * T * D * QD, 5: 2 * T * 2 * I * D, 6: 2 * T * D * I,
                  7: 2 * B * V * D}
@@ -613,16 +647,21 @@ def run_other(args, cfg, rank, world):
         gemm_kinds = [1, 4, 5, 6]
         dom = max(gemm_kinds, key=lambda k: kinds[k]["per_step_us"])
         ach = flops[dom] / (kinds[dom]["avg_us"] * 1e-6) / 1e12
-        roofline = {"bound": "tensor", "kernel": kinds[dom]["name"] + " (tcgen05 GEMM)", "achieved": round(ach, 1),
+        dominant = {"bound": "tensor", "kernel": kinds[dom]["name"] + " (tcgen05 GEMM)", "achieved": round(ach, 1),
                     "peak": bf16_sust, "peak_source": peak_src + " bf16 sustained (fp16 operands run at the bf16 rate)",
                     "unit": "TFLOP/s", "frac": round(ach / bf16_sust, 4),
-                    "traffic": ncu_traffic(args.config, kinds[dom]["name"]),
-                    "algorithmic_flops_per_launch": flops[dom], "avg_launch_us": round(kinds[dom]["avg_us"], 2)}
+                    "traffic": ncu_traffic(cfg["id"], kinds[dom]["name"]),
+                    "algorithmic_flops_per_launch": flops[dom], "avg_launch_us": round(kinds[dom]["avg_us"], 2),
+                    "timing": SERIAL_NOTE}
         attn_pairs = sum(int(l) * (int(l) + 1) // 2 for l in lens)
         total_flops = L * sum(flops[k] for k in gemm_kinds) + flops[7] + L * attn_pairs * 4 * s.head_dim * s.n_heads
-        extra = {"step_tflop": total_flops / 1e12,
-                 "step_tc_frac": round(total_flops / (ms_max / args.steps * 1e-3) / 1e12 / bf16_burst, 4),
-                 "prefill_step_stats": step_lat}
+        achieved = total_flops / (step_ms * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": bf16_burst,
+                    "peak_source": peak_src + " bf16 burst (fp16 operands run at the bf16 rate)", "unit": "TFLOP/s",
+                    "frac": round(achieved / bf16_burst, 4), "flop_per_step": total_flops,
+                    "frac_of_sustained": round(achieved / bf16_sust, 4),
+                    "note": "whole prefill step (projection GEMMs, causal attention, LM head) over the timed step"}
+        extra = {"step_tflop": total_flops / 1e12, "prefill_step_stats": step_lat}
     else:
         ctx = float(np.mean(lens)) + ND / 2
         kv_bytes = attn_bytes_layer(s, float(np.sum(lens)) + B * ND / 2)
@@ -631,28 +670,95 @@ def run_other(args, cfg, rank, world):
             kinds[kd]["GB/s"] = round(b / (kinds[kd]["avg_us"] * 1e-6) / 1e9, 1)
         dom = max(byts, key=lambda k: kinds[k]["per_step_us"])
         ach = byts[dom] / (kinds[dom]["avg_us"] * 1e-6) / 1e9
-        roofline = {"bound": "hbm", "kernel": kinds[dom]["name"], "achieved": round(ach, 1), "peak": hbm,
+        dominant = {"bound": "hbm", "kernel": kinds[dom]["name"], "achieved": round(ach, 1), "peak": hbm,
                     "peak_source": peak_src, "unit": "GB/s", "frac": round(ach / hbm, 4),
-                    "traffic": ncu_traffic(args.config, kinds[dom]["name"]),
-                    "algorithmic_bytes_per_launch": byts[dom], "avg_launch_us": round(kinds[dom]["avg_us"], 2)}
+                    "traffic": ncu_traffic(cfg["id"], kinds[dom]["name"]),
+                    "algorithmic_bytes_per_launch": byts[dom], "avg_launch_us": round(kinds[dom]["avg_us"], 2),
+                    "timing": SERIAL_NOTE}
         step_b = step_bytes(s, B, ctx)
-        step_us = ms_max / args.steps / ND * 1e3
+        step_us = step_ms / ND * 1e3
+        achieved = step_b / (step_us * 1e-6) / 1e9
+        roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "peak_source": peak_src,
+                    "unit": "GB/s", "frac": round(achieved / hbm, 4), "bytes_per_step": step_b,
+                    "note": "whole decode step (every weight and cached K/V byte once) over the timed steps"}
         extra = {"decode_step_us": round(step_us, 2), "decode_step_stats": step_lat, "decode_step_bytes": step_b,
-                 "decode_step_hbm_frac": round(step_b / (step_us * 1e-6) / 1e9 / hbm, 4),
                  "mean_cached_len": float(np.mean(lens))}
+
+    # ---- end to end through the C ABI with host buffers (copies inside the timed region) ----
+    e2e = e2e_other(qw, eng, kind, seqs, lens, ND, s, rng_seed, args.steps, world, units_per_step)
     out = {"metric": METRIC, "value": round(value, 2), "unit": cfg["unit"], "n_gpus": world, "steps": args.steps,
-           "warmup": args.warmup, "ms_per_step": round(ms_max / args.steps, 4), "higher_is_better": True,
+           "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f16 tensor-core operands (bf16 weights converted), f32 accumulate, f16 KV cache"
-           if (int(lens.sum()) if kind == "prefill" else B) > 8 else
-           "bf16 weights x f32 activations, f32 accumulate, f16 KV cache",
+           if T > 8 else "bf16 weights x f32 activations, f32 accumulate, f16 KV cache",
            "data": "synthetic (seeded random-init bf16 weights N(0,0.02), uniform-random token ids)",
            "config": dict({"workload": cfg["workload"], "batch": B, "l2": "working set exceeds L2; no flush"}, **extra),
-           "roofline": roofline,
+           "roofline": roofline, "dominant_kernel": dominant,
            "kernels": {v["name"]: {k: (round(x, 2) if isinstance(x, float) else x) for k, x in v.items() if k != "name"}
                        for v in kinds.values()},
-           "gpu_launches": launches[0], "clocks": clk.summary()}
+           "kernels_timing": SERIAL_NOTE,
+           "e2e": e2e, "gpu_launches": launches[0], "clocks": clk.summary()}
     eng.close()
     return out
+
+
+def e2e_other(qw, eng, kind, seqs, lens, ND, s, seed, steps, world, units_per_step):
+    """The workload's metric through the C ABI from pinned host buffers, host<->device copies
+    inside the timed region. Decode: every decode step copies the B token ids in, runs
+    qw_decode_step and reads the B picks back (the host feeds them to the next step), i.e. a
+    host-driven serving loop. Prefill: every step copies the prompt ids in, runs qw_prefill
+    and reads the B picks back."""
+    import torch
+    st = eng.stream
+    B = len(seqs)
+    n = max(1, min(steps, 5))
+    if kind == "prefill":
+        T = int(np.sum(lens))
+        h_in = torch.from_numpy(synth.make_tokens(s.vocab, T, seed).astype(np.int32)).pin_memory()
+        d_in = torch.empty(T, dtype=torch.int32, device="cuda")
+        h_out = torch.empty(B, dtype=torch.int32).pin_memory()
+        d_out = torch.empty(B, dtype=torch.int32, device="cuda")
+        t0 = None
+        for i in range(n + 1):
+            if i == 1:
+                t0 = time.perf_counter()
+            qw.qw_kv_reset(eng.kv, -1, st)
+            for sq in seqs:
+                qw.qw_kv_reserve(eng.kv, sq, int(lens[sq]), st)
+            with torch.cuda.stream(st):
+                d_in.copy_(h_in, non_blocking=True)
+            qw.qw_prefill(eng.model, eng.kv, seqs, [int(x) for x in lens], d_in.data_ptr(), 0, d_out.data_ptr(), st)
+            with torch.cuda.stream(st):
+                h_out.copy_(d_out, non_blocking=True)
+            st.synchronize()
+        dt = time.perf_counter() - t0
+        h2d, d2h = T * 4, B * 4
+    else:
+        h_in = torch.zeros(B, dtype=torch.int32).pin_memory()
+        h_out = torch.empty(B, dtype=torch.int32).pin_memory()
+        d_in = torch.empty(B, dtype=torch.int32, device="cuda")
+        d_out = torch.empty(B, dtype=torch.int32, device="cuda")
+        t0 = None
+        for i in range(n + 1):
+            if i == 1:
+                t0 = time.perf_counter()
+            for sq in seqs:
+                qw.qw_kv_truncate(eng.kv, sq, int(lens[sq]), st)
+            h_in.zero_()
+            for _ in range(ND):
+                with torch.cuda.stream(st):
+                    d_in.copy_(h_in, non_blocking=True)
+                qw.qw_decode_step(eng.model, eng.kv, seqs, d_in.data_ptr(), 0, d_out.data_ptr(), st)
+                with torch.cuda.stream(st):
+                    h_out.copy_(d_out, non_blocking=True)
+                st.synchronize()
+                h_in.copy_(h_out)
+        dt = time.perf_counter() - t0
+        h2d, d2h = B * 4 * ND, B * 4 * ND
+    if qw.qw_sync_status(eng.model, st) != 0:
+        raise RuntimeError(f"device status after the e2e loop: {qw.qw_last_error()}")
+    val = reduce_sum(units_per_step * n / dt, world)
+    return {"value": round(val, 2), "unit": "tok/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": n}
 
 
 def barrier(world):
@@ -684,19 +790,80 @@ def reduce_sum(v, world):
 # ---------------------------------------------------------------------------------------
 # oracle timing (cpu_baseline leg and the reference arm)
 # ---------------------------------------------------------------------------------------
+class _NamedWeights:
+    """Weight provider of the oracle over the HF-named bf16 arrays this bench already drew."""
+
+    def __init__(self, s, named):
+        self.shape, self.named_ = s, named
+
+    @property
+    def embed(self):
+        return self.named_["model.embed_tokens.weight"]
+
+    @property
+    def final_norm(self):
+        return self.named_["model.norm.weight"]
+
+    def layer(self, i):
+        pre = f"model.layers.{i}."
+        return {k[len(pre):]: v for k, v in self.named_.items() if k.startswith(pre)}
+
+
+_ORACLES = {}
+
+
+def oracle_model(s):
+    """The fp64 oracle of shape `s` with every layer widened up front (kept for the run)."""
+    import oracle
+    if s.n_layers not in _ORACLES:
+        m = oracle.Model(_NamedWeights(s, model_weights(s)))
+        for i in range(s.n_layers):
+            m.layer(i)
+        _ = m.embed32
+        _ORACLES[s.n_layers] = m
+    return _ORACLES[s.n_layers]
+
+
 def oracle_sample(cfg, n_decode: int, seed: int):
     """Generated tokens per second of the fp64 oracle on prefill + n_decode greedy steps."""
     import oracle
     s = cfg["shape"]
-    m = oracle.Model(synth.Weights(s, seed=0))
-    for i in range(s.n_layers):
-        m.layer(i)
-    _ = m.embed32
+    m = oracle_model(s)
     prompt = synth.make_tokens(s.vocab, cfg["prompt"], seed).tolist()
     t0 = time.perf_counter()
     oracle.generate(m, prompt, n_decode, keep_hidden=False)
     dt = time.perf_counter() - t0
     return (n_decode + 1) / dt, dt
+
+
+def oracle_decode_sample(s, ctx: int, n_steps: int, seed: int):
+    """Decode tokens per second of the fp64 oracle: one sequence over a cache of `ctx` tokens
+    (injected by the counter-based KV fill, as the long-context workload does; the values do
+    not change the work of a step), n_steps greedy decode steps."""
+    import oracle
+    m = oracle_model(s)
+    pos = np.arange(ctx)
+    prior = {l: (synth.kv_fill_values(77, l, 0, pos, s.n_kv_heads, s.head_dim).astype(np.float64),
+                 synth.kv_fill_values(77, l, 1, pos, s.n_kv_heads, s.head_dim).astype(np.float64))
+             for l in range(s.n_layers)}
+    cache = oracle.SeqCache(s.n_layers, prior=lambda l: prior[l], prior_len=ctx)
+    tok = int(synth.make_tokens(s.vocab, 1, seed)[0])
+    t0 = time.perf_counter()
+    for _ in range(n_steps):
+        tok = oracle.argmax_lowest(oracle.forward(m, [tok], cache)["logits"])
+    dt = time.perf_counter() - t0
+    return n_steps / dt, dt
+
+
+def oracle_prefill_sample(s, n_tokens: int, seed: int):
+    """Prefill tokens per second of the fp64 oracle on one sequence of n_tokens."""
+    import oracle
+    m = oracle_model(s)
+    toks = synth.make_tokens(s.vocab, n_tokens, seed).tolist()
+    t0 = time.perf_counter()
+    oracle.forward(m, toks, oracle.SeqCache(s.n_layers))
+    dt = time.perf_counter() - t0
+    return n_tokens / dt, dt
 
 
 def cores():
@@ -706,11 +873,31 @@ def cores():
         return os.cpu_count()
 
 
-def cpu_baseline(cfg, n_decode=96):
-    v, dt = oracle_sample(cfg, n_decode, 4242)
-    return {"value": round(v, 4), "unit": cfg["unit"], "cores": cores(), "kind": "oracle",
-            "sample": f"fp64 NumPy oracle, {cfg['prompt']}-token prompt prefill + {n_decode} greedy decode steps "
-                      f"of the same model shape, batch 1 ({dt:.1f} s)"}
+def cpu_baseline(cfg):
+    """The oracle as it stands on this host's cores, on a bounded sample of the workload."""
+    kind, s = cfg["kind"], cfg["shape"]
+    if kind == "generate":
+        n = 96 if s.n_layers > 1 else 32
+        v, dt = oracle_sample(cfg, n, 4242)
+        sample = (f"fp64 NumPy oracle, {cfg['prompt']}-token prompt prefill + {n} greedy decode steps of the same "
+                  f"model shape, batch 1 ({dt:.1f} s)")
+    elif kind == "decode":
+        n = 8
+        v, dt = oracle_decode_sample(s, cfg["prompt"], n, 4242)
+        sample = (f"fp64 NumPy oracle, 1 of the {cfg['B']} sequences decoding {n} greedy steps over a "
+                  f"{cfg['prompt']}-token cache ({dt:.1f} s); sequences are independent, so its rate per token is "
+                  f"the oracle's rate for the batch")
+    elif kind == "prefill":
+        v, dt = oracle_prefill_sample(s, cfg["prompt"], 4242)
+        sample = (f"fp64 NumPy oracle, prefill of 1 of the {cfg['B']} sequences of {cfg['prompt']} tokens "
+                  f"({dt:.1f} s); sequences are independent")
+    else:
+        lens = synth.make_lengths(cfg["B"], 1024, 32768, 2000)
+        n = 4
+        v, dt = oracle_decode_sample(s, int(lens.min()), n, 4242)
+        sample = (f"fp64 NumPy oracle, the shortest of the {cfg['B']} sequences ({int(lens.min())} cached tokens) "
+                  f"decoding {n} greedy steps ({dt:.1f} s); longer caches cost more per step")
+    return {"value": round(v, 4), "unit": cfg["unit"], "cores": cores(), "kind": "oracle", "sample": sample}
 
 
 def run_reference(args, cfg):
@@ -723,14 +910,45 @@ def run_reference(args, cfg):
     tokens = (n_dec + 1) * args.steps
     total = sum(samples)
     val = tokens / total
-    return {"impl": "reference", "metric": METRIC, "value": round(val, 4), "unit": cfg["unit"], "n_gpus": 1,
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    return {"impl": "reference", "metric": METRIC, "value": round(val, 4), "unit": cfg["unit"], "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded random-init bf16 weights widened to fp64)",
-            "config": {"workload": cfg["workload"], "sample": f"prefill {cfg['prompt']} + {n_dec} decode steps per step"},
+            "config": {"workload": cfg["workload"], "sample": f"prefill {cfg['prompt']} + {n_dec} decode steps per step",
+                       "processes": "rank 0 alone runs the oracle on the host cores"},
             "cpu_baseline": {"value": round(val, 4), "unit": cfg["unit"], "cores": cores(), "kind": "oracle",
                              "sample": f"prefill + {n_dec} greedy decode steps per bench step"},
             "e2e": {"value": round(val, 4), "unit": cfg["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# workloads of the default line besides the headline, under these keys
+SUB_KEYS = {2: "b64_decode", 3: "prefill_16x512", 0: "one_block", 4: "long_context_b8"}
+COMMON_KEYS = ("metric", "n_gpus", "steps", "warmup", "higher_is_better", "scaling", "vs_baseline", "data")
+
+
+def free_port() -> int:
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def replica_command(n: int, argv) -> list:
+    """The command that runs this bench as n replica processes (one per GPU) on this node."""
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+            "--master-addr=127.0.0.1", f"--master-port={free_port()}", os.path.abspath(__file__)] + list(argv)
+
+
+def workload(args, cid: int, alone: bool) -> dict:
+    cfg = dict(CONFIGS[cid])
+    cfg["id"] = cid
+    if alone and args.prompt_len > 0 and cid in (2, 3):
+        cfg["prompt"] = args.prompt_len
+        cfg["workload"] += f" [reduced: {args.prompt_len} tokens per sequence]"
+    if alone and args.decode_steps > 0 and cid in (2, 4):
+        cfg["n_decode"] = args.decode_steps
+        cfg["workload"] += f" [reduced: {args.decode_steps} decode steps]"
+    return cfg
 
 
 def main():
@@ -739,38 +957,46 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=1, choices=[0, 1, 2, 3, 4])
+    ap.add_argument("--config", type=int, default=None, choices=[0, 1, 2, 3, 4],
+                    help="run one workload alone (default: all five, the B=1 generation as headline)")
     ap.add_argument("--persistent", action="store_true",
                     help="decode steps of <= 4 sequences as one persistent kernel")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prompt-len", type=int, default=0,
-                    help="configs 2/3: tokens per sequence instead of the configured length (smaller case for profiling)")
+                    help="with --config 2/3: tokens per sequence instead of the configured length (smaller case "
+                         "for profiling)")
     ap.add_argument("--decode-steps", type=int, default=0,
-                    help="configs 2/4: decode steps per timed step instead of the configured count")
+                    help="with --config 2/4: decode steps per timed step instead of the configured count")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
-    cfg = dict(CONFIGS[args.config])
-    if args.prompt_len > 0 and args.config in (2, 3):
-        cfg["prompt"] = args.prompt_len
-        cfg["workload"] += f" [reduced: {args.prompt_len} tokens per sequence]"
-    if args.decode_steps > 0 and args.config in (2, 4):
-        cfg["n_decode"] = args.decode_steps
-        cfg["workload"] += f" [reduced: {args.decode_steps} decode steps]"
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # replicas: one process per GPU, launched here when no launcher did it
+        sys.exit(subprocess.call(replica_command(args.gpus, sys.argv[1:])))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.impl == "reference":
         if rank == 0:
-            print(json.dumps(run_reference(args, cfg)), flush=True)
+            print(json.dumps(run_reference(args, workload(args, 1 if args.config is None else args.config, True))),
+                  flush=True)
         return
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("gloo")
-    out = run_ours(args, cfg, rank, world) if args.config in (0, 1) else run_other(args, cfg, rank, world)
+    ids = [args.config] if args.config is not None else [1, 2, 3, 0, 4]
+    results = []
+    for cid in ids:
+        cfg = workload(args, cid, args.config is not None)
+        out = run_ours(args, cfg, rank, world) if cid in (0, 1) else run_other(args, cfg, rank, world)
+        results.append((cid, cfg, out))
     if rank == 0:
-        if not args.no_cpu_baseline and args.config in (0, 1):
-            out["cpu_baseline"] = cpu_baseline(cfg)
-        print(json.dumps(out), flush=True)
+        if not args.no_cpu_baseline:
+            for cid, cfg, out in results:
+                out["cpu_baseline"] = cpu_baseline(cfg)
+        head = results[0][2]
+        for cid, cfg, out in results[1:]:
+            head[SUB_KEYS[cid]] = {k: v for k, v in out.items() if k not in COMMON_KEYS}
+        print(json.dumps(head), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

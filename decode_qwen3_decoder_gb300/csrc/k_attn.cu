@@ -23,26 +23,6 @@
 
 namespace {
 
-template <typename... KArgs, typename... Args>
-cudaError_t launch_k(const LaunchCtx& c, void (*kern)(KArgs...), dim3 grid, dim3 block,
-                     size_t smem, Args&&... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = c.stream;
-    cudaLaunchAttribute attr[1];
-    cfg.numAttrs = 0;
-    if (c.pdl) {
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-    }
-    if (c.counter) ++*c.counter;
-    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
-}
-
 __device__ __forceinline__ uint4 ldg_nc(const void* p) {
     uint4 r;
     asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -182,6 +162,9 @@ __global__ void __launch_bounds__(AW * 32) k_attn_paged(const __grid_constant__ 
                 if (lane == 0) atomicOr(p.status, QW_DEV_BAD_POS);
             } else {
                 f16* pool = (warp == 2 ? p.kv.k : p.kv.v) + (size_t)p.layer * p.kv.layer_stride;
+                if (f16_out_of_range(y[0]) || f16_out_of_range(y[1]) || f16_out_of_range(y[2]) ||
+                    f16_out_of_range(y[3]))
+                    atomicOr(p.status, QW_DEV_RANGE);
                 uint2 packed;
                 packed.x = pack_h2(y[0], y[1]);
                 packed.y = pack_h2(y[2], y[3]);

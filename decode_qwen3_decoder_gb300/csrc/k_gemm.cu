@@ -225,6 +225,13 @@ __device__ void epi_heads(const GemmKParams& p, const f16* EH, const float* nws,
             b[8 * k + 2 * i + 1] = h_hi(wb[i]);
         }
     }
+    {
+        // the tile was staged as fp16: a projection beyond the fp16 range is inf here
+        bool big = false;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) big |= f16_out_of_range(a[k]) || f16_out_of_range(b[k]);
+        if (big && t < ntok) atomicOr(p.status, QW_DEV_RANGE);
+    }
     if (!isv) {
         float ss = 0.f;
 #pragma unroll
@@ -285,6 +292,10 @@ __device__ void epi_silu(const GemmKParams& p, const float* E, int tok0, int nto
         v[4 * k + 2] = __fdividef(g.z, 1.0f + __expf(-g.z)) * u.z;
         v[4 * k + 3] = __fdividef(g.w, 1.0f + __expf(-g.w)) * u.w;
     }
+    bool big = false;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) big |= f16_out_of_range(v[k]);
+    if (big) atomicOr(p.status, QW_DEV_RANGE);
     store16h(p.out_h + (size_t)(tok0 + t) * p.ld_out + tile * 64 + 16 * q, v);
 }
 

@@ -522,6 +522,9 @@ __global__ void __launch_bounds__(MK_THREADS, 1) k_decode_mk(const MkParams p) {
                                 if (lane == 0) atomicOr(p.status, QW_DEV_BAD_POS);
                             } else {
                                 f16* pool = (wt == 2 ? p.kv.k : p.kv.v) + (size_t)l * p.kv.layer_stride;
+                                if (f16_out_of_range(y[0]) || f16_out_of_range(y[1]) || f16_out_of_range(y[2]) ||
+                                    f16_out_of_range(y[3]))
+                                    atomicOr(p.status, QW_DEV_RANGE);
                                 uint2 pk;
                                 pk.x = pack_h2(y[0], y[1]);
                                 pk.y = pack_h2(y[2], y[3]);
@@ -699,8 +702,9 @@ __global__ void __launch_bounds__(MK_THREADS, 1) k_decode_mk(const MkParams p) {
         // ---- gate/up + SiLU*mul (Paso 6), post-attention RMSNorm fused -----------------
         stage_norm(nb + p.D);
         ok = consume(PH_GU, l, [&](int row, int t, const float* v) {
-            __stcg(reinterpret_cast<unsigned short*>(p.act) + (size_t)t * p.I + row,
-                   __half_as_ushort(__float2half_rn(v[0] / (1.0f + expf(-v[0])) * v[1])));
+            const float a = v[0] / (1.0f + expf(-v[0])) * v[1];
+            if (f16_out_of_range(a)) atomicOr(p.status, QW_DEV_RANGE);
+            __stcg(reinterpret_cast<unsigned short*>(p.act) + (size_t)t * p.I + row, __half_as_ushort(__float2half_rn(a)));
         });
         if (!(ok = gsync(ok))) break;
 

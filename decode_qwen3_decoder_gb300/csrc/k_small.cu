@@ -9,26 +9,6 @@
 
 namespace {
 
-template <typename... KArgs, typename... Args>
-cudaError_t launch_k(const LaunchCtx& c, void (*kern)(KArgs...), dim3 grid, dim3 block,
-                     size_t smem, Args&&... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = c.stream;
-    cudaLaunchAttribute attr[1];
-    cfg.numAttrs = 0;
-    if (c.pdl) {
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-    }
-    if (c.counter) ++*c.counter;
-    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
-}
-
 __device__ __forceinline__ uint4 ldg_stream(const void* p) {
     uint4 r;
     asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -189,6 +169,7 @@ struct GemvP {
     float* out;
     f16* out_h;
     unsigned long long* best;
+    int* status;  // G_GATEUP: QW_DEV_RANGE when an fp16 activation would overflow
 };
 
 constexpr int GEMV_WARPS = 4;
@@ -418,7 +399,9 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) k_gemv(GemvP p) {
                             *o = (first_rows ? xres[rr] : *o) + acc[rr][0][t];
                         } else if (MODE == G_GATEUP) {
                             const float g = acc[rr][0][t], u = acc[rr][NW - 1][t];
-                            p.out_h[(size_t)t * p.n_out + row] = __float2half_rn(silu_f(g) * u);
+                            const float a = silu_f(g) * u;
+                            if (f16_out_of_range(a)) atomicOr(p.status, QW_DEV_RANGE);
+                            p.out_h[(size_t)t * p.n_out + row] = __float2half_rn(a);
                         } else {
                             if (p.out) p.out[(size_t)t * p.n_out + row] = acc[rr][0][t];
                             best[t] = u64_max(best[t], argmax_key(acc[rr][0][t], row));
@@ -531,10 +514,10 @@ cudaError_t launch_gemv_qkv(const LaunchCtx& c, int T, const float* x, const bf1
 
 cudaError_t launch_gemv_gateup(const LaunchCtx& c, int T, const float* x, const bf16* norm_w,
                                float eps, const bf16* Wg, const bf16* Wu, int inter, int K, f16* act,
-                               const QWeights* qg, const QWeights* qu) {
+                               int* status, const QWeights* qg, const QWeights* qu) {
     GemvP p = {};
     p.x = x; p.norm_w = norm_w; p.eps = eps; p.W = Wg; p.W2 = Wu; p.n_out = inter; p.K = K; p.T = T;
-    p.out_h = act;
+    p.out_h = act; p.status = status;
     if (qg) { p.qw = qg->codes; p.sb = qg->sb; p.qw2 = qu->codes; p.sb2 = qu->sb; }
     return gemv_any<G_GATEUP>(c, p, qg ? qg->bits : 16, 0);
 }
@@ -624,6 +607,8 @@ __global__ void __launch_bounds__(256) k_qknorm_rope_append(
 #pragma unroll
             for (int j = 0; j < 4; ++j) y[j] = o[j];
         }
+        if (f16_out_of_range(y[0]) || f16_out_of_range(y[1]) || f16_out_of_range(y[2]) || f16_out_of_range(y[3]))
+            atomicOr(status, QW_DEV_RANGE);
         uint2 packed;
         packed.x = pack_h2(y[0], y[1]);
         packed.y = pack_h2(y[2], y[3]);
@@ -737,6 +722,19 @@ __global__ void k_convert_bf16_f16(const bf16* __restrict__ src, f16* __restrict
             }
         }
     }
+}
+
+__global__ void k_check_abs(const bf16* __restrict__ w, size_t n, float limit, int* status) {
+    bool big = false;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+        big |= !(fabsf(__bfloat162float(w[i])) <= limit);
+    if (big) atomicOr(status, QW_DEV_RANGE);
+}
+
+cudaError_t launch_check_abs(const LaunchCtx& c, const bf16* w, size_t n, float limit, int* status) {
+    if (n == 0) return cudaSuccess;
+    return launch_k(c, k_check_abs, dim3((unsigned)std::min<size_t>((n + 255) / 256, 1024)), dim3(256), 0, w, n,
+                    limit, status);
 }
 
 cudaError_t launch_convert_bf16_f16(const LaunchCtx& c, const bf16* src, f16* dst, size_t n, int* status) {

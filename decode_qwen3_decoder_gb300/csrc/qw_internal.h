@@ -78,6 +78,8 @@ __device__ __forceinline__ float warp_max(float v) {
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
     return v;
 }
+// A value that an fp16 store would not hold (beyond the largest finite fp16, or NaN).
+__device__ __forceinline__ bool f16_out_of_range(float v) { return !(fabsf(v) <= 65504.f); }
 // Key that orders like the float value, with the lowest index winning ties under max.
 __device__ __forceinline__ unsigned long long argmax_key(float v, int idx) {
     uint32_t u = __float_as_uint(v);
@@ -111,12 +113,39 @@ struct LaunchCtx {
     int* counter; // incremented per launch (kernel count bookkeeping)
 };
 
+#ifdef __CUDACC__
+#include <utility>
+// Launch a kernel on c.stream, with programmatic stream serialization when c.pdl is set,
+// counting the launch in c.counter.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(const LaunchCtx& c, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                     Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = c.stream;
+    cudaLaunchAttribute attr[1];
+    cfg.numAttrs = 0;
+    if (c.pdl) {
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    if (c.counter) ++*c.counter;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+#endif
+
 cudaError_t launch_step_begin(const LaunchCtx& c, const StepDesc& sd, const int32_t* ids,
                               const bf16* embed, int vocab, int hidden, float* x, TokView tv,
                               KVView kv, int* status);
 cudaError_t launch_rmsnorm(const LaunchCtx& c, const float* x, const int* rows, int n_rows,
                            int hidden, const bf16* w, float eps, f16* h);
 cudaError_t launch_convert_bf16_f16(const LaunchCtx& c, const bf16* src, f16* dst, size_t n, int* status);
+// Sets QW_DEV_RANGE when some |w[i]| > limit (i < n).
+cudaError_t launch_check_abs(const LaunchCtx& c, const bf16* w, size_t n, float limit, int* status);
 // Grouped affine weight codes of one matrix [rows, K]: codes (one per byte at 8 bits, two per
 // byte at 4, the even input in the low nibble) and one (scale, bias) half2 word per group of
 // 64 inputs, scale in the low half.
@@ -133,7 +162,7 @@ cudaError_t launch_gemv_qkv(const LaunchCtx& c, int T, const float* x, const bf1
                             const bf16* W, int n_out, int K, float* out, const QWeights* qw = nullptr);
 cudaError_t launch_gemv_gateup(const LaunchCtx& c, int T, const float* x, const bf16* norm_w,
                                float eps, const bf16* Wg, const bf16* Wu, int inter, int K, f16* act,
-                               const QWeights* qg = nullptr, const QWeights* qu = nullptr);
+                               int* status, const QWeights* qg = nullptr, const QWeights* qu = nullptr);
 cudaError_t launch_gemv_resid(const LaunchCtx& c, int T, const f16* act, const bf16* W, int n_out,
                               int K, float* x, const QWeights* qw = nullptr);
 cudaError_t launch_gemv_lmhead(const LaunchCtx& c, int B, const float* x, const int* rows,

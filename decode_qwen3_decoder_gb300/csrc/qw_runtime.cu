@@ -361,6 +361,22 @@ extern "C" qw_status qw_init_weights(const qw_config* cfg, const qw_weight_ptrs*
         fail(QW_ERR_CUDA, "final norm / embedding copy failed");
         return fail_free(QW_ERR_CUDA);
     }
+    // An RMSNorm output over n values has |y_i| <= sqrt(n) * |w_i| (since x_i^2 <= n * mean(x^2)),
+    // so norm weights below 65504 / sqrt(n) keep every normalised fp16 operand (h, q, k) finite.
+    {
+        const float lim_d = 65504.f / std::sqrt((float)D), lim_h = 65504.f / std::sqrt((float)d);
+        cudaError_t e = cudaSuccess;
+        for (int l = 0; l < cfg->n_layers && e == cudaSuccess; ++l) {
+            const bf16* nb = m->norms + (size_t)l * (2 * D + 2 * d);
+            e = launch_check_abs(pc, nb, 2 * D, lim_d, m->status);
+            if (e == cudaSuccess) e = launch_check_abs(pc, nb + 2 * D, 2 * d, lim_h, m->status);
+        }
+        if (e == cudaSuccess) e = launch_check_abs(pc, m->fnorm, D, lim_d, m->status);
+        if (e != cudaSuccess) {
+            fail(QW_ERR_CUDA, "norm weight check failed: %s", cudaGetErrorString(e));
+            return fail_free(QW_ERR_CUDA);
+        }
+    }
     // RoPE table (Paso 4): angle = pos * theta^(-i/64), evaluated in fp64, stored as fp32.
     {
         const size_t n = (size_t)cfg->max_context * 64;
@@ -398,7 +414,8 @@ extern "C" qw_status qw_init_weights(const qw_config* cfg, const qw_weight_ptrs*
             return fail_free(QW_ERR_CUDA);
         }
         if (word & QW_DEV_RANGE) {
-            fail(QW_ERR_INVALID_ARG, "a weight is outside the fp16 range (|w| > 65504)");
+            fail(QW_ERR_INVALID_ARG,
+                 "a weight is outside the fp16 range (|w| > 65504), or a norm weight exceeds 65504 / sqrt(n)");
             return fail_free(QW_ERR_INVALID_ARG);
         }
     }
@@ -937,7 +954,7 @@ static qw_status run_layers(qw_model* m, qw_kv* kv, const StepDesc& sd, bool pre
             {
                 PROF(QW_PROF_GATEUP);
                 LAUNCH(launch_gemv_gateup(lc, T, x, w_post, c.rms_eps, m->bg + (size_t)l * I * D,
-                                          m->bu + (size_t)l * I * D, I, D, act, qq ? &qq[2] : nullptr,
+                                          m->bu + (size_t)l * I * D, I, D, act, m->status, qq ? &qq[2] : nullptr,
                                           qq ? &qq[3] : nullptr));
             }
             PROF(QW_PROF_DOWN);
@@ -1026,13 +1043,14 @@ static qw_status run_step(qw_model* m, qw_kv* kv, const StepDesc& sd, bool prefi
     CUDA_TRY(launch_step_begin(lc0, sd, tokens, m->embed, c.vocab, D, m->x, tv, kvv, m->status));
     // A decode batch of >= 16 sequences runs as two halves on two streams, so that one
     // half's latency-bound projections overlap the other half's HBM-bound attention.
-    const bool two = !prefill && !small && !dbg && m->prof_kind == QW_PROF_OFF && m->split_decode && T >= 16;
+    // With the debug dumps on, each half writes its own rows of them (the same kernels run).
+    const bool two = !prefill && !small && m->prof_kind == QW_PROF_OFF && m->split_decode && T >= 16;
     if (two) {
         const int h0 = T / 2;
         CUDA_TRY(cudaEventRecord(m->ev_fork, st));
         CUDA_TRY(cudaStreamWaitEvent(m->aux_stream, m->ev_fork, 0));
-        QW_TRY(run_layers(m, kv, sd, prefill, max_keys, 0, h0, st, false, launches, pc));
-        QW_TRY(run_layers(m, kv, sd, prefill, max_keys, h0, T - h0, m->aux_stream, false, launches, pc));
+        QW_TRY(run_layers(m, kv, sd, prefill, max_keys, 0, h0, st, dbg, launches, pc));
+        QW_TRY(run_layers(m, kv, sd, prefill, max_keys, h0, T - h0, m->aux_stream, dbg, launches, pc));
         CUDA_TRY(cudaEventRecord(m->ev_join, m->aux_stream));
         CUDA_TRY(cudaStreamWaitEvent(st, m->ev_join, 0));
     } else {
@@ -1210,6 +1228,11 @@ static qw_status generate_impl(qw_model* m, qw_kv* kv, int B, const int* seq_ids
         if (lens[b] < 1) return fail(QW_ERR_INVALID_ARG, "lens[%d] < 1", b);
         const int s = seq_ids[b];
         if (kv->len[s] != 0) return fail(QW_ERR_BAD_STATE, "generate needs empty sequences (%d is not)", s);
+        // every position the loop writes must fit the context, or a decode step would fail
+        // after the prefill has already advanced the cache
+        if ((long long)lens[b] + n_decode > m->cfg.max_context)
+            return fail(QW_ERR_INVALID_ARG, "sequence %d: prompt %d + %d decode tokens > max_context %d", s, lens[b],
+                        n_decode, m->cfg.max_context);
         if ((long long)kv->pt[s].size() * 16 < (long long)lens[b] + n_decode)
             return fail(QW_ERR_KV_FULL, "sequence %d not reserved for prompt + %d decode tokens", s, n_decode);
         total += lens[b];
@@ -1286,6 +1309,7 @@ extern "C" qw_status qw_sync_status(qw_model* m, void* stream_) {
     if (word & QW_DEV_BAD_TOKEN) return fail(QW_ERR_BAD_TOKEN, "a token id was outside [0, vocab)");
     if (word & QW_DEV_BAD_POS) return fail(QW_ERR_BAD_POS, "a position had no reserved page");
     if (word & QW_DEV_TIMEOUT) return fail(QW_ERR_TIMEOUT, "a bounded wait in a kernel timed out");
-    if (word & QW_DEV_RANGE) return fail(QW_ERR_INVALID_ARG, "a value was outside the fp16 range");
+    if (word & QW_DEV_RANGE)
+        return fail(QW_ERR_RANGE, "an activation or K/V value stored as fp16 was outside its range (|v| > 65504)");
     return QW_OK;
 }

@@ -19,7 +19,7 @@ from . import _build
 QW_OK = 0
 STATUS_NAMES = {0: "QW_OK", -1: "QW_ERR_INVALID_ARG", -2: "QW_ERR_KV_FULL", -3: "QW_ERR_BAD_STATE",
                 -4: "QW_ERR_CUDA", -5: "QW_ERR_BAD_TOKEN", -6: "QW_ERR_TIMEOUT",
-                -7: "QW_ERR_UNSUPPORTED", -8: "QW_ERR_BAD_POS"}
+                -7: "QW_ERR_UNSUPPORTED", -8: "QW_ERR_BAD_POS", -9: "QW_ERR_RANGE"}
 
 
 class QwError(RuntimeError):

@@ -47,7 +47,9 @@ typedef enum {
     QW_ERR_BAD_TOKEN = -5,   /* device status: a token id outside [0, vocab)                  */
     QW_ERR_TIMEOUT = -6,     /* device status: a bounded wait inside a kernel gave up          */
     QW_ERR_UNSUPPORTED = -7, /* a shape this build has no kernel for                          */
-    QW_ERR_BAD_POS = -8      /* device status: a position with no page in the page table      */
+    QW_ERR_BAD_POS = -8,     /* device status: a position with no page in the page table      */
+    QW_ERR_RANGE = -9        /* device status: an activation or K/V value stored as fp16 was
+                              * beyond the fp16 range (|v| > 65504, or NaN)                    */
 } qw_status;
 
 /* Model shape. Per-layer dims of Qwen3-0.6B: hidden 1024, 16 query / 8 KV heads of 128,
@@ -106,8 +108,10 @@ size_t qw_model_workspace_bytes(const qw_config* cfg);
  * q|k|v rows concatenated per layer, norm weights copied as bf16), build the fp32 RoPE
  * cos/sin table (host fp64, Paso 4) and carve the activation buffers. Synchronises
  * `stream`; the source tensors may be freed afterwards except embed_tokens, which the
- * embedding gather keeps reading and must outlive the model. A weight beyond the fp16 range
- * gives QW_ERR_INVALID_ARG. ws_bytes >= qw_model_workspace_bytes(cfg), workspace 256-byte
+ * embedding gather keeps reading and must outlive the model. A weight beyond the fp16 range,
+ * or a norm weight above 65504 / sqrt(n) (n = hidden for the layer and final norms, head_dim
+ * for the QK-norms; it would let a normalised fp16 operand overflow), gives
+ * QW_ERR_INVALID_ARG. ws_bytes >= qw_model_workspace_bytes(cfg), workspace 256-byte
  * aligned. On success *out owns host state only. */
 qw_status qw_init_weights(const qw_config* cfg, const qw_weight_ptrs* w, void* dev_workspace,
                           size_t ws_bytes, void* stream, qw_model** out);
@@ -183,7 +187,11 @@ qw_status qw_generate_eos(qw_model* m, qw_kv* kv, int B, const int* seq_ids, con
                           int32_t* host_out_counts, void* stream);
 
 /* Synchronise `stream`, read and clear the device status word. Returns QW_OK or the first
- * of QW_ERR_BAD_TOKEN, QW_ERR_BAD_POS, QW_ERR_TIMEOUT that the word records. */
+ * of QW_ERR_BAD_TOKEN, QW_ERR_BAD_POS, QW_ERR_TIMEOUT, QW_ERR_RANGE that the word records.
+ * QW_ERR_RANGE: a value the step stores as fp16 (the attention values appended to the KV
+ * cache, the SwiGLU activation, the raw q|k|v projections staged for the QK-norm) was
+ * beyond the fp16 range; the outputs of that step are not valid. (The normalised operands
+ * cannot overflow: qw_init_weights refuses norm weights above 65504 / sqrt(n).) */
 qw_status qw_sync_status(qw_model* m, void* stream);
 
 /* Message for the calling thread's last error ("" if none). Valid until the next call. */
@@ -331,8 +339,10 @@ qw_status qw_sample_top_p(int B, int vocab, const float* dev_logits, size_t ld, 
  * that every GPU loading the library holds until exit. B > QW_NOALLOC_MAX_ROWS gives
  * QW_ERR_INVALID_ARG. The first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call before any stream
- * capture. All calls share the array and each clears the keys it uses, so calls whose work
- * overlaps on the GPU race: issue them on one stream. */
+ * capture. The address is kept for the life of the process: after cudaDeviceReset on a
+ * device (which also invalidates every model and buffer on it), this entry point must not be
+ * called on that device again in the same process. All calls share the array and each clears
+ * the keys it uses, so calls whose work overlaps on the GPU race: issue them on one stream. */
 #define QW_NOALLOC_MAX_ROWS 8
 qw_status qw_lm_head_argmax_noalloc(const qw_model* m, int B, const float* dev_x, float* dev_logits,
                                     int32_t* dev_next_ids, void* stream);

@@ -3,13 +3,16 @@ bench.py times (same shapes, batch composition, input recipe and call sequence),
 sampled sequences that the oracle recomputes one by one:
 
   * batched decode: 64 sequences, 1024-token prompts prefilled 16 sequences per call, then
-    greedy decode steps of all 64 (two-stream split path) -- sequences 0 and 63;
+    4 greedy decode steps of all 64 (two-stream split path: sequences 0-31 on one stream,
+    32-63 on the other) -- sequences 0, 31, 32 and 63, the hidden state after every layer
+    of every decode step, the logits and the ids;
   * prefill: 16 x 512 tokens in one call -- sequences 0 and 15 (every layer's hidden state,
     the final logits and ids), plus positions and KV slots of all 8192 tokens;
   * long-context ragged decode: 8 sequences with cached lengths drawn uniform in
     [1024, 32768] (seed 2000) and filled by the counter-based generator -- the shortest
-    sequence end to end through 28 layers, and the longest layer by layer (the oracle's layer
-    takes the GPU's input to that layer and the injected prefix of that layer).
+    sequence end to end through 28 layers, and the longest through all 28 layers one layer at
+    a time (the oracle's layer takes the GPU's input to that layer and the injected prefix of
+    that layer).
 
 Sequences never interact, so checking a subset of a batch is a valid check of the batch."""
 
@@ -35,7 +38,7 @@ def _engine(pkg, **kw):
 
 
 def test_batched_decode_b64_full(qw, om):
-    B, P, ND = 64, 1024, 2
+    B, P, ND = 64, 1024, 4
     eng = _engine(qw, max_tokens=16 * P, max_batch=B, max_context=P + ND + 16,
                   kv_pages=B * ((P + ND + 15) // 16 + 1) + 8, max_seqs=B)
     try:
@@ -48,7 +51,7 @@ def test_batched_decode_b64_full(qw, om):
             g = run.prefill(seqs, [toks[b].tolist() for b in seqs], debug=False, reserve_extra=ND)
             nxt[a:a + 16] = g["next"]
             logits[a:a + 16] = g["logits"]
-        sample = [0, 63]
+        sample = [0, 31, 32, 63]   # first and last sequence of each half of the two-stream split
         caches = {}
         for b in sample:
             caches[b] = oracle.SeqCache(S.n_layers)
@@ -57,10 +60,12 @@ def test_batched_decode_b64_full(qw, om):
             check_token(nxt[b], o["logits"])
         for step in range(ND):
             feed = nxt.copy()
-            d = run.decode(list(range(B)), feed.tolist(), debug=False)
+            d = run.decode(list(range(B)), feed.tolist(), debug=True)
             assert d["status"] == 0
+            np.testing.assert_array_equal(d["pos"], np.full(B, P + step))
             for b in sample:
                 o = oracle.forward(om, [int(feed[b])], caches[b])
+                check_hidden(d["hidden"][:, b:b + 1], o["hidden"])
                 check_logits(d["logits"][b], o["logits"])
                 check_token(d["next"][b], o["logits"])
             nxt = d["next"].astype(np.int64)
@@ -124,9 +129,9 @@ def test_long_context_ragged_decode_full(qw, om):
             check_logits(d["logits"][short], o["logits"])
             check_token(d["next"][short], o["logits"])
             if step == 0:
-                # longest sequence: sampled layers, each from the GPU's own input to it
+                # longest sequence: every layer, each from the GPU's own input to it
                 n = int(lens[long_])
-                for layer in (0, 13, 27):
+                for layer in range(S.n_layers):
                     x_in = (om.embed_rows([int(feed[long_])]) if layer == 0
                             else d["hidden"][layer - 1, long_:long_ + 1])
                     c = oracle.SeqCache(S.n_layers, prior=prior_for(n), prior_len=n)

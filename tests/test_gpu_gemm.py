@@ -91,8 +91,8 @@ def test_batch_invariance_and_determinism(blk):
 @pytest.mark.parametrize("B", [17, 32])
 def test_two_stream_decode(blk, B):
     """A decode batch of >= 16 sequences runs as two halves on two streams (ragged halves for
-    odd B); every sequence still matches the oracle, and the one-chain run agrees within
-    rounding."""
+    odd B); every sequence's hidden state after the layer, logits and id match the oracle,
+    and the one-chain run agrees within rounding."""
     run, om = blk
     qw, eng = run.qw, run.eng
     seqs = list(range(B))
@@ -110,10 +110,13 @@ def test_two_stream_decode(blk, B):
             caches.append(c)
         logits = []
         for step in range(2):
-            d = run.decode(seqs, forced[step].tolist(), debug=False)
+            # the split run also dumps every layer's hidden state (each half writes its rows)
+            d = run.decode(seqs, forced[step].tolist(), debug=bool(split))
             assert d["status"] == 0
             for b in range(B):
                 o = oracle.forward(om, [int(forced[step, b])], caches[b])
+                if split:
+                    check_hidden(d["hidden"][:, b:b + 1], o["hidden"])
                 check_logits(d["logits"][b], o["logits"])
                 check_token(d["next"][b], o["logits"])
             logits.append(d["logits"])

@@ -208,11 +208,17 @@ def test_degenerate_calls_are_rejected(one_block):
         lambda: qw.qw_decode_step(eng.model, eng.kv, [1, 1], t, 0, n, eng.stream),       # repeated id
         lambda: qw.qw_decode_step(eng.model, eng.kv, list(range(17)), t, 0, n, eng.stream),  # > max_batch
     ]
+    # generate: pages reserved beyond max_context (512) do not let prompt + decode steps pass it
+    qw.qw_kv_reserve(eng.kv, 2, 600, eng.stream)
+    h_prompt = np.ones(8, np.int32)
+    h_out = np.zeros((1, 506), np.int32)
+    calls.append(lambda: qw.qw_generate(eng.model, eng.kv, [2], [8], h_prompt, 505, h_out, eng.stream))
     for call in calls:
         with pytest.raises(qw.QwError) as e:
             call()
         assert e.value.status == -1
         assert qw.qw_kv_length(eng.kv, 0) == 0 and qw.qw_kv_length(eng.kv, 1) == 0
+        assert qw.qw_kv_length(eng.kv, 2) == 0
     qw.qw_kv_reset(eng.kv, -1, eng.stream)
 
 

@@ -97,3 +97,31 @@ def test_ncu_traffic_needs_the_captured_source():
         assert bench.ncu_traffic(*key) is None
     finally:
         bench.NCU_TRAFFIC[key] = saved
+
+
+def test_gpus_flag_spawns_replica_processes():
+    """`bench.py --gpus 2` without a launcher re-runs itself as two processes under
+    torch.distributed.run (127.0.0.1). Checked with the reference arm, which needs no GPU:
+    rank 0 alone runs the oracle and prints the one line, the other rank exits 0."""
+    import json
+    import subprocess
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR",
+                                                             "MASTER_PORT")}
+    env["OMP_NUM_THREADS"] = "2"
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--impl", "reference",
+                        "--config", "0", "--steps", "1", "--warmup", "3"],
+                       capture_output=True, text=True, timeout=900, env=env, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    out = json.loads(lines[0])
+    assert out["impl"] == "reference" and out["n_gpus"] == 2 and out["value"] > 0
+
+
+def test_replica_command():
+    sys.path.insert(0, ROOT)
+    import bench
+    cmd = bench.replica_command(4, ["--steps", "5"])
+    assert cmd[1:3] == ["-m", "torch.distributed.run"]
+    assert "--nproc-per-node=4" in cmd and "--master-addr=127.0.0.1" in cmd
+    assert cmd[-3:] == [os.path.join(ROOT, "bench.py"), "--steps", "5"]
