@@ -38,10 +38,12 @@ __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g));
 // Step begin: embedding gather (Paso 2) + per-token sequence/position bookkeeping (Paso 9:
 // positions continue from the sequence's current length).
 // =======================================================================================
+// ss (optional): per token, the sum of squares of x over each 128-feature block
+// [t][hidden / 128] (the batched decode-step kernel builds its first RMSNorm from it).
 __global__ void __launch_bounds__(256) k_step_begin(StepDesc sd, const int32_t* __restrict__ ids,
                                                     const bf16* __restrict__ embed, int vocab,
                                                     int hidden, float* __restrict__ x, TokView tv,
-                                                    KVView kv, int* status) {
+                                                    KVView kv, int* status, float* __restrict__ ss) {
     pdl_launch();
     pdl_wait();
     const int t = blockIdx.x;
@@ -56,6 +58,10 @@ __global__ void __launch_bounds__(256) k_step_begin(StepDesc sd, const int32_t* 
         float4 o = bad ? make_float4(0.f, 0.f, 0.f, 0.f)
                        : make_float4(bf_lo(w.x), bf_hi(w.x), bf_lo(w.y), bf_hi(w.y));
         *reinterpret_cast<float4*>(dst + k) = o;
+        if (ss) {  // a warp covers the 128 features of block k / 128
+            const float q = warp_sum(o.x * o.x + o.y * o.y + o.z * o.z + o.w * o.w);
+            if ((threadIdx.x & 31) == 0) ss[(size_t)t * (hidden / 128) + k / 128] = q;
+        }
     }
     if (threadIdx.x == 0) {
         const int seq = sd.seq[b];
@@ -73,9 +79,9 @@ __global__ void __launch_bounds__(256) k_step_begin(StepDesc sd, const int32_t* 
 
 cudaError_t launch_step_begin(const LaunchCtx& c, const StepDesc& sd, const int32_t* ids,
                               const bf16* embed, int vocab, int hidden, float* x, TokView tv,
-                              KVView kv, int* status) {
+                              KVView kv, int* status, float* ss) {
     return launch_k(c, k_step_begin, dim3(sd.T), dim3(256), 0, sd, ids, embed, vocab, hidden, x, tv,
-                    kv, status);
+                    kv, status, ss);
 }
 
 // =======================================================================================

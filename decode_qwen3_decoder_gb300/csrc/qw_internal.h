@@ -140,7 +140,7 @@ cudaError_t launch_k(const LaunchCtx& c, void (*kern)(KArgs...), dim3 grid, dim3
 
 cudaError_t launch_step_begin(const LaunchCtx& c, const StepDesc& sd, const int32_t* ids,
                               const bf16* embed, int vocab, int hidden, float* x, TokView tv,
-                              KVView kv, int* status);
+                              KVView kv, int* status, float* ss = nullptr);
 cudaError_t launch_rmsnorm(const LaunchCtx& c, const float* x, const int* rows, int n_rows,
                            int hidden, const bf16* w, float eps, f16* h);
 cudaError_t launch_convert_bf16_f16(const LaunchCtx& c, const bf16* src, f16* dst, size_t n, int* status);
@@ -261,6 +261,56 @@ cudaError_t launch_sample_top_p(cudaStream_t st, int B, int V, const float* logi
 cudaError_t launch_gemm_tc(const LaunchCtx& c, int epi, const GemmArgs& a);
 bool gemm_tc_encode_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                         uint32_t box_rows);
+
+// Batched decode step as one cooperative kernel (k_step.cu): every layer of a decode step of
+// 16-64 sequences. The batch runs as two halves of at most 32 tokens; CTAs [0, gp) compute the
+// projections (tcgen05, weights streamed ahead through a TMA ring), CTAs [gp, grid) the
+// attention; phases are ordered by counters in global memory.
+constexpr int kStepMaxHalf = 32;     // tokens per half
+constexpr int kStepDoneSlots = 48;   // completion counters per (layer, half)
+constexpr int kStepDoneStride = 32;  // ints between counters (one 128-byte line each)
+struct StepKParams {
+    int L, D, I, QD, QKVR, n_heads, n_kv;
+    float eps, scale_log2;
+    const bf16* norms;  // per layer [input D][post-attention D][q_norm 128][k_norm 128]
+    const float* rope_cos;
+    const float* rope_sin;
+    float* x;           // [T][D] residual stream
+    f16* q;             // [T][QD] normalised, rotated queries
+    f16* attn;          // [T][QD] attention output
+    f16* act;           // [T][I] SiLU(gate) * up
+    float* part;        // split-K partials [2][units][32][128]
+    float* ss;          // [T][D / 128] sums of squares of x per 128-feature block
+    int* tick;          // [2][tiles] split-K arrival tickets (reset by the last arrival)
+    int* done;          // [L][2][kStepDoneSlots][kStepDoneStride] completion counters (zeroed before the launch)
+    float* att_po;      // attention partials [T][n_heads][att_stride][128]
+    float* att_pml;     // [T][n_heads][att_stride][2]
+    int* att_cnt;       // [T][n_kv] split arrival tickets (reset by the last arrival)
+    int att_stride;
+    TokView tv;
+    KVView kv;
+    int* status;
+    int* abort_g;       // set on a failed wait: every CTA stops
+    int T, nh[2], t0[2];
+    int chunk, nsplit;  // attention keys per split (multiple of 16), splits per token
+    int gp;             // CTAs of the projection role
+    float* dbg_hidden;  // optional [L][T][D]
+    int32_t* dbg_pos;
+    int32_t* dbg_slot;
+    f16* dbg_attn;      // optional [L][T][QD]
+    unsigned long long wait_ns;  // bound of every wait on another CTA
+    int extra;          // extra arrivals the first o_proj unit waits for (0 in normal use)
+    unsigned long long* trace;   // optional: per CTA trace_n records of 5 words (see qw_trace_set)
+    int trace_n;
+};
+size_t step_part_floats(int D, int I, int QKVR, int n_kv);
+int step_tiles(int D, int I, int QKVR);
+bool step_shape_ok(int D, int I, int QD, int QKVR, int n_heads, int n_kv);
+int step_smem_bytes();
+int step_blocks_per_sm();  // 0: the kernel cannot be resident (no launch possible)
+cudaError_t launch_decode_step(cudaStream_t st, const StepKParams& p, const CUtensorMap* tm_qkv,
+                               const CUtensorMap* tm_o, const CUtensorMap* tm_gu, const CUtensorMap* tm_dn,
+                               int grid);
 
 // Persistent decode kernel (k_mk.cu): one cooperative launch per decode step of <= 8 tokens.
 struct MkParams {

@@ -90,6 +90,7 @@ struct WsLayout {
     size_t wqkv, wo, wgu, wd, embed16, bqkv, bo, bg, bu, bd, norms, fnorm, rcos, rsin;
     size_t x, h, qkv, q, attn, act, part_o, part_ml, counters;
     size_t tok_seq, tok_pos, tok_slot, last, best, status, gen_tok, gen_cur, gen_out, mk_sync;
+    size_t st_part, st_ss, st_done, st_tick, st_abort;  // batched decode-step kernel
     size_t total;
     int part_T;
 };
@@ -137,6 +138,16 @@ static WsLayout layout_for(const qw_config& c) {
     L.best = take((size_t)c.max_batch * 8);
     L.status = take(4);
     L.mk_sync = take(16);  // persistent decode kernel: arrivals, generation, ticket, abort
+    {
+        // batched decode-step kernel: split-K partials, per-block sums of squares of x,
+        // completion counters and arrival tickets (adjacent: one memset clears both), abort word
+        const int QKVR = (int)QKV;
+        L.st_part = take(step_part_floats((int)D, (int)I, QKVR, c.n_kv_heads) * 4);
+        L.st_ss = take((size_t)2 * kStepMaxHalf * (D / 128) * 4);
+        L.st_done = take((size_t)c.n_layers * 2 * kStepDoneSlots * kStepDoneStride * 4);
+        L.st_tick = take((size_t)2 * step_tiles((int)D, (int)I, QKVR) * 4);
+        L.st_abort = take(4);
+    }
     L.gen_tok = take(T * 4);
     L.gen_cur = take((size_t)c.max_batch * 4);
     L.gen_out = take((size_t)c.max_batch * ((size_t)c.max_context + 1) * 4);
@@ -169,6 +180,14 @@ struct qw_model {
     int mk_grid;       // CTAs of the persistent decode kernel (0: not available)
     int mk_max_t;      // most tokens it takes
     bool use_mk;       // decode steps of <= mk_max_t tokens run as one persistent kernel
+    // batched decode-step kernel (decode steps of 16 .. 2 * kStepMaxHalf tokens)
+    bool step_ok;      // shape supported and one CTA per SM can be resident
+    bool use_step;     // QW_OPT_DECODE_STEP_KERNEL
+    int step_gp;       // CTAs of its projection role
+    unsigned long long step_wait_ns;  // bound of its waits on other CTAs
+    int step_extra;    // test-only: extra arrivals its first o_proj unit waits for
+    float *st_part, *st_ss;
+    int *st_done, *st_tick, *st_abort;
     unsigned long long* best;
     int32_t *gen_tok, *gen_cur, *gen_out;
     float* dbg_hidden;
@@ -294,6 +313,11 @@ extern "C" qw_status qw_init_weights(const qw_config* cfg, const qw_weight_ptrs*
     m->best = (unsigned long long*)(b + L.best);
     m->status = (int*)(b + L.status);
     m->mk_sync = (unsigned*)(b + L.mk_sync);
+    m->st_part = (float*)(b + L.st_part);
+    m->st_ss = (float*)(b + L.st_ss);
+    m->st_done = (int*)(b + L.st_done);
+    m->st_tick = (int*)(b + L.st_tick);
+    m->st_abort = (int*)(b + L.st_abort);
     m->gen_tok = (int32_t*)(b + L.gen_tok);
     m->gen_cur = (int32_t*)(b + L.gen_cur);
     m->gen_out = (int32_t*)(b + L.gen_out);
@@ -453,6 +477,19 @@ extern "C" qw_status qw_init_weights(const qw_config* cfg, const qw_weight_ptrs*
     m->mk_grid = mk_grid_size();
     m->mk_max_t = m->mk_grid > 0 ? std::min(mk_max_tokens(cfg->hidden, cfg->inter, cfg->n_heads * cfg->head_dim), 8) : 0;
     m->use_mk = false;  // opt in with QW_OPT_PERSISTENT_DECODE
+    m->step_ok = step_shape_ok((int)D, (int)I, (int)QD, m->qkv_rows, cfg->n_heads, cfg->n_kv_heads) &&
+                 step_blocks_per_sm() >= 1 &&
+                 m->num_sms >= 16;
+    m->use_step = false;  // opt in with QW_OPT_DECODE_STEP_KERNEL
+    m->step_gp = std::max(1, std::min(64, m->num_sms / 2));
+    m->step_wait_ns = 2000000000ull;
+    m->step_extra = 0;
+    if (cudaMemsetAsync(b + L.st_done, 0, L.st_abort + 4 - L.st_done, st) != cudaSuccess ||
+        cudaMemsetAsync(b + L.st_part, 0, L.st_ss - L.st_part, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess) {
+        fail(QW_ERR_CUDA, "workspace clear failed");
+        return fail_free(QW_ERR_CUDA);
+    }
     *out = m;
     return QW_OK;
 }
@@ -594,6 +631,22 @@ extern "C" qw_status qw_set_option(qw_model* m, int option, int value) {
             return QW_OK;
         case QW_OPT_SPLIT_DECODE:
             m->split_decode = value != 0;
+            return QW_OK;
+        case QW_OPT_DECODE_STEP_KERNEL:
+            if (value && !m->step_ok) return fail(QW_ERR_UNSUPPORTED, "decode-step kernel unavailable for this shape");
+            m->use_step = value != 0;
+            return QW_OK;
+        case QW_OPT_STEP_PROJ_CTAS:
+            if (value < 1 || value > m->num_sms - 1) return fail(QW_ERR_INVALID_ARG, "projection CTAs outside [1, SMs)");
+            m->step_gp = value;
+            return QW_OK;
+        case QW_OPT_TEST_WAIT_LIMIT_US:
+            if (value < 1) return fail(QW_ERR_INVALID_ARG, "wait limit must be >= 1 us");
+            m->step_wait_ns = (unsigned long long)value * 1000ull;
+            return QW_OK;
+        case QW_OPT_TEST_EXTRA_ARRIVALS:
+            if (value < 0) return fail(QW_ERR_INVALID_ARG, "extra arrivals must be >= 0");
+            m->step_extra = value;
             return QW_OK;
         default:
             return fail(QW_ERR_INVALID_ARG, "unknown option %d", option);
@@ -1040,12 +1093,58 @@ static qw_status run_step(qw_model* m, qw_kv* kv, const StepDesc& sd, bool prefi
     // The first kernel of a step waits for everything before it (no programmatic overlap), so
     // kernels of this step may read state written by earlier steps before their own wait.
     const LaunchCtx lc0 = {st, false, launches};
-    CUDA_TRY(launch_step_begin(lc0, sd, tokens, m->embed, c.vocab, D, m->x, tv, kvv, m->status));
+    const bool engine = !prefill && m->use_step && m->qbits == 16 && T >= 16 && T <= 2 * kStepMaxHalf &&
+                        (m->prof_kind == QW_PROF_OFF || m->prof_kind == QW_PROF_STEP);
+    CUDA_TRY(launch_step_begin(lc0, sd, tokens, m->embed, c.vocab, D, m->x, tv, kvv, m->status,
+                               engine ? m->st_ss : nullptr));
+    if (engine) {
+        // every layer of the step in one cooperative kernel (counters cleared first)
+        CUDA_TRY(cudaMemsetAsync(m->st_done, 0, (size_t)c.n_layers * 2 * kStepDoneSlots * kStepDoneStride * 4, st));
+        StepKParams sp = {};
+        sp.L = c.n_layers; sp.D = D; sp.I = I; sp.QD = QD; sp.QKVR = m->qkv_rows;
+        sp.n_heads = c.n_heads; sp.n_kv = c.n_kv_heads; sp.eps = c.rms_eps;
+        sp.scale_log2 = 0.08838834764831845f * 1.4426950408889634f;  // 128^-0.5 * log2(e)
+        sp.norms = m->norms; sp.rope_cos = m->rcos; sp.rope_sin = m->rsin;
+        sp.x = m->x; sp.q = m->q; sp.attn = m->attn; sp.act = m->act;
+        sp.part = m->st_part; sp.ss = m->st_ss; sp.tick = m->st_tick; sp.done = m->st_done;
+        sp.att_po = m->part_o; sp.att_pml = m->part_ml; sp.att_cnt = m->counters; sp.att_stride = kMaxSplits;
+        sp.tv = tv; sp.kv = kvv; sp.status = m->status; sp.abort_g = m->st_abort;
+        sp.T = T;
+        sp.nh[0] = T / 2; sp.nh[1] = T - T / 2;
+        sp.t0[0] = 0; sp.t0[1] = T / 2;
+        sp.gp = m->step_gp;
+        {
+            // attention units: ~3 per attention warp per layer and half
+            const int pairs = sp.nh[1] * c.n_kv_heads;
+            const int warps = (m->num_sms - sp.gp) * 8;
+            const int want = std::max(1, std::min(kMaxSplits, (3 * warps + pairs - 1) / pairs));
+            int chunk = std::max(64, ((max_keys + want - 1) / want + 15) / 16 * 16);
+            while ((max_keys + chunk - 1) / chunk > kMaxSplits) chunk += 16;
+            sp.chunk = chunk;
+            sp.nsplit = (max_keys + chunk - 1) / chunk;
+        }
+        sp.dbg_hidden = dbg ? m->dbg_hidden : nullptr;
+        sp.dbg_pos = dbg ? m->dbg_pos : nullptr;
+        sp.dbg_slot = dbg ? m->dbg_slot : nullptr;
+        sp.dbg_attn = dbg ? m->dbg_attn : nullptr;
+        sp.wait_ns = m->step_wait_ns;
+        sp.extra = m->step_extra;
+        sp.trace = m->trace;
+        sp.trace_n = m->trace_n;
+        {
+            int pc0[16] = {0};
+            ProfScope prof_scope_(m, QW_PROF_STEP, pc0, st);
+            if (launches) ++*launches;
+            CUDA_TRY(launch_decode_step(st, sp, &m->tm_wqkv, &m->tm_wo, &m->tm_wgu, &m->tm_wd, m->num_sms));
+        }
+    }
     // A decode batch of >= 16 sequences runs as two halves on two streams, so that one
     // half's latency-bound projections overlap the other half's HBM-bound attention.
     // With the debug dumps on, each half writes its own rows of them (the same kernels run).
-    const bool two = !prefill && !small && m->prof_kind == QW_PROF_OFF && m->split_decode && T >= 16;
-    if (two) {
+    const bool two = !engine && !prefill && !small && m->prof_kind == QW_PROF_OFF && m->split_decode && T >= 16;
+    if (engine) {
+        // the layers ran above
+    } else if (two) {
         const int h0 = T / 2;
         CUDA_TRY(cudaEventRecord(m->ev_fork, st));
         CUDA_TRY(cudaStreamWaitEvent(m->aux_stream, m->ev_fork, 0));
@@ -1175,6 +1274,9 @@ extern "C" qw_status qw_decode_step(qw_model* m, qw_kv* kv, int B, const int* se
         key.push_back(m->use_mk ? 1 : 0);
         key.push_back(m->pdl ? 1 : 0);
         key.push_back(m->split_decode ? 1 : 0);
+        key.push_back(m->use_step ? m->step_gp : 0);
+        key.push_back((long long)m->step_wait_ns);
+        key.push_back(m->step_extra);
         key.push_back(m->prof_kind || m->trace ? (long long)m->prof_gen : 0);
         for (int b = 0; b < B; ++b) key.push_back(seq_ids[b]);
         auto it = m->graphs.find(key);
@@ -1306,6 +1408,12 @@ extern "C" qw_status qw_sync_status(qw_model* m, void* stream_) {
     CUDA_TRY(cudaMemcpy(&word, m->status, 4, cudaMemcpyDeviceToHost));
     CUDA_TRY(cudaMemset(m->status, 0, 4));
     CUDA_TRY(cudaMemset(m->mk_sync, 0, 16));
+    CUDA_TRY(cudaMemset(m->st_abort, 0, 4));
+    if (word & QW_DEV_TIMEOUT) {
+        // a kernel that gave up may have left arrival tickets behind
+        CUDA_TRY(cudaMemset(m->st_tick, 0, (size_t)2 * step_tiles(m->cfg.hidden, m->cfg.inter, m->qkv_rows) * 4));
+        CUDA_TRY(cudaMemset(m->counters, 0, (size_t)m->L.part_T * m->cfg.n_kv_heads * 4));
+    }
     if (word & QW_DEV_BAD_TOKEN) return fail(QW_ERR_BAD_TOKEN, "a token id was outside [0, vocab)");
     if (word & QW_DEV_BAD_POS) return fail(QW_ERR_BAD_POS, "a position had no reserved page");
     if (word & QW_DEV_TIMEOUT) return fail(QW_ERR_TIMEOUT, "a bounded wait in a kernel timed out");

@@ -276,6 +276,10 @@ def qw_lm_head_argmax_noalloc(model: int, B: int, x_ptr: int, logits_ptr: int, n
 QW_OPT_PERSISTENT_DECODE = 1
 QW_OPT_PDL = 2
 QW_OPT_SPLIT_DECODE = 3
+QW_OPT_DECODE_STEP_KERNEL = 4
+QW_OPT_STEP_PROJ_CTAS = 5
+QW_OPT_TEST_WAIT_LIMIT_US = 6
+QW_OPT_TEST_EXTRA_ARRIVALS = 7
 
 
 def qw_set_option(model: int, option: int, value: int) -> None:

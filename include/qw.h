@@ -260,8 +260,25 @@ enum {
     /* 1 (default): a decode step of >= 16 sequences runs as two halves on two streams whose
      * kernels overlap (each half's projections run while the other half's attention reads
      * the KV cache); 0: one chain. Results agree within rounding (the attention's key split
-     * depends on the batch size). */
-    QW_OPT_SPLIT_DECODE = 3
+     * depends on the batch size). Not used for steps the decode-step kernel runs. */
+    QW_OPT_SPLIT_DECODE = 3,
+    /* 1 (where the shape allows it and one 256-thread CTA per SM fits; default 0): the layers of
+     * a decode step of 16 .. 64 sequences run as ONE cooperative kernel -- the batch as two
+     * halves, projection CTAs (tcgen05 GEMMs with weights streamed ahead) and attention CTAs
+     * ordered by counters in global memory, so one half's projections overlap the other
+     * half's attention without kernel boundaries; 0: the launch-per-phase path. Both compute
+     * the same operations; results agree within rounding. */
+    QW_OPT_DECODE_STEP_KERNEL = 4,
+    /* CTAs given to the projection role of the decode-step kernel (default min(64, SMs / 2));
+     * the rest run attention. Valid: 1 .. SMs - 1. */
+    QW_OPT_STEP_PROJ_CTAS = 5,
+    /* Bound, in microseconds, of every wait of the decode-step kernel on another CTA (default
+     * 2,000,000). When a wait runs out the kernel sets QW_ERR_TIMEOUT in the status word, every
+     * CTA stops, and qw_sync_status reports it and clears the kernel's counters. For tests. */
+    QW_OPT_TEST_WAIT_LIMIT_US = 6,
+    /* Test only: the first o_proj unit of the decode-step kernel waits for this many arrivals
+     * more than the attention provides (default 0), so that its wait runs out. */
+    QW_OPT_TEST_EXTRA_ARRIVALS = 7
 };
 qw_status qw_set_option(qw_model* m, int option, int value);
 

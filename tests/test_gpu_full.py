@@ -3,9 +3,10 @@ bench.py times (same shapes, batch composition, input recipe and call sequence),
 sampled sequences that the oracle recomputes one by one:
 
   * batched decode: 64 sequences, 1024-token prompts prefilled 16 sequences per call, then
-    4 greedy decode steps of all 64 (two-stream split path: sequences 0-31 on one stream,
-    32-63 on the other) -- sequences 0, 31, 32 and 63, the hidden state after every layer
-    of every decode step, the logits and the ids;
+    4 greedy decode steps of all 64, through the two-stream split path (sequences 0-31 on one
+    stream, 32-63 on the other) and again, from the same cache and with the same tokens,
+    through the decode-step kernel (the same halves) -- sequences 0, 31, 32 and 63, the
+    hidden state after every layer of every decode step, the logits and the ids;
   * prefill: 16 x 512 tokens in one call -- sequences 0 and 15 (every layer's hidden state,
     the final logits and ids), plus positions and KV slots of all 8192 tokens;
   * long-context ragged decode: 8 sequences with cached lengths drawn uniform in
@@ -58,17 +59,35 @@ def test_batched_decode_b64_full(qw, om):
             o = oracle.forward(om, toks[b].tolist(), caches[b])
             check_logits(logits[b], o["logits"])
             check_token(nxt[b], o["logits"])
+        feeds, want = [], []
         for step in range(ND):
             feed = nxt.copy()
             d = run.decode(list(range(B)), feed.tolist(), debug=True)
             assert d["status"] == 0
             np.testing.assert_array_equal(d["pos"], np.full(B, P + step))
+            outs = {}
             for b in sample:
                 o = oracle.forward(om, [int(feed[b])], caches[b])
                 check_hidden(d["hidden"][:, b:b + 1], o["hidden"])
                 check_logits(d["logits"][b], o["logits"])
                 check_token(d["next"][b], o["logits"])
+                outs[b] = o
+            feeds.append(feed)
+            want.append(outs)
             nxt = d["next"].astype(np.int64)
+        # the same steps through the decode-step kernel, fed the same tokens, from the same cache
+        qw.qw.qw_set_option(eng.model, qw.qw.QW_OPT_DECODE_STEP_KERNEL, 1)
+        for b in range(B):
+            qw.qw.qw_kv_truncate(eng.kv, b, P, eng.stream)
+        for step in range(ND):
+            d = run.decode(list(range(B)), feeds[step].tolist(), debug=True)
+            assert d["status"] == 0
+            np.testing.assert_array_equal(d["pos"], np.full(B, P + step))
+            for b in sample:
+                o = want[step][b]
+                check_hidden(d["hidden"][:, b:b + 1], o["hidden"])
+                check_logits(d["logits"][b], o["logits"])
+                check_token(d["next"][b], o["logits"])
     finally:
         eng.close()
 

@@ -88,42 +88,74 @@ def test_batch_invariance_and_determinism(blk):
     check_logits(d1["logits"][0], res[0][5], tol=2e-2)
 
 
+MODES = {  # (QW_OPT_DECODE_STEP_KERNEL, QW_OPT_SPLIT_DECODE)
+    "step_kernel": (1, 1),   # the whole decode step as one cooperative kernel
+    "two_streams": (0, 1),   # launch per phase, two halves on two streams
+    "one_chain": (0, 0),     # launch per phase, one chain
+}
+
+
 @pytest.mark.parametrize("B", [17, 32])
-def test_two_stream_decode(blk, B):
-    """A decode batch of >= 16 sequences runs as two halves on two streams (ragged halves for
-    odd B); every sequence's hidden state after the layer, logits and id match the oracle,
-    and the one-chain run agrees within rounding."""
+def test_batched_decode_paths(blk, B):
+    """A decode batch of >= 16 sequences through each of its three paths (ragged halves for
+    odd B): every sequence's hidden state after the layer, logits and id match the oracle,
+    and the paths agree with each other within rounding."""
     run, om = blk
     qw, eng = run.qw, run.eng
     seqs = list(range(B))
     prompts = [synth.make_tokens(S1.vocab, 2 + (i % 5), 1100 + i).tolist() for i in range(B)]
     forced = synth.make_tokens(S1.vocab, 2 * B, 1177).reshape(2, B)
     out = {}
-    for split in (1, 0):
-        qw.qw_set_option(eng.model, qw.QW_OPT_SPLIT_DECODE, split)
-        qw.qw_kv_reset(eng.kv, -1, eng.stream)
-        g = run.prefill(seqs, prompts, debug=False, reserve_extra=3)
-        caches = []
-        for b, p in enumerate(prompts):
-            c = oracle.SeqCache(1)
-            oracle.forward(om, p, c)
-            caches.append(c)
-        logits = []
-        for step in range(2):
-            # the split run also dumps every layer's hidden state (each half writes its rows)
-            d = run.decode(seqs, forced[step].tolist(), debug=bool(split))
-            assert d["status"] == 0
-            for b in range(B):
-                o = oracle.forward(om, [int(forced[step, b])], caches[b])
-                if split:
-                    check_hidden(d["hidden"][:, b:b + 1], o["hidden"])
-                check_logits(d["logits"][b], o["logits"])
-                check_token(d["next"][b], o["logits"])
-            logits.append(d["logits"])
-        out[split] = logits
-    qw.qw_set_option(eng.model, qw.QW_OPT_SPLIT_DECODE, 1)
-    for a, b in zip(out[1], out[0]):
-        check_logits(a, b, tol=2e-2)
+    try:
+        for mode, (step, split) in MODES.items():
+            qw.qw_set_option(eng.model, qw.QW_OPT_DECODE_STEP_KERNEL, step)
+            qw.qw_set_option(eng.model, qw.QW_OPT_SPLIT_DECODE, split)
+            qw.qw_kv_reset(eng.kv, -1, eng.stream)
+            run.prefill(seqs, prompts, debug=False, reserve_extra=3)
+            caches = []
+            for b, p in enumerate(prompts):
+                c = oracle.SeqCache(1)
+                oracle.forward(om, p, c)
+                caches.append(c)
+            logits = []
+            for step_i in range(2):
+                # the first step dumps every layer's hidden state; the second replays a graph
+                d = run.decode(seqs, forced[step_i].tolist(), debug=(step_i == 0))
+                assert d["status"] == 0
+                for b in range(B):
+                    o = oracle.forward(om, [int(forced[step_i, b])], caches[b])
+                    if step_i == 0:
+                        check_hidden(d["hidden"][:, b:b + 1], o["hidden"])
+                    check_logits(d["logits"][b], o["logits"])
+                    check_token(d["next"][b], o["logits"])
+                logits.append(d["logits"])
+            out[mode] = logits
+    finally:
+        qw.qw_set_option(eng.model, qw.QW_OPT_DECODE_STEP_KERNEL, 0)
+        qw.qw_set_option(eng.model, qw.QW_OPT_SPLIT_DECODE, 1)
+    for mode in ("two_streams", "one_chain"):
+        for a, b in zip(out["step_kernel"], out[mode]):
+            check_logits(a, b, tol=2e-2)
+
+
+def test_step_kernel_deterministic(blk):
+    """The decode-step kernel adds its split-K partials and attention splits in a fixed order:
+    two runs of the same batch give bit-identical logits."""
+    run, _ = blk
+    qw, eng = run.qw, run.eng
+    B = 24
+    prompts = [synth.make_tokens(S1.vocab, 3 + i % 4, 1300 + i).tolist() for i in range(B)]
+    res = []
+    qw.qw_set_option(eng.model, qw.QW_OPT_DECODE_STEP_KERNEL, 1)
+    try:
+        for _ in range(2):
+            qw.qw_kv_reset(eng.kv, -1, eng.stream)
+            g = run.prefill(list(range(B)), prompts, debug=False, reserve_extra=2)
+            d = run.decode(list(range(B)), g["next"].tolist(), debug=False)
+            res.append(d["logits"])
+    finally:
+        qw.qw_set_option(eng.model, qw.QW_OPT_DECODE_STEP_KERNEL, 0)
+    np.testing.assert_array_equal(res[0], res[1])
 
 
 class _PeakyQK:

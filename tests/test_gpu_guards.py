@@ -101,3 +101,47 @@ def test_norm_weight_too_large_is_refused(qw):
     with pytest.raises(qw.qw.QwError) as e:
         qw.qw.Engine(S1, dict(w.named()), max_tokens=16, max_batch=4, max_context=64, kv_pages=8, max_seqs=4)
     assert e.value.status == -1
+
+
+def test_step_kernel_wait_runs_out(qw):
+    """A bounded wait of the decode-step kernel that runs out: with a 1 ms limit and one
+    arrival more than the attention provides, the first o_proj unit gives up, the kernel
+    stops every CTA and qw_sync_status reports QW_ERR_TIMEOUT (no trap, no fault). The next
+    normal step on the same model, from the same cache, matches the oracle."""
+    import oracle
+    from gpu_util import check_hidden, check_logits, check_token
+
+    s = S1
+    eng = qw.qw.Engine(s, dict(weights(s).named()), max_tokens=64, max_batch=16, max_context=64, kv_pages=64,
+                       max_seqs=16)
+    try:
+        run = Run(qw, eng)
+        om = oracle.Model(weights(s))
+        B = 16
+        seqs = list(range(B))
+        prompts = [synth.make_tokens(s.vocab, 2 + i % 3, 2100 + i).tolist() for i in range(B)]
+        g = run.prefill(seqs, prompts, debug=False, reserve_extra=2)
+        feed = g["next"].tolist()
+        qw.qw.qw_set_option(eng.model, qw.qw.QW_OPT_DECODE_STEP_KERNEL, 1)
+        qw.qw.qw_set_option(eng.model, qw.qw.QW_OPT_TEST_WAIT_LIMIT_US, 1000)
+        qw.qw.qw_set_option(eng.model, qw.qw.QW_OPT_TEST_EXTRA_ARRIVALS, 1)
+        try:
+            d = run.decode(seqs, feed, debug=False, check=False)
+        finally:
+            qw.qw.qw_set_option(eng.model, qw.qw.QW_OPT_TEST_EXTRA_ARRIVALS, 0)
+            qw.qw.qw_set_option(eng.model, qw.qw.QW_OPT_TEST_WAIT_LIMIT_US, 2000000)
+        assert d["status"] == -6, qw.qw.qw_last_error()
+        # the timed-out step is discarded: every sequence back to its prompt
+        for sq, p in zip(seqs, prompts):
+            qw.qw.qw_kv_truncate(eng.kv, sq, len(p), eng.stream)
+        d = run.decode(seqs, feed, debug=True)
+        assert d["status"] == 0
+        for b, p in enumerate(prompts):
+            c = oracle.SeqCache(1)
+            oracle.forward(om, p, c)
+            o = oracle.forward(om, [feed[b]], c)
+            check_hidden(d["hidden"][:, b:b + 1], o["hidden"])
+            check_logits(d["logits"][b], o["logits"])
+            check_token(d["next"][b], o["logits"])
+    finally:
+        eng.close()

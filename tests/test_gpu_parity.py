@@ -208,8 +208,9 @@ def test_degenerate_calls_are_rejected(one_block):
         lambda: qw.qw_decode_step(eng.model, eng.kv, [1, 1], t, 0, n, eng.stream),       # repeated id
         lambda: qw.qw_decode_step(eng.model, eng.kv, list(range(17)), t, 0, n, eng.stream),  # > max_batch
     ]
-    # generate: pages reserved beyond max_context (512) do not let prompt + decode steps pass it
-    qw.qw_kv_reserve(eng.kv, 2, 600, eng.stream)
+    # generate: prompt + decode steps beyond max_context (512) are refused before any work,
+    # although the reserved pages hold them
+    qw.qw_kv_reserve(eng.kv, 2, 512, eng.stream)
     h_prompt = np.ones(8, np.int32)
     h_out = np.zeros((1, 506), np.int32)
     calls.append(lambda: qw.qw_generate(eng.model, eng.kv, [2], [8], h_prompt, 505, h_out, eng.stream))
@@ -281,10 +282,21 @@ def one_block_long_batch(qw):
     eng.close()
 
 
-def test_injected_long_cache_batched_decode(one_block_long_batch):
-    """More than 8 sequences (tensor-core projections) with caches longer than 4096 keys: the
-    evenly split decode attention behind the q|k|v epilogue."""
-    test_injected_long_cache_forced_decode(one_block_long_batch, (5000, 17, 4100, 300, 6001, 2, 4097, 900, 33, 5555))
+@pytest.mark.parametrize("lens", [(5000, 17, 4100, 300, 6001, 2, 4097, 900, 33, 5555),
+                                  (5000, 17, 4100, 300, 6001, 2, 4097, 900, 33, 5555, 1, 64, 65, 2000, 16, 7000)])
+def test_injected_long_cache_batched_decode(one_block_long_batch, lens):
+    """More than 8 sequences (tensor-core projections) with caches longer than 4096 keys: 10
+    sequences take the evenly split decode attention behind the q|k|v epilogue; 16 run both
+    through the launch-per-phase path and through the decode-step kernel (ragged caches from
+    1 to 7000 keys)."""
+    run = one_block_long_batch[0]
+    modes = (0, 1) if len(lens) >= 16 else (0,)
+    try:
+        for mode in modes:
+            run.qw.qw_set_option(run.eng.model, run.qw.QW_OPT_DECODE_STEP_KERNEL, mode)
+            test_injected_long_cache_forced_decode(one_block_long_batch, lens)
+    finally:
+        run.qw.qw_set_option(run.eng.model, run.qw.QW_OPT_DECODE_STEP_KERNEL, 0)
 
 
 @pytest.mark.parametrize("lens", [(2047, 3001), (1, 300, 4000), (5000, 700, 6100)])
