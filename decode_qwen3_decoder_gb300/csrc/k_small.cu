@@ -39,11 +39,13 @@ __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + expf(-g));
 // positions continue from the sequence's current length).
 // =======================================================================================
 // ss (optional): per token, the sum of squares of x over each 128-feature block
-// [t][hidden / 128] (the batched decode-step kernel builds its first RMSNorm from it).
+// [t][hidden / 128], and xw = fp16(x * nw) [t][hidden] with nw the first layer's input-norm
+// weight (the batched decode-step kernel builds its first RMSNorm from these).
 __global__ void __launch_bounds__(256) k_step_begin(StepDesc sd, const int32_t* __restrict__ ids,
                                                     const bf16* __restrict__ embed, int vocab,
                                                     int hidden, float* __restrict__ x, TokView tv,
-                                                    KVView kv, int* status, float* __restrict__ ss) {
+                                                    KVView kv, int* status, float* __restrict__ ss,
+                                                    const bf16* __restrict__ nw, f16* __restrict__ xw) {
     pdl_launch();
     pdl_wait();
     const int t = blockIdx.x;
@@ -61,6 +63,11 @@ __global__ void __launch_bounds__(256) k_step_begin(StepDesc sd, const int32_t* 
         if (ss) {  // a warp covers the 128 features of block k / 128
             const float q = warp_sum(o.x * o.x + o.y * o.y + o.z * o.z + o.w * o.w);
             if ((threadIdx.x & 31) == 0) ss[(size_t)t * (hidden / 128) + k / 128] = q;
+            const uint2 wv = *reinterpret_cast<const uint2*>(nw + k);
+            uint2 h;
+            h.x = pack_h2(o.x * bf_lo(wv.x), o.y * bf_hi(wv.x));
+            h.y = pack_h2(o.z * bf_lo(wv.y), o.w * bf_hi(wv.y));
+            *reinterpret_cast<uint2*>(xw + (size_t)t * hidden + k) = h;
         }
     }
     if (threadIdx.x == 0) {
@@ -79,9 +86,9 @@ __global__ void __launch_bounds__(256) k_step_begin(StepDesc sd, const int32_t* 
 
 cudaError_t launch_step_begin(const LaunchCtx& c, const StepDesc& sd, const int32_t* ids,
                               const bf16* embed, int vocab, int hidden, float* x, TokView tv,
-                              KVView kv, int* status, float* ss) {
+                              KVView kv, int* status, float* ss, const bf16* w, f16* xw) {
     return launch_k(c, k_step_begin, dim3(sd.T), dim3(256), 0, sd, ids, embed, vocab, hidden, x, tv,
-                    kv, status, ss);
+                    kv, status, ss, w, xw);
 }
 
 // =======================================================================================

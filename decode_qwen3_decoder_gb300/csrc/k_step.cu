@@ -13,34 +13,39 @@
 //  * CTAs [0, gp) -- projection role. Each phase (q|k|v, o_proj, gate/up, down_proj of one
 //    layer and half) is a set of units = (128-row weight tile, K range); unit u of phase i
 //    belongs to CTA (u + 13 i) mod gp. A producer warp streams the weight k-blocks of the
-//    CTA's units, in program order, through an 8-stage TMA ring (128 x 64 fp16, 128-byte
+//    CTA's units, in program order, through an 11-stage TMA ring (128 x 64 fp16, 128-byte
 //    swizzle): weights depend on nothing computed in the step, so the ring runs ahead across
-//    phases and layers while the CTA waits for activations. Per unit, four warps wait for
-//    the unit's inputs, build the token operand in shared memory (for q|k|v and gate/up the
-//    RMSNorm is applied here, from per-block sums of squares that the residual epilogues
-//    write), one thread issues tcgen05.mma (M = 128 weight rows, N = 16/32 tokens, fp16, fp32
-//    accumulator in TMEM), and the four warps write the fp32 partial to global memory. The
-//    last unit of a tile to arrive (an atomic ticket) adds the K-range partials in a fixed
-//    order and applies the epilogue: QK-norm + RoPE + KV append (q|k|v), x += (o_proj,
-//    down_proj, plus the new per-block sums of squares), SiLU(gate) * up (gate/up). It then
-//    bumps the phase's completion counter.
+//    phases and layers while the CTA waits for activations. Per unit, once its inputs are
+//    complete, one thread loads the token operand (32 rows of the half, K range of the unit)
+//    with TMA from an fp16 activation buffer, one thread issues tcgen05.mma (M = 128 weight
+//    rows, N = 32 tokens, fp16, fp32 accumulator in TMEM), and four warps write the fp32
+//    partial to global memory. The last unit of a tile to arrive (an atomic ticket) adds the
+//    K-range partials in a fixed order and applies the epilogue:
+//      q|k|v     x RMSNorm scale of the token, QK-norm + RoPE + KV append, q stored;
+//      gate/up   x RMSNorm scale, SiLU(gate) * up stored;
+//      o / down  x += W h, the token's sums of squares per 128-feature block, and
+//                fp16(x * w) for the next RMSNorm (w = its weight): the next q|k|v or
+//                gate/up operand, whose 1/RMS is applied in that epilogue (RMSNorm is a
+//                per-token scale, so it commutes with the projection).
+//    It then bumps the phase's completion counter.
 //  * CTAs [gp, grid) -- attention role. Eight warps each take (token, KV head, key range)
-//    units of each layer and half, wait for that KV head's q|k|v tiles, and run a flash-
-//    decode online softmax over the cached 16-key pages (two pages in flight per warp) for
-//    both query heads of the KV head; key ranges merge in the warp that finishes last.
+//    units of each layer and half and run a flash-decode online softmax over the cached
+//    16-key pages for both query heads of the KV head; each warp streams its pages (K and V,
+//    4 KB each) with bulk TMA copies into its own 3-stage ring. Key ranges merge in the warp
+//    that finishes last.
 //
-// Dependencies (per layer l and half h): q|k|v tiles of KV head g -> attention of (., g) ->
-// o_proj units of K range g -> gate/up -> down_proj units of K range s (act features of
-// gate/up tiles [6s, 6s + 6)) -> q|k|v of layer l + 1. The projection program interleaves
-// the halves (o, gate/up, down, next q|k|v of A; then of B) so that half B's chain runs while
-// half A's attention runs and vice versa. Every unit waits only on units that come earlier
-// in the other CTAs' programs, and all CTAs are co-resident (cooperative launch), so the
-// waits end. Each wait is bounded: on timeout the kernel records QW_DEV_TIMEOUT, raises a
-// global abort word that stops every CTA, lets its copies and MMAs complete, frees TMEM and
-// returns.
+// Dependencies (per layer l and half h): all q|k|v tiles -> attention of (., g) -> o_proj
+// units of K range g -> gate/up -> down_proj units of K range s (act features of gate/up
+// tiles [6s, 6s + 6)) -> q|k|v of layer l + 1. The projection program interleaves the halves
+// (o, gate/up, down, next q|k|v of A; then of B) so that half B's chain runs while half A's
+// attention runs and vice versa. Every unit waits only on units that come earlier in the
+// other CTAs' programs, and all CTAs are co-resident (cooperative launch), so the waits end.
+// Each wait is bounded: on timeout the kernel records QW_DEV_TIMEOUT, raises a global abort
+// word that stops every CTA, lets its copies and MMAs complete, frees TMEM and returns.
 //
-// Cross-CTA data is read with ld.global.cg (L2), never through the non-coherent path;
-// producers publish with __threadfence() before their counter increments.
+// Cross-CTA data is read with ld.global.cg (L2) or TMA, never through the non-coherent path;
+// producers publish with __threadfence() (and a generic-to-async proxy fence, since the
+// consumers read with TMA) before their counter increments.
 #include "qw_internal.h"
 #include "tc_sm103.cuh"
 #include "gemm_epi.cuh"
@@ -48,20 +53,29 @@
 namespace {
 
 constexpr int ST_THREADS = 256;
-constexpr int ST_NST = 8;                                // weight ring stages
+constexpr int ST_NST = 11;                               // weight ring stages
 constexpr int ST_STAGE = BM * BK * 2;                    // one 128 x 64 fp16 k-block (16 KB)
 constexpr int ST_MAXKB = 8;                              // k-blocks per unit
-constexpr int ST_BBYTES = ST_MAXKB * kStepMaxHalf * 128; // token operand (32 KB)
-constexpr int ST_EBYTES = 32 * EP * 4;                   // epilogue staging tile
+constexpr int ST_N = kStepMaxHalf;                       // MMA N: the 32 token rows of a half
+constexpr int ST_BBOX = ST_N * 128;                      // one [32][64] fp16 operand box (4 KB)
+constexpr int ST_BBYTES = ST_MAXKB * ST_BBOX;            // token operand (32 KB)
+constexpr int A_NPS = 3;                                 // attention: page stages per warp
+constexpr int A_STAGE = 2 * 16 * 128 * 2;                // K and V of one 16-key page (8 KB)
+// shared memory (offsets from a 1024-aligned base). Projection role: weight ring, then the
+// token operand, whose space the epilogue reuses for its staging tile. Attention role: one
+// page ring per warp over the same space.
 constexpr int SO_B = ST_NST * ST_STAGE;
-constexpr int SO_E = SO_B + ST_BBYTES;
-constexpr int SO_NW = SO_E + ST_EBYTES;
+constexpr int SO_END0 = SO_B + ST_BBYTES;
+static_assert((ST_THREADS / 32) * A_NPS * A_STAGE <= SO_END0, "attention rings fit the projection space");
+static_assert(32 * EP * 4 <= ST_BBYTES, "epilogue staging fits the operand space");
+constexpr int SO_NW = SO_END0;
 constexpr int SO_META = SO_NW + 256 * 4;
 constexpr int SO_RED = SO_META + 64 * 4;
 constexpr int SO_RS = SO_RED + 4 * 32 * 4;
 constexpr int SO_BAR = SO_RS + 32 * 4;
-constexpr int ST_NBAR = 2 * ST_NST + 3;  // full[], empty[], operand ready, accumulator ready, MMA drain
-constexpr int SO_MISC = SO_BAR + ST_NBAR * 8;
+constexpr int ST_NBAR = 2 * ST_NST + 3;  // full[], empty[], operand full, accumulator ready, MMA drain
+constexpr int SO_ABAR = SO_BAR + ST_NBAR * 8;
+constexpr int SO_MISC = SO_ABAR + (ST_THREADS / 32) * A_NPS * 8;
 constexpr int ST_SMEM = 1024 + SO_MISC + 64;
 
 enum { KQKV = 0, KO = 1, KGU = 2, KDN = 3 };
@@ -130,22 +144,26 @@ __device__ __forceinline__ int ld_relaxed(const int* a) {
     asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
     return v;
 }
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
 __device__ __forceinline__ uint4 ldcg16(const void* a) { return __ldcg(reinterpret_cast<const uint4*>(a)); }
+// generic-proxy global writes of this thread vs. later TMA reads (either side of a handoff)
+__device__ __forceinline__ void fence_proxy_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
 // Bounded wait that ignores the abort flags: used to let this CTA's own copies and MMAs land
 // before it exits.
-__device__ __forceinline__ void mbar_drain(uint32_t bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity) {
     const uint64_t t0 = globaltimer_ns();
     while (!mbar_try_wait(bar, parity))
-        if (globaltimer_ns() - t0 > kTcWaitNs) break;
+        if (globaltimer_ns() - t0 > kTcWaitNs) return false;
+    return true;
 }
 
 // Wait until *ctr >= target, bounded by p.wait_ns; gives up at once if the grid aborted. A
-// timeout records QW_DEV_TIMEOUT and aborts the grid.
-// The counter is polled with relaxed loads (a backoff keeps the L2 line free for the
-// increments) and one fence orders the reads that follow the successful poll.
+// timeout records QW_DEV_TIMEOUT and aborts the grid. The counter is polled with relaxed
+// loads (a backoff keeps the line free for the increments); one fence orders what follows.
 __device__ bool wait_ge(const StepKParams& p, const int* ctr, int target) {
     if (ld_relaxed(ctr) >= target) {
         __threadfence();
@@ -261,8 +279,10 @@ __device__ __forceinline__ void page_step(WarpSoftmax& w, const uint4 (&kk)[8], 
 }
 
 // Attention of token `tok` (query heads 2g, 2g+1 over KV head g), keys [k0, k1), by one warp.
-// Returns false if the grid aborted.
-__device__ bool attn_unit(const StepKParams& p, int l, int h, int tok, int g, int s, int n_act, int k0, int k1) {
+// The warp's pages stream through its ring (A_NPS stages at `ring`, barriers from `bar0`);
+// pc counts the pages this warp has streamed (it sets each stage's phase).
+__device__ void attn_unit(const StepKParams& p, int l, int h, int tok, int g, int s, int n_act, int k0, int k1,
+                          uint8_t* ring, uint32_t bar0, uint32_t& pc) {
     const int lane = threadIdx.x & 31, half = lane >> 4, dl = (lane & 15) * 8;
     WarpSoftmax w;
     {
@@ -285,30 +305,41 @@ __device__ bool attn_unit(const StepKParams& p, int l, int h, int tok, int g, in
     const int* pt = p.kv.page_table + (size_t)seq * p.kv.max_pages_per_seq;
     const f16* Kl = p.kv.k + (size_t)l * p.kv.layer_stride;
     const f16* Vl = p.kv.v + (size_t)l * p.kv.layer_stride;
-    const int p0 = k0 >> 4, p1 = (k1 + 15) >> 4;
-    uint4 ka[8], va[8], kb[8], vb[8];
-    int nva = 0, nvb = 0;
+    const int p0 = k0 >> 4, np = ((k1 + 15) >> 4) - p0;
     // page ids of the first 32 pages of the range, one per lane (one load for all of them)
-    const int pt_lane = (p0 + lane < p1) ? pt[p0 + lane] : -1;
-    // two pages in flight: the next page is requested before the current one is used
-    auto fetch = [&](int pg, uint4(&kk)[8], uint4(&vv)[8], int& nv) {
-        const int page = (pg - p0 < 32) ? __shfl_sync(0xffffffffu, pt_lane, (pg - p0) & 31) : pt[pg];
-        nv = (page < 0 || page >= p.kv.n_pages) ? 0 : min(16, k1 - pg * 16);  // a missing page is reported by the append
-        const size_t off = ((size_t)(nv > 0 ? page : 0) * p.n_kv + g) * 16 * 128 + dl;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) kk[i] = ldcg16(Kl + off + (size_t)(2 * i + half) * 128);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) vv[i] = ldcg16(Vl + off + (size_t)(2 * i + half) * 128);
+    const int pt_lane = (lane < np) ? pt[p0 + lane] : -1;
+    auto page_of = [&](int i) {  // called by all lanes
+        const int pid = (i < 32) ? __shfl_sync(0xffffffffu, pt_lane, i & 31) : pt[p0 + i];
+        return (pid < 0 || pid >= p.kv.n_pages) ? -1 : pid;  // a missing page is reported by the append
     };
-    fetch(p0, ka, va, nva);
-    for (int pg = p0; pg < p1; pg += 2) {
-        if (pg + 1 < p1) fetch(pg + 1, kb, vb, nvb);
-        page_step(w, ka, va, nva, half);
-        if (pg + 1 < p1) {
-            if (pg + 2 < p1) fetch(pg + 2, ka, va, nva);
-            page_step(w, kb, vb, nvb, half);
+    auto issue = [&](int i) {  // called by all lanes; lane 0 copies page i into its stage
+        const int pid = page_of(i);
+        if (lane == 0) {
+            const uint32_t k = pc + (uint32_t)i, st = k % A_NPS;
+            const uint32_t bar = bar0 + 8 * st;
+            const size_t off = ((size_t)(pid < 0 ? 0 : pid) * p.n_kv + g) * 16 * 128;
+            mbar_expect_tx(bar, A_STAGE);
+            bulk_g2s(smem_u32(ring + st * A_STAGE), Kl + off, A_STAGE / 2, bar);
+            bulk_g2s(smem_u32(ring + st * A_STAGE + A_STAGE / 2), Vl + off, A_STAGE / 2, bar);
         }
+    };
+    for (int i = 0; i < np && i < A_NPS; ++i) issue(i);
+    for (int i = 0; i < np; ++i) {
+        const uint32_t k = pc + (uint32_t)i, st = k % A_NPS;
+        if (!mbar_drain(bar0 + 8 * st, (k / A_NPS) & 1u) && lane == 0) atomicOr(p.status, QW_DEV_TIMEOUT);
+        const uint8_t* pk = ring + st * A_STAGE;
+        uint4 kk[8], vv[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            kk[j] = *reinterpret_cast<const uint4*>(pk + ((2 * j + half) * 128 + dl) * 2);
+            vv[j] = *reinterpret_cast<const uint4*>(pk + A_STAGE / 2 + ((2 * j + half) * 128 + dl) * 2);
+        }
+        const int nvalid = page_of(i) < 0 ? 0 : min(16, k1 - (p0 + i) * 16);
+        page_step(w, kk, vv, nvalid, half);
+        __syncwarp();
+        if (i + A_NPS < np) issue(i + A_NPS);
     }
+    pc += (uint32_t)np;
     // the two half-warps saw alternate keys with the same running max
     w.l0 += __shfl_xor_sync(0xffffffffu, w.l0, 16);
     w.l1 += __shfl_xor_sync(0xffffffffu, w.l1, 16);
@@ -335,10 +366,11 @@ __device__ bool attn_unit(const StepKParams& p, int l, int h, int tok, int g, in
     int* att_done = done_ctr(p, l, h, DS_ATT + g);
     if (n_act == 1) {
         store8(oo, 1.0f / ll);
+        fence_proxy_global();
         __threadfence();
         __syncwarp();
         if (lane == 0) atomicAdd(att_done, 1);
-        return true;
+        return;
     }
     const size_t slot = ((size_t)tok * p.n_heads + head) * p.att_stride + s;
     float4* po = reinterpret_cast<float4*>(p.att_po + slot * 128 + dl);
@@ -350,10 +382,10 @@ __device__ bool attn_unit(const StepKParams& p, int l, int h, int tok, int g, in
     int last = 0;
     if (lane == 0) last = (atomicAdd(p.att_cnt + (size_t)tok * p.n_kv + g, 1) == n_act - 1);
     last = __shfl_sync(0xffffffffu, last, 0);
-    if (!last) return true;
+    if (!last) return;
     __threadfence();
     const size_t base = ((size_t)tok * p.n_heads + head) * p.att_stride;
-    // the splits' (max, sum): lane j of each half-warp holds split j (16 per round)
+    // the splits' maxima: lane j of each half-warp holds split j (16 per round)
     float M = -INFINITY;
     for (int j0 = 0; j0 < n_act; j0 += 16) {
         const int j = j0 + (lane & 15);
@@ -390,78 +422,15 @@ __device__ bool attn_unit(const StepKParams& p, int l, int h, int tok, int g, in
     }
     store8(A, 1.0f / L);
     if (lane == 0) p.att_cnt[(size_t)tok * p.n_kv + g] = 0;
+    fence_proxy_global();
     __threadfence();
     __syncwarp();
     if (lane == 0) atomicAdd(att_done, 1);
-    return true;
-}
-
-// ---- projection role: the token operand ---------------------------------------------------
-
-// Token operand of a unit: rows t < N (zero at t >= nh), K range [k0, k0 + kb * 64), as
-// kb blocks of [N][64] fp16 in the 128-byte swizzle layout (16-byte chunk c of row t at
-// chunk c ^ (t & 7)). kind q|k|v and gate/up: RMSNorm(x) * w; o_proj: attn; down_proj: act.
-// Token operand of a unit: rows t < N (zero at t >= nh), K range [k0, k0 + kb * 64), as
-// kb blocks of [N][64] fp16 in the 128-byte swizzle layout (16-byte chunk c of row t at
-// chunk c ^ (t & 7)). kind q|k|v and gate/up: RMSNorm(x) * w; o_proj: attn; down_proj: act.
-// The loads of a batch are unconditional (indices clamped into the valid rows) so that they
-// are all in flight together; only their use is predicated.
-__device__ void build_operand(const StepKParams& p, int kind, int l, int tok0, int nh, int N, int k0, int kb,
-                              uint8_t* B, const float* s_rs) {
-    constexpr int R = 8;  // chunks per thread per batch
-    const int tid = threadIdx.x;
-    const int per_row = kb * 8;  // 16-byte chunks per token row
-    const int total = N * per_row;
-    const bf16* nw = p.norms + (size_t)l * (2 * p.D + 256) + (kind == KGU ? p.D : 0);
-    const bool normed = (kind == KQKV || kind == KGU);
-    for (int i0 = tid; i0 < total; i0 += 128 * R) {
-        float4 xa[R], xb[R];
-        uint4 w[R];
-        int tt[R], cc[R];
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const int i = min(i0 + 128 * r, total - 1);
-            tt[r] = i / per_row;
-            cc[r] = i - tt[r] * per_row;
-            const size_t row = (size_t)(tok0 + min(tt[r], nh - 1));
-            const int k = k0 + cc[r] * 8;
-            if (normed) {
-                xa[r] = __ldcg(reinterpret_cast<const float4*>(p.x + row * p.D + k));
-                xb[r] = __ldcg(reinterpret_cast<const float4*>(p.x + row * p.D + k + 4));
-                w[r] = __ldg(reinterpret_cast<const uint4*>(nw + k));
-            } else {
-                w[r] = ldcg16(kind == KO ? (const void*)(p.attn + row * p.QD + k) : (const void*)(p.act + row * p.I + k));
-            }
-        }
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            if (i0 + 128 * r < total) {
-                const int t = tt[r];
-                uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                if (t < nh) {
-                    if (normed) {
-                        const float rs = s_rs[t];
-                        v.x = pack_h2(xa[r].x * rs * bf_lo(w[r].x), xa[r].y * rs * bf_hi(w[r].x));
-                        v.y = pack_h2(xa[r].z * rs * bf_lo(w[r].y), xa[r].w * rs * bf_hi(w[r].y));
-                        v.z = pack_h2(xb[r].x * rs * bf_lo(w[r].z), xb[r].y * rs * bf_hi(w[r].z));
-                        v.w = pack_h2(xb[r].z * rs * bf_lo(w[r].w), xb[r].w * rs * bf_hi(w[r].w));
-                    } else {
-                        v = w[r];
-                    }
-                }
-                const int blk = cc[r] >> 3, c16 = cc[r] & 7;
-                *reinterpret_cast<uint4*>(B + (size_t)blk * N * 128 + t * 128 + ((c16 ^ (t & 7)) << 4)) = v;
-            }
-        }
-    }
 }
 
 }  // namespace
 
-__global__ void __launch_bounds__(ST_THREADS, 1)
-    k_step(const __grid_constant__ CUtensorMap tm_qkv, const __grid_constant__ CUtensorMap tm_o,
-           const __grid_constant__ CUtensorMap tm_gu, const __grid_constant__ CUtensorMap tm_dn,
-           const __grid_constant__ StepKParams p) {
+__global__ void __launch_bounds__(ST_THREADS, 1) k_step(const __grid_constant__ StepMaps mp, const __grid_constant__ StepKParams p) {
     extern __shared__ uint8_t st_smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(st_smem_raw) + 1023) & ~(uintptr_t)1023);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -471,17 +440,26 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
         // ---------------- attention role ----------------
         const int aw = (c - p.gp) * (ST_THREADS / 32) + warp;
         const int naw = ((int)gridDim.x - p.gp) * (ST_THREADS / 32);
-        __shared__ volatile int a_ok;
+        uint8_t* ring = smem + warp * A_NPS * A_STAGE;
+        const uint32_t bar0 = smem_u32(smem + SO_ABAR + warp * A_NPS * 8);
+        volatile int* a_ok = reinterpret_cast<volatile int*>(smem + SO_MISC);
+        if (lane == 0) {
+            for (int i = 0; i < A_NPS; ++i) mbar_init(bar0 + 8 * i, 1);
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        }
+        __syncwarp();
+        uint32_t pc = 0;
         int nrec = 0;
         for (int l = 0; l < p.L; ++l) {
             for (int h = 0; h < 2; ++h) {
                 // one thread per CTA waits for every q|k|v tile of (l, h); the warps follow
                 const uint64_t tw = p.trace ? globaltimer_ns() : 0;
-                if (threadIdx.x == 0) a_ok = wait_ge(p, done_ctr(p, l, h, DS_QKV_ALL), p.QKVR / 128) ? 1 : 0;
+                if (threadIdx.x == 0) *a_ok = wait_ge(p, done_ctr(p, l, h, DS_QKV_ALL), p.QKVR / 128) ? 1 : 0;
                 __syncthreads();
-                const int go = a_ok;
+                const int go = *a_ok;
                 __syncthreads();  // read by all before thread 0 can write the next phase's flag
-                if (!go) return;
+                if (!go) return;  // nothing of this warp is in flight between phases
+                if (lane == 0) fence_proxy_global();  // this warp's copies read what the q|k|v epilogues wrote
                 const uint64_t ts = p.trace ? globaltimer_ns() : 0;
                 const int nh = p.nh[h];
                 const int U = nh * p.n_kv * p.nsplit;
@@ -494,20 +472,20 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
                     const int n_act = (n_keys + p.chunk - 1) / p.chunk;
                     if (s >= n_act) continue;
                     const uint64_t tu = p.trace ? globaltimer_ns() : 0;
-                    attn_unit(p, l, h, tok, g, s, n_act, s * p.chunk, min((s + 1) * p.chunk, n_keys));
+                    attn_unit(p, l, h, tok, g, s, n_act, s * p.chunk, min((s + 1) * p.chunk, n_keys), ring, bar0, pc);
                     if (p.trace && warp == 0 && lane == 0)
                         trace_rec(p, nrec++, (1ull << 40) | ((unsigned long long)l << 24) | ((unsigned long long)h << 20) | u,
                                   tw, ts, tu, globaltimer_ns());
                 }
             }
         }
-        return;  // the attention role uses no mbarriers and no tensor memory
+        return;
     }
 
     // ---------------- projection role ----------------
     uint8_t* ring = smem;
     uint8_t* Bop = smem + SO_B;
-    float* E = reinterpret_cast<float*>(smem + SO_E);
+    float* E = reinterpret_cast<float*>(smem + SO_B);  // epilogue staging over the operand space
     float* nws = reinterpret_cast<float*>(smem + SO_NW);
     int* tpos = reinterpret_cast<int*>(smem + SO_META);
     int* tdst = tpos + 32;
@@ -515,8 +493,8 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
     float* s_rs = reinterpret_cast<float*>(smem + SO_RS);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + SO_BAR);
     uint64_t* empty = full + ST_NST;
-    uint64_t* bready = empty + ST_NST;
-    uint64_t* accf = bready + 1;
+    uint64_t* bfull = empty + ST_NST;
+    uint64_t* accf = bfull + 1;
     uint64_t* mdrain = accf + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SO_MISC);
     volatile int* abort_s = reinterpret_cast<volatile int*>(smem + SO_MISC + 4);
@@ -527,7 +505,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
             mbar_init(smem_u32(full + s), 1);
             mbar_init(smem_u32(empty + s), 1);
         }
-        mbar_init(smem_u32(bready), 1);
+        mbar_init(smem_u32(bfull), 1);
         mbar_init(smem_u32(accf), 1);
         mbar_init(smem_u32(mdrain), 1);
         *abort_s = 0;
@@ -535,10 +513,10 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     if (warp == 4 && lane == 0) {
-        tma_prefetch_desc(&tm_qkv);
-        tma_prefetch_desc(&tm_o);
-        tma_prefetch_desc(&tm_gu);
-        tma_prefetch_desc(&tm_dn);
+        for (int i = 0; i < 4; ++i) tma_prefetch_desc(&mp.w[i]);
+        tma_prefetch_desc(&mp.xw);
+        tma_prefetch_desc(&mp.attn);
+        tma_prefetch_desc(&mp.act);
     }
     if (warp == 5) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
@@ -562,7 +540,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
                 int kind, l, h;
                 if (!phase_at(p, i, kind, l, h)) continue;
                 const Geo G = geo(p, kind);
-                const CUtensorMap* map = kind == KQKV ? &tm_qkv : kind == KO ? &tm_o : kind == KGU ? &tm_gu : &tm_dn;
+                const CUtensorMap* map = &mp.w[kind];
                 const int rows_per_layer = kind == KQKV ? p.QKVR : kind == KGU ? 2 * p.I : p.D;
                 for (int u = first_unit(c, i, gp); u < G.tiles * G.S && ok; u += gp) {
                     const int tile = u / G.S, split = u % G.S;
@@ -591,14 +569,13 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
         if (lane == 0) {
             uint32_t rc = 0, uc = 0;
             bool ok = true, issued = false;
+            constexpr uint32_t idesc = idesc_f16(BM, ST_N);
             for (int i = 0; i < NP && ok; ++i) {
                 int kind, l, h;
                 if (!phase_at(p, i, kind, l, h)) continue;
                 const Geo G = geo(p, kind);
-                const int N = p.nh[h] <= 16 ? 16 : 32;
-                const uint32_t idesc = idesc_f16(BM, N);
                 for (int u = first_unit(c, i, gp); u < G.tiles * G.S && ok; u += gp) {
-                    if (!mbar_wait(smem_u32(bready), uc & 1u, abort_s)) {
+                    if (!mbar_wait(smem_u32(bfull), uc & 1u, abort_s)) {
                         *abort_s = 1;
                         ok = false;
                         break;
@@ -614,7 +591,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
                         }
                         tc_fence_after();
                         const uint64_t ad = sw128_desc(smem_u32(ring + s * ST_STAGE));
-                        const uint64_t bd = sw128_desc(smem_u32(Bop + j * N * 128));
+                        const uint64_t bd = sw128_desc(smem_u32(Bop + j * ST_BBOX));
 #pragma unroll
                         for (int k = 0; k < BK / 16; ++k)
                             umma_f16(tmem, ad + 2 * k, bd + 2 * k, idesc, (j > 0 || k > 0) ? 1u : 0u);
@@ -634,9 +611,9 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
         }
         __syncwarp();
     } else if (warp < 4) {
-        // ---- operand builders + epilogue (threads 0-127 = TMEM lanes = tile rows) ----
+        // ---- operand loads + epilogue (threads 0-127 = TMEM lanes = tile rows) ----
         const int tid = threadIdx.x;
-        uint32_t uc = 0;
+        uint32_t uc = 0, bc = 0;
         bool ok = true;
         int nrec = 0;
         uint64_t tr0 = 0, tr1 = 0, tr2 = 0;
@@ -645,11 +622,11 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
             if (!phase_at(p, i, kind, l, h)) continue;
             const Geo G = geo(p, kind);
             const int nh = p.nh[h], tok0 = p.t0[h];
-            const int N = nh <= 16 ? 16 : 32;
             const int UT = unit_off(p, 4);
+            const CUtensorMap* bmap = (kind == KO) ? &mp.attn : (kind == KDN) ? &mp.act : &mp.xw;
             for (int u = first_unit(c, i, gp); u < G.tiles * G.S; u += gp) {
                 const int tile = u / G.S, split = u % G.S;
-                // 1. wait for this unit's inputs
+                // 1. wait for this unit's inputs, then load its token operand with TMA
                 if (tid == 0 && p.trace) tr0 = globaltimer_ns();
                 if (tid == 0) {
                     const int* ctr = nullptr;
@@ -669,7 +646,15 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
                         ctr = done_ctr(p, l, h, DS_GU + split);
                         target = geo(p, KGU).tiles / DN_SPLIT;
                     }
-                    *s_flag = (ctr == nullptr || wait_ge(p, ctr, target)) ? 1 : 0;
+                    const bool good = (ctr == nullptr || wait_ge(p, ctr, target));
+                    *s_flag = good ? 1 : 0;
+                    if (good) {
+                        fence_proxy_global();  // the copies read what other CTAs' epilogues wrote
+                        mbar_expect_tx(smem_u32(bfull), G.kb * ST_BBOX);
+                        for (int j = 0; j < G.kb; ++j)
+                            tma_load_2d(smem_u32(Bop + j * ST_BBOX), bmap, smem_u32(bfull), (split * G.kb + j) * BK, tok0);
+                        ++bc;
+                    }
                 }
                 named_bar_epi();
                 if (!*s_flag) {
@@ -677,21 +662,14 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
                     break;
                 }
                 if (tid == 0 && p.trace) tr1 = globaltimer_ns();
-                // 2. token operand (RMSNorm scale per token from the per-block sums of squares)
-                if (kind == KQKV || kind == KGU) {
-                    if (tid < nh) {
-                        const float* sp = p.ss + (size_t)(tok0 + tid) * (p.D / 128);
-                        float acc = 0.f;
-                        for (int b = 0; b < p.D / 128; ++b) acc += __ldcg(sp + b);
-                        s_rs[tid] = rsqrtf(acc / (float)p.D + p.eps);
-                    }
-                    named_bar_epi();
+                // the RMSNorm scale of each token (q|k|v, gate/up) from its per-block sums of squares
+                if ((kind == KQKV || kind == KGU) && tid < nh) {
+                    const float* sp = p.ss + (size_t)(tok0 + tid) * (p.D / 128);
+                    float acc = 0.f;
+                    for (int b = 0; b < p.D / 128; ++b) acc += __ldcg(sp + b);
+                    s_rs[tid] = rsqrtf(acc / (float)p.D + p.eps);
                 }
-                build_operand(p, kind, l, tok0, nh, N, split * G.kb * BK, G.kb, Bop, s_rs);
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                named_bar_epi();
-                if (tid == 0) mbar_arrive(smem_u32(bready));
-                // 3. accumulator -> fp32 partial of this K range
+                // 2. accumulator -> fp32 partial of this K range ([row][token], this thread's row)
                 if (!mbar_wait(smem_u32(accf), uc & 1u, abort_s)) {
                     *abort_s = 1;
                     ok = false;
@@ -704,58 +682,80 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
                 TMEM_LD32(tmem + ((uint32_t)(warp * 32) << 16), r);
                 tmem_wait_ld();
                 tc_fence_before();
-                float* part_u = p.part + ((size_t)h * UT + unit_off(p, kind) + u) * (32 * 128);
-#pragma unroll
-                for (int t = 0; t < 32; ++t)
-                    if (t < nh) __stcg(part_u + t * 128 + tid, __uint_as_float(r[t]));
-                __threadfence();
-                named_bar_epi();
                 int* tick = p.tick + h * tile_off(p, 4) + tile_off(p, kind) + tile;
-                if (tid == 0) *s_flag = (atomicAdd(tick, 1) == G.S - 1) ? 1 : 0;
-                named_bar_epi();
-                if (!*s_flag) {
-                    if (tid == 0) trace_rec(p, nrec++, ((unsigned long long)i << 16) | u, tr0, tr1, tr2, globaltimer_ns());
-                    continue;
-                }
-                // 4. last K range of the tile: sum the partials in order, apply the epilogue
-                const uint64_t tr3 = (tid == 0 && p.trace) ? globaltimer_ns() : 0;
-                __threadfence();
                 float v[32];
+                {
+                    float4* part_u = reinterpret_cast<float4*>(p.part + (((size_t)h * UT + unit_off(p, kind) + u) * 128 + tid) * 32);
 #pragma unroll
-                for (int t = 0; t < 32; ++t) v[t] = 0.f;
-                const float* pt0 = p.part + ((size_t)h * UT + unit_off(p, kind) + tile * G.S) * (32 * 128) + tid;
-                uint64_t tr6 = 0;
-                // every slot has 32 token rows: all 32 loads of a partial are issued together
-                // (rows at or past nh hold stale values that are never used)
-                for (int s2 = 0; s2 < G.S; ++s2) {
-                    float pv[32];
+                    for (int q = 0; q < 8; ++q)
+                        __stcg(part_u + q, make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                                       __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3])));
+                    __threadfence();
+                    named_bar_epi();
+                    if (tid == 0) *s_flag = (atomicAdd(tick, 1) == G.S - 1) ? 1 : 0;
+                    named_bar_epi();
+                    if (!*s_flag) {
+                        if (tid == 0) trace_rec(p, nrec++, ((unsigned long long)i << 16) | u, tr0, tr1, tr2, globaltimer_ns());
+                        continue;
+                    }
+                    // 3. last K range of the tile: add the partials in order, two at a time
+                    __threadfence();
 #pragma unroll
-                    for (int t = 0; t < 32; ++t) pv[t] = __ldcg(pt0 + (size_t)s2 * (32 * 128) + t * 128);
+                    for (int t = 0; t < 32; ++t) v[t] = 0.f;
+                    const float4* pt0 = reinterpret_cast<const float4*>(
+                        p.part + (((size_t)h * UT + unit_off(p, kind) + tile * G.S) * 128 + tid) * 32);
+                    for (int s2 = 0; s2 < G.S; s2 += 2) {
+                        float4 a[8], b[8];
+                        const int s3 = min(s2 + 1, G.S - 1);
 #pragma unroll
-                    for (int t = 0; t < 32; ++t) v[t] += pv[t];
-                    if (s2 == 0 && tid == 0 && p.trace) {
-                        float z = 0.f;
+                        for (int q = 0; q < 8; ++q) {
+                            a[q] = __ldcg(pt0 + (size_t)s2 * 128 * 8 + q);
+                            b[q] = __ldcg(pt0 + (size_t)s3 * 128 * 8 + q);
+                        }
+                        const bool two = s2 + 1 < G.S;
 #pragma unroll
-                        for (int t = 0; t < 32; ++t) z += v[t];
-                        tr6 = globaltimer_ns() + (z == 12345.f ? 1 : 0);
+                        for (int q = 0; q < 8; ++q) {
+                            v[4 * q] += a[q].x;
+                            v[4 * q + 1] += a[q].y;
+                            v[4 * q + 2] += a[q].z;
+                            v[4 * q + 3] += a[q].w;
+                            if (two) {
+                                v[4 * q] += b[q].x;
+                                v[4 * q + 1] += b[q].y;
+                                v[4 * q + 2] += b[q].z;
+                                v[4 * q + 3] += b[q].w;
+                            }
+                        }
                     }
                 }
-                const uint64_t tr4 = (tid == 0 && p.trace) ? globaltimer_ns() : 0;
+                const uint64_t tr3 = (tid == 0 && p.trace) ? globaltimer_ns() : 0;
                 int done_slot;
                 if (kind == KO || kind == KDN) {
                     const int m = tile * BM + tid;
+                    // the next RMSNorm's weight: post-attention of layer l, or input of layer l + 1
+                    const bf16* wn = (kind == KO) ? p.norms + (size_t)l * (2 * p.D + 256) + p.D
+                                     : (l + 1 < p.L) ? p.norms + (size_t)(l + 1) * (2 * p.D + 256)
+                                                     : nullptr;
+                    const float wm = wn ? __bfloat162float(wn[m]) : 0.f;
                     float xo[32];
 #pragma unroll
                     for (int t = 0; t < 32; ++t) xo[t] = __ldcg(p.x + (size_t)(tok0 + min(t, nh - 1)) * p.D + m);
+                    bool big = false;
 #pragma unroll
                     for (int t = 0; t < 32; ++t) {
                         if (t < nh) {
                             const float xn = xo[t] + v[t];
                             __stcg(p.x + (size_t)(tok0 + t) * p.D + m, xn);
                             v[t] = xn;
+                            if (wn) {
+                                const float y = xn * wm;
+                                big |= f16_out_of_range(y);
+                                p.xw[(size_t)(tok0 + t) * p.D + m] = __float2half_rn(y);
+                            }
                             if (kind == KDN && p.dbg_hidden) p.dbg_hidden[((size_t)l * p.T + tok0 + t) * p.D + m] = xn;
                         }
                     }
+                    if (big) atomicOr(p.status, QW_DEV_RANGE);
 #pragma unroll
                     for (int t = 0; t < 32; ++t) {
                         if (t < nh) {
@@ -770,7 +770,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
                     done_slot = kind == KO ? DS_O : DS_DN;
                 } else if (kind == KGU) {
 #pragma unroll
-                    for (int t = 0; t < 32; ++t) E[t * EP + tid] = v[t];
+                    for (int t = 0; t < 32; ++t) E[t * EP + tid] = v[t] * s_rs[t < nh ? t : 0];
                     named_bar_epi();
                     GemmKParams gk = {};
                     gk.out_h = p.act;
@@ -781,7 +781,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
                 } else {
                     f16* EH = reinterpret_cast<f16*>(E);
 #pragma unroll
-                    for (int t = 0; t < 32; ++t) EH[t * EPH + tid] = __float2half_rn(v[t]);
+                    for (int t = 0; t < 32; ++t) EH[t * EPH + tid] = __float2half_rn(v[t] * s_rs[t < nh ? t : 0]);
                     GemmKParams gk = {};
                     const bf16* nb = p.norms + (size_t)l * (2 * p.D + 256);
                     gk.q_out = p.q;
@@ -809,7 +809,9 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
                                                                                           : tile - p.n_heads - p.n_kv;
                     done_slot = DS_QKV + g;
                 }
-                const uint64_t tr5 = (tid == 0 && p.trace) ? globaltimer_ns() : 0;
+                const uint64_t tr4 = (tid == 0 && p.trace) ? globaltimer_ns() : 0;
+                fence_proxy_global();
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // staging before the next operand copy
                 __threadfence();
                 named_bar_epi();
                 if (tid == 0) {
@@ -817,12 +819,14 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
                     __threadfence();
                     atomicAdd(done_ctr(p, l, h, done_slot), 1);
                     if (kind == KQKV) atomicAdd(done_ctr(p, l, h, DS_QKV_ALL), 1);
-                    trace_rec(p, nrec++, (1ull << 39) | ((unsigned long long)i << 16) | u, tr0, tr1, tr6, globaltimer_ns(),
-                              tr3, tr4, tr5);
+                    trace_rec(p, nrec++, (1ull << 39) | ((unsigned long long)i << 16) | u, tr0, tr1, tr2, globaltimer_ns(),
+                              tr3, tr4, 0);
                 }
             }
         }
         if (!ok) *abort_s = 1;
+        // a token operand copy whose unit was abandoned must land before the CTA exits
+        if (tid == 0 && bc > uc) mbar_drain(smem_u32(bfull), (bc - 1) & 1u);
     }
     tc_fence_before();
     __syncthreads();
@@ -857,9 +861,7 @@ int step_blocks_per_sm() {
     return n;
 }
 
-cudaError_t launch_decode_step(cudaStream_t st, const StepKParams& p, const CUtensorMap* tm_qkv,
-                               const CUtensorMap* tm_o, const CUtensorMap* tm_gu, const CUtensorMap* tm_dn,
-                               int grid) {
+cudaError_t launch_decode_step(cudaStream_t st, const StepKParams& p, const StepMaps& maps, int grid) {
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(k_step, cudaFuncAttributeMaxDynamicSharedMemorySize, ST_SMEM);
@@ -876,5 +878,5 @@ cudaError_t launch_decode_step(cudaStream_t st, const StepKParams& p, const CUte
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, k_step, *tm_qkv, *tm_o, *tm_gu, *tm_dn, p);
+    return cudaLaunchKernelEx(&cfg, k_step, maps, p);
 }

@@ -140,7 +140,8 @@ cudaError_t launch_k(const LaunchCtx& c, void (*kern)(KArgs...), dim3 grid, dim3
 
 cudaError_t launch_step_begin(const LaunchCtx& c, const StepDesc& sd, const int32_t* ids,
                               const bf16* embed, int vocab, int hidden, float* x, TokView tv,
-                              KVView kv, int* status, float* ss = nullptr);
+                              KVView kv, int* status, float* ss = nullptr, const bf16* w = nullptr,
+                              f16* xw = nullptr);
 cudaError_t launch_rmsnorm(const LaunchCtx& c, const float* x, const int* rows, int n_rows,
                            int hidden, const bf16* w, float eps, f16* h);
 cudaError_t launch_convert_bf16_f16(const LaunchCtx& c, const bf16* src, f16* dst, size_t n, int* status);
@@ -281,6 +282,7 @@ struct StepKParams {
     f16* act;           // [T][I] SiLU(gate) * up
     float* part;        // split-K partials [2][units][32][128]
     float* ss;          // [T][D / 128] sums of squares of x per 128-feature block
+    f16* xw;            // [2 * kStepMaxHalf][D] fp16(x * w), w = the next RMSNorm's weight
     int* tick;          // [2][tiles] split-K arrival tickets (reset by the last arrival)
     int* done;          // [L][2][kStepDoneSlots][kStepDoneStride] completion counters (zeroed before the launch)
     float* att_po;      // attention partials [T][n_heads][att_stride][128]
@@ -308,9 +310,13 @@ int step_tiles(int D, int I, int QKVR);
 bool step_shape_ok(int D, int I, int QD, int QKVR, int n_heads, int n_kv);
 int step_smem_bytes();
 int step_blocks_per_sm();  // 0: the kernel cannot be resident (no launch possible)
-cudaError_t launch_decode_step(cudaStream_t st, const StepKParams& p, const CUtensorMap* tm_qkv,
-                               const CUtensorMap* tm_o, const CUtensorMap* tm_gu, const CUtensorMap* tm_dn,
-                               int grid);
+// Tensor maps: weights (q|k|v, o, gate/up, down; boxes of 128 rows) and token operands (xw,
+// attn, act; boxes of 32 rows), all fp16 with 64-column boxes and the 128-byte swizzle.
+struct StepMaps {
+    CUtensorMap w[4];
+    CUtensorMap xw, attn, act;
+};
+cudaError_t launch_decode_step(cudaStream_t st, const StepKParams& p, const StepMaps& maps, int grid);
 
 // Persistent decode kernel (k_mk.cu): one cooperative launch per decode step of <= 8 tokens.
 struct MkParams {

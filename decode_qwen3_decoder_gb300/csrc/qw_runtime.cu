@@ -90,7 +90,7 @@ struct WsLayout {
     size_t wqkv, wo, wgu, wd, embed16, bqkv, bo, bg, bu, bd, norms, fnorm, rcos, rsin;
     size_t x, h, qkv, q, attn, act, part_o, part_ml, counters;
     size_t tok_seq, tok_pos, tok_slot, last, best, status, gen_tok, gen_cur, gen_out, mk_sync;
-    size_t st_part, st_ss, st_done, st_tick, st_abort;  // batched decode-step kernel
+    size_t st_part, st_ss, st_xw, st_done, st_tick, st_abort;  // batched decode-step kernel
     size_t total;
     int part_T;
 };
@@ -144,6 +144,7 @@ static WsLayout layout_for(const qw_config& c) {
         const int QKVR = (int)QKV;
         L.st_part = take(step_part_floats((int)D, (int)I, QKVR, c.n_kv_heads) * 4);
         L.st_ss = take((size_t)2 * kStepMaxHalf * (D / 128) * 4);
+        L.st_xw = take((size_t)2 * kStepMaxHalf * D * 2);
         L.st_done = take((size_t)c.n_layers * 2 * kStepDoneSlots * kStepDoneStride * 4);
         L.st_tick = take((size_t)2 * step_tiles((int)D, (int)I, QKVR) * 4);
         L.st_abort = take(4);
@@ -187,7 +188,9 @@ struct qw_model {
     unsigned long long step_wait_ns;  // bound of its waits on other CTAs
     int step_extra;    // test-only: extra arrivals its first o_proj unit waits for
     float *st_part, *st_ss;
+    f16* st_xw;
     int *st_done, *st_tick, *st_abort;
+    StepMaps st_maps;
     unsigned long long* best;
     int32_t *gen_tok, *gen_cur, *gen_out;
     float* dbg_hidden;
@@ -315,6 +318,7 @@ extern "C" qw_status qw_init_weights(const qw_config* cfg, const qw_weight_ptrs*
     m->mk_sync = (unsigned*)(b + L.mk_sync);
     m->st_part = (float*)(b + L.st_part);
     m->st_ss = (float*)(b + L.st_ss);
+    m->st_xw = (f16*)(b + L.st_xw);
     m->st_done = (int*)(b + L.st_done);
     m->st_tick = (int*)(b + L.st_tick);
     m->st_abort = (int*)(b + L.st_abort);
@@ -480,6 +484,15 @@ extern "C" qw_status qw_init_weights(const qw_config* cfg, const qw_weight_ptrs*
     m->step_ok = step_shape_ok((int)D, (int)I, (int)QD, m->qkv_rows, cfg->n_heads, cfg->n_kv_heads) &&
                  step_blocks_per_sm() >= 1 &&
                  m->num_sms >= 16;
+    if (m->step_ok) {
+        m->st_maps.w[0] = m->tm_wqkv;
+        m->st_maps.w[1] = m->tm_wo;
+        m->st_maps.w[2] = m->tm_wgu;
+        m->st_maps.w[3] = m->tm_wd;
+        m->step_ok = gemm_tc_encode_map(&m->st_maps.xw, m->st_xw, 2 * kStepMaxHalf, D, kStepMaxHalf) &&
+                     gemm_tc_encode_map(&m->st_maps.attn, m->attn, cfg->max_tokens, QD, kStepMaxHalf) &&
+                     gemm_tc_encode_map(&m->st_maps.act, m->act, cfg->max_tokens, I, kStepMaxHalf);
+    }
     m->use_step = false;  // opt in with QW_OPT_DECODE_STEP_KERNEL
     m->step_gp = std::max(1, std::min(64, m->num_sms / 2));
     m->step_wait_ns = 2000000000ull;
@@ -1096,7 +1109,7 @@ static qw_status run_step(qw_model* m, qw_kv* kv, const StepDesc& sd, bool prefi
     const bool engine = !prefill && m->use_step && m->qbits == 16 && T >= 16 && T <= 2 * kStepMaxHalf &&
                         (m->prof_kind == QW_PROF_OFF || m->prof_kind == QW_PROF_STEP);
     CUDA_TRY(launch_step_begin(lc0, sd, tokens, m->embed, c.vocab, D, m->x, tv, kvv, m->status,
-                               engine ? m->st_ss : nullptr));
+                               engine ? m->st_ss : nullptr, m->norms, m->st_xw));
     if (engine) {
         // every layer of the step in one cooperative kernel (counters cleared first)
         CUDA_TRY(cudaMemsetAsync(m->st_done, 0, (size_t)c.n_layers * 2 * kStepDoneSlots * kStepDoneStride * 4, st));
@@ -1106,7 +1119,7 @@ static qw_status run_step(qw_model* m, qw_kv* kv, const StepDesc& sd, bool prefi
         sp.scale_log2 = 0.08838834764831845f * 1.4426950408889634f;  // 128^-0.5 * log2(e)
         sp.norms = m->norms; sp.rope_cos = m->rcos; sp.rope_sin = m->rsin;
         sp.x = m->x; sp.q = m->q; sp.attn = m->attn; sp.act = m->act;
-        sp.part = m->st_part; sp.ss = m->st_ss; sp.tick = m->st_tick; sp.done = m->st_done;
+        sp.part = m->st_part; sp.ss = m->st_ss; sp.xw = m->st_xw; sp.tick = m->st_tick; sp.done = m->st_done;
         sp.att_po = m->part_o; sp.att_pml = m->part_ml; sp.att_cnt = m->counters; sp.att_stride = kMaxSplits;
         sp.tv = tv; sp.kv = kvv; sp.status = m->status; sp.abort_g = m->st_abort;
         sp.T = T;
@@ -1135,7 +1148,7 @@ static qw_status run_step(qw_model* m, qw_kv* kv, const StepDesc& sd, bool prefi
             int pc0[16] = {0};
             ProfScope prof_scope_(m, QW_PROF_STEP, pc0, st);
             if (launches) ++*launches;
-            CUDA_TRY(launch_decode_step(st, sp, &m->tm_wqkv, &m->tm_wo, &m->tm_wgu, &m->tm_wd, m->num_sms));
+            CUDA_TRY(launch_decode_step(st, sp, m->st_maps, m->num_sms));
         }
     }
     // A decode batch of >= 16 sequences runs as two halves on two streams, so that one
