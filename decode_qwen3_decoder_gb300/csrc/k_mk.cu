@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(MK_THREADS, 1) k_decode_mk(const MkParams p) {
     uint8_t* actb = smem + MK_NST * MK_STAGE;  // activation rows / attention team scratch
     uint64_t* full = reinterpret_cast<uint64_t*>(actb + MK_ACT);
     uint64_t* empty = full + MK_NST;
-    __shared__ float s_rs[8];
+    __shared__ float s_red[MK_CONS_WARPS][MK_TMAX];  // per-warp sums of squares of the staged rows
     __shared__ unsigned long long s_best[MK_CONS_WARPS][MK_TMAX];
     __shared__ int s_last;
     __shared__ volatile uint32_t s_issued;
@@ -371,34 +371,130 @@ __global__ void __launch_bounds__(MK_THREADS, 1) k_decode_mk(const MkParams p) {
         return good;
     };
 
-    // RMSNorm of the T residual rows into fp32 shared memory (Paso 3): one pass over x
-    // (through L2) into shared memory, then the per-row scale in place.
+    // RMSNorm input of the T residual rows (Paso 3) in one pass: x * w (w = the norm weight)
+    // into fp32 shared memory while each warp sums its tokens' squares (s_red). 1/RMS is a
+    // per-token scale, so the consumers apply it to the reduced products (rs_of).
     auto stage_norm = [&](const bf16* w) {
-        for (int i = threadIdx.x; i < T * p.D / 4; i += MK_CONS_THREADS)
-            *reinterpret_cast<float4*>(hs + i * 4) = __ldcg(reinterpret_cast<const float4*>(p.x) + i);
-        named_sync(1, MK_CONS_THREADS);
-        for (int t = warp; t < T; t += MK_CONS_WARPS) {
-            float ss = 0.f;
-            for (int k = lane * 4; k < p.D; k += 128) {
-                const float4 v = *reinterpret_cast<const float4*>(hs + t * p.D + k);
-                ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-            }
-            ss = warp_sum(ss);
-            if (lane == 0) s_rs[t] = rsqrtf(ss / (float)p.D + p.eps);
-        }
-        named_sync(1, MK_CONS_THREADS);
+        float ssp[MK_TMAX];
+#pragma unroll
+        for (int t = 0; t < MK_TMAX; ++t) ssp[t] = 0.f;
         for (int i = threadIdx.x; i < T * p.D / 4; i += MK_CONS_THREADS) {
             const int t = i / (p.D / 4), k = (i % (p.D / 4)) * 4;
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(p.x) + i);
             const uint2 wb = *reinterpret_cast<const uint2*>(w + k);
-            const float r = s_rs[t];
-            float4 v = *reinterpret_cast<float4*>(hs + i * 4);
-            v.x *= r * bf_lo(wb.x);
-            v.y *= r * bf_hi(wb.x);
-            v.z *= r * bf_lo(wb.y);
-            v.w *= r * bf_hi(wb.y);
-            *reinterpret_cast<float4*>(hs + i * 4) = v;
+            const float q = v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+#pragma unroll
+            for (int u = 0; u < MK_TMAX; ++u)
+                if (u == t) ssp[u] += q;
+            *reinterpret_cast<float4*>(hs + i * 4) =
+                make_float4(v.x * bf_lo(wb.x), v.y * bf_hi(wb.x), v.z * bf_lo(wb.y), v.w * bf_hi(wb.y));
+        }
+#pragma unroll
+        for (int t = 0; t < MK_TMAX; ++t) {
+            const float q = warp_sum(ssp[t]);
+            if (lane == 0) s_red[warp][t] = q;
         }
         named_sync(1, MK_CONS_THREADS);
+    };
+    // 1/RMS of token t from the per-warp sums of squares (fixed order)
+    auto rs_of = [&](int t) {
+        float q = 0.f;
+#pragma unroll
+        for (int w = 0; w < MK_CONS_WARPS; ++w) q += s_red[w][t];
+        return rsqrtf(q / (float)p.D + p.eps);
+    };
+
+    // Weights of one layer phase: the CTA's slice is at most MK_NST ring stages, all issued
+    // ahead by the producer. Every warp reduces work items across all of those stages at once,
+    // then one CTA barrier releases the stages, and the rows' sums (items added in fixed
+    // order) go out. More stages than the ring are taken in batches.
+    __shared__ float s_part2[2][MK_NST * MK_ITEMS][MK_TMAX];
+    auto consume_all = [&](int kind, int l, bool normed, auto&& out) -> bool {
+        const Slice sl = slice_of(p, kind, l, c, G);
+        const int S = (kind == PH_GU) ? 1 : sl.K / MK_SEG;  // items per row (gate and up: one each)
+        const int ipr = (kind == PH_GU) ? 2 : S;
+        const uint32_t rb = (uint32_t)sl.K * 2u;
+        const int n_st = (sl.n + sl.rs - 1) / sl.rs;
+        bool good = true;
+        for (int b0 = 0; b0 < n_st; b0 += MK_NST) {
+            const int nb = min(MK_NST, n_st - b0);
+            const int rows_b = min(sl.n - b0 * sl.rs, nb * sl.rs);
+            const int items_b = rows_b * ipr;  // stages hold MK_ITEMS items each but the last
+            float (*part)[MK_TMAX] = s_part2[(it + b0) & 1u];
+            for (int item = warp; item < items_b && good; item += MK_CONS_WARPS) {
+                const int sb = item / MK_ITEMS, ii = item % MK_ITEMS;
+                const uint32_t k = it + b0 + sb;
+                const int st = k % MK_NST;
+                const int nr = min(sl.rs, rows_b - sb * sl.rs);  // rows in this stage
+                if (!mb_wait(su32(full + st), (k / MK_NST) & 1u, p.abort_g)) {
+                    good = false;
+                    if (lane == 0) {
+                        atomicOr(p.status, QW_DEV_TIMEOUT);
+                        atomicExch(p.abort_g, 1);
+                    }
+                    break;
+                }
+                uint32_t wa, aa;
+                const uint32_t st_addr = su32(ring + st * MK_STAGE);
+                if (kind == PH_GU) {
+                    wa = st_addr + ((ii & 1) * nr + (ii >> 1)) * rb;
+                    aa = hs_addr;
+                } else {
+                    wa = st_addr + (ii / S) * rb + (ii % S) * (MK_SEG * 2);
+                    aa = hs_addr + (ii % S) * (MK_SEG * 4);
+                }
+                uint4 wv[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) wv[q] = lds128(wa + (q * 256 + lane * 8) * 2);
+                float acc[MK_TMAX][4];
+#pragma unroll
+                for (int t = 0; t < MK_TMAX; ++t) {
+                    if (t < T) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const uint32_t ap = aa + (uint32_t)(t * sl.K + q * 256 + lane * 8) * 4u;
+                            acc[t][q] = dot8b(wv[q], lds128f(ap), lds128f(ap + 16), 0.f);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int t = 0; t < MK_TMAX; ++t) {
+                    if (t < T) {
+                        const float v = warp_sum((acc[t][0] + acc[t][1]) + (acc[t][2] + acc[t][3]));
+                        if (lane == t) part[item][t] = v;
+                    }
+                }
+            }
+            if (!good) s_fail = 1;
+            named_sync(5, MK_CONS_THREADS);
+            if (warp == 0 && lane < nb) mb_arrive(su32(empty + (it + b0 + lane) % MK_NST));  // stages consumed
+            good = good && (s_fail == 0);
+            if (good) {
+                for (int r = warp; r < rows_b; r += MK_CONS_WARPS) {
+                    if (lane < T) {
+                        const int base = (r / sl.rs) * MK_ITEMS + (r % sl.rs) * ipr;
+                        float v[2];
+                        if (kind == PH_GU) {
+                            v[0] = part[base][lane];
+                            v[1] = part[base + 1][lane];
+                        } else {
+                            float a = 0.f;
+                            for (int q = 0; q < S; ++q) a += part[base + q][lane];
+                            v[0] = a;
+                            v[1] = 0.f;
+                        }
+                        if (normed) {
+                            const float rs = rs_of(lane);
+                            v[0] *= rs;
+                            v[1] *= rs;
+                        }
+                        out(sl.r0 + b0 * sl.rs + r, lane, v);
+                    }
+                }
+            }
+        }
+        it += (uint32_t)n_st;
+        return good;
     };
     // fp16 activation rows [T][K] (through L2) widened into fp32 shared memory.
     auto stage_h = [&](const f16* src, int K) {
@@ -457,7 +553,7 @@ __global__ void __launch_bounds__(MK_THREADS, 1) k_decode_mk(const MkParams p) {
         // ---- q|k|v projections (Paso 5), input RMSNorm fused -------------------------
         prefetch_kv(l);
         stage_norm(nb);
-        ok = consume(PH_QKV, l, [&](int row, int t, const float* v) { __stcg(p.qkv + (size_t)t * p.QKV + row, v[0]); });
+        ok = consume_all(PH_QKV, l, true, [&](int row, int t, const float* v) { __stcg(p.qkv + (size_t)t * p.QKV + row, v[0]); });
         if (!(ok = gsync(ok))) break;
 
         // ---- attention (Paso 5): QK-norm, RoPE, KV append, split-KV online softmax -----
@@ -693,7 +789,7 @@ __global__ void __launch_bounds__(MK_THREADS, 1) k_decode_mk(const MkParams p) {
 
         // ---- o_proj + residual (Pasos 5, 7) -------------------------------------------
         stage_h(p.o, p.QD);
-        ok = consume(PH_O, l, [&](int row, int t, const float* v) {
+        ok = consume_all(PH_O, l, false, [&](int row, int t, const float* v) {
             float* xp = p.x + (size_t)t * p.D + row;
             __stcg(xp, __ldcg(xp) + v[0]);
         });
@@ -701,7 +797,7 @@ __global__ void __launch_bounds__(MK_THREADS, 1) k_decode_mk(const MkParams p) {
 
         // ---- gate/up + SiLU*mul (Paso 6), post-attention RMSNorm fused -----------------
         stage_norm(nb + p.D);
-        ok = consume(PH_GU, l, [&](int row, int t, const float* v) {
+        ok = consume_all(PH_GU, l, true, [&](int row, int t, const float* v) {
             const float a = v[0] / (1.0f + expf(-v[0])) * v[1];
             if (f16_out_of_range(a)) atomicOr(p.status, QW_DEV_RANGE);
             __stcg(reinterpret_cast<unsigned short*>(p.act) + (size_t)t * p.I + row, __half_as_ushort(__float2half_rn(a)));
@@ -710,7 +806,7 @@ __global__ void __launch_bounds__(MK_THREADS, 1) k_decode_mk(const MkParams p) {
 
         // ---- down_proj + residual (Pasos 6, 7) ----------------------------------------
         stage_h(p.act, p.I);
-        ok = consume(PH_D, l, [&](int row, int t, const float* v) {
+        ok = consume_all(PH_D, l, false, [&](int row, int t, const float* v) {
             float* xp = p.x + (size_t)t * p.D + row;
             const float nv = __ldcg(xp) + v[0];
             __stcg(xp, nv);
@@ -725,11 +821,13 @@ __global__ void __launch_bounds__(MK_THREADS, 1) k_decode_mk(const MkParams p) {
         unsigned long long best[MK_TMAX];
 #pragma unroll
         for (int t = 0; t < MK_TMAX; ++t) best[t] = 0ull;
+        const float rs_lane = lane < T ? rs_of(lane) : 0.f;  // this lane's token (lane = t below)
         ok = consume(PH_LM, 0, [&](int row, int t, const float* v) {
-            if (p.logits) __stcg(p.logits + (size_t)t * p.V + row, v[0]);
+            const float y = v[0] * rs_lane;
+            if (p.logits) __stcg(p.logits + (size_t)t * p.V + row, y);
 #pragma unroll
             for (int q = 0; q < MK_TMAX; ++q)
-                if (q == t) best[q] = u64_max(best[q], argmax_key(v[0], row));
+                if (q == t) best[q] = u64_max(best[q], argmax_key(y, row));
         });
         if (!ok) s_fail = 1;
 #pragma unroll
