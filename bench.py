@@ -197,12 +197,15 @@ def peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-def kernel_bytes(kind: int, s, T: int, B: int) -> float:
-    """Algorithmic bytes of one launch of a kernel kind (weights once + activations in/out)."""
+def kernel_bytes(kind: int, s, T: int, B: int, ctx: float = 0.0) -> float:
+    """Algorithmic bytes of one launch of a kernel kind (weights once + activations in/out;
+    ctx: cached keys read by an attention launch)."""
     D, I, QD, KD, V = s.hidden, s.inter, s.n_heads * s.head_dim, s.n_kv_heads * s.head_dim, s.vocab
     QKV = QD + 2 * KD
     if kind == 1:   # q|k|v projection (+ fused input RMSNorm)
         return QKV * D * 2 + T * D * 4 + T * QKV * 4 + D * 2
+    if kind == 3:   # attention fused with o_proj (one token): o_proj weights + the cached K/V once
+        return D * QD * 2 + ctx * KD * 2 * 2 + s.n_kv_heads * T * D * 4
     if kind == 4:   # o_proj + residual
         return D * QD * 2 + T * QD * 2 + 2 * T * D * 4
     if kind == 5:   # gate/up + SiLU*mul (+ fused post-attention RMSNorm)
@@ -227,7 +230,8 @@ def step_bytes(s, B: int, ctx: float) -> float:
 SERIAL_NOTE = ("CUDA events around each launch of the kind, in one extra step with programmatic dependent "
                "launch off (serialised); the timed steps overlap launches")
 
-KIND_NAMES = {1: "qkv_proj(rmsnorm fused)", 2: "qknorm_rope_append", 3: "attention", 4: "o_proj+residual",
+KIND_NAMES = {1: "qkv_proj(rmsnorm fused)", 2: "qknorm_rope_append", 3: "attention(+o_proj fused at B=1)",
+              4: "o_proj+residual",
               5: "gate_up+silu_mul(rmsnorm fused)", 6: "down_proj+residual", 7: "lm_head+argmax",
               9: "k_decode_mk (persistent decode step)"}
 # names on the tensor-core path (more than 8 token rows)
@@ -345,7 +349,10 @@ def run_ours(args, cfg, rank, world):
     # same workload right after the timed region)
     hbm, bf16_burst, bf16_sust, peak_src = peaks()
     persistent = args.persistent and B <= 4
-    n_launch_per_step = {9: 1} if persistent else {1: s.n_layers, 4: s.n_layers, 5: s.n_layers, 6: s.n_layers, 7: 1}
+    # one token per step: attention and o_proj run as one kernel (kind 3)
+    n_launch_per_step = ({9: 1} if persistent else
+                         {1: s.n_layers, 3: s.n_layers, 5: s.n_layers, 6: s.n_layers, 7: 1} if B == 1 else
+                         {1: s.n_layers, 4: s.n_layers, 5: s.n_layers, 6: s.n_layers, 7: 1})
     kinds = {}
     for kind, nl in n_launch_per_step.items():
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * nl)]
@@ -367,7 +374,8 @@ def run_ours(args, cfg, rank, world):
         qw.qw_profile_set(eng.model, 0, None, 0)
         st.synchronize()
         avg_us = statistics.mean(durs) * 1e3
-        nbytes = step_bytes(s, B, statistics.mean(ctxs)) if kind == 9 else kernel_bytes(kind, s, B, B)
+        nbytes = (step_bytes(s, B, statistics.mean(ctxs)) if kind == 9 else
+                  kernel_bytes(kind, s, B, B, statistics.mean(ctxs)))
         kinds[kind] = dict(name=KIND_NAMES[kind], launches_per_step=nl, avg_us=avg_us,
                            total_us_per_step=avg_us * nl, bytes=nbytes)
     dom = max(kinds, key=lambda k: kinds[k]["total_us_per_step"])

@@ -383,6 +383,379 @@ cudaError_t launch_attn_paged(const LaunchCtx& c, int T, int layer, const f16* q
 }
 
 // =======================================================================================
+// k_attn_oproj: decode attention of ONE token over a short cache fused with o_proj (Pasos 5
+// and 7), for the latency-bound batch-1 decode step. o_proj is split by KV head: with heads
+// 2g, 2g+1 reading KV head g, the 256 attention outputs of g are exactly inputs
+// [256 g, 256 g + 256) of o_proj, so x += Wo o becomes x += sum_g Wo[:, 256 g ..] o_g. CTA
+// (rb, g) computes the attention of KV head g -- QK-norm and RoPE of its two query heads and
+// of the new key, online softmax over the cached pages plus the new key (taken from
+// registers, rounded to fp16 as the cache stores it) -- and the partial product of o_proj rows
+// [32 rb, 32 rb + 32) over that head's inputs into part[g][row]. The 32 CTAs of a head repeat
+// its attention (a few cached pages) instead of waiting for each other; the CTAs with rb == 0
+// append the new K/V. The partials are added to x, in order of g, by the next kernels
+// (gate/up reads x + sum_g part[g] for its RMSNorm, down_proj adds them to the residual it
+// updates). Nothing of the cached pages or of o_proj depends on the step, so before the
+// dependency wait each CTA loads its o_proj weights into registers and bulk-copies the head's
+// cached K/V pages (at most AO_MAXPG) into shared memory.
+// =======================================================================================
+namespace {
+
+constexpr int AO_ROWS = 32;    // o_proj rows per CTA (8 per warp)
+constexpr int AO_MAXPG = 12;   // cached pages held in shared memory (192 keys)
+constexpr int AO_PAGE = 16 * 128 * 2;  // K (or V) of one 16-key page of one head (4 KB)
+constexpr unsigned long long AO_WAIT_NS = 2000000000ull;
+
+struct AttnOP {
+    const float* qkv;  // [(n_heads + 2 n_kv) * 128] fp32
+    const bf16* q_norm;
+    const bf16* k_norm;
+    float eps;
+    const float* rope_cos;
+    const float* rope_sin;
+    int32_t* dbg_pos;
+    int32_t* dbg_slot;
+    int* status;
+    f16* dbg_attn;  // optional [n_heads * 128]
+    int n_heads, n_kv, D, QD;
+    int seq;        // the token's sequence (its cached length and pages are read before the wait)
+    TokView tv;
+    KVView kv;
+    int layer;
+    const bf16* Wo;  // [D][QD] of this layer
+    float* part;     // [n_kv][D]
+    float scale_log2;
+};
+
+__device__ __forceinline__ float dot8_bf(const uint4 w, const float4 a0, const float4 a1) {
+    float acc = bf_lo(w.x) * a0.x;
+    acc = fmaf(bf_hi(w.x), a0.y, acc);
+    acc = fmaf(bf_lo(w.y), a0.z, acc);
+    acc = fmaf(bf_hi(w.y), a0.w, acc);
+    acc = fmaf(bf_lo(w.z), a1.x, acc);
+    acc = fmaf(bf_hi(w.z), a1.y, acc);
+    acc = fmaf(bf_lo(w.w), a1.z, acc);
+    acc = fmaf(bf_hi(w.w), a1.w, acc);
+    return acc;
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(128) k_attn_oproj(const __grid_constant__ AttnOP p) {
+    extern __shared__ __align__(128) uint8_t ao_pages[];  // [page][K 4 KB | V 4 KB]
+    __shared__ __align__(8) uint64_t ao_bar;
+    __shared__ int ao_np, ao_bad;
+    pdl_launch();
+    const int rb = blockIdx.x, g = blockIdx.y;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const f16* Kl = p.kv.k + (size_t)p.layer * p.kv.layer_stride;
+    const f16* Vl = p.kv.v + (size_t)p.layer * p.kv.layer_stride;
+    const int* pt = p.kv.page_table + (size_t)p.seq * p.kv.max_pages_per_seq;
+    // before the wait: the cached pages of head g (the length and page table were written
+    // before this step began) and this CTA's o_proj weights
+    if (threadIdx.x == 0) {
+        const uint32_t bar = (uint32_t)__cvta_generic_to_shared(&ao_bar);
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        const int cached = p.kv.len[p.seq];
+        const int np = min((cached + 15) >> 4, AO_MAXPG);
+        int bad = 0;
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(np * 2 * AO_PAGE) : "memory");
+        for (int i = 0; i < np; ++i) {
+            int page = pt[i];
+            if (page < 0 || page >= p.kv.n_pages) {
+                bad = 1;  // reported by the append; any valid block keeps the copy in bounds
+                page = 0;
+            }
+            const size_t off = ((size_t)page * p.n_kv + g) * 16 * 128;
+            const uint32_t dst = (uint32_t)__cvta_generic_to_shared(ao_pages + (size_t)i * 2 * AO_PAGE);
+            asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                         "l"(Kl + off), "r"(AO_PAGE), "r"(bar)
+                         : "memory");
+            asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst + AO_PAGE),
+                         "l"(Vl + off), "r"(AO_PAGE), "r"(bar)
+                         : "memory");
+        }
+        ao_np = np;
+        ao_bad = bad;
+    }
+    uint4 wo[8];
+#pragma unroll
+    for (int r = 0; r < 8; ++r)
+        wo[r] = ldg_nc(p.Wo + (size_t)(rb * AO_ROWS + warp * 8 + r) * p.QD + 256 * g + lane * 8);
+    pdl_wait();
+
+    __shared__ float sq[2][128];            // rotated q of heads 2g, 2g+1
+    __shared__ float skv[2][128];           // the new k (rotated) and v, as fp16 values
+    __shared__ float so[4][2][128];         // per-warp partial outputs
+    __shared__ float smm[4][2], sll[4][2];  // per-warp running max / sum
+    __shared__ __align__(16) float ob[256]; // attention output of head pair g, fp16 values
+    const int NH = p.n_heads + 2 * p.n_kv;
+    const int half = lane >> 4, dl = (lane & 15) * 8;
+    const int pos = p.tv.pos[0];
+    // 1. QK-norm + RoPE of the query heads (warps 0, 1) and the new key (warp 2); v (warp 3)
+    {
+        const int hh = warp < 2 ? 2 * g + warp : (warp == 2 ? p.n_heads + g : p.n_heads + p.n_kv + g);
+        const float4 xv = *reinterpret_cast<const float4*>(p.qkv + (size_t)hh * 128 + lane * 4);
+        float y[4] = {xv.x, xv.y, xv.z, xv.w};
+        if (warp < 3) {
+            const bf16* nw = warp < 2 ? p.q_norm : p.k_norm;
+            const float ss = warp_sum(y[0] * y[0] + y[1] * y[1] + y[2] * y[2] + y[3] * y[3]);
+            const float r = rsqrtf(ss * (1.0f / 128.0f) + p.eps);
+            const uint2 wb = *reinterpret_cast<const uint2*>(nw + lane * 4);
+            y[0] *= r * bf_lo(wb.x);
+            y[1] *= r * bf_hi(wb.x);
+            y[2] *= r * bf_lo(wb.y);
+            y[3] *= r * bf_hi(wb.y);
+            const int i0 = (lane & 15) * 4;
+            const float4 cs = *reinterpret_cast<const float4*>(p.rope_cos + (size_t)pos * 64 + i0);
+            const float4 sn = *reinterpret_cast<const float4*>(p.rope_sin + (size_t)pos * 64 + i0);
+            const float c[4] = {cs.x, cs.y, cs.z, cs.w}, sv[4] = {sn.x, sn.y, sn.z, sn.w};
+            float o[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float pj = __shfl_xor_sync(0xffffffffu, y[j], 16);
+                o[j] = (lane < 16) ? (y[j] * c[j] - pj * sv[j]) : (pj * sv[j] + y[j] * c[j]);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) y[j] = o[j];
+        }
+        if (warp < 2) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) sq[warp][lane * 4 + j] = y[j];
+        } else {
+            const uint32_t w0 = pack_h2(y[0], y[1]), w1 = pack_h2(y[2], y[3]);
+            skv[warp - 2][lane * 4 + 0] = h_lo(w0);
+            skv[warp - 2][lane * 4 + 1] = h_hi(w0);
+            skv[warp - 2][lane * 4 + 2] = h_lo(w1);
+            skv[warp - 2][lane * 4 + 3] = h_hi(w1);
+            if (rb == 0) {  // one CTA per KV head appends
+                const int pi = pos >> 4;
+                const int page = (pi < p.kv.max_pages_per_seq) ? pt[pi] : -1;
+                if (page < 0 || page >= p.kv.n_pages) {
+                    if (lane == 0) atomicOr(p.status, QW_DEV_BAD_POS);
+                } else {
+                    f16* pool = (warp == 2 ? p.kv.k : p.kv.v) + (size_t)p.layer * p.kv.layer_stride;
+                    if (f16_out_of_range(y[0]) || f16_out_of_range(y[1]) || f16_out_of_range(y[2]) ||
+                        f16_out_of_range(y[3]))
+                        atomicOr(p.status, QW_DEV_RANGE);
+                    *reinterpret_cast<uint2*>(pool + (((size_t)page * p.n_kv + g) * 16 + (pos & 15)) * 128 + lane * 4) =
+                        make_uint2(w0, w1);
+                    if (p.dbg_pos && warp == 2 && g == 0 && lane == 0) {
+                        p.dbg_pos[0] = pos;
+                        p.dbg_slot[0] = page * 16 + (pos & 15);
+                    }
+                }
+            }
+        }
+    }
+    // the cached pages have landed (bounded wait)
+    {
+        const uint32_t bar = (uint32_t)__cvta_generic_to_shared(&ao_bar);
+        const uint64_t t0 = globaltimer_ns();
+        uint32_t done = 0;
+        while (true) {
+            asm volatile(
+                "{\n\t.reg .pred q;\n\t"
+                "mbarrier.try_wait.parity.shared::cta.b64 q, [%1], 0;\n\t"
+                "selp.u32 %0, 1, 0, q;\n\t}"
+                : "=r"(done)
+                : "r"(bar)
+                : "memory");
+            if (done) break;
+            if (globaltimer_ns() - t0 > AO_WAIT_NS) {
+                if (threadIdx.x == 0) atomicOr(p.status, QW_DEV_TIMEOUT);
+                break;
+            }
+        }
+    }
+    __syncthreads();
+    // 2. online softmax over the cached keys [0, pos) (pages round-robin over the warps; the
+    //    page of the new position only below it) and, on warp 0, the new key
+    float q0[8], q1[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        q0[i] = sq[0][dl + i] * p.scale_log2;
+        q1[i] = sq[1][dl + i] * p.scale_log2;
+    }
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f, o0[8], o1[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o0[i] = o1[i] = 0.f;
+    const int np = ao_np;
+    for (int pg = warp; pg < np && !ao_bad; pg += 4) {
+        const int nvalid = min(16, pos - pg * 16);
+        const uint8_t* kp = ao_pages + (size_t)pg * 2 * AO_PAGE;
+        uint4 kr[8], vr[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            kr[i] = *reinterpret_cast<const uint4*>(kp + ((2 * i + half) * 128 + dl) * 2);
+            vr[i] = *reinterpret_cast<const uint4*>(kp + AO_PAGE + ((2 * i + half) * 128 + dl) * 2);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (2 * i + half >= nvalid) vr[i] = make_uint4(0u, 0u, 0u, 0u);
+        float s0[8], s1[8], pm0 = -INFINITY, pm1 = -INFINITY;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float d0 = half_warp_sum(dot8q(q0, kr[i]));
+            const float d1 = half_warp_sum(dot8q(q1, kr[i]));
+            const bool valid = (2 * i + half) < nvalid;
+            s0[i] = valid ? d0 : -INFINITY;
+            s1[i] = valid ? d1 : -INFINITY;
+            pm0 = fmaxf(pm0, s0[i]);
+            pm1 = fmaxf(pm1, s1[i]);
+        }
+        pm0 = fmaxf(pm0, __shfl_xor_sync(0xffffffffu, pm0, 16));
+        pm1 = fmaxf(pm1, __shfl_xor_sync(0xffffffffu, pm1, 16));
+        const float n0 = fmaxf(m0, pm0), n1 = fmaxf(m1, pm1);
+        if (n0 == -INFINITY) continue;
+        const float a0 = exp2f(m0 - n0), a1 = exp2f(m1 - n1);
+        m0 = n0;
+        m1 = n1;
+        l0 *= a0;
+        l1 *= a1;
+#pragma unroll
+        for (int d = 0; d < 8; ++d) {
+            o0[d] *= a0;
+            o1[d] *= a1;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float e0 = exp2f(s0[i] - m0), e1 = exp2f(s1[i] - m1);
+            l0 += e0;
+            l1 += e1;
+            const uint32_t vw[4] = {vr[i].x, vr[i].y, vr[i].z, vr[i].w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float va = h_lo(vw[j]), vb = h_hi(vw[j]);
+                o0[2 * j] = fmaf(e0, va, o0[2 * j]);
+                o0[2 * j + 1] = fmaf(e0, vb, o0[2 * j + 1]);
+                o1[2 * j] = fmaf(e1, va, o1[2 * j]);
+                o1[2 * j + 1] = fmaf(e1, vb, o1[2 * j + 1]);
+            }
+        }
+    }
+    if (warp == 0) {
+        // the new key: both half-warps move the max, half 0 adds its weight
+        float d0 = 0.f, d1 = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            d0 = fmaf(q0[i], skv[0][dl + i], d0);
+            d1 = fmaf(q1[i], skv[0][dl + i], d1);
+        }
+        d0 = half_warp_sum(d0);
+        d1 = half_warp_sum(d1);
+        const float n0 = fmaxf(m0, d0), n1 = fmaxf(m1, d1);
+        const float a0 = exp2f(m0 - n0), a1 = exp2f(m1 - n1);
+        m0 = n0;
+        m1 = n1;
+        l0 *= a0;
+        l1 *= a1;
+#pragma unroll
+        for (int d = 0; d < 8; ++d) {
+            o0[d] *= a0;
+            o1[d] *= a1;
+        }
+        if (half == 0) {
+            const float e0 = exp2f(d0 - m0), e1 = exp2f(d1 - m1);
+            l0 += e0;
+            l1 += e1;
+#pragma unroll
+            for (int d = 0; d < 8; ++d) {
+                o0[d] = fmaf(e0, skv[1][dl + d], o0[d]);
+                o1[d] = fmaf(e1, skv[1][dl + d], o1[d]);
+            }
+        }
+    }
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 16);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 16);
+#pragma unroll
+    for (int d = 0; d < 8; ++d) {
+        o0[d] += __shfl_xor_sync(0xffffffffu, o0[d], 16);
+        o1[d] += __shfl_xor_sync(0xffffffffu, o1[d], 16);
+    }
+    if (lane < 16) {
+#pragma unroll
+        for (int d = 0; d < 8; ++d) {
+            so[warp][0][dl + d] = o0[d];
+            so[warp][1][dl + d] = o1[d];
+        }
+    }
+    if (lane == 0) {
+        smm[warp][0] = m0;
+        smm[warp][1] = m1;
+        sll[warp][0] = l0;
+        sll[warp][1] = l1;
+    }
+    __syncthreads();
+    {
+        // 128 threads: thread -> (head hh, dims 2*(tid%64), +1); warps without keys add nothing
+        const int hh = threadIdx.x >> 6, d2 = (threadIdx.x & 63) * 2;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) M = fmaxf(M, smm[w][hh]);
+        float L = 0.f, O0 = 0.f, O1 = 0.f;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            const float f = smm[w][hh] == -INFINITY ? 0.f : exp2f(smm[w][hh] - M);
+            L += sll[w][hh] * f;
+            O0 += so[w][hh][d2] * f;
+            O1 += so[w][hh][d2 + 1] * f;
+        }
+        const uint32_t hv = pack_h2(O0 / L, O1 / L);  // the attention output as the unfused path stores it
+        ob[hh * 128 + d2] = h_lo(hv);
+        ob[hh * 128 + d2 + 1] = h_hi(hv);
+        if (p.dbg_attn && rb == 0)
+            *reinterpret_cast<uint32_t*>(p.dbg_attn + (size_t)(2 * g + hh) * 128 + d2) = hv;
+    }
+    __syncthreads();
+    // 3. o_proj partial of this CTA's rows over KV head g's inputs
+    const float4 a0 = *reinterpret_cast<const float4*>(&ob[lane * 8]);
+    const float4 a1 = *reinterpret_cast<const float4*>(&ob[lane * 8 + 4]);
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        const float acc = warp_sum(dot8_bf(wo[r], a0, a1));
+        if (lane == 0) p.part[(size_t)g * p.D + rb * AO_ROWS + warp * 8 + r] = acc;
+    }
+}
+
+int attn_oproj_max_keys() { return AO_MAXPG * 16; }
+
+cudaError_t launch_attn_oproj(const LaunchCtx& c, int seq, int layer, const AttnFuse& fz, int n_heads, int n_kv,
+                              TokView tv, KVView kv, const bf16* Wo, int D, float* part, f16* dbg_attn) {
+    if (D % AO_ROWS) return cudaErrorInvalidValue;
+    static bool attr_set = false;
+    const int smem = AO_MAXPG * 2 * AO_PAGE;
+    if (!attr_set) {
+        cudaError_t e = cudaFuncSetAttribute(k_attn_oproj, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    AttnOP p = {};
+    p.qkv = fz.qkv;
+    p.q_norm = fz.q_norm;
+    p.k_norm = fz.k_norm;
+    p.eps = fz.eps;
+    p.rope_cos = fz.rope_cos;
+    p.rope_sin = fz.rope_sin;
+    p.dbg_pos = fz.dbg_pos;
+    p.dbg_slot = fz.dbg_slot;
+    p.status = fz.status;
+    p.dbg_attn = dbg_attn;
+    p.n_heads = n_heads;
+    p.n_kv = n_kv;
+    p.D = D;
+    p.QD = n_heads * 128;
+    p.seq = seq;
+    p.tv = tv;
+    p.kv = kv;
+    p.layer = layer;
+    p.Wo = Wo;
+    p.part = part;
+    p.scale_log2 = 0.08838834764831845f * 1.4426950408889634f;  // 128^-0.5 * log2(e)
+    return launch_k(c, k_attn_oproj, dim3(D / AO_ROWS, n_kv), dim3(128), (size_t)smem, p);
+}
+
+// =======================================================================================
 // Warp-level helpers of the mma.sync paths (decode attention) and of the prefill kernel's
 // Q staging: cp.async copies, ldmatrix, m16n8k16 MMA.
 // =======================================================================================

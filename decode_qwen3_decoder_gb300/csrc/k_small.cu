@@ -183,6 +183,10 @@ struct GemvP {
     f16* out_h;
     unsigned long long* best;
     int* status;  // G_GATEUP: QW_DEV_RANGE when an fp16 activation would overflow
+    // optional o_proj partial sums not yet in x: the residual seen by this kernel is
+    // x + sum_g xadd[g][t][:] (g < n_add, added in order); G_GATEUP and G_RESID
+    const float* xadd;
+    int n_add;
 };
 
 constexpr int GEMV_WARPS = 4;
@@ -306,7 +310,12 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) k_gemv(GemvP p) {
 #pragma unroll
         for (int rr = 0; rr < RPW; ++rr) {
             const int row = gw * RPW + rr;
-            xres[rr] = (lane < p.T && row < p.n_out) ? p.out[(size_t)lane * p.n_out + row] : 0.f;
+            float v = 0.f;
+            if (lane < p.T && row < p.n_out) {
+                v = p.out[(size_t)lane * p.n_out + row];
+                for (int g = 0; g < p.n_add; ++g) v += p.xadd[((size_t)g * p.T + lane) * p.n_out + row];
+            }
+            xres[rr] = v;
         }
         for (int i = tid; i < TT * K / 8; i += blockDim.x) {
             const int t = i / (K / 8), k8 = (i % (K / 8)) * 8;
@@ -332,8 +341,27 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) k_gemv(GemvP p) {
             const float* xr = p.x + (size_t)(live ? (p.rows ? p.rows[t] : t) : 0) * K;
 #pragma unroll
             for (int c = 0; c < NCH; ++c) {
-                const float4 v = live ? *reinterpret_cast<const float4*>(xr + (tid + c * 128) * 4)
-                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+                float4 v = live ? *reinterpret_cast<const float4*>(xr + (tid + c * 128) * 4)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+                if (live && p.n_add) {  // o_proj partials (decode rows: row t is token t)
+                    float4 a[8];
+                    const int na = min(p.n_add, 8);
+                    for (int g = 0; g < na; ++g)
+                        a[g] = *reinterpret_cast<const float4*>(p.xadd + ((size_t)g * p.T + t) * K + (tid + c * 128) * 4);
+                    for (int g = 0; g < na; ++g) {
+                        v.x += a[g].x;
+                        v.y += a[g].y;
+                        v.z += a[g].z;
+                        v.w += a[g].w;
+                    }
+                    for (int g = 8; g < p.n_add; ++g) {
+                        const float4 b = *reinterpret_cast<const float4*>(p.xadd + ((size_t)g * p.T + t) * K + (tid + c * 128) * 4);
+                        v.x += b.x;
+                        v.y += b.y;
+                        v.z += b.z;
+                        v.w += b.w;
+                    }
+                }
                 *reinterpret_cast<float4*>(hs + t * K + (tid + c * 128) * 4) = v;
                 part += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
             }
@@ -409,7 +437,10 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) k_gemv(GemvP p) {
                             p.out[(size_t)t * p.n_out + row] = acc[rr][0][t];
                         } else if (MODE == G_RESID) {
                             float* o = p.out + (size_t)t * p.n_out + row;
-                            *o = (first_rows ? xres[rr] : *o) + acc[rr][0][t];
+                            float base = first_rows ? xres[rr] : *o;
+                            if (!first_rows)
+                                for (int g = 0; g < p.n_add; ++g) base += p.xadd[((size_t)g * p.T + t) * p.n_out + row];
+                            *o = base + acc[rr][0][t];
                         } else if (MODE == G_GATEUP) {
                             const float g = acc[rr][0][t], u = acc[rr][NW - 1][t];
                             const float a = silu_f(g) * u;
@@ -527,18 +558,18 @@ cudaError_t launch_gemv_qkv(const LaunchCtx& c, int T, const float* x, const bf1
 
 cudaError_t launch_gemv_gateup(const LaunchCtx& c, int T, const float* x, const bf16* norm_w,
                                float eps, const bf16* Wg, const bf16* Wu, int inter, int K, f16* act,
-                               int* status, const QWeights* qg, const QWeights* qu) {
+                               int* status, const QWeights* qg, const QWeights* qu, const float* xadd, int n_add) {
     GemvP p = {};
     p.x = x; p.norm_w = norm_w; p.eps = eps; p.W = Wg; p.W2 = Wu; p.n_out = inter; p.K = K; p.T = T;
-    p.out_h = act; p.status = status;
+    p.out_h = act; p.status = status; p.xadd = xadd; p.n_add = xadd ? n_add : 0;
     if (qg) { p.qw = qg->codes; p.sb = qg->sb; p.qw2 = qu->codes; p.sb2 = qu->sb; }
     return gemv_any<G_GATEUP>(c, p, qg ? qg->bits : 16, 0);
 }
 
 cudaError_t launch_gemv_resid(const LaunchCtx& c, int T, const f16* act, const bf16* W, int n_out,
-                              int K, float* x, const QWeights* qw) {
+                              int K, float* x, const QWeights* qw, const float* xadd, int n_add) {
     GemvP p = {};
-    p.act = act; p.W = W; p.n_out = n_out; p.K = K; p.T = T; p.out = x;
+    p.act = act; p.W = W; p.n_out = n_out; p.K = K; p.T = T; p.out = x; p.xadd = xadd; p.n_add = xadd ? n_add : 0;
     if (qw) { p.qw = qw->codes; p.sb = qw->sb; }
     return gemv_any<G_RESID>(c, p, qw ? qw->bits : 16, 0);
 }

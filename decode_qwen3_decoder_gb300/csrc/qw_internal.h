@@ -163,9 +163,12 @@ cudaError_t launch_gemv_qkv(const LaunchCtx& c, int T, const float* x, const bf1
                             const bf16* W, int n_out, int K, float* out, const QWeights* qw = nullptr);
 cudaError_t launch_gemv_gateup(const LaunchCtx& c, int T, const float* x, const bf16* norm_w,
                                float eps, const bf16* Wg, const bf16* Wu, int inter, int K, f16* act,
-                               int* status, const QWeights* qg = nullptr, const QWeights* qu = nullptr);
+                               int* status, const QWeights* qg = nullptr, const QWeights* qu = nullptr,
+                               const float* xadd = nullptr, int n_add = 0);
+// x += W act; with xadd, the residual is x + sum_g xadd[g][t][:] (g < n_add) first.
 cudaError_t launch_gemv_resid(const LaunchCtx& c, int T, const f16* act, const bf16* W, int n_out,
-                              int K, float* x, const QWeights* qw = nullptr);
+                              int K, float* x, const QWeights* qw = nullptr, const float* xadd = nullptr,
+                              int n_add = 0);
 cudaError_t launch_gemv_lmhead(const LaunchCtx& c, int B, const float* x, const int* rows,
                                const bf16* norm_w, float eps, const bf16* E, int vocab, int K,
                                float* logits, unsigned long long* best);
@@ -188,6 +191,14 @@ struct AttnFuse {
     int32_t* dbg_slot;
     int* status;
 };
+// Decode attention of one token (sequence `seq`) over a cache of at most attn_oproj_max_keys()
+// keys, fused with o_proj split by KV head: CTA (rb, g) computes the attention of KV head g
+// (both its query heads; QK-norm, RoPE; the CTAs with rb == 0 append the new K/V) and the
+// o_proj partial of rows [rb * 32, rb * 32 + 32) over that head's 256 inputs into
+// part[g][row]; the partials are added to x by the following gate/up and down_proj kernels.
+int attn_oproj_max_keys();
+cudaError_t launch_attn_oproj(const LaunchCtx& c, int seq, int layer, const AttnFuse& fz, int n_heads, int n_kv,
+                              TokView tv, KVView kv, const bf16* Wo, int D, float* part, f16* dbg_attn);
 cudaError_t launch_attn_paged(const LaunchCtx& c, int T, int layer, const f16* q, int n_heads,
                               int n_kv, TokView tv, KVView kv, int chunk, int n_splits,
                               float* part_o, float* part_ml, int* counters, f16* out,

@@ -91,6 +91,7 @@ struct WsLayout {
     size_t x, h, qkv, q, attn, act, part_o, part_ml, counters;
     size_t tok_seq, tok_pos, tok_slot, last, best, status, gen_tok, gen_cur, gen_out, mk_sync;
     size_t st_part, st_ss, st_xw, st_done, st_tick, st_abort;  // batched decode-step kernel
+    size_t op_part;  // o_proj partials of the fused small-batch decode attention [n_kv][4][D]
     size_t total;
     int part_T;
 };
@@ -149,6 +150,7 @@ static WsLayout layout_for(const qw_config& c) {
         L.st_tick = take((size_t)2 * step_tiles((int)D, (int)I, QKVR) * 4);
         L.st_abort = take(4);
     }
+    L.op_part = take((size_t)c.n_kv_heads * 4 * D * 4);
     L.gen_tok = take(T * 4);
     L.gen_cur = take((size_t)c.max_batch * 4);
     L.gen_out = take((size_t)c.max_batch * ((size_t)c.max_context + 1) * 4);
@@ -188,6 +190,7 @@ struct qw_model {
     unsigned long long step_wait_ns;  // bound of its waits on other CTAs
     int step_extra;    // test-only: extra arrivals its first o_proj unit waits for
     float *st_part, *st_ss;
+    float* op_part;
     f16* st_xw;
     int *st_done, *st_tick, *st_abort;
     StepMaps st_maps;
@@ -318,6 +321,7 @@ extern "C" qw_status qw_init_weights(const qw_config* cfg, const qw_weight_ptrs*
     m->mk_sync = (unsigned*)(b + L.mk_sync);
     m->st_part = (float*)(b + L.st_part);
     m->st_ss = (float*)(b + L.st_ss);
+    m->op_part = (float*)(b + L.op_part);
     m->st_xw = (f16*)(b + L.st_xw);
     m->st_done = (int*)(b + L.st_done);
     m->st_tick = (int*)(b + L.st_tick);
@@ -918,6 +922,11 @@ static qw_status run_layers(qw_model* m, qw_kv* kv, const StepDesc& sd, bool pre
     // small decode batches over long caches: separate QK-norm/RoPE/append, then the
     // evenly split decode attention (short caches keep the fused per-pair kernel)
     const bool long_decode = !prefill && small && (long long)T * max_keys >= kLongDecodeKeys;
+    // decode of one token over a short cache (bf16 weights): attention and o_proj in one kernel,
+    // its per-KV-head partials added to x by the gate/up and down_proj kernels
+    const bool fuse_ao = !prefill && small && !long_decode && m->qbits == 16 && T == 1 &&
+                         max_keys <= attn_oproj_max_keys() && D % 32 == 0;
+    const float* xadd = fuse_ao ? m->op_part : nullptr;
     float* x = m->x + (size_t)t0 * D;
     f16* h = m->h + (size_t)t0 * D;
     f16* q = m->q + (size_t)t0 * QD;
@@ -980,6 +989,12 @@ static qw_status run_layers(qw_model* m, qw_kv* kv, const StepDesc& sd, bool pre
                 LAUNCH(launch_attn_decode(lc, T, l, q, c.n_heads, c.n_kv_heads, kvv, &kv->tm_k, &kv->tm_v, sd.seq + t0,
                                           max_keys, kMaxSplits,
                                           part_o, part_ml, counters, attn, m->status, m->num_sms));
+            } else if (fuse_ao) {
+                AttnFuse fz = {qkv, w_qn, w_kn, c.rms_eps, m->rcos, m->rsin, lpos, lslot, m->status};
+                PROF(QW_PROF_ATTN);
+                LAUNCH(launch_attn_oproj(lc, sd.seq[t0], l, fz, c.n_heads, c.n_kv_heads, tv, kvv, m->bo + (size_t)l * D * QD, D,
+                                         m->op_part,
+                                         (dbg && m->dbg_attn) ? m->dbg_attn + ((size_t)l * sd.T + t0) * QD : nullptr));
             } else {
                 // decode: one new token per sequence; QK-norm, RoPE and the KV append run inside
                 AttnFuse fz = {qkv, w_qn, w_kn, c.rms_eps, m->rcos, m->rsin, lpos, lslot, m->status};
@@ -1001,10 +1016,12 @@ static qw_status run_layers(qw_model* m, qw_kv* kv, const StepDesc& sd, bool pre
                                           max_keys, kMaxSplits,
                                           part_o, part_ml, counters, attn, m->status, m->num_sms));
         }
-        if (dbg && m->dbg_attn)
+        if (dbg && m->dbg_attn && !fuse_ao)
             CUDA_TRY(cudaMemcpyAsync(m->dbg_attn + ((size_t)l * sd.T + t0) * QD, attn, (size_t)T * QD * sizeof(f16),
                                      cudaMemcpyDeviceToDevice, st));
-        if (small) {
+        if (fuse_ao) {
+            // o_proj ran inside the attention kernel
+        } else if (small) {
             PROF(QW_PROF_OPROJ);
             LAUNCH(launch_gemv_resid(lc, T, attn, m->bo + (size_t)l * D * QD, D, QD, x, qq ? &qq[1] : nullptr));
         } else {
@@ -1021,10 +1038,11 @@ static qw_status run_layers(qw_model* m, qw_kv* kv, const StepDesc& sd, bool pre
                 PROF(QW_PROF_GATEUP);
                 LAUNCH(launch_gemv_gateup(lc, T, x, w_post, c.rms_eps, m->bg + (size_t)l * I * D,
                                           m->bu + (size_t)l * I * D, I, D, act, m->status, qq ? &qq[2] : nullptr,
-                                          qq ? &qq[3] : nullptr));
+                                          qq ? &qq[3] : nullptr, xadd, c.n_kv_heads));
             }
             PROF(QW_PROF_DOWN);
-            LAUNCH(launch_gemv_resid(lc, T, act, m->bd + (size_t)l * D * I, D, I, x, qq ? &qq[4] : nullptr));
+            LAUNCH(launch_gemv_resid(lc, T, act, m->bd + (size_t)l * D * I, D, I, x, qq ? &qq[4] : nullptr, xadd,
+                                     c.n_kv_heads));
         } else {
             {
                 PROF(QW_PROF_RMSNORM);
