@@ -339,31 +339,42 @@ __global__ void __launch_bounds__(GEMV_WARPS * 32) k_gemv(GemvP p) {
             float part = 0.f;
             const bool live = t < p.T;
             const float* xr = p.x + (size_t)(live ? (p.rows ? p.rows[t] : t) : 0) * K;
+            // every x load of the row first (unconditional: row 0 stands in for a dead row), so
+            // that they are in flight together
+            float4 v[NCH > 0 ? NCH : 1];
 #pragma unroll
-            for (int c = 0; c < NCH; ++c) {
-                float4 v = live ? *reinterpret_cast<const float4*>(xr + (tid + c * 128) * 4)
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
-                if (live && p.n_add) {  // o_proj partials (decode rows: row t is token t)
-                    float4 a[8];
-                    const int na = min(p.n_add, 8);
-                    for (int g = 0; g < na; ++g)
-                        a[g] = *reinterpret_cast<const float4*>(p.xadd + ((size_t)g * p.T + t) * K + (tid + c * 128) * 4);
-                    for (int g = 0; g < na; ++g) {
-                        v.x += a[g].x;
-                        v.y += a[g].y;
-                        v.z += a[g].z;
-                        v.w += a[g].w;
+            for (int c = 0; c < NCH; ++c) v[c] = *reinterpret_cast<const float4*>(xr + (tid + c * 128) * 4);
+            if (live && p.n_add) {  // o_proj partials not yet in x (decode rows: row t is token t)
+                constexpr int GB = NCH <= 2 ? 8 : (NCH <= 4 ? 4 : 1);  // partials in flight per batch
+                for (int g0 = 0; g0 < p.n_add; g0 += GB) {
+                    // GB partials' loads in flight (indices clamped), added in order of g
+                    float4 a[GB][NCH > 0 ? NCH : 1];
+#pragma unroll
+                    for (int j = 0; j < GB; ++j) {
+                        const int g = min(g0 + j, p.n_add - 1);
+#pragma unroll
+                        for (int c = 0; c < NCH; ++c)
+                            a[j][c] = *reinterpret_cast<const float4*>(p.xadd + ((size_t)g * p.T + t) * K + (tid + c * 128) * 4);
                     }
-                    for (int g = 8; g < p.n_add; ++g) {
-                        const float4 b = *reinterpret_cast<const float4*>(p.xadd + ((size_t)g * p.T + t) * K + (tid + c * 128) * 4);
-                        v.x += b.x;
-                        v.y += b.y;
-                        v.z += b.z;
-                        v.w += b.w;
+#pragma unroll
+                    for (int j = 0; j < GB; ++j) {
+                        if (g0 + j < p.n_add) {
+#pragma unroll
+                            for (int c = 0; c < NCH; ++c) {
+                                v[c].x += a[j][c].x;
+                                v[c].y += a[j][c].y;
+                                v[c].z += a[j][c].z;
+                                v[c].w += a[j][c].w;
+                            }
+                        }
                     }
                 }
-                *reinterpret_cast<float4*>(hs + t * K + (tid + c * 128) * 4) = v;
-                part += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+            }
+#pragma unroll
+            for (int c = 0; c < NCH; ++c) {
+                if (!live) v[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+                *reinterpret_cast<float4*>(hs + t * K + (tid + c * 128) * 4) = v[c];
+                part += v[c].x * v[c].x + v[c].y * v[c].y + v[c].z * v[c].z + v[c].w * v[c].w;
             }
             part = warp_sum(part);
             if (lane == 0) red[warp][t] = part;
