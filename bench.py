@@ -197,11 +197,17 @@ def peaks():
     return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-def kernel_bytes(kind: int, s, T: int, B: int, ctx: float = 0.0) -> float:
+def kernel_bytes(kind: int, s, T: int, B: int, ctx: float = 0.0, clusters: bool = False) -> float:
     """Algorithmic bytes of one launch of a kernel kind (weights once + activations in/out;
-    ctx: cached keys read by an attention launch)."""
+    ctx: cached keys read by an attention launch). clusters: the batch-1 path of two cluster
+    kernels per layer, whose attention launch (kind 3) also does q|k|v and whose MLP launch
+    (kind 5) also does down_proj."""
     D, I, QD, KD, V = s.hidden, s.inter, s.n_heads * s.head_dim, s.n_kv_heads * s.head_dim, s.vocab
     QKV = QD + 2 * KD
+    if clusters and kind == 3:   # x + partials in, q|k|v + o_proj weights, cached K/V, o_proj partials out
+        return QKV * D * 2 + D * QD * 2 + ctx * KD * 2 * 2 + 2 * KD * 2 + (1 + 16) * D * 4 + s.n_kv_heads * D * 4
+    if clusters and kind == 5:   # x + o_proj partials in, gate/up/down weights, down_proj partials out
+        return 3 * I * D * 2 + (1 + s.n_kv_heads) * D * 4 + 16 * D * 4
     if kind == 1:   # q|k|v projection (+ fused input RMSNorm)
         return QKV * D * 2 + T * D * 4 + T * QKV * 4 + D * 2
     if kind == 3:   # attention fused with o_proj (one token): o_proj weights + the cached K/V once
@@ -230,6 +236,9 @@ def step_bytes(s, B: int, ctx: float) -> float:
 SERIAL_NOTE = ("CUDA events around each launch of the kind, in one extra step with programmatic dependent "
                "launch off (serialised); the timed steps overlap launches")
 
+# the batch-1 path of two cluster kernels per layer
+CLUSTER_KIND_NAMES = {3: "rmsnorm+qkv+attention+o_proj (cluster kernel)",
+                      5: "rmsnorm+gate_up+swiglu+down_proj (cluster kernel)", 7: "lm_head+argmax"}
 KIND_NAMES = {1: "qkv_proj(rmsnorm fused)", 2: "qknorm_rope_append", 3: "attention(+o_proj fused at B=1)",
               4: "o_proj+residual",
               5: "gate_up+silu_mul(rmsnorm fused)", 6: "down_proj+residual", 7: "lm_head+argmax",
@@ -305,6 +314,7 @@ def run_ours(args, cfg, rank, world):
 
     for _ in range(args.warmup):
         one_step()
+    step_launches = qw.qw_last_launch_count(eng.model)  # of the last decode step
     st.synchronize()
     status = qw.qw_sync_status(eng.model, st)
     if status != 0:
@@ -349,8 +359,12 @@ def run_ours(args, cfg, rank, world):
     # same workload right after the timed region)
     hbm, bf16_burst, bf16_sust, peak_src = peaks()
     persistent = args.persistent and B <= 4
-    # one token per step: attention and o_proj run as one kernel (kind 3)
+    # one token per step: two cluster kernels per layer (step begin + 2 per layer + LM head +
+    # finalize), else attention and o_proj as one kernel (kind 3)
+    clusters = not persistent and B == 1 and step_launches == 2 * s.n_layers + 3
+    names = CLUSTER_KIND_NAMES if clusters else KIND_NAMES
     n_launch_per_step = ({9: 1} if persistent else
+                         {3: s.n_layers, 5: s.n_layers, 7: 1} if clusters else
                          {1: s.n_layers, 3: s.n_layers, 5: s.n_layers, 6: s.n_layers, 7: 1} if B == 1 else
                          {1: s.n_layers, 4: s.n_layers, 5: s.n_layers, 6: s.n_layers, 7: 1})
     kinds = {}
@@ -375,8 +389,8 @@ def run_ours(args, cfg, rank, world):
         st.synchronize()
         avg_us = statistics.mean(durs) * 1e3
         nbytes = (step_bytes(s, B, statistics.mean(ctxs)) if kind == 9 else
-                  kernel_bytes(kind, s, B, B, statistics.mean(ctxs)))
-        kinds[kind] = dict(name=KIND_NAMES[kind], launches_per_step=nl, avg_us=avg_us,
+                  kernel_bytes(kind, s, B, B, statistics.mean(ctxs), clusters))
+        kinds[kind] = dict(name=names[kind], launches_per_step=nl, avg_us=avg_us,
                            total_us_per_step=avg_us * nl, bytes=nbytes)
     dom = max(kinds, key=lambda k: kinds[k]["total_us_per_step"])
     dk = kinds[dom]
@@ -422,7 +436,7 @@ def run_ours(args, cfg, rank, world):
                           "unit": "GB/s", "frac": round(step_b / (decode_us * 1e-6) / 1e9 / hbm, 4),
                           "bytes_per_step": step_b, "step_us": round(decode_us, 2),
                           "note": "whole decode step (weights + KV read once) over the event-timed graph replay"},
-        "kernels": {KIND_NAMES[k]: {"avg_us": round(v["avg_us"], 3), "per_step_us": round(v["total_us_per_step"], 2),
+        "kernels": {names[k]: {"avg_us": round(v["avg_us"], 3), "per_step_us": round(v["total_us_per_step"], 2),
                                     "GB/s": round(v["bytes"] / (v["avg_us"] * 1e-6) / 1e9, 1)}
                     for k, v in kinds.items()},
         "kernels_timing": SERIAL_NOTE,

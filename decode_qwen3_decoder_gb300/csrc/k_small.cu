@@ -587,10 +587,10 @@ cudaError_t launch_gemv_resid(const LaunchCtx& c, int T, const f16* act, const b
 
 cudaError_t launch_gemv_lmhead(const LaunchCtx& c, int B, const float* x, const int* rows,
                                const bf16* norm_w, float eps, const bf16* E, int vocab, int K,
-                               float* logits, unsigned long long* best) {
+                               float* logits, unsigned long long* best, const float* xadd, int n_add) {
     GemvP p = {};
     p.x = x; p.rows = rows; p.norm_w = norm_w; p.eps = eps; p.W = E; p.n_out = vocab; p.K = K;
-    p.T = B; p.out = logits; p.best = best;
+    p.T = B; p.out = logits; p.best = best; p.xadd = xadd; p.n_add = xadd ? n_add : 0;
     return gemv_dispatch<G_LMHEAD, 16>(c, p, num_sms() * 8);
 }
 

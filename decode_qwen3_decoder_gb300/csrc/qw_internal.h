@@ -136,6 +136,30 @@ cudaError_t launch_k(const LaunchCtx& c, void (*kern)(KArgs...), dim3 grid, dim3
     if (c.counter) ++*c.counter;
     return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
 }
+// launch_k with thread-block clusters of `cluster` CTAs along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kc(const LaunchCtx& c, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                      unsigned cluster, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = c.stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (c.pdl) {
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
+        cfg.numAttrs = 2;
+    }
+    if (c.counter) ++*c.counter;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 #endif
 
 cudaError_t launch_step_begin(const LaunchCtx& c, const StepDesc& sd, const int32_t* ids,
@@ -169,9 +193,11 @@ cudaError_t launch_gemv_gateup(const LaunchCtx& c, int T, const float* x, const 
 cudaError_t launch_gemv_resid(const LaunchCtx& c, int T, const f16* act, const bf16* W, int n_out,
                               int K, float* x, const QWeights* qw = nullptr, const float* xadd = nullptr,
                               int n_add = 0);
+// xadd / n_add: partial vectors [n_add][B][K] added to the rows of x (in order) before the norm
 cudaError_t launch_gemv_lmhead(const LaunchCtx& c, int B, const float* x, const int* rows,
                                const bf16* norm_w, float eps, const bf16* E, int vocab, int K,
-                               float* logits, unsigned long long* best);
+                               float* logits, unsigned long long* best, const float* xadd = nullptr,
+                               int n_add = 0);
 cudaError_t launch_finalize(const LaunchCtx& c, const StepDesc& sd, unsigned long long* best,
                             int32_t* next_ids, KVView kv);
 cudaError_t launch_qknorm_rope_append(const LaunchCtx& c, int T, int layer, const float* qkv,
@@ -199,6 +225,67 @@ struct AttnFuse {
 int attn_oproj_max_keys();
 cudaError_t launch_attn_oproj(const LaunchCtx& c, int seq, int layer, const AttnFuse& fz, int n_heads, int n_kv,
                               TokView tv, KVView kv, const bf16* Wo, int D, float* part, f16* dbg_attn);
+// Batch-1 decode layer as two 16-CTA cluster launches (k_dec1.cu), for hidden 1024, inter
+// 128 x {16, 24, 32}, n_kv <= 8 and caches of at most dec1_max_keys() keys.
+// Attention kernel: x = xin + sum_{c < n_add} dpart[c]; RMSNorm; q|k|v of KV head g gathered
+// in cluster g; QK-norm, RoPE, KV append, attention; o_proj rows of the head's inputs into
+// opart[g][D]. Cluster 0 writes x to xout.
+struct Dec1Attn {
+    const float* xin;
+    const float* dpart;  // [n_add][D]
+    int n_add;
+    float* xout;         // [D]
+    const bf16* w_in;
+    float eps;
+    const bf16* Wqkv;    // [QD + 2 KD][D] of the layer
+    const bf16* q_norm;
+    const bf16* k_norm;
+    const float* rope_cos;
+    const float* rope_sin;
+    KVView kv;
+    int layer;
+    int seq;             // the token's sequence
+    const int* pos;      // [1] its position (written by the step-begin kernel)
+    const bf16* Wo;      // [D][QD] of the layer
+    float* opart;        // [n_kv][D]
+    f16* dbg_attn;       // optional [QD]
+    int32_t* dbg_pos;
+    int32_t* dbg_slot;
+    int* status;
+    int n_kv, QD, KD;
+    float scale_log2;
+    // optional %globaltimer records: CTA c of this launch writes 8 values at
+    // trace[((2 layer) * gridDim.x + c) * 8]
+    unsigned long long* trace;
+};
+// MLP kernel: x = xin + sum_{g < n_add} opart[g]; RMSNorm; gate/up + SwiGLU of 8 x 16 CTAs'
+// unit slices; split-K down_proj reduced per cluster into dpart[c][D] (c < dec1_parts()).
+// Cluster 0 writes x to xout.
+struct Dec1Mlp {
+    const float* xin;
+    const float* opart;  // [n_add][D]
+    int n_add;
+    float* xout;         // [D]
+    const bf16* w_post;
+    float eps;
+    const bf16* Wg;      // [I][D] of the layer
+    const bf16* Wu;      // [I][D]
+    const bf16* WdT;     // [I][D]: down_proj transposed
+    float* dpart;        // [dec1_parts()][D]
+    int I;
+    int* status;
+    int layer;
+    unsigned long long* trace;  // as Dec1Attn's, at trace[((2 layer + 1) * gridDim.x + c) * 8]
+};
+bool dec1_available(int D, int I, int QD, int n_heads, int n_kv);
+int dec1_max_keys();
+int dec1_parts();
+cudaError_t launch_dec1_attn(const LaunchCtx& c, const Dec1Attn& p);
+cudaError_t launch_dec1_mlp(const LaunchCtx& c, const Dec1Mlp& p);
+// out[i] = x[i] + sum_{c < n} part[c][i], i < D
+cudaError_t launch_dec1_sum(const LaunchCtx& c, const float* x, const float* part, int n, int D, float* out);
+// dst[z] = src[z] transposed ([rows][cols] -> [cols][rows]), z < batch
+cudaError_t launch_transpose_bf16(cudaStream_t st, const bf16* src, int rows, int cols, int batch, bf16* dst);
 cudaError_t launch_attn_paged(const LaunchCtx& c, int T, int layer, const f16* q, int n_heads,
                               int n_kv, TokView tv, KVView kv, int chunk, int n_splits,
                               float* part_o, float* part_ml, int* counters, f16* out,

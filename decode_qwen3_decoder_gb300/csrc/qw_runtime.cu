@@ -86,12 +86,19 @@ static bool config_ok(const qw_config* c, std::string* why) {
     return true;
 }
 
+// The batch-1 decode layer as two cluster kernels: shapes it serves (the device check is
+// dec1_available, at init).
+static bool dec1_shape(const qw_config& c) {
+    return c.hidden == 1024 && c.n_kv_heads <= 8 && (c.inter == 2048 || c.inter == 3072 || c.inter == 4096);
+}
+
 struct WsLayout {
     size_t wqkv, wo, wgu, wd, embed16, bqkv, bo, bg, bu, bd, norms, fnorm, rcos, rsin;
     size_t x, h, qkv, q, attn, act, part_o, part_ml, counters;
     size_t tok_seq, tok_pos, tok_slot, last, best, status, gen_tok, gen_cur, gen_out, mk_sync;
     size_t st_part, st_ss, st_xw, st_done, st_tick, st_abort;  // batched decode-step kernel
     size_t op_part;  // o_proj partials of the fused small-batch decode attention [n_kv][4][D]
+    size_t bdT, d1_y, d1_dpart;  // batch-1 cluster path: down_proj transposed, layer input x, partials
     size_t total;
     int part_T;
 };
@@ -151,6 +158,11 @@ static WsLayout layout_for(const qw_config& c) {
         L.st_abort = take(4);
     }
     L.op_part = take((size_t)c.n_kv_heads * 4 * D * 4);
+    if (dec1_shape(c)) {
+        L.bdT = take(NL * I * D * 2);
+        L.d1_y = take(D * 4);
+        L.d1_dpart = take((size_t)dec1_parts() * D * 4);
+    }
     L.gen_tok = take(T * 4);
     L.gen_cur = take((size_t)c.max_batch * 4);
     L.gen_out = take((size_t)c.max_batch * ((size_t)c.max_context + 1) * 4);
@@ -191,6 +203,10 @@ struct qw_model {
     int step_extra;    // test-only: extra arrivals its first o_proj unit waits for
     float *st_part, *st_ss;
     float* op_part;
+    bf16* bdT;          // [n_layers][inter][hidden]: down_proj transposed (batch-1 cluster path)
+    float *d1_y, *d1_dpart;
+    bool dec1_ok;       // the batch-1 cluster path fits this shape and device
+    bool use_dec1;      // QW_OPT_BATCH1_CLUSTERS
     f16* st_xw;
     int *st_done, *st_tick, *st_abort;
     StepMaps st_maps;
@@ -322,6 +338,9 @@ extern "C" qw_status qw_init_weights(const qw_config* cfg, const qw_weight_ptrs*
     m->st_part = (float*)(b + L.st_part);
     m->st_ss = (float*)(b + L.st_ss);
     m->op_part = (float*)(b + L.op_part);
+    m->bdT = L.bdT ? (bf16*)(b + L.bdT) : nullptr;
+    m->d1_y = L.d1_y ? (float*)(b + L.d1_y) : nullptr;
+    m->d1_dpart = L.d1_dpart ? (float*)(b + L.d1_dpart) : nullptr;
     m->st_xw = (f16*)(b + L.st_xw);
     m->st_done = (int*)(b + L.st_done);
     m->st_tick = (int*)(b + L.st_tick);
@@ -498,6 +517,12 @@ extern "C" qw_status qw_init_weights(const qw_config* cfg, const qw_weight_ptrs*
                      gemm_tc_encode_map(&m->st_maps.act, m->act, cfg->max_tokens, I, kStepMaxHalf);
     }
     m->use_step = false;  // opt in with QW_OPT_DECODE_STEP_KERNEL
+    m->dec1_ok = m->bdT && dec1_available((int)D, (int)I, (int)QD, cfg->n_heads, cfg->n_kv_heads);
+    if (m->dec1_ok && launch_transpose_bf16(st, m->bd, (int)D, (int)I, cfg->n_layers, m->bdT) != cudaSuccess) {
+        fail(QW_ERR_CUDA, "down_proj transpose failed");
+        return fail_free(QW_ERR_CUDA);
+    }
+    m->use_dec1 = m->dec1_ok;  // QW_OPT_BATCH1_CLUSTERS
     m->step_gp = std::max(1, std::min(64, m->num_sms / 2));
     m->step_wait_ns = 2000000000ull;
     m->step_extra = 0;
@@ -664,6 +689,10 @@ extern "C" qw_status qw_set_option(qw_model* m, int option, int value) {
         case QW_OPT_TEST_EXTRA_ARRIVALS:
             if (value < 0) return fail(QW_ERR_INVALID_ARG, "extra arrivals must be >= 0");
             m->step_extra = value;
+            return QW_OK;
+        case QW_OPT_BATCH1_CLUSTERS:
+            if (value && !m->dec1_ok) return fail(QW_ERR_UNSUPPORTED, "batch-1 cluster path unavailable for this shape or device");
+            m->use_dec1 = value != 0;
             return QW_OK;
         default:
             return fail(QW_ERR_INVALID_ARG, "unknown option %d", option);
@@ -898,6 +927,12 @@ static SplitPlan plan_splits(const qw_model* m, int T, int max_keys) {
     return {chunk, std::max(n, 1)};
 }
 
+// A decode step of one token (bf16 weights, short cache) runs each layer as two cluster
+// launches; the LM head then adds the last layer's down_proj partials to x.
+static bool dec1_step(const qw_model* m, const StepDesc& sd, bool prefill, int max_keys) {
+    return m->use_dec1 && !prefill && sd.T == 1 && m->qbits == 16 && max_keys <= dec1_max_keys();
+}
+
 // Token rows [t0, t0 + n) of a step through every layer, on stream st. The rows of a
 // decode step are independent sequences, so a batch can run as several such ranges on
 // different streams; every buffer is addressed at row t0 (the tensor-core operands through
@@ -938,6 +973,40 @@ static qw_status run_layers(qw_model* m, qw_kv* kv, const StepDesc& sd, bool pre
     int* counters = m->counters + (size_t)t0 * c.n_kv_heads;
     int32_t* dbg_pos = dbg ? m->dbg_pos + t0 : nullptr;
     int32_t* dbg_slot = dbg ? m->dbg_slot + t0 : nullptr;
+    if (dec1_step(m, sd, prefill, max_keys)) {
+        // x (m->x) -> [attention kernel: x + partials into d1_y, o_proj partials] -> [MLP
+        // kernel: d1_y + o_proj partials into m->x, down_proj partials] -> next layer
+        const int np = dec1_parts();
+        for (int l = 0; l < c.n_layers; ++l) {
+            const bf16* nb = m->norms + (size_t)l * (2 * D + 2 * d);
+            Dec1Attn a = {};
+            a.xin = m->x; a.dpart = m->d1_dpart; a.n_add = l == 0 ? 0 : np; a.xout = m->d1_y;
+            a.w_in = nb; a.eps = c.rms_eps; a.Wqkv = m->bqkv + (size_t)l * m->qkv_rows * D;
+            a.q_norm = nb + 2 * D; a.k_norm = nb + 2 * D + d; a.rope_cos = m->rcos; a.rope_sin = m->rsin;
+            a.kv = kvv; a.layer = l; a.seq = sd.seq[0]; a.pos = tv.pos;
+            a.Wo = m->bo + (size_t)l * D * QD; a.opart = m->op_part;
+            a.dbg_attn = (dbg && m->dbg_attn) ? m->dbg_attn + (size_t)l * QD : nullptr;
+            a.dbg_pos = l == 0 ? dbg_pos : nullptr; a.dbg_slot = l == 0 ? dbg_slot : nullptr;
+            a.status = m->status; a.n_kv = c.n_kv_heads; a.QD = QD; a.KD = c.n_kv_heads * d;
+            a.scale_log2 = 0.08838834764831845f * 1.4426950408889634f;  // 128^-0.5 * log2(e)
+            a.trace = m->trace;
+            {
+                PROF(QW_PROF_ATTN);
+                LAUNCH(launch_dec1_attn(lc, a));
+            }
+            Dec1Mlp f = {};
+            f.xin = m->d1_y; f.opart = m->op_part; f.n_add = c.n_kv_heads; f.xout = m->x;
+            f.w_post = nb + D; f.eps = c.rms_eps;
+            f.Wg = m->bg + (size_t)l * I * D; f.Wu = m->bu + (size_t)l * I * D; f.WdT = m->bdT + (size_t)l * I * D;
+            f.dpart = m->d1_dpart; f.I = I; f.status = m->status; f.layer = l; f.trace = m->trace;
+            {
+                PROF(QW_PROF_GATEUP);
+                LAUNCH(launch_dec1_mlp(lc, f));
+            }
+            if (dbg) LAUNCH(launch_dec1_sum(lc, m->x, m->d1_dpart, np, D, m->dbg_hidden + (size_t)l * D));
+        }
+        return QW_OK;
+    }
     for (int l = 0; l < c.n_layers; ++l) {
         const bf16* nb = m->norms + (size_t)l * (2 * D + 2 * d);
         const bf16* w_in = nb;
@@ -1194,8 +1263,10 @@ static qw_status run_step(qw_model* m, qw_kv* kv, const StepDesc& sd, bool prefi
     // products cost more than the tensor-core GEMM, which streams the head once for any B.
     if (B < kLmGemmMinRows) {
         PROF(QW_PROF_LMHEAD);
+        const bool d1 = !engine && dec1_step(m, sd, prefill, max_keys);  // x + the last down_proj partials
+        if (d1) lc.pdl = pdl_on;
         CUDA_TRY(launch_gemv_lmhead(lc, B, m->x, m->last, m->fnorm, c.rms_eps, m->embed, c.vocab, D, logits,
-                                    m->best));
+                                    m->best, d1 ? m->d1_dpart : nullptr, d1 ? dec1_parts() : 0));
     } else {
         {
             PROF(QW_PROF_RMSNORM);
@@ -1308,6 +1379,7 @@ extern "C" qw_status qw_decode_step(qw_model* m, qw_kv* kv, int B, const int* se
         key.push_back(m->use_step ? m->step_gp : 0);
         key.push_back((long long)m->step_wait_ns);
         key.push_back(m->step_extra);
+        key.push_back(m->use_dec1 ? 1 : 0);
         key.push_back(m->prof_kind || m->trace ? (long long)m->prof_gen : 0);
         for (int b = 0; b < B; ++b) key.push_back(seq_ids[b]);
         auto it = m->graphs.find(key);

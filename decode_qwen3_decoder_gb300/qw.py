@@ -280,6 +280,7 @@ QW_OPT_DECODE_STEP_KERNEL = 4
 QW_OPT_STEP_PROJ_CTAS = 5
 QW_OPT_TEST_WAIT_LIMIT_US = 6
 QW_OPT_TEST_EXTRA_ARRIVALS = 7
+QW_OPT_BATCH1_CLUSTERS = 8
 
 
 def qw_set_option(model: int, option: int, value: int) -> None:

@@ -278,7 +278,14 @@ enum {
     QW_OPT_TEST_WAIT_LIMIT_US = 6,
     /* Test only: the first o_proj unit of the decode-step kernel waits for this many arrivals
      * more than the attention provides (default 0), so that its wait runs out. */
-    QW_OPT_TEST_EXTRA_ARRIVALS = 7
+    QW_OPT_TEST_EXTRA_ARRIVALS = 7,
+    /* 1 (default where available: hidden 1024, inter 2048/3072/4096, n_kv_heads <= 8, and the
+     * device fits the 16-CTA clusters): a decode step of ONE token with bf16 weights over a
+     * cache of at most 128 keys runs each layer as two cluster launches -- (RMSNorm, q|k|v,
+     * QK-norm, RoPE, KV append, attention, o_proj) and (RMSNorm, gate/up, SwiGLU, down_proj),
+     * with the exchanges inside a layer through distributed shared memory; 0: the
+     * launch-per-phase path. Both compute the same operations; results agree within rounding. */
+    QW_OPT_BATCH1_CLUSTERS = 8
 };
 qw_status qw_set_option(qw_model* m, int option, int value);
 
@@ -287,7 +294,11 @@ qw_status qw_set_option(qw_model* m, int option, int value);
  * B_c = dev_buf + c * 8n of each CTA c: B_c[2k], B_c[2k+1] = arrival / release of grid
  * barrier k < n; B_c[2n + 2j], B_c[2n + 2j + 1] = start / end of the first consumer warp's
  * wait for weight stage j < 2n; B_c[6n + j] = when the producer issued stage j < 2n.
- * NULL turns it off. */
+ * Batch-1 decode steps on the cluster path (QW_OPT_BATCH1_CLUSTERS) write, for layer l, launch
+ * k (0: attention kernel, 1: MLP kernel) and CTA c < 128, eight values at
+ * dev_buf[((2l + k) * 128 + c) * 8]: entry, weights issued, dependency wait over, x staged,
+ * then three points of the kernel's phases, and exit (per_cta is not used; the buffer holds
+ * n_layers * 2048 values). NULL turns it off. */
 qw_status qw_trace_set(qw_model* m, unsigned long long* dev_buf, int per_cta);
 
 /* CTAs of the persistent decode kernel (one per SM), 0 if unavailable. */
