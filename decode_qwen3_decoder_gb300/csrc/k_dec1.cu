@@ -211,8 +211,8 @@ __device__ __forceinline__ float4 stage_norm(const float* xin, const float* part
 __global__ void __launch_bounds__(D1_THREADS, 2) k_dec1_attn(const __grid_constant__ Dec1Attn p) {
     extern __shared__ __align__(128) uint8_t d1_sm[];
     __shared__ float red[D1_WARPS];
-    __shared__ float so[D1_WARPS][2][128];
-    __shared__ float smm[D1_WARPS][2], sll[D1_WARPS][2];
+    __shared__ float so[D1_WARPS][128];  // per-warp partial output of its head
+    __shared__ float smm[D1_WARPS], sll[D1_WARPS];
     __shared__ __align__(8) uint64_t bar_g;  // the head's 512 gathered q|k|v values have landed
     pdl_launch();
     unsigned long long* tr = p.trace ? p.trace + ((size_t)2 * p.layer * gridDim.x + blockIdx.x) * 8 : nullptr;
@@ -356,19 +356,18 @@ __global__ void __launch_bounds__(D1_THREADS, 2) k_dec1_attn(const __grid_consta
     trace_at(tr, 4);
     if (bad && t == 0 && rank == 0) atomicOr(p.status, QW_DEV_BAD_POS);
 
-    // ---- online softmax over the cached keys [0, pos) (pages round-robin over the warps;
-    //      the page of the new position only below it) and, on warp 0, the new key
+    // ---- online softmax over the cached keys [0, pos): warp w serves head 2g + (w & 1) on
+    //      pages w/2, w/2 + 4 (the page of the new position only below it); the new key goes
+    //      to the warp of the head with the fewest pages
+    const int hh = warp & 1;
     const int half = lane >> 4, dl = (lane & 15) * 8;
-    float q0[8], q1[8];
+    float q[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        q0[i] = sq[0][dl + i] * p.scale_log2;
-        q1[i] = sq[1][dl + i] * p.scale_log2;
-    }
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f, o0[8], o1[8];
+    for (int i = 0; i < 8; ++i) q[i] = sq[hh][dl + i] * p.scale_log2;
+    float m = -INFINITY, l = 0.f, o[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) o0[i] = o1[i] = 0.f;
-    for (int pg = warp; pg < np && !bad; pg += D1_WARPS) {
+    for (int i = 0; i < 8; ++i) o[i] = 0.f;
+    for (int pg = warp >> 1; pg < np && !bad; pg += D1_WARPS / 2) {
         const int nvalid = min(16, pos - pg * 16);
         const uint8_t* kp = pg_s + (size_t)pg * 2 * D1_PAGE;
         uint4 kr[8], vr[8];
@@ -380,118 +379,84 @@ __global__ void __launch_bounds__(D1_THREADS, 2) k_dec1_attn(const __grid_consta
 #pragma unroll
         for (int i = 0; i < 8; ++i)
             if (2 * i + half >= nvalid) vr[i] = make_uint4(0u, 0u, 0u, 0u);
-        float s0[8], s1[8], pm0 = -INFINITY, pm1 = -INFINITY;
+        float sc[8], pm = -INFINITY;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const float d0 = half_sum(dot8h(q0, kr[i]));
-            const float d1 = half_sum(dot8h(q1, kr[i]));
-            const bool valid = (2 * i + half) < nvalid;
-            s0[i] = valid ? d0 : -INFINITY;
-            s1[i] = valid ? d1 : -INFINITY;
-            pm0 = fmaxf(pm0, s0[i]);
-            pm1 = fmaxf(pm1, s1[i]);
+            const float d = half_sum(dot8h(q, kr[i]));
+            sc[i] = (2 * i + half) < nvalid ? d : -INFINITY;
+            pm = fmaxf(pm, sc[i]);
         }
-        pm0 = fmaxf(pm0, __shfl_xor_sync(0xffffffffu, pm0, 16));
-        pm1 = fmaxf(pm1, __shfl_xor_sync(0xffffffffu, pm1, 16));
-        const float n0 = fmaxf(m0, pm0), n1 = fmaxf(m1, pm1);
-        if (n0 == -INFINITY) continue;
-        const float a0 = exp2f(m0 - n0), a1 = exp2f(m1 - n1);
-        m0 = n0;
-        m1 = n1;
-        l0 *= a0;
-        l1 *= a1;
+        pm = fmaxf(pm, __shfl_xor_sync(0xffffffffu, pm, 16));
+        const float n = fmaxf(m, pm);
+        if (n == -INFINITY) continue;
+        const float a = exp2f(m - n);
+        m = n;
+        l *= a;
 #pragma unroll
-        for (int d = 0; d < 8; ++d) {
-            o0[d] *= a0;
-            o1[d] *= a1;
-        }
+        for (int d = 0; d < 8; ++d) o[d] *= a;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            const float e0 = exp2f(s0[i] - m0), e1 = exp2f(s1[i] - m1);
-            l0 += e0;
-            l1 += e1;
+            const float e = exp2f(sc[i] - m);
+            l += e;
             const uint32_t vw[4] = {vr[i].x, vr[i].y, vr[i].z, vr[i].w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const float va = h_lo(vw[j]), vb = h_hi(vw[j]);
-                o0[2 * j] = fmaf(e0, va, o0[2 * j]);
-                o0[2 * j + 1] = fmaf(e0, vb, o0[2 * j + 1]);
-                o1[2 * j] = fmaf(e1, va, o1[2 * j]);
-                o1[2 * j + 1] = fmaf(e1, vb, o1[2 * j + 1]);
+                o[2 * j] = fmaf(e, h_lo(vw[j]), o[2 * j]);
+                o[2 * j + 1] = fmaf(e, h_hi(vw[j]), o[2 * j + 1]);
             }
         }
     }
     trace_at(tr, 5);
-    if (warp == 0) {
+    if (warp == hh + 2 * (np & 3)) {
         // the new key: both half-warps move the max, half 0 adds its weight
-        float d0 = 0.f, d1 = 0.f;
+        float d = 0.f;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            d0 = fmaf(q0[i], skv[0][dl + i], d0);
-            d1 = fmaf(q1[i], skv[0][dl + i], d1);
-        }
-        d0 = half_sum(d0);
-        d1 = half_sum(d1);
-        const float n0 = fmaxf(m0, d0), n1 = fmaxf(m1, d1);
-        const float a0 = exp2f(m0 - n0), a1 = exp2f(m1 - n1);
-        m0 = n0;
-        m1 = n1;
-        l0 *= a0;
-        l1 *= a1;
+        for (int i = 0; i < 8; ++i) d = fmaf(q[i], skv[0][dl + i], d);
+        d = half_sum(d);
+        const float n = fmaxf(m, d);
+        const float a = exp2f(m - n);
+        m = n;
+        l *= a;
 #pragma unroll
-        for (int d = 0; d < 8; ++d) {
-            o0[d] *= a0;
-            o1[d] *= a1;
-        }
+        for (int j = 0; j < 8; ++j) o[j] *= a;
         if (half == 0) {
-            const float e0 = exp2f(d0 - m0), e1 = exp2f(d1 - m1);
-            l0 += e0;
-            l1 += e1;
+            const float e = exp2f(d - m);
+            l += e;
 #pragma unroll
-            for (int d = 0; d < 8; ++d) {
-                o0[d] = fmaf(e0, skv[1][dl + d], o0[d]);
-                o1[d] = fmaf(e1, skv[1][dl + d], o1[d]);
-            }
+            for (int j = 0; j < 8; ++j) o[j] = fmaf(e, skv[1][dl + j], o[j]);
         }
     }
     trace_at(tr, 6);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 16);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 16);
+    l += __shfl_xor_sync(0xffffffffu, l, 16);
 #pragma unroll
-    for (int d = 0; d < 8; ++d) {
-        o0[d] += __shfl_xor_sync(0xffffffffu, o0[d], 16);
-        o1[d] += __shfl_xor_sync(0xffffffffu, o1[d], 16);
-    }
+    for (int d = 0; d < 8; ++d) o[d] += __shfl_xor_sync(0xffffffffu, o[d], 16);
     if (lane < 16) {
 #pragma unroll
-        for (int d = 0; d < 8; ++d) {
-            so[warp][0][dl + d] = o0[d];
-            so[warp][1][dl + d] = o1[d];
-        }
+        for (int d = 0; d < 8; ++d) so[warp][dl + d] = o[d];
     }
     if (lane == 0) {
-        smm[warp][0] = m0;
-        smm[warp][1] = m1;
-        sll[warp][0] = l0;
-        sll[warp][1] = l1;
+        smm[warp] = m;
+        sll[warp] = l;
     }
     __syncthreads();
     {
-        // thread -> (head hh, dimension d); warps without keys add nothing
-        const int hh = t >> 7, d = t & 127;
+        // thread -> (head h, dimension d) over the four warps of that head, in order; warps
+        // without keys add nothing
+        const int h = t >> 7, d = t & 127;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < D1_WARPS; ++w) M = fmaxf(M, smm[w][hh]);
+        for (int j = 0; j < 4; ++j) M = fmaxf(M, smm[h + 2 * j]);
         float L = 0.f, O = 0.f;
 #pragma unroll
-        for (int w = 0; w < D1_WARPS; ++w) {
-            const float f = smm[w][hh] == -INFINITY ? 0.f : exp2f(smm[w][hh] - M);
-            L += sll[w][hh] * f;
-            O += so[w][hh][d] * f;
+        for (int j = 0; j < 4; ++j) {
+            const int w = h + 2 * j;
+            const float f = smm[w] == -INFINITY ? 0.f : exp2f(smm[w] - M);
+            L += sll[w] * f;
+            O += so[w][d] * f;
         }
         const __half oh = __float2half_rn(O / L);  // the attention output as the unfused path stores it
-        ob[hh * 128 + d] = __half2float(oh);
-        if (p.dbg_attn && rank == 0) p.dbg_attn[(size_t)(2 * g + hh) * 128 + d] = oh;
+        ob[h * 128 + d] = __half2float(oh);
+        if (p.dbg_attn && rank == 0) p.dbg_attn[(size_t)(2 * g + h) * 128 + d] = oh;
     }
     __syncthreads();
     // ---- o_proj rows [64 rank, +64) over head g's 256 inputs -------------------------
