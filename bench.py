@@ -78,10 +78,10 @@ CONFIGS = {
 # DRAM bytes per launch of a kernel from one ncu capture (summaries under profiles/), reported
 # as roofline.traffic only while the kernel's source file is byte-identical to the capture's.
 NCU_TRAFFIC = {
-    (1, "gate_up+silu_mul(rmsnorm fused)"): (12606976, "decode_qwen3_decoder_gb300/csrc/k_small.cu",
-                                             "60ff501555a32c105747c8e175d3bbe27852b6a4931a769598a5ae541815842e"),
-    (1, "qkv_proj(rmsnorm fused)"): (8409344, "decode_qwen3_decoder_gb300/csrc/k_small.cu",
-                                     "60ff501555a32c105747c8e175d3bbe27852b6a4931a769598a5ae541815842e"),
+    # batch-1 cluster path: one launch captured in a 28-layer decode step (cache of ~7 keys;
+    # the K/V bytes of the bench's ~37-key caches add 0.15 MB per launch)
+    (1, "rmsnorm+qkv+attention+o_proj (cluster kernel)"): (12770816, "decode_qwen3_decoder_gb300/csrc/k_dec1.cu",
+                                                           "7e1fe5802acbcb219dd291bfb310820b3641150a1aa55a60f154ed4a087c5744"),
     (3, "gate_up+silu_mul"): (29395200 + 668160, "decode_qwen3_decoder_gb300/csrc/k_gemm.cu",
                               "ac14bf4a7fabf4ebcb03ecc75dc46125c104e7ad15728ab9ed1e163b507579cc"),
     (3, "qkv_proj+qk_norm+rope+kv_append"): (25560832 + 10699520, "decode_qwen3_decoder_gb300/csrc/k_gemm.cu",

@@ -522,7 +522,9 @@ extern "C" qw_status qw_init_weights(const qw_config* cfg, const qw_weight_ptrs*
         fail(QW_ERR_CUDA, "down_proj transpose failed");
         return fail_free(QW_ERR_CUDA);
     }
-    m->use_dec1 = m->dec1_ok;  // QW_OPT_BATCH1_CLUSTERS
+    // QW_OPT_BATCH1_CLUSTERS: on by default for stacks of layers, where each kernel's weight
+    // fetch overlaps the previous kernel (one layer measured faster on the per-phase path)
+    m->use_dec1 = m->dec1_ok && cfg->n_layers > 1;
     m->step_gp = std::max(1, std::min(64, m->num_sms / 2));
     m->step_wait_ns = 2000000000ull;
     m->step_extra = 0;
