@@ -241,8 +241,7 @@ CLUSTER_KIND_NAMES = {3: "rmsnorm+qkv+attention+o_proj (cluster kernel)",
                       5: "rmsnorm+gate_up+swiglu+down_proj (cluster kernel)", 7: "lm_head+argmax"}
 KIND_NAMES = {1: "qkv_proj(rmsnorm fused)", 2: "qknorm_rope_append", 3: "attention(+o_proj fused at B=1)",
               4: "o_proj+residual",
-              5: "gate_up+silu_mul(rmsnorm fused)", 6: "down_proj+residual", 7: "lm_head+argmax",
-              9: "k_decode_mk (persistent decode step)"}
+              5: "gate_up+silu_mul(rmsnorm fused)", 6: "down_proj+residual", 7: "lm_head+argmax"}
 # names on the tensor-core path (more than 8 token rows)
 TC_KIND_NAMES = {1: "qkv_proj+qk_norm+rope+kv_append", 3: "attention", 4: "o_proj+residual",
                  5: "gate_up+silu_mul", 6: "down_proj+residual", 7: "lm_head+argmax", 8: "rmsnorm"}
@@ -289,8 +288,6 @@ def run_ours(args, cfg, rank, world):
     eng = qw.Engine(s, model_weights(s), max_tokens=max(B * P, 8), max_batch=max(B, 8), max_context=max_ctx,
                     kv_pages=B * ((max_ctx + 15) // 16) + 8, max_seqs=max(B, 8))
     st = eng.stream
-    if args.persistent:
-        qw.qw_set_option(eng.model, qw.QW_OPT_PERSISTENT_DECODE, 1)
     seqs = list(range(B))
     prompt = synth.make_tokens(s.vocab, B * P, rank_token_seed(cfg["id"], rank))
     d_prompt = torch.tensor(prompt, dtype=torch.int32, device="cuda")
@@ -358,13 +355,11 @@ def run_ours(args, cfg, rank, world):
     # (events bracket the launches inside the captured decode graphs; measured on the
     # same workload right after the timed region)
     hbm, bf16_burst, bf16_sust, peak_src = peaks()
-    persistent = args.persistent and B <= 4
     # one token per step: two cluster kernels per layer (step begin + 2 per layer + LM head +
     # finalize), else attention and o_proj as one kernel (kind 3)
-    clusters = not persistent and B == 1 and step_launches == 2 * s.n_layers + 3
+    clusters = B == 1 and step_launches == 2 * s.n_layers + 3
     names = CLUSTER_KIND_NAMES if clusters else KIND_NAMES
-    n_launch_per_step = ({9: 1} if persistent else
-                         {3: s.n_layers, 5: s.n_layers, 7: 1} if clusters else
+    n_launch_per_step = ({3: s.n_layers, 5: s.n_layers, 7: 1} if clusters else
                          {1: s.n_layers, 3: s.n_layers, 5: s.n_layers, 6: s.n_layers, 7: 1} if B == 1 else
                          {1: s.n_layers, 4: s.n_layers, 5: s.n_layers, 6: s.n_layers, 7: 1})
     kinds = {}
@@ -388,8 +383,7 @@ def run_ours(args, cfg, rank, world):
         qw.qw_profile_set(eng.model, 0, None, 0)
         st.synchronize()
         avg_us = statistics.mean(durs) * 1e3
-        nbytes = (step_bytes(s, B, statistics.mean(ctxs)) if kind == 9 else
-                  kernel_bytes(kind, s, B, B, statistics.mean(ctxs), clusters))
+        nbytes = kernel_bytes(kind, s, B, B, statistics.mean(ctxs), clusters)
         kinds[kind] = dict(name=names[kind], launches_per_step=nl, avg_us=avg_us,
                            total_us_per_step=avg_us * nl, bytes=nbytes)
     dom = max(kinds, key=lambda k: kinds[k]["total_us_per_step"])
@@ -985,8 +979,6 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=None, choices=[0, 1, 2, 3, 4],
                     help="run one workload alone (default: all five, the B=1 generation as headline)")
-    ap.add_argument("--persistent", action="store_true",
-                    help="decode steps of <= 4 sequences as one persistent kernel")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--prompt-len", type=int, default=0,
                     help="with --config 2/3: tokens per sequence instead of the configured length (smaller case "

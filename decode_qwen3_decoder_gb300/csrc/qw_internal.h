@@ -416,49 +416,3 @@ struct StepMaps {
 };
 cudaError_t launch_decode_step(cudaStream_t st, const StepKParams& p, const StepMaps& maps, int grid);
 
-// Persistent decode kernel (k_mk.cu): one cooperative launch per decode step of <= 8 tokens.
-struct MkParams {
-    // model
-    const bf16* wqkv;  // bf16 packed weights
-    const bf16* wo;
-    const bf16* wg;
-    const bf16* wu;
-    const bf16* wd;
-    const bf16* embed;
-    const bf16* norms;  // per layer [in D][post D][q_norm 128][k_norm 128]
-    const bf16* fnorm;
-    const float* rcos;
-    const float* rsin;
-    int n_layers, D, I, QD, QKV, V, n_heads, n_kv;
-    float eps;
-    float scale_log2;
-    // step
-    int T;
-    int seq[8];
-    const int32_t* ids;
-    int32_t* next_ids;
-    float* logits;
-    KVView kv;
-    int chunk, n_splits;
-    // workspace
-    float* x;
-    float* qkv;
-    f16* o;
-    f16* act;
-    float* part_o;
-    float* part_ml;
-    int* counters;
-    unsigned long long* best;
-    int* status;
-    unsigned* sync;  // [0] arrivals, [1] generation, [2] LM-head ticket
-    int* abort_g;
-    float* dbg_hidden;
-    int32_t* dbg_pos;
-    int32_t* dbg_slot;
-    unsigned long long* trace;  // optional: [grid][trace_n][2] barrier arrival / release times
-    int trace_n;
-};
-int mk_smem_bytes();
-int mk_max_tokens(int D, int I, int QD);
-int mk_grid_size();
-cudaError_t launch_decode_mk(const LaunchCtx& c, const MkParams& p, int grid);

@@ -95,7 +95,7 @@ static bool dec1_shape(const qw_config& c) {
 struct WsLayout {
     size_t wqkv, wo, wgu, wd, embed16, bqkv, bo, bg, bu, bd, norms, fnorm, rcos, rsin;
     size_t x, h, qkv, q, attn, act, part_o, part_ml, counters;
-    size_t tok_seq, tok_pos, tok_slot, last, best, status, gen_tok, gen_cur, gen_out, mk_sync;
+    size_t tok_seq, tok_pos, tok_slot, last, best, status, gen_tok, gen_cur, gen_out;
     size_t st_part, st_ss, st_xw, st_done, st_tick, st_abort;  // batched decode-step kernel
     size_t op_part;  // o_proj partials of the fused small-batch decode attention [n_kv][4][D]
     size_t bdT, d1_y, d1_dpart;  // batch-1 cluster path: down_proj transposed, layer input x, partials
@@ -145,7 +145,6 @@ static WsLayout layout_for(const qw_config& c) {
     L.last = take((size_t)c.max_batch * 4);
     L.best = take((size_t)c.max_batch * 8);
     L.status = take(4);
-    L.mk_sync = take(16);  // persistent decode kernel: arrivals, generation, ticket, abort
     {
         // batched decode-step kernel: split-K partials, per-block sums of squares of x,
         // completion counters and arrival tickets (adjacent: one memset clears both), abort word
@@ -191,10 +190,6 @@ struct qw_model {
     float *rcos, *rsin, *x, *qkv, *part_o, *part_ml;
     f16 *h, *q, *attn, *act;
     int *counters, *tok_seq, *tok_pos, *tok_slot, *last, *status;
-    unsigned* mk_sync;
-    int mk_grid;       // CTAs of the persistent decode kernel (0: not available)
-    int mk_max_t;      // most tokens it takes
-    bool use_mk;       // decode steps of <= mk_max_t tokens run as one persistent kernel
     // batched decode-step kernel (decode steps of 16 .. 2 * kStepMaxHalf tokens)
     bool step_ok;      // shape supported and one CTA per SM can be resident
     bool use_step;     // QW_OPT_DECODE_STEP_KERNEL
@@ -334,7 +329,6 @@ extern "C" qw_status qw_init_weights(const qw_config* cfg, const qw_weight_ptrs*
     m->last = (int*)(b + L.last);
     m->best = (unsigned long long*)(b + L.best);
     m->status = (int*)(b + L.status);
-    m->mk_sync = (unsigned*)(b + L.mk_sync);
     m->st_part = (float*)(b + L.st_part);
     m->st_ss = (float*)(b + L.st_ss);
     m->op_part = (float*)(b + L.op_part);
@@ -452,8 +446,7 @@ extern "C" qw_status qw_init_weights(const qw_config* cfg, const qw_weight_ptrs*
         }
     }
     if (cudaMemsetAsync(m->counters, 0, (size_t)L.part_T * cfg->n_kv_heads * 4, st) != cudaSuccess ||
-        cudaMemsetAsync(m->best, 0, (size_t)cfg->max_batch * 8, st) != cudaSuccess ||
-        cudaMemsetAsync(m->mk_sync, 0, 16, st) != cudaSuccess) {
+        cudaMemsetAsync(m->best, 0, (size_t)cfg->max_batch * 8, st) != cudaSuccess) {
         fail(QW_ERR_CUDA, "workspace clear failed");
         return fail_free(QW_ERR_CUDA);
     }
@@ -501,9 +494,6 @@ extern "C" qw_status qw_init_weights(const qw_config* cfg, const qw_weight_ptrs*
     m->prof_gen = 0;
     m->trace = nullptr;
     m->trace_n = 0;
-    m->mk_grid = mk_grid_size();
-    m->mk_max_t = m->mk_grid > 0 ? std::min(mk_max_tokens(cfg->hidden, cfg->inter, cfg->n_heads * cfg->head_dim), 8) : 0;
-    m->use_mk = false;  // opt in with QW_OPT_PERSISTENT_DECODE
     m->step_ok = step_shape_ok((int)D, (int)I, (int)QD, m->qkv_rows, cfg->n_heads, cfg->n_kv_heads) &&
                  step_blocks_per_sm() >= 1 &&
                  m->num_sms >= 16;
@@ -627,7 +617,6 @@ extern "C" qw_status qw_quantize_weights(qw_model* m, int bits, void* dev_buf, s
     if (!m) return fail(QW_ERR_INVALID_ARG, "model is NULL");
     if (bits != 8 && bits != 4) return fail(QW_ERR_INVALID_ARG, "bits must be 8 or 4");
     if (m->qbits != 16) return fail(QW_ERR_BAD_STATE, "the weights are already quantized");
-    if (m->use_mk) return fail(QW_ERR_BAD_STATE, "the persistent decode kernel reads bf16 weights; turn it off first");
     const qw_config& c = m->cfg;
     const int QD = c.n_heads * c.head_dim;
     if (c.hidden != 1024 || (QD != 2048 && QD != 3072) || (c.inter != 2048 && c.inter != 3072))
@@ -660,16 +649,10 @@ extern "C" qw_status qw_trace_set(qw_model* m, unsigned long long* dev_buf, int 
     return QW_OK;
 }
 
-extern "C" int qw_persistent_grid(const qw_model* m) { return m ? m->mk_grid : 0; }
 
 extern "C" qw_status qw_set_option(qw_model* m, int option, int value) {
     if (!m) return fail(QW_ERR_INVALID_ARG, "model is NULL");
     switch (option) {
-        case QW_OPT_PERSISTENT_DECODE:
-            if (value && m->mk_max_t == 0) return fail(QW_ERR_UNSUPPORTED, "persistent decode kernel unavailable");
-            if (value && m->qbits != 16) return fail(QW_ERR_UNSUPPORTED, "the persistent decode kernel reads bf16 weights");
-            m->use_mk = value != 0;
-            return QW_OK;
         case QW_OPT_PDL:
             m->pdl = value != 0;
             return QW_OK;
@@ -1156,42 +1139,6 @@ static qw_status run_step(qw_model* m, qw_kv* kv, const StepDesc& sd, bool prefi
     if (!small && !prefill && T > m->L.part_T) return fail(QW_ERR_UNSUPPORTED, "decode batch beyond partial buffers");
 
     int pc[16] = {0};
-    if (!prefill && m->use_mk && T <= m->mk_max_t) {
-        // one cooperative launch for the whole decode step
-        const int units_teams = 3 * m->mk_grid;
-        const int pairs = T * c.n_kv_heads;
-        int want = std::max(1, std::min((units_teams + pairs - 1) / pairs, kMaxSplits));
-        int chunk = std::max(64, ((max_keys + want - 1) / want + 15) / 16 * 16);
-        int nspl = (max_keys + chunk - 1) / chunk;
-        while (nspl > kMaxSplits) {
-            chunk += 16;
-            nspl = (max_keys + chunk - 1) / chunk;
-        }
-        MkParams mp = {};
-        mp.wqkv = m->bqkv; mp.wo = m->bo; mp.wg = m->bg; mp.wu = m->bu; mp.wd = m->bd;
-        mp.embed = m->embed; mp.norms = m->norms; mp.fnorm = m->fnorm;
-        mp.rcos = m->rcos; mp.rsin = m->rsin;
-        mp.n_layers = c.n_layers; mp.D = D; mp.I = I; mp.QD = QD; mp.QKV = m->qkv_rows; mp.V = c.vocab;
-        mp.n_heads = c.n_heads; mp.n_kv = c.n_kv_heads; mp.eps = c.rms_eps;
-        mp.scale_log2 = 0.08838834764831845f * 1.4426950408889634f;
-        mp.T = T;
-        for (int b = 0; b < T; ++b) mp.seq[b] = sd.seq[b];
-        mp.ids = tokens; mp.next_ids = next; mp.logits = logits;
-        mp.kv = kvv; mp.chunk = chunk; mp.n_splits = std::max(nspl, 1);
-        mp.x = m->x; mp.qkv = m->qkv; mp.o = m->attn; mp.act = m->act;
-        mp.part_o = m->part_o; mp.part_ml = m->part_ml; mp.counters = m->counters; mp.best = m->best;
-        mp.status = m->status; mp.sync = m->mk_sync; mp.abort_g = (int*)(m->mk_sync + 3);
-        mp.dbg_hidden = dbg ? m->dbg_hidden : nullptr;
-        mp.dbg_pos = dbg ? m->dbg_pos : nullptr;
-        mp.dbg_slot = dbg ? m->dbg_slot : nullptr;
-        mp.trace = m->trace;
-        mp.trace_n = m->trace_n;
-        int pc0[16] = {0};
-        ProfScope prof_scope_(m, QW_PROF_STEP, pc0, st);
-        LaunchCtx lc1 = {st, false, launches};
-        CUDA_TRY(launch_decode_mk(lc1, mp, m->mk_grid));
-        return QW_OK;
-    }
     // The first kernel of a step waits for everything before it (no programmatic overlap), so
     // kernels of this step may read state written by earlier steps before their own wait.
     const LaunchCtx lc0 = {st, false, launches};
@@ -1375,7 +1322,6 @@ extern "C" qw_status qw_decode_step(qw_model* m, qw_kv* kv, int B, const int* se
         key.push_back((long long)(uintptr_t)kv);
         key.push_back(sp.chunk);
         key.push_back(m->prof_kind);
-        key.push_back(m->use_mk ? 1 : 0);
         key.push_back(m->pdl ? 1 : 0);
         key.push_back(m->split_decode ? 1 : 0);
         key.push_back(m->use_step ? m->step_gp : 0);
@@ -1512,7 +1458,6 @@ extern "C" qw_status qw_sync_status(qw_model* m, void* stream_) {
     int word = 0;
     CUDA_TRY(cudaMemcpy(&word, m->status, 4, cudaMemcpyDeviceToHost));
     CUDA_TRY(cudaMemset(m->status, 0, 4));
-    CUDA_TRY(cudaMemset(m->mk_sync, 0, 16));
     CUDA_TRY(cudaMemset(m->st_abort, 0, 4));
     if (word & QW_DEV_TIMEOUT) {
         // a kernel that gave up may have left arrival tickets behind

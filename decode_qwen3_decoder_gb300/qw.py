@@ -86,7 +86,6 @@ SIGNATURES = {
     "qw_profile_set": (_I, [_VP, _I, _P(_VP), _I]),
     "qw_set_option": (_I, [_VP, _I, _I]),
     "qw_trace_set": (_I, [_VP, _VP, _I]),
-    "qw_persistent_grid": (_I, [_VP]),
     "qw_lm_head_argmax_noalloc": (_I, [_VP, _I, _VP, _VP, _VP, _VP]),
 }
 
@@ -273,7 +272,6 @@ def qw_lm_head_argmax_noalloc(model: int, B: int, x_ptr: int, logits_ptr: int, n
     _check(load().qw_lm_head_argmax_noalloc(model, B, x_ptr, logits_ptr or None, next_ptr, _stream(stream)))
 
 
-QW_OPT_PERSISTENT_DECODE = 1
 QW_OPT_PDL = 2
 QW_OPT_SPLIT_DECODE = 3
 QW_OPT_DECODE_STEP_KERNEL = 4
@@ -289,10 +287,6 @@ def qw_set_option(model: int, option: int, value: int) -> None:
 
 def qw_trace_set(model: int, buf_ptr: int, per_cta: int) -> None:
     _check(load().qw_trace_set(model, buf_ptr or None, per_cta))
-
-
-def qw_persistent_grid(model: int) -> int:
-    return load().qw_persistent_grid(model)
 
 
 def qw_profile_set(model: int, kind: int, events, n_events: int) -> None:

@@ -209,9 +209,8 @@ void qw_free_kv(qw_kv* kv);
  * not graph-captured. */
 qw_status qw_debug_set(qw_model* m, float* dev_hidden, int32_t* dev_positions, int32_t* dev_slots);
 
-/* While qw_debug_set is on and dev_attn is non-NULL, prefill calls and decode calls that run
- * layer by layer (more than the persistent decode kernel's batch) also copy each layer's
- * attention output, the input of o_proj, to dev_attn[layer][t][n_heads * head_dim] (fp16,
+/* While qw_debug_set is on and dev_attn is non-NULL, prefill and decode calls also copy each
+ * layer's attention output, the input of o_proj, to dev_attn[layer][t][n_heads * head_dim] (fp16,
  * t < that call's token count). NULL turns it off. */
 qw_status qw_debug_set_attn(qw_model* m, void* dev_attn);
 
@@ -246,15 +245,12 @@ enum {
     QW_PROF_DOWN = 6,     /* down_proj + residual                                         */
     QW_PROF_LMHEAD = 7,   /* final norm + tied LM head + argmax                           */
     QW_PROF_RMSNORM = 8,  /* stand-alone RMSNorm (tensor-core path)                       */
-    QW_PROF_STEP = 9      /* the persistent decode kernel (a whole decode step)           */
+    QW_PROF_STEP = 9      /* the decode-step kernel (every layer of a decode step)         */
 };
 
 /* Options for qw_set_option. */
 enum {
-    /* 1: decode steps of <= 4 tokens run as one persistent cooperative kernel (needs one
-     * 416-thread CTA per SM); 0 (default): as one launch per layer phase. Both compute the
-     * same operations. */
-    QW_OPT_PERSISTENT_DECODE = 1,
+    /* (option 1 is not used) */
     /* 1 (default): consecutive launches use programmatic dependent launch. */
     QW_OPT_PDL = 2,
     /* 1 (default): a decode step of >= 16 sequences runs as two halves on two streams whose
@@ -290,20 +286,15 @@ enum {
 };
 qw_status qw_set_option(qw_model* m, int option, int value);
 
-/* Inspection of the persistent decode kernel: when dev_buf is non-NULL (per_cta = n), every
- * following persistent decode step writes %globaltimer values (ns, uint64) into the block
- * B_c = dev_buf + c * 8n of each CTA c: B_c[2k], B_c[2k+1] = arrival / release of grid
- * barrier k < n; B_c[2n + 2j], B_c[2n + 2j + 1] = start / end of the first consumer warp's
- * wait for weight stage j < 2n; B_c[6n + j] = when the producer issued stage j < 2n.
+/* Inspection (%globaltimer values, ns, uint64) while dev_buf is non-NULL; NULL turns it off.
+ * Decode-step kernel (QW_OPT_DECODE_STEP_KERNEL): CTA c writes up to per_cta records of 8
+ * values at dev_buf[(c * per_cta + k) * 8] (record id, then its phase times).
  * Batch-1 decode steps on the cluster path (QW_OPT_BATCH1_CLUSTERS) write, for layer l, launch
  * k (0: attention kernel, 1: MLP kernel) and CTA c < 128, eight values at
  * dev_buf[((2l + k) * 128 + c) * 8]: entry, weights issued, dependency wait over, x staged,
  * then three points of the kernel's phases, and exit (per_cta is not used; the buffer holds
  * n_layers * 2048 values). NULL turns it off. */
 qw_status qw_trace_set(qw_model* m, unsigned long long* dev_buf, int per_cta);
-
-/* CTAs of the persistent decode kernel (one per SM), 0 if unavailable. */
-int qw_persistent_grid(const qw_model* m);
 
 /* Bracket the j-th launch of kernel kind `kind` in every following prefill/decode call with
  * cudaEventRecord(events[2j]) before and cudaEventRecord(events[2j+1]) after it, on the
@@ -328,7 +319,7 @@ size_t qw_quantize_bytes(const qw_model* m, int bits);
  * the tensor-core paths use the dequantized weights (written over the model's fp16 copies),
  * so every call computes with the same quantized model. Irreversible for this model handle.
  * Asynchronous on `stream`. Errors: QW_ERR_INVALID_ARG (bits, buffer), QW_ERR_BAD_STATE
- * (already quantized, or the persistent decode kernel is on), QW_ERR_UNSUPPORTED (a shape
+ * (already quantized), QW_ERR_UNSUPPORTED (a shape
  * other than hidden 1024 with o_proj / down_proj inputs of 2048 or 3072). */
 qw_status qw_quantize_weights(qw_model* m, int bits, void* dev_buf, size_t bytes, void* stream);
 

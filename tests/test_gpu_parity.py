@@ -241,31 +241,6 @@ def test_config1_greedy_28_layers(full_model):
     assert n >= 32
 
 
-def test_persistent_decode_matches_per_phase_launches(one_block):
-    """Decode steps as one persistent kernel and as one launch per phase agree."""
-    run, _ = one_block
-    qw, eng = run.qw, run.eng
-    seqs = [1, 4, 6]
-    prompts = [synth.make_tokens(synth.ONE_BLOCK.vocab, n, 60 + n).tolist() for n in (3, 9, 17)]
-    forced = synth.make_tokens(synth.ONE_BLOCK.vocab, 9, 61).reshape(3, 3)
-    outs = []
-    for mk in (1, 0):
-        qw.qw_set_option(eng.model, qw.QW_OPT_PERSISTENT_DECODE, mk)
-        qw.qw_kv_reset(eng.kv, -1, eng.stream)
-        run.prefill(seqs, prompts, debug=False, reserve_extra=4)
-        steps = []
-        for i in range(3):
-            d = run.decode(seqs, forced[i].tolist(), debug=(i == 1))
-            assert d["status"] == 0
-            steps.append((d["logits"], d["next"], d.get("hidden")))
-        outs.append(steps)
-    qw.qw_set_option(eng.model, qw.QW_OPT_PERSISTENT_DECODE, 1)
-    for (la, na, ha), (lb, nb, hb) in zip(*outs):
-        assert np.max(np.abs(la - lb)) < 1e-2
-        if ha is not None:
-            check_hidden(ha, hb, tol=1e-3)
-
-
 @pytest.fixture(scope="module")
 def one_block_long(qw):
     eng = engine(qw, synth.ONE_BLOCK, max_tokens=64, max_batch=8, max_context=8192, kv_pages=1300,
