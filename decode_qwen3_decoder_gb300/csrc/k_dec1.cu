@@ -69,11 +69,14 @@ constexpr int mlp_smem() {
 }
 
 __device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-__device__ __forceinline__ void cp16(void* dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(su32(dst)), "l"(src) : "memory");
+// Bulk copy (TMA engine, not the SM's load/store pipeline) of `bytes` (a multiple of 16, both
+// addresses 16-byte aligned) into shared memory, completing on a local mbarrier.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     su32(dst)),
+                 "l"(src), "r"(bytes), "r"(su32(bar))
+                 : "memory");
 }
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -214,6 +217,8 @@ __global__ void __launch_bounds__(D1_THREADS, 2) k_dec1_attn(const __grid_consta
     __shared__ float so[D1_WARPS][128];  // per-warp partial output of its head
     __shared__ float smm[D1_WARPS], sll[D1_WARPS];
     __shared__ __align__(8) uint64_t bar_g;  // the head's 512 gathered q|k|v values have landed
+    __shared__ __align__(8) uint64_t bar_w;  // the o_proj slice and the cached pages have landed
+    __shared__ int s_np, s_bad;
     pdl_launch();
     unsigned long long* tr = p.trace ? p.trace + ((size_t)2 * p.layer * gridDim.x + blockIdx.x) * 8 : nullptr;
     trace_at(tr, 0);
@@ -233,26 +238,33 @@ __global__ void __launch_bounds__(D1_THREADS, 2) k_dec1_attn(const __grid_consta
     const int* pt = p.kv.page_table + (size_t)p.seq * p.kv.max_pages_per_seq;
 
     // ---- before the wait --------------------------------------------------------------
-    // o_proj rows [64 rank, +64), inputs [256 g, +256): 64 rows x 32 chunks of 16 bytes
-    for (int i = t; i < D1_ROWS_O * 32; i += D1_THREADS) {
-        const int r = i >> 5, c = i & 31;
-        cp16(wo_s + r * 256 + c * 8, p.Wo + (size_t)(D1_ROWS_O * rank + r) * p.QD + 256 * g + c * 8);
-    }
-    // the cached pages of head g (length and page table were set before the step began)
-    const int cached = p.kv.len[p.seq];
-    const int np = min((cached + 15) >> 4, D1_MAXPG);
-    int bad = 0;
-    for (int i = t; i < np * 512; i += D1_THREADS) {
-        const int pi = i >> 9, w = i & 511;  // w < 256: a 16-byte chunk of K, else of V
-        int page = pt[pi];
-        if (page < 0 || page >= p.kv.n_pages) {
-            bad = 1;  // no copy from outside the pool; the attention is skipped and reported
-            page = 0;
+    // one thread issues the bulk copies: the o_proj rows [64 rank, +64) over inputs
+    // [256 g, +256) (64 rows of 512 bytes) and the cached K/V pages of head g (the length and
+    // page table were set before the step began)
+    if (t == 0) {
+        const int cached = p.kv.len[p.seq];
+        const int np = min((cached + 15) >> 4, D1_MAXPG);
+        mbar_init_tx(&bar_w, (uint32_t)(D1_ROWS_O * 512 + np * 2 * D1_PAGE));
+        for (int r = 0; r < D1_ROWS_O; ++r)
+            bulk_g2s(wo_s + r * 256, p.Wo + (size_t)(D1_ROWS_O * rank + r) * p.QD + 256 * g, 512, &bar_w);
+        int bad = 0, pages[D1_MAXPG];
+#pragma unroll
+        for (int pi = 0; pi < D1_MAXPG; ++pi) pages[pi] = pi < np ? pt[pi] : 0;  // loads in flight together
+#pragma unroll
+        for (int pi = 0; pi < D1_MAXPG; ++pi) {
+            if (pi >= np) break;
+            int page = pages[pi];
+            if (page < 0 || page >= p.kv.n_pages) {
+                bad = 1;  // no copy from outside the pool; the attention is skipped and reported
+                page = 0;
+            }
+            const size_t off = ((size_t)page * p.n_kv + g) * 16 * 128;
+            bulk_g2s(pg_s + pi * 2 * D1_PAGE, Kl + off, D1_PAGE, &bar_w);
+            bulk_g2s(pg_s + pi * 2 * D1_PAGE + D1_PAGE, Vl + off, D1_PAGE, &bar_w);
         }
-        const size_t off = ((size_t)page * p.n_kv + g) * 16 * 128 + (size_t)(w & 255) * 8;
-        cp16(pg_s + pi * 2 * D1_PAGE + (w >> 8) * D1_PAGE + (w & 255) * 16, ((w >> 8) ? Vl : Kl) + off);
+        s_np = np;
+        s_bad = bad;
     }
-    cp_commit();
     // q|k|v rows of head g held by this CTA: local rows [32 rank, +32) of the head's 512
     // (q of heads 2g, 2g+1 = rows 0..255, then k = 256..383, then v = 384..511)
     uint4 wq[4][4];
@@ -351,8 +363,9 @@ __global__ void __launch_bounds__(D1_THREADS, 2) k_dec1_attn(const __grid_consta
             }
         }
     }
-    cp_wait_all();
-    bad = __syncthreads_or(bad);
+    if (!mbar_wait0(&bar_w) && t == 0) atomicOr(p.status, QW_DEV_TIMEOUT);
+    __syncthreads();
+    const int np = s_np, bad = s_bad;
     trace_at(tr, 4);
     if (bad && t == 0 && rank == 0) atomicOr(p.status, QW_DEV_BAD_POS);
 
@@ -487,6 +500,7 @@ __global__ void __launch_bounds__(D1_THREADS, 2) k_dec1_mlp(const __grid_constan
     __shared__ float red[D1_WARPS];
     __shared__ float sact[NA];
     __shared__ __align__(8) uint64_t bar_r;  // all 8 partial slices have landed
+    __shared__ __align__(8) uint64_t bar_w;  // the shared-memory weight rows have landed
     pdl_launch();
     unsigned long long* tr = p.trace ? p.trace + ((size_t)(2 * p.layer + 1) * gridDim.x + blockIdx.x) * 8 : nullptr;
     trace_at(tr, 0);
@@ -495,16 +509,13 @@ __global__ void __launch_bounds__(D1_THREADS, 2) k_dec1_mlp(const __grid_constan
     const int a0 = (c * D1_CLM + rank) * NA;  // first intermediate unit of this CTA
 
     // ---- before the wait: weights ----------------------------------------------------
-    for (int i = t; i < 2 * NS * 128; i += D1_THREADS) {
-        const int r = i >> 7, ch = i & 127;
-        const bf16* src = (r < NS ? p.Wg : p.Wu) + (size_t)(a0 + 16 + (NS > 0 ? r % NS : 0)) * D1_D + ch * 8;
-        cp16(gu_s + r * D1_D + ch * 8, src);
+    if (t == 0) {  // one thread issues the bulk copies of the rows kept in shared memory
+        mbar_init_tx(&bar_w, (uint32_t)((2 * NS + NA) * D1_D * 2));
+        for (int r = 0; r < 2 * NS; ++r)
+            bulk_g2s(gu_s + r * D1_D, (r < NS ? p.Wg : p.Wu) + (size_t)(a0 + 16 + (NS > 0 ? r % NS : 0)) * D1_D,
+                     D1_D * 2, &bar_w);
+        for (int r = 0; r < NA; ++r) bulk_g2s(wd_s + r * D1_D, p.WdT + (size_t)(a0 + r) * D1_D, D1_D * 2, &bar_w);
     }
-    for (int i = t; i < NA * 128; i += D1_THREADS) {
-        const int r = i >> 7, ch = i & 127;
-        cp16(wd_s + r * D1_D + ch * 8, p.WdT + (size_t)(a0 + r) * D1_D + ch * 8);
-    }
-    cp_commit();
     // registers: gate rows a0 + 2w, a0 + 2w + 1 and the same up rows
     uint4 wr[4][4];
 #pragma unroll
@@ -524,7 +535,7 @@ __global__ void __launch_bounds__(D1_THREADS, 2) k_dec1_mlp(const __grid_constan
     const float4 xv = stage_norm(p.xin, p.opart, p.n_add, wn, p.eps, hs, red);
     if (c == 0 && (t >> 5) == rank) *reinterpret_cast<float4*>(p.xout + 4 * t) = xv;
     trace_at(tr, 2);
-    cp_wait_all();
+    if (!mbar_wait0(&bar_w) && t == 0) atomicOr(p.status, QW_DEV_TIMEOUT);
     __syncthreads();
     trace_at(tr, 3);
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
