@@ -80,17 +80,16 @@ CONFIGS = {
 NCU_TRAFFIC = {
     # batch-1 cluster path: one launch captured in a 28-layer decode step (cache of ~7 keys;
     # the K/V bytes of the bench's ~37-key caches add 0.15 MB per launch)
-    (1, "rmsnorm+qkv+attention+o_proj (cluster kernel)"): (12770816, "decode_qwen3_decoder_gb300/csrc/k_dec1.cu",
-                                                           "7e1fe5802acbcb219dd291bfb310820b3641150a1aa55a60f154ed4a087c5744"),
-    (3, "gate_up+silu_mul"): (29395200 + 668160, "decode_qwen3_decoder_gb300/csrc/k_gemm.cu",
-                              "ac14bf4a7fabf4ebcb03ecc75dc46125c104e7ad15728ab9ed1e163b507579cc"),
-    (3, "qkv_proj+qk_norm+rope+kv_append"): (25560832 + 10699520, "decode_qwen3_decoder_gb300/csrc/k_gemm.cu",
-                                             "ac14bf4a7fabf4ebcb03ecc75dc46125c104e7ad15728ab9ed1e163b507579cc"),
-    # batched decode attention: measured on 256-token caches (two 32-token launches, 35.83 MB
-    # each, 1.064 x their algorithmic bytes) and scaled by the key count to one 64-token launch
-    # of the full workload (285.2 MB algorithmic); the traffic grows with the keys read
-    (2, "attention"): (303361426, "decode_qwen3_decoder_gb300/csrc/k_attn.cu",
-                       "0d66968b12b44735a08f408243699a895815c7cc6effd772c4a675a1e9d25935"),
+    (1, "rmsnorm+qkv+attention+o_proj (cluster kernel)"): (12778496, "decode_qwen3_decoder_gb300/csrc/k_dec1.cu",
+                                                           "7e5a847ccbe0c3ab3df3ed926f476cd4f9736cf95e691b66ced7d984c32540f0"),
+    # 16 x 512 prefill, one gate/up launch (CTA pairs): read 29.39 MB + written 0.82 MB
+    (3, "gate_up+silu_mul"): (29385984 + 822528, "decode_qwen3_decoder_gb300/csrc/k_gemm.cu",
+                              "b9a1cb9f933fb98cbef3992ee013642777ea92516c576e65e423e1b31237671f"),
+    # batched decode attention: one 32-sequence launch of the two-stream path over 1026-key
+    # caches read 136.50 MB and wrote 2.77 MB, 1.033 x its algorithmic bytes; the bench times
+    # one 64-sequence launch per layer (285.2 MB algorithmic), so 1.033 x 285.2 MB
+    (2, "attention"): (294611600, "decode_qwen3_decoder_gb300/csrc/k_attn.cu",
+                       "c7d1340c9aacb00eb320a872b80d25332c032f92af8f54b65538ea7a40888f8d"),
 }
 
 
