@@ -24,7 +24,7 @@ LIB = os.path.join(LIBDIR, "libqw.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O3",
                      "--expt-relaxed-constexpr", "-I", INCLUDE]
-SOURCES = ["qw_runtime.cu", "k_small.cu", "k_attn.cu", "k_gemm.cu", "k_noalloc.cu", "k_sample.cu", "k_step.cu", "k_dec1.cu"]
+SOURCES = ["qw_runtime.cu", "k_small.cu", "k_attn.cu", "k_gemm.cu", "k_noalloc.cu", "k_sample.cu", "k_step.cu", "k_dec1.cu", "k_lmhead.cu"]
 
 
 def _nvcc() -> str:

@@ -198,6 +198,12 @@ cudaError_t launch_gemv_lmhead(const LaunchCtx& c, int B, const float* x, const 
                                const bf16* norm_w, float eps, const bf16* E, int vocab, int K,
                                float* logits, unsigned long long* best, const float* xadd = nullptr,
                                int n_add = 0);
+// Final RMSNorm + tied LM head + argmax of ONE row (k_lmhead.cu): the embedding streamed through
+// a ring of TMA bulk copies; the same operations, in the same order, as launch_gemv_lmhead.
+bool lmhead1_ok(int K, int vocab);
+cudaError_t launch_lmhead1(const LaunchCtx& c, const float* x, const int* rows, const bf16* norm_w, float eps,
+                           const bf16* E, int vocab, int K, float* logits, unsigned long long* best,
+                           const float* xadd, int n_add, int* status, int num_sms);
 cudaError_t launch_finalize(const LaunchCtx& c, const StepDesc& sd, unsigned long long* best,
                             int32_t* next_ids, KVView kv);
 cudaError_t launch_qknorm_rope_append(const LaunchCtx& c, int T, int layer, const float* qkv,

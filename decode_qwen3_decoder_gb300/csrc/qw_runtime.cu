@@ -1214,8 +1214,12 @@ static qw_status run_step(qw_model* m, qw_kv* kv, const StepDesc& sd, bool prefi
         PROF(QW_PROF_LMHEAD);
         const bool d1 = !engine && dec1_step(m, sd, prefill, max_keys);  // x + the last down_proj partials
         if (d1) lc.pdl = pdl_on;
-        CUDA_TRY(launch_gemv_lmhead(lc, B, m->x, m->last, m->fnorm, c.rms_eps, m->embed, c.vocab, D, logits,
-                                    m->best, d1 ? m->d1_dpart : nullptr, d1 ? dec1_parts() : 0));
+        if (B == 1 && lmhead1_ok(D, c.vocab))
+            CUDA_TRY(launch_lmhead1(lc, m->x, m->last, m->fnorm, c.rms_eps, m->embed, c.vocab, D, logits, m->best,
+                                    d1 ? m->d1_dpart : nullptr, d1 ? dec1_parts() : 0, m->status, m->num_sms));
+        else
+            CUDA_TRY(launch_gemv_lmhead(lc, B, m->x, m->last, m->fnorm, c.rms_eps, m->embed, c.vocab, D, logits,
+                                        m->best, d1 ? m->d1_dpart : nullptr, d1 ? dec1_parts() : 0));
     } else {
         {
             PROF(QW_PROF_RMSNORM);
