@@ -958,6 +958,12 @@ static qw_status run_layers(qw_model* m, qw_kv* kv, const StepDesc& sd, bool pre
     int* counters = m->counters + (size_t)t0 * c.n_kv_heads;
     int32_t* dbg_pos = dbg ? m->dbg_pos + t0 : nullptr;
     int32_t* dbg_slot = dbg ? m->dbg_slot + t0 : nullptr;
+    // SMs a decode GEMM of one half of the two-stream split may spread over: 3/8 of the GPU
+    // (32 CTAs for q|k|v, 48 for gate/up, 7-way split-K clusters for o_proj and down_proj at
+    // 152 SMs), so that the other half's attention keeps the rest. Measured at B = 64 x 1024
+    // keys on one box: 3029 us per step with every GEMM spread over all SMs, 2908 with 1/2,
+    // 2760 with 1/3, 2687 with 3/8, 3000 with 1/4.
+    const int gsms = (!prefill && T < sd.T) ? std::max(8, m->num_sms * 3 / 8) : m->num_sms;
     if (dec1_step(m, sd, prefill, max_keys)) {
         // x (m->x) -> [attention kernel: x + partials into d1_y, o_proj partials] -> [MLP
         // kernel: d1_y + o_proj partials into m->x, down_proj partials] -> next layer
@@ -1016,7 +1022,7 @@ static qw_status run_layers(qw_model* m, qw_kv* kv, const StepDesc& sd, bool pre
             GemmArgs g = {};
             g.tmA = &m->tm_wqkv; g.tmB = m->tm_h; g.b_row0 = t0;
             g.a_row0 = l * m->qkv_rows; g.M = m->qkv_rows; g.K = D; g.T = T;
-            g.status = m->status; g.num_sms = m->num_sms;
+            g.status = m->status; g.num_sms = gsms;
             g.q_out = q; g.q_norm = w_qn; g.k_norm = w_kn; g.eps = c.rms_eps;
             g.rope_cos = m->rcos; g.rope_sin = m->rsin; g.tv = tv; g.kv = kvv; g.layer = l;
             g.n_heads = c.n_heads; g.n_kv = c.n_kv_heads;
@@ -1083,7 +1089,7 @@ static qw_status run_layers(qw_model* m, qw_kv* kv, const StepDesc& sd, bool pre
             GemmArgs g = {};
             g.tmA = &m->tm_wo; g.tmB = m->tm_attn; g.b_row0 = t0;
             g.a_row0 = l * D; g.M = D; g.K = QD; g.T = T;
-            g.out_f32 = x; g.ld_out = D; g.status = m->status; g.num_sms = m->num_sms;
+            g.out_f32 = x; g.ld_out = D; g.status = m->status; g.num_sms = gsms;
             LAUNCH(launch_gemm_tc(lc, EPI_RESID_F32, g));
         }
         // --- feed-forward sublayer (Paso 6) ---
@@ -1105,7 +1111,7 @@ static qw_status run_layers(qw_model* m, qw_kv* kv, const StepDesc& sd, bool pre
             GemmArgs g = {};
             g.tmA = &m->tm_wgu; g.tmB = m->tm_h; g.b_row0 = t0;
             g.a_row0 = l * 2 * I; g.M = 2 * I; g.K = D; g.T = T;
-            g.out_h = act; g.ld_out = I; g.status = m->status; g.num_sms = m->num_sms;
+            g.out_h = act; g.ld_out = I; g.status = m->status; g.num_sms = gsms;
             {
                 PROF(QW_PROF_GATEUP);
                 LAUNCH(launch_gemm_tc(lc, EPI_SILU_MUL, g));
@@ -1113,7 +1119,7 @@ static qw_status run_layers(qw_model* m, qw_kv* kv, const StepDesc& sd, bool pre
             GemmArgs g2 = {};
             g2.tmA = &m->tm_wd; g2.tmB = m->tm_act; g2.b_row0 = t0;
             g2.a_row0 = l * D; g2.M = D; g2.K = I; g2.T = T;
-            g2.out_f32 = x; g2.ld_out = D; g2.status = m->status; g2.num_sms = m->num_sms;
+            g2.out_f32 = x; g2.ld_out = D; g2.status = m->status; g2.num_sms = gsms;
             PROF(QW_PROF_DOWN);
             LAUNCH(launch_gemm_tc(lc, EPI_RESID_F32, g2));
         }
