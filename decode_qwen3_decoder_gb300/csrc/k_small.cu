@@ -99,9 +99,15 @@ __global__ void __launch_bounds__(256) k_rmsnorm(const float* __restrict__ x, co
                                                  int n_rows, int hidden, const bf16* __restrict__ w,
                                                  float eps, f16* __restrict__ h) {
     pdl_launch();
-    pdl_wait();
     const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
+    // the norm weights are constant: requested before the dependency wait
+    uint2 wv[8];
+    if (hidden == 1024) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) wv[u] = *reinterpret_cast<const uint2*>(w + lane * 4 + u * 128);
+    }
+    pdl_wait();
     if (r < n_rows && hidden == 1024) {
         // the model's width: the row's 8 float4 per lane are requested together and kept in
         // registers (one round trip, no second read)
@@ -117,7 +123,7 @@ __global__ void __launch_bounds__(256) k_rmsnorm(const float* __restrict__ x, co
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             const int k = lane * 4 + u * 128;
-            const uint2 wb = *reinterpret_cast<const uint2*>(w + k);
+            const uint2 wb = wv[u];
             uint2 o;
             o.x = pack_h2(v[u].x * rs * bf_lo(wb.x), v[u].y * rs * bf_hi(wb.x));
             o.y = pack_h2(v[u].z * rs * bf_lo(wb.y), v[u].w * rs * bf_hi(wb.y));
