@@ -3,8 +3,8 @@
 //
 // At batch 1 the head is a 311 MB read for 1024 MACs per row. The GEMV family reaches ~80% of
 // HBM on it: each warp issues its rows' loads, waits for them, reduces, and only then issues
-// the next rows. Here a producer warp keeps LM_NST stages of 16 rows (32 KB) in flight per SM
-// with cp.async.bulk (the TMA engine; the weights depend on nothing computed in the step, so
+// the next rows. Here a producer warp per CTA (two CTAs per SM) keeps LM_NST stages of 16 rows
+// (32 KB) in flight with cp.async.bulk (the TMA engine; the weights depend on nothing computed in the step, so
 // the first stages are issued before the dependency wait), and 8 consumer warps reduce each
 // stage from shared memory (2 rows per warp) against h held in registers.
 //
@@ -21,7 +21,7 @@ constexpr int LM_CONS_WARPS = 8;
 constexpr int LM_THREADS = (LM_CONS_WARPS + 1) * 32;  // + the producer warp
 constexpr int LM_ROWS = 2 * LM_CONS_WARPS;   // rows per stage
 constexpr int LM_STAGE = LM_ROWS * LM_K * 2; // 32 KB
-constexpr int LM_NST = 6;
+constexpr int LM_NST = 3;
 constexpr int LM_SMEM = LM_NST * LM_STAGE;
 constexpr unsigned long long LM_WAIT_NS = 2000000000ull;
 
@@ -87,7 +87,7 @@ struct LmP {
 
 }  // namespace
 
-__global__ void __launch_bounds__(LM_THREADS, 1) k_lmhead1(const __grid_constant__ LmP p) {
+__global__ void __launch_bounds__(LM_THREADS, 2) k_lmhead1(const __grid_constant__ LmP p) {
     extern __shared__ __align__(128) uint8_t lm_sm[];  // [LM_NST][LM_ROWS][1024] bf16
     __shared__ __align__(8) uint64_t full[LM_NST], empty[LM_NST];
     __shared__ __align__(16) float hs[LM_K];
@@ -257,6 +257,6 @@ cudaError_t launch_lmhead1(const LaunchCtx& c, const float* x, const int* rows, 
     p.xadd = xadd;
     p.n_add = xadd ? n_add : 0;
     p.status = status;
-    const int grid = std::min(num_sms > 0 ? num_sms : 148, vocab / LM_ROWS);
+    const int grid = std::min(2 * (num_sms > 0 ? num_sms : 148), vocab / LM_ROWS);
     return launch_k(c, k_lmhead1, dim3(grid), dim3(LM_THREADS), (size_t)LM_SMEM, p);
 }
