@@ -51,6 +51,7 @@ constexpr int D1_NB = 16;                // clusters of the MLP kernel = its dow
 constexpr int D1_ROWS_O = D1_D / D1_CL;  // o_proj rows per CTA (64)
 constexpr int D1_ROWS_M = D1_D / D1_CLM; // down_proj rows each MLP CTA sums (128)
 constexpr unsigned long long D1_WAIT_NS = 2000000000ull;
+constexpr int D1_TRACE_CTAS = 128;       // trace records per launch (both grids have <= 128 CTAs)
 
 // attention kernel, dynamic shared memory: o_proj slice [64][256] bf16 | cached pages
 // [D1_MAXPG][K 4 KB | V 4 KB] | h [1024] fp32 | gathered q|k|v of the head [512] fp32
@@ -220,7 +221,7 @@ __global__ void __launch_bounds__(D1_THREADS, 2) k_dec1_attn(const __grid_consta
     __shared__ __align__(8) uint64_t bar_w;  // the o_proj slice and the cached pages have landed
     __shared__ int s_np, s_bad;
     pdl_launch();
-    unsigned long long* tr = p.trace ? p.trace + ((size_t)2 * p.layer * gridDim.x + blockIdx.x) * 8 : nullptr;
+    unsigned long long* tr = p.trace ? p.trace + ((size_t)2 * p.layer * D1_TRACE_CTAS + blockIdx.x) * 8 : nullptr;
     trace_at(tr, 0);
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const int rank = (int)cluster_rank(), g = (int)cluster_id();
@@ -502,7 +503,7 @@ __global__ void __launch_bounds__(D1_THREADS, 2) k_dec1_mlp(const __grid_constan
     __shared__ __align__(8) uint64_t bar_r;  // all 8 partial slices have landed
     __shared__ __align__(8) uint64_t bar_w;  // the shared-memory weight rows have landed
     pdl_launch();
-    unsigned long long* tr = p.trace ? p.trace + ((size_t)(2 * p.layer + 1) * gridDim.x + blockIdx.x) * 8 : nullptr;
+    unsigned long long* tr = p.trace ? p.trace + ((size_t)(2 * p.layer + 1) * D1_TRACE_CTAS + blockIdx.x) * 8 : nullptr;
     trace_at(tr, 0);
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const int rank = (int)cluster_rank(), c = (int)cluster_id();

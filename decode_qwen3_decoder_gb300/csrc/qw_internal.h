@@ -261,7 +261,7 @@ struct Dec1Attn {
     int n_kv, QD, KD;
     float scale_log2;
     // optional %globaltimer records: CTA c of this launch writes 8 values at
-    // trace[((2 layer) * gridDim.x + c) * 8]
+    // trace[((2 layer) * 128 + c) * 8]
     unsigned long long* trace;
 };
 // MLP kernel: x = xin + sum_{g < n_add} opart[g]; RMSNorm; gate/up + SwiGLU of 8 x 16 CTAs'
@@ -281,7 +281,7 @@ struct Dec1Mlp {
     int I;
     int* status;
     int layer;
-    unsigned long long* trace;  // as Dec1Attn's, at trace[((2 layer + 1) * gridDim.x + c) * 8]
+    unsigned long long* trace;  // as Dec1Attn's, at trace[((2 layer + 1) * 128 + c) * 8]
 };
 bool dec1_available(int D, int I, int QD, int n_heads, int n_kv);
 int dec1_max_keys();
