@@ -80,8 +80,9 @@ CONFIGS = {
 NCU_TRAFFIC = {
     # batch-1 cluster path: one launch captured in a 28-layer decode step (cache of ~7 keys;
     # the K/V bytes of the bench's ~37-key caches add 0.15 MB per launch)
-    (1, "rmsnorm+qkv+attention+o_proj (cluster kernel)"): (12778496, "decode_qwen3_decoder_gb300/csrc/k_dec1.cu",
-                                                           "7e5a847ccbe0c3ab3df3ed926f476cd4f9736cf95e691b66ced7d984c32540f0"),
+    (1, "rmsnorm+qkv+attention+o_proj (cluster kernel)"): (12777728, "decode_qwen3_decoder_gb300/csrc/k_dec1.cu",
+                                                           "63a938243564671fd3850eee2c08fa8fbff4f5a38bae0e034d0c868edb646a51"),
+
     # 16 x 512 prefill, one gate/up launch (CTA pairs): read 29.39 MB + written 0.82 MB
     (3, "gate_up+silu_mul"): (29385984 + 822528, "decode_qwen3_decoder_gb300/csrc/k_gemm.cu",
                               "b9a1cb9f933fb98cbef3992ee013642777ea92516c576e65e423e1b31237671f"),
