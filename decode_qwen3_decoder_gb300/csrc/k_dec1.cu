@@ -5,13 +5,13 @@
 // products; as four launches (q|k|v, attention + o_proj, gate/up, down_proj) every link
 // pays a kernel hand-off plus an L2 round trip for its input. Here the chain is cut at the
 // two places where a result must be gathered from the whole GPU, and every other exchange
-// stays inside a 16-CTA thread-block cluster (distributed shared memory, cluster barrier):
+// stays inside a thread-block cluster (distributed shared memory):
 //
 //  k_dec1_attn  one cluster per KV head g (grid n_kv x 16). Each CTA rebuilds x (the layer
 //               input: x + the previous layer's down_proj partials, in a fixed order), its
 //               RMSNorm, and 32 of the 512 q|k|v rows of head g (q of heads 2g and 2g+1, k, v
-//               of g). The 32 results go to every CTA of the cluster (st.shared::cluster);
-//               after the cluster barrier each CTA holds q, k, v of head g and runs QK-norm,
+//               of g). The 32 results go to every CTA of the cluster; once all 512 have
+//               landed each CTA holds q, k, v of head g and runs QK-norm,
 //               RoPE and the attention over the cached pages plus the new key (rank 0 also
 //               appends K/V to the cache), then o_proj rows [64 r, 64 r + 64) over head g's 256
 //               inputs into opart[g]. Cluster 0 writes x.
@@ -33,9 +33,10 @@
 // a relaxed cluster barrier), so no fence sits on the critical path; every wait on an
 // mbarrier is bounded and reports QW_DEV_TIMEOUT.
 // Nothing read before griddepcontrol.wait is written by an earlier kernel of the step: the
-// weights (q|k|v rows in registers, o_proj / gate-up / down slices and the cached K/V pages
-// copied into shared memory with cp.async), the norm weights, the cached length and page
-// table. Every reduction has a fixed order, so a step is deterministic.
+// weights (q|k|v and gate/up rows in registers; o_proj, extra gate/up and down_proj rows and
+// the cached K/V pages bulk-copied into shared memory by one thread, cp.async.bulk on an
+// mbarrier), the norm weights, the cached length and page table. Every reduction has a fixed
+// order, so a step is deterministic.
 #include "qw_internal.h"
 
 namespace {

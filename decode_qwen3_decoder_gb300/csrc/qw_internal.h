@@ -231,7 +231,7 @@ struct AttnFuse {
 int attn_oproj_max_keys();
 cudaError_t launch_attn_oproj(const LaunchCtx& c, int seq, int layer, const AttnFuse& fz, int n_heads, int n_kv,
                               TokView tv, KVView kv, const bf16* Wo, int D, float* part, f16* dbg_attn);
-// Batch-1 decode layer as two 16-CTA cluster launches (k_dec1.cu), for hidden 1024, inter
+// Batch-1 decode layer as two cluster launches (k_dec1.cu), for hidden 1024, inter
 // 128 x {16, 24, 32}, n_kv <= 8 and caches of at most dec1_max_keys() keys.
 // Attention kernel: x = xin + sum_{c < n_add} dpart[c]; RMSNorm; q|k|v of KV head g gathered
 // in cluster g; QK-norm, RoPE, KV append, attention; o_proj rows of the head's inputs into
@@ -264,7 +264,7 @@ struct Dec1Attn {
     // trace[((2 layer) * 128 + c) * 8]
     unsigned long long* trace;
 };
-// MLP kernel: x = xin + sum_{g < n_add} opart[g]; RMSNorm; gate/up + SwiGLU of 8 x 16 CTAs'
+// MLP kernel: x = xin + sum_{g < n_add} opart[g]; RMSNorm; gate/up + SwiGLU of 16 x 8 CTAs'
 // unit slices; split-K down_proj reduced per cluster into dpart[c][D] (c < dec1_parts()).
 // Cluster 0 writes x to xout.
 struct Dec1Mlp {

@@ -276,7 +276,7 @@ enum {
      * more than the attention provides (default 0), so that its wait runs out. */
     QW_OPT_TEST_EXTRA_ARRIVALS = 7,
     /* 1 (default where available: hidden 1024, inter 2048/3072/4096, n_kv_heads <= 8, more
-     * than one layer, and the device fits the 16-CTA clusters): a decode step of ONE token with
+     * than one layer, and the device fits the kernels' 16- and 8-CTA clusters): a decode step of ONE token with
      * bf16 weights over a
      * cache of at most 128 keys runs each layer as two cluster launches -- (RMSNorm, q|k|v,
      * QK-norm, RoPE, KV append, attention, o_proj) and (RMSNorm, gate/up, SwiGLU, down_proj),

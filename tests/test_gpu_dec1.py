@@ -1,5 +1,5 @@
-"""Batch-1 decode as two 16-CTA cluster launches per layer (QW_OPT_BATCH1_CLUSTERS, on by
-default where the shape and the device allow it) against the oracle: every layer's hidden
+"""Batch-1 decode as two thread-block-cluster launches per layer (QW_OPT_BATCH1_CLUSTERS, on by
+default for multi-layer models where the shape and the device allow it) against the oracle: every layer's hidden
 state, the KV slot, the logits and the greedy id of each decode step, for cached lengths
 that start, cross and end 16-key pages up to the path's 128-key limit and the step after it
 (which takes the launch-per-phase path); the attention outputs against the launch-per-phase
