@@ -80,8 +80,9 @@ CONFIGS = {
 NCU_TRAFFIC = {
     # batch-1 cluster path: one launch captured in a 28-layer decode step (cache of ~7 keys;
     # the K/V bytes of the bench's ~37-key caches add 0.15 MB per launch)
-    (1, "rmsnorm+qkv+attention+o_proj (cluster kernel)"): (12777728, "decode_qwen3_decoder_gb300/csrc/k_dec1.cu",
-                                                           "63a938243564671fd3850eee2c08fa8fbff4f5a38bae0e034d0c868edb646a51"),
+    (1, "rmsnorm+qkv+attention+o_proj (cluster kernel)"): (12779008, "decode_qwen3_decoder_gb300/csrc/k_dec1.cu",
+                                                           "3e8d08a46222756f1ca35c208d8a2bfd2c4566d38efaea94c69d21c19465cd71"),
+
 
     # 16 x 512 prefill, one gate/up launch (CTA pairs): read 29.39 MB + written 0.82 MB
     (3, "gate_up+silu_mul"): (29385984 + 822528, "decode_qwen3_decoder_gb300/csrc/k_gemm.cu",
