@@ -147,3 +147,33 @@ def test_repeat_is_bit_identical(one):
             tok = int(d["next"][0])
         seen.append(np.stack(lg))
     assert np.array_equal(seen[0], seen[1])
+
+
+def test_trace_records_follow_the_documented_layout(full):
+    """qw_trace_set on the cluster path: for every layer, launch (attention, MLP) and CTA, eight
+    %globaltimer values at ((2 l + k) * 128 + c) * 8, in order (entry <= ... <= exit), each launch's
+    dependency wait after the previous launch's earliest exit, and nothing written elsewhere."""
+    import torch
+    run = full
+    qw = run.qw
+    _set(run, True)
+    L = S.n_layers
+    prompt = synth.make_tokens(S.vocab, 5, 4500).tolist()
+    qw.qw_kv_reset(run.eng.kv, -1, run.eng.stream)
+    g = run.prefill([0], [prompt], debug=False, reserve_extra=4)
+    buf = torch.zeros(L * 2 * 128 * 8 + 64, dtype=torch.int64, device="cuda")
+    qw.qw_trace_set(run.eng.model, buf.data_ptr(), 8)
+    try:
+        run.decode([0], [int(g["next"][0])], debug=False)
+    finally:
+        qw.qw_trace_set(run.eng.model, 0, 0)
+    tr = buf.cpu().numpy()
+    assert not tr[L * 2 * 128 * 8:].any()
+    tr = tr[:L * 2 * 128 * 8].reshape(L, 2, 128, 8)
+    assert (tr > 0).all()
+    assert (np.diff(tr, axis=3) >= 0).all()
+    for l in range(L):
+        # the MLP kernel's wait ends after the attention kernel's CTAs have all exited
+        assert tr[l, 1, :, 1].min() >= tr[l, 0, :, 7].max()
+        if l:
+            assert tr[l, 0, :, 1].min() >= tr[l - 1, 1, :, 7].max()
