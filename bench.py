@@ -80,8 +80,8 @@ CONFIGS = {
 NCU_TRAFFIC = {
     # batch-1 cluster path: one launch captured in a 28-layer decode step (cache of ~7 keys;
     # the K/V bytes of the bench's ~37-key caches add 0.15 MB per launch)
-    (1, "rmsnorm+qkv+attention+o_proj (cluster kernel)"): (12779008, "decode_qwen3_decoder_gb300/csrc/k_dec1.cu",
-                                                           "3e8d08a46222756f1ca35c208d8a2bfd2c4566d38efaea94c69d21c19465cd71"),
+    (1, "rmsnorm+qkv+attention+o_proj (cluster kernel)"): (12744448, "decode_qwen3_decoder_gb300/csrc/k_dec1.cu",
+                                                           "47f5ba5eece4a18f9646982d763c8af8ff0387b20584c6883ec4610537133ad2"),
 
 
     # 16 x 512 prefill, one gate/up launch (CTA pairs): read 29.39 MB + written 0.82 MB
@@ -205,10 +205,10 @@ def kernel_bytes(kind: int, s, T: int, B: int, ctx: float = 0.0, clusters: bool 
     (kind 5) also does down_proj."""
     D, I, QD, KD, V = s.hidden, s.inter, s.n_heads * s.head_dim, s.n_kv_heads * s.head_dim, s.vocab
     QKV = QD + 2 * KD
-    if clusters and kind == 3:   # x + partials in, q|k|v + o_proj weights, cached K/V, o_proj partials out
-        return QKV * D * 2 + D * QD * 2 + ctx * KD * 2 * 2 + 2 * KD * 2 + (1 + 16) * D * 4 + s.n_kv_heads * D * 4
-    if clusters and kind == 5:   # x + o_proj partials in, gate/up/down weights, down_proj partials out
-        return 3 * I * D * 2 + (1 + s.n_kv_heads) * D * 4 + 16 * D * 4
+    if clusters and kind == 3:   # x + 8 down_proj slots in, q|k|v + o_proj weights, cached K/V, o_proj partials out
+        return QKV * D * 2 + D * QD * 2 + ctx * KD * 2 * 2 + 2 * KD * 2 + (1 + 8) * D * 4 + s.n_kv_heads * D * 4
+    if clusters and kind == 5:   # x + o_proj partials in, gate/up/down weights, down_proj partials added into 8 slots
+        return 3 * I * D * 2 + (1 + s.n_kv_heads) * D * 4 + 8 * D * 4
     if kind == 1:   # q|k|v projection (+ fused input RMSNorm)
         return QKV * D * 2 + T * D * 4 + T * QKV * 4 + D * 2
     if kind == 3:   # attention fused with o_proj (one token): o_proj weights + the cached K/V once

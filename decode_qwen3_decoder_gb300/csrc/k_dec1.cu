@@ -20,10 +20,14 @@
 //               (fp16-rounded as the activation is stored), then the split-K product of
 //               down_proj over those 24 inputs for all 1024 outputs. The 8 partial vectors of a
 //               cluster are summed through distributed shared memory (CTA r adds rows
-//               [128 r, 128 r + 128) over ranks 0..7 in order) into dpart[c]. Cluster 0 writes
-//               x + sum opart.
+//               [128 r, 128 r + 128) over ranks 0..7 in order) and added into slot c / 2 of
+//               dpart. Cluster 0 writes x + sum opart.
 //
-// The next kernel adds the 16 down_proj partials to x itself, so a layer is two launches.
+// The next kernel adds the 8 down_proj slots to x itself, so a layer is two launches. A slot
+// takes exactly two atomic adds onto zero (the attention kernel of the same layer clears the
+// set, and two sets alternate by layer so that it never clears one still being read); with
+// two addends the sum is the same in either order, so the step stays deterministic while
+// the reader loads 8 vectors instead of 16.
 // The MLP clusters are 8 CTAs so that both kernels' clusters fit on the GPU together (a
 // 16-CTA cluster needs 16 free CTA slots in one GPC), which lets each kernel's CTAs start and
 // fetch their weights while the other kernel runs.
@@ -36,7 +40,7 @@
 // weights (q|k|v and gate/up rows in registers; o_proj, extra gate/up and down_proj rows and
 // the cached K/V pages bulk-copied into shared memory by one thread, cp.async.bulk on an
 // mbarrier), the norm weights, the cached length and page table. Every reduction has a fixed
-// order, so a step is deterministic.
+// order (or, for the paired slots, two commuting addends), so a step is deterministic.
 #include "qw_internal.h"
 
 namespace {
@@ -48,7 +52,8 @@ constexpr int D1_WARPS = D1_THREADS / 32;
 constexpr int D1_MAXPG = 8;              // cached 16-key pages held in shared memory (128 keys)
 constexpr int D1_PAGE = 16 * 128 * 2;    // bytes of K (or V) of one page of one KV head
 constexpr int D1_CLM = 8;                // CTAs per cluster of the MLP kernel
-constexpr int D1_NB = 16;                // clusters of the MLP kernel = its down_proj partials
+constexpr int D1_NB = 16;                // clusters of the MLP kernel
+constexpr int D1_NP = D1_NB / 2;         // down_proj partials: clusters 2k, 2k + 1 add into slot k
 constexpr int D1_ROWS_O = D1_D / D1_CL;  // o_proj rows per CTA (64)
 constexpr int D1_ROWS_M = D1_D / D1_CLM; // down_proj rows each MLP CTA sums (128)
 constexpr unsigned long long D1_WAIT_NS = 2000000000ull;
@@ -177,25 +182,24 @@ __device__ __forceinline__ void trace_at(unsigned long long* tr, int k) {
 
 // x = xin + sum_{c < n_add} part[c] (added in order of c), then h = x * rsqrt(mean(x^2) + eps) * w
 // into hs; thread t owns x[4t .. 4t + 4). Returns this thread's x.
+// NMAX: the most partials (n_add <= NMAX), all loaded in one round trip.
+template <int NMAX>
 __device__ __forceinline__ float4 stage_norm(const float* xin, const float* part, int n_add, uint2 wv, float eps,
                                              float* hs, float* red) {
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     float4 v = *reinterpret_cast<const float4*>(xin + 4 * t);
+    if (n_add > 0) {
+        float4 a[NMAX];
 #pragma unroll
-    for (int c0 = 0; c0 < D1_NB; c0 += 8) {
-        if (c0 < n_add) {
-            float4 a[8];
+        for (int c = 0; c < NMAX; ++c)
+            a[c] = *reinterpret_cast<const float4*>(part + (size_t)min(c, n_add - 1) * D1_D + 4 * t);
 #pragma unroll
-            for (int c = 0; c < 8; ++c)
-                a[c] = *reinterpret_cast<const float4*>(part + (size_t)min(c0 + c, n_add - 1) * D1_D + 4 * t);
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                if (c0 + c < n_add) {
-                    v.x += a[c].x;
-                    v.y += a[c].y;
-                    v.z += a[c].z;
-                    v.w += a[c].w;
-                }
+        for (int c = 0; c < NMAX; ++c) {
+            if (c < n_add) {
+                v.x += a[c].x;
+                v.y += a[c].y;
+                v.z += a[c].z;
+                v.w += a[c].w;
             }
         }
     }
@@ -284,6 +288,12 @@ __global__ void __launch_bounds__(D1_THREADS, 2) k_dec1_attn(const __grid_consta
     cluster_arrive_relaxed();
     pdl_wait();
     trace_at(tr, 1);
+    // the partial set this layer's MLP kernel adds into starts at zero; its last reader (the
+    // attention kernel of the layer before, or the LM head of the step before) has completed
+    {
+        const int i = blockIdx.x * D1_THREADS + t;
+        if (i < D1_NP * D1_D / 4) reinterpret_cast<float4*>(p.dclear)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
     // the token's position and its RoPE row (in flight while x is staged)
     const int pos = p.pos[0];
     const int i0 = (lane & 15) * 4;
@@ -291,7 +301,7 @@ __global__ void __launch_bounds__(D1_THREADS, 2) k_dec1_attn(const __grid_consta
     const float4 sn = *reinterpret_cast<const float4*>(p.rope_sin + (size_t)pos * 64 + i0);
 
     // ---- x, RMSNorm, q|k|v --------------------------------------------------------------
-    const float4 xv = stage_norm(p.xin, p.dpart, p.n_add, wn, p.eps, hs, red);
+    const float4 xv = stage_norm<D1_NP>(p.xin, p.dpart, p.n_add, wn, p.eps, hs, red);
     if (g == 0 && (t >> 4) == rank) *reinterpret_cast<float4*>(p.xout + 4 * t) = xv;
     cluster_wait();  // every CTA's mbarrier is initialised
     __syncthreads();
@@ -534,7 +544,7 @@ __global__ void __launch_bounds__(D1_THREADS, 2) k_dec1_mlp(const __grid_constan
     trace_at(tr, 1);
 
     // ---- x + o_proj partials, RMSNorm, gate/up, SwiGLU -------------------------------
-    const float4 xv = stage_norm(p.xin, p.opart, p.n_add, wn, p.eps, hs, red);
+    const float4 xv = stage_norm<8>(p.xin, p.opart, p.n_add, wn, p.eps, hs, red);
     if (c == 0 && (t >> 5) == rank) *reinterpret_cast<float4*>(p.xout + 4 * t) = xv;
     trace_at(tr, 2);
     if (!mbar_wait0(&bar_w) && t == 0) atomicOr(p.status, QW_DEV_TIMEOUT);
@@ -605,7 +615,9 @@ __global__ void __launch_bounds__(D1_THREADS, 2) k_dec1_mlp(const __grid_constan
         float s = 0.f;
 #pragma unroll
         for (int r = 0; r < D1_CLM; ++r) s += rbuf[r * D1_ROWS_M + t];
-        p.dpart[(size_t)c * D1_D + D1_ROWS_M * rank + t] = s;
+        // clusters 2k and 2k + 1 meet in slot k, zeroed beforehand: 0 + a + b = a + b in
+        // either order (two addends), so the sum does not depend on which lands first
+        atomicAdd(p.dpart + (size_t)(c >> 1) * D1_D + D1_ROWS_M * rank + t, s);
     }
     trace_at(tr, 7);
 }
@@ -694,7 +706,7 @@ cudaError_t mlp_go(const LaunchCtx& c, const Dec1Mlp& p) {
 }  // namespace
 
 int dec1_max_keys() { return D1_MAXPG * 16; }
-int dec1_parts() { return D1_NB; }
+int dec1_parts() { return D1_NP; }
 
 bool dec1_available(int D, int I, int QD, int n_heads, int n_kv) {
     if (D != D1_D || QD != n_heads * 128 || n_heads != 2 * n_kv || n_kv < 1 || n_kv > 8) return false;

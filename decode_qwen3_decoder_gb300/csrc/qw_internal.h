@@ -240,6 +240,7 @@ struct Dec1Attn {
     const float* xin;
     const float* dpart;  // [n_add][D]
     int n_add;
+    float* dclear;       // [dec1_parts()][D] set to zero: the set this layer's MLP kernel adds into
     float* xout;         // [D]
     const bf16* w_in;
     float eps;
@@ -265,7 +266,8 @@ struct Dec1Attn {
     unsigned long long* trace;
 };
 // MLP kernel: x = xin + sum_{g < n_add} opart[g]; RMSNorm; gate/up + SwiGLU of 16 x 8 CTAs'
-// unit slices; split-K down_proj reduced per cluster into dpart[c][D] (c < dec1_parts()).
+// unit slices; split-K down_proj reduced per cluster and added into dpart[c / 2][D]
+// (dec1_parts() slots, zero on entry).
 // Cluster 0 writes x to xout.
 struct Dec1Mlp {
     const float* xin;
@@ -277,7 +279,7 @@ struct Dec1Mlp {
     const bf16* Wg;      // [I][D] of the layer
     const bf16* Wu;      // [I][D]
     const bf16* WdT;     // [I][D]: down_proj transposed
-    float* dpart;        // [dec1_parts()][D]
+    float* dpart;        // [dec1_parts()][D], zero on entry: clusters 2k, 2k + 1 add into slot k
     int I;
     int* status;
     int layer;

@@ -160,7 +160,7 @@ static WsLayout layout_for(const qw_config& c) {
     if (dec1_shape(c)) {
         L.bdT = take(NL * I * D * 2);
         L.d1_y = take(D * 4);
-        L.d1_dpart = take((size_t)dec1_parts() * D * 4);
+        L.d1_dpart = take((size_t)2 * dec1_parts() * D * 4);  // two sets, alternating by layer
     }
     L.gen_tok = take(T * 4);
     L.gen_cur = take((size_t)c.max_batch * 4);
@@ -971,7 +971,11 @@ static qw_status run_layers(qw_model* m, qw_kv* kv, const StepDesc& sd, bool pre
         for (int l = 0; l < c.n_layers; ++l) {
             const bf16* nb = m->norms + (size_t)l * (2 * D + 2 * d);
             Dec1Attn a = {};
-            a.xin = m->x; a.dpart = m->d1_dpart; a.n_add = l == 0 ? 0 : np; a.xout = m->d1_y;
+            // layer l's attention kernel clears set l % 2, its MLP kernel adds into it, and the
+            // next layer's attention kernel (or the LM head) reads it
+            float* dset = m->d1_dpart + (size_t)(l & 1) * np * D;
+            float* dprev = m->d1_dpart + (size_t)((l + 1) & 1) * np * D;
+            a.xin = m->x; a.dpart = dprev; a.n_add = l == 0 ? 0 : np; a.dclear = dset; a.xout = m->d1_y;
             a.w_in = nb; a.eps = c.rms_eps; a.Wqkv = m->bqkv + (size_t)l * m->qkv_rows * D;
             a.q_norm = nb + 2 * D; a.k_norm = nb + 2 * D + d; a.rope_cos = m->rcos; a.rope_sin = m->rsin;
             a.kv = kvv; a.layer = l; a.seq = sd.seq[0]; a.pos = tv.pos;
@@ -989,12 +993,12 @@ static qw_status run_layers(qw_model* m, qw_kv* kv, const StepDesc& sd, bool pre
             f.xin = m->d1_y; f.opart = m->op_part; f.n_add = c.n_kv_heads; f.xout = m->x;
             f.w_post = nb + D; f.eps = c.rms_eps;
             f.Wg = m->bg + (size_t)l * I * D; f.Wu = m->bu + (size_t)l * I * D; f.WdT = m->bdT + (size_t)l * I * D;
-            f.dpart = m->d1_dpart; f.I = I; f.status = m->status; f.layer = l; f.trace = m->trace;
+            f.dpart = dset; f.I = I; f.status = m->status; f.layer = l; f.trace = m->trace;
             {
                 PROF(QW_PROF_GATEUP);
                 LAUNCH(launch_dec1_mlp(lc, f));
             }
-            if (dbg) LAUNCH(launch_dec1_sum(lc, m->x, m->d1_dpart, np, D, m->dbg_hidden + (size_t)l * D));
+            if (dbg) LAUNCH(launch_dec1_sum(lc, m->x, dset, np, D, m->dbg_hidden + (size_t)l * D));
         }
         return QW_OK;
     }
@@ -1222,10 +1226,13 @@ static qw_status run_step(qw_model* m, qw_kv* kv, const StepDesc& sd, bool prefi
         if (d1) lc.pdl = pdl_on;
         if (B == 1 && lmhead1_ok(D, c.vocab))
             CUDA_TRY(launch_lmhead1(lc, m->x, m->last, m->fnorm, c.rms_eps, m->embed, c.vocab, D, logits, m->best,
-                                    d1 ? m->d1_dpart : nullptr, d1 ? dec1_parts() : 0, m->status, m->num_sms));
+                                    d1 ? m->d1_dpart + (size_t)((c.n_layers - 1) & 1) * dec1_parts() * D : nullptr,
+                                    d1 ? dec1_parts() : 0, m->status, m->num_sms));
         else
             CUDA_TRY(launch_gemv_lmhead(lc, B, m->x, m->last, m->fnorm, c.rms_eps, m->embed, c.vocab, D, logits,
-                                        m->best, d1 ? m->d1_dpart : nullptr, d1 ? dec1_parts() : 0));
+                                        m->best,
+                                        d1 ? m->d1_dpart + (size_t)((c.n_layers - 1) & 1) * dec1_parts() * D : nullptr,
+                                        d1 ? dec1_parts() : 0));
     } else {
         {
             PROF(QW_PROF_RMSNORM);
