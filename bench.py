@@ -296,23 +296,30 @@ def run_ours(args, cfg, rank, world):
     d_out = torch.zeros((ND + 1, B), dtype=torch.int32, device="cuda")
     launches = [0]
 
-    def one_step():
+    def prefill():
         qw.qw_kv_reset(eng.kv, -1, st)
         for sq in seqs:
             qw.qw_kv_reserve(eng.kv, sq, P + ND, st)
-        qw.qw_prefill(eng.model, eng.kv, seqs, [P] * B, d_prompt.data_ptr(), 0, d_cur.data_ptr(), st)
+        qw.qw_prefill(eng.model, eng.kv, seqs, [P] * B, d_prompt.data_ptr(), 0, d_out[0].data_ptr(), st)
         launches[0] += qw.qw_last_launch_count(eng.model)
-        with torch.cuda.stream(st):
-            d_out[0].copy_(d_cur)
-        for i in range(1, ND + 1):
-            qw.qw_decode_step(eng.model, eng.kv, seqs, d_cur.data_ptr(), 0, d_cur.data_ptr(), st)
+
+    def decode_all():
+        """The ND greedy steps, row i of d_out feeding row i + 1, as qw_decode_steps graphs."""
+        done, n = 0, 0
+        while done < ND:
+            n = min(qw.QW_MAX_GRAPH_STEPS, ND - done)
+            qw.qw_decode_steps(eng.model, eng.kv, seqs, n, d_out[done].data_ptr(), d_out[done + 1].data_ptr(), st)
             launches[0] += qw.qw_last_launch_count(eng.model)
-            with torch.cuda.stream(st):
-                d_out[i].copy_(d_cur)
+            done += n
+        return n
+
+    def one_step():
+        prefill()
+        return decode_all()
 
     for _ in range(args.warmup):
-        one_step()
-    step_launches = qw.qw_last_launch_count(eng.model)  # of the last decode step
+        n_last = one_step()
+    step_launches = qw.qw_last_launch_count(eng.model) // n_last  # per decode step
     st.synchronize()
     status = qw.qw_sync_status(eng.model, st)
     if status != 0:
@@ -338,19 +345,26 @@ def run_ours(args, cfg, rank, world):
     if status != 0:
         raise RuntimeError(f"device status {status} in the timed region: {qw.qw_last_error()}")
 
-    # ---- decode-step latency alone (same graphs), for the record ----
-    qw.qw_kv_reset(eng.kv, -1, st)
-    for sq in seqs:
-        qw.qw_kv_reserve(eng.kv, sq, P + ND, st)
-    qw.qw_prefill(eng.model, eng.kv, seqs, [P] * B, d_prompt.data_ptr(), 0, d_cur.data_ptr(), st)
+    # ---- decode-step latency alone (the timed region's graphs), for the record ----
+    prefill()
+    ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ea.record(st)
+    decode_all()
+    eb.record(st)
+    st.synchronize()
+    decode_us = ea.elapsed_time(eb) * 1e3 / ND
+    # spread of single steps: one graph per step (qw_decode_step), an event between steps
+    prefill()
+    with torch.cuda.stream(st):
+        d_cur.copy_(d_out[0])
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(ND + 1)]
     evs[0].record(st)
     for i in range(ND):
         qw.qw_decode_step(eng.model, eng.kv, seqs, d_cur.data_ptr(), 0, d_cur.data_ptr(), st)
         evs[i + 1].record(st)
     st.synchronize()
-    decode_us = evs[0].elapsed_time(evs[ND]) * 1e3 / ND
-    decode_stats = step_stats(evs)
+    decode_stats = dict(step_stats(evs), graphs="one per step (qw_decode_step)",
+                        mean_us=round(evs[0].elapsed_time(evs[ND]) * 1e3 / ND, 2))
 
     # ---- per-kernel timing with CUDA events around each launch of one kernel kind ----
     # (events bracket the launches inside the captured decode graphs; measured on the
@@ -449,7 +463,7 @@ def run_ours(args, cfg, rank, world):
 
 
 def time_quantized_decode(qw, s, P: int, ND: int, hbm: float):
-    """B=1 decode steps (graph replays) with the layers' projections quantized to 8 and 4 bits
+    """B=1 decode steps (multi-step graph replays) with the layers' projections quantized to 8 and 4 bits
     (qw_quantize_weights; the tied LM head stays bf16), on the default workload's prompt
     length and step count: microseconds per step and the HBM fraction of the bytes a step
     reads (codes + scales, LM head, KV)."""
@@ -461,16 +475,19 @@ def time_quantized_decode(qw, s, P: int, ND: int, hbm: float):
         eng.quantize(bits)
         st = eng.stream
         d_prompt = torch.tensor(synth.make_tokens(s.vocab, P, 4242).astype(np.int32), device="cuda")
-        d_cur = torch.zeros(1, dtype=torch.int32, device="cuda")
+        d_out = torch.zeros((ND + 1, 1), dtype=torch.int32, device="cuda")
 
-        def steps(n):
+        def steps(n):   # n <= ND decode steps in qw_decode_steps graphs, as the bf16 line
             qw.qw_kv_reset(eng.kv, -1, st)
             qw.qw_kv_reserve(eng.kv, 0, P + ND, st)
-            qw.qw_prefill(eng.model, eng.kv, [0], [P], d_prompt.data_ptr(), 0, d_cur.data_ptr(), st)
+            qw.qw_prefill(eng.model, eng.kv, [0], [P], d_prompt.data_ptr(), 0, d_out[0].data_ptr(), st)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(st)
-            for _ in range(n):
-                qw.qw_decode_step(eng.model, eng.kv, [0], d_cur.data_ptr(), 0, d_cur.data_ptr(), st)
+            done = 0
+            while done < n:
+                k = min(qw.QW_MAX_GRAPH_STEPS, n - done)
+                qw.qw_decode_steps(eng.model, eng.kv, [0], k, d_out[done].data_ptr(), d_out[done + 1].data_ptr(), st)
+                done += k
             b.record(st)
             st.synchronize()
             return a.elapsed_time(b) * 1e3 / n

@@ -95,7 +95,7 @@ static bool dec1_shape(const qw_config& c) {
 struct WsLayout {
     size_t wqkv, wo, wgu, wd, embed16, bqkv, bo, bg, bu, bd, norms, fnorm, rcos, rsin;
     size_t x, h, qkv, q, attn, act, part_o, part_ml, counters;
-    size_t tok_seq, tok_pos, tok_slot, last, best, status, gen_tok, gen_cur, gen_out;
+    size_t tok_seq, tok_pos, tok_slot, last, best, status, gen_tok, gen_out;
     size_t st_part, st_ss, st_xw, st_done, st_tick, st_abort;  // batched decode-step kernel
     size_t op_part;  // o_proj partials of the fused small-batch decode attention [n_kv][4][D]
     size_t bdT, d1_y, d1_dpart;  // batch-1 cluster path: down_proj transposed, layer input x, partials
@@ -163,7 +163,6 @@ static WsLayout layout_for(const qw_config& c) {
         L.d1_dpart = take((size_t)2 * dec1_parts() * D * 4);  // two sets, alternating by layer
     }
     L.gen_tok = take(T * 4);
-    L.gen_cur = take((size_t)c.max_batch * 4);
     L.gen_out = take((size_t)c.max_batch * ((size_t)c.max_context + 1) * 4);
     L.total = off;
     return L;
@@ -206,7 +205,7 @@ struct qw_model {
     int *st_done, *st_tick, *st_abort;
     StepMaps st_maps;
     unsigned long long* best;
-    int32_t *gen_tok, *gen_cur, *gen_out;
+    int32_t *gen_tok, *gen_out;
     float* dbg_hidden;
     int32_t *dbg_pos, *dbg_slot;
     f16* dbg_attn;
@@ -340,7 +339,6 @@ extern "C" qw_status qw_init_weights(const qw_config* cfg, const qw_weight_ptrs*
     m->st_tick = (int*)(b + L.st_tick);
     m->st_abort = (int*)(b + L.st_abort);
     m->gen_tok = (int32_t*)(b + L.gen_tok);
-    m->gen_cur = (int32_t*)(b + L.gen_cur);
     m->gen_out = (int32_t*)(b + L.gen_out);
     m->use_clock = 0;
     m->last_launches = 0;
@@ -1299,26 +1297,104 @@ extern "C" qw_status qw_prefill(qw_model* m, qw_kv* kv, int B, const int* seq_id
     return QW_OK;
 }
 
-extern "C" qw_status qw_decode_step(qw_model* m, qw_kv* kv, int B, const int* seq_ids,
-                                    const int32_t* dev_token_ids, float* dev_logits, int32_t* dev_next_ids,
-                                    void* stream_) {
+// Checks a decode batch whose sequences each take n_steps more tokens; fills sd (one token
+// per sequence) and the largest reserved capacity of the batch.
+static qw_status decode_prepare(qw_model* m, qw_kv* kv, int B, const int* seq_ids, int n_steps, StepDesc& sd,
+                                int& cap) {
     QW_TRY(check_batch(m, kv, B, seq_ids));
-    if (!dev_token_ids || !dev_next_ids) return fail(QW_ERR_INVALID_ARG, "NULL argument");
     if (B > m->cfg.max_tokens) return fail(QW_ERR_INVALID_ARG, "B > max_tokens");
-    StepDesc sd = {};
+    sd = StepDesc{};
     sd.B = B;
     sd.T = B;
-    int cap = 0;
+    cap = 0;
     for (int b = 0; b < B; ++b) {
         const int s = seq_ids[b];
         const int capacity = std::min((int)kv->pt[s].size() * 16, m->cfg.max_context);
-        if (kv->len[s] + 1 > capacity)
-            return fail(QW_ERR_KV_FULL, "sequence %d has no reserved slot for position %d", s, kv->len[s]);
+        if ((long long)kv->len[s] + n_steps > capacity)
+            return fail(QW_ERR_KV_FULL, "sequence %d has no reserved slot for position %d", s,
+                        std::max(kv->len[s], capacity));
         sd.seq[b] = s;
         sd.start[b] = b;
         cap = std::max(cap, capacity);
     }
     sd.start[B] = B;
+    return QW_OK;
+}
+
+// n_steps decode steps replayed from one CUDA graph: step i reads its tokens from
+// tokens_i = (i == 0 ? tokens : next + (i - 1) * next_stride) and writes its picks to
+// next + i * next_stride (next_stride 0: every step in place); the last step writes logits.
+// Each step begins with a kernel launched without programmatic overlap, so a step's kernels
+// may read what earlier steps wrote before their dependency wait, as in separate graphs.
+static qw_status decode_graph(qw_model* m, qw_kv* kv, const StepDesc& sd, int cap, int n_steps,
+                              const int32_t* tokens, float* logits, int32_t* next, int next_stride,
+                              cudaStream_t st) {
+    const int B = sd.B;
+    // graph key: everything baked into the captured kernels
+    const SplitPlan sp = plan_splits(m, B, cap);
+    std::vector<long long> key;
+    key.reserve(B + 20);
+    key.push_back(B);
+    key.push_back(cap);
+    key.push_back(n_steps);
+    key.push_back(next_stride);
+    key.push_back((long long)(uintptr_t)tokens);
+    key.push_back((long long)(uintptr_t)logits);
+    key.push_back((long long)(uintptr_t)next);
+    key.push_back((long long)(uintptr_t)kv);
+    key.push_back(sp.chunk);
+    key.push_back(m->prof_kind);
+    key.push_back(m->pdl ? 1 : 0);
+    key.push_back(m->split_decode ? 1 : 0);
+    key.push_back(m->use_step ? m->step_gp : 0);
+    key.push_back((long long)m->step_wait_ns);
+    key.push_back(m->step_extra);
+    key.push_back(m->use_dec1 ? 1 : 0);
+    key.push_back(m->prof_kind || m->trace ? (long long)m->prof_gen : 0);
+    for (int b = 0; b < B; ++b) key.push_back(sd.seq[b]);
+    auto it = m->graphs.find(key);
+    if (it == m->graphs.end()) {
+        if (m->graphs.size() >= 64) {  // evict the least recently used entry
+            auto lru = m->graphs.begin();
+            for (auto jt = m->graphs.begin(); jt != m->graphs.end(); ++jt)
+                if (jt->second.last_use < lru->second.last_use) lru = jt;
+            cudaGraphExecDestroy(lru->second.exec);
+            m->graphs.erase(lru);
+        }
+        int launches = 0;
+        cudaGraph_t graph = nullptr;
+        CUDA_TRY(cudaStreamBeginCapture(m->cap_stream, cudaStreamCaptureModeThreadLocal));
+        qw_status s = QW_OK;
+        for (int i = 0; i < n_steps && s == QW_OK; ++i)
+            s = run_step(m, kv, sd, false, cap, i == 0 ? tokens : next + (size_t)(i - 1) * next_stride,
+                         i == n_steps - 1 ? logits : nullptr, next + (size_t)i * next_stride, m->cap_stream, false,
+                         &launches);
+        cudaError_t e = cudaStreamEndCapture(m->cap_stream, &graph);
+        if (s != QW_OK) {
+            if (graph) cudaGraphDestroy(graph);
+            return s;
+        }
+        if (e != cudaSuccess) return fail(QW_ERR_CUDA, "graph capture failed: %s", cudaGetErrorString(e));
+        cudaGraphExec_t exec = nullptr;
+        e = cudaGraphInstantiate(&exec, graph, 0);
+        cudaGraphDestroy(graph);
+        if (e != cudaSuccess) return fail(QW_ERR_CUDA, "graph instantiate failed: %s", cudaGetErrorString(e));
+        it = m->graphs.emplace(key, GraphEntry{exec, launches, 0}).first;
+    }
+    it->second.last_use = ++m->use_clock;
+    CUDA_TRY(cudaGraphLaunch(it->second.exec, st));
+    m->last_launches = it->second.launches;
+    for (int b = 0; b < B; ++b) kv->len[sd.seq[b]] += n_steps;
+    return QW_OK;
+}
+
+extern "C" qw_status qw_decode_step(qw_model* m, qw_kv* kv, int B, const int* seq_ids,
+                                    const int32_t* dev_token_ids, float* dev_logits, int32_t* dev_next_ids,
+                                    void* stream_) {
+    if (!dev_token_ids || !dev_next_ids) return fail(QW_ERR_INVALID_ARG, "NULL argument");
+    StepDesc sd;
+    int cap = 0;
+    QW_TRY(decode_prepare(m, kv, B, seq_ids, 1, sd, cap));
     cudaStream_t st = (cudaStream_t)stream_;
     if (m->dbg_hidden) {
         int launches = 0;
@@ -1326,59 +1402,33 @@ extern "C" qw_status qw_decode_step(qw_model* m, qw_kv* kv, int B, const int* se
         for (int b = 0; b < B; ++b) max_keys = std::max(max_keys, kv->len[seq_ids[b]] + 1);
         QW_TRY(run_step(m, kv, sd, false, max_keys, dev_token_ids, dev_logits, dev_next_ids, st, true, &launches));
         m->last_launches = launches;
-    } else {
-        // graph key: everything baked into the captured kernels
-        const SplitPlan sp = plan_splits(m, B, cap);
-        std::vector<long long> key;
-        key.reserve(B + 8);
-        key.push_back(B);
-        key.push_back(cap);
-        key.push_back((long long)(uintptr_t)dev_token_ids);
-        key.push_back((long long)(uintptr_t)dev_logits);
-        key.push_back((long long)(uintptr_t)dev_next_ids);
-        key.push_back((long long)(uintptr_t)kv);
-        key.push_back(sp.chunk);
-        key.push_back(m->prof_kind);
-        key.push_back(m->pdl ? 1 : 0);
-        key.push_back(m->split_decode ? 1 : 0);
-        key.push_back(m->use_step ? m->step_gp : 0);
-        key.push_back((long long)m->step_wait_ns);
-        key.push_back(m->step_extra);
-        key.push_back(m->use_dec1 ? 1 : 0);
-        key.push_back(m->prof_kind || m->trace ? (long long)m->prof_gen : 0);
-        for (int b = 0; b < B; ++b) key.push_back(seq_ids[b]);
-        auto it = m->graphs.find(key);
-        if (it == m->graphs.end()) {
-            if (m->graphs.size() >= 64) {  // evict the least recently used entry
-                auto lru = m->graphs.begin();
-                for (auto jt = m->graphs.begin(); jt != m->graphs.end(); ++jt)
-                    if (jt->second.last_use < lru->second.last_use) lru = jt;
-                cudaGraphExecDestroy(lru->second.exec);
-                m->graphs.erase(lru);
-            }
-            int launches = 0;
-            cudaGraph_t graph = nullptr;
-            CUDA_TRY(cudaStreamBeginCapture(m->cap_stream, cudaStreamCaptureModeThreadLocal));
-            qw_status s = run_step(m, kv, sd, false, cap, dev_token_ids, dev_logits, dev_next_ids, m->cap_stream,
-                                   false, &launches);
-            cudaError_t e = cudaStreamEndCapture(m->cap_stream, &graph);
-            if (s != QW_OK) {
-                if (graph) cudaGraphDestroy(graph);
-                return s;
-            }
-            if (e != cudaSuccess) return fail(QW_ERR_CUDA, "graph capture failed: %s", cudaGetErrorString(e));
-            cudaGraphExec_t exec = nullptr;
-            e = cudaGraphInstantiate(&exec, graph, 0);
-            cudaGraphDestroy(graph);
-            if (e != cudaSuccess) return fail(QW_ERR_CUDA, "graph instantiate failed: %s", cudaGetErrorString(e));
-            it = m->graphs.emplace(key, GraphEntry{exec, launches, 0}).first;
-        }
-        it->second.last_use = ++m->use_clock;
-        CUDA_TRY(cudaGraphLaunch(it->second.exec, st));
-        m->last_launches = it->second.launches;
+        for (int b = 0; b < B; ++b) kv->len[seq_ids[b]] += 1;
+        return QW_OK;
     }
-    for (int b = 0; b < B; ++b) kv->len[seq_ids[b]] += 1;
-    return QW_OK;
+    return decode_graph(m, kv, sd, cap, 1, dev_token_ids, dev_logits, dev_next_ids, 0, st);
+}
+
+extern "C" qw_status qw_decode_steps(qw_model* m, qw_kv* kv, int B, const int* seq_ids, int n_steps,
+                                     const int32_t* dev_token_ids, int32_t* dev_out_ids, void* stream_) {
+    if (!dev_token_ids || !dev_out_ids) return fail(QW_ERR_INVALID_ARG, "NULL argument");
+    if (n_steps < 1 || n_steps > QW_MAX_GRAPH_STEPS)
+        return fail(QW_ERR_INVALID_ARG, "n_steps %d outside [1, %d]", n_steps, QW_MAX_GRAPH_STEPS);
+    StepDesc sd;
+    int cap = 0;
+    QW_TRY(decode_prepare(m, kv, B, seq_ids, n_steps, sd, cap));
+    cudaStream_t st = (cudaStream_t)stream_;
+    if (m->dbg_hidden || m->prof_kind || m->trace) {
+        // the debug dumps, profiling events and trace records describe one step: step by step
+        int total = 0;
+        for (int i = 0; i < n_steps; ++i) {
+            QW_TRY(qw_decode_step(m, kv, B, seq_ids, i == 0 ? dev_token_ids : dev_out_ids + (size_t)(i - 1) * B,
+                                  nullptr, dev_out_ids + (size_t)i * B, stream_));
+            total += m->last_launches;
+        }
+        m->last_launches = total;
+        return QW_OK;
+    }
+    return decode_graph(m, kv, sd, cap, n_steps, dev_token_ids, nullptr, dev_out_ids, B, st);
 }
 
 // Paso 9 over a batch: prefill, then decode steps feeding each pick back on the device. With
@@ -1409,9 +1459,8 @@ static qw_status generate_impl(qw_model* m, qw_kv* kv, int B, const int* seq_ids
     }
     if (total > m->cfg.max_tokens) return fail(QW_ERR_INVALID_ARG, "prompts exceed max_tokens");
     CUDA_TRY(cudaMemcpyAsync(m->gen_tok, host_prompt_ids, (size_t)total * 4, cudaMemcpyHostToDevice, st));
-    QW_TRY(qw_prefill(m, kv, B, seq_ids, lens, m->gen_tok, nullptr, m->gen_cur, st));
+    QW_TRY(qw_prefill(m, kv, B, seq_ids, lens, m->gen_tok, nullptr, m->gen_out, st));
     int launches = m->last_launches;
-    CUDA_TRY(cudaMemcpyAsync(m->gen_out, m->gen_cur, (size_t)B * 4, cudaMemcpyDeviceToDevice, st));
     std::vector<int32_t> tmp((size_t)(n_decode + 1) * B);
     std::vector<int> stop_at(B, -1);  // index of a sequence's first EOS pick
     int n_stopped = 0, seen = 0;      // picks [0, seen) were read on the host
@@ -1430,13 +1479,19 @@ static qw_status generate_impl(qw_model* m, qw_kv* kv, int B, const int* seq_ids
         return QW_OK;
     };
     if (eos_id >= 0) QW_TRY(look(0));
+    // picks i = 1 .. n_decode: each chunk of steps is one graph that feeds row i - 1 of gen_out
+    // and writes row i (chunks of kEosCheck steps with an EOS, so the host can stop early; for
+    // more than 8 sequences, whose steps are hundreds of launches each, chunks of kEosCheck too,
+    // which keeps each graph to a few thousand nodes)
     int last = 0;
-    for (int i = 1; i <= n_decode && n_stopped < B; ++i) {
-        QW_TRY(qw_decode_step(m, kv, B, seq_ids, m->gen_cur, nullptr, m->gen_cur, st));
+    const int chunk = eos_id >= 0 || B > 8 ? kEosCheck : QW_MAX_GRAPH_STEPS;
+    while (last < n_decode && n_stopped < B) {
+        const int n = std::min(chunk, n_decode - last);
+        QW_TRY(qw_decode_steps(m, kv, B, seq_ids, n, m->gen_out + (size_t)last * B, m->gen_out + (size_t)(last + 1) * B,
+                               st));
         launches += m->last_launches;
-        CUDA_TRY(cudaMemcpyAsync(m->gen_out + (size_t)i * B, m->gen_cur, (size_t)B * 4, cudaMemcpyDeviceToDevice, st));
-        last = i;
-        if (eos_id >= 0 && i % kEosCheck == 0) QW_TRY(look(i));
+        last += n;
+        if (eos_id >= 0) QW_TRY(look(last));
     }
     QW_TRY(look(last));
     for (int b = 0; b < B; ++b) {

@@ -66,6 +66,7 @@ SIGNATURES = {
     "qw_kv_length": (_I, [_VP, _I]),
     "qw_prefill": (_I, [_VP, _VP, _I, _P(_I), _P(_I), _VP, _VP, _VP, _VP]),
     "qw_decode_step": (_I, [_VP, _VP, _I, _P(_I), _VP, _VP, _VP, _VP]),
+    "qw_decode_steps": (_I, [_VP, _VP, _I, _P(_I), _I, _VP, _VP, _VP]),
     "qw_generate": (_I, [_VP, _VP, _I, _P(_I), _P(_I), _P(ctypes.c_int32), _I,
                          _P(ctypes.c_int32), _VP]),
     "qw_generate_eos": (_I, [_VP, _VP, _I, _P(_I), _P(_I), _P(ctypes.c_int32), _I, _I,
@@ -181,6 +182,12 @@ def qw_decode_step(model: int, kv: int, seq_ids: Sequence[int], tokens_ptr: int,
                                  logits_ptr or None, next_ptr, _stream(stream)))
 
 
+def qw_decode_steps(model: int, kv: int, seq_ids: Sequence[int], n_steps: int, tokens_ptr: int, out_ptr: int,
+                    stream=None) -> None:
+    _check(load().qw_decode_steps(model, kv, len(seq_ids), _ints(seq_ids), n_steps, tokens_ptr, out_ptr,
+                                  _stream(stream)))
+
+
 def qw_generate(model: int, kv: int, seq_ids: Sequence[int], lens: Sequence[int], host_prompt,
                 n_decode: int, host_out, stream=None) -> None:
     """host_prompt / host_out: contiguous int32 numpy arrays (sum(lens)) / (B, n_decode + 1)."""
@@ -279,6 +286,8 @@ QW_OPT_STEP_PROJ_CTAS = 5
 QW_OPT_TEST_WAIT_LIMIT_US = 6
 QW_OPT_TEST_EXTRA_ARRIVALS = 7
 QW_OPT_BATCH1_CLUSTERS = 8
+
+QW_MAX_GRAPH_STEPS = 64   # most decode steps of one qw_decode_steps call
 
 
 def qw_set_option(model: int, option: int, value: int) -> None:

@@ -163,11 +163,26 @@ qw_status qw_decode_step(qw_model* m, qw_kv* kv, int B, const int* seq_ids,
                          const int32_t* dev_token_ids, float* dev_logits, int32_t* dev_next_ids,
                          void* stream);
 
+/* n_steps greedy decode steps of the same B sequences (the loop of Paso 9, every pick fed
+ * back on the device) replayed from ONE CUDA graph, cached per (B, seq_ids, n_steps,
+ * pointers): no host work and no graph boundary between the steps. dev_token_ids [B]: the
+ * tokens of the first step; dev_out_ids [n_steps, B] int32: row i holds step i's picks and
+ * is step i + 1's input (dev_token_ids may be dev_out_ids - B, i.e. the row before). No
+ * logits are written. Each sequence must be reserved for n_steps more tokens (else
+ * QW_ERR_KV_FULL, nothing launched); 1 <= n_steps <= QW_MAX_GRAPH_STEPS (else
+ * QW_ERR_INVALID_ARG). The picks, cache contents and lengths are those of n_steps calls of
+ * qw_decode_step (each step starts with a full dependency on the one before). With the debug
+ * dumps, profiling events or trace records set the steps run one graph each. */
+#define QW_MAX_GRAPH_STEPS 64
+qw_status qw_decode_steps(qw_model* m, qw_kv* kv, int B, const int* seq_ids, int n_steps,
+                          const int32_t* dev_token_ids, int32_t* dev_out_ids, void* stream);
+
 /* Greedy generation from HOST buffers (Paso 9 at temperature 0, no EOS stop): copies the
  * concatenated prompts (host_prompt_ids, sum(lens) int32) to the device, prefills, runs
  * n_decode decode steps feeding each pick back on the device, copies the picks to
  * host_out_ids ([B, n_decode + 1] int32, row b = sequence b) and synchronises `stream`.
- * Sequences must be empty and reserved for lens[b] + n_decode tokens. */
+ * Sequences must be empty and reserved for lens[b] + n_decode tokens. The decode steps run
+ * as qw_decode_steps graphs of up to QW_MAX_GRAPH_STEPS steps. */
 qw_status qw_generate(qw_model* m, qw_kv* kv, int B, const int* seq_ids, const int* lens,
                       const int32_t* host_prompt_ids, int n_decode, int32_t* host_out_ids,
                       void* stream);

@@ -26,7 +26,7 @@ def lib():
 
 def test_header_declares_the_boundary():
     names = _declared()
-    for fn in ("qw_init_weights", "qw_prefill", "qw_decode_step", "qw_kv_alloc", "qw_kv_reset",
+    for fn in ("qw_init_weights", "qw_prefill", "qw_decode_step", "qw_decode_steps", "qw_kv_alloc", "qw_kv_reset",
                "qw_kv_reserve", "qw_generate", "qw_sync_status", "qw_last_error"):
         assert fn in names
 
@@ -39,6 +39,19 @@ def test_library_exports_every_declared_symbol(lib):
 def test_binding_covers_header():
     from decode_qwen3_decoder_gb300 import qw
     assert set(qw.SIGNATURES) == _declared()
+
+
+def test_binding_constants_match_header():
+    """Every QW_OPT_* option, QW_PROF_* kind and QW_MAX_GRAPH_STEPS the binding defines has the
+    header's value."""
+    from decode_qwen3_decoder_gb300 import qw
+    src = open(os.path.join(ROOT, "include", "qw.h")).read()
+    vals = {k: int(v) for k, v in re.findall(r"\b(QW_(?:OPT|PROF)_[A-Z0-9_]+)\s*=\s*(\d+)", src)}
+    vals.update({k: int(v) for k, v in re.findall(r"#define\s+(QW_[A-Z0-9_]+)\s+(\d+)", src)})
+    names = [n for n in dir(qw) if n.startswith(("QW_OPT_", "QW_PROF_")) or n == "QW_MAX_GRAPH_STEPS"]
+    assert "QW_MAX_GRAPH_STEPS" in names and "QW_OPT_BATCH1_CLUSTERS" in names
+    for n in names:
+        assert n in vals and getattr(qw, n) == vals[n], n
 
 
 def test_host_only_calls_without_gpu(lib):
