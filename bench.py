@@ -370,9 +370,9 @@ def run_ours(args, cfg, rank, world):
     # (events bracket the launches inside the captured decode graphs; measured on the
     # same workload right after the timed region)
     hbm, bf16_burst, bf16_sust, peak_src = peaks()
-    # one token per step: two cluster kernels per layer (step begin + 2 per layer + LM head +
-    # finalize), else attention and o_proj as one kernel (kind 3)
-    clusters = B == 1 and step_launches == 2 * s.n_layers + 3
+    # one token per step: two cluster kernels per layer (step begin + 2 per layer + the LM
+    # head, which also ends the step), else attention and o_proj as one kernel (kind 3)
+    clusters = B == 1 and step_launches == 2 * s.n_layers + 2
     names = CLUSTER_KIND_NAMES if clusters else KIND_NAMES
     n_launch_per_step = ({3: s.n_layers, 5: s.n_layers, 7: 1} if clusters else
                          {1: s.n_layers, 3: s.n_layers, 5: s.n_layers, 6: s.n_layers, 7: 1} if B == 1 else

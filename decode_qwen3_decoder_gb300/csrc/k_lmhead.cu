@@ -12,6 +12,10 @@
 // in order, the sum of squares per 128-thread layout, h = x * rsqrt(mean + eps) * w in fp32,
 // each lane's 32 products in the same order and the same butterfly sum, and the packed
 // (value, index) keys, so both kernels give the same logits and ids bit for bit.
+//
+// It can also end the step (Paso 9's bookkeeping, otherwise a kernel of its own): the CTA
+// that finishes last, counted on a word that every launch leaves at zero, writes the greedy
+// id and advances the sequence's cached length.
 #include "qw_internal.h"
 
 namespace {
@@ -83,6 +87,13 @@ struct LmP {
     const float* xadd;    // optional partials [n_add][1024] added to x in order
     int n_add;
     int* status;
+    // optional step finalize by the CTA that finishes last (next_id == nullptr: none): the
+    // greedy id to next_id[0], best cleared, kv_len[seq] += len_add; done counts finished
+    // CTAs (zero between launches, reset by that CTA)
+    int32_t* next_id;
+    int* kv_len;
+    int seq, len_add;
+    unsigned int* done;
 };
 
 }  // namespace
@@ -230,6 +241,17 @@ __global__ void __launch_bounds__(LM_THREADS, 2) k_lmhead1(const __grid_constant
         unsigned long long b = 0ull;
         for (int w2 = 0; w2 < LM_CONS_WARPS; ++w2) b = u64_max(b, sbest[w2]);
         atomicMax(p.best, b);
+        if (p.next_id) {
+            // every CTA's maximum is in before its count; the last to count sees them all
+            __threadfence();
+            if (atomicAdd(p.done, 1u) == gridDim.x - 1) {
+                __threadfence();
+                const unsigned long long key = atomicExch(p.best, 0ull);
+                p.next_id[0] = (int32_t)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
+                p.kv_len[p.seq] += p.len_add;
+                atomicExch(p.done, 0u);
+            }
+        }
     }
 }
 
@@ -237,7 +259,8 @@ bool lmhead1_ok(int K, int vocab) { return K == LM_K && vocab % LM_ROWS == 0; }
 
 cudaError_t launch_lmhead1(const LaunchCtx& c, const float* x, const int* rows, const bf16* norm_w, float eps,
                            const bf16* E, int vocab, int K, float* logits, unsigned long long* best,
-                           const float* xadd, int n_add, int* status, int num_sms) {
+                           const float* xadd, int n_add, int* status, int num_sms, int32_t* next_id, int* kv_len,
+                           int seq, int len_add, unsigned int* done) {
     if (!lmhead1_ok(K, vocab)) return cudaErrorInvalidValue;
     static bool attr_set = false;
     if (!attr_set) {
@@ -257,6 +280,11 @@ cudaError_t launch_lmhead1(const LaunchCtx& c, const float* x, const int* rows, 
     p.xadd = xadd;
     p.n_add = xadd ? n_add : 0;
     p.status = status;
+    p.next_id = next_id;
+    p.kv_len = kv_len;
+    p.seq = seq;
+    p.len_add = len_add;
+    p.done = done;
     const int grid = std::min(2 * (num_sms > 0 ? num_sms : 148), vocab / LM_ROWS);
     return launch_k(c, k_lmhead1, dim3(grid), dim3(LM_THREADS), (size_t)LM_SMEM, p);
 }

@@ -203,7 +203,8 @@ cudaError_t launch_gemv_lmhead(const LaunchCtx& c, int B, const float* x, const 
 bool lmhead1_ok(int K, int vocab);
 cudaError_t launch_lmhead1(const LaunchCtx& c, const float* x, const int* rows, const bf16* norm_w, float eps,
                            const bf16* E, int vocab, int K, float* logits, unsigned long long* best,
-                           const float* xadd, int n_add, int* status, int num_sms);
+                           const float* xadd, int n_add, int* status, int num_sms, int32_t* next_id = nullptr,
+                           int* kv_len = nullptr, int seq = 0, int len_add = 0, unsigned int* done = nullptr);
 cudaError_t launch_finalize(const LaunchCtx& c, const StepDesc& sd, unsigned long long* best,
                             int32_t* next_ids, KVView kv);
 cudaError_t launch_qknorm_rope_append(const LaunchCtx& c, int T, int layer, const float* qkv,

@@ -143,7 +143,7 @@ static WsLayout layout_for(const qw_config& c) {
     L.tok_pos = take(T * 4);
     L.tok_slot = take(T * 4);
     L.last = take((size_t)c.max_batch * 4);
-    L.best = take((size_t)c.max_batch * 8);
+    L.best = take((size_t)(c.max_batch + 1) * 8);  // argmax keys, then the head's finish counter
     L.status = take(4);
     {
         // batched decode-step kernel: split-K partials, per-block sums of squares of x,
@@ -205,6 +205,7 @@ struct qw_model {
     int *st_done, *st_tick, *st_abort;
     StepMaps st_maps;
     unsigned long long* best;
+    unsigned int* lm_done;  // finished-CTA count of the batch-1 LM head (zero between launches)
     int32_t *gen_tok, *gen_out;
     float* dbg_hidden;
     int32_t *dbg_pos, *dbg_slot;
@@ -327,6 +328,7 @@ extern "C" qw_status qw_init_weights(const qw_config* cfg, const qw_weight_ptrs*
     m->tok_slot = (int*)(b + L.tok_slot);
     m->last = (int*)(b + L.last);
     m->best = (unsigned long long*)(b + L.best);
+    m->lm_done = (unsigned int*)(m->best + cfg->max_batch);
     m->status = (int*)(b + L.status);
     m->st_part = (float*)(b + L.st_part);
     m->st_ss = (float*)(b + L.st_ss);
@@ -444,7 +446,7 @@ extern "C" qw_status qw_init_weights(const qw_config* cfg, const qw_weight_ptrs*
         }
     }
     if (cudaMemsetAsync(m->counters, 0, (size_t)L.part_T * cfg->n_kv_heads * 4, st) != cudaSuccess ||
-        cudaMemsetAsync(m->best, 0, (size_t)cfg->max_batch * 8, st) != cudaSuccess) {
+        cudaMemsetAsync(m->best, 0, (size_t)(cfg->max_batch + 1) * 8, st) != cudaSuccess) {
         fail(QW_ERR_CUDA, "workspace clear failed");
         return fail_free(QW_ERR_CUDA);
     }
@@ -1222,15 +1224,18 @@ static qw_status run_step(qw_model* m, qw_kv* kv, const StepDesc& sd, bool prefi
         PROF(QW_PROF_LMHEAD);
         const bool d1 = !engine && dec1_step(m, sd, prefill, max_keys);  // x + the last down_proj partials
         if (d1) lc.pdl = pdl_on;
-        if (B == 1 && lmhead1_ok(D, c.vocab))
+        if (B == 1 && lmhead1_ok(D, c.vocab)) {
+            // the head's last CTA also ends the step (id, length): no finalize launch
             CUDA_TRY(launch_lmhead1(lc, m->x, m->last, m->fnorm, c.rms_eps, m->embed, c.vocab, D, logits, m->best,
                                     d1 ? m->d1_dpart + (size_t)((c.n_layers - 1) & 1) * dec1_parts() * D : nullptr,
-                                    d1 ? dec1_parts() : 0, m->status, m->num_sms));
-        else
-            CUDA_TRY(launch_gemv_lmhead(lc, B, m->x, m->last, m->fnorm, c.rms_eps, m->embed, c.vocab, D, logits,
-                                        m->best,
-                                        d1 ? m->d1_dpart + (size_t)((c.n_layers - 1) & 1) * dec1_parts() * D : nullptr,
-                                        d1 ? dec1_parts() : 0));
+                                    d1 ? dec1_parts() : 0, m->status, m->num_sms, next, kvv.len, sd.seq[0],
+                                    sd.start[1] - sd.start[0], m->lm_done));
+            return QW_OK;
+        }
+        CUDA_TRY(launch_gemv_lmhead(lc, B, m->x, m->last, m->fnorm, c.rms_eps, m->embed, c.vocab, D, logits,
+                                    m->best,
+                                    d1 ? m->d1_dpart + (size_t)((c.n_layers - 1) & 1) * dec1_parts() * D : nullptr,
+                                    d1 ? dec1_parts() : 0));
     } else {
         {
             PROF(QW_PROF_RMSNORM);

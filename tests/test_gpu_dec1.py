@@ -73,7 +73,8 @@ def test_full_model_decode_matches_oracle(full):
 
 
 def test_launch_count_two_per_layer(full):
-    """Without the debug dumps a step is: step begin, 2 launches per layer, LM head, finalize."""
+    """Without the debug dumps a step is: step begin, 2 launches per layer, and the LM head
+    (whose last CTA writes the id and advances the length)."""
     run = full
     qw = run.qw
     prompt = synth.make_tokens(S.vocab, 7, 4101).tolist()
@@ -82,7 +83,7 @@ def test_launch_count_two_per_layer(full):
         qw.qw_kv_reset(run.eng.kv, -1, run.eng.stream)
         g = run.prefill([0], [prompt], debug=False, reserve_extra=4)
         run.decode([0], [int(g["next"][0])], debug=False)
-        assert qw.qw_last_launch_count(run.eng.model) == 3 + per_layer * S.n_layers
+        assert qw.qw_last_launch_count(run.eng.model) == 2 + per_layer * S.n_layers
     _set(run, True)
 
 
