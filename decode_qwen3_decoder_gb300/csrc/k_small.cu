@@ -46,8 +46,10 @@ __global__ void __launch_bounds__(256) k_step_begin(StepDesc sd, const int32_t* 
                                                     int hidden, float* __restrict__ x, TokView tv,
                                                     KVView kv, int* status, float* __restrict__ ss,
                                                     const bf16* __restrict__ nw, f16* __restrict__ xw) {
-    pdl_launch();
+    // dependents start after the wait: what they read before their own wait (cached lengths,
+    // page tables, K/V) is then complete even when this kernel was launched early
     pdl_wait();
+    pdl_launch();
     const int t = blockIdx.x;
     int b = 0;
     while (b + 1 < sd.B && sd.start[b + 1] <= t) ++b;

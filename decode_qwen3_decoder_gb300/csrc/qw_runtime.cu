@@ -224,6 +224,7 @@ struct qw_model {
     int last_launches;
     int num_sms;
     bool pdl;
+    bool chain_step;    // set while a multi-step graph captures its second and later steps
     // profiling: events around launches of one kernel kind
     int prof_kind;
     unsigned long long* trace;
@@ -1149,9 +1150,11 @@ static qw_status run_step(qw_model* m, qw_kv* kv, const StepDesc& sd, bool prefi
     if (!small && !prefill && T > m->L.part_T) return fail(QW_ERR_UNSUPPORTED, "decode batch beyond partial buffers");
 
     int pc[16] = {0};
-    // The first kernel of a step waits for everything before it (no programmatic overlap), so
-    // kernels of this step may read state written by earlier steps before their own wait.
-    const LaunchCtx lc0 = {st, false, launches};
+    // The first kernel of a step waits for everything before it, so kernels of this step may
+    // read state written by earlier steps before their own wait. Inside a multi-step graph it
+    // is launched early (programmatic overlap with the previous step's last kernel) but lets
+    // its dependents start only once its own dependency wait has returned.
+    const LaunchCtx lc0 = {st, m->chain_step && m->pdl && m->prof_kind == QW_PROF_OFF, launches};
     const bool engine = !prefill && m->use_step && m->qbits == 16 && T >= 16 && T <= 2 * kStepMaxHalf &&
                         (m->prof_kind == QW_PROF_OFF || m->prof_kind == QW_PROF_STEP);
     CUDA_TRY(launch_step_begin(lc0, sd, tokens, m->embed, c.vocab, D, m->x, tv, kvv, m->status,
@@ -1370,10 +1373,13 @@ static qw_status decode_graph(qw_model* m, qw_kv* kv, const StepDesc& sd, int ca
         cudaGraph_t graph = nullptr;
         CUDA_TRY(cudaStreamBeginCapture(m->cap_stream, cudaStreamCaptureModeThreadLocal));
         qw_status s = QW_OK;
-        for (int i = 0; i < n_steps && s == QW_OK; ++i)
+        for (int i = 0; i < n_steps && s == QW_OK; ++i) {
+            m->chain_step = i > 0;
             s = run_step(m, kv, sd, false, cap, i == 0 ? tokens : next + (size_t)(i - 1) * next_stride,
                          i == n_steps - 1 ? logits : nullptr, next + (size_t)i * next_stride, m->cap_stream, false,
                          &launches);
+        }
+        m->chain_step = false;
         cudaError_t e = cudaStreamEndCapture(m->cap_stream, &graph);
         if (s != QW_OK) {
             if (graph) cudaGraphDestroy(graph);
