@@ -246,7 +246,7 @@ qw_status qw_kv_pool_ptrs(const qw_kv* kv, void** dev_k, void** dev_v, int* n_pa
 qw_status qw_kv_fill_synthetic(qw_kv* kv, int seq_id, int n_tokens, uint64_t seed, void* stream);
 
 /* Number of kernels the last prefill / decode call enqueued (graph replays count the
- * kernels inside the graph). */
+ * kernels inside the graph; a qw_decode_steps call counts all its steps). */
 int qw_last_launch_count(const qw_model* m);
 
 /* Kernel kinds for qw_profile_set. */
