@@ -72,3 +72,22 @@ def test_host_only_calls_without_gpu(lib):
     assert "weight pointers" in qw.qw_last_error() or "NULL" in qw.qw_last_error()
     assert qw.qw_kv_length(None, 0) == -1
     assert qw.qw_kv_free_pages(None) == -1
+
+
+def test_decode_calls_refuse_bad_arguments_on_the_host(lib):
+    """qw_decode_step / qw_decode_steps check their arguments before touching the device:
+    NULL buffers, step counts outside [1, QW_MAX_GRAPH_STEPS] and a NULL model are refused
+    with QW_ERR_INVALID_ARG and a message."""
+    from decode_qwen3_decoder_gb300 import qw
+    L = qw.load()
+    seqs = (ctypes.c_int * 1)(0)
+    buf = ctypes.c_void_p(16)   # never dereferenced: every call below is refused first
+    assert L.qw_decode_step(None, None, 1, seqs, None, None, buf, None) == -1
+    assert "NULL" in qw.qw_last_error()
+    for n in (0, -3, qw.QW_MAX_GRAPH_STEPS + 1):
+        assert L.qw_decode_steps(None, None, 1, seqs, n, buf, buf, None) == -1
+        assert "n_steps" in qw.qw_last_error()
+    assert L.qw_decode_steps(None, None, 1, seqs, 1, None, buf, None) == -1
+    assert "NULL" in qw.qw_last_error()
+    assert L.qw_decode_steps(None, None, 1, seqs, 4, buf, buf, None) == -1
+    assert "NULL" in qw.qw_last_error()   # model or kv
